@@ -1,0 +1,42 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA GPU (sm_103a); runs the library's kernels")
+    config.addinivalue_line(
+        "markers", "slow: full-size workloads (seconds to generate)")
+
+
+def _has_gpu() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def pytest_collection_modifyitems(config, items):
+    if _has_gpu():
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def spmv_lib():
+    """The compiled C-ABI library (built in-tree if it is missing)."""
+    from sparse_matrix_vector_gb300 import _lib
+    if not _lib.library_exists():
+        import __graft_entry__
+        __graft_entry__.build()
+    return _lib.load()

@@ -1,0 +1,326 @@
+"""Pins for the oracle: each check compares it with something other than
+itself (a pure-Python dense product, a closed form, scipy, the page's worked
+example, hand-derived encodings, invariants). The last test plants mistakes
+in copies of the oracle's C source and checks that some pin fails for each.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.sparse as sp
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "delta_examples.json")
+
+
+# ---------------------------------------------------------------- helpers
+
+def random_csr(seed, n_rows, n_cols, density=0.3, dtype=np.float32,
+               empty_rows=(), full_rows=()):
+    rng = np.random.default_rng(seed)
+    mask = rng.random((n_rows, n_cols)) < density
+    for r in empty_rows:
+        mask[r] = False
+    for r in full_rows:
+        mask[r] = True
+    rows, cols = np.nonzero(mask)
+    lengths = mask.sum(axis=1)
+    rp = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    vals = rng.uniform(-1, 1, size=rows.size).astype(dtype)
+    x = rng.uniform(-1, 1, size=n_cols).astype(dtype)
+    return rp, cols.astype(np.int32), vals, x
+
+
+def dense_rows(rp, ci, vals, n_cols):
+    """Dense matrix as Python lists of floats (fp64)."""
+    n_rows = len(rp) - 1
+    a = [[0.0] * n_cols for _ in range(n_rows)]
+    for i in range(n_rows):
+        for k in range(int(rp[i]), int(rp[i + 1])):
+            a[i][int(ci[k])] = float(vals[k])
+    return a
+
+
+def dense_matvec(a, x):
+    """Textbook dense product, column order, pure Python."""
+    y, s = [], []
+    for row in a:
+        acc = 0.0
+        acc_abs = 0.0
+        for j, aij in enumerate(row):
+            p = aij * float(x[j])
+            acc = acc + p
+            acc_abs = acc_abs + abs(p)
+        y.append(acc)
+        s.append(acc_abs)
+    return np.array(y), np.array(s)
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_dense_bruteforce():
+    cases = [
+        dict(seed=11, n_rows=17, n_cols=23, density=0.3),
+        dict(seed=12, n_rows=40, n_cols=9, density=0.5, empty_rows=(0, 5, 39)),
+        dict(seed=13, n_rows=32, n_cols=64, density=0.1, full_rows=(3, 31)),
+        dict(seed=14, n_rows=1, n_cols=1, density=1.0),
+        dict(seed=15, n_rows=64, n_cols=64, density=0.05, dtype=np.float16),
+    ]
+    for c in cases:
+        rp, ci, vals, x = random_csr(**c)
+        y, s = oracle.csr_spmv(rp, ci, vals, x)
+        y_ref, s_ref = dense_matvec(dense_rows(rp, ci, vals, c["n_cols"]), x)
+        # zeros add exactly and columns are sorted: bit-for-bit equal
+        assert np.array_equal(y, y_ref), c
+        assert np.array_equal(s, s_ref), c
+
+
+def pin_identity_and_permutation():
+    rng = np.random.default_rng(21)
+    n = 257
+    x = rng.uniform(-1, 1, n).astype(np.float32)
+    rp = np.arange(n + 1, dtype=np.int32)
+    eye_cols = np.arange(n, dtype=np.int32)
+    ones = np.ones(n, dtype=np.float32)
+    y, s = oracle.csr_spmv(rp, eye_cols, ones, x)
+    assert np.array_equal(y, x.astype(np.float64))
+    assert np.array_equal(s, np.abs(x).astype(np.float64))
+    perm = rng.permutation(n).astype(np.int32)
+    y = oracle.csr_spmv(rp, perm, ones, x, with_abs=False)
+    assert np.array_equal(y, x[perm].astype(np.float64))
+    # a non-symmetric permutation distinguishes P x from P^T x
+    inv = np.argsort(perm)
+    assert not np.array_equal(x[perm], x[inv])
+
+
+def pin_laplacian_constant():
+    nx, ny = 9, 7
+    m = workloads.laplacian(nx, ny, seed=0)
+    nbrs = m.row_lengths() - 1
+    r = np.arange(m.n_rows)
+    interior = (r % nx > 0) & (r % nx < nx - 1) & (r // nx > 0) & (r // nx < ny - 1)
+    # any finite c: the sorted-order partial sums are -c, -2c, 2c, c, 0
+    for c in (0.7318937, -3.25e7, 1.0e-30):
+        y = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values,
+                            np.full(m.n_rows, c, np.float64), with_abs=False)
+        assert np.all(y[interior] == 0.0)
+    # boundary rows: c * (4 - #neighbours); dyadic c keeps every partial exact
+    for c in (0.75, -1.5, 2.0 ** -10 * 3):
+        y = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values,
+                            np.full(m.n_rows, c, np.float64), with_abs=False)
+        assert np.array_equal(y, c * (4.0 - nbrs))
+
+
+def pin_row_of_ones():
+    rng = np.random.default_rng(31)
+    n = 1000
+    x = rng.uniform(-1, 1, n)
+    rp = np.array([0, n], dtype=np.int32)
+    y, s = oracle.csr_spmv(rp, np.arange(n, dtype=np.int32),
+                           np.ones(n, np.float32), x)
+    acc = 0.0
+    acc_abs = 0.0
+    for v in x:
+        acc = acc + float(v)
+        acc_abs = acc_abs + abs(float(v))
+    assert y[0] == acc and s[0] == acc_abs
+
+
+def pin_scipy():
+    mats = [workloads.tiny(), workloads.laplacian(40, 30),
+            workloads.powerlaw(n=5000, nnz=27000, max_len=300),
+            workloads.fem(4, 3, 2), workloads.llm(0.7, n=256)]
+    for m in mats:
+        y, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x)
+        a = sp.csr_matrix((m.values.astype(np.float64), m.col_idx, m.row_ptr),
+                          shape=(m.n_rows, m.n_cols))
+        y_sp = a @ m.x.astype(np.float64)
+        assert np.all(np.abs(y - y_sp) <= 1e-14 * s + 1e-300), m.name
+        s_sp = abs(a) @ np.abs(m.x.astype(np.float64))
+        assert np.allclose(s, s_sp, rtol=1e-13, atol=0), m.name
+
+
+def pin_delta_golden():
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        cols = np.array(c["cols"], dtype=np.int64)
+        n = cols.size
+        vals = (np.arange(1, n + 1) * 0.125).astype(np.float16)
+        rp = np.array([0, n], dtype=np.int64)
+        m = oracle.delta_encode(64, rp, cols, vals)
+        d = m.deltas()
+        if c["kind"] == "printed":
+            kept = m.values != 0
+            assert list(d[kept][:len(c["deltas_prefix"])]) == c["deltas_prefix"]
+            continue
+        assert list(d) == c["deltas"], c
+        assert list((m.values == 0).astype(int)) == c["pad"], c
+        assert list(m.words) == c["words"], c
+        assert m.n_entries % 8 == 0
+        # non-padding entries carry the input values in order
+        assert np.array_equal(m.values[m.values != 0], vals.view(np.uint16))
+
+
+def expected_pad_counts(rp, ci):
+    """Closed form of the reading: a gap d (first gap = first column) needs
+    max(0, floor((d - 1) / 15)) padding entries; rows round up to 8."""
+    rp = np.asarray(rp, np.int64)
+    ci = np.asarray(ci, np.int64)
+    n_rows = rp.size - 1
+    lengths = np.diff(rp)
+    prev = np.zeros_like(ci)
+    first = np.zeros(ci.size, bool)
+    first[rp[:-1][lengths > 0]] = True
+    prev[~first] = ci[np.nonzero(~first)[0] - 1]
+    gaps = ci - prev
+    pads_per = np.maximum(0, (gaps - 1) // 15)
+    row_of = np.repeat(np.arange(n_rows), lengths)
+    row_pads = np.bincount(row_of, weights=pads_per, minlength=n_rows).astype(np.int64)
+    unaligned = lengths + row_pads
+    aligned = (unaligned + 7) // 8 * 8
+    return int(pads_per.sum()), int((aligned - unaligned).sum()), aligned
+
+
+def pin_delta_roundtrip_and_counts():
+    mats = [workloads.llm(0.3, n=200), workloads.llm(0.9, n=333),
+            workloads.from_lengths("mixed", np.r_[0, 1, 7, 8, 9, 0, 64, 3],
+                                   400, seed=5, dtype=np.float16)]
+    for m in mats:
+        vals = m.values.astype(np.float16)
+        vals[vals == 0] = np.float16(0.5)   # the round trip needs no +-0.0
+        enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, vals)
+        gaps, aligns, aligned = expected_pad_counts(m.row_ptr, m.col_idx)
+        assert enc.gap_pads == gaps and enc.align_pads == aligns
+        assert np.array_equal(np.diff(enc.row_ptr), aligned)
+        assert enc.n_entries == m.nnz + gaps + aligns
+        d = enc.deltas()
+        assert d.max(initial=0) <= 15
+        rp, col, v = oracle.delta_decode(enc)
+        assert np.array_equal(rp, m.row_ptr.astype(np.int64))
+        assert np.array_equal(col, m.col_idx.astype(np.int64))
+        assert np.array_equal(v.view(np.uint16), vals.view(np.uint16))
+        # columns rebuilt by a running sum of the codes, row by row
+        for r in range(min(m.n_rows, 20)):
+            e0, e1 = enc.row_ptr[r], enc.row_ptr[r + 1]
+            c = np.cumsum(d[e0:e1].astype(np.int64))
+            kept = enc.values[e0:e1] != 0
+            assert np.array_equal(c[kept], m.col_idx[m.row_ptr[r]:m.row_ptr[r + 1]])
+
+
+ALL_PINS = [pin_dense_bruteforce, pin_identity_and_permutation,
+            pin_laplacian_constant, pin_row_of_ones, pin_scipy,
+            pin_delta_golden, pin_delta_roundtrip_and_counts]
+
+
+# ---------------------------------------------------------------- tests
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_delta_rejects_unsorted_or_duplicate():
+    rp = np.array([0, 3], np.int64)
+    vals = np.ones(3, np.float16)
+    with pytest.raises(ValueError):
+        oracle.delta_encode(10, rp, np.array([1, 5, 3]), vals)
+    with pytest.raises(ValueError):
+        oracle.delta_encode(10, rp, np.array([1, 5, 5]), vals)
+
+
+def test_delta_spmv_equals_csr_spmv():
+    m = workloads.llm(0.5, n=300)
+    enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, m.values)
+    y1, s1 = oracle.delta_spmv(enc, m.x)
+    y2, s2 = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x)
+    assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
+
+
+# mutations of the oracle source: (name, old text, new text)
+MUTANTS = [
+    ("dropped_term", "k < row_ptr[i + 1]; ++k) {\n      double prod",
+     "k < row_ptr[i + 1] - 1; ++k) {\n      double prod"),
+    ("wrong_sign", "acc = acc + prod;", "acc = acc - prod;"),
+    ("wrong_x_index", "values[k] * x[col_idx[k]]",
+     "values[k] * x[col_idx[row_ptr[i]]]"),
+    ("wrong_value_index", "values[k] * x[col_idx[k]]",
+     "values[row_ptr[i]] * x[col_idx[k]]"),
+    ("abs_sum_signed", "(prod < 0.0 ? -prod : prod)", "prod"),
+    ("pad_threshold", "#define DELTA_MAX 15", "#define DELTA_MAX 14"),
+    ("prev_not_reset", "int64_t prev = 0;", "int64_t prev = 1;"),
+    ("nibble_order", "DELTA_BITS * (e % ROW_ALIGN)",
+     "DELTA_BITS * (7 - e % ROW_ALIGN)"),
+    ("no_row_alignment", "count % ROW_ALIGN != 0", "count % 1 != 0"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = oracle.source_text()
+    assert old in src, name
+    lib = oracle.compile_variant(src.replace(old, new), str(tmp_path), name)
+    failures = 0
+    with oracle.use_library(lib):
+        for pin in ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError, IndexError):
+                failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
+
+
+# ---------------------------------------------------------------- generators
+
+def test_tiny_shape():
+    m = workloads.tiny()
+    assert m.n_rows == 1000 and m.nnz == 5000
+    assert np.all(m.row_lengths() == 5)
+    for r in range(m.n_rows):
+        c = m.col_idx[m.row_ptr[r]:m.row_ptr[r + 1]]
+        assert np.all(np.diff(c) > 0)
+    assert m.values.dtype == np.float32 and np.all(np.abs(m.values) <= 1)
+
+
+def test_laplacian_counts():
+    for nx, ny in ((1, 1), (1, 6), (5, 1), (13, 4)):
+        m = workloads.laplacian(nx, ny)
+        assert m.nnz == 5 * nx * ny - 2 * nx - 2 * ny
+    m = workloads.laplacian()
+    assert (m.n_rows, m.nnz) == (999_000, 4_991_002)
+
+
+def test_powerlaw_stats():
+    m = workloads.powerlaw()
+    L = m.row_lengths()
+    assert m.n_rows == 916_428 and m.nnz == 5_105_039
+    assert L.min() >= 1 and L.max() <= 4334
+    assert 0.55 < (L == 1).mean() < 0.75
+    key = np.repeat(np.arange(m.n_rows, dtype=np.int64), L) * m.n_cols + m.col_idx
+    assert np.all(np.diff(key) > 0)   # sorted, distinct inside rows
+
+
+def test_fem_structure():
+    assert workloads.fem_nnz(120, 60, 30) == 53_514_279
+    m = workloads.fem(5, 4, 3)
+    assert m.n_rows == 3 * 6 * 5 * 4
+    assert m.nnz == workloads.fem_nnz(5, 4, 3)
+    assert m.row_lengths().max() == 81
+    a = sp.csr_matrix((m.values, m.col_idx, m.row_ptr), shape=(m.n_rows,) * 2)
+    assert (a != a.T).nnz == 0          # bit-exact symmetry
+    rng = np.random.default_rng(0)
+    ad = a.astype(np.float64)
+    for _ in range(5):
+        v = rng.standard_normal(m.n_rows)
+        assert v @ (ad @ v) > 0
+
+
+def test_llm_values():
+    m = workloads.llm(0.5, n=512)
+    assert m.values.dtype == np.float16 and m.x.dtype == np.float16
+    assert not np.any(m.values == 0)
+    assert abs(m.nnz / 512 ** 2 - 0.5) < 0.01
+    assert workloads.llm_seed(0.3) == 43 and workloads.llm_seed(0.9) == 49
