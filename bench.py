@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of y = A x on GB300 through the C ABI (include/spmv.h).
+
+One step = one spmv_run (the whole path: tile kernel or DELTA4 decode kernel)
+over one resident copy of the workload. Copies rotate so that the footprint
+of the timed loop is several times the L2 size: every step streams its matrix
+from HBM. Steps are captured into CUDA graphs and replayed; the timed region
+is bracketed by a barrier and torch.cuda.synchronize() and measured with CUDA
+events on the launching stream.
+
+Metric (effective bandwidth): bytes = values + indices + row pointers (as
+stored by the format, padding included) + x read once + y written, divided by
+the time per step; GFLOP/s = 2 * nnz / time.
+
+  python bench.py                       # default workload: 5-point Laplacian
+  python bench.py --workload llm50_delta4
+  python bench.py --workload all        # one JSON line per workload
+  python bench.py --impl reference      # the fp64 CPU oracle on the same config
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("SpMV effective GB/s (fraction of GB300 HBM peak) and GFLOP/s "
+          "per matrix")
+FALLBACK_HBM_GBS = 6800.0
+
+# workload name -> (generator key, format, description)
+WORKLOADS = {
+    "tiny": ("tiny", "csr", "tiny_1000x1000_5perrow_f32_csr"),
+    "laplacian": ("laplacian", "csr", "laplacian_5pt_1000x999_f32_csr"),
+    "powerlaw": ("powerlaw", "csr", "powerlaw_zipf2_916428_5105039nnz_f32_csr"),
+    "fem": ("fem", "csr", "fem_hex_120x60x30_3dof_f32_csr"),
+}
+for _s in (30, 50, 70, 90):
+    WORKLOADS[f"llm{_s}_csr"] = (f"llm{_s}", "csr",
+                                 f"llm_12288x12288_sparsity{_s}_f16_csr")
+    WORKLOADS[f"llm{_s}_delta4"] = (f"llm{_s}", "delta4",
+                                    f"llm_12288x12288_sparsity{_s}_f16_delta4")
+DEFAULT_WORKLOAD = "laplacian"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    p = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc", "spmv_kernels.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_sha") != kernel_source_sha():
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (read only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception as e:  # nvidia-smi missing: report no clocks
+            log("clock sampling unavailable:", e)
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_call(m, fmt, frac):
+    """The oracle as it stands on the first ceil(frac * n_rows) rows of the
+    workload: returns (rows, algorithmic bytes, nonzeros, zero-arg call)."""
+    import oracle
+    rows = max(1, min(m.n_rows, int(math.ceil(m.n_rows * frac))))
+    rp = m.row_ptr[:rows + 1]
+    ci, vals = m.col_idx[:rp[-1]], m.values[:rp[-1]]
+    if fmt == "delta4":
+        enc = oracle.delta_encode(m.n_cols, rp, ci, vals)
+        nbytes = (enc.n_entries * 2 + enc.n_entries // 2 + (rows + 1) * 4
+                  + m.n_cols * 2 + rows * 4)
+        return rows, nbytes, int(rp[-1]), (lambda: oracle.delta_spmv(enc, m.x))
+    nbytes = (int(rp[-1]) * (vals.dtype.itemsize + 4) + (rows + 1) * 4
+              + m.n_cols * m.x.dtype.itemsize + rows * 4)
+    return rows, nbytes, int(rp[-1]), (lambda: oracle.csr_spmv(rp, ci, vals, m.x))
+
+
+def oracle_baseline(m, fmt, budget_s: float):
+    """cpu_baseline: time the oracle (fp64, one CPU thread) as it stands on a
+    bounded sample: whole-matrix calls repeated for about budget_s (at least
+    two), or one call on a leading block of rows if a whole call is too slow.
+    Returns (GB/s, sample description)."""
+    rows, nbytes, nnz, call = oracle_call(m, fmt, 1.0)
+    t0 = time.perf_counter()
+    call()
+    t_full = time.perf_counter() - t0
+    if t_full * 2 > budget_s:
+        rows, nbytes, nnz, call = oracle_call(m, fmt, budget_s / 2 / t_full)
+        t0 = time.perf_counter()
+        call()
+        dt = time.perf_counter() - t0
+        return nbytes / dt / 1e9, f"rows 0..{rows - 1} of {m.n_rows}, 1 call"
+    reps = max(2, int(budget_s / max(t_full, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        call()
+    dt = (time.perf_counter() - t0) / reps
+    return nbytes / dt / 1e9, f"whole matrix, {reps} calls"
+
+
+def algorithmic_bytes_csr(m):
+    vs = m.values.dtype.itemsize
+    return (m.nnz * (vs + 4) + (m.n_rows + 1) * 4 + m.n_cols * m.x.dtype.itemsize
+            + m.n_rows * 4)
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the fp64 CPU oracle, as it stands, on this config.
+    Each step is one oracle call on a bounded sample of the workload (the
+    whole matrix when the K + W calls fit about two minutes, else a leading
+    block of rows), so that the run ends within a few minutes."""
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads
+    key, fmt, desc = WORKLOADS[args.workload]
+    m = workloads.make(key)
+    steps, warmup = args.steps or 5, max(0, args.warmup)
+
+    rows, nbytes, nnz, call = oracle_call(m, fmt, 1.0)
+    t0 = time.perf_counter()
+    call()
+    t_full = time.perf_counter() - t0
+    budget = 120.0
+    if t_full * (steps + warmup) > budget:
+        frac = budget / (t_full * (steps + warmup))
+        rows, nbytes, nnz, call = oracle_call(m, fmt, frac)
+    sample = (f"rows 0..{rows - 1} of {m.n_rows} ({nnz} nonzeros) per step"
+              if rows < m.n_rows else "whole matrix per step")
+    for _ in range(warmup):
+        call()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call()
+    dt = (time.perf_counter() - t0) / steps
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": 1, "steps": steps, "warmup": warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "n_rows": m.n_rows, "nnz": m.nnz,
+                       "format": fmt},
+            "gflops": 2 * nnz / dt / 1e9,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_one(args, name, world, rank, local, pg):
+    import torch
+    import workloads
+    import sparse_matrix_vector_gb300 as S
+
+    key, fmt, desc = WORKLOADS[name]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t0 = time.perf_counter()
+    m = workloads.make(key)
+    log(f"[{name}] generated in {time.perf_counter() - t0:.1f}s "
+        f"rows={m.n_rows} nnz={m.nnz}")
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+
+    first = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
+    info = first.info
+    nbytes = int(info["algorithmic_bytes"])
+    copies = max(1, math.ceil(3 * l2 / nbytes))
+    plans = [first] + [S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols,
+                                          format=fmt) for _ in range(copies - 1)]
+    xdt = torch.float32 if m.x.dtype == np.float32 else torch.float16
+    xs = [torch.from_numpy(m.x).to(dev) for _ in range(copies)]
+    ys = [torch.empty(m.n_rows, dtype=torch.float32, device=dev) for _ in range(copies)]
+    assert xs[0].dtype == xdt
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_src = load_peak()
+
+    steps = args.steps
+    if not steps:   # ~1.5 s of timed work at 70% of peak, at least 200 steps
+        est = nbytes / (0.7 * peak * 1e9)
+        steps = max(200, int(1.5 / est))
+        steps = int(math.ceil(steps / copies) * copies)
+    warmup = max(3, args.warmup)
+
+    def launch(j):
+        S.spmv_run(plans[j % copies], xs[j % copies], ys[j % copies], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for j in range(warmup):
+            launch(j)
+    torch.cuda.synchronize(dev)
+
+    # capture the timed steps into graphs of at most 4096 launches each
+    graphs = []
+    chunk = 4096
+    for g0 in range(0, steps, chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(g0, min(steps, g0 + chunk)):
+                launch(j)
+        graphs.append(g)
+    with torch.cuda.stream(stream):   # one untimed replay (graph upload)
+        for g in graphs[:1]:
+            g.replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    if pg is not None:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sec_per_step = ms / 1e3 / steps
+    value = world * nbytes / sec_per_step / 1e9
+    per_launch = nbytes / sec_per_step / 1e9
+    gflops = world * 2 * m.nnz / sec_per_step / 1e9
+
+    # end to end through the C ABI with pinned host buffers
+    x_host = torch.from_numpy(m.x).pin_memory().numpy()
+    y_host = torch.empty(m.n_rows, dtype=torch.float32).pin_memory().numpy()
+    e2e_steps = max(20, min(2000, int(0.5 / max(sec_per_step * 4, 1e-6))))
+    for _ in range(3):
+        S.spmv_run_host(plans[0], x_host, y_host, stream=stream)
+    if pg is not None:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for j in range(e2e_steps):
+        S.spmv_run_host(plans[j % copies], x_host, y_host, stream=stream)
+    e2e_sec = (time.perf_counter() - t0) / e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_sec], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_sec = float(t.item())
+
+    line = None
+    if rank == 0:
+        traffic = recorded_traffic(name)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if fmt == "csr" and m.values.dtype == np.float32 else "f16",
+            "data": "synthetic",
+            "config": {"workload": desc, "format": fmt, "n_rows": m.n_rows,
+                       "n_cols": m.n_cols, "nnz": m.nnz,
+                       "stored_entries": int(info["n_entries"]),
+                       "algorithmic_bytes": nbytes,
+                       "bins_rows": info["rows_per_bin"],
+                       "bins_tiles": info["tiles_per_bin"],
+                       "grid": info["grid"], "x_in_smem": bool(info["x_in_smem"]),
+                       "l2": (f"rotating {copies} resident copies, "
+                              f"{copies * nbytes / 2**20:.0f} MiB >= 3x L2 "
+                              f"({l2 / 2**20:.0f} MiB)"),
+                       "timing": "CUDA graphs of back-to-back spmv_run, CUDA "
+                                 "events on the launching stream",
+                       "parallelism": f"replicas{world}"},
+            "gflops": gflops,
+            "roofline": {"bound": "hbm", "achieved": per_launch, "peak": peak,
+                         "unit": "GB/s", "frac": per_launch / peak,
+                         "peak_source": peak_src, "traffic": traffic},
+            "e2e": {"value": world * nbytes / e2e_sec / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": int(m.n_cols * m.x.dtype.itemsize),
+                    "d2h_bytes_per_step": int(m.n_rows * 4),
+                    "ms_per_step": e2e_sec * 1e3},
+            "gpu_launches": int(info["launches_per_run"]) * steps,
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            cpu_gbs, sample = oracle_baseline(m, fmt, args.cpu_budget)
+            line["cpu_baseline"] = {"value": cpu_gbs, "unit": "GB/s", "cores": 1,
+                                    "kind": "oracle", "sample": sample}
+    for p in plans:
+        S.spmv_plan_destroy(p)
+    del xs, ys, graphs
+    torch.cuda.empty_cache()
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: ~1.5 s of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="one of %s, or 'all'" % ", ".join(WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    if args.workload != "all" and args.workload not in WORKLOADS:
+        ap.error(f"unknown workload {args.workload}")
+
+    if args.impl == "reference":
+        if args.workload == "all":
+            for name in WORKLOADS:
+                args.workload = name
+                run_reference(args, world, rank)
+            return 0
+        return run_reference(args, world, rank)
+
+    import torch
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist.group.WORLD
+    names = list(WORKLOADS) if args.workload == "all" else [args.workload]
+    for name in names:
+        line = bench_one(args, name, world, rank, local, pg)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    if pg is not None:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

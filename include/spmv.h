@@ -1,0 +1,232 @@
+/*
+ * spmv.h -- C ABI of the GB300 sparse matrix-vector multiply library.
+ *
+ * The library computes y = A x on one CUDA device (sm_103a) for a sparse
+ * matrix A stored either as
+ *   - CSR (row_ptr / col_idx / values), values fp32 or fp16; or
+ *   - DELTA4: fp16 values with 4-bit column deltas packed eight to a 32-bit
+ *     word, zero-valued padding entries where a gap does not fit in 4 bits,
+ *     and CSR-like row pointers over the stored entries.
+ * x is fp32 for fp32 CSR and fp16 otherwise; y is always fp32 and every
+ * product is accumulated in fp32.
+ *
+ * Sources (web pages, by title and section):
+ *   [CSR]   "CUDA CSR SpMV optimisation" (codechina.net), section 2.1: the CSR
+ *           arrays and the definition y[row] = sum over k in
+ *           [row_ptr[row], row_ptr[row+1]) of values[k] * x[col_idx[k]];
+ *           section 2.2: one-time upload of the arrays with cudaMalloc and
+ *           an asynchronous copy, then kernel launches chosen by the format.
+ *   [MACKO] "MACKO-SpMV" (maplevalley.com.cn), section 2.1: the format
+ *           struct {values with zero placeholders, 4-bit deltas, row
+ *           pointers} and its four encoding steps; section 2.2: the warp
+ *           decode (prefix sum of deltas) and half2 multiply.
+ *   [SPGEMM] "Hash-based multi-phase SpGEMM" (mlqm.cn), section 2.1.1: rows
+ *           grouped by work into bins served by partial-warp, warp and
+ *           block-per-row kernels; section 5.2: batching of tiny rows.
+ *
+ * Conventions for every call:
+ *   - Host pointers are read only during the call; nothing keeps them.
+ *   - Device pointers (x_dev, y_dev) are caller-owned CUDA device memory on
+ *     the device the plan was created on.
+ *   - Errors are returned as spmv_status; no call aborts, throws or prints.
+ *   - A plan is not thread-safe: calls that use one plan must be ordered
+ *     (one host thread, one stream or explicit stream ordering), because a
+ *     run may use scratch memory owned by the plan.
+ */
+#ifndef SPMV_GB300_SPMV_H
+#define SPMV_GB300_SPMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPMV_ABI_VERSION 1
+
+typedef enum spmv_status {
+  SPMV_OK = 0,
+  SPMV_ERR_INVALID_ARG = 1,      /* null pointer, negative size, bad enum   */
+  SPMV_ERR_BAD_ROW_PTR = 2,      /* row_ptr[0] != 0, decreasing, or last != nnz */
+  SPMV_ERR_COL_OUT_OF_RANGE = 3, /* a column (or decoded column) >= n_cols  */
+  SPMV_ERR_UNSORTED_OR_DUPLICATE_COLS = 4, /* DELTA4 needs increasing cols */
+  SPMV_ERR_UNSUPPORTED = 5,      /* format / dtype combination not provided */
+  SPMV_ERR_OUT_OF_MEMORY = 6,    /* host or device allocation failed        */
+  SPMV_ERR_CUDA = 7,             /* a CUDA runtime call failed (no device…) */
+  SPMV_ERR_TOO_LARGE = 8,        /* sizes exceed 32-bit device indexing     */
+  SPMV_ERR_WRONG_DEVICE = 9,     /* current device differs from the plan's  */
+  SPMV_ERR_DEVICE_STATUS = 10    /* a kernel reported an error in the plan's
+                                    device status word (bounded wait expired) */
+} spmv_status;
+
+typedef enum spmv_dtype { SPMV_F32 = 0, SPMV_F16 = 1 } spmv_dtype;
+
+typedef enum spmv_format {
+  SPMV_FORMAT_CSR = 0,    /* [CSR] section 2.1                                */
+  SPMV_FORMAT_DELTA4 = 1  /* [MACKO] section 2.1, 4-bit deltas                */
+} spmv_format;
+
+/* A CSR matrix in HOST memory ([CSR] section 2.1).
+ * row_ptr: n_rows+1 offsets, row_ptr[0] == 0, non-decreasing, last == nnz.
+ * col_idx: nnz column indices in [0, n_cols). Any order and repeats are
+ *          accepted for SPMV_FORMAT_CSR (repeats add up); DELTA4 needs
+ *          strictly increasing columns inside every row.
+ * values:  nnz elements of value_dtype (fp16 given as its 16-bit pattern). */
+typedef struct spmv_csr {
+  int32_t n_rows;
+  int32_t n_cols;
+  int64_t nnz;
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  const void* values;
+  spmv_dtype value_dtype;
+} spmv_csr;
+
+/* A DELTA4 matrix in HOST memory ([MACKO] section 2.1), as produced by
+ * spmv_convert. Encoding of each row, with the running column c starting at
+ * 0 at the start of the row:
+ *   for each nonzero (in increasing column order) at column j:
+ *     d = j - c; while d > 15 emit (+0.0, 15), c += 15, d -= 15;
+ *     emit (value, d); c = j;
+ *   then emit (+0.0, 0) until the row holds a multiple of 8 entries.
+ * Entry e stores its value in values[e] and its 4-bit delta in bits
+ * 4*(e%8)..4*(e%8)+3 of words[e/8]. row_ptr[r] is the index of the first
+ * entry of row r (always a multiple of 8). A stored +0.0 (bits 0x0000) is
+ * indistinguishable from padding; decoding drops every such entry. */
+typedef struct spmv_delta {
+  int32_t n_rows;
+  int32_t n_cols;
+  int64_t nnz;              /* nonzeros encoded (entries that are not padding) */
+  int64_t n_entries;        /* stored entries, padding included              */
+  int64_t n_gap_pads;       /* padding entries inserted for gaps > 15        */
+  int64_t n_align_pads;     /* padding entries that round rows up to 8       */
+  int64_t n_explicit_zeros; /* input values equal to +0.0 (stored as such)   */
+  uint16_t* values;         /* n_entries fp16 bit patterns                   */
+  uint32_t* words;          /* n_entries / 8 words of packed deltas          */
+  int64_t* row_ptr;         /* n_rows + 1 entry offsets                      */
+} spmv_delta;
+
+/* Planner knobs ([SPGEMM] section 2.1.1 grouping; [MACKO] section 3.3
+ * dynamic scheduling). Zero / negative fields mean "library default". */
+typedef struct spmv_plan_options {
+  int32_t tile_nnz;      /* nonzero budget of a short-row tile             */
+  int32_t tile_rows;     /* row budget of a short-row tile                 */
+  int32_t cta_row_min;   /* rows longer than this get a CTA of their own   */
+  int32_t split_row_min; /* rows longer than this are split across CTAs    */
+  int32_t split_chunk;   /* nonzeros per chunk of a split row              */
+  int32_t x_smem;        /* -1 auto, 0 never, 1 whenever x fits: stage x in
+                            shared memory once per CTA                     */
+  int32_t lanes;         /* 0 auto, else force 1..32 lanes per short row   */
+  int32_t reserved[9];
+} spmv_plan_options;
+
+/* What the planner decided; filled by spmv_plan_inspect / spmv_plan_get_info.
+ * Bins ([SPGEMM] section 2.1.1, adapted to nonzeros per row):
+ *   0 sub-warp: short rows batched in tiles, 1..16 lanes per row
+ *   1 warp:     short rows batched in tiles, 32 lanes per row
+ *   2 CTA:      one CTA per row
+ *   3 split:    a row cut into chunks, one CTA per chunk, partial sums
+ *               combined by the last chunk to finish                      */
+typedef struct spmv_plan_info {
+  int32_t n_rows;
+  int32_t n_cols;
+  int64_t nnz;
+  int32_t format;
+  int32_t value_dtype;
+  int64_t n_entries;         /* stored entries (== nnz for CSR)            */
+  int64_t n_tiles;           /* work units of one run                      */
+  int64_t rows_per_bin[4];
+  int64_t tiles_per_bin[4];
+  int64_t n_split_rows;
+  int32_t x_in_smem;         /* 1 when x is staged in shared memory        */
+  int32_t grid;              /* CTAs of the main launch                    */
+  int32_t block;             /* threads per CTA                            */
+  int32_t launches_per_run;  /* kernel launches issued by one spmv_run     */
+  int64_t matrix_bytes;      /* stored matrix: values + indices + row ptrs */
+  int64_t aux_bytes;         /* planner tables and scratch on the device   */
+  int64_t algorithmic_bytes; /* matrix_bytes + x read once + y written     */
+  int64_t reserved[8];
+} spmv_plan_info;
+
+typedef struct spmv_plan spmv_plan;
+
+/* Short English text for a status code (static storage). */
+const char* spmv_status_string(spmv_status status);
+
+/* Returns SPMV_ABI_VERSION of the built library. */
+int32_t spmv_abi_version(void);
+
+/* Fill *opts with the library defaults. */
+void spmv_plan_options_init(spmv_plan_options* opts);
+
+/* [MACKO] section 2.1: convert a CSR matrix with fp16 values into DELTA4
+ * on the host. The library allocates out->values, out->words and
+ * out->row_ptr with malloc; release them with spmv_delta_free. On error
+ * *out is left zeroed. Errors: INVALID_ARG, BAD_ROW_PTR, COL_OUT_OF_RANGE,
+ * UNSORTED_OR_DUPLICATE_COLS, UNSUPPORTED (fp32 values), OUT_OF_MEMORY. */
+spmv_status spmv_convert(const spmv_csr* csr, spmv_delta* out);
+
+/* Free the arrays of a spmv_delta filled by spmv_convert and zero it. */
+void spmv_delta_free(spmv_delta* d);
+
+/* Host-only dry run of the planner: validates csr exactly as
+ * spmv_plan_create does and reports the bins and tiles it would build,
+ * without touching any CUDA device (device-dependent fields -- grid,
+ * x_in_smem -- assume a 152-SM device). opts may be NULL. */
+spmv_status spmv_plan_inspect(const spmv_csr* csr, spmv_format format,
+                              const spmv_plan_options* opts,
+                              spmv_plan_info* info);
+
+/* Build a plan on the current CUDA device ([CSR] section 2.2): validate,
+ * convert (DELTA4), bin the rows, then copy the matrix and the planner's
+ * tables into device memory owned by the plan. The caller may free its host
+ * arrays as soon as this returns. Synchronous. On error *out is NULL. */
+spmv_status spmv_plan_create(const spmv_csr* csr, spmv_format format,
+                             spmv_plan** out);
+
+/* As spmv_plan_create, with planner options (opts may be NULL). */
+spmv_status spmv_plan_create_ex(const spmv_csr* csr, spmv_format format,
+                                const spmv_plan_options* opts,
+                                spmv_plan** out);
+
+/* Build a DELTA4 plan directly from an already converted matrix (for
+ * weights converted once ahead of time). Every stored entry's decoded column
+ * must be < n_cols and row_ptr entries must be multiples of 8. */
+spmv_status spmv_plan_create_delta(const spmv_delta* delta,
+                                   const spmv_plan_options* opts,
+                                   spmv_plan** out);
+
+/* Copy the plan's planner report into *info. */
+spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info);
+
+/* y = A x, asynchronously on `stream` (a cudaStream_t; NULL = legacy
+ * default stream). x_dev: n_cols elements (fp32 for fp32 CSR plans, fp16
+ * otherwise), aligned to its element size; y_dev: n_rows fp32, aligned to 4
+ * bytes, fully overwritten (rows without nonzeros get 0). x and y must not
+ * overlap. DELTA4 plans multiply padding entries as 0 * x[c], so x must be
+ * finite there. Does not synchronize. Errors: INVALID_ARG, WRONG_DEVICE,
+ * CUDA (launch failure). */
+spmv_status spmv_run(spmv_plan* plan, const void* x_dev, float* y_dev,
+                     void* stream);
+
+/* End-to-end variant with HOST buffers: copies x_host (n_cols elements of
+ * the plan's x type) into a plan-owned device buffer, runs y = A x, copies
+ * y back into y_host (n_rows fp32) and synchronizes `stream`. Pinned host
+ * memory gives the fastest copies. */
+spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
+                          void* stream);
+
+/* Synchronize the plan's device and read its device status word: OK, or
+ * DEVICE_STATUS if a kernel reported an error since the last check (the
+ * word is cleared by this call). */
+spmv_status spmv_plan_check(spmv_plan* plan);
+
+/* Release the plan and its device memory (synchronizes the device first).
+ * NULL is accepted. */
+void spmv_plan_destroy(spmv_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPMV_GB300_SPMV_H */

@@ -1,0 +1,15 @@
+"""GB300-native sparse matrix-vector multiply y = A x (fp32 CSR, fp16 CSR and
+the 4-bit column-delta format) behind a C ABI, ``include/spmv.h``.
+
+The compiled library is ``libspmv_gb300.so`` next to this file (built by
+``sparse_matrix_vector_gb300.build``). This package only marshals arguments.
+"""
+from .api import (  # noqa: F401
+    DeltaMatrix, Plan, SpmvError, spmv_abi_version, spmv_convert,
+    spmv_plan_check, spmv_plan_create, spmv_plan_create_delta,
+    spmv_plan_destroy, spmv_plan_inspect, spmv_plan_options, spmv_run,
+    spmv_run_host, spmv_status_string,
+)
+from ._lib import (  # noqa: F401
+    SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4,
+)

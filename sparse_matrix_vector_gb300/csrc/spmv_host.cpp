@@ -1,0 +1,758 @@
+// Host half of the library: argument validation, the DELTA4 converter, the
+// row-binning planner, plan lifetime and the run entry points.
+//
+// Sources (web pages, by title and section):
+//   "CUDA CSR SpMV optimisation" (codechina.net), 2.1: CSR arrays and the
+//     row sum that defines y; 2.2: upload once, then launch by format.
+//   "MACKO-SpMV" (maplevalley.com.cn), 2.1: delta coding, zero padding for
+//     gaps that do not fit 4 bits, 8 nibbles per 32-bit word, row alignment;
+//     3.3: splitting long rows ("dynamic scheduling").
+//   "Hash-based multi-phase SpGEMM" (mlqm.cn), 2.1.1 and 2.2: rows grouped by
+//     work into bins handled by partial-warp, warp and block-per-row
+//     kernels; 5.2: batching of tiny rows.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "spmv_internal.h"
+
+// The opaque handle of the public header.
+struct spmv_plan {
+  spmv::Plan impl;
+};
+
+namespace spmv {
+namespace {
+
+// Device indexing is 32-bit; keep clear of INT32_MAX so that padded spans
+// (up to one vector past the end) never overflow.
+constexpr int64_t kMaxIndex = (int64_t)INT32_MAX - 4096;
+constexpr size_t kXsAutoBytes = 48 * 1024;   // auto-stage x up to this size
+constexpr size_t kXsMaxBytes = 160 * 1024;   // hard limit when forced
+constexpr int kPadElems = 16;                // zero tail after device arrays
+constexpr int kAssumedSms = 152;             // for host-only inspection
+
+size_t dtype_size(spmv_dtype t) { return t == SPMV_F16 ? 2 : 4; }
+
+bool valid_dtype(int t) { return t == SPMV_F32 || t == SPMV_F16; }
+bool valid_format(int f) {
+  return f == SPMV_FORMAT_CSR || f == SPMV_FORMAT_DELTA4;
+}
+
+// Structure checks shared by every entry point that takes a CSR matrix.
+spmv_status validate_csr(const spmv_csr* m, bool need_sorted) {
+  if (!m) return SPMV_ERR_INVALID_ARG;
+  if (m->n_rows < 0 || m->n_cols < 0 || m->nnz < 0) return SPMV_ERR_INVALID_ARG;
+  if (!valid_dtype(m->value_dtype)) return SPMV_ERR_INVALID_ARG;
+  if (!m->row_ptr) return SPMV_ERR_INVALID_ARG;
+  if (m->nnz > 0 && (!m->col_idx || !m->values)) return SPMV_ERR_INVALID_ARG;
+  if (m->nnz > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+  const int32_t* rp = m->row_ptr;
+  if (rp[0] != 0) return SPMV_ERR_BAD_ROW_PTR;
+  for (int32_t r = 0; r < m->n_rows; ++r)
+    if (rp[r + 1] < rp[r]) return SPMV_ERR_BAD_ROW_PTR;
+  if ((int64_t)rp[m->n_rows] != m->nnz) return SPMV_ERR_BAD_ROW_PTR;
+  for (int64_t k = 0; k < m->nnz; ++k) {
+    int32_t c = m->col_idx[k];
+    if (c < 0 || c >= m->n_cols) return SPMV_ERR_COL_OUT_OF_RANGE;
+  }
+  if (need_sorted) {
+    for (int32_t r = 0; r < m->n_rows; ++r)
+      for (int32_t k = rp[r] + 1; k < rp[r + 1]; ++k)
+        if (m->col_idx[k] <= m->col_idx[k - 1])
+          return SPMV_ERR_UNSORTED_OR_DUPLICATE_COLS;
+  }
+  return SPMV_OK;
+}
+
+// ------------------------------------------------------------ DELTA4 codec
+constexpr int kDeltaCap = 15;   // largest 4-bit code
+constexpr int kRowAlign = 8;    // entries per packed word
+
+// Stored entries of one row under the encoding of the header comment.
+int64_t delta_row_entries(const int32_t* cols, int32_t len, int64_t* gaps) {
+  int64_t n = 0, c = 0;
+  for (int32_t k = 0; k < len; ++k) {
+    int64_t gap = (int64_t)cols[k] - c;
+    if (gap > kDeltaCap) {
+      int64_t pads = (gap - 1) / kDeltaCap;
+      n += pads;
+      *gaps += pads;
+    }
+    n += 1;
+    c = cols[k];
+  }
+  return n;
+}
+
+inline void emit(uint16_t* vals, uint32_t* words, int64_t e, uint16_t bits,
+                 uint32_t code) {
+  vals[e] = bits;
+  words[e >> 3] |= code << (4 * (uint32_t)(e & 7));
+}
+
+// ------------------------------------------------------------ lanes choice
+// Short-row tiles reduce each row with g = 2^lg lanes. Cost estimate of a
+// choice: for every warp, sum over passes of the slowest row it owns in that
+// pass (ceil(len / g) additions) plus lg shuffle steps; the tile costs as
+// much as its slowest warp.
+int choose_lanes_log2(const int32_t* rp, int r0, int r1) {
+  const int R = r1 - r0;
+  int best_lg = 0;
+  int64_t best = INT64_MAX;
+  for (int lg = 0; lg <= 5; ++lg) {
+    const int g = 1 << lg;
+    const int per_pass = kThreads >> lg;
+    const int per_warp = 32 >> lg;
+    int64_t worst = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      int64_t t = 0;
+      for (int p0 = 0; p0 < R; p0 += per_pass) {
+        const int rs = p0 + w * per_warp;
+        if (rs >= R) break;
+        int64_t m = 0;
+        for (int q = 0; q < per_warp && rs + q < R; ++q) {
+          const int64_t len = rp[r0 + rs + q + 1] - rp[r0 + rs + q];
+          m = std::max(m, (len + g - 1) / g);
+        }
+        t += m + lg + 1;
+      }
+      worst = std::max(worst, t);
+    }
+    if (worst < best) {
+      best = worst;
+      best_lg = lg;
+    }
+  }
+  return best_lg;
+}
+
+int ilog2(int v) {
+  int l = 0;
+  while ((1 << (l + 1)) <= v) ++l;
+  return l;
+}
+
+}  // namespace
+
+Options resolve_options(const spmv_plan_options* o) {
+  Options r;
+  r.tile_nnz = kMaxTileNnz;
+  r.tile_rows = kMaxTileRows;
+  r.cta_row_min = 256;
+  r.split_row_min = 16384;
+  r.split_chunk = 4096;
+  r.x_smem = -1;
+  r.lanes = 0;
+  if (o) {
+    if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, kMaxTileNnz);
+    if (o->tile_rows > 0) r.tile_rows = std::min(o->tile_rows, kMaxTileRows);
+    if (o->cta_row_min > 0) r.cta_row_min = o->cta_row_min;
+    if (o->split_row_min > 0) r.split_row_min = o->split_row_min;
+    if (o->split_chunk > 0) r.split_chunk = std::max(o->split_chunk, 64);
+    if (o->x_smem >= 0) r.x_smem = o->x_smem ? 1 : 0;
+    if (o->lanes > 0) r.lanes = 1 << ilog2(std::min(o->lanes, 32));
+  }
+  // a row that may sit in a short-row tile must fit one on its own
+  r.cta_row_min = std::min(r.cta_row_min, r.tile_nnz);
+  r.split_row_min = std::max(r.split_row_min, r.cta_row_min);
+  return r;
+}
+
+spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
+                           CsrTables* out, spmv_plan_info* info) {
+  out->tiles.clear();
+  out->splits.clear();
+  out->n_chunks = 0;
+  try {
+    int r = 0;
+    while (r < n_rows) {
+      const int64_t len = (int64_t)rp[r + 1] - rp[r];
+      if (len > o.split_row_min) {
+        const int64_t nch = (len + o.split_chunk - 1) / o.split_chunk;
+        const int64_t sid = (int64_t)out->splits.size();
+        if (sid > (int64_t)kSplitIdMask || out->n_chunks + nch > kMaxIndex)
+          return SPMV_ERR_TOO_LARGE;
+        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)nch});
+        for (int64_t k = 0; k < nch; ++k) {
+          const int64_t b = rp[r] + k * o.split_chunk;
+          const int64_t e = std::min<int64_t>(b + o.split_chunk, rp[r + 1]);
+          out->tiles.push_back({r, (int32_t)b, (int32_t)e,
+                                (int32_t)((kKindSplit << kKindShift) |
+                                          (uint32_t)sid)});
+        }
+        out->n_chunks += nch;
+        info->rows_per_bin[3] += 1;
+        info->tiles_per_bin[3] += nch;
+        ++r;
+        continue;
+      }
+      if (len > o.cta_row_min) {
+        out->tiles.push_back(
+            {r, rp[r], rp[r + 1], (int32_t)(kKindRow << kKindShift)});
+        info->rows_per_bin[2] += 1;
+        info->tiles_per_bin[2] += 1;
+        ++r;
+        continue;
+      }
+      const int r0 = r;
+      int64_t nz = 0;
+      while (r < n_rows && r - r0 < o.tile_rows) {
+        const int64_t l = (int64_t)rp[r + 1] - rp[r];
+        if (l > o.cta_row_min || nz + l > o.tile_nnz) break;
+        nz += l;
+        ++r;
+      }
+      const int lg = o.lanes ? ilog2(o.lanes) : choose_lanes_log2(rp, r0, r);
+      out->tiles.push_back(
+          {r0, rp[r0], rp[r],
+           (int32_t)((kKindStream << kKindShift) | ((uint32_t)lg << kLanesShift) |
+                     (uint32_t)(r - r0))});
+      const int bin = lg == 5 ? 1 : 0;
+      info->rows_per_bin[bin] += r - r0;
+      info->tiles_per_bin[bin] += 1;
+    }
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  if ((int64_t)out->tiles.size() > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+  info->n_tiles = (int64_t)out->tiles.size();
+  info->n_split_rows = (int64_t)out->splits.size();
+  return SPMV_OK;
+}
+
+namespace {
+
+// ------------------------------------------------------------ CUDA helpers
+struct DeviceGuard {
+  int saved = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&saved) != cudaSuccess) return;
+    ok = (saved == dev) || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (saved >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != saved)
+      cudaSetDevice(saved);
+  }
+};
+
+template <typename T>
+spmv_status dev_alloc(T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc((void**)p, bytes);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  return e == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
+}
+
+// Allocate bytes_alloc, zero them, copy bytes_copy from host.
+template <typename T>
+spmv_status dev_upload(T** p, const void* host, size_t bytes_copy,
+                       size_t bytes_alloc) {
+  spmv_status s = dev_alloc(p, bytes_alloc);
+  if (s != SPMV_OK) return s;
+  if (cudaMemset(*p, 0, bytes_alloc ? bytes_alloc : 16) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  if (bytes_copy &&
+      cudaMemcpy(*p, host, bytes_copy, cudaMemcpyHostToDevice) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  return SPMV_OK;
+}
+
+void free_plan(spmv_plan* plan) {
+  if (!plan) return;
+  Plan* p = &plan->impl;
+  {
+    DeviceGuard g(p->device);
+    void* bufs[] = {p->row_ptr, p->col_idx, p->values, p->words,
+                    p->tiles,   p->splits,  p->partials, p->counters,
+                    p->status,  p->x_stage, p->y_stage};
+    for (void* b : bufs)
+      if (b) cudaFree(b);
+  }
+  delete plan;
+}
+
+spmv_status bind_device(Plan* p) {
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    cudaGetLastError();
+    return SPMV_ERR_CUDA;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount,
+                             p->device) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  p->sm_count = sms;
+  return SPMV_OK;
+}
+
+spmv_status common_buffers(Plan* p) {
+  const size_t xs = p->dtype == SPMV_F32 && p->format == SPMV_FORMAT_CSR ? 4 : 2;
+  spmv_status s;
+  if ((s = dev_upload(&p->status, nullptr, 0, 16)) != SPMV_OK) return s;
+  if ((s = dev_alloc(&p->x_stage, (size_t)p->n_cols * xs + 16)) != SPMV_OK)
+    return s;
+  if ((s = dev_alloc(&p->y_stage, (size_t)p->n_rows * 4 + 16)) != SPMV_OK)
+    return s;
+  return SPMV_OK;
+}
+
+void fill_bytes(spmv_plan_info* info, size_t x_elem) {
+  info->algorithmic_bytes = info->matrix_bytes +
+                            (int64_t)info->n_cols * (int64_t)x_elem +
+                            (int64_t)info->n_rows * 4;
+}
+
+spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
+  CsrTables t;
+  spmv_plan_info& info = p->info;
+  spmv_status s = plan_csr_tiles(m->n_rows, m->row_ptr, o, &t, &info);
+  if (s != SPMV_OK) return s;
+  if ((s = bind_device(p)) != SPMV_OK) return s;
+  const size_t vs = dtype_size(m->value_dtype);
+  const size_t xbytes = (size_t)m->n_cols * vs;
+  p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
+            : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
+  p->dyn_smem = p->x_smem ? (xbytes + 15) / 16 * 16 : 0;
+  p->n_tiles = (int64_t)t.tiles.size();
+  p->split_chunk = o.split_chunk;
+  if (set_kernel_smem_limits(p->dyn_smem, 0) != 0) return SPMV_ERR_CUDA;
+  if (p->x_smem) {
+    int occ = csr_kernel_occupancy(m->value_dtype, true, p->dyn_smem);
+    if (occ <= 0) return SPMV_ERR_CUDA;
+    p->grid = (int)std::min<int64_t>(p->n_tiles, (int64_t)occ * p->sm_count);
+  } else {
+    p->grid = (int)p->n_tiles;
+  }
+  const size_t nnz_alloc = (size_t)m->nnz + kPadElems;
+  if ((s = dev_upload(&p->row_ptr, m->row_ptr, ((size_t)m->n_rows + 1) * 4,
+                      ((size_t)m->n_rows + 1) * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->col_idx, m->col_idx, (size_t)m->nnz * 4,
+                      nnz_alloc * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->values, m->values, (size_t)m->nnz * vs,
+                      nnz_alloc * vs)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->tiles, t.tiles.data(), t.tiles.size() * sizeof(Tile),
+                      t.tiles.size() * sizeof(Tile))) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->splits, t.splits.data(),
+                      t.splits.size() * sizeof(SplitInfo),
+                      t.splits.size() * sizeof(SplitInfo))) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->partials, nullptr, 0,
+                      (size_t)t.n_chunks * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->counters, nullptr, 0,
+                      t.splits.size() * 4)) != SPMV_OK) return s;
+  if ((s = common_buffers(p)) != SPMV_OK) return s;
+  info.x_in_smem = p->x_smem ? 1 : 0;
+  info.grid = p->grid;
+  info.block = kThreads;
+  info.launches_per_run = p->n_tiles > 0 ? 1 : 0;
+  info.matrix_bytes = (int64_t)m->nnz * (int64_t)(vs + 4) +
+                      ((int64_t)m->n_rows + 1) * 4;
+  info.aux_bytes = (int64_t)(t.tiles.size() * sizeof(Tile) +
+                             t.splits.size() * (sizeof(SplitInfo) + 4) +
+                             (size_t)t.n_chunks * 4);
+  fill_bytes(&info, vs);
+  return SPMV_OK;
+}
+
+spmv_status validate_delta(const spmv_delta* d, int64_t* nnz_out) {
+  if (!d) return SPMV_ERR_INVALID_ARG;
+  if (d->n_rows < 0 || d->n_cols < 0 || d->n_entries < 0 || !d->row_ptr)
+    return SPMV_ERR_INVALID_ARG;
+  if (d->n_entries > 0 && (!d->values || !d->words)) return SPMV_ERR_INVALID_ARG;
+  if (d->n_entries > kMaxIndex || (d->n_entries & 7)) {
+    return d->n_entries > kMaxIndex ? SPMV_ERR_TOO_LARGE : SPMV_ERR_BAD_ROW_PTR;
+  }
+  const int64_t* rp = d->row_ptr;
+  if (rp[0] != 0 || rp[d->n_rows] != d->n_entries) return SPMV_ERR_BAD_ROW_PTR;
+  int64_t nnz = 0;
+  for (int32_t r = 0; r < d->n_rows; ++r) {
+    if (rp[r + 1] < rp[r] || (rp[r] & 7)) return SPMV_ERR_BAD_ROW_PTR;
+    int64_t c = 0;
+    for (int64_t e = rp[r]; e < rp[r + 1]; ++e) {
+      c += (d->words[e >> 3] >> (4 * (e & 7))) & 0xFu;
+      if (d->values[e] != 0) ++nnz;
+    }
+    if (rp[r + 1] > rp[r] && c >= d->n_cols) return SPMV_ERR_COL_OUT_OF_RANGE;
+  }
+  *nnz_out = nnz;
+  return SPMV_OK;
+}
+
+spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
+  spmv_status s;
+  spmv_plan_info& info = p->info;
+  if ((s = bind_device(p)) != SPMV_OK) return s;
+  const size_t xbytes = (size_t)d->n_cols * 2;
+  p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
+            : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
+  p->dyn_smem = p->x_smem ? (xbytes + 15) / 16 * 16 : 0;
+  if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
+  int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
+  if (occ <= 0) return SPMV_ERR_CUDA;
+  p->grid = (int)std::min<int64_t>(d->n_rows, (int64_t)occ * p->sm_count);
+  p->n_tiles = d->n_rows;
+  std::vector<int32_t> rp32;
+  try {
+    rp32.resize((size_t)d->n_rows + 1);
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  for (int32_t r = 0; r <= d->n_rows; ++r) rp32[r] = (int32_t)d->row_ptr[r];
+  const size_t e_alloc = (size_t)d->n_entries + 8 * kPadElems;
+  if ((s = dev_upload(&p->row_ptr, rp32.data(), rp32.size() * 4,
+                      rp32.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->values, d->values, (size_t)d->n_entries * 2,
+                      e_alloc * 2)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->words, d->words, (size_t)d->n_entries / 2,
+                      e_alloc / 2)) != SPMV_OK) return s;
+  if ((s = common_buffers(p)) != SPMV_OK) return s;
+  info.n_tiles = d->n_rows;
+  info.rows_per_bin[2] = d->n_rows;   // one CTA per row
+  info.tiles_per_bin[2] = d->n_rows;
+  info.x_in_smem = p->x_smem ? 1 : 0;
+  info.grid = p->grid;
+  info.block = kThreads;
+  info.launches_per_run = d->n_rows > 0 ? 1 : 0;
+  info.matrix_bytes = d->n_entries * 2 + d->n_entries / 2 +
+                      ((int64_t)d->n_rows + 1) * 4;
+  info.aux_bytes = 0;
+  fill_bytes(&info, 2);
+  return SPMV_OK;
+}
+
+}  // namespace
+}  // namespace spmv
+
+using namespace spmv;
+
+extern "C" {
+
+const char* spmv_status_string(spmv_status s) {
+  switch (s) {
+    case SPMV_OK: return "ok";
+    case SPMV_ERR_INVALID_ARG: return "invalid argument";
+    case SPMV_ERR_BAD_ROW_PTR: return "malformed row pointers";
+    case SPMV_ERR_COL_OUT_OF_RANGE: return "column index out of range";
+    case SPMV_ERR_UNSORTED_OR_DUPLICATE_COLS:
+      return "columns not strictly increasing within a row";
+    case SPMV_ERR_UNSUPPORTED: return "unsupported format / dtype combination";
+    case SPMV_ERR_OUT_OF_MEMORY: return "out of memory";
+    case SPMV_ERR_CUDA: return "CUDA runtime error";
+    case SPMV_ERR_TOO_LARGE: return "sizes exceed 32-bit device indexing";
+    case SPMV_ERR_WRONG_DEVICE: return "current device is not the plan's device";
+    case SPMV_ERR_DEVICE_STATUS: return "a kernel reported an error";
+  }
+  return "unknown status";
+}
+
+int32_t spmv_abi_version(void) { return SPMV_ABI_VERSION; }
+
+void spmv_plan_options_init(spmv_plan_options* o) {
+  if (!o) return;
+  std::memset(o, 0, sizeof(*o));
+  Options r = resolve_options(nullptr);
+  o->tile_nnz = r.tile_nnz;
+  o->tile_rows = r.tile_rows;
+  o->cta_row_min = r.cta_row_min;
+  o->split_row_min = r.split_row_min;
+  o->split_chunk = r.split_chunk;
+  o->x_smem = r.x_smem;
+  o->lanes = r.lanes;
+}
+
+spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  spmv_status s = validate_csr(m, true);
+  if (s != SPMV_OK) return s;
+  if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+  const int32_t* rp = m->row_ptr;
+  const uint16_t* v = static_cast<const uint16_t*>(m->values);
+  int64_t* erp = static_cast<int64_t*>(std::malloc(((size_t)m->n_rows + 1) * 8));
+  if (!erp) return SPMV_ERR_OUT_OF_MEMORY;
+  int64_t total = 0, gaps = 0, aligns = 0;
+  erp[0] = 0;
+  for (int32_t r = 0; r < m->n_rows; ++r) {
+    int64_t n = delta_row_entries(m->col_idx + rp[r], rp[r + 1] - rp[r], &gaps);
+    int64_t padded = (n + kRowAlign - 1) / kRowAlign * kRowAlign;
+    aligns += padded - n;
+    total += padded;
+    erp[r + 1] = total;
+  }
+  uint16_t* vals = static_cast<uint16_t*>(std::malloc((size_t)total * 2 + 16));
+  uint32_t* words =
+      static_cast<uint32_t*>(std::calloc((size_t)total / kRowAlign + 1, 4));
+  if (!vals || !words) {
+    std::free(erp);
+    std::free(vals);
+    std::free(words);
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  int64_t zeros = 0;
+  for (int32_t r = 0; r < m->n_rows; ++r) {
+    int64_t e = erp[r], c = 0;
+    for (int32_t k = rp[r]; k < rp[r + 1]; ++k) {
+      const int64_t col = m->col_idx[k];
+      int64_t gap = col - c;
+      for (; gap > kDeltaCap; gap -= kDeltaCap) emit(vals, words, e++, 0, kDeltaCap);
+      emit(vals, words, e++, v[k], (uint32_t)gap);
+      zeros += v[k] == 0;
+      c = col;
+    }
+    while (e < erp[r + 1]) emit(vals, words, e++, 0, 0);
+  }
+  out->n_rows = m->n_rows;
+  out->n_cols = m->n_cols;
+  out->nnz = m->nnz;
+  out->n_entries = total;
+  out->n_gap_pads = gaps;
+  out->n_align_pads = aligns;
+  out->n_explicit_zeros = zeros;
+  out->values = vals;
+  out->words = words;
+  out->row_ptr = erp;
+  return SPMV_OK;
+}
+
+void spmv_delta_free(spmv_delta* d) {
+  if (!d) return;
+  std::free(d->values);
+  std::free(d->words);
+  std::free(d->row_ptr);
+  std::memset(d, 0, sizeof(*d));
+}
+
+spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
+                              const spmv_plan_options* opts,
+                              spmv_plan_info* info) {
+  if (!info || !valid_format(format)) return SPMV_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  const bool delta = format == SPMV_FORMAT_DELTA4;
+  spmv_status s = validate_csr(m, delta);
+  if (s != SPMV_OK) return s;
+  Options o = resolve_options(opts);
+  info->n_rows = m->n_rows;
+  info->n_cols = m->n_cols;
+  info->nnz = m->nnz;
+  info->format = format;
+  info->value_dtype = m->value_dtype;
+  info->block = kThreads;
+  if (delta) {
+    if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+    int64_t gaps = 0, total = 0;
+    for (int32_t r = 0; r < m->n_rows; ++r) {
+      int64_t n = delta_row_entries(m->col_idx + m->row_ptr[r],
+                                    m->row_ptr[r + 1] - m->row_ptr[r], &gaps);
+      total += (n + kRowAlign - 1) / kRowAlign * kRowAlign;
+    }
+    if (total > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+    info->n_entries = total;
+    info->n_tiles = m->n_rows;
+    info->rows_per_bin[2] = m->n_rows;
+    info->tiles_per_bin[2] = m->n_rows;
+    info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * 2 <=
+                      (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);
+    info->grid = (int32_t)std::min<int64_t>(m->n_rows, 8LL * kAssumedSms);
+    info->launches_per_run = m->n_rows > 0;
+    info->matrix_bytes = total * 2 + total / 2 + ((int64_t)m->n_rows + 1) * 4;
+    fill_bytes(info, 2);
+    return SPMV_OK;
+  }
+  CsrTables t;
+  s = plan_csr_tiles(m->n_rows, m->row_ptr, o, &t, info);
+  if (s != SPMV_OK) return s;
+  const size_t vs = dtype_size(m->value_dtype);
+  info->n_entries = m->nnz;
+  info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * vs <=
+                    (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);
+  info->grid = info->x_in_smem
+                   ? (int32_t)std::min<int64_t>(info->n_tiles, 8LL * kAssumedSms)
+                   : (int32_t)info->n_tiles;
+  info->launches_per_run = info->n_tiles > 0;
+  info->matrix_bytes = m->nnz * (int64_t)(vs + 4) + ((int64_t)m->n_rows + 1) * 4;
+  info->aux_bytes = (int64_t)(t.tiles.size() * sizeof(Tile) +
+                              t.splits.size() * (sizeof(SplitInfo) + 4) +
+                              (size_t)t.n_chunks * 4);
+  fill_bytes(info, vs);
+  return SPMV_OK;
+}
+
+spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
+                                const spmv_plan_options* opts,
+                                spmv_plan** out) {
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!valid_format(format)) return SPMV_ERR_INVALID_ARG;
+  const bool delta = format == SPMV_FORMAT_DELTA4;
+  spmv_status s = validate_csr(m, delta);
+  if (s != SPMV_OK) return s;
+  if (delta && m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+  Options o = resolve_options(opts);
+  spmv_plan* plan = new (std::nothrow) spmv_plan();
+  if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
+  Plan* p = &plan->impl;
+  p->format = format;
+  p->dtype = m->value_dtype;
+  p->n_rows = m->n_rows;
+  p->n_cols = m->n_cols;
+  p->nnz = m->nnz;
+  p->info.n_rows = m->n_rows;
+  p->info.n_cols = m->n_cols;
+  p->info.nnz = m->nnz;
+  p->info.format = format;
+  p->info.value_dtype = m->value_dtype;
+  if (delta) {
+    spmv_delta d;
+    s = spmv_convert(m, &d);
+    if (s == SPMV_OK) {
+      if (d.n_entries > kMaxIndex) {
+        s = SPMV_ERR_TOO_LARGE;
+      } else {
+        p->n_entries = d.n_entries;
+        p->info.n_entries = d.n_entries;
+        s = create_delta_plan(&d, o, p);
+      }
+      spmv_delta_free(&d);
+    }
+  } else {
+    p->n_entries = m->nnz;
+    p->info.n_entries = m->nnz;
+    s = create_csr_plan(m, o, p);
+  }
+  if (s != SPMV_OK) {
+    free_plan(plan);
+    return s;
+  }
+  *out = plan;
+  return SPMV_OK;
+}
+
+spmv_status spmv_plan_create(const spmv_csr* m, spmv_format format,
+                             spmv_plan** out) {
+  return spmv_plan_create_ex(m, format, nullptr, out);
+}
+
+spmv_status spmv_plan_create_delta(const spmv_delta* d,
+                                   const spmv_plan_options* opts,
+                                   spmv_plan** out) {
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  int64_t nnz = 0;
+  spmv_status s = validate_delta(d, &nnz);
+  if (s != SPMV_OK) return s;
+  Options o = resolve_options(opts);
+  spmv_plan* plan = new (std::nothrow) spmv_plan();
+  if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
+  Plan* p = &plan->impl;
+  p->format = SPMV_FORMAT_DELTA4;
+  p->dtype = SPMV_F16;
+  p->n_rows = d->n_rows;
+  p->n_cols = d->n_cols;
+  p->nnz = nnz;
+  p->n_entries = d->n_entries;
+  p->info.n_rows = d->n_rows;
+  p->info.n_cols = d->n_cols;
+  p->info.nnz = nnz;
+  p->info.format = SPMV_FORMAT_DELTA4;
+  p->info.value_dtype = SPMV_F16;
+  p->info.n_entries = d->n_entries;
+  s = create_delta_plan(d, o, p);
+  if (s != SPMV_OK) {
+    free_plan(plan);
+    return s;
+  }
+  *out = plan;
+  return SPMV_OK;
+}
+
+spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info) {
+  if (!plan || !info) return SPMV_ERR_INVALID_ARG;
+  *info = plan->impl.info;
+  return SPMV_OK;
+}
+
+static spmv_status check_run_args(const Plan& p, const void* x, const float* y,
+                                  size_t* x_elem) {
+  const size_t xs =
+      (p.format == SPMV_FORMAT_CSR && p.dtype == SPMV_F32) ? 4 : 2;
+  *x_elem = xs;
+  if ((p.n_cols > 0 && !x) || (p.n_rows > 0 && !y)) return SPMV_ERR_INVALID_ARG;
+  if (((uintptr_t)x % xs) || ((uintptr_t)y % 4)) return SPMV_ERR_INVALID_ARG;
+  const uintptr_t x0 = (uintptr_t)x, x1 = x0 + (uintptr_t)p.n_cols * xs;
+  const uintptr_t y0 = (uintptr_t)y, y1 = y0 + (uintptr_t)p.n_rows * 4;
+  if (p.n_cols > 0 && p.n_rows > 0 && x0 < y1 && y0 < x1)
+    return SPMV_ERR_INVALID_ARG;
+  return SPMV_OK;
+}
+
+spmv_status spmv_run(spmv_plan* plan, const void* x, float* y, void* stream) {
+  if (!plan) return SPMV_ERR_INVALID_ARG;
+  Plan& p = plan->impl;
+  size_t xs;
+  spmv_status s = check_run_args(p, x, y, &xs);
+  if (s != SPMV_OK) return s;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
+  if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
+  if (p.n_rows == 0) return SPMV_OK;
+  int rc = p.format == SPMV_FORMAT_CSR ? launch_csr(p, x, y, stream)
+                                       : launch_delta(p, x, y, stream);
+  return rc == 0 ? SPMV_OK : SPMV_ERR_CUDA;
+}
+
+spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
+                          void* stream) {
+  if (!plan) return SPMV_ERR_INVALID_ARG;
+  Plan& p = plan->impl;
+  if ((p.n_cols > 0 && !x_host) || (p.n_rows > 0 && !y_host))
+    return SPMV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
+  if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xs =
+      (p.format == SPMV_FORMAT_CSR && p.dtype == SPMV_F32) ? 4 : 2;
+  if (p.n_cols > 0 &&
+      cudaMemcpyAsync(p.x_stage, x_host, (size_t)p.n_cols * xs,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  spmv_status s = spmv_run(plan, p.x_stage, p.y_stage, stream);
+  if (s != SPMV_OK) return s;
+  if (p.n_rows > 0 &&
+      cudaMemcpyAsync(y_host, p.y_stage, (size_t)p.n_rows * 4,
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
+}
+
+spmv_status spmv_plan_check(spmv_plan* plan) {
+  if (!plan) return SPMV_ERR_INVALID_ARG;
+  Plan& p = plan->impl;
+  DeviceGuard g(p.device);
+  if (!g.ok) return SPMV_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPMV_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, p.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  if (word != 0) {
+    cudaMemset(p.status, 0, 4);
+    return SPMV_ERR_DEVICE_STATUS;
+  }
+  return SPMV_OK;
+}
+
+void spmv_plan_destroy(spmv_plan* plan) {
+  if (!plan) return;
+  free_plan(plan);
+}
+
+}  // extern "C"

@@ -1,0 +1,232 @@
+"""CPU tests of the C ABI: the library loads, exports every function that
+include/spmv.h declares, its structs match the C layout, host-side
+validation and the DELTA4 converter behave, and the planner's bins are
+consistent. Nothing here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from sparse_matrix_vector_gb300 import _lib
+import sparse_matrix_vector_gb300 as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spmv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(spmv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(spmv_lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(spmv_lib, n), n
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_abi_version_and_status_strings(spmv_lib):
+    assert S.spmv_abi_version() == 1
+    for code in range(11):
+        s = S.spmv_status_string(code)
+        assert s and s != "unknown status"
+    assert S.spmv_status_string(99) == "unknown status"
+
+
+STRUCTS = {
+    "spmv_csr": _lib.spmv_csr, "spmv_delta": _lib.spmv_delta,
+    "spmv_plan_options": _lib.spmv_plan_options,
+    "spmv_plan_info": _lib.spmv_plan_info,
+}
+
+
+def test_struct_layout_matches_c(tmp_path):
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spmv.h"',
+             'int main(void) {']
+    for cname, ct in STRUCTS.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in ct._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe),
+                    str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True,
+                         text=True).stdout.split("\n")
+    got = {}
+    for line in out:
+        if line:
+            s, f, v = line.split()
+            got[(s, f)] = int(v)
+    for cname, ct in STRUCTS.items():
+        assert got[(cname, "size")] == ctypes.sizeof(ct), cname
+        for f, _ in ct._fields_:
+            assert got[(cname, f)] == getattr(ct, f).offset, (cname, f)
+
+
+def _csr(rp, ci, vals, n_cols):
+    return S.api._host_csr(np.asarray(rp), np.asarray(ci), np.asarray(vals), n_cols)
+
+
+@pytest.mark.parametrize("rp,ci,n_cols,err", [
+    ([1, 2], [0, 0], 4, 2),            # row_ptr[0] != 0
+    ([0, 2, 1], [0, 1], 4, 2),         # decreasing
+    ([0, 1], [0, 1], 4, 2),            # last != nnz
+    ([0, 2], [0, 4], 4, 3),            # column == n_cols
+    ([0, 2], [-1, 1], 4, 3),           # negative column
+])
+def test_validation_errors(spmv_lib, rp, ci, n_cols, err):
+    vals = np.ones(len(ci), np.float32)
+    h = _csr(rp, ci, vals, n_cols)
+    h.struct.nnz = len(ci)
+    info = _lib.spmv_plan_info()
+    st = spmv_lib.spmv_plan_inspect(ctypes.byref(h.struct), 0, None,
+                                    ctypes.byref(info))
+    assert st == err
+    out = ctypes.c_void_p()
+    # validation comes before any device call, so this needs no GPU
+    st = spmv_lib.spmv_plan_create(ctypes.byref(h.struct), 0, ctypes.byref(out))
+    assert st == err and not out.value
+
+
+def test_delta_needs_sorted_fp16(spmv_lib):
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_convert([0, 3], [1, 5, 3], np.ones(3, np.float16), 10)
+    assert e.value.status == 4
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_convert([0, 2], [1, 1], np.ones(2, np.float16), 10)
+    assert e.value.status == 4
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_convert([0, 2], [1, 2], np.ones(2, np.float32), 10)
+    assert e.value.status == 5
+    # CSR accepts unsorted and repeated columns
+    S.spmv_plan_inspect([0, 3], [5, 1, 5], np.ones(3, np.float32), 10)
+
+
+def test_null_and_bad_args(spmv_lib):
+    info = _lib.spmv_plan_info()
+    assert spmv_lib.spmv_plan_inspect(None, 0, None, ctypes.byref(info)) == 1
+    h = _csr([0, 1], [0], np.ones(1, np.float32), 1)
+    assert spmv_lib.spmv_plan_inspect(ctypes.byref(h.struct), 7, None,
+                                      ctypes.byref(info)) == 1
+    h.struct.value_dtype = 5
+    assert spmv_lib.spmv_plan_inspect(ctypes.byref(h.struct), 0, None,
+                                      ctypes.byref(info)) == 1
+    assert spmv_lib.spmv_run(None, None, None, None) == 1
+    assert spmv_lib.spmv_run_host(None, None, None, None) == 1
+    assert spmv_lib.spmv_plan_check(None) == 1
+    spmv_lib.spmv_plan_destroy(None)
+    d = _lib.spmv_delta()
+    spmv_lib.spmv_delta_free(ctypes.byref(d))
+    assert spmv_lib.spmv_convert(None, ctypes.byref(d)) == 1
+
+
+def _converter_matches_oracle(m, n_cols=None):
+    n_cols = m.n_cols if n_cols is None else n_cols
+    got = S.spmv_convert(m.row_ptr, m.col_idx, m.values, n_cols)
+    ref = oracle.delta_encode(n_cols, m.row_ptr, m.col_idx, m.values)
+    assert np.array_equal(got.row_ptr, ref.row_ptr)
+    assert np.array_equal(got.values, ref.values)
+    assert np.array_equal(got.words, ref.words)
+    assert got.n_gap_pads == ref.gap_pads and got.n_align_pads == ref.align_pads
+    assert got.nnz == m.nnz
+    return got
+
+
+@pytest.mark.parametrize("sparsity", [0.3, 0.5, 0.7, 0.9, 0.99])
+def test_converter_bit_exact_llm_small(spmv_lib, sparsity):
+    _converter_matches_oracle(workloads.llm(sparsity, n=700))
+
+
+def test_converter_bit_exact_edge_rows(spmv_lib):
+    lengths = np.array([0, 1, 8, 7, 9, 0, 0, 16, 33, 1, 2000])
+    m = workloads.from_lengths("edges", lengths, 5000, seed=9, dtype=np.float16)
+    _converter_matches_oracle(m)
+    # first column 0, exact multiples of 15, a gap spanning the whole row
+    rp = np.array([0, 4, 6, 7], np.int32)
+    ci = np.array([0, 15, 30, 31, 0, 4999, 2999], np.int32)
+    vals = np.arange(1, 8).astype(np.float16)
+    m = workloads.CSRInput("hand", 3, 5000, rp, ci, vals, np.zeros(5000, np.float16))
+    _converter_matches_oracle(m)
+    # explicit +0.0 values are stored as such and counted
+    vals0 = vals.copy()
+    vals0[2] = 0
+    got = S.spmv_convert(rp, ci, vals0, 5000)
+    assert got.n_explicit_zeros == 1
+
+
+@pytest.mark.slow
+def test_converter_bit_exact_llm_full(spmv_lib):
+    _converter_matches_oracle(workloads.llm(0.9))
+
+
+def expected_bins(lengths, opts):
+    """Bins the planner must produce, computed from the row lengths alone."""
+    split = lengths > opts.split_row_min
+    cta = (lengths > opts.cta_row_min) & ~split
+    chunks = np.sum((lengths[split] + opts.split_chunk - 1) // opts.split_chunk)
+    return int(cta.sum()), int(split.sum()), int(chunks)
+
+
+@pytest.mark.parametrize("kw", [{}, {"cta_row_min": 32}, {"split_row_min": 300,
+                                                         "split_chunk": 128},
+                                {"tile_nnz": 300, "tile_rows": 64},
+                                {"lanes": 4}])
+def test_planner_bins(spmv_lib, kw):
+    m = workloads.powerlaw(n=40000, nnz=223000, max_len=2000)
+    opts = S.spmv_plan_options(**kw)
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols,
+                               options=opts)
+    L = m.row_lengths()
+    n_cta, n_split, n_chunks = expected_bins(L, opts)
+    assert sum(info["rows_per_bin"]) == m.n_rows
+    assert info["rows_per_bin"][2] == n_cta == info["tiles_per_bin"][2]
+    assert info["rows_per_bin"][3] == n_split == info["n_split_rows"]
+    assert info["tiles_per_bin"][3] == n_chunks
+    short = L[L <= min(opts.cta_row_min, opts.tile_nnz)]
+    min_tiles = max(int(np.ceil(short.sum() / opts.tile_nnz)),
+                    int(np.ceil(short.size / opts.tile_rows)))
+    assert info["tiles_per_bin"][0] + info["tiles_per_bin"][1] >= min_tiles
+    assert info["n_tiles"] == sum(info["tiles_per_bin"])
+    if kw.get("lanes"):
+        assert info["tiles_per_bin"][1] == 0
+    assert info["algorithmic_bytes"] == (8 * m.nnz + 4 * (m.n_rows + 1)
+                                         + 4 * m.n_cols + 4 * m.n_rows)
+
+
+def test_planner_regular_matrices_pick_lanes(spmv_lib):
+    lap = workloads.laplacian(300, 200)
+    info = S.spmv_plan_inspect(lap.row_ptr, lap.col_idx, lap.values, lap.n_cols)
+    assert info["rows_per_bin"][0] == lap.n_rows   # short rows, sub-warp bin
+    fem = workloads.fem(6, 5, 4)
+    info = S.spmv_plan_inspect(fem.row_ptr, fem.col_idx, fem.values, fem.n_cols)
+    assert info["rows_per_bin"][2] == 0 and info["rows_per_bin"][3] == 0
+    llm = workloads.llm(0.3, n=2048)
+    info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols)
+    assert info["rows_per_bin"][2] == llm.n_rows   # one CTA per row
+    assert info["x_in_smem"] == 1
+    info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
+                               format="delta4")
+    enc = oracle.delta_encode(llm.n_cols, llm.row_ptr, llm.col_idx, llm.values)
+    assert info["n_entries"] == enc.n_entries
+    assert info["matrix_bytes"] == 2 * enc.n_entries + enc.n_entries // 2 + 4 * (llm.n_rows + 1)
+
+
+def test_empty_and_degenerate_inspect(spmv_lib):
+    info = S.spmv_plan_inspect(np.zeros(1, np.int32), np.zeros(0, np.int32),
+                               np.zeros(0, np.float32), 0)
+    assert info["n_tiles"] == 0 and info["launches_per_run"] == 0
+    info = S.spmv_plan_inspect(np.zeros(5001, np.int32), np.zeros(0, np.int32),
+                               np.zeros(0, np.float32), 3)
+    assert sum(info["rows_per_bin"]) == 5000 and info["n_tiles"] >= 5

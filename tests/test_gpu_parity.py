@@ -1,0 +1,352 @@
+"""GPU parity: the library's kernels (through the C ABI) against the fp64
+oracle, element by element, on the seeded workloads and on edge cases.
+
+Tolerances (per row i, s_i = sum_j |a_ij x_j| from the oracle):
+  fp32 CSR:                   |y - y_ref| <= 1e-5 * s_i + 1e-30
+  fp16 values (CSR, DELTA4):  |y - y_ref| <= 2e-3 * s_i
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+S = pytest.importorskip("sparse_matrix_vector_gb300")
+
+pytestmark = pytest.mark.gpu
+
+TOL32 = 1e-5
+TOL16 = 2e-3
+
+
+@functools.lru_cache(maxsize=None)
+def full(name):
+    return workloads.make(name)
+
+
+_REF = {}
+
+
+def reference(m):
+    """Oracle result for a workload object (cached by identity)."""
+    hit = _REF.get(id(m))
+    if hit is None or hit[0] is not m:
+        hit = (m, oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x))
+        _REF[id(m)] = hit
+    return hit[1]
+
+
+def run_gpu(m, fmt="csr", options=None, x=None, stream=None, repeat=1):
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols,
+                              format=fmt, options=options)
+    xt = torch.from_numpy(np.ascontiguousarray(m.x if x is None else x)).to(dev)
+    outs = []
+    for _ in range(repeat):
+        y = torch.full((m.n_rows,), float("nan"), dtype=torch.float32, device=dev)
+        S.spmv_run(plan, xt, y, stream=stream)
+        outs.append(y)
+    torch.cuda.synchronize()
+    S.spmv_plan_check(plan)
+    info = plan.info
+    S.spmv_plan_destroy(plan)
+    ys = [o.cpu().numpy() for o in outs]
+    return (ys if repeat > 1 else ys[0]), info
+
+
+def assert_parity(m, y, tol, y_ref=None, s=None):
+    if y_ref is None:
+        y_ref, s = reference(m)
+    y = y.astype(np.float64)
+    assert y.shape == y_ref.shape
+    assert np.all(np.isfinite(y)), "non-finite outputs (unwritten rows?)"
+    err = np.abs(y - y_ref)
+    bound = tol * s + 1e-30
+    bad = np.nonzero(err > bound)[0]
+    assert bad.size == 0, (f"{m.name}: {bad.size} rows out of tolerance, first "
+                           f"{bad[:5]}, max |dy|/s = {np.max(err / np.maximum(s, 1e-300)):.3e}")
+
+
+def tol_for(m):
+    return TOL32 if m.values.dtype == np.float32 else TOL16
+
+
+# ------------------------------------------------------------ the workloads
+
+SMALL = {
+    "tiny": lambda: workloads.tiny(),
+    "laplacian_small": lambda: workloads.laplacian(300, 211),
+    "powerlaw_small": lambda: workloads.powerlaw(n=50000, nnz=278500, max_len=4334),
+    "fem_small": lambda: workloads.fem(12, 9, 7),
+    "llm30_small": lambda: workloads.llm(0.3, n=1536),
+    "llm90_small": lambda: workloads.llm(0.9, n=2000),
+}
+
+
+@functools.lru_cache(maxsize=None)
+def small(name):
+    return SMALL[name]()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_csr(name):
+    m = small(name)
+    y, _ = run_gpu(m)
+    assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("name", ["llm30_small", "llm90_small"])
+def test_small_delta4(name):
+    m = small(name)
+    y, info = run_gpu(m, "delta4")
+    assert info["format"] == 1
+    assert_parity(m, y, TOL16)
+
+
+@pytest.mark.parametrize("name", ["tiny", "laplacian", "powerlaw", "fem",
+                                  "llm30", "llm50", "llm70", "llm90"])
+def test_full_size_csr(name):
+    m = full(name)
+    y, info = run_gpu(m)
+    assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("name", ["llm30", "llm50", "llm70", "llm90"])
+def test_full_size_delta4(name):
+    m = full(name)
+    y, info = run_gpu(m, "delta4")
+    assert info["n_entries"] >= m.nnz
+    assert_parity(m, y, TOL16)
+
+
+# ------------------------------------------------------------ forced paths
+
+@pytest.mark.parametrize("kw", [
+    {"lanes": 1}, {"lanes": 2}, {"lanes": 4}, {"lanes": 8}, {"lanes": 16},
+    {"lanes": 32}, {"cta_row_min": 16}, {"split_row_min": 200, "split_chunk": 64},
+    {"split_row_min": 1000, "split_chunk": 1000}, {"tile_nnz": 97, "tile_rows": 13},
+    {"x_smem": 0}, {"x_smem": 1}, {"tile_rows": 1},
+])
+def test_forced_planner_paths(kw):
+    m = workloads.powerlaw(n=30000, nnz=167000, max_len=3000, seed=11)
+    opts = S.spmv_plan_options(**kw)
+    y, info = run_gpu(m, options=opts)
+    assert_parity(m, y, TOL32)
+
+
+@pytest.mark.parametrize("kw", [{"x_smem": 0}, {"x_smem": 1},
+                                {"split_row_min": 500, "split_chunk": 300}])
+def test_forced_paths_fp16_csr(kw):
+    m = workloads.llm(0.8, n=1000, seed=3)
+    y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
+    assert_parity(m, y, TOL16)
+
+
+@pytest.mark.parametrize("x_smem", [0, 1])
+def test_delta4_x_paths(x_smem):
+    m = workloads.llm(0.6, n=3000, seed=8)
+    y, info = run_gpu(m, "delta4", options=S.spmv_plan_options(x_smem=x_smem))
+    assert info["x_in_smem"] == x_smem
+    assert_parity(m, y, TOL16)
+
+
+# ------------------------------------------------------------ edge cases
+
+def make(name, rp, ci, vals, n_cols, x):
+    return workloads.CSRInput(name, len(rp) - 1, n_cols, np.asarray(rp, np.int32),
+                              np.asarray(ci, np.int32), np.asarray(vals),
+                              np.asarray(x), {})
+
+
+def test_empty_matrix():
+    m = make("empty", [0], [], np.zeros(0, np.float32), 5, np.ones(5, np.float32))
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, 5)
+    x = torch.ones(5, device="cuda")
+    y = torch.empty(0, device="cuda")
+    S.spmv_run(plan, x, y)
+    torch.cuda.synchronize()
+    assert plan.info["launches_per_run"] == 0
+
+
+def test_rows_without_nonzeros():
+    n = 5000
+    m = make("zero_nnz", np.zeros(n + 1), [], np.zeros(0, np.float32), 7,
+             np.ones(7, np.float32))
+    y, _ = run_gpu(m)
+    assert np.all(y == 0)
+
+
+def test_one_by_one_and_single_row():
+    m = make("1x1", [0, 1], [0], np.array([3.0], np.float32), 1,
+             np.array([2.0], np.float32))
+    y, _ = run_gpu(m)
+    assert y[0] == 6.0
+    n = 250_000
+    rng = np.random.default_rng(4)
+    m = make("one_long_row", [0, n], np.arange(n), rng.uniform(-1, 1, n).astype(np.float32),
+             n, rng.uniform(-1, 1, n).astype(np.float32))
+    y, info = run_gpu(m)
+    assert info["rows_per_bin"][3] == 1
+    assert_parity(m, y, TOL32)
+
+
+@pytest.mark.parametrize("fmt", ["csr", "delta4"])
+def test_interleaved_empty_and_long_rows(fmt):
+    lengths = np.tile([0, 1, 0, 3, 9, 0, 257, 0, 5000, 2, 20000, 0], 40)
+    dt = np.float32 if fmt == "csr" else np.float16
+    m = workloads.from_lengths("mixed", lengths, 30000, seed=13, dtype=dt)
+    y, _ = run_gpu(m, fmt)
+    assert_parity(m, y, tol_for(m))
+
+
+def test_rectangular():
+    m = workloads.from_lengths("wide", np.full(10, 3000), 100_000, seed=1)
+    y, _ = run_gpu(m)
+    assert_parity(m, y, TOL32)
+    m = workloads.from_lengths("tall", np.random.default_rng(2).integers(0, 4, 100_000),
+                               3, seed=2)
+    y, _ = run_gpu(m)
+    assert_parity(m, y, TOL32)
+
+
+def test_unsorted_duplicates_and_explicit_zeros():
+    rng = np.random.default_rng(6)
+    n_rows, n_cols = 3000, 500
+    lengths = rng.integers(0, 40, n_rows)
+    rp = np.concatenate([[0], np.cumsum(lengths)])
+    ci = rng.integers(0, n_cols, rp[-1])           # unsorted, with repeats
+    vals = rng.uniform(-1, 1, rp[-1]).astype(np.float32)
+    vals[::7] = 0.0
+    m = make("unsorted", rp, ci, vals, n_cols, rng.uniform(-1, 1, n_cols).astype(np.float32))
+    y, _ = run_gpu(m)
+    assert_parity(m, y, TOL32)
+
+
+def test_unaligned_row_starts_every_length():
+    # row lengths 0..40 repeated: every start offset modulo 4 and 8 appears
+    lengths = np.tile(np.arange(41), 30)
+    m = workloads.from_lengths("ragged", lengths, 4096, seed=21)
+    for kw in ({}, {"lanes": 1}, {"lanes": 32}, {"cta_row_min": 8}):
+        y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
+        assert_parity(m, y, TOL32)
+
+
+def test_x_unaligned_pointer_staging():
+    # x starts 4 bytes past a 16-byte boundary: scalar staging path
+    m = workloads.tiny()
+    dev = torch.device("cuda", 0)
+    big = torch.zeros(m.n_cols + 4, dtype=torch.float32, device=dev)
+    big[1:1 + m.n_cols] = torch.from_numpy(m.x).to(dev)
+    x = big[1:1 + m.n_cols]
+    assert x.data_ptr() % 16 == 4
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols,
+                              options=S.spmv_plan_options(x_smem=1))
+    y = torch.empty(m.n_rows, dtype=torch.float32, device=dev)
+    S.spmv_run(plan, x, y)
+    torch.cuda.synchronize()
+    assert_parity(m, y.cpu().numpy(), TOL32)
+
+
+def test_delta4_gap_patterns():
+    # first column 0, gaps of exactly 15/16/30/31, a gap across the row
+    rows = [[0, 15, 30, 31, 47], [16], [31, 32, 33, 34, 35, 36, 37, 38],
+            [0], [4095], list(range(0, 4096, 17)), list(range(2000, 2050)),
+            list(range(0, 4096, 2))]
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])])
+    ci = np.concatenate([np.array(r) for r in rows])
+    rng = np.random.default_rng(5)
+    vals = rng.normal(0, 0.5, ci.size).astype(np.float16)
+    vals[vals == 0] = np.float16(0.25)
+    m = make("gaps", rp, ci, vals, 4096, rng.normal(0, 1, 4096).astype(np.float16))
+    for kw in ({}, {"x_smem": 0}):
+        y, _ = run_gpu(m, "delta4", options=S.spmv_plan_options(**kw))
+        assert_parity(m, y, TOL16)
+
+
+def test_plan_from_converted_delta():
+    m = workloads.llm(0.75, n=900, seed=4)
+    d = S.spmv_convert(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    plan = S.spmv_plan_create_delta(d)
+    dev = torch.device("cuda", 0)
+    y = torch.empty(m.n_rows, dtype=torch.float32, device=dev)
+    S.spmv_run(plan, torch.from_numpy(m.x).to(dev), y)
+    torch.cuda.synchronize()
+    y2, _ = run_gpu(m, "delta4")
+    assert np.array_equal(y.cpu().numpy(), y2)
+    assert_parity(m, y2, TOL16)
+
+
+def test_delta_plan_rejects_bad_columns():
+    m = workloads.llm(0.75, n=64, seed=4)
+    d = S.spmv_convert(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    d.n_cols = int(m.col_idx.max())          # last column now out of range
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_plan_create_delta(d)
+    assert e.value.status == 3
+
+
+# ------------------------------------------------------------ runtime behaviour
+
+def test_repeated_runs_identical_and_split_counters_rearm():
+    m = workloads.powerlaw(n=20000, nnz=111000, max_len=3000, seed=2)
+    ys, info = run_gpu(m, options=S.spmv_plan_options(split_row_min=300, split_chunk=100),
+                       repeat=4)
+    assert info["rows_per_bin"][3] > 0
+    for y in ys[1:]:
+        assert np.array_equal(y, ys[0])
+    assert_parity(m, ys[0], TOL32)
+
+
+def test_side_stream_and_graph_capture():
+    m = small("powerlaw_small")
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    x = torch.from_numpy(m.x).to(dev)
+    y = torch.zeros(m.n_rows, dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        S.spmv_run(plan, x, y)
+    s.synchronize()
+    y_stream = y.cpu().numpy().copy()
+    g = torch.cuda.CUDAGraph()
+    y.zero_()
+    with torch.cuda.graph(g):
+        S.spmv_run(plan, x, y)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), y_stream)
+    assert_parity(m, y_stream, TOL32)
+    S.spmv_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("fmt,name", [("csr", "laplacian_small"), ("delta4", "llm90_small")])
+def test_run_host_end_to_end(fmt, name):
+    m = small(name)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
+    xh = torch.from_numpy(m.x).pin_memory().numpy()
+    yh = torch.empty(m.n_rows, dtype=torch.float32).pin_memory().numpy()
+    S.spmv_run_host(plan, xh, yh)
+    assert_parity(m, yh, tol_for(m))
+    S.spmv_plan_destroy(plan)
+
+
+def test_argument_errors():
+    m = small("tiny")
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    dev = torch.device("cuda", 0)
+    x = torch.from_numpy(m.x).to(dev)
+    with pytest.raises(TypeError):
+        S.spmv_run(plan, x.half(), torch.empty(m.n_rows, device=dev))
+    with pytest.raises(ValueError):
+        S.spmv_run(plan, x[:-1], torch.empty(m.n_rows, device=dev))
+    buf = torch.empty(m.n_rows + m.n_cols, device=dev)
+    with pytest.raises(S.SpmvError) as e:         # x and y overlap
+        S.spmv_run(plan, buf.data_ptr(), buf.data_ptr() + 8)
+    assert e.value.status == 1
+    S.spmv_plan_destroy(plan)
+    with pytest.raises(ValueError):
+        S.spmv_run(plan, x, torch.empty(m.n_rows, device=dev))
