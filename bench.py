@@ -264,7 +264,9 @@ def bench_one(args, name, world, rank, local, pg):
     first = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
     info = first.info
     nbytes = int(info["algorithmic_bytes"])
-    copies = max(1, math.ceil(3 * l2 / nbytes))
+    # rotate copies until the loop's footprint is >= 3x L2 (at most 64 copies:
+    # below ~6 MB per copy the workload is latency-bound and stays L2-resident)
+    copies = min(64, max(1, math.ceil(3 * l2 / nbytes)))
     plans = [first] + [S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols,
                                           format=fmt) for _ in range(copies - 1)]
     xdt = torch.float32 if m.x.dtype == np.float32 else torch.float16
@@ -275,9 +277,9 @@ def bench_one(args, name, world, rank, local, pg):
     peak, peak_src = load_peak()
 
     steps = args.steps
-    if not steps:   # ~1.5 s of timed work at 70% of peak, at least 200 steps
-        est = nbytes / (0.7 * peak * 1e9)
-        steps = max(200, int(1.5 / est))
+    if not steps:   # ~1.5 s of timed work at 70% of peak (>= 3 us a step)
+        est = max(nbytes / (0.7 * peak * 1e9), 3e-6)
+        steps = min(200_000, max(200, int(1.5 / est)))
         steps = int(math.ceil(steps / copies) * copies)
     warmup = max(3, args.warmup)
 
@@ -363,8 +365,10 @@ def bench_one(args, name, world, rank, local, pg):
                        "bins_tiles": info["tiles_per_bin"],
                        "grid": info["grid"], "x_in_smem": bool(info["x_in_smem"]),
                        "l2": (f"rotating {copies} resident copies, "
-                              f"{copies * nbytes / 2**20:.0f} MiB >= 3x L2 "
-                              f"({l2 / 2**20:.0f} MiB)"),
+                              f"{copies * nbytes / 2**20:.0f} MiB "
+                              + (">= 3x" if copies * nbytes >= 3 * l2 else
+                                 "< L2: latency-bound, L2-resident,")
+                              + f" L2 ({l2 / 2**20:.0f} MiB)"),
                        "timing": "CUDA graphs of back-to-back spmv_run, CUDA "
                                  "events on the launching stream",
                        "parallelism": f"replicas{world}"},
