@@ -216,6 +216,33 @@ spmv_status spmv_run(spmv_plan* plan, const void* x_dev, float* y_dev,
 spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
                           void* stream);
 
+/* Allocation-free y = A x for a CSR matrix the caller already holds in
+ * device memory (the pages have no counterpart: this entry point exists for
+ * callers that may not allocate device memory -- a latency-critical loop
+ * after its set-up phase, where cudaMalloc could synchronise the device; a
+ * component inside a memory pool that owns all device memory; a plug-in
+ * handed device buffers but no allocator. spmv_plan_create allocates, so
+ * those callers cannot use plans).
+ * row_ptr (n_rows+1), col_idx (nnz), values (nnz, value_dtype) and x (n_cols,
+ * fp32 for SPMV_F32 values, fp16 for SPMV_F16) are caller-owned DEVICE
+ * arrays on the current device and must form a valid CSR matrix (row_ptr
+ * non-decreasing from 0 to nnz, columns in [0, n_cols)); they are not
+ * validated. Alignment: col_idx 16 bytes, values 16 (fp32) or 8 (fp16)
+ * bytes, row_ptr and y 4 bytes. y (n_rows fp32) is overwritten. Runs two
+ * kernels on `stream`; calls no allocating routine.
+ * Scratch: a file-scope device array of 768 KiB per device, shared by all
+ * calls and held until the process exits; calls that overlap on the GPU
+ * race on it, so order them (one stream). The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.
+ * Errors: INVALID_ARG (negative sizes, null or misaligned pointers),
+ * TOO_LARGE (nnz > 134,217,728, the scratch limit), CUDA. */
+spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols, int64_t nnz,
+                                 const int32_t* row_ptr,
+                                 const int32_t* col_idx, const void* values,
+                                 spmv_dtype value_dtype, const void* x,
+                                 float* y, void* stream);
+
 /* Synchronize the plan's device and read its device status word: OK, or
  * DEVICE_STATUS if a kernel reported an error since the last check (the
  * word is cleared by this call). */

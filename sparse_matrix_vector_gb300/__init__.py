@@ -6,6 +6,7 @@ The compiled library is ``libspmv_gb300.so`` next to this file (built by
 """
 from .api import (  # noqa: F401
     DeltaMatrix, Plan, SpmvError, spmv_abi_version, spmv_convert,
+    spmv_csr_run_noalloc,
     spmv_plan_check, spmv_plan_create, spmv_plan_create_delta,
     spmv_plan_destroy, spmv_plan_inspect, spmv_plan_options, spmv_run,
     spmv_run_host, spmv_status_string,

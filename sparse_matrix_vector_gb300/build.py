@@ -19,7 +19,7 @@ LIB_NAME = "libspmv_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["spmv_host.cpp", "spmv_kernels.cu"]
+SOURCES = ["spmv_host.cpp", "spmv_kernels.cu", "spmv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
