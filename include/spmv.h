@@ -116,17 +116,24 @@ typedef struct spmv_plan_options {
   int32_t split_chunk;   /* nonzeros per chunk of a split row              */
   int32_t x_smem;        /* -1 auto, 0 never, 1 whenever x fits: stage x in
                             shared memory once per CTA                     */
-  int32_t lanes;         /* 0 auto, else force 1..32 lanes per short row   */
-  int32_t reserved[9];
+  int32_t reduce;        /* short-row tiles: 0 auto (per tile, by a cost
+                            model of its row lengths), 1 lanes mode (rows
+                            summed by `lanes` lanes from shared memory),
+                            2 walk mode (per-thread segmented sums)        */
+  int32_t lanes;         /* lanes per row in forced lanes mode: 1..32      */
+  int32_t reserved[8];
 } spmv_plan_options;
 
 /* What the planner decided; filled by spmv_plan_inspect / spmv_plan_get_info.
- * Bins ([SPGEMM] section 2.1.1, adapted to nonzeros per row):
- *   0 sub-warp: short rows batched in tiles, 1..16 lanes per row
- *   1 warp:     short rows batched in tiles, 32 lanes per row
- *   2 CTA:      one CTA per row
- *   3 split:    a row cut into chunks, one CTA per chunk, partial sums
- *               combined by the last chunk to finish                      */
+ * Row bins ([SPGEMM] section 2.1.1, adapted to nonzeros per row; a short-row
+ * tile hands every thread 8 consecutive nonzeros, so the bin says how many
+ * threads cooperate on a row):
+ *   0 sub-warp: <= 8 nonzeros (1-2 threads)
+ *   1 warp:     9..256 nonzeros (up to 33 threads)
+ *   2 CTA:      257..split_row_min nonzeros (up to the whole CTA)
+ *   3 split:    longer rows, cut into chunks across CTAs
+ * tiles_per_bin: [0] short-row tiles (any mix of bins 0-2), [1] unused,
+ * [2] single-row tiles, [3] split chunks. */
 typedef struct spmv_plan_info {
   int32_t n_rows;
   int32_t n_cols;
@@ -145,7 +152,8 @@ typedef struct spmv_plan_info {
   int64_t matrix_bytes;      /* stored matrix: values + indices + row ptrs */
   int64_t aux_bytes;         /* planner tables and scratch on the device   */
   int64_t algorithmic_bytes; /* matrix_bytes + x read once + y written     */
-  int64_t reserved[8];
+  int64_t walk_tiles;        /* short-row tiles reduced in walk mode       */
+  int64_t reserved[7];
 } spmv_plan_info;
 
 typedef struct spmv_plan spmv_plan;

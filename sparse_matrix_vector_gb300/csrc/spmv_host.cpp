@@ -95,12 +95,48 @@ inline void emit(uint16_t* vals, uint32_t* words, int64_t e, uint16_t bits,
   words[e >> 3] |= code << (4 * (uint32_t)(e & 7));
 }
 
-// ------------------------------------------------------------ lanes choice
-// Short-row tiles reduce each row with g = 2^lg lanes. Cost estimate of a
-// choice: for every warp, sum over passes of the slowest row it owns in that
-// pass (ceil(len / g) additions) plus lg shuffle steps; the tile costs as
-// much as its slowest warp.
-int choose_lanes_log2(const int32_t* rp, int r0, int r1) {
+}  // namespace
+
+Options resolve_options(const spmv_plan_options* o) {
+  Options r;
+  r.tile_nnz = kStreamTileCap;
+  r.tile_rows = kTileRowsCap;
+  r.cta_row_min = kStreamTileCap;
+  r.split_row_min = kTileCap;
+  r.split_chunk = kTileCap;
+  r.x_smem = -1;
+  r.reduce = -1;
+  r.lanes_log2 = 0;
+  if (o) {
+    if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, kStreamTileCap);
+    if (o->tile_rows > 0) r.tile_rows = std::min(o->tile_rows, kTileRowsCap);
+    if (o->cta_row_min > 0) r.cta_row_min = o->cta_row_min;
+    if (o->split_row_min > 0) r.split_row_min = o->split_row_min;
+    if (o->split_chunk > 0) r.split_chunk = std::min(std::max(o->split_chunk, 64), kTileCap);
+    if (o->x_smem >= 0) r.x_smem = o->x_smem ? 1 : 0;
+    if (o->reduce == 1) {
+      r.reduce = 0;
+      int l = 0;
+      while ((2 << l) <= std::min(std::max(o->lanes, 1), 32)) ++l;
+      r.lanes_log2 = l;
+    } else if (o->reduce == 2) {
+      r.reduce = 1;
+    }
+  }
+  // a row that may sit in a short-row tile must fit one on its own, and a
+  // row that is not split must fit one stage
+  r.cta_row_min = std::min(r.cta_row_min, r.tile_nnz);
+  r.split_row_min = std::min(std::max(r.split_row_min, r.cta_row_min), kTileCap);
+  return r;
+}
+
+// Reduction of a short-row tile. Lanes mode: products are parked in shared
+// memory and each row is summed by g = 2^lg lanes; a warp pays, per pass of
+// its rows, the slowest row's ceil(len / g) dependent additions plus lg
+// shuffles. Walk mode: every thread sums its own 8 products by row and rows
+// that cross threads are finished from per-thread carries; its cost is
+// roughly fixed (binary search, walk, carries). Pick the cheaper one.
+static uint32_t choose_reduction(const int32_t* rp, int r0, int r1) {
   const int R = r1 - r0;
   int best_lg = 0;
   int64_t best = INT64_MAX;
@@ -119,7 +155,7 @@ int choose_lanes_log2(const int32_t* rp, int r0, int r1) {
           const int64_t len = rp[r0 + rs + q + 1] - rp[r0 + rs + q];
           m = std::max(m, (len + g - 1) / g);
         }
-        t += m + lg + 1;
+        t += 4 * m + 8 * lg + 40;  // ~cycles: dependent adds, shuffles, loads
       }
       worst = std::max(worst, t);
     }
@@ -128,39 +164,20 @@ int choose_lanes_log2(const int32_t* rp, int r0, int r1) {
       best_lg = lg;
     }
   }
-  return best_lg;
+  const int64_t walk_cost = 600;  // ~cycles: search, walk, carries, extra pass
+  if (best > walk_cost) return kStreamWalk;
+  return (uint32_t)best_lg << kLanesShift;
 }
 
-int ilog2(int v) {
-  int l = 0;
-  while ((1 << (l + 1)) <= v) ++l;
-  return l;
-}
-
-}  // namespace
-
-Options resolve_options(const spmv_plan_options* o) {
-  Options r;
-  r.tile_nnz = kMaxTileNnz;
-  r.tile_rows = kMaxTileRows;
-  r.cta_row_min = 256;
-  r.split_row_min = 16384;
-  r.split_chunk = 4096;
-  r.x_smem = -1;
-  r.lanes = 0;
-  if (o) {
-    if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, kMaxTileNnz);
-    if (o->tile_rows > 0) r.tile_rows = std::min(o->tile_rows, kMaxTileRows);
-    if (o->cta_row_min > 0) r.cta_row_min = o->cta_row_min;
-    if (o->split_row_min > 0) r.split_row_min = o->split_row_min;
-    if (o->split_chunk > 0) r.split_chunk = std::max(o->split_chunk, 64);
-    if (o->x_smem >= 0) r.x_smem = o->x_smem ? 1 : 0;
-    if (o->lanes > 0) r.lanes = 1 << ilog2(std::min(o->lanes, 32));
-  }
-  // a row that may sit in a short-row tile must fit one on its own
-  r.cta_row_min = std::min(r.cta_row_min, r.tile_nnz);
-  r.split_row_min = std::max(r.split_row_min, r.cta_row_min);
-  return r;
+// Bin of a row by how many threads cooperate on it (nonzeros per row): a
+// short-row tile gives every thread 8 consecutive nonzeros, so a row of <= 8
+// spans at most 2 threads (sub-warp), <= 256 at most 33 (warp), a longer row
+// up to the whole CTA; rows above split_row_min are split across CTAs.
+static int row_bin(int64_t len, const Options& o) {
+  if (len > o.split_row_min) return 3;
+  if (len > 256) return 2;
+  if (len > 8) return 1;
+  return 0;
 }
 
 spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
@@ -177,12 +194,13 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
         const int64_t sid = (int64_t)out->splits.size();
         if (sid > (int64_t)kSplitIdMask || out->n_chunks + nch > kMaxIndex)
           return SPMV_ERR_TOO_LARGE;
-        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)nch});
+        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)nch, rp[r], 0});
         for (int64_t k = 0; k < nch; ++k) {
           const int64_t b = rp[r] + k * o.split_chunk;
           const int64_t e = std::min<int64_t>(b + o.split_chunk, rp[r + 1]);
+          const uint32_t flags = (k == 0 ? kSplitFirst : 0u) | (k == nch - 1 ? kSplitLast : 0u);
           out->tiles.push_back({r, (int32_t)b, (int32_t)e,
-                                (int32_t)((kKindSplit << kKindShift) |
+                                (int32_t)((kKindSplit << kKindShift) | flags |
                                           (uint32_t)sid)});
         }
         out->n_chunks += nch;
@@ -194,7 +212,7 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
       if (len > o.cta_row_min) {
         out->tiles.push_back(
             {r, rp[r], rp[r + 1], (int32_t)(kKindRow << kKindShift)});
-        info->rows_per_bin[2] += 1;
+        info->rows_per_bin[row_bin(len, o)] += 1;
         info->tiles_per_bin[2] += 1;
         ++r;
         continue;
@@ -205,16 +223,16 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
         const int64_t l = (int64_t)rp[r + 1] - rp[r];
         if (l > o.cta_row_min || nz + l > o.tile_nnz) break;
         nz += l;
+        info->rows_per_bin[row_bin(l, o)] += 1;
         ++r;
       }
-      const int lg = o.lanes ? ilog2(o.lanes) : choose_lanes_log2(rp, r0, r);
-      out->tiles.push_back(
-          {r0, rp[r0], rp[r],
-           (int32_t)((kKindStream << kKindShift) | ((uint32_t)lg << kLanesShift) |
-                     (uint32_t)(r - r0))});
-      const int bin = lg == 5 ? 1 : 0;
-      info->rows_per_bin[bin] += r - r0;
-      info->tiles_per_bin[bin] += 1;
+      const uint32_t mode = o.reduce == 1   ? kStreamWalk
+                            : o.reduce == 0 ? ((uint32_t)o.lanes_log2 << kLanesShift)
+                                            : choose_reduction(rp, r0, r);
+      out->tiles.push_back({r0, rp[r0], rp[r],
+                            (int32_t)((kKindStream << kKindShift) | mode | (uint32_t)(r - r0))});
+      if (mode & kStreamWalk) info->walk_tiles += 1;
+      info->tiles_per_bin[0] += 1;
     }
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
@@ -273,7 +291,7 @@ void free_plan(spmv_plan* plan) {
   Plan* p = &plan->impl;
   {
     DeviceGuard g(p->device);
-    void* bufs[] = {p->row_ptr, p->col_idx, p->values, p->words,
+    void* bufs[] = {p->row_ptr, p->col_idx, p->values,   p->words,
                     p->tiles,   p->splits,  p->partials, p->counters,
                     p->status,  p->x_stage, p->y_stage};
     for (void* b : bufs)
@@ -322,20 +340,20 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
   const size_t xbytes = (size_t)m->n_cols * vs;
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
             : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
-  p->dyn_smem = p->x_smem ? (xbytes + 15) / 16 * 16 : 0;
+  p->dyn_smem = (p->x_smem ? (xbytes + 15) / 16 * 16 : 0) +
+                kStages * csr_stage_bytes(m->value_dtype);
   p->n_tiles = (int64_t)t.tiles.size();
   p->split_chunk = o.split_chunk;
   if (set_kernel_smem_limits(p->dyn_smem, 0) != 0) return SPMV_ERR_CUDA;
-  if (p->x_smem) {
-    int occ = csr_kernel_occupancy(m->value_dtype, true, p->dyn_smem);
+  {
+    // persistent grid: every resident CTA pulls tiles until none is left
+    int occ = csr_kernel_occupancy(m->value_dtype, p->x_smem, p->dyn_smem);
     if (occ <= 0) return SPMV_ERR_CUDA;
     p->grid = (int)std::min<int64_t>(p->n_tiles, (int64_t)occ * p->sm_count);
-  } else {
-    p->grid = (int)p->n_tiles;
   }
   const size_t nnz_alloc = (size_t)m->nnz + kPadElems;
   if ((s = dev_upload(&p->row_ptr, m->row_ptr, ((size_t)m->n_rows + 1) * 4,
-                      ((size_t)m->n_rows + 1) * 4)) != SPMV_OK) return s;
+                      ((size_t)m->n_rows + 1 + kPadElems) * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->col_idx, m->col_idx, (size_t)m->nnz * 4,
                       nnz_alloc * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->values, m->values, (size_t)m->nnz * vs,
@@ -466,7 +484,8 @@ void spmv_plan_options_init(spmv_plan_options* o) {
   o->split_row_min = r.split_row_min;
   o->split_chunk = r.split_chunk;
   o->x_smem = r.x_smem;
-  o->lanes = r.lanes;
+  o->reduce = 0;
+  o->lanes = 0;
 }
 
 spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
@@ -574,9 +593,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   info->n_entries = m->nnz;
   info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * vs <=
                     (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);
-  info->grid = info->x_in_smem
-                   ? (int32_t)std::min<int64_t>(info->n_tiles, 8LL * kAssumedSms)
-                   : (int32_t)info->n_tiles;
+  info->grid = (int32_t)std::min<int64_t>(info->n_tiles, 4LL * kAssumedSms);
   info->launches_per_run = info->n_tiles > 0;
   info->matrix_bytes = m->nnz * (int64_t)(vs + 4) + ((int64_t)m->n_rows + 1) * 4;
   info->aux_bytes = (int64_t)(t.tiles.size() * sizeof(Tile) +

@@ -13,27 +13,39 @@ namespace spmv {
 // ---------------------------------------------------------------- geometry
 constexpr int kThreads = 256;            // CTA size of every kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kVec = 4;                  // col_idx elements per 16-byte load
-constexpr int kStreamVecs = 2;           // 4-element vectors per thread per tile
-// A short-row tile holds at most this many nonzeros: its aligned span of
-// kVec-element vectors must fit kThreads * kStreamVecs vectors.
-constexpr int kMaxTileNnz = kThreads * kVec * kStreamVecs - (kVec - 1);
-constexpr int kMaxTileRows = 1024;       // row offsets staged in shared memory
-constexpr int kProdCap = kThreads * kVec * kStreamVecs;  // products per tile
-constexpr int kRowUnroll = 2;            // vectors in flight per thread, long rows
+// CSR kernel: every work unit holds at most kTileCap nonzeros; its column,
+// value and row-pointer slices are staged in shared memory by TMA bulk
+// copies through a ring of kStages buffers.
+#ifndef SPMV_TILE_CAP
+#define SPMV_TILE_CAP 2048
+#endif
+#ifndef SPMV_STAGES
+#define SPMV_STAGES 2
+#endif
+constexpr int kTileCap = SPMV_TILE_CAP;
+// A short-row tile gives each thread one chunk of 8 consecutive nonzeros, so
+// its aligned span (start rounded down to 8) must fit kThreads * 8.
+constexpr int kStreamTileCap = (kTileCap < kThreads * 8 ? kTileCap : kThreads * 8) - 16;
+constexpr int kTileRowsCap = 512;        // rows of a short-row tile
+constexpr int kStages = SPMV_STAGES;
 constexpr int kDeltaWordsPerRound = kThreads;  // one 32-bit delta word per thread
 
 // Tile descriptor (one int4 per work unit of the CSR kernel).
-//   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | lg << 16 | rows}
+//   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | WALK? | lg << 16 | rows}
+//                   (WALK: reduce by per-thread walk; else 2^lg lanes per row)
 //   CTA-row tile:   {row,       nnz_begin, nnz_end, KIND_ROW}
-//   split chunk:    {row,       nnz_begin, nnz_end, KIND_SPLIT | split_id}
+//   split chunk:    {row,       nnz_begin, nnz_end, KIND_SPLIT | FIRST? | LAST? | split_id}
+//                   (FIRST / LAST: the chunk is the row's first / last one)
 constexpr uint32_t kKindShift = 30;
 constexpr uint32_t kKindStream = 0u;
 constexpr uint32_t kKindRow = 1u;
 constexpr uint32_t kKindSplit = 2u;
-constexpr uint32_t kLanesShift = 16;     // log2(lanes per row), 3 bits
 constexpr uint32_t kRowsMask = 0xFFFFu;  // rows of a short-row tile
-constexpr uint32_t kSplitIdMask = (1u << kKindShift) - 1u;
+constexpr uint32_t kLanesShift = 16;     // log2(lanes per row), 3 bits
+constexpr uint32_t kStreamWalk = 1u << 20;
+constexpr uint32_t kSplitFirst = 1u << 29;
+constexpr uint32_t kSplitLast = 1u << 28;
+constexpr uint32_t kSplitIdMask = (1u << 28) - 1u;
 
 struct Tile {
   int32_t a, b, c, d;
@@ -42,6 +54,8 @@ struct Tile {
 struct SplitInfo {
   int32_t first_slot;  // index of chunk 0's partial sum in the scratch array
   int32_t n_chunks;
+  int32_t row_begin;   // row_ptr[row]: chunk k starts at row_begin + k * chunk
+  int32_t reserved;
 };
 
 // Effective planner settings (defaults filled, limits applied).
@@ -52,7 +66,8 @@ struct Options {
   int split_row_min;
   int split_chunk;
   int x_smem;  // -1 auto, 0 off, 1 on
-  int lanes;   // 0 auto
+  int reduce;  // short-row tiles: -1 per-tile choice, 0 lanes mode, 1 walk mode
+  int lanes_log2;  // lanes mode when forced
 };
 
 Options resolve_options(const spmv_plan_options* o);
@@ -105,6 +120,7 @@ struct Plan {
 int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem);
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem);
 int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn);
+size_t csr_stage_bytes(spmv_dtype dtype);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 

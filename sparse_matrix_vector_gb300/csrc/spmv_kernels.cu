@@ -1,17 +1,21 @@
 // Device half of the library: the sm_103a kernels of y = A x.
 //
-// CSR kernel (one launch, one work unit per CTA, or a grid-stride loop when x
-// is staged in shared memory). Work units come from the host planner:
-//   short-row tile  -- a run of consecutive short rows whose nonzeros are
-//                      streamed with 16-byte loads across the whole CTA
-//                      (coalesced regardless of where rows start), multiplied
-//                      by the gathered x, parked in shared memory, then
-//                      reduced with 2^lg lanes per row (sub-warp / warp bins);
-//   CTA-row tile    -- one long row, the CTA strides over it, CTA reduction;
-//   split chunk     -- a slice of a very long row; the chunk's partial sum
-//                      goes to plan-owned scratch and the last chunk to
-//                      finish (atomic counter) adds the partials in chunk
-//                      order and writes y.
+// CSR kernel: persistent CTAs walk contiguous blocks of the work units and
+// stream each unit's column, value and row-pointer slices into shared memory
+// with TMA bulk copies (cp.async.bulk + mbarrier), keeping kStages units in
+// flight per CTA. Work units come from the host planner:
+//   short-row tile  -- a run of consecutive rows (<= 2032 nonzeros): every
+//                      thread multiplies 8 consecutive staged nonzeros by the
+//                      gathered x; rows are then summed either by 2^lg lanes
+//                      from shared memory (lanes mode, regular rows) or by a
+//                      per-thread walk with carries across threads (walk
+//                      mode, irregular rows) -- sub-warp / warp / CTA bins;
+//   CTA-row tile    -- one row of up to 2048 nonzeros, CTA-wide reduction;
+//   split chunk     -- a 2048-nonzero slice of a longer row; a CTA adds the
+//                      consecutive chunks it owns in per-thread registers;
+//                      a row shared by several CTAs is finished through
+//                      plan-owned scratch by the CTA that completes it
+//                      (atomic chunk count), in chunk order.
 // Sources: "CUDA CSR SpMV optimisation" (codechina.net) 2.1 (row sum), 3.1
 // (read-only path and shared-memory staging of x), 3.2 (vector loads), 4.1
 // (warp per row with shuffle reduction); "Hash-based multi-phase SpGEMM"
@@ -38,30 +42,6 @@ namespace {
 
 // ------------------------------------------------------------ load helpers
 // Matrix data is read exactly once: read-only path, no L1 allocation.
-__device__ __forceinline__ int4 ld_stream_i4(const int32_t* p) {
-  int4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
-  float4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-      : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-      : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
-  uint2 r;
-  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-      : "=r"(r.x), "=r"(r.y)
-      : "l"(p));
-  return r;
-}
-
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   uint4 r;
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -75,38 +55,6 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
   asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
   return r;
 }
-
-template <int Q>
-__device__ __forceinline__ int lane_of(const int4& c) {
-  return Q == 0 ? c.x : Q == 1 ? c.y : Q == 2 ? c.z : c.w;
-}
-
-// Four consecutive matrix values, widened to fp32 on use.
-template <typename VT>
-struct Vals4;
-
-template <>
-struct Vals4<float> {
-  float4 v;
-  __device__ __forceinline__ void load(const float* p) { v = ld_stream_f4(p); }
-  template <int Q>
-  __device__ __forceinline__ float get() const {
-    return Q == 0 ? v.x : Q == 1 ? v.y : Q == 2 ? v.z : v.w;
-  }
-};
-
-template <>
-struct Vals4<__half> {
-  uint2 v;
-  __device__ __forceinline__ void load(const __half* p) { v = ld_stream_u2(p); }
-  template <int Q>
-  __device__ __forceinline__ float get() const {
-    const uint32_t w = Q < 2 ? v.x : v.y;
-    const unsigned short h =
-        (unsigned short)((Q & 1) ? (w >> 16) : (w & 0xFFFFu));
-    return __half2float(__ushort_as_half(h));
-  }
-};
 
 // x gathered through shared memory (staged) or the read-only path.
 template <bool XS>
@@ -154,6 +102,76 @@ __device__ __forceinline__ void stage_x(XT* xs, const XT* x, int n) {
   __syncthreads();
 }
 
+// ------------------------------------------------------------ TMA / mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Every wait on a barrier gives up after this many polls (each poll may
+// itself suspend the thread for a while): the kernel then records an error
+// in the plan's status word instead of hanging.
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (TMA) writes to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes and both
+// addresses are multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ------------------------------------------------------------ CSR kernel
 struct CsrArgs {
   const int32_t* __restrict__ row_ptr;
@@ -168,54 +186,131 @@ struct CsrArgs {
   float* partials;
   int32_t* counters;
   int split_chunk;
+  int32_t* status;
 };
 
-// Short-row tile: rows [r0, r0+R), nonzeros [s, e).
-template <typename VT, typename XT, bool XS>
-__device__ __forceinline__ void stream_tile(const CsrArgs& a, const int4 t,
-                                            const XT* xs, float* s_prod,
-                                            int* s_rp) {
-  const int tid = threadIdx.x;
-  const int r0 = t.x, s = t.y, e = t.z;
-  const uint32_t meta = (uint32_t)t.w;
-  const int R = (int)(meta & kRowsMask);
-  const int lg = (int)((meta >> kLanesShift) & 7u);
-  const int a0 = s & ~(kVec - 1);           // 16-byte aligned start
-  const int s_rel = s - a0, e_rel = e - a0;
-  const int nvec = (e_rel + kVec - 1) / kVec;
-  const VT* val = static_cast<const VT*>(a.val);
-  const XT* xg = static_cast<const XT*>(a.x);
+// Shared-memory stage of one work unit: the columns and values of its
+// nonzero span (aligned out to multiples of 8 elements) and, for a short-row
+// tile, its row pointers (aligned out to multiples of 4).
+template <typename VT>
+struct Stage {
+  static constexpr int kColBytes = (kTileCap + 16) * 4;
+  static constexpr int kValBytes = ((kTileCap + 16) * (int)sizeof(VT) + 15) / 16 * 16;
+  static constexpr int kRpBytes = (kTileRowsCap + 8) * 4;
+  static constexpr int kBytes = kColBytes + kValBytes + kRpBytes;
+};
 
-  int4 c[kStreamVecs];
-  Vals4<VT> v[kStreamVecs];
-#pragma unroll
-  for (int k = 0; k < kStreamVecs; ++k) {
-    const int j = tid + k * kThreads;
-    if (j < nvec) {
-      c[k] = ld_stream_i4(a.col + a0 + j * kVec);
-      v[k].load(val + a0 + j * kVec);
-    }
+__device__ __forceinline__ bool is_sentinel(const int4& d) { return d.w == -1; }
+
+// CTA b owns the contiguous block of work units [first_unit(b), first_unit(b+1)):
+// consecutive chunks of a split row then mostly stay in one CTA.
+__device__ __forceinline__ int first_unit(const CsrArgs& a, int b) {
+  return (int)(((long long)b * a.n_tiles) / gridDim.x);
+}
+
+// Thread 0: start the TMA copies of the work unit with descriptor d into a
+// stage (valid == false marks the stage as the end of this CTA's work and
+// completes its barrier phase).
+template <typename VT>
+__device__ __forceinline__ void issue_tile(const CsrArgs& a, unsigned char* stage,
+                                           uint64_t* bar, int4* desc, bool valid,
+                                           const int4 d, uint64_t pol) {
+  if (!valid) {
+    *desc = make_int4(0, 0, 0, -1);
+    mbar_arrive(bar);
+    return;
   }
-  for (int i = tid; i <= R; i += kThreads) s_rp[i] = __ldg(a.row_ptr + r0 + i) - a0;
+  *desc = d;
+  const int a0 = d.y & ~7, a1 = (d.z + 7) & ~7;
+  const uint32_t ncol = (uint32_t)(a1 - a0) * 4u;
+  const uint32_t nval = (uint32_t)(a1 - a0) * (uint32_t)sizeof(VT);
+  uint32_t nrp = 0;
+  int ra0 = 0;
+  if (((uint32_t)d.w >> kKindShift) == kKindStream) {
+    const int R = (int)((uint32_t)d.w & kRowsMask);
+    ra0 = d.x & ~3;
+    nrp = (uint32_t)((((d.x + R + 1) + 3) & ~3) - ra0) * 4u;
+  }
+  const uint32_t total = ncol + nval + nrp;
+  if (total == 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  mbar_arrive_expect_tx(bar, total);
+  if (ncol) bulk_g2s(stage, a.col + a0, ncol, bar, pol);
+  if (nval)
+    bulk_g2s(stage + Stage<VT>::kColBytes, static_cast<const VT*>(a.val) + a0, nval, bar, pol);
+  if (nrp)
+    bulk_g2s(stage + Stage<VT>::kColBytes + Stage<VT>::kValBytes, a.row_ptr + ra0, nrp, bar,
+             pol);
+}
+
+// Eight staged values starting at element 8c, widened to fp32.
+__device__ __forceinline__ void stage_vals8(const float* v, int c, float (&o)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(v)[2 * c];
+  const float4 b = reinterpret_cast<const float4*>(v)[2 * c + 1];
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void stage_vals8(const __half* v, int c, float (&o)[8]) {
+  const uint4 a = reinterpret_cast<const uint4*>(v)[c];
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-  for (int k = 0; k < kStreamVecs; ++k) {
-    const int j = tid + k * kThreads;
-    if (j < nvec) {
-      const int rel = j * kVec;
-      float4 p;
-      p.x = (rel + 0 >= s_rel && rel + 0 < e_rel)
-                ? v[k].template get<0>() * gather<XS>(xg, xs, lane_of<0>(c[k])) : 0.f;
-      p.y = (rel + 1 >= s_rel && rel + 1 < e_rel)
-                ? v[k].template get<1>() * gather<XS>(xg, xs, lane_of<1>(c[k])) : 0.f;
-      p.z = (rel + 2 >= s_rel && rel + 2 < e_rel)
-                ? v[k].template get<2>() * gather<XS>(xg, xs, lane_of<2>(c[k])) : 0.f;
-      p.w = (rel + 3 >= s_rel && rel + 3 < e_rel)
-                ? v[k].template get<3>() * gather<XS>(xg, xs, lane_of<3>(c[k])) : 0.f;
-      *reinterpret_cast<float4*>(s_prod + rel) = p;
-    }
+  for (int h = 0; h < 4; ++h) {
+    __half2 p;
+    *reinterpret_cast<uint32_t*>(&p) = w[h];
+    const float2 f = __half22float2(p);
+    o[2 * h] = f.x;
+    o[2 * h + 1] = f.y;
+  }
+}
+
+// Products of the 8 staged nonzeros of chunk c (elements outside
+// [lo_rel, hi_rel) give 0 and gather nothing).
+template <typename VT, typename XT, bool XS>
+__device__ __forceinline__ void chunk_products(const int* s_col, const VT* s_val, int c,
+                                               int lo_rel, int hi_rel, const XT* xg,
+                                               const XT* xs, float (&p)[8]) {
+  const int4 c0 = reinterpret_cast<const int4*>(s_col)[2 * c];
+  const int4 c1 = reinterpret_cast<const int4*>(s_col)[2 * c + 1];
+  const int cols[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  float v[8];
+  stage_vals8(s_val, c, v);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int el = 8 * c + q;
+    p[q] = (el >= lo_rel && el < hi_rel) ? v[q] * gather<XS>(xg, xs, cols[q]) : 0.f;
+  }
+}
+
+// Short-row tile from a stage, lanes mode (rows of similar length): every
+// thread multiplies its 8 staged nonzeros by the gathered x and parks the
+// products in place of the staged columns; then each row is summed by
+// g = 2^lg lanes and a shuffle reduction.
+template <typename VT, typename XT, bool XS>
+__device__ __forceinline__ void stream_tile_lanes(const CsrArgs& a, const int4 d,
+                                                  unsigned char* stage, const XT* xs) {
+  const int tid = threadIdx.x;
+  const int r0 = d.x, s = d.y, e = d.z;
+  const int R = (int)((uint32_t)d.w & kRowsMask);
+  const int lg = (int)(((uint32_t)d.w >> kLanesShift) & 7u);
+  const int a0 = s & ~7;
+  const int s_rel = s - a0, e_rel = e - a0;
+  const int n8 = (e_rel + 7) >> 3;
+  int* s_col = reinterpret_cast<int*>(stage);
+  const VT* s_val = reinterpret_cast<const VT*>(stage + Stage<VT>::kColBytes);
+  const int* s_rp =
+      reinterpret_cast<const int*>(stage + Stage<VT>::kColBytes + Stage<VT>::kValBytes) +
+      (r0 - (r0 & ~3));
+  float* s_prod = reinterpret_cast<float*>(s_col);  // products replace the columns
+  const XT* xg = static_cast<const XT*>(a.x);
+  for (int c = tid; c < n8; c += kThreads) {
+    float p[8];
+    chunk_products<VT, XT, XS>(s_col, s_val, c, s_rel, e_rel, xg, xs, p);
+    reinterpret_cast<float4*>(s_prod)[2 * c] = make_float4(p[0], p[1], p[2], p[3]);
+    reinterpret_cast<float4*>(s_prod)[2 * c + 1] = make_float4(p[4], p[5], p[6], p[7]);
   }
   __syncthreads();
-
   const int g = 1 << lg;
   const int per_pass = kThreads >> lg;
   const int grp = tid >> lg, lig = tid & (g - 1);
@@ -223,7 +318,8 @@ __device__ __forceinline__ void stream_tile(const CsrArgs& a, const int4 t,
     const int r = base + grp;
     float acc = 0.f;
     if (r < R) {
-      const int b = s_rp[r], en = s_rp[r + 1];
+      const int b = s_rp[r] - a0, en = s_rp[r + 1] - a0;
+#pragma unroll 4
       for (int i = b + lig; i < en; i += g) acc += s_prod[i];
     }
     for (int o = g >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -231,90 +327,247 @@ __device__ __forceinline__ void stream_tile(const CsrArgs& a, const int4 t,
   }
 }
 
-// Per-thread partial sum of nonzeros [b, e) of one row.
+// Short-row tile from a stage, walk mode (rows of any lengths): rows
+// [r0, r0+R), nonzeros [s, e). Thread t owns the 8 staged nonzeros [8t, 8t+8) (stage-relative; the stage
+// starts at s rounded down to 8) and keeps their products in registers. It
+// finds the row of its first nonzero by binary search over the staged row
+// pointers and walks its 8 nonzeros: a row that starts and ends inside its
+// range is written to y at once; the partial of a row that continues past
+// its range is parked in s_carry[t]; the thread where a row that began in an
+// earlier thread ends adds the parked partials of the threads the row spans
+// (in thread order) to its own. Rows without nonzeros are written as 0 by a
+// separate pass. Work per thread is bounded whatever the row lengths are.
 template <typename VT, typename XT, bool XS>
-__device__ __forceinline__ float range_sum(const CsrArgs& a, int b, int e,
-                                           const XT* xs) {
+__device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
+                                                 unsigned char* stage, const XT* xs,
+                                                 float* s_carry) {
   const int tid = threadIdx.x;
-  const int a0 = b & ~(kVec - 1);
-  const int b_rel = b - a0, e_rel = e - a0;
-  const int nvec = (e_rel + kVec - 1) / kVec;
-  const VT* val = static_cast<const VT*>(a.val) + a0;
-  const int32_t* col = a.col + a0;
+  const int r0 = d.x, s = d.y, e = d.z;
+  const int R = (int)((uint32_t)d.w & kRowsMask);
+  const int a0 = s & ~7;
+  const int s_rel = s - a0, e_rel = e - a0;
+  const int* s_col = reinterpret_cast<const int*>(stage);
+  const VT* s_val = reinterpret_cast<const VT*>(stage + Stage<VT>::kColBytes);
+  // B[r] = row_ptr[r0 + r] - a0, for r in [0, R]
+  const int* s_rp =
+      reinterpret_cast<const int*>(stage + Stage<VT>::kColBytes + Stage<VT>::kValBytes) +
+      (r0 - (r0 & ~3));
+  const XT* xg = static_cast<const XT*>(a.x);
+  float* y = a.y + r0;
+
+  const int lo = max(8 * tid, s_rel), hi = min(8 * tid + 8, e_rel);
+  bool closes = false;  // this thread ends a row that began in an earlier thread
+  int close_row = 0;
+  float close_val = 0.f;
+  if (lo < hi) {
+    float p[8];
+    chunk_products<VT, XT, XS>(s_col, s_val, tid, s_rel, e_rel, xg, xs, p);
+    // row containing nonzero lo: the largest r < R with B[r] <= lo
+    int l = 0, h = R - 1;
+    while (l < h) {
+      const int mid = (l + h + 1) >> 1;
+      if (s_rp[mid] - a0 <= lo)
+        l = mid;
+      else
+        h = mid - 1;
+    }
+    int row = l;
+    int row_end = s_rp[row + 1] - a0;
+    bool inside = (s_rp[row] - a0) >= lo;
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = 8 * tid + q;
+      if (j >= lo && j < hi) {
+        if (j >= row_end) {  // the current row ended just before j
+          if (inside) {
+            y[row] = acc;
+          } else {
+            closes = true;
+            close_row = row;
+            close_val = acc;
+          }
+          do {
+            ++row;
+            row_end = s_rp[row + 1] - a0;
+          } while (row_end <= j);  // skip rows without nonzeros
+          inside = true;
+          acc = 0.f;
+        }
+        acc += p[q];
+      }
+    }
+    if (row_end > hi) {
+      s_carry[tid] = acc;  // the row goes on in the next thread(s)
+    } else if (inside) {
+      y[row] = acc;
+    } else {
+      closes = true;
+      close_row = row;
+      close_val = acc;
+    }
+  }
+  for (int r = tid; r < R; r += kThreads)
+    if (s_rp[r] == s_rp[r + 1]) y[r] = 0.f;
+  __syncthreads();
+  if (closes) {
+    float sum = 0.f;
+    for (int t = (s_rp[close_row] - a0) >> 3; t < tid; ++t) sum += s_carry[t];
+    y[close_row] = sum + close_val;
+  }
+}
+
+// Per-thread partial sum of a staged slice [b, e) of one row.
+template <typename VT, typename XT, bool XS>
+__device__ __forceinline__ float chunk_sum(const CsrArgs& a, const int4 d,
+                                           unsigned char* stage, const XT* xs) {
+  const int a0 = d.y & ~7;
+  const int lo_rel = d.y - a0, hi_rel = d.z - a0;
+  const int n8 = (hi_rel + 7) >> 3;
+  const int* s_col = reinterpret_cast<const int*>(stage);
+  const VT* s_val = reinterpret_cast<const VT*>(stage + Stage<VT>::kColBytes);
   const XT* xg = static_cast<const XT*>(a.x);
   float acc = 0.f;
-  for (int j0 = tid; j0 < nvec; j0 += kThreads * kRowUnroll) {
-    int4 c[kRowUnroll];
-    Vals4<VT> v[kRowUnroll];
+  for (int c = threadIdx.x; c < n8; c += kThreads) {
+    float p[8];
+    chunk_products<VT, XT, XS>(s_col, s_val, c, lo_rel, hi_rel, xg, xs, p);
 #pragma unroll
-    for (int u = 0; u < kRowUnroll; ++u) {
-      const int j = j0 + u * kThreads;
-      if (j < nvec) {
-        c[u] = ld_stream_i4(col + j * kVec);
-        v[u].load(val + j * kVec);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kRowUnroll; ++u) {
-      const int j = j0 + u * kThreads;
-      if (j < nvec) {
-        const int rel = j * kVec;
-        if (rel + 0 >= b_rel && rel + 0 < e_rel)
-          acc = fmaf(v[u].template get<0>(), gather<XS>(xg, xs, lane_of<0>(c[u])), acc);
-        if (rel + 1 >= b_rel && rel + 1 < e_rel)
-          acc = fmaf(v[u].template get<1>(), gather<XS>(xg, xs, lane_of<1>(c[u])), acc);
-        if (rel + 2 >= b_rel && rel + 2 < e_rel)
-          acc = fmaf(v[u].template get<2>(), gather<XS>(xg, xs, lane_of<2>(c[u])), acc);
-        if (rel + 3 >= b_rel && rel + 3 < e_rel)
-          acc = fmaf(v[u].template get<3>(), gather<XS>(xg, xs, lane_of<3>(c[u])), acc);
-      }
-    }
+    for (int q = 0; q < 8; ++q) acc += p[q];
   }
   return acc;
 }
 
-// Thread 0 of a split chunk: publish the partial; the last chunk of the row
-// to arrive adds all partials in chunk order, writes y and re-arms the
-// counter for the next run.
-__device__ __forceinline__ void split_finish(const CsrArgs& a, int row, int b,
-                                             int sid, float part) {
+// Thread 0, at the end of this CTA's piece of split row `row` (its chunks
+// starting at nonzero b0 and ending with the chunk that starts at b): if the
+// piece is the whole row, write y; otherwise publish the piece's partial at
+// the slot of its first chunk and count its chunks. The CTA that completes the
+// count adds all slots of the row in chunk order (slots of other pieces'
+// interior chunks hold 0), writes y, and clears the slots and the counter for
+// the next run. Only rows that cross a CTA boundary take this path.
+__device__ __forceinline__ void split_publish(const CsrArgs& a, int row, int sid,
+                                              bool whole, int b0, int b, float part) {
+  if (whole) {
+    a.y[row] = part;
+    return;
+  }
   const SplitInfo si = a.splits[sid];
-  const int chunk = (b - __ldg(a.row_ptr + row)) / a.split_chunk;
-  a.partials[si.first_slot + chunk] = part;
+  const int k0 = (b0 - si.row_begin) / a.split_chunk;
+  const int k = (b - si.row_begin) / a.split_chunk;
+  a.partials[si.first_slot + k0] = part;
   __threadfence();
-  const int arrived = atomicAdd(a.counters + sid, 1);
-  if (arrived == si.n_chunks - 1) {
+  const int add = k - k0 + 1;
+  const int before = atomicAdd(a.counters + sid, add);
+  if (before + add == si.n_chunks) {
     __threadfence();
     float sum = 0.f;
-    for (int k = 0; k < si.n_chunks; ++k) sum += __ldcg(a.partials + si.first_slot + k);
+    for (int j = 0; j < si.n_chunks; ++j) {
+      sum += __ldcg(a.partials + si.first_slot + j);
+      a.partials[si.first_slot + j] = 0.f;
+    }
     a.y[row] = sum;
     a.counters[sid] = 0;
   }
 }
 
+// Persistent CSR kernel: each CTA walks its contiguous block of work units;
+// thread 0 keeps kStages units in flight (TMA bulk copies into a ring of shared
+// memory stages) while the CTA computes the oldest one.
 template <typename VT, typename XT, bool XS>
 __global__ void __launch_bounds__(kThreads) csr_kernel(const CsrArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
-  __shared__ __align__(16) float s_prod[kProdCap];
-  __shared__ int s_rp[kMaxTileRows + 1];
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  __shared__ __align__(8) uint64_t s_bar[kStages];
+  __shared__ int4 s_desc[kStages];
   __shared__ float s_red[kWarps];
-  XT* xs = reinterpret_cast<XT*>(dyn_smem);
+  __shared__ float s_carry[kThreads];
+  unsigned char* stages = dyn_smem;
+  const int u_begin = first_unit(a, blockIdx.x);
+  const int u_end = first_unit(a, blockIdx.x + 1);
+  XT* xs = reinterpret_cast<XT*>(dyn_smem + kStages * Stage<VT>::kBytes);
+  const int tid = threadIdx.x;
+  uint64_t pol = 0;
+  int4 next_d = make_int4(0, 0, 0, 0);  // thread 0: descriptor of the next unit to issue
+  int next_u = u_begin;                 // thread 0: that unit
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&s_bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    pol = policy_evict_first();
+    int4 d0[kStages];
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+      d0[s] = next_u + s < u_end ? __ldg(a.tiles + next_u + s) : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+      issue_tile<VT>(a, stages + s * Stage<VT>::kBytes, &s_bar[s], &s_desc[s],
+                     next_u + s < u_end, d0[s], pol);
+    next_u += kStages;
+    // the descriptor for the next refill is loaded one unit ahead, so the
+    // refill never waits for it
+    if (next_u < u_end) next_d = __ldg(a.tiles + next_u);
+  }
   if (XS) stage_x<XT>(xs, static_cast<const XT*>(a.x), a.n_cols);
-  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-    const int4 d = __ldg(a.tiles + t);
-    const uint32_t kind = (uint32_t)d.w >> kKindShift;
+  bool aborted = false;
+  float row_acc = 0.f;  // this thread's share of the current split-row piece
+  int piece_b0 = -1;    // first nonzero of that piece, -1 when none is open
+  bool piece_first = false;
+  int i = 0;  // work units consumed; each consumption re-issues its stage
+  for (;; ++i) {
+    const int s = i % kStages;
+    const uint32_t parity = (uint32_t)(i / kStages) & 1u;
+    const bool ok = mbar_wait_bounded(&s_bar[s], parity);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    const int4 d = s_desc[s];
+    if (is_sentinel(d)) break;
+    unsigned char* stage = stages + s * Stage<VT>::kBytes;
+    const uint32_t w = (uint32_t)d.w;
+    const uint32_t kind = w >> kKindShift;
     if (kind == kKindStream) {
-      stream_tile<VT, XT, XS>(a, d, xs, s_prod, s_rp);
+      if (w & kStreamWalk)
+        stream_tile_walk<VT, XT, XS>(a, d, stage, xs, s_carry);
+      else
+        stream_tile_lanes<VT, XT, XS>(a, d, stage, xs);
+    } else if (kind == kKindRow) {
+      const float part = cta_sum(chunk_sum<VT, XT, XS>(a, d, stage, xs), s_red);
+      if (tid == 0) a.y[d.x] = part;
     } else {
-      const float part = cta_sum(range_sum<VT, XT, XS>(a, d.y, d.z, xs), s_red);
-      if (threadIdx.x == 0) {
-        if (kind == kKindRow)
-          a.y[d.x] = part;
-        else
-          split_finish(a, d.x, d.y, (int)((uint32_t)d.w & kSplitIdMask), part);
+      if (piece_b0 < 0) {
+        piece_b0 = d.y;
+        piece_first = (w & kSplitFirst) != 0;
+      }
+      row_acc += chunk_sum<VT, XT, XS>(a, d, stage, xs);
+      const bool last = (w & kSplitLast) != 0;
+      if (last || u_begin + i == u_end - 1) {  // row ends, or this CTA's share does
+        const float part = cta_sum(row_acc, s_red);
+        if (tid == 0)
+          split_publish(a, d.x, (int)(w & kSplitIdMask), piece_first && last, piece_b0, d.y,
+                        part);
+        row_acc = 0.f;
+        piece_b0 = -1;
       }
     }
-    __syncthreads();  // shared buffers are reused by the next tile
+    __syncthreads();  // stage s is free again
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      const bool valid = next_u < u_end;
+      issue_tile<VT>(a, stage, &s_bar[s], &s_desc[s], valid, next_d, pol);
+      ++next_u;
+      if (next_u < u_end) next_d = __ldg(a.tiles + next_u);
+    }
+  }
+  if (tid == 0 && aborted) {
+    atomicExch(a.status, 1);
+    // let copies still in flight land before the CTA's shared memory goes:
+    // stage s was filled 1 + #{j < i : j % kStages == s} times
+    for (int s = 0; s < kStages; ++s) {
+      const int fills = 1 + (i > s ? (i - 1 - s) / kStages + 1 : 0);
+      mbar_wait_bounded(&s_bar[s], (uint32_t)(fills - 1) & 1u);
+    }
   }
 }
 
@@ -342,7 +595,7 @@ __device__ __forceinline__ __half gather_h(const __half* xg, const __half* xs, i
 
 template <bool XS>
 __global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ int s_tot[2][kWarps];
   __shared__ float s_red[kWarps];
   __half* xs = reinterpret_cast<__half*>(dyn_smem);
@@ -440,6 +693,11 @@ const void* csr_fn() {
   return reinterpret_cast<const void*>(&csr_kernel<VT, XT, XS>);
 }
 
+template <typename VT>
+constexpr size_t stage_bytes() {
+  return (size_t)Stage<VT>::kBytes;
+}
+
 const void* csr_entry(spmv_dtype dt, bool xs) {
   if (dt == SPMV_F32) return xs ? csr_fn<float, float, true>() : csr_fn<float, float, false>();
   return xs ? csr_fn<__half, __half, true>() : csr_fn<__half, __half, false>();
@@ -468,8 +726,13 @@ int delta_kernel_occupancy(bool x_smem, size_t dyn_smem) {
   return n;
 }
 
+size_t csr_stage_bytes(spmv_dtype dtype) {
+  return dtype == SPMV_F32 ? stage_bytes<float>() : stage_bytes<__half>();
+}
+
 int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn) {
-  const void* fns[] = {csr_entry(SPMV_F32, true), csr_entry(SPMV_F16, true)};
+  const void* fns[] = {csr_entry(SPMV_F32, true), csr_entry(SPMV_F16, true),
+                       csr_entry(SPMV_F32, false), csr_entry(SPMV_F16, false)};
   if (csr_dyn > 0)
     for (const void* f : fns)
       if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -497,6 +760,7 @@ int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
   a.partials = p.partials;
   a.counters = p.counters;
   a.split_chunk = p.split_chunk;
+  a.status = p.status;
   void* args[] = {&a};
   return cudaLaunchKernel(csr_entry(p.dtype, p.x_smem), dim3((unsigned)p.grid),
                           dim3(kThreads), args, p.dyn_smem,

@@ -171,51 +171,74 @@ def test_converter_bit_exact_llm_full(spmv_lib):
     _converter_matches_oracle(workloads.llm(0.9))
 
 
+def effective(opts):
+    """The planner's limits after its clamps (tile_nnz <= 2032, rows that
+    are not split fit one 2048-nonzero stage)."""
+    tile_nnz = min(opts.tile_nnz, 2032)
+    cta = min(opts.cta_row_min, tile_nnz)
+    srm = min(max(opts.split_row_min, cta), 2048)
+    return tile_nnz, cta, srm, min(max(opts.split_chunk, 64), 2048)
+
+
 def expected_bins(lengths, opts):
-    """Bins the planner must produce, computed from the row lengths alone."""
-    split = lengths > opts.split_row_min
-    cta = (lengths > opts.cta_row_min) & ~split
-    chunks = np.sum((lengths[split] + opts.split_chunk - 1) // opts.split_chunk)
-    return int(cta.sum()), int(split.sum()), int(chunks)
+    """Bins and tiles the planner must produce, from the row lengths alone."""
+    tile_nnz, cta, srm, chunk = effective(opts)
+    split = lengths > srm
+    single = (lengths > cta) & ~split
+    bins = [int(np.sum((lengths <= 8) & ~split)),
+            int(np.sum((lengths > 8) & (lengths <= 256) & ~split)),
+            int(np.sum((lengths > 256) & ~split)), int(split.sum())]
+    chunks = int(np.sum((lengths[split] + chunk - 1) // chunk))
+    return bins, int(single.sum()), chunks, tile_nnz, cta
 
 
-@pytest.mark.parametrize("kw", [{}, {"cta_row_min": 32}, {"split_row_min": 300,
-                                                         "split_chunk": 128},
-                                {"tile_nnz": 300, "tile_rows": 64},
-                                {"lanes": 4}])
+@pytest.mark.parametrize("kw", [{}, {"cta_row_min": 32},
+                                {"cta_row_min": 200, "split_row_min": 300,
+                                 "split_chunk": 128},
+                                {"tile_nnz": 300, "tile_rows": 64}])
 def test_planner_bins(spmv_lib, kw):
-    m = workloads.powerlaw(n=40000, nnz=223000, max_len=2000)
+    m = workloads.powerlaw(n=40000, nnz=223000, max_len=2500)
     opts = S.spmv_plan_options(**kw)
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols,
                                options=opts)
     L = m.row_lengths()
-    n_cta, n_split, n_chunks = expected_bins(L, opts)
+    bins, n_single, n_chunks, tile_nnz, cta = expected_bins(L, opts)
+    assert info["rows_per_bin"] == bins
     assert sum(info["rows_per_bin"]) == m.n_rows
-    assert info["rows_per_bin"][2] == n_cta == info["tiles_per_bin"][2]
-    assert info["rows_per_bin"][3] == n_split == info["n_split_rows"]
+    assert info["tiles_per_bin"][2] == n_single
     assert info["tiles_per_bin"][3] == n_chunks
-    short = L[L <= min(opts.cta_row_min, opts.tile_nnz)]
-    min_tiles = max(int(np.ceil(short.sum() / opts.tile_nnz)),
+    assert info["n_split_rows"] == bins[3]
+    short = L[L <= cta]
+    min_tiles = max(int(np.ceil(short.sum() / tile_nnz)),
                     int(np.ceil(short.size / opts.tile_rows)))
-    assert info["tiles_per_bin"][0] + info["tiles_per_bin"][1] >= min_tiles
+    assert info["tiles_per_bin"][0] >= min_tiles
     assert info["n_tiles"] == sum(info["tiles_per_bin"])
-    if kw.get("lanes"):
-        assert info["tiles_per_bin"][1] == 0
     assert info["algorithmic_bytes"] == (8 * m.nnz + 4 * (m.n_rows + 1)
                                          + 4 * m.n_cols + 4 * m.n_rows)
 
 
-def test_planner_regular_matrices_pick_lanes(spmv_lib):
+def test_planner_bins_of_the_workload_shapes(spmv_lib):
     lap = workloads.laplacian(300, 200)
     info = S.spmv_plan_inspect(lap.row_ptr, lap.col_idx, lap.values, lap.n_cols)
-    assert info["rows_per_bin"][0] == lap.n_rows   # short rows, sub-warp bin
+    assert info["rows_per_bin"] == [lap.n_rows, 0, 0, 0]   # sub-warp
+    assert info["walk_tiles"] == 0                           # regular rows: lanes mode
+    pl = workloads.powerlaw(n=40000, nnz=223000, max_len=2500)
+    info = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols)
+    assert info["walk_tiles"] > 0                            # irregular rows: walk mode
+    for reduce, walk in ((1, 0), (2, info["tiles_per_bin"][0])):
+        forced = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols,
+                                     options=S.spmv_plan_options(reduce=reduce, lanes=4))
+        assert forced["walk_tiles"] == walk
     fem = workloads.fem(6, 5, 4)
     info = S.spmv_plan_inspect(fem.row_ptr, fem.col_idx, fem.values, fem.n_cols)
-    assert info["rows_per_bin"][2] == 0 and info["rows_per_bin"][3] == 0
+    assert info["rows_per_bin"] == [0, fem.n_rows, 0, 0]   # warp
     llm = workloads.llm(0.3, n=2048)
     info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols)
-    assert info["rows_per_bin"][2] == llm.n_rows   # one CTA per row
+    assert info["rows_per_bin"] == [0, 0, llm.n_rows, 0]   # CTA
     assert info["x_in_smem"] == 1
+    big = workloads.llm(0.3, n=4096)
+    info = S.spmv_plan_inspect(big.row_ptr, big.col_idx, big.values, big.n_cols)
+    assert info["rows_per_bin"] == [0, 0, 0, big.n_rows]   # split
     info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
                                format="delta4")
     enc = oracle.delta_encode(llm.n_cols, llm.row_ptr, llm.col_idx, llm.values)

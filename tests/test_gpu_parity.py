@@ -125,10 +125,13 @@ def test_full_size_delta4(name):
 # ------------------------------------------------------------ forced paths
 
 @pytest.mark.parametrize("kw", [
-    {"lanes": 1}, {"lanes": 2}, {"lanes": 4}, {"lanes": 8}, {"lanes": 16},
-    {"lanes": 32}, {"cta_row_min": 16}, {"split_row_min": 200, "split_chunk": 64},
-    {"split_row_min": 1000, "split_chunk": 1000}, {"tile_nnz": 97, "tile_rows": 13},
-    {"x_smem": 0}, {"x_smem": 1}, {"tile_rows": 1},
+    {}, {"cta_row_min": 16}, {"cta_row_min": 1},
+    {"cta_row_min": 100, "split_row_min": 200, "split_chunk": 64},
+    {"cta_row_min": 900, "split_row_min": 1000, "split_chunk": 1000},
+    {"tile_nnz": 97, "tile_rows": 13}, {"tile_nnz": 8}, {"tile_rows": 1},
+    {"x_smem": 0}, {"x_smem": 1},
+    {"reduce": 1, "lanes": 1}, {"reduce": 1, "lanes": 4}, {"reduce": 1, "lanes": 32},
+    {"reduce": 2}, {"reduce": 2, "tile_nnz": 97},
 ])
 def test_forced_planner_paths(kw):
     m = workloads.powerlaw(n=30000, nnz=167000, max_len=3000, seed=11)
@@ -138,7 +141,8 @@ def test_forced_planner_paths(kw):
 
 
 @pytest.mark.parametrize("kw", [{"x_smem": 0}, {"x_smem": 1},
-                                {"split_row_min": 500, "split_chunk": 300}])
+                                {"cta_row_min": 100, "split_row_min": 150,
+                                 "split_chunk": 64}])
 def test_forced_paths_fp16_csr(kw):
     m = workloads.llm(0.8, n=1000, seed=3)
     y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
@@ -229,7 +233,8 @@ def test_unaligned_row_starts_every_length():
     # row lengths 0..40 repeated: every start offset modulo 4 and 8 appears
     lengths = np.tile(np.arange(41), 30)
     m = workloads.from_lengths("ragged", lengths, 4096, seed=21)
-    for kw in ({}, {"lanes": 1}, {"lanes": 32}, {"cta_row_min": 8}):
+    for kw in ({}, {"tile_nnz": 40}, {"tile_rows": 3}, {"cta_row_min": 8},
+               {"reduce": 2}, {"reduce": 1, "lanes": 2}):
         y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
         assert_parity(m, y, TOL32)
 
@@ -292,7 +297,8 @@ def test_delta_plan_rejects_bad_columns():
 
 def test_repeated_runs_identical_and_split_counters_rearm():
     m = workloads.powerlaw(n=20000, nnz=111000, max_len=3000, seed=2)
-    ys, info = run_gpu(m, options=S.spmv_plan_options(split_row_min=300, split_chunk=100),
+    ys, info = run_gpu(m, options=S.spmv_plan_options(cta_row_min=200, split_row_min=300,
+                                                      split_chunk=100),
                        repeat=4)
     assert info["rows_per_bin"][3] > 0
     for y in ys[1:]:
