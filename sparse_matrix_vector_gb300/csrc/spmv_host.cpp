@@ -181,11 +181,44 @@ static int row_bin(int64_t len, const Options& o) {
 }
 
 spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
-                           CsrTables* out, spmv_plan_info* info) {
+                           int max_ctas, CsrTables* out, spmv_plan_info* info) {
   out->tiles.clear();
   out->splits.clear();
+  out->cta_first.clear();
   out->n_chunks = 0;
+  // Weight of a row: its nonzeros plus one (row pointer, y write). The
+  // matrix is cut into G contiguous shares of equal weight, one per CTA
+  // (persistent grid), and no short-row or single-row tile crosses a share
+  // boundary, so every CTA gets the same amount of work.
+  const int64_t total_w = (int64_t)rp[n_rows] + n_rows;
+  constexpr int64_t kMinShare = 1024;
+  const int G = (int)std::max<int64_t>(
+      1, std::min<int64_t>(max_ctas, (total_w + kMinShare - 1) / kMinShare));
+  auto boundary = [&](int b) { return (int64_t)((__int128)b * total_w / G); };
+  int64_t cum = 0;  // weight of the tiles emitted so far
+  int next_b = 1;
+  // short-row tiles of a share are sized evenly: the share's weight over the
+  // fewest tiles that respect tile_nnz
+  int64_t target = 0;
+  int64_t share_tiles = 0;  // planned short-row tiles left in this share
+  auto share_target = [&]() {
+    const int64_t left = (next_b < G ? boundary(next_b) : total_w) - cum;
+    const int64_t cap = (int64_t)o.tile_nnz + 64;
+    share_tiles = std::max<int64_t>(1, (left + cap - 1) / cap);
+    return (left + share_tiles - 1) / share_tiles;
+  };
   try {
+    out->cta_first.push_back(0);
+    target = share_target();
+    auto mark = [&]() {
+      bool moved = false;
+      while (next_b < G && cum >= boundary(next_b)) {
+        out->cta_first.push_back((int32_t)out->tiles.size());
+        ++next_b;
+        moved = true;
+      }
+      if (moved) target = share_target();
+    };
     int r = 0;
     while (r < n_rows) {
       const int64_t len = (int64_t)rp[r + 1] - rp[r];
@@ -196,12 +229,14 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
           return SPMV_ERR_TOO_LARGE;
         out->splits.push_back({(int32_t)out->n_chunks, (int32_t)nch, rp[r], 0});
         for (int64_t k = 0; k < nch; ++k) {
+          mark();
           const int64_t b = rp[r] + k * o.split_chunk;
           const int64_t e = std::min<int64_t>(b + o.split_chunk, rp[r + 1]);
           const uint32_t flags = (k == 0 ? kSplitFirst : 0u) | (k == nch - 1 ? kSplitLast : 0u);
           out->tiles.push_back({r, (int32_t)b, (int32_t)e,
                                 (int32_t)((kKindSplit << kKindShift) | flags |
                                           (uint32_t)sid)});
+          cum += (e - b) + (k == 0 ? 1 : 0);
         }
         out->n_chunks += nch;
         info->rows_per_bin[3] += 1;
@@ -209,20 +244,29 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
         ++r;
         continue;
       }
+      mark();
       if (len > o.cta_row_min) {
         out->tiles.push_back(
             {r, rp[r], rp[r + 1], (int32_t)(kKindRow << kKindShift)});
         info->rows_per_bin[row_bin(len, o)] += 1;
         info->tiles_per_bin[2] += 1;
+        cum += len + 1;
         ++r;
         continue;
       }
+      const int64_t limit = next_b < G ? boundary(next_b) : INT64_MAX;
       const int r0 = r;
-      int64_t nz = 0;
+      int64_t nz = 0, w = 0;
       while (r < n_rows && r - r0 < o.tile_rows) {
         const int64_t l = (int64_t)rp[r + 1] - rp[r];
         if (l > o.cta_row_min || nz + l > o.tile_nnz) break;
+        // the last planned tile of a share takes whatever is left of it
+        // a tile ends once it reaches its share's boundary (the row that
+        // crosses it stays in); the last planned tile of a share takes
+        // whatever is left of the share
+        if (r > r0 && (cum + w >= limit || (share_tiles > 1 && w + l + 1 > target))) break;
         nz += l;
+        w += l + 1;
         info->rows_per_bin[row_bin(l, o)] += 1;
         ++r;
       }
@@ -233,13 +277,17 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
                             (int32_t)((kKindStream << kKindShift) | mode | (uint32_t)(r - r0))});
       if (mode & kStreamWalk) info->walk_tiles += 1;
       info->tiles_per_bin[0] += 1;
+      cum += w;
+      --share_tiles;
     }
+    while ((int)out->cta_first.size() <= G) out->cta_first.push_back((int32_t)out->tiles.size());
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
   }
   if ((int64_t)out->tiles.size() > kMaxIndex) return SPMV_ERR_TOO_LARGE;
   info->n_tiles = (int64_t)out->tiles.size();
   info->n_split_rows = (int64_t)out->splits.size();
+  info->grid = G;
   return SPMV_OK;
 }
 
@@ -291,9 +339,9 @@ void free_plan(spmv_plan* plan) {
   Plan* p = &plan->impl;
   {
     DeviceGuard g(p->device);
-    void* bufs[] = {p->row_ptr, p->col_idx, p->values,   p->words,
-                    p->tiles,   p->splits,  p->partials, p->counters,
-                    p->status,  p->x_stage, p->y_stage};
+    void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->words,
+                    p->tiles,   p->splits,   p->partials, p->counters,
+                    p->status,  p->x_stage,  p->y_stage,  p->cta_first};
     for (void* b : bufs)
       if (b) cudaFree(b);
   }
@@ -333,8 +381,7 @@ void fill_bytes(spmv_plan_info* info, size_t x_elem) {
 spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
   CsrTables t;
   spmv_plan_info& info = p->info;
-  spmv_status s = plan_csr_tiles(m->n_rows, m->row_ptr, o, &t, &info);
-  if (s != SPMV_OK) return s;
+  spmv_status s;
   if ((s = bind_device(p)) != SPMV_OK) return s;
   const size_t vs = dtype_size(m->value_dtype);
   const size_t xbytes = (size_t)m->n_cols * vs;
@@ -342,15 +389,15 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
             : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
   p->dyn_smem = (p->x_smem ? (xbytes + 15) / 16 * 16 : 0) +
                 kStages * csr_stage_bytes(m->value_dtype);
-  p->n_tiles = (int64_t)t.tiles.size();
   p->split_chunk = o.split_chunk;
   if (set_kernel_smem_limits(p->dyn_smem, 0) != 0) return SPMV_ERR_CUDA;
-  {
-    // persistent grid: every resident CTA pulls tiles until none is left
-    int occ = csr_kernel_occupancy(m->value_dtype, p->x_smem, p->dyn_smem);
-    if (occ <= 0) return SPMV_ERR_CUDA;
-    p->grid = (int)std::min<int64_t>(p->n_tiles, (int64_t)occ * p->sm_count);
-  }
+  // persistent grid: at most every CTA that fits on the device at once
+  const int occ = csr_kernel_occupancy(m->value_dtype, p->x_smem, p->dyn_smem);
+  if (occ <= 0) return SPMV_ERR_CUDA;
+  s = plan_csr_tiles(m->n_rows, m->row_ptr, o, occ * p->sm_count, &t, &info);
+  if (s != SPMV_OK) return s;
+  p->n_tiles = (int64_t)t.tiles.size();
+  p->grid = info.grid;
   const size_t nnz_alloc = (size_t)m->nnz + kPadElems;
   if ((s = dev_upload(&p->row_ptr, m->row_ptr, ((size_t)m->n_rows + 1) * 4,
                       ((size_t)m->n_rows + 1 + kPadElems) * 4)) != SPMV_OK) return s;
@@ -360,6 +407,8 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
                       nnz_alloc * vs)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->tiles, t.tiles.data(), t.tiles.size() * sizeof(Tile),
                       t.tiles.size() * sizeof(Tile))) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->cta_first, t.cta_first.data(), t.cta_first.size() * 4,
+                      t.cta_first.size() * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->splits, t.splits.data(),
                       t.splits.size() * sizeof(SplitInfo),
                       t.splits.size() * sizeof(SplitInfo))) != SPMV_OK) return s;
@@ -376,7 +425,7 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
                       ((int64_t)m->n_rows + 1) * 4;
   info.aux_bytes = (int64_t)(t.tiles.size() * sizeof(Tile) +
                              t.splits.size() * (sizeof(SplitInfo) + 4) +
-                             (size_t)t.n_chunks * 4);
+                             (size_t)t.n_chunks * 4 + t.cta_first.size() * 4);
   fill_bytes(&info, vs);
   return SPMV_OK;
 }
@@ -587,18 +636,18 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
     return SPMV_OK;
   }
   CsrTables t;
-  s = plan_csr_tiles(m->n_rows, m->row_ptr, o, &t, info);
+  s = plan_csr_tiles(m->n_rows, m->row_ptr, o, 5 * kAssumedSms, &t, info);
   if (s != SPMV_OK) return s;
   const size_t vs = dtype_size(m->value_dtype);
   info->n_entries = m->nnz;
   info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * vs <=
                     (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);
-  info->grid = (int32_t)std::min<int64_t>(info->n_tiles, 4LL * kAssumedSms);
+
   info->launches_per_run = info->n_tiles > 0;
   info->matrix_bytes = m->nnz * (int64_t)(vs + 4) + ((int64_t)m->n_rows + 1) * 4;
   info->aux_bytes = (int64_t)(t.tiles.size() * sizeof(Tile) +
                               t.splits.size() * (sizeof(SplitInfo) + 4) +
-                              (size_t)t.n_chunks * 4);
+                              (size_t)t.n_chunks * 4 + t.cta_first.size() * 4);
   fill_bytes(info, vs);
   return SPMV_OK;
 }

@@ -76,11 +76,14 @@ Options resolve_options(const spmv_plan_options* o);
 struct CsrTables {
   std::vector<Tile> tiles;
   std::vector<SplitInfo> splits;
+  std::vector<int32_t> cta_first;  // CTA b runs tiles [cta_first[b], cta_first[b+1])
   int64_t n_chunks = 0;
 };
 
+// Cut the rows into work units and deal them to at most `max_ctas` CTAs as
+// contiguous blocks of equal weight (nonzeros + rows).
 spmv_status plan_csr_tiles(int n_rows, const int32_t* row_ptr,
-                           const Options& opt, CsrTables* out,
+                           const Options& opt, int max_ctas, CsrTables* out,
                            spmv_plan_info* info);
 
 // Device resources of a plan.
@@ -106,6 +109,7 @@ struct Plan {
   // planner tables and scratch (device)
   Tile* tiles = nullptr;
   SplitInfo* splits = nullptr;
+  int32_t* cta_first = nullptr;
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
   int32_t* status = nullptr;    // device status word

@@ -155,6 +155,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue, and wait until every kernel this one depends on has finished and
+// its memory is visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -180,6 +190,7 @@ struct CsrArgs {
   const void* __restrict__ x;
   float* __restrict__ y;
   const int4* __restrict__ tiles;
+  const int32_t* __restrict__ cta_first;
   int n_tiles;
   int n_cols;
   const SplitInfo* __restrict__ splits;
@@ -201,12 +212,6 @@ struct Stage {
 };
 
 __device__ __forceinline__ bool is_sentinel(const int4& d) { return d.w == -1; }
-
-// CTA b owns the contiguous block of work units [first_unit(b), first_unit(b+1)):
-// consecutive chunks of a split row then mostly stay in one CTA.
-__device__ __forceinline__ int first_unit(const CsrArgs& a, int b) {
-  return (int)(((long long)b * a.n_tiles) / gridDim.x);
-}
 
 // Thread 0: start the TMA copies of the work unit with descriptor d into a
 // stage (valid == false marks the stage as the end of this CTA's work and
@@ -480,8 +485,9 @@ __global__ void __launch_bounds__(kThreads) csr_kernel(const CsrArgs a) {
   __shared__ float s_red[kWarps];
   __shared__ float s_carry[kThreads];
   unsigned char* stages = dyn_smem;
-  const int u_begin = first_unit(a, blockIdx.x);
-  const int u_end = first_unit(a, blockIdx.x + 1);
+  // this CTA's contiguous block of work units (equal weight per CTA)
+  const int u_begin = __ldg(a.cta_first + blockIdx.x);
+  const int u_end = __ldg(a.cta_first + blockIdx.x + 1);
   XT* xs = reinterpret_cast<XT*>(dyn_smem + kStages * Stage<VT>::kBytes);
   const int tid = threadIdx.x;
   uint64_t pol = 0;
@@ -507,7 +513,12 @@ __global__ void __launch_bounds__(kThreads) csr_kernel(const CsrArgs a) {
     // the descriptor for the next refill is loaded one unit ahead, so the
     // refill never waits for it
     if (next_u < u_end) next_d = __ldg(a.tiles + next_u);
+    pdl_launch_dependents();
   }
+  // Everything above reads only plan-owned data (tiles and the matrix, which
+  // no kernel writes); x, y and the split scratch are touched only after the
+  // kernels this launch depends on have completed.
+  pdl_wait();
   if (XS) stage_x<XT>(xs, static_cast<const XT*>(a.x), a.n_cols);
   bool aborted = false;
   float row_acc = 0.f;  // this thread's share of the current split-row piece
@@ -599,7 +610,6 @@ __global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
   __shared__ int s_tot[2][kWarps];
   __shared__ float s_red[kWarps];
   __half* xs = reinterpret_cast<__half*>(dyn_smem);
-  if (XS) stage_x<__half>(xs, a.x, a.n_cols);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
   int r = blockIdx.x;
@@ -617,6 +627,10 @@ __global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
     cw = ld_stream_u32(a.words + rb + tid);
     cv = ld_stream_u4(a.vals + rb + tid);
   }
+  // plan-owned matrix data only above this point; x and y below
+  if (tid == 0) pdl_launch_dependents();
+  pdl_wait();
+  if (XS) stage_x<__half>(xs, a.x, a.n_cols);
   float acc = 0.f;
   int base = 0, buf = 0;
   while (true) {
@@ -708,6 +722,25 @@ const void* delta_entry(bool xs) {
             : reinterpret_cast<const void*>(&delta4_kernel<false>);
 }
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel on the stream drains; it orders itself with
+// griddepcontrol.wait before touching anything that kernel may write. Every
+// CTA of these grids is resident at once (persistent grids), so CTAs that
+// wait can never keep the kernel they wait on from running.
+int launch_pdl(const void* fn, int grid, size_t smem, void* stream, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? 0 : -1;
+}
+
 }  // namespace
 
 int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem) {
@@ -754,6 +787,7 @@ int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
   a.x = x;
   a.y = y;
   a.tiles = reinterpret_cast<const int4*>(p.tiles);
+  a.cta_first = p.cta_first;
   a.n_tiles = (int)p.n_tiles;
   a.n_cols = p.n_cols;
   a.splits = p.splits;
@@ -762,11 +796,7 @@ int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
   a.split_chunk = p.split_chunk;
   a.status = p.status;
   void* args[] = {&a};
-  return cudaLaunchKernel(csr_entry(p.dtype, p.x_smem), dim3((unsigned)p.grid),
-                          dim3(kThreads), args, p.dyn_smem,
-                          static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? 0
-             : -1;
+  return launch_pdl(csr_entry(p.dtype, p.x_smem), p.grid, p.dyn_smem, stream, args);
 }
 
 int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
@@ -780,10 +810,7 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.n_rows = p.n_rows;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
-  return cudaLaunchKernel(delta_entry(p.x_smem), dim3((unsigned)p.grid), dim3(kThreads),
-                          args, p.dyn_smem, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? 0
-             : -1;
+  return launch_pdl(delta_entry(p.x_smem), p.grid, p.dyn_smem, stream, args);
 }
 
 }  // namespace spmv

@@ -222,7 +222,7 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     info = S.spmv_plan_inspect(lap.row_ptr, lap.col_idx, lap.values, lap.n_cols)
     assert info["rows_per_bin"] == [lap.n_rows, 0, 0, 0]   # sub-warp
     assert info["walk_tiles"] == 0                           # regular rows: lanes mode
-    pl = workloads.powerlaw(n=40000, nnz=223000, max_len=2500)
+    pl = workloads.powerlaw(n=300000, nnz=1_670_000, max_len=2500)
     info = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols)
     assert info["walk_tiles"] > 0                            # irregular rows: walk mode
     for reduce, walk in ((1, 0), (2, info["tiles_per_bin"][0])):

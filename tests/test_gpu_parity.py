@@ -356,3 +356,48 @@ def test_argument_errors():
     S.spmv_plan_destroy(plan)
     with pytest.raises(ValueError):
         S.spmv_run(plan, x, torch.empty(m.n_rows, device=dev))
+
+
+@pytest.mark.parametrize("name", ["laplacian_small", "powerlaw_small", "fem_small"])
+def test_chained_runs_respect_dependencies(name):
+    """y1 = A x, y2 = A y1, y3 = A y2 launched back to back on one stream
+    (kernels may start before their predecessor ends and must order their
+    reads of x after it): every link matches the oracle applied to the GPU's
+    own input. Output buffers start as NaN so an early read would show."""
+    m = small(name)
+    assert m.n_rows == m.n_cols
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    x0 = torch.from_numpy(m.x).to(dev)
+    for _ in range(5):
+        ys = [torch.full((m.n_rows,), float("nan"), dtype=torch.float32, device=dev)
+              for _ in range(3)]
+        torch.cuda.synchronize()
+        S.spmv_run(plan, x0, ys[0])
+        S.spmv_run(plan, ys[0], ys[1])
+        S.spmv_run(plan, ys[1], ys[2])
+        torch.cuda.synchronize()
+        inputs = [m.x] + [y.cpu().numpy() for y in ys[:2]]
+        for xin, y in zip(inputs, ys):
+            y_ref, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, xin)
+            assert_parity(m, y.cpu().numpy(), TOL32, y_ref, s)
+    S.spmv_plan_destroy(plan)
+
+
+def test_chained_delta4_after_torch_kernels():
+    """DELTA4 runs whose x is produced by a torch kernel right before them."""
+    m = small("llm90_small")
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format="delta4")
+    x = torch.from_numpy(m.x).to(dev)
+    y1 = torch.full((m.n_rows,), float("nan"), device=dev)
+    y2 = torch.full((m.n_rows,), float("nan"), device=dev)
+    S.spmv_run(plan, x, y1)
+    x2 = (y1 * 0.01).half()          # torch kernels between the two runs
+    S.spmv_run(plan, x2, y2)
+    torch.cuda.synchronize()
+    y_ref, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x)
+    assert_parity(m, y1.cpu().numpy(), TOL16, y_ref, s)
+    y_ref2, s2 = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, x2.cpu().numpy())
+    assert_parity(m, y2.cpu().numpy(), TOL16, y_ref2, s2)
+    S.spmv_plan_destroy(plan)
