@@ -31,7 +31,10 @@ namespace {
 // Device indexing is 32-bit; keep clear of INT32_MAX so that padded spans
 // (up to one vector past the end) never overflow.
 constexpr int64_t kMaxIndex = (int64_t)INT32_MAX - 4096;
-constexpr size_t kXsAutoBytes = 48 * 1024;   // auto-stage x up to this size
+// x is gathered through L1 by default: staging it in shared memory costs a
+// copy per CTA and, for the LLM shapes, a third of the CTAs per SM, and was
+// measured slower on GB300 than L1-resident gathers.
+constexpr size_t kXsAutoBytes = 0;
 constexpr size_t kXsMaxBytes = 160 * 1024;   // hard limit when forced
 constexpr int kPadElems = 16;                // zero tail after device arrays
 constexpr int kAssumedSms = 152;             // for host-only inspection
@@ -291,6 +294,77 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
   return SPMV_OK;
 }
 
+spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out,
+                             spmv_plan_info* info) {
+  out->units.clear();
+  out->warp_base.clear();
+  out->cta_first.clear();
+  out->row_split.clear();
+  out->splits.clear();
+  out->n_chunks = 0;
+  const int64_t* rp = d->row_ptr;
+  // weight of a unit: its entries, plus 8 for the row it starts
+  const int64_t total_w = d->n_entries + 8 * (int64_t)d->n_rows;
+  constexpr int64_t kMinShare = 4096;
+  const int G = (int)std::max<int64_t>(
+      1, std::min<int64_t>(max_ctas, (total_w + kMinShare - 1) / kMinShare));
+  auto boundary = [&](int b) { return (int64_t)((__int128)b * total_w / G); };
+  int64_t cum = 0;
+  int next_b = 1;
+  try {
+    out->row_split.assign((size_t)d->n_rows, -1);
+    out->cta_first.push_back(0);
+    for (int32_t r = 0; r < d->n_rows; ++r) {
+      const int64_t w0 = rp[r] >> 3, w1 = rp[r + 1] >> 3, nw = w1 - w0;
+      const int64_t n_u = std::max<int64_t>(1, (nw + kDeltaUnitWords - 1) / kDeltaUnitWords);
+      const int64_t per = n_u > 1 ? (nw + n_u - 1) / n_u : std::max<int64_t>(nw, 1);
+      if (n_u > 1) {
+        if (out->n_chunks + n_u > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+        out->row_split[r] = (int32_t)out->splits.size();
+        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)n_u, (int32_t)w0, (int32_t)per});
+        out->n_chunks += n_u;
+        info->rows_per_bin[3] += 1;
+      } else {
+        info->rows_per_bin[nw * 8 > 256 ? 2 : (nw * 8 > 8 ? 1 : 0)] += 1;
+      }
+      int64_t col = 0;  // running column of the row, before word w
+      int64_t w = w0;
+      for (int64_t k = 0; k < n_u; ++k) {
+        const int64_t ub = std::min(w0 + k * per, w1), ue = std::min(ub + per, w1);
+        while (next_b < G && cum >= boundary(next_b)) {
+          out->cta_first.push_back((int32_t)out->units.size());
+          ++next_b;
+        }
+        // starting column of each warp's words of the unit (warp 0's is the
+        // unit's own starting column)
+        for (int wi = 0; wi < kWarps; ++wi) {
+          const int64_t seg = std::min(ub + (int64_t)wi * kDeltaWarpWords, ue);
+          for (; w < seg; ++w) {
+            const uint32_t word = d->words[w];
+            for (int q = 0; q < 8; ++q) col += (word >> (4 * q)) & 0xFu;
+          }
+          if (col > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+          out->warp_base.push_back((int32_t)col);
+        }
+        const uint32_t flags = (k == 0 ? kUnitFirst : 0u) | (k == n_u - 1 ? kUnitLast : 0u);
+        out->units.push_back({(int32_t)((uint32_t)r | flags), (int32_t)ub, (int32_t)ue,
+                              out->warp_base[out->warp_base.size() - kWarps]});
+        cum += (ue - ub) * 8 + (k == 0 ? 8 : 0);
+      }
+    }
+    while ((int)out->cta_first.size() <= G) out->cta_first.push_back((int32_t)out->units.size());
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  if ((int64_t)out->units.size() > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+  info->n_tiles = (int64_t)out->units.size();
+  info->n_split_rows = (int64_t)out->splits.size();
+  info->tiles_per_bin[2] = info->n_tiles - out->n_chunks;
+  info->tiles_per_bin[3] = out->n_chunks;
+  info->grid = G;
+  return SPMV_OK;
+}
+
 namespace {
 
 // ------------------------------------------------------------ CUDA helpers
@@ -341,7 +415,8 @@ void free_plan(spmv_plan* plan) {
     DeviceGuard g(p->device);
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->words,
                     p->tiles,   p->splits,   p->partials, p->counters,
-                    p->status,  p->x_stage,  p->y_stage,  p->cta_first};
+                    p->status,  p->x_stage,  p->y_stage,  p->cta_first,
+                    p->row_split, p->warp_base};
     for (void* b : bufs)
       if (b) cudaFree(b);
   }
@@ -457,41 +532,47 @@ spmv_status validate_delta(const spmv_delta* d, int64_t* nnz_out) {
 spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   spmv_status s;
   spmv_plan_info& info = p->info;
+  if (d->n_rows > (int32_t)kUnitRowMask) return SPMV_ERR_TOO_LARGE;
   if ((s = bind_device(p)) != SPMV_OK) return s;
   const size_t xbytes = (size_t)d->n_cols * 2;
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
             : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
-  p->dyn_smem = p->x_smem ? (xbytes + 15) / 16 * 16 : 0;
+  p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
+                kDeltaStages * delta_stage_bytes();
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
+  const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
-  p->grid = (int)std::min<int64_t>(d->n_rows, (int64_t)occ * p->sm_count);
-  p->n_tiles = d->n_rows;
-  std::vector<int32_t> rp32;
-  try {
-    rp32.resize((size_t)d->n_rows + 1);
-  } catch (const std::bad_alloc&) {
-    return SPMV_ERR_OUT_OF_MEMORY;
-  }
-  for (int32_t r = 0; r <= d->n_rows; ++r) rp32[r] = (int32_t)d->row_ptr[r];
+  DeltaTables t;
+  if ((s = plan_delta_units(d, occ * p->sm_count, &t, &info)) != SPMV_OK) return s;
+  p->grid = info.grid;
+  p->n_tiles = (int64_t)t.units.size();
   const size_t e_alloc = (size_t)d->n_entries + 8 * kPadElems;
-  if ((s = dev_upload(&p->row_ptr, rp32.data(), rp32.size() * 4,
-                      rp32.size() * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->values, d->values, (size_t)d->n_entries * 2,
                       e_alloc * 2)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->words, d->words, (size_t)d->n_entries / 2,
                       e_alloc / 2)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->tiles, t.units.data(), t.units.size() * sizeof(Tile),
+                      t.units.size() * sizeof(Tile))) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->warp_base, t.warp_base.data(), t.warp_base.size() * 4,
+                      t.warp_base.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->cta_first, t.cta_first.data(), t.cta_first.size() * 4,
+                      t.cta_first.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->row_split, t.row_split.data(), t.row_split.size() * 4,
+                      t.row_split.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->splits, t.splits.data(), t.splits.size() * sizeof(SplitInfo),
+                      t.splits.size() * sizeof(SplitInfo))) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->partials, nullptr, 0, (size_t)t.n_chunks * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
-  info.n_tiles = d->n_rows;
-  info.rows_per_bin[2] = d->n_rows;   // one CTA per row
-  info.tiles_per_bin[2] = d->n_rows;
   info.x_in_smem = p->x_smem ? 1 : 0;
-  info.grid = p->grid;
   info.block = kThreads;
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = d->n_entries * 2 + d->n_entries / 2 +
                       ((int64_t)d->n_rows + 1) * 4;
-  info.aux_bytes = 0;
+  info.aux_bytes = (int64_t)(t.units.size() * sizeof(Tile) + t.warp_base.size() * 4 +
+                             t.cta_first.size() * 4 + t.row_split.size() * 4 +
+                             t.splits.size() * (sizeof(SplitInfo) + 4) +
+                             (size_t)t.n_chunks * 4);
   fill_bytes(&info, 2);
   return SPMV_OK;
 }
@@ -616,24 +697,22 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   info->block = kThreads;
   if (delta) {
     if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
-    int64_t gaps = 0, total = 0;
-    for (int32_t r = 0; r < m->n_rows; ++r) {
-      int64_t n = delta_row_entries(m->col_idx + m->row_ptr[r],
-                                    m->row_ptr[r + 1] - m->row_ptr[r], &gaps);
-      total += (n + kRowAlign - 1) / kRowAlign * kRowAlign;
+    spmv_delta d;
+    if ((s = spmv_convert(m, &d)) != SPMV_OK) return s;
+    if (d.n_entries > kMaxIndex) {
+      spmv_delta_free(&d);
+      return SPMV_ERR_TOO_LARGE;
     }
-    if (total > kMaxIndex) return SPMV_ERR_TOO_LARGE;
-    info->n_entries = total;
-    info->n_tiles = m->n_rows;
-    info->rows_per_bin[2] = m->n_rows;
-    info->tiles_per_bin[2] = m->n_rows;
+    DeltaTables t;
+    s = plan_delta_units(&d, 5 * kAssumedSms, &t, info);
+    info->n_entries = d.n_entries;
     info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * 2 <=
                       (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);
-    info->grid = (int32_t)std::min<int64_t>(m->n_rows, 8LL * kAssumedSms);
     info->launches_per_run = m->n_rows > 0;
-    info->matrix_bytes = total * 2 + total / 2 + ((int64_t)m->n_rows + 1) * 4;
+    info->matrix_bytes = d.n_entries * 2 + d.n_entries / 2 + ((int64_t)m->n_rows + 1) * 4;
     fill_bytes(info, 2);
-    return SPMV_OK;
+    spmv_delta_free(&d);
+    return s;
   }
   CsrTables t;
   s = plan_csr_tiles(m->n_rows, m->row_ptr, o, 5 * kAssumedSms, &t, info);

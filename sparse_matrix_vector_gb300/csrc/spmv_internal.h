@@ -28,7 +28,21 @@ constexpr int kTileCap = SPMV_TILE_CAP;
 constexpr int kStreamTileCap = (kTileCap < kThreads * 8 ? kTileCap : kThreads * 8) - 16;
 constexpr int kTileRowsCap = 512;        // rows of a short-row tile
 constexpr int kStages = SPMV_STAGES;
-constexpr int kDeltaWordsPerRound = kThreads;  // one 32-bit delta word per thread
+// DELTA4 kernel: a work unit is a slice of one row of at most
+// kDeltaUnitWords packed words (8 entries each), 2 words per thread, so warp
+// w decodes the unit's words [64w, 64w + 64).
+constexpr int kDeltaLaneWords = 2;
+constexpr int kDeltaWarpWords = 32 * kDeltaLaneWords;
+constexpr int kDeltaUnitWords = kDeltaWarpWords * kWarps;
+#ifndef SPMV_DELTA_STAGES
+#define SPMV_DELTA_STAGES 2
+#endif
+constexpr int kDeltaStages = SPMV_DELTA_STAGES;
+// DELTA4 unit descriptor: {row | FIRST | LAST, word_begin, word_end, column
+// before the unit's first entry}; FIRST / LAST: first / last unit of the row.
+constexpr uint32_t kUnitFirst = 1u << 31;
+constexpr uint32_t kUnitLast = 1u << 30;
+constexpr uint32_t kUnitRowMask = (1u << 30) - 1u;
 
 // Tile descriptor (one int4 per work unit of the CSR kernel).
 //   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | WALK? | lg << 16 | rows}
@@ -86,6 +100,20 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* row_ptr,
                            const Options& opt, int max_ctas, CsrTables* out,
                            spmv_plan_info* info);
 
+// Host-side result of planning a DELTA4 matrix.
+struct DeltaTables {
+  std::vector<Tile> units;
+  std::vector<int32_t> warp_base;  // per unit, kWarps columns: the column before
+                                   // the first entry of each warp's words
+  std::vector<int32_t> cta_first;  // CTA b runs units [cta_first[b], cta_first[b+1])
+  std::vector<int32_t> row_split;  // per row: index into splits, or -1
+  std::vector<SplitInfo> splits;   // {first_slot, n_units, row's first word, words per unit}
+  int64_t n_chunks = 0;
+};
+
+spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out,
+                             spmv_plan_info* info);
+
 // Device resources of a plan.
 struct Plan {
   int device = -1;
@@ -110,6 +138,8 @@ struct Plan {
   Tile* tiles = nullptr;
   SplitInfo* splits = nullptr;
   int32_t* cta_first = nullptr;
+  int32_t* row_split = nullptr;  // DELTA4: split id per row or -1
+  int32_t* warp_base = nullptr;  // DELTA4: kWarps starting columns per unit
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
   int32_t* status = nullptr;    // device status word
@@ -125,6 +155,8 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem);
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem);
 int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn);
 size_t csr_stage_bytes(spmv_dtype dtype);
+size_t delta_stage_bytes();
+size_t delta_x_smem_bytes(int n_cols);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 

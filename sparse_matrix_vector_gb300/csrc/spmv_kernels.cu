@@ -22,14 +22,13 @@
 // (mlqm.cn) 2.1.1 / 2.2 (rows binned to partial-warp, warp and block-per-row
 // kernels); "MACKO-SpMV" (maplevalley.com.cn) 3.3 (splitting long rows).
 //
-// DELTA4 kernel ("MACKO-SpMV" 2.2): one CTA per row (grid-stride over rows).
-// A round covers 256 packed words (2048 entries): thread t loads word t (four
-// bytes of nibbles, coalesced) and the eight fp16 values of those entries (16
-// bytes, coalesced); the columns are rebuilt by a per-thread sum of 8 nibbles,
-// a 5-step __shfl_up_sync inclusive scan inside each warp and a prefix over the
-// CTA's warp totals; products are taken in half2 (__hmul2) and accumulated in
-// fp32. The next round's loads are issued before the current round is
-// decoded, across row boundaries too.
+// DELTA4 kernel ("MACKO-SpMV" 2.2): persistent like the CSR kernel; a work
+// unit is a slice of one row (at most 512 packed words = 4096 entries) whose
+// starting column, and each warp's starting column in it, the planner
+// stored, so units and warps are independent. Lane l of warp w decodes two
+// words: a per-lane sum of their 16 nibbles and a 5-step __shfl_up_sync
+// inclusive scan give the column before its first entry; products are taken
+// in half2 (__hmul2) and accumulated in fp32 per row across units.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -39,22 +38,6 @@
 
 namespace spmv {
 namespace {
-
-// ------------------------------------------------------------ load helpers
-// Matrix data is read exactly once: read-only path, no L1 allocation.
-__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p) {
-  uint32_t r;
-  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
 
 // x gathered through shared memory (staged) or the read-only path.
 template <bool XS>
@@ -584,14 +567,55 @@ __global__ void __launch_bounds__(kThreads) csr_kernel(const CsrArgs a) {
 
 // ------------------------------------------------------------ DELTA4 kernel
 struct DeltaArgs {
-  const int32_t* __restrict__ row_ptr;  // entry offsets, multiples of 8
   const uint32_t* __restrict__ words;   // 8 nibbles per word
-  const uint4* __restrict__ vals;       // 8 fp16 values per 16 bytes
+  const __half* __restrict__ vals;      // 8 fp16 values per word, 16 bytes
   const __half* __restrict__ x;
   float* __restrict__ y;
-  int n_rows;
+  const int4* __restrict__ units;       // {row | FIRST | LAST, wb, we, column base}
+  const int32_t* __restrict__ warp_base;  // kWarps starting columns per unit
+  const int32_t* __restrict__ cta_first;
+  const int32_t* __restrict__ row_split;
+  const SplitInfo* __restrict__ splits;  // {first_slot, n_units, row word, words/unit}
+  float* partials;
+  int32_t* counters;
+  int32_t* status;
   int n_cols;
 };
+
+// Shared-memory stage of one DELTA4 unit: the warps' starting columns, the
+// unit's words (aligned out to 4 words) and its values (16 bytes per word).
+struct DeltaStage {
+  static constexpr int kBaseBytes = kWarps * 4;
+  static constexpr int kWordBytes = (kDeltaUnitWords + 8) * 4;
+  static constexpr int kValBytes = kDeltaUnitWords * 16;
+  static constexpr int kBytes = kBaseBytes + kWordBytes + kValBytes;
+};
+static_assert(DeltaStage::kBaseBytes % 16 == 0, "stage regions must stay 16-byte aligned");
+
+// x in shared memory, skewed by one 4-byte word per 128 bytes: lanes that
+// gather at a 64-byte stride (16 entries per lane at 50% density) then hit
+// distinct banks. Half i lives at i + 2 * (i / 64).
+__device__ __forceinline__ int x_skew(int i) { return i + 2 * (i >> 6); }
+
+__device__ __forceinline__ void stage_x_skewed(__half* xs, const __half* x, int n) {
+  uint32_t* dst = reinterpret_cast<uint32_t*>(xs);
+  const int pairs = n >> 1;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    for (int v = threadIdx.x; v < (pairs >> 2); v += kThreads) {
+      const uint4 q = __ldg(src + v);
+      const int j = 4 * v;  // first pair of the vector; 4 pairs never cross a 32-pair row
+      dst[j + (j >> 5)] = q.x;
+      dst[j + 1 + (j >> 5)] = q.y;
+      dst[j + 2 + (j >> 5)] = q.z;
+      dst[j + 3 + (j >> 5)] = q.w;
+    }
+    for (int i = ((pairs >> 2) << 3) + threadIdx.x; i < n; i += kThreads) xs[x_skew(i)] = x[i];
+  } else {
+    for (int i = threadIdx.x; i < n; i += kThreads) xs[x_skew(i)] = x[i];
+  }
+  __syncthreads();
+}
 
 // Sum of the eight 4-bit fields of w (<= 120).
 __device__ __forceinline__ int nibble_sum(uint32_t w) {
@@ -599,106 +623,200 @@ __device__ __forceinline__ int nibble_sum(uint32_t w) {
   return (int)((b * 0x01010101u) >> 24);
 }
 
-template <bool XS>
-__device__ __forceinline__ __half gather_h(const __half* xg, const __half* xs, int c) {
-  return XS ? xs[c] : __ldg(xg + c);
+// acc + (float)h, one fp32 rounding (mixed-precision add, f16 operand).
+__device__ __forceinline__ float add_f16(float acc, __half h) {
+  asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(__half_as_ushort(h)));
+  return acc;
 }
 
 template <bool XS>
+__device__ __forceinline__ __half gather_h(const __half* xg, const __half* xs, int c) {
+  return XS ? xs[x_skew(c)] : __ldg(xg + c);
+}
+
+// Decode one word (8 entries) starting after column `col`: add each delta,
+// gather x, multiply pairs in half2, add both products to fp32 accumulators.
+template <bool XS>
+__device__ __forceinline__ void decode_word(uint32_t w, const uint4 v, int& col,
+                                            const __half* xg, const __half* xs,
+                                            float& acc0, float& acc1) {
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    col += (int)((w >> (8 * h)) & 0xFu);
+    const __half x0 = gather_h<XS>(xg, xs, col);
+    col += (int)((w >> (8 * h + 4)) & 0xFu);
+    const __half x1 = gather_h<XS>(xg, xs, col);
+    __half2 av;
+    *reinterpret_cast<uint32_t*>(&av) = vw[h];
+    const __half2 prod = __hmul2(av, __halves2half2(x0, x1));
+    acc0 = add_f16(acc0, __low2half(prod));
+    acc1 = add_f16(acc1, __high2half(prod));
+  }
+}
+
+// Thread 0: start the TMA copies of DELTA4 unit u (descriptor d) into a stage.
+__device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* stage,
+                                           uint64_t* bar, int4* desc, int u, const int4 d,
+                                           uint64_t pol) {
+  if (u < 0) {
+    *desc = make_int4(-1, 0, 0, 0);
+    mbar_arrive(bar);
+    return;
+  }
+  *desc = d;
+  const int wb = d.y, we = d.z;
+  const int wa = wb & ~3;
+  const uint32_t nwb = (uint32_t)(((we + 3) & ~3) - wa) * 4u;
+  const uint32_t nvb = (uint32_t)(we - wb) * 16u;
+  if (nvb == 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  mbar_arrive_expect_tx(bar, DeltaStage::kBaseBytes + nwb + nvb);
+  bulk_g2s(stage, a.warp_base + (size_t)u * kWarps, DeltaStage::kBaseBytes, bar, pol);
+  bulk_g2s(stage + DeltaStage::kBaseBytes, a.words + wa, nwb, bar, pol);
+  bulk_g2s(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes, a.vals + (size_t)wb * 8,
+           nvb, bar, pol);
+}
+
+// Thread 0, at the end of this CTA's piece of a row split into units: as
+// split_publish for CSR, with units in place of chunks.
+__device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool whole,
+                                              int wb0, int wb, float part) {
+  if (whole) {
+    a.y[row] = part;
+    return;
+  }
+  const int sid = __ldg(a.row_split + row);
+  const SplitInfo si = a.splits[sid];
+  const int k0 = (wb0 - si.row_begin) / si.reserved;
+  const int k = (wb - si.row_begin) / si.reserved;
+  a.partials[si.first_slot + k0] = part;
+  __threadfence();
+  const int add = k - k0 + 1;
+  const int before = atomicAdd(a.counters + sid, add);
+  if (before + add == si.n_chunks) {
+    __threadfence();
+    float sum = 0.f;
+    for (int j = 0; j < si.n_chunks; ++j) {
+      sum += __ldcg(a.partials + si.first_slot + j);
+      a.partials[si.first_slot + j] = 0.f;
+    }
+    a.y[row] = sum;
+    a.counters[sid] = 0;
+  }
+}
+
+// Persistent DELTA4 kernel ("MACKO-SpMV" 2.2): each CTA walks its block of
+// units (equal weight per CTA); thread 0 keeps kDeltaStages units in flight
+// with TMA bulk copies. In a unit, warp w decodes words [64w, 64w+64) and
+// lane l words 64w+2l and 64w+2l+1 (16 entries): the column before the
+// lane's first entry is the warp's starting column (from the planner) plus
+// the lane's nibble sum put through a 5-step __shfl_up_sync inclusive scan.
+// Products are formed in half2 and accumulated in fp32 across the units of a
+// row; the row total is a CTA reduction.
+template <bool XS>
 __global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
   extern __shared__ __align__(128) unsigned char dyn_smem[];
-  __shared__ int s_tot[2][kWarps];
+  __shared__ __align__(8) uint64_t s_bar[kDeltaStages];
+  __shared__ int4 s_desc[kDeltaStages];
   __shared__ float s_red[kWarps];
-  __half* xs = reinterpret_cast<__half*>(dyn_smem);
+  __shared__ int s_fail;
+  unsigned char* stages = dyn_smem;
+  __half* xs = reinterpret_cast<__half*>(dyn_smem + kDeltaStages * DeltaStage::kBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = gridDim.x;
-  int r = blockIdx.x;
-  if (r >= a.n_rows) return;
-  int rb = __ldg(a.row_ptr + r) >> 3;         // first word of this round
-  int w_end = __ldg(a.row_ptr + r + 1) >> 3;  // one past the row's last word
-  int nr = r + G, nb0 = 0, nb1 = 0;           // next row and its word range
-  if (nr < a.n_rows) {
-    nb0 = __ldg(a.row_ptr + nr) >> 3;
-    nb1 = __ldg(a.row_ptr + nr + 1) >> 3;
+  const int u_begin = __ldg(a.cta_first + blockIdx.x);
+  const int u_end = __ldg(a.cta_first + blockIdx.x + 1);
+  uint64_t pol = 0;
+  int4 next_d = make_int4(0, 0, 0, 0);
+  int next_u = u_begin;
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kDeltaStages; ++s) mbar_init(&s_bar[s], 1);
+    fence_mbar_init();
+    s_fail = 0;
   }
-  uint32_t cw = 0;
-  uint4 cv = make_uint4(0u, 0u, 0u, 0u);
-  if (rb + tid < w_end) {
-    cw = ld_stream_u32(a.words + rb + tid);
-    cv = ld_stream_u4(a.vals + rb + tid);
+  __syncthreads();
+  if (tid == 0) {
+    pol = policy_evict_first();
+    int4 d0[kDeltaStages];
+#pragma unroll
+    for (int s = 0; s < kDeltaStages; ++s)
+      d0[s] = next_u + s < u_end ? __ldg(a.units + next_u + s) : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < kDeltaStages; ++s)
+      issue_unit(a, stages + s * DeltaStage::kBytes, &s_bar[s], &s_desc[s],
+                 next_u + s < u_end ? next_u + s : -1, d0[s], pol);
+    next_u += kDeltaStages;
+    if (next_u < u_end) next_d = __ldg(a.units + next_u);
+    pdl_launch_dependents();
   }
-  // plan-owned matrix data only above this point; x and y below
-  if (tid == 0) pdl_launch_dependents();
+  // plan-owned data only above; x and y below
   pdl_wait();
-  if (XS) stage_x<__half>(xs, a.x, a.n_cols);
-  float acc = 0.f;
-  int base = 0, buf = 0;
-  while (true) {
-    const bool row_done = rb + kDeltaWordsPerRound >= w_end;
-    // issue the next round's loads before decoding this one
-    const int fb = row_done ? nb0 : rb + kDeltaWordsPerRound;
-    const int fe = row_done ? nb1 : w_end;
-    const bool have_next = !row_done || nr < a.n_rows;
-    uint32_t pw = 0;
-    uint4 pv = make_uint4(0u, 0u, 0u, 0u);
-    if (have_next && fb + tid < fe) {
-      pw = ld_stream_u32(a.words + fb + tid);
-      pv = ld_stream_u4(a.vals + fb + tid);
+  if (XS) stage_x_skewed(xs, a.x, a.n_cols);
+  float acc0 = 0.f, acc1 = 0.f;  // this thread's share of the current row piece
+  int piece_wb0 = -1;
+  bool piece_first = false;
+  int i = 0;
+  for (;; ++i) {
+    const int s = i % kDeltaStages;
+    const uint32_t parity = (uint32_t)(i / kDeltaStages) & 1u;
+    const bool ok = mbar_wait_bounded(&s_bar[s], parity);
+    if (!ok) s_fail = 1;  // seen by all after the barrier that ends this unit
+    const int4 d = s_desc[s];
+    if (d.x == -1) break;  // uniform: every thread reads the same descriptor
+    unsigned char* stage = stages + s * DeltaStage::kBytes;
+    const uint32_t rw = (uint32_t)d.x;
+    const int row = (int)(rw & kUnitRowMask);
+    const int wb = d.y, n_w = d.z - d.y;
+    if (piece_wb0 < 0) {
+      piece_wb0 = wb;
+      piece_first = (rw & kUnitFirst) != 0;
     }
-    // columns: base + (warps before) + (lanes before) + (nibbles before)
-    const int ls = nibble_sum(cw);
+    const int* s_base = reinterpret_cast<const int*>(stage);
+    const uint32_t* s_words =
+        reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
+    const uint4* s_vals =
+        reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
+    const int j0 = kDeltaLaneWords * tid;  // this lane's first word in the unit
+    const uint32_t w0 = (ok && j0 < n_w) ? s_words[j0] : 0u;
+    const uint32_t w1 = (ok && j0 + 1 < n_w) ? s_words[j0 + 1] : 0u;
+    const int ls = nibble_sum(w0) + nibble_sum(w1);
     int incl = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int up = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += up;
     }
-    if (lane == 31) s_tot[buf][warp] = incl;
-    __syncthreads();
-    int pre = 0, tot = 0;
-#pragma unroll
-    for (int w2 = 0; w2 < kWarps; ++w2) {
-      const int t = s_tot[buf][w2];
-      tot += t;
-      pre += w2 < warp ? t : 0;
+    if (ok && j0 < n_w) {
+      int col = s_base[warp] + incl - ls;  // column before this lane's first entry
+      decode_word<XS>(w0, s_vals[j0], col, a.x, xs, acc0, acc1);
+      if (j0 + 1 < n_w) decode_word<XS>(w1, s_vals[j0 + 1], col, a.x, xs, acc0, acc1);
     }
-    buf ^= 1;
-    if (rb + tid < w_end) {
-      int col = base + pre + incl - ls;
-      const uint32_t vw[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        col += (int)((cw >> (8 * h)) & 0xFu);
-        const __half x0 = gather_h<XS>(a.x, xs, col);
-        col += (int)((cw >> (8 * h + 4)) & 0xFu);
-        const __half x1 = gather_h<XS>(a.x, xs, col);
-        __half2 av;
-        *reinterpret_cast<uint32_t*>(&av) = vw[h];
-        const float2 f = __half22float2(__hmul2(av, __halves2half2(x0, x1)));
-        acc += f.x;
-        acc += f.y;
-      }
+    const bool last = (rw & kUnitLast) != 0;
+    if (last || u_begin + i == u_end - 1) {  // row ends, or this CTA's share does
+      const float part = cta_sum(acc0 + acc1, s_red);
+      if (tid == 0) delta_publish(a, row, piece_first && last, piece_wb0, wb, part);
+      acc0 = acc1 = 0.f;
+      piece_wb0 = -1;
     }
-    base += tot;
-    if (row_done) {
-      const float sum = cta_sum(acc, s_red);
-      if (tid == 0) a.y[r] = sum;
-      acc = 0.f;
-      base = 0;
-      r = nr;
-      if (r >= a.n_rows) break;
-      rb = nb0;
-      w_end = nb1;
-      nr = r + G;
-      if (nr < a.n_rows) {
-        nb0 = __ldg(a.row_ptr + nr) >> 3;
-        nb1 = __ldg(a.row_ptr + nr + 1) >> 3;
-      }
-    } else {
-      rb += kDeltaWordsPerRound;
+    __syncthreads();  // stage s is free again
+    if (s_fail) break;
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      issue_unit(a, stage, &s_bar[s], &s_desc[s], next_u < u_end ? next_u : -1, next_d, pol);
+      ++next_u;
+      if (next_u < u_end) next_d = __ldg(a.units + next_u);
     }
-    cw = pw;
-    cv = pv;
+  }
+  if (tid == 0 && s_fail) {
+    atomicExch(a.status, 1);
+    // let copies still in flight land before the CTA's shared memory goes
+    for (int s = 0; s < kDeltaStages; ++s) {
+      const int fills = 1 + (i > s ? (i - 1 - s) / kDeltaStages + 1 : 0);
+      mbar_wait_bounded(&s_bar[s], (uint32_t)(fills - 1) & 1u);
+    }
   }
 }
 
@@ -759,6 +877,12 @@ int delta_kernel_occupancy(bool x_smem, size_t dyn_smem) {
   return n;
 }
 
+size_t delta_stage_bytes() { return (size_t)DeltaStage::kBytes; }
+
+size_t delta_x_smem_bytes(int n_cols) {
+  return ((size_t)n_cols + 2 * ((size_t)n_cols / 64) + 16) * 2;
+}
+
 size_t csr_stage_bytes(spmv_dtype dtype) {
   return dtype == SPMV_F32 ? stage_bytes<float>() : stage_bytes<__half>();
 }
@@ -800,14 +924,20 @@ int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
 }
 
 int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
-  if (p.n_rows == 0) return 0;
+  if (p.n_tiles == 0) return 0;
   DeltaArgs a;
-  a.row_ptr = p.row_ptr;
   a.words = p.words;
-  a.vals = reinterpret_cast<const uint4*>(p.values);
+  a.vals = static_cast<const __half*>(p.values);
   a.x = static_cast<const __half*>(x);
   a.y = y;
-  a.n_rows = p.n_rows;
+  a.units = reinterpret_cast<const int4*>(p.tiles);
+  a.warp_base = p.warp_base;
+  a.cta_first = p.cta_first;
+  a.row_split = p.row_split;
+  a.splits = p.splits;
+  a.partials = p.partials;
+  a.counters = p.counters;
+  a.status = p.status;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
   return launch_pdl(delta_entry(p.x_smem), p.grid, p.dyn_smem, stream, args);

@@ -235,7 +235,10 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     llm = workloads.llm(0.3, n=2048)
     info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols)
     assert info["rows_per_bin"] == [0, 0, llm.n_rows, 0]   # CTA
-    assert info["x_in_smem"] == 1
+    assert info["x_in_smem"] == 0                            # x via L1 by default
+    forced = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
+                                 options=S.spmv_plan_options(x_smem=1))
+    assert forced["x_in_smem"] == 1
     big = workloads.llm(0.3, n=4096)
     info = S.spmv_plan_inspect(big.row_ptr, big.col_idx, big.values, big.n_cols)
     assert info["rows_per_bin"] == [0, 0, 0, big.n_rows]   # split
