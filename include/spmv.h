@@ -120,7 +120,8 @@ typedef struct spmv_plan_options {
                             model of its row lengths), 1 lanes mode (rows
                             summed by `lanes` lanes from shared memory),
                             2 walk mode (per-thread segmented sums)        */
-  int32_t lanes;         /* lanes per row in forced lanes mode: 1..32      */
+  int32_t lanes;         /* lanes per row in forced lanes mode: 1..256
+                            (rounded down to a power of two)               */
   int32_t reserved[8];
 } spmv_plan_options;
 
@@ -164,7 +165,11 @@ const char* spmv_status_string(spmv_status status);
 /* Returns SPMV_ABI_VERSION of the built library. */
 int32_t spmv_abi_version(void);
 
-/* Fill *opts with the library defaults. */
+/* Fill *opts with "library default" in every field (sizes 0, x_smem -1,
+ * reduce 0). The defaults themselves depend on the matrix's value type and
+ * are chosen when the plan is made: a stage holds 2048 nonzeros (fp32 or
+ * fp16), short-row tiles take up to 16 fewer, rows above half of that get
+ * a tile of their own, and split chunks take up to a full stage. */
 void spmv_plan_options_init(spmv_plan_options* opts);
 
 /* [MACKO] section 2.1: convert a CSR matrix with fp16 values into DELTA4

@@ -100,27 +100,30 @@ inline void emit(uint16_t* vals, uint32_t* words, int64_t e, uint16_t bits,
 
 }  // namespace
 
-Options resolve_options(const spmv_plan_options* o) {
+Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype) {
   Options r;
-  r.tile_nnz = kStreamTileCap;
+  const int cap = tile_cap(dtype);
+  r.tile_nnz = cap - 16;
   r.tile_rows = kTileRowsCap;
-  r.cta_row_min = kStreamTileCap;
-  r.split_row_min = kTileCap;
-  r.split_chunk = kTileCap;
+  // a row too long to share a short-row tile with another of its length
+  // gets a tile of its own (products summed in registers, no parking)
+  r.cta_row_min = (cap - 16) / 2;
+  r.split_row_min = cap;
+  r.split_chunk = cap;
   r.x_smem = -1;
   r.reduce = -1;
   r.lanes_log2 = 0;
   if (o) {
-    if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, kStreamTileCap);
+    if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, cap - 16);
     if (o->tile_rows > 0) r.tile_rows = std::min(o->tile_rows, kTileRowsCap);
     if (o->cta_row_min > 0) r.cta_row_min = o->cta_row_min;
     if (o->split_row_min > 0) r.split_row_min = o->split_row_min;
-    if (o->split_chunk > 0) r.split_chunk = std::min(std::max(o->split_chunk, 64), kTileCap);
+    if (o->split_chunk > 0) r.split_chunk = std::min(std::max(o->split_chunk, 64), cap);
     if (o->x_smem >= 0) r.x_smem = o->x_smem ? 1 : 0;
     if (o->reduce == 1) {
       r.reduce = 0;
       int l = 0;
-      while ((2 << l) <= std::min(std::max(o->lanes, 1), 32)) ++l;
+      while ((2 << l) <= std::min(std::max(o->lanes, 1), kThreads)) ++l;
       r.lanes_log2 = l;
     } else if (o->reduce == 2) {
       r.reduce = 1;
@@ -129,7 +132,7 @@ Options resolve_options(const spmv_plan_options* o) {
   // a row that may sit in a short-row tile must fit one on its own, and a
   // row that is not split must fit one stage
   r.cta_row_min = std::min(r.cta_row_min, r.tile_nnz);
-  r.split_row_min = std::min(std::max(r.split_row_min, r.cta_row_min), kTileCap);
+  r.split_row_min = std::min(std::max(r.split_row_min, r.cta_row_min), cap);
   return r;
 }
 
@@ -139,37 +142,63 @@ Options resolve_options(const spmv_plan_options* o) {
 // shuffles. Walk mode: every thread sums its own 8 products by row and rows
 // that cross threads are finished from per-thread carries; its cost is
 // roughly fixed (binary search, walk, carries). Pick the cheaper one.
-static uint32_t choose_reduction(const int32_t* rp, int r0, int r1) {
-  const int R = r1 - r0;
+static int64_t lanes_cost(const int32_t* rp, int r0, int r1, int lg);
+
+// Lanes-mode width for a tile: the g = 2^lg with the cheapest cost.
+static uint32_t choose_lanes(const int32_t* rp, int r0, int r1) {
   int best_lg = 0;
   int64_t best = INT64_MAX;
-  for (int lg = 0; lg <= 5; ++lg) {
-    const int g = 1 << lg;
-    const int per_pass = kThreads >> lg;
-    const int per_warp = 32 >> lg;
-    int64_t worst = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      int64_t t = 0;
-      for (int p0 = 0; p0 < R; p0 += per_pass) {
-        const int rs = p0 + w * per_warp;
-        if (rs >= R) break;
-        int64_t m = 0;
-        for (int q = 0; q < per_warp && rs + q < R; ++q) {
-          const int64_t len = rp[r0 + rs + q + 1] - rp[r0 + rs + q];
-          m = std::max(m, (len + g - 1) / g);
-        }
-        t += 4 * m + 8 * lg + 40;  // ~cycles: dependent adds, shuffles, loads
-      }
-      worst = std::max(worst, t);
-    }
-    if (worst < best) {
-      best = worst;
+  for (int lg = 0; lg <= 8; ++lg) {
+    const int64_t c = lanes_cost(rp, r0, r1, lg);
+    if (c < best) {
+      best = c;
       best_lg = lg;
     }
   }
-  const int64_t walk_cost = 600;  // ~cycles: search, walk, carries, extra pass
-  if (best > walk_cost) return kStreamWalk;
   return (uint32_t)best_lg << kLanesShift;
+}
+
+static uint32_t choose_reduction(const int32_t* rp, int r0, int r1) {
+  const uint32_t lanes = choose_lanes(rp, r0, r1);
+  const int64_t best = lanes_cost(rp, r0, r1, (int)(lanes >> kLanesShift));
+  const int64_t walk_cost = 600;  // ~cycles: search, walk, carries, extra pass
+  return best > walk_cost ? kStreamWalk : lanes;
+}
+
+// ~cycles of lanes mode with g = 2^lg: per warp, the sum over its passes of
+// the slowest row's dependent additions plus shuffles and loads; the tile
+// costs as much as its slowest warp.
+static int64_t lanes_cost(const int32_t* rp, int r0, int r1, int lg) {
+  const int R = r1 - r0;
+  const int g = 1 << lg;
+  const int per_pass = kThreads >> lg;
+  if (lg > 5) {  // a row per group of g/32 warps, one barrier per pass
+    int64_t t = 0;
+    for (int p0 = 0; p0 < R; p0 += per_pass) {
+      int64_t m = 0;
+      for (int q = 0; q < per_pass && p0 + q < R; ++q)
+        m = std::max<int64_t>(m, ((int64_t)rp[r0 + p0 + q + 1] - rp[r0 + p0 + q] + g - 1) / g);
+      t += 4 * m + 8 * 5 + 40 + 100;
+    }
+    return t;
+  }
+  const int per_warp = 32 >> lg;
+  int64_t worst = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    int64_t t = 0;
+    for (int p0 = 0; p0 < R; p0 += per_pass) {
+      const int rs = p0 + w * per_warp;
+      if (rs >= R) break;
+      int64_t m = 0;
+      for (int q = 0; q < per_warp && rs + q < R; ++q) {
+        const int64_t len = rp[r0 + rs + q + 1] - rp[r0 + rs + q];
+        m = std::max(m, (len + g - 1) / g);
+      }
+      t += 4 * m + 8 * lg + 40;
+    }
+    worst = std::max(worst, t);
+  }
+  return worst;
 }
 
 // Bin of a row by how many threads cooperate on it (nonzeros per row): a
@@ -226,15 +255,17 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
     while (r < n_rows) {
       const int64_t len = (int64_t)rp[r + 1] - rp[r];
       if (len > o.split_row_min) {
+        // the fewest chunks of at most split_chunk, all of (nearly) equal size
         const int64_t nch = (len + o.split_chunk - 1) / o.split_chunk;
+        const int64_t per = (len + nch - 1) / nch;
         const int64_t sid = (int64_t)out->splits.size();
         if (sid > (int64_t)kSplitIdMask || out->n_chunks + nch > kMaxIndex)
           return SPMV_ERR_TOO_LARGE;
-        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)nch, rp[r], 0});
+        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)nch, rp[r], (int32_t)per});
         for (int64_t k = 0; k < nch; ++k) {
           mark();
-          const int64_t b = rp[r] + k * o.split_chunk;
-          const int64_t e = std::min<int64_t>(b + o.split_chunk, rp[r + 1]);
+          const int64_t b = rp[r] + k * per;
+          const int64_t e = std::min<int64_t>(b + per, rp[r + 1]);
           const uint32_t flags = (k == 0 ? kSplitFirst : 0u) | (k == nch - 1 ? kSplitLast : 0u);
           out->tiles.push_back({r, (int32_t)b, (int32_t)e,
                                 (int32_t)((kKindSplit << kKindShift) | flags |
@@ -273,9 +304,12 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
         info->rows_per_bin[row_bin(l, o)] += 1;
         ++r;
       }
-      const uint32_t mode = o.reduce == 1   ? kStreamWalk
-                            : o.reduce == 0 ? ((uint32_t)o.lanes_log2 << kLanesShift)
-                                            : choose_reduction(rp, r0, r);
+      // walk mode gives each thread 8 nonzeros, so larger tiles use lanes mode
+      const bool walk_fits = nz <= kStreamTileCap;
+      const uint32_t mode = (o.reduce == 1 && walk_fits) ? kStreamWalk
+                            : o.reduce != -1 ? ((uint32_t)o.lanes_log2 << kLanesShift)
+                            : walk_fits     ? choose_reduction(rp, r0, r)
+                                            : choose_lanes(rp, r0, r);
       out->tiles.push_back({r0, rp[r0], rp[r],
                             (int32_t)((kKindStream << kKindShift) | mode | (uint32_t)(r - r0))});
       if (mode & kStreamWalk) info->walk_tiles += 1;
@@ -606,16 +640,10 @@ int32_t spmv_abi_version(void) { return SPMV_ABI_VERSION; }
 
 void spmv_plan_options_init(spmv_plan_options* o) {
   if (!o) return;
+  // every size knob 0 = the default for the matrix's value type, chosen when
+  // the plan is made (the stage holds more fp16 than fp32 nonzeros)
   std::memset(o, 0, sizeof(*o));
-  Options r = resolve_options(nullptr);
-  o->tile_nnz = r.tile_nnz;
-  o->tile_rows = r.tile_rows;
-  o->cta_row_min = r.cta_row_min;
-  o->split_row_min = r.split_row_min;
-  o->split_chunk = r.split_chunk;
-  o->x_smem = r.x_smem;
-  o->reduce = 0;
-  o->lanes = 0;
+  o->x_smem = -1;
 }
 
 spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
@@ -688,7 +716,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   const bool delta = format == SPMV_FORMAT_DELTA4;
   spmv_status s = validate_csr(m, delta);
   if (s != SPMV_OK) return s;
-  Options o = resolve_options(opts);
+  Options o = resolve_options(opts, m->value_dtype);
   info->n_rows = m->n_rows;
   info->n_cols = m->n_cols;
   info->nnz = m->nnz;
@@ -741,7 +769,7 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
   spmv_status s = validate_csr(m, delta);
   if (s != SPMV_OK) return s;
   if (delta && m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
-  Options o = resolve_options(opts);
+  Options o = resolve_options(opts, m->value_dtype);
   spmv_plan* plan = new (std::nothrow) spmv_plan();
   if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
   Plan* p = &plan->impl;
@@ -794,7 +822,7 @@ spmv_status spmv_plan_create_delta(const spmv_delta* d,
   int64_t nnz = 0;
   spmv_status s = validate_delta(d, &nnz);
   if (s != SPMV_OK) return s;
-  Options o = resolve_options(opts);
+  Options o = resolve_options(opts, SPMV_F16);
   spmv_plan* plan = new (std::nothrow) spmv_plan();
   if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
   Plan* p = &plan->impl;

@@ -22,9 +22,18 @@ constexpr int kWarps = kThreads / 32;
 #ifndef SPMV_STAGES
 #define SPMV_STAGES 2
 #endif
+#ifndef SPMV_TILE_CAP_F16
+#define SPMV_TILE_CAP_F16 2048
+#endif
+// Stage capacity in nonzeros, per value type. Larger fp16 stages (2560,
+// 3072) measured slower on the same plans: the shared memory they take from
+// the L1 carve-out is what caches the gathered x.
 constexpr int kTileCap = SPMV_TILE_CAP;
+constexpr int kTileCapF16 = SPMV_TILE_CAP_F16;
+constexpr int tile_cap(spmv_dtype t) { return t == SPMV_F16 ? kTileCapF16 : kTileCap; }
 // A short-row tile gives each thread one chunk of 8 consecutive nonzeros, so
 // its aligned span (start rounded down to 8) must fit kThreads * 8.
+// (walk mode; lanes mode takes any tile that fits a stage, tile_cap - 16).
 constexpr int kStreamTileCap = (kTileCap < kThreads * 8 ? kTileCap : kThreads * 8) - 16;
 constexpr int kTileRowsCap = 512;        // rows of a short-row tile
 constexpr int kStages = SPMV_STAGES;
@@ -55,7 +64,7 @@ constexpr uint32_t kKindStream = 0u;
 constexpr uint32_t kKindRow = 1u;
 constexpr uint32_t kKindSplit = 2u;
 constexpr uint32_t kRowsMask = 0xFFFFu;  // rows of a short-row tile
-constexpr uint32_t kLanesShift = 16;     // log2(lanes per row), 3 bits
+constexpr uint32_t kLanesShift = 16;     // log2(lanes per row), 4 bits (1..256 lanes)
 constexpr uint32_t kStreamWalk = 1u << 20;
 constexpr uint32_t kSplitFirst = 1u << 29;
 constexpr uint32_t kSplitLast = 1u << 28;
@@ -69,7 +78,7 @@ struct SplitInfo {
   int32_t first_slot;  // index of chunk 0's partial sum in the scratch array
   int32_t n_chunks;
   int32_t row_begin;   // row_ptr[row]: chunk k starts at row_begin + k * chunk
-  int32_t reserved;
+  int32_t reserved;    // CSR: nonzeros per chunk; DELTA4: words per unit
 };
 
 // Effective planner settings (defaults filled, limits applied).
@@ -84,7 +93,7 @@ struct Options {
   int lanes_log2;  // lanes mode when forced
 };
 
-Options resolve_options(const spmv_plan_options* o);
+Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype);
 
 // Host-side result of planning a CSR matrix.
 struct CsrTables {

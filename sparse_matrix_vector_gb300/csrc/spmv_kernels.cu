@@ -188,8 +188,9 @@ struct CsrArgs {
 // tile, its row pointers (aligned out to multiples of 4).
 template <typename VT>
 struct Stage {
-  static constexpr int kColBytes = (kTileCap + 16) * 4;
-  static constexpr int kValBytes = ((kTileCap + 16) * (int)sizeof(VT) + 15) / 16 * 16;
+  static constexpr int kCap = sizeof(VT) == 2 ? kTileCapF16 : kTileCap;
+  static constexpr int kColBytes = (kCap + 16) * 4;
+  static constexpr int kValBytes = ((kCap + 16) * (int)sizeof(VT) + 15) / 16 * 16;
   static constexpr int kRpBytes = (kTileRowsCap + 8) * 4;
   static constexpr int kBytes = kColBytes + kValBytes + kRpBytes;
 };
@@ -274,14 +275,16 @@ __device__ __forceinline__ void chunk_products(const int* s_col, const VT* s_val
 // Short-row tile from a stage, lanes mode (rows of similar length): every
 // thread multiplies its 8 staged nonzeros by the gathered x and parks the
 // products in place of the staged columns; then each row is summed by
-// g = 2^lg lanes and a shuffle reduction.
+// g = 2^lg lanes and a shuffle reduction (g = 64..256: by g / 32 warps, whose
+// sums meet in shared memory).
 template <typename VT, typename XT, bool XS>
 __device__ __forceinline__ void stream_tile_lanes(const CsrArgs& a, const int4 d,
-                                                  unsigned char* stage, const XT* xs) {
+                                                  unsigned char* stage, const XT* xs,
+                                                  float* s_red) {
   const int tid = threadIdx.x;
   const int r0 = d.x, s = d.y, e = d.z;
   const int R = (int)((uint32_t)d.w & kRowsMask);
-  const int lg = (int)(((uint32_t)d.w >> kLanesShift) & 7u);
+  const int lg = (int)(((uint32_t)d.w >> kLanesShift) & 15u);
   const int a0 = s & ~7;
   const int s_rel = s - a0, e_rel = e - a0;
   const int n8 = (e_rel + 7) >> 3;
@@ -310,8 +313,20 @@ __device__ __forceinline__ void stream_tile_lanes(const CsrArgs& a, const int4 d
 #pragma unroll 4
       for (int i = b + lig; i < en; i += g) acc += s_prod[i];
     }
-    for (int o = g >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lig == 0 && r < R) a.y[r0 + r] = acc;
+    if (lg <= 5) {
+      for (int o = g >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lig == 0 && r < R) a.y[r0 + r] = acc;
+    } else {  // a group of g / 32 warps per row: warp sums, then the group's first thread
+      acc = warp_sum(acc);
+      if ((tid & 31) == 0) s_red[tid >> 5] = acc;
+      __syncthreads();
+      if (lig == 0 && r < R) {
+        float t = 0.f;
+        for (int w = 0; w < (g >> 5); ++w) t += s_red[(tid >> 5) + w];
+        a.y[r0 + r] = t;
+      }
+      __syncthreads();
+    }
   }
 }
 
@@ -439,8 +454,8 @@ __device__ __forceinline__ void split_publish(const CsrArgs& a, int row, int sid
     return;
   }
   const SplitInfo si = a.splits[sid];
-  const int k0 = (b0 - si.row_begin) / a.split_chunk;
-  const int k = (b - si.row_begin) / a.split_chunk;
+  const int k0 = (b0 - si.row_begin) / si.reserved;
+  const int k = (b - si.row_begin) / si.reserved;
   a.partials[si.first_slot + k0] = part;
   __threadfence();
   const int add = k - k0 + 1;
@@ -525,7 +540,7 @@ __global__ void __launch_bounds__(kThreads) csr_kernel(const CsrArgs a) {
       if (w & kStreamWalk)
         stream_tile_walk<VT, XT, XS>(a, d, stage, xs, s_carry);
       else
-        stream_tile_lanes<VT, XT, XS>(a, d, stage, xs);
+        stream_tile_lanes<VT, XT, XS>(a, d, stage, xs, s_red);
     } else if (kind == kKindRow) {
       const float part = cta_sum(chunk_sum<VT, XT, XS>(a, d, stage, xs), s_red);
       if (tid == 0) a.y[d.x] = part;

@@ -171,25 +171,28 @@ def test_converter_bit_exact_llm_full(spmv_lib):
     _converter_matches_oracle(workloads.llm(0.9))
 
 
-def effective(opts):
-    """The planner's limits after its clamps (tile_nnz <= 2032, rows that
-    are not split fit one 2048-nonzero stage)."""
-    tile_nnz = min(opts.tile_nnz, 2032)
-    cta = min(opts.cta_row_min, tile_nnz)
-    srm = min(max(opts.split_row_min, cta), 2048)
-    return tile_nnz, cta, srm, min(max(opts.split_chunk, 64), 2048)
+def effective(opts, cap=2048):
+    """The planner's limits after defaults (0 fields) and clamps, for a
+    stage of `cap` nonzeros (2048): tile_nnz <= cap - 16, single-row tiles
+    by default above half of that, rows that are not split fit one stage,
+    chunks of 64..cap nonzeros."""
+    tile_nnz = min(opts.tile_nnz or cap - 16, cap - 16)
+    cta = min(opts.cta_row_min or (cap - 16) // 2, tile_nnz)
+    srm = min(max(opts.split_row_min or cap, cta), cap)
+    chunk = min(max(opts.split_chunk, 64), cap) if opts.split_chunk else cap
+    return tile_nnz, cta, srm, chunk, opts.tile_rows or 512
 
 
 def expected_bins(lengths, opts):
     """Bins and tiles the planner must produce, from the row lengths alone."""
-    tile_nnz, cta, srm, chunk = effective(opts)
+    tile_nnz, cta, srm, chunk, tile_rows = effective(opts)
     split = lengths > srm
     single = (lengths > cta) & ~split
     bins = [int(np.sum((lengths <= 8) & ~split)),
             int(np.sum((lengths > 8) & (lengths <= 256) & ~split)),
             int(np.sum((lengths > 256) & ~split)), int(split.sum())]
     chunks = int(np.sum((lengths[split] + chunk - 1) // chunk))
-    return bins, int(single.sum()), chunks, tile_nnz, cta
+    return bins, int(single.sum()), chunks, tile_nnz, cta, tile_rows
 
 
 @pytest.mark.parametrize("kw", [{}, {"cta_row_min": 32},
@@ -202,7 +205,7 @@ def test_planner_bins(spmv_lib, kw):
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols,
                                options=opts)
     L = m.row_lengths()
-    bins, n_single, n_chunks, tile_nnz, cta = expected_bins(L, opts)
+    bins, n_single, n_chunks, tile_nnz, cta, tile_rows = expected_bins(L, opts)
     assert info["rows_per_bin"] == bins
     assert sum(info["rows_per_bin"]) == m.n_rows
     assert info["tiles_per_bin"][2] == n_single
@@ -210,7 +213,7 @@ def test_planner_bins(spmv_lib, kw):
     assert info["n_split_rows"] == bins[3]
     short = L[L <= cta]
     min_tiles = max(int(np.ceil(short.sum() / tile_nnz)),
-                    int(np.ceil(short.size / opts.tile_rows)))
+                    int(np.ceil(short.size / tile_rows)))
     assert info["tiles_per_bin"][0] >= min_tiles
     assert info["n_tiles"] == sum(info["tiles_per_bin"])
     assert info["algorithmic_bytes"] == (8 * m.nnz + 4 * (m.n_rows + 1)
@@ -239,7 +242,7 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     forced = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
                                  options=S.spmv_plan_options(x_smem=1))
     assert forced["x_in_smem"] == 1
-    big = workloads.llm(0.3, n=4096)
+    big = workloads.llm(0.3, n=6144)   # ~4300 nonzeros per row > one stage (2048)
     info = S.spmv_plan_inspect(big.row_ptr, big.col_idx, big.values, big.n_cols)
     assert info["rows_per_bin"] == [0, 0, 0, big.n_rows]   # split
     info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,

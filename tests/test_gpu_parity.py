@@ -131,6 +131,8 @@ def test_full_size_delta4(name):
     {"tile_nnz": 97, "tile_rows": 13}, {"tile_nnz": 8}, {"tile_rows": 1},
     {"x_smem": 0}, {"x_smem": 1},
     {"reduce": 1, "lanes": 1}, {"reduce": 1, "lanes": 4}, {"reduce": 1, "lanes": 32},
+    {"reduce": 1, "lanes": 64}, {"reduce": 1, "lanes": 256},
+    {"reduce": 1, "lanes": 128, "tile_rows": 3},
     {"reduce": 2}, {"reduce": 2, "tile_nnz": 97},
 ])
 def test_forced_planner_paths(kw):
@@ -142,7 +144,8 @@ def test_forced_planner_paths(kw):
 
 @pytest.mark.parametrize("kw", [{"x_smem": 0}, {"x_smem": 1},
                                 {"cta_row_min": 100, "split_row_min": 150,
-                                 "split_chunk": 64}])
+                                 "split_chunk": 64},
+                                {"cta_row_min": 2000, "reduce": 1, "lanes": 128}])
 def test_forced_paths_fp16_csr(kw):
     m = workloads.llm(0.8, n=1000, seed=3)
     y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
