@@ -74,11 +74,16 @@ struct Tile {
   int32_t a, b, c, d;
 };
 
+// A row whose sum is assembled from partial sums.
+//   CSR:    {first slot, chunks, row_ptr[row] (chunk k starts at row_begin +
+//            k * per_chunk), nonzeros per chunk}
+//   DELTA4: {first slot, units, the row's first word (unit k starts at
+//            row_begin + k * per_unit), words per unit}
 struct SplitInfo {
-  int32_t first_slot;  // index of chunk 0's partial sum in the scratch array
-  int32_t n_chunks;
-  int32_t row_begin;   // row_ptr[row]: chunk k starts at row_begin + k * chunk
-  int32_t reserved;    // CSR: nonzeros per chunk; DELTA4: words per unit
+  int32_t first_slot;  // index of the first partial sum in the scratch array
+  int32_t n_chunks;    // partial sums to wait for
+  int32_t row_begin;
+  int32_t reserved;
 };
 
 // Effective planner settings (defaults filled, limits applied).

@@ -187,6 +187,10 @@ struct CsrArgs {
 // nonzero span (aligned out to multiples of 8 elements) and, for a short-row
 // tile, its row pointers (aligned out to multiples of 4).
 template <typename VT>
+struct Stage;
+template <typename VT>
+constexpr int kCsrCtasPerSm = sizeof(VT) == 2 ? 6 : 5;
+template <typename VT>
 struct Stage {
   static constexpr int kCap = sizeof(VT) == 2 ? kTileCapF16 : kTileCap;
   static constexpr int kColBytes = (kCap + 16) * 4;
@@ -336,9 +340,10 @@ __device__ __forceinline__ void stream_tile_lanes(const CsrArgs& a, const int4 d
 // finds the row of its first nonzero by binary search over the staged row
 // pointers and walks its 8 nonzeros: a row that starts and ends inside its
 // range is written to y at once; the partial of a row that continues past
-// its range is parked in s_carry[t]; the thread where a row that began in an
-// earlier thread ends adds the parked partials of the threads the row spans
-// (in thread order) to its own. Rows without nonzeros are written as 0 by a
+// its range is a carry; the thread where a row that began in an earlier
+// thread ends adds the carries of the threads the row spans, which a
+// segmented scan over the CTA (shuffles within warps, warp totals through
+// shared memory) has summed. Rows without nonzeros are written as 0 by a
 // separate pass. Work per thread is bounded whatever the row lengths are.
 template <typename VT, typename XT, bool XS>
 __device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
@@ -359,6 +364,13 @@ __device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
   float* y = a.y + r0;
 
   const int lo = max(8 * tid, s_rel), hi = min(8 * tid + 8, e_rel);
+  // Carries: a row that runs past this thread's nonzeros leaves its partial
+  // sum in v; head is false only for a thread that lies wholly inside a row
+  // begun by an earlier thread. A segmented inclusive scan of (v, head) over
+  // the CTA then hands a thread that ends such a row the sum of that row's
+  // carries, in a fixed order and in O(log) steps whatever the row's length.
+  float v = 0.f;
+  bool head = true;
   bool closes = false;  // this thread ends a row that began in an earlier thread
   int close_row = 0;
   float close_val = 0.f;
@@ -400,8 +412,9 @@ __device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
         acc += p[q];
       }
     }
-    if (row_end > hi) {
-      s_carry[tid] = acc;  // the row goes on in the next thread(s)
+    if (row_end > hi) {  // the row goes on in the next thread(s)
+      v = acc;
+      head = inside;
     } else if (inside) {
       y[row] = acc;
     } else {
@@ -412,12 +425,32 @@ __device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
   }
   for (int r = tid; r < R; r += kThreads)
     if (s_rp[r] == s_rp[r + 1]) y[r] = 0.f;
-  __syncthreads();
-  if (closes) {
-    float sum = 0.f;
-    for (int t = (s_rp[close_row] - a0) >> 3; t < tid; ++t) sum += s_carry[t];
-    y[close_row] = sum + close_val;
+  // warp-level segmented scan: (u, hu) (+) (v, h) = (h ? v : u + v, hu | h)
+  const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+  for (int dd = 1; dd < 32; dd <<= 1) {
+    const float uv = __shfl_up_sync(0xffffffffu, v, dd);
+    const int uh = __shfl_up_sync(0xffffffffu, head ? 1 : 0, dd);
+    if (lane >= dd && !head) {
+      v += uv;
+      head = uh != 0;
+    }
   }
+  int* s_head = reinterpret_cast<int*>(s_carry + kWarps);
+  if (lane == 31) {
+    s_carry[wid] = v;
+    s_head[wid] = head ? 1 : 0;
+  }
+  __syncthreads();
+  // the scan's value entering this warp: earlier warps' totals, segmented
+  float pv = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < kWarps; ++w2)
+    if (w2 < wid) pv = s_head[w2] ? s_carry[w2] : pv + s_carry[w2];
+  const float full = head ? v : v + pv;
+  float before = __shfl_up_sync(0xffffffffu, full, 1);
+  if (lane == 0) before = pv;
+  if (closes) y[close_row] = before + close_val;
 }
 
 // Per-thread partial sum of a staged slice [b, e) of one row.
@@ -475,13 +508,15 @@ __device__ __forceinline__ void split_publish(const CsrArgs& a, int row, int sid
 // Persistent CSR kernel: each CTA walks its contiguous block of work units;
 // thread 0 keeps kStages units in flight (TMA bulk copies into a ring of shared
 // memory stages) while the CTA computes the oldest one.
+// Register budget: as many CTAs per SM as the planner's shared-memory budget
+// lets in (5 with fp32 stages, 6 with fp16 ones).
 template <typename VT, typename XT, bool XS>
-__global__ void __launch_bounds__(kThreads) csr_kernel(const CsrArgs a) {
+__global__ void __launch_bounds__(kThreads, kCsrCtasPerSm<VT>) csr_kernel(const CsrArgs a) {
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_bar[kStages];
   __shared__ int4 s_desc[kStages];
   __shared__ float s_red[kWarps];
-  __shared__ float s_carry[kThreads];
+  __shared__ float s_carry[2 * kWarps];  // walk mode: warp totals and head flags
   unsigned char* stages = dyn_smem;
   // this CTA's contiguous block of work units (equal weight per CTA)
   const int u_begin = __ldg(a.cta_first + blockIdx.x);
