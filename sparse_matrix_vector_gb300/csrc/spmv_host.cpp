@@ -350,6 +350,8 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
     out->cta_first.push_back(0);
     for (int32_t r = 0; r < d->n_rows; ++r) {
       const int64_t w0 = rp[r] >> 3, w1 = rp[r + 1] >> 3, nw = w1 - w0;
+      const bool half = nw <= kDeltaUnitWords / 2;
+      const int64_t warp_words = half ? kDeltaWarpWords / 2 : kDeltaWarpWords;
       const int64_t n_u = std::max<int64_t>(1, (nw + kDeltaUnitWords - 1) / kDeltaUnitWords);
       const int64_t per = n_u > 1 ? (nw + n_u - 1) / n_u : std::max<int64_t>(nw, 1);
       if (n_u > 1) {
@@ -372,7 +374,7 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
         // starting column of each warp's words of the unit (warp 0's is the
         // unit's own starting column)
         for (int wi = 0; wi < kWarps; ++wi) {
-          const int64_t seg = std::min(ub + (int64_t)wi * kDeltaWarpWords, ue);
+          const int64_t seg = std::min(ub + (int64_t)wi * warp_words, ue);
           for (; w < seg; ++w) {
             const uint32_t word = d->words[w];
             for (int q = 0; q < 8; ++q) col += (word >> (4 * q)) & 0xFu;
@@ -380,7 +382,8 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
           if (col > INT32_MAX) return SPMV_ERR_TOO_LARGE;
           out->warp_base.push_back((int32_t)col);
         }
-        const uint32_t flags = (k == 0 ? kUnitFirst : 0u) | (k == n_u - 1 ? kUnitLast : 0u);
+        const uint32_t flags = (k == 0 ? kUnitFirst : 0u) | (k == n_u - 1 ? kUnitLast : 0u) |
+                               (half ? kUnitHalf : 0u);
         out->units.push_back({(int32_t)((uint32_t)r | flags), (int32_t)ub, (int32_t)ue,
                               out->warp_base[out->warp_base.size() - kWarps]});
         cum += (ue - ub) * 8 + (k == 0 ? 8 : 0);
@@ -582,8 +585,11 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
                 kDeltaStages * delta_stage_bytes();
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
+  int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
+#ifdef SPMV_DELTA_MAX_CTAS_PER_SM
+  occ = std::min(occ, SPMV_DELTA_MAX_CTAS_PER_SM);
+#endif
   DeltaTables t;
   if ((s = plan_delta_units(d, occ * p->sm_count, &t, &info)) != SPMV_OK) return s;
   p->grid = info.grid;

@@ -51,7 +51,11 @@ constexpr int kDeltaStages = SPMV_DELTA_STAGES;
 // before the unit's first entry}; FIRST / LAST: first / last unit of the row.
 constexpr uint32_t kUnitFirst = 1u << 31;
 constexpr uint32_t kUnitLast = 1u << 30;
-constexpr uint32_t kUnitRowMask = (1u << 30) - 1u;
+// HALF: one word per lane (warp w decodes words [32w, 32w + 32)), for rows
+// of at most kDeltaUnitWords / 2 words, which would leave most warps idle
+// at two words per lane.
+constexpr uint32_t kUnitHalf = 1u << 29;
+constexpr uint32_t kUnitRowMask = (1u << 29) - 1u;
 
 // Tile descriptor (one int4 per work unit of the CSR kernel).
 //   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | WALK? | lg << 16 | rows}

@@ -188,8 +188,14 @@ struct CsrArgs {
 // tile, its row pointers (aligned out to multiples of 4).
 template <typename VT>
 struct Stage;
+#ifndef SPMV_CSR_CTAS_F16
+#define SPMV_CSR_CTAS_F16 6
+#endif
+#ifndef SPMV_CSR_CTAS_F32
+#define SPMV_CSR_CTAS_F32 5
+#endif
 template <typename VT>
-constexpr int kCsrCtasPerSm = sizeof(VT) == 2 ? 6 : 5;
+constexpr int kCsrCtasPerSm = sizeof(VT) == 2 ? SPMV_CSR_CTAS_F16 : SPMV_CSR_CTAS_F32;
 template <typename VT>
 struct Stage {
   static constexpr int kCap = sizeof(VT) == 2 ? kTileCapF16 : kTileCap;
@@ -761,13 +767,17 @@ __device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool 
 // Persistent DELTA4 kernel ("MACKO-SpMV" 2.2): each CTA walks its block of
 // units (equal weight per CTA); thread 0 keeps kDeltaStages units in flight
 // with TMA bulk copies. In a unit, warp w decodes words [64w, 64w+64) and
-// lane l words 64w+2l and 64w+2l+1 (16 entries): the column before the
+// lane l words 64w+2l and 64w+2l+1 (16 entries; in a HALF unit, of a short
+// row, words [32w, 32w+32) and word 32w+l): the column before the
 // lane's first entry is the warp's starting column (from the planner) plus
 // the lane's nibble sum put through a 5-step __shfl_up_sync inclusive scan.
 // Products are formed in half2 and accumulated in fp32 across the units of a
 // row; the row total is a CTA reduction.
+#ifndef SPMV_DELTA_MIN_BLOCKS
+#define SPMV_DELTA_MIN_BLOCKS 6
+#endif
 template <bool XS>
-__global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
+__global__ void __launch_bounds__(kThreads, SPMV_DELTA_MIN_BLOCKS) delta4_kernel(const DeltaArgs a) {
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_bar[kDeltaStages];
   __shared__ int4 s_desc[kDeltaStages];
@@ -829,9 +839,10 @@ __global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
         reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
     const uint4* s_vals =
         reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
-    const int j0 = kDeltaLaneWords * tid;  // this lane's first word in the unit
+    const bool two = (rw & kUnitHalf) == 0;  // words per lane: 2, or 1 for a short row
+    const int j0 = two ? kDeltaLaneWords * tid : tid;  // this lane's first word in the unit
     const uint32_t w0 = (ok && j0 < n_w) ? s_words[j0] : 0u;
-    const uint32_t w1 = (ok && j0 + 1 < n_w) ? s_words[j0 + 1] : 0u;
+    const uint32_t w1 = (two && ok && j0 + 1 < n_w) ? s_words[j0 + 1] : 0u;
     const int ls = nibble_sum(w0) + nibble_sum(w1);
     int incl = ls;
 #pragma unroll
@@ -842,7 +853,7 @@ __global__ void __launch_bounds__(kThreads) delta4_kernel(const DeltaArgs a) {
     if (ok && j0 < n_w) {
       int col = s_base[warp] + incl - ls;  // column before this lane's first entry
       decode_word<XS>(w0, s_vals[j0], col, a.x, xs, acc0, acc1);
-      if (j0 + 1 < n_w) decode_word<XS>(w1, s_vals[j0 + 1], col, a.x, xs, acc0, acc1);
+      if (two && j0 + 1 < n_w) decode_word<XS>(w1, s_vals[j0 + 1], col, a.x, xs, acc0, acc1);
     }
     const bool last = (rw & kUnitLast) != 0;
     if (last || u_begin + i == u_end - 1) {  // row ends, or this CTA's share does
