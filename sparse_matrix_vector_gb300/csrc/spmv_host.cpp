@@ -585,11 +585,8 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
                 kDeltaStages * delta_stage_bytes();
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
+  const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
-#ifdef SPMV_DELTA_MAX_CTAS_PER_SM
-  occ = std::min(occ, SPMV_DELTA_MAX_CTAS_PER_SM);
-#endif
   DeltaTables t;
   if ((s = plan_delta_units(d, occ * p->sm_count, &t, &info)) != SPMV_OK) return s;
   p->grid = info.grid;
