@@ -160,6 +160,16 @@ def test_delta4_x_paths(x_smem):
     assert_parity(m, y, TOL16)
 
 
+def test_delta4_mixed_rows_deterministic():
+    lengths = np.tile([0, 1, 0, 3, 9, 0, 257, 0, 5000, 2, 20000, 0, 700, 64, 65], 30)
+    m = workloads.from_lengths("mixed16", lengths, 30000, seed=17, dtype=np.float16)
+    ys, info = run_gpu(m, "delta4", repeat=3)
+    assert info["n_split_rows"] > 0
+    for y in ys[1:]:
+        assert np.array_equal(y, ys[0])
+    assert_parity(m, ys[0], TOL16)
+
+
 # ------------------------------------------------------------ edge cases
 
 def make(name, rp, ci, vals, n_cols, x):
