@@ -350,8 +350,10 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
     out->cta_first.push_back(0);
     for (int32_t r = 0; r < d->n_rows; ++r) {
       const int64_t w0 = rp[r] >> 3, w1 = rp[r + 1] >> 3, nw = w1 - w0;
-      const bool half = nw <= kDeltaUnitWords / 2;
-      const int64_t warp_words = half ? kDeltaWarpWords / 2 : kDeltaWarpWords;
+      // words per lane: the least that fits the row in one unit, else the most
+      uint32_t lg = 0;
+      while ((1 << lg) < kDeltaMaxLaneWords && nw > (int64_t)kDeltaThreads << lg) ++lg;
+      const int64_t warp_words = (int64_t)32 << lg;
       const int64_t n_u = std::max<int64_t>(1, (nw + kDeltaUnitWords - 1) / kDeltaUnitWords);
       const int64_t per = n_u > 1 ? (nw + n_u - 1) / n_u : std::max<int64_t>(nw, 1);
       if (n_u > 1) {
@@ -373,7 +375,7 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
         }
         // starting column of each warp's words of the unit (warp 0's is the
         // unit's own starting column)
-        for (int wi = 0; wi < kWarps; ++wi) {
+        for (int wi = 0; wi < kDeltaWarps; ++wi) {
           const int64_t seg = std::min(ub + (int64_t)wi * warp_words, ue);
           for (; w < seg; ++w) {
             const uint32_t word = d->words[w];
@@ -383,9 +385,9 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
           out->warp_base.push_back((int32_t)col);
         }
         const uint32_t flags = (k == 0 ? kUnitFirst : 0u) | (k == n_u - 1 ? kUnitLast : 0u) |
-                               (half ? kUnitHalf : 0u);
+                               (lg << kUnitLgShift);
         out->units.push_back({(int32_t)((uint32_t)r | flags), (int32_t)ub, (int32_t)ue,
-                              out->warp_base[out->warp_base.size() - kWarps]});
+                              out->warp_base[out->warp_base.size() - kDeltaWarps]});
         cum += (ue - ub) * 8 + (k == 0 ? 8 : 0);
       }
     }
@@ -585,8 +587,11 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
                 kDeltaStages * delta_stage_bytes();
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
+  // as for CSR: leave L1 (which caches the x gathers) a share of the SM's
+  // unified memory
+  int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
+  occ = std::min<int>(occ, std::max<int>(1, (int)(kCsrSmemBudget / (p->dyn_smem + 1024))));
   DeltaTables t;
   if ((s = plan_delta_units(d, occ * p->sm_count, &t, &info)) != SPMV_OK) return s;
   p->grid = info.grid;
@@ -610,7 +615,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
-  info.block = kThreads;
+  info.block = kDeltaThreads;
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = d->n_entries * 2 + d->n_entries / 2 +
                       ((int64_t)d->n_rows + 1) * 4;
@@ -733,7 +738,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   info->nnz = m->nnz;
   info->format = format;
   info->value_dtype = m->value_dtype;
-  info->block = kThreads;
+  info->block = delta ? kDeltaThreads : kThreads;
   if (delta) {
     if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
     spmv_delta d;
@@ -743,7 +748,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
       return SPMV_ERR_TOO_LARGE;
     }
     DeltaTables t;
-    s = plan_delta_units(&d, 5 * kAssumedSms, &t, info);
+    s = plan_delta_units(&d, 8 * kAssumedSms, &t, info);
     info->n_entries = d.n_entries;
     info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * 2 <=
                       (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);

@@ -38,24 +38,33 @@ constexpr int kStreamTileCap = (kTileCap < kThreads * 8 ? kTileCap : kThreads * 
 constexpr int kTileRowsCap = 512;        // rows of a short-row tile
 constexpr int kStages = SPMV_STAGES;
 // DELTA4 kernel: a work unit is a slice of one row of at most
-// kDeltaUnitWords packed words (8 entries each), 2 words per thread, so warp
-// w decodes the unit's words [64w, 64w + 64).
-constexpr int kDeltaLaneWords = 2;
-constexpr int kDeltaWarpWords = 32 * kDeltaLaneWords;
-constexpr int kDeltaUnitWords = kDeltaWarpWords * kWarps;
+// kDeltaUnitWords packed words (8 entries each), decoded by a CTA of
+// kDeltaThreads threads, LW = 1, 2, ... kDeltaMaxLaneWords consecutive words
+// per thread (the least LW that fits the row in one unit, else the most), so
+// warp w decodes the unit's words [32 LW w, 32 LW (w + 1)).
+#ifndef SPMV_DELTA_THREADS
+#define SPMV_DELTA_THREADS 256
+#endif
+constexpr int kDeltaThreads = SPMV_DELTA_THREADS;
+constexpr int kDeltaWarps = kDeltaThreads / 32;
+#ifndef SPMV_DELTA_UNIT_WORDS
+#define SPMV_DELTA_UNIT_WORDS 512
+#endif
+constexpr int kDeltaUnitWords = SPMV_DELTA_UNIT_WORDS;
+constexpr int kDeltaMaxLaneWords = kDeltaUnitWords / kDeltaThreads;
+static_assert(kDeltaMaxLaneWords == 1 || kDeltaMaxLaneWords == 2 || kDeltaMaxLaneWords == 4,
+              "words per lane must be 1, 2 or 4");
 #ifndef SPMV_DELTA_STAGES
 #define SPMV_DELTA_STAGES 2
 #endif
 constexpr int kDeltaStages = SPMV_DELTA_STAGES;
-// DELTA4 unit descriptor: {row | FIRST | LAST, word_begin, word_end, column
-// before the unit's first entry}; FIRST / LAST: first / last unit of the row.
+// DELTA4 unit descriptor: {row | FIRST | LAST | log2(LW) << kUnitLgShift,
+// word_begin, word_end, column before the unit's first entry}; FIRST / LAST:
+// first / last unit of the row.
 constexpr uint32_t kUnitFirst = 1u << 31;
 constexpr uint32_t kUnitLast = 1u << 30;
-// HALF: one word per lane (warp w decodes words [32w, 32w + 32)), for rows
-// of at most kDeltaUnitWords / 2 words, which would leave most warps idle
-// at two words per lane.
-constexpr uint32_t kUnitHalf = 1u << 29;
-constexpr uint32_t kUnitRowMask = (1u << 29) - 1u;
+constexpr uint32_t kUnitLgShift = 28;
+constexpr uint32_t kUnitRowMask = (1u << 28) - 1u;
 
 // Tile descriptor (one int4 per work unit of the CSR kernel).
 //   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | WALK? | lg << 16 | rows}

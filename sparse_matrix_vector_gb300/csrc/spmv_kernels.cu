@@ -69,6 +69,21 @@ __device__ __forceinline__ float cta_sum(float v, float* s_red) {
   return t;
 }
 
+// Sum over a block of NW warps; the result is valid in thread 0. Fixed order.
+template <int NW>
+__device__ __forceinline__ float block_sum(float v, float* s_red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (warp == 0) {
+    t = lane < NW ? s_red[lane] : 0.f;
+    t = warp_sum(t);
+  }
+  return t;
+}
+
 // Copy x (n elements) into shared memory, 16 bytes at a time when aligned.
 template <typename XT>
 __device__ __forceinline__ void stage_x(XT* xs, const XT* x, int n) {
@@ -628,7 +643,7 @@ struct DeltaArgs {
   const __half* __restrict__ x;
   float* __restrict__ y;
   const int4* __restrict__ units;       // {row | FIRST | LAST, wb, we, column base}
-  const int32_t* __restrict__ warp_base;  // kWarps starting columns per unit
+  const int32_t* __restrict__ warp_base;  // kDeltaWarps starting columns per unit
   const int32_t* __restrict__ cta_first;
   const int32_t* __restrict__ row_split;
   const SplitInfo* __restrict__ splits;  // {first_slot, n_units, row word, words/unit}
@@ -641,7 +656,7 @@ struct DeltaArgs {
 // Shared-memory stage of one DELTA4 unit: the warps' starting columns, the
 // unit's words (aligned out to 4 words) and its values (16 bytes per word).
 struct DeltaStage {
-  static constexpr int kBaseBytes = kWarps * 4;
+  static constexpr int kBaseBytes = kDeltaWarps * 4;
   static constexpr int kWordBytes = (kDeltaUnitWords + 8) * 4;
   static constexpr int kValBytes = kDeltaUnitWords * 16;
   static constexpr int kBytes = kBaseBytes + kWordBytes + kValBytes;
@@ -658,7 +673,7 @@ __device__ __forceinline__ void stage_x_skewed(__half* xs, const __half* x, int 
   const int pairs = n >> 1;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
     const uint4* src = reinterpret_cast<const uint4*>(x);
-    for (int v = threadIdx.x; v < (pairs >> 2); v += kThreads) {
+    for (int v = threadIdx.x; v < (pairs >> 2); v += kDeltaThreads) {
       const uint4 q = __ldg(src + v);
       const int j = 4 * v;  // first pair of the vector; 4 pairs never cross a 32-pair row
       dst[j + (j >> 5)] = q.x;
@@ -666,9 +681,9 @@ __device__ __forceinline__ void stage_x_skewed(__half* xs, const __half* x, int 
       dst[j + 2 + (j >> 5)] = q.z;
       dst[j + 3 + (j >> 5)] = q.w;
     }
-    for (int i = ((pairs >> 2) << 3) + threadIdx.x; i < n; i += kThreads) xs[x_skew(i)] = x[i];
+    for (int i = ((pairs >> 2) << 3) + threadIdx.x; i < n; i += kDeltaThreads) xs[x_skew(i)] = x[i];
   } else {
-    for (int i = threadIdx.x; i < n; i += kThreads) xs[x_skew(i)] = x[i];
+    for (int i = threadIdx.x; i < n; i += kDeltaThreads) xs[x_skew(i)] = x[i];
   }
   __syncthreads();
 }
@@ -730,7 +745,7 @@ __device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* st
     return;
   }
   mbar_arrive_expect_tx(bar, DeltaStage::kBaseBytes + nwb + nvb);
-  bulk_g2s(stage, a.warp_base + (size_t)u * kWarps, DeltaStage::kBaseBytes, bar, pol);
+  bulk_g2s(stage, a.warp_base + (size_t)u * kDeltaWarps, DeltaStage::kBaseBytes, bar, pol);
   bulk_g2s(stage + DeltaStage::kBaseBytes, a.words + wa, nwb, bar, pol);
   bulk_g2s(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes, a.vals + (size_t)wb * 8,
            nvb, bar, pol);
@@ -774,14 +789,15 @@ __device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool 
 // Products are formed in half2 and accumulated in fp32 across the units of a
 // row; the row total is a CTA reduction.
 #ifndef SPMV_DELTA_MIN_BLOCKS
-#define SPMV_DELTA_MIN_BLOCKS 6
+#define SPMV_DELTA_MIN_BLOCKS (kDeltaThreads == 128 ? 8 : 6)
 #endif
 template <bool XS>
-__global__ void __launch_bounds__(kThreads, SPMV_DELTA_MIN_BLOCKS) delta4_kernel(const DeltaArgs a) {
+__global__ void __launch_bounds__(kDeltaThreads, SPMV_DELTA_MIN_BLOCKS)
+    delta4_kernel(const DeltaArgs a) {
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_bar[kDeltaStages];
   __shared__ int4 s_desc[kDeltaStages];
-  __shared__ float s_red[kWarps];
+  __shared__ float s_red[kDeltaWarps];
   __shared__ int s_fail;
   unsigned char* stages = dyn_smem;
   __half* xs = reinterpret_cast<__half*>(dyn_smem + kDeltaStages * DeltaStage::kBytes);
@@ -839,11 +855,15 @@ __global__ void __launch_bounds__(kThreads, SPMV_DELTA_MIN_BLOCKS) delta4_kernel
         reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
     const uint4* s_vals =
         reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
-    const bool two = (rw & kUnitHalf) == 0;  // words per lane: 2, or 1 for a short row
-    const int j0 = two ? kDeltaLaneWords * tid : tid;  // this lane's first word in the unit
-    const uint32_t w0 = (ok && j0 < n_w) ? s_words[j0] : 0u;
-    const uint32_t w1 = (two && ok && j0 + 1 < n_w) ? s_words[j0 + 1] : 0u;
-    const int ls = nibble_sum(w0) + nibble_sum(w1);
+    const int lg = (int)((rw >> kUnitLgShift) & 3u);  // log2(words per lane)
+    const int j0 = tid << lg;  // this lane's first word in the unit
+    uint32_t wd[kDeltaMaxLaneWords];
+    int ls = 0;
+#pragma unroll
+    for (int q = 0; q < kDeltaMaxLaneWords; ++q) {
+      wd[q] = (q < (1 << lg) && ok && j0 + q < n_w) ? s_words[j0 + q] : 0u;
+      ls += nibble_sum(wd[q]);
+    }
     int incl = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -852,12 +872,14 @@ __global__ void __launch_bounds__(kThreads, SPMV_DELTA_MIN_BLOCKS) delta4_kernel
     }
     if (ok && j0 < n_w) {
       int col = s_base[warp] + incl - ls;  // column before this lane's first entry
-      decode_word<XS>(w0, s_vals[j0], col, a.x, xs, acc0, acc1);
-      if (two && j0 + 1 < n_w) decode_word<XS>(w1, s_vals[j0 + 1], col, a.x, xs, acc0, acc1);
+#pragma unroll
+      for (int q = 0; q < kDeltaMaxLaneWords; ++q)
+        if (q < (1 << lg) && j0 + q < n_w)
+          decode_word<XS>(wd[q], s_vals[j0 + q], col, a.x, xs, acc0, acc1);
     }
     const bool last = (rw & kUnitLast) != 0;
     if (last || u_begin + i == u_end - 1) {  // row ends, or this CTA's share does
-      const float part = cta_sum(acc0 + acc1, s_red);
+      const float part = block_sum<kDeltaWarps>(acc0 + acc1, s_red);
       if (tid == 0) delta_publish(a, row, piece_first && last, piece_wb0, wb, part);
       acc0 = acc1 = 0.f;
       piece_wb0 = -1;
@@ -906,10 +928,10 @@ const void* delta_entry(bool xs) {
 // griddepcontrol.wait before touching anything that kernel may write. Every
 // CTA of these grids is resident at once (persistent grids), so CTAs that
 // wait can never keep the kernel they wait on from running.
-int launch_pdl(const void* fn, int grid, size_t smem, void* stream, void** args) {
+int launch_pdl(const void* fn, int grid, int block, size_t smem, void* stream, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3((unsigned)block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
@@ -932,7 +954,7 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem) {
 
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(x_smem), kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(x_smem), kDeltaThreads,
                                                     dyn_smem) != cudaSuccess)
     return -1;
   return n;
@@ -981,7 +1003,7 @@ int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
   a.split_chunk = p.split_chunk;
   a.status = p.status;
   void* args[] = {&a};
-  return launch_pdl(csr_entry(p.dtype, p.x_smem), p.grid, p.dyn_smem, stream, args);
+  return launch_pdl(csr_entry(p.dtype, p.x_smem), p.grid, kThreads, p.dyn_smem, stream, args);
 }
 
 int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
@@ -1001,7 +1023,7 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.status = p.status;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
-  return launch_pdl(delta_entry(p.x_smem), p.grid, p.dyn_smem, stream, args);
+  return launch_pdl(delta_entry(p.x_smem), p.grid, kDeltaThreads, p.dyn_smem, stream, args);
 }
 
 }  // namespace spmv
