@@ -492,10 +492,15 @@ void fill_bytes(spmv_plan_info* info, size_t x_elem) {
                             (int64_t)info->n_rows * 4;
 }
 
-// Shared memory the CSR kernel's CTAs may take per SM (of 256 KB unified
-// with L1). Measured: fp32 stages at 6 CTAs per SM (223 KB) ran 10-25%
-// slower than at 5 (187 KB) on the Laplacian, FEM and power-law matrices.
-constexpr size_t kCsrSmemBudget = 192 * 1024;
+// Shared memory the kernels' CTAs may hold per SM (dynamic + static + the
+// runtime's per-CTA reservation) of the 256 KB that L1 and shared memory
+// share. The carve-out is chosen in steps (..., 164, 196, 228 KB); above
+// 196 KB, L1 is left with 28 KB, too few lines to keep the x gathers' misses
+// in flight: random gathers from an L2-resident vector then run at half
+// their rate (measured 0.46 against 0.94 per clock per SM), and fp32 CSR at
+// 6 CTAs per SM ran 10-25% slower than at 5 on the Laplacian, FEM and
+// power-law matrices.
+constexpr size_t kSmemBudget = 196 * 1024;
 
 spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
   CsrTables t;
@@ -510,12 +515,10 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
                 kStages * csr_stage_bytes(m->value_dtype);
   p->split_chunk = o.split_chunk;
   if (set_kernel_smem_limits(p->dyn_smem, 0) != 0) return SPMV_ERR_CUDA;
-  // persistent grid: at most every CTA that fits on the device at once, and
-  // no more per SM than leave the L1 part of the unified data cache (which
-  // keeps the x gathers close) a third of its size
-  int occ = csr_kernel_occupancy(m->value_dtype, p->x_smem, p->dyn_smem);
+  // persistent grid: every CTA that fits on the device at once within the
+  // shared-memory budget (so that L1 keeps at least 60 KB for the x gathers)
+  const int occ = csr_kernel_occupancy(m->value_dtype, p->x_smem, p->dyn_smem, kSmemBudget);
   if (occ <= 0) return SPMV_ERR_CUDA;
-  occ = std::min<int>(occ, std::max<int>(1, (int)(kCsrSmemBudget / (p->dyn_smem + 1024))));
   s = plan_csr_tiles(m->n_rows, m->row_ptr, o, occ * p->sm_count, &t, &info);
   if (s != SPMV_OK) return s;
   p->n_tiles = (int64_t)t.tiles.size();
@@ -587,11 +590,9 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
                 kDeltaStages * delta_stage_bytes();
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  // as for CSR: leave L1 (which caches the x gathers) a share of the SM's
-  // unified memory
-  int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem);
+  // as for CSR: within the shared-memory budget that leaves L1 its share
+  const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem, kSmemBudget);
   if (occ <= 0) return SPMV_ERR_CUDA;
-  occ = std::min<int>(occ, std::max<int>(1, (int)(kCsrSmemBudget / (p->dyn_smem + 1024))));
   DeltaTables t;
   if ((s = plan_delta_units(d, occ * p->sm_count, &t, &info)) != SPMV_OK) return s;
   p->grid = info.grid;

@@ -178,8 +178,8 @@ struct Plan {
 };
 
 // Kernel-side entry points (spmv_kernels.cu).
-int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem);
-int delta_kernel_occupancy(bool x_smem, size_t dyn_smem);
+int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t budget);
+int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget);
 int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn);
 size_t csr_stage_bytes(spmv_dtype dtype);
 size_t delta_stage_bytes();

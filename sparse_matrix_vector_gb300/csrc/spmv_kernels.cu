@@ -944,20 +944,29 @@ int launch_pdl(const void* fn, int grid, int block, size_t smem, void* stream, v
 
 }  // namespace
 
-int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem) {
+// CTAs per SM that fit, and at most as many as keep the shared memory they
+// hold (dynamic + static + the per-CTA reservation) within `budget` bytes.
+int occupancy_within(const void* fn, int block, size_t dyn_smem, size_t budget) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, csr_entry(dtype, x_smem),
-                                                    kThreads, dyn_smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, dyn_smem) != cudaSuccess)
     return -1;
-  return n;
+  cudaFuncAttributes fa;
+  int reserved = 0, dev = 0;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+          cudaSuccess)
+    return -1;
+  const size_t per_cta = dyn_smem + fa.sharedSizeBytes + (size_t)reserved;
+  const int cap = (int)(budget / per_cta);
+  return n < cap ? n : (cap > 0 ? cap : 1);
 }
 
-int delta_kernel_occupancy(bool x_smem, size_t dyn_smem) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(x_smem), kDeltaThreads,
-                                                    dyn_smem) != cudaSuccess)
-    return -1;
-  return n;
+int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t budget) {
+  return occupancy_within(csr_entry(dtype, x_smem), kThreads, dyn_smem, budget);
+}
+
+int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget) {
+  return occupancy_within(delta_entry(x_smem), kDeltaThreads, dyn_smem, budget);
 }
 
 size_t delta_stage_bytes() { return (size_t)DeltaStage::kBytes; }
