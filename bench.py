@@ -148,6 +148,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms: float, device, pg) -> float:
+    """The slowest rank's timed-region length (ms); every rank gets it."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX, group=pg)
+    torch.distributed.barrier(group=pg)
+    return float(t.item())
+
+
+def job_throughput(nbytes: int, world: int, ms: float, steps: int):
+    """Seconds per step, whole-job GB/s (every rank ran `steps` runs of
+    `nbytes` in `ms`) and one launch's GB/s."""
+    sec_per_step = ms / 1e3 / steps
+    return sec_per_step, world * nbytes / sec_per_step / 1e9, nbytes / sec_per_step / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -319,16 +337,9 @@ def bench_one(args, name, world, rank, local, pg):
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev, pg)
     torch.cuda.synchronize(dev)
-    sec_per_step = ms / 1e3 / steps
-    value = world * nbytes / sec_per_step / 1e9
-    per_launch = nbytes / sec_per_step / 1e9
+    sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
     gflops = world * 2 * m.nnz / sec_per_step / 1e9
 
     # end to end through the C ABI with pinned host buffers
