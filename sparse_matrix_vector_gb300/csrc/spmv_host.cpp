@@ -588,7 +588,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
             : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
-                kDeltaStages * delta_stage_bytes();
+                delta_stages_bytes(p->x_smem);
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
   // as for CSR: within the shared-memory budget that leaves L1 its share
   const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem, kSmemBudget);
@@ -616,7 +616,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
-  info.block = kDeltaThreads;
+  info.block = delta_use_pc(p->x_smem) ? kDeltaThreads + 32 : kDeltaThreads;
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = d->n_entries * 2 + d->n_entries / 2 +
                       ((int64_t)d->n_rows + 1) * 4;

@@ -726,6 +726,39 @@ __device__ __forceinline__ void decode_word(uint32_t w, const uint4 v, int& col,
   }
 }
 
+// fp32 acc + a * x for fp16 a and x: the product is exact in fp32, so one
+// fp32 rounding (mixed-precision fma).
+__device__ __forceinline__ float fma_f16(float acc, uint16_t a, uint16_t x) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(x));
+  return acc;
+}
+
+// Decode one word (8 entries) whose first entry follows column `col`, with x
+// read through L1. The eight columns come from byte-wise prefix sums of the
+// nibbles: with lo / hi the even / odd nibbles spread into bytes, byte j of
+// P = (lo + hi) * 0x01010101 is the sum of nibbles 0..2j+1 (at most 120, so
+// no carries), and byte j of P - hi the sum of nibbles 0..2j; each column is
+// one byte extract and one address, and each entry one mixed fma.
+__device__ __forceinline__ void decode_word_l1(uint32_t w, const uint4 v, int& col,
+                                               const __half* xg, float& acc0, float& acc1) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t P = (lo + hi) * 0x01010101u;
+  const uint32_t Q = P - hi;
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(xg) + col;
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t c0 = __byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
+    const uint32_t c1 = __byte_perm(P, 0u, 0x4440u + (uint32_t)j);
+    const uint16_t x0 = __ldg(xb + c0);
+    const uint16_t x1 = __ldg(xb + c1);
+    acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), x0);
+    acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), x1);
+  }
+  col += (int)(P >> 24);
+}
+
 // Thread 0: start the TMA copies of DELTA4 unit u (descriptor d) into a stage.
 __device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* stage,
                                            uint64_t* bar, int4* desc, int u, const int4 d,
@@ -788,6 +821,11 @@ __device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool 
 // the lane's nibble sum put through a 5-step __shfl_up_sync inclusive scan.
 // Products are formed in half2 and accumulated in fp32 across the units of a
 // row; the row total is a CTA reduction.
+// Decode of the x-through-L1 path: 2 byte-prefix columns and mixed fma
+// (decode_word_l1), 1 per-entry columns and half2 products (decode_word).
+#ifndef SPMV_DELTA_DECODE
+#define SPMV_DELTA_DECODE 2
+#endif
 #ifndef SPMV_DELTA_MIN_BLOCKS
 #define SPMV_DELTA_MIN_BLOCKS (kDeltaThreads == 128 ? 8 : 6)
 #endif
@@ -874,8 +912,12 @@ __global__ void __launch_bounds__(kDeltaThreads, SPMV_DELTA_MIN_BLOCKS)
       int col = s_base[warp] + incl - ls;  // column before this lane's first entry
 #pragma unroll
       for (int q = 0; q < kDeltaMaxLaneWords; ++q)
-        if (q < (1 << lg) && j0 + q < n_w)
-          decode_word<XS>(wd[q], s_vals[j0 + q], col, a.x, xs, acc0, acc1);
+        if (q < (1 << lg) && j0 + q < n_w) {
+          if (XS || SPMV_DELTA_DECODE == 1)
+            decode_word<XS>(wd[q], s_vals[j0 + q], col, a.x, xs, acc0, acc1);
+          else
+            decode_word_l1(wd[q], s_vals[j0 + q], col, a.x, acc0, acc1);
+        }
     }
     const bool last = (rw & kUnitLast) != 0;
     if (last || u_begin + i == u_end - 1) {  // row ends, or this CTA's share does
@@ -899,6 +941,154 @@ __global__ void __launch_bounds__(kDeltaThreads, SPMV_DELTA_MIN_BLOCKS)
     for (int s = 0; s < kDeltaStages; ++s) {
       const int fills = 1 + (i > s ? (i - 1 - s) / kDeltaStages + 1 : 0);
       mbar_wait_bounded(&s_bar[s], (uint32_t)(fills - 1) & 1u);
+    }
+  }
+}
+
+// ------------------------------------- DELTA4, producer / consumer variant
+// One producer warp issues the TMA copies; the kDeltaWarps consumer warps
+// decode. A stage is handed back by each consumer warp arriving on the
+// stage's "empty" mbarrier once it has read it, so consumer warps never wait
+// for one another per unit (no CTA barrier in the loop): a warp that is done
+// with a unit moves on to the next staged one. A row's total is formed when
+// its last unit ends: each warp parks its shuffle-reduced sum in a slot, and
+// the warp whose shared-memory atomicAdd completes the slot's count adds the
+// kDeltaWarps sums in warp order (deterministic) and publishes the row.
+#ifndef SPMV_DELTA_PC_STAGES
+#define SPMV_DELTA_PC_STAGES 3
+#endif
+#ifndef SPMV_DELTA_PC_MIN_BLOCKS
+#define SPMV_DELTA_PC_MIN_BLOCKS 5
+#endif
+constexpr int kPcStages = SPMV_DELTA_PC_STAGES;
+// row sums in flight: warps are less than kPcStages units apart
+constexpr int kPcSlots = kPcStages + 2;
+constexpr int kPcThreads = kDeltaThreads + 32;
+
+__global__ void __launch_bounds__(kPcThreads, SPMV_DELTA_PC_MIN_BLOCKS)
+    delta4_pc_kernel(const DeltaArgs a) {
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  __shared__ __align__(8) uint64_t s_full[kPcStages];
+  __shared__ __align__(8) uint64_t s_empty[kPcStages];
+  __shared__ int4 s_desc[kPcStages];
+  __shared__ float s_part[kPcSlots][kDeltaWarps];
+  __shared__ int s_cnt[kPcSlots];
+  unsigned char* stages = dyn_smem;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u_begin = __ldg(a.cta_first + blockIdx.x);
+  const int n_units = __ldg(a.cta_first + blockIdx.x + 1) - u_begin;
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kPcStages; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kDeltaWarps);
+    }
+#pragma unroll
+    for (int k = 0; k < kPcSlots; ++k) s_cnt[k] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();  // the only CTA-wide barrier
+
+  if (warp == kDeltaWarps) {  // producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n_units; ++i) {
+        const int s = i % kPcStages;
+        if (i >= kPcStages &&
+            !mbar_wait_bounded(&s_empty[s], (uint32_t)(i / kPcStages - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        issue_unit(a, stages + s * DeltaStage::kBytes, &s_full[s], &s_desc[s], u_begin + i,
+                   __ldg(a.units + u_begin + i), pol);
+        issued = i + 1;
+        if (issued == kPcStages) pdl_launch_dependents();
+      }
+      if (issued < kPcStages) pdl_launch_dependents();
+      if (!ok) {
+        atomicExch(a.status, 1);
+        // let copies still in flight land before the CTA's shared memory goes
+        for (int j = (issued > kPcStages ? issued - kPcStages : 0); j < issued; ++j)
+          mbar_wait_bounded(&s_full[j % kPcStages], (uint32_t)(j / kPcStages) & 1u);
+      }
+    }
+    return;
+  }
+
+  // consumers; plan-owned data only above, x and y below
+  pdl_wait();
+  float acc0 = 0.f, acc1 = 0.f;  // this thread's share of the current row piece
+  int piece_wb0 = -1;
+  bool piece_first = false;
+  int slot = 0;
+  for (int i = 0; i < n_units; ++i) {
+    const int s = i % kPcStages;
+    if (!mbar_wait_bounded(&s_full[s], (uint32_t)(i / kPcStages) & 1u)) {
+      if (lane == 0) atomicExch(a.status, 1);
+      break;
+    }
+    const int4 d = s_desc[s];
+    const unsigned char* stage = stages + s * DeltaStage::kBytes;
+    const uint32_t rw = (uint32_t)d.x;
+    const int row = (int)(rw & kUnitRowMask);
+    const int wb = d.y, n_w = d.z - d.y;
+    if (piece_wb0 < 0) {
+      piece_wb0 = wb;
+      piece_first = (rw & kUnitFirst) != 0;
+    }
+    const int* s_base = reinterpret_cast<const int*>(stage);
+    const uint32_t* s_words =
+        reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
+    const uint4* s_vals =
+        reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
+    const int lg = (int)((rw >> kUnitLgShift) & 3u);  // log2(words per lane)
+    const int j0 = tid << lg;  // this lane's first word in the unit
+    uint32_t wd[kDeltaMaxLaneWords];
+    uint4 vd[kDeltaMaxLaneWords];
+    int ls = 0;
+#pragma unroll
+    for (int q = 0; q < kDeltaMaxLaneWords; ++q) {
+      const bool in = q < (1 << lg) && j0 + q < n_w;
+      wd[q] = in ? s_words[j0 + q] : 0u;
+      vd[q] = in ? s_vals[j0 + q] : make_uint4(0, 0, 0, 0);
+      ls += nibble_sum(wd[q]);
+    }
+    const int base = s_base[warp];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[s]);  // this warp is done with the stage
+    int incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    if (j0 < n_w) {
+      int col = base + incl - ls;  // column before this lane's first entry
+#pragma unroll
+      for (int q = 0; q < kDeltaMaxLaneWords; ++q)
+        if (q < (1 << lg) && j0 + q < n_w) decode_word_l1(wd[q], vd[q], col, a.x, acc0, acc1);
+    }
+    const bool last = (rw & kUnitLast) != 0;
+    if (last || i == n_units - 1) {  // row ends, or this CTA's share does
+      const float v = warp_sum(acc0 + acc1);
+      if (lane == 0) {
+        s_part[slot][warp] = v;
+        __threadfence_block();
+        if (atomicAdd(&s_cnt[slot], 1) == kDeltaWarps - 1) {
+          __threadfence_block();
+          const volatile float* sp = s_part[slot];
+          float t = 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < kDeltaWarps; ++w2) t += sp[w2];
+          s_cnt[slot] = 0;
+          delta_publish(a, row, piece_first && last, piece_wb0, wb, t);
+        }
+      }
+      slot = slot + 1 == kPcSlots ? 0 : slot + 1;
+      acc0 = acc1 = 0.f;
+      piece_wb0 = -1;
     }
   }
 }
@@ -966,7 +1156,14 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t 
 }
 
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget) {
+  if (delta_use_pc(x_smem))
+    return occupancy_within(reinterpret_cast<const void*>(&delta4_pc_kernel), kPcThreads,
+                            dyn_smem, budget);
   return occupancy_within(delta_entry(x_smem), kDeltaThreads, dyn_smem, budget);
+}
+
+size_t delta_stages_bytes(bool x_smem) {
+  return (size_t)(delta_use_pc(x_smem) ? kPcStages : kDeltaStages) * DeltaStage::kBytes;
 }
 
 size_t delta_stage_bytes() { return (size_t)DeltaStage::kBytes; }
@@ -988,8 +1185,11 @@ int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn) {
                                (int)csr_dyn) != cudaSuccess)
         return -1;
   if (delta_dyn > 0 &&
-      cudaFuncSetAttribute(delta_entry(true), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)delta_dyn) != cudaSuccess)
+      (cudaFuncSetAttribute(delta_entry(true), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            (int)delta_dyn) != cudaSuccess ||
+       cudaFuncSetAttribute(reinterpret_cast<const void*>(&delta4_pc_kernel),
+                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            (int)delta_dyn) != cudaSuccess))
     return -1;
   return 0;
 }
@@ -1032,6 +1232,9 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.status = p.status;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
+  if (delta_use_pc(p.x_smem))
+    return launch_pdl(reinterpret_cast<const void*>(&delta4_pc_kernel), p.grid, kPcThreads,
+                      p.dyn_smem, stream, args);
   return launch_pdl(delta_entry(p.x_smem), p.grid, kDeltaThreads, p.dyn_smem, stream, args);
 }
 
