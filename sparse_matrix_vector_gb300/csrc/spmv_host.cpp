@@ -31,10 +31,16 @@ namespace {
 // Device indexing is 32-bit; keep clear of INT32_MAX so that padded spans
 // (up to one vector past the end) never overflow.
 constexpr int64_t kMaxIndex = (int64_t)INT32_MAX - 4096;
-// x is gathered through L1 by default: staging it in shared memory costs a
-// copy per CTA and, for the LLM shapes, a third of the CTAs per SM, and was
-// measured slower on GB300 than L1-resident gathers.
+// CSR: x is gathered through L1 by default: staging it in shared memory
+// costs a copy per CTA and, for the LLM shapes, a third of the CTAs per SM,
+// and was measured slower on GB300 than L1-resident gathers.
 constexpr size_t kXsAutoBytes = 0;
+// DELTA4: the producer / consumer kernel shares one shared-memory copy of x
+// among three groups of warps; up to 32 KB of x (16,384 columns) two such
+// CTAs still fit an SM, and gathers from shared memory beat L1 there
+// (12288-column LLM matrices, 30/50/70/90%: 0.47/0.44/0.40/0.27 of HBM peak
+// through L1, 0.47/0.46/0.48/0.30 from shared memory).
+constexpr size_t kXsAutoBytesDelta = 32 * 1024;
 constexpr size_t kXsMaxBytes = 160 * 1024;   // hard limit when forced
 constexpr int kPadElems = 16;                // zero tail after device arrays
 constexpr int kAssumedSms = 152;             // for host-only inspection
@@ -586,16 +592,22 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if ((s = bind_device(p)) != SPMV_OK) return s;
   const size_t xbytes = (size_t)d->n_cols * 2;
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
-            : o.x_smem == -1 ? xbytes <= kXsAutoBytes : false;
+            : o.x_smem == -1 ? xbytes <= kXsAutoBytesDelta : false;
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
                 delta_stages_bytes(p->x_smem);
   if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
   // as for CSR: within the shared-memory budget that leaves L1 its share
   const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem, kSmemBudget);
   if (occ <= 0) return SPMV_ERR_CUDA;
+  // a CTA may run several blocks of units (groups); the plan deals units to
+  // groups, the grid has one CTA per `groups` of them
+  const int groups = delta_groups(p->x_smem);
   DeltaTables t;
-  if ((s = plan_delta_units(d, occ * p->sm_count, &t, &info)) != SPMV_OK) return s;
-  p->grid = info.grid;
+  if ((s = plan_delta_units(d, occ * p->sm_count * groups, &t, &info)) != SPMV_OK) return s;
+  p->grid = (info.grid + groups - 1) / groups;
+  while ((int64_t)t.cta_first.size() < (int64_t)p->grid * groups + 1)
+    t.cta_first.push_back((int32_t)t.units.size());
+  info.grid = p->grid;
   p->n_tiles = (int64_t)t.units.size();
   const size_t e_alloc = (size_t)d->n_entries + 8 * kPadElems;
   if ((s = dev_upload(&p->values, d->values, (size_t)d->n_entries * 2,
@@ -616,7 +628,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
-  info.block = delta_use_pc(p->x_smem) ? kDeltaThreads + 32 : kDeltaThreads;
+  info.block = delta_block(p->x_smem);
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = d->n_entries * 2 + d->n_entries / 2 +
                       ((int64_t)d->n_rows + 1) * 4;
@@ -748,11 +760,15 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
       spmv_delta_free(&d);
       return SPMV_ERR_TOO_LARGE;
     }
+    const bool xs = o.x_smem != 0 && (size_t)m->n_cols * 2 <=
+                    (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytesDelta);
+    const int groups = delta_groups(xs);
     DeltaTables t;
-    s = plan_delta_units(&d, 8 * kAssumedSms, &t, info);
+    s = plan_delta_units(&d, (xs ? 2 : 5) * kAssumedSms * groups, &t, info);
+    info->grid = (info->grid + groups - 1) / groups;
+    info->block = delta_block(xs);
     info->n_entries = d.n_entries;
-    info->x_in_smem = o.x_smem != 0 && (size_t)m->n_cols * 2 <=
-                      (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytes);
+    info->x_in_smem = xs ? 1 : 0;
     info->launches_per_run = m->n_rows > 0;
     info->matrix_bytes = d.n_entries * 2 + d.n_entries / 2 + ((int64_t)m->n_rows + 1) * 4;
     fill_bytes(info, 2);

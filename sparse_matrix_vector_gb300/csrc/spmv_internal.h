@@ -180,12 +180,15 @@ struct Plan {
 // Kernel-side entry points (spmv_kernels.cu).
 int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t budget);
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget);
-// DELTA4 with x through L1 runs the producer / consumer kernel.
+// DELTA4 runs the producer / consumer kernel (the CTA-barrier kernel stays
+// for comparison builds).
 #ifndef SPMV_DELTA_PC
 #define SPMV_DELTA_PC 1
 #endif
-inline bool delta_use_pc(bool x_smem) { return SPMV_DELTA_PC && !x_smem; }
+inline bool delta_use_pc(bool) { return SPMV_DELTA_PC != 0; }
 size_t delta_stages_bytes(bool x_smem);
+int delta_groups(bool x_smem);  // unit blocks ("virtual CTAs") per CTA
+int delta_block(bool x_smem);   // threads per CTA
 int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn);
 size_t csr_stage_bytes(spmv_dtype dtype);
 size_t delta_stage_bytes();

@@ -666,26 +666,34 @@ static_assert(DeltaStage::kBaseBytes % 16 == 0, "stage regions must stay 16-byte
 // x in shared memory, skewed by one 4-byte word per 128 bytes: lanes that
 // gather at a 64-byte stride (16 entries per lane at 50% density) then hit
 // distinct banks. Half i lives at i + 2 * (i / 64).
-__device__ __forceinline__ int x_skew(int i) { return i + 2 * (i >> 6); }
+// Skewed copy of x (half i at i + 2 * (i / 64)) for the CTA-barrier kernel,
+// whose lanes gather 64 bytes apart at 50% density; the producer / consumer
+// kernel measured best on the plain copy (SPMV_X_SKEW 0 there).
+#ifndef SPMV_X_SKEW
+#define SPMV_X_SKEW 0
+#endif
+__device__ __forceinline__ int x_skew(int i) { return SPMV_X_SKEW ? i + 2 * (i >> 6) : i; }
 
-__device__ __forceinline__ void stage_x_skewed(__half* xs, const __half* x, int n) {
+__device__ __forceinline__ void stage_x_skewed(__half* xs, const __half* x, int n,
+                                               bool sync = true, int nthreads = kDeltaThreads) {
   uint32_t* dst = reinterpret_cast<uint32_t*>(xs);
   const int pairs = n >> 1;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
     const uint4* src = reinterpret_cast<const uint4*>(x);
-    for (int v = threadIdx.x; v < (pairs >> 2); v += kDeltaThreads) {
+    for (int v = threadIdx.x; v < (pairs >> 2); v += nthreads) {
       const uint4 q = __ldg(src + v);
       const int j = 4 * v;  // first pair of the vector; 4 pairs never cross a 32-pair row
-      dst[j + (j >> 5)] = q.x;
-      dst[j + 1 + (j >> 5)] = q.y;
-      dst[j + 2 + (j >> 5)] = q.z;
-      dst[j + 3 + (j >> 5)] = q.w;
+      const int o = SPMV_X_SKEW ? j + (j >> 5) : j;
+      dst[o] = q.x;
+      dst[o + 1] = q.y;
+      dst[o + 2] = q.z;
+      dst[o + 3] = q.w;
     }
-    for (int i = ((pairs >> 2) << 3) + threadIdx.x; i < n; i += kDeltaThreads) xs[x_skew(i)] = x[i];
+    for (int i = ((pairs >> 2) << 3) + threadIdx.x; i < n; i += nthreads) xs[x_skew(i)] = x[i];
   } else {
-    for (int i = threadIdx.x; i < n; i += kDeltaThreads) xs[x_skew(i)] = x[i];
+    for (int i = threadIdx.x; i < n; i += nthreads) xs[x_skew(i)] = x[i];
   }
-  __syncthreads();
+  if (sync) __syncthreads();
 }
 
 // Sum of the eight 4-bit fields of w (<= 120).
@@ -755,6 +763,25 @@ __device__ __forceinline__ void decode_word_l1(uint32_t w, const uint4 v, int& c
     const uint16_t x1 = __ldg(xb + c1);
     acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), x0);
     acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), x1);
+  }
+  col += (int)(P >> 24);
+}
+
+// decode_word_l1 with x from the skewed shared-memory copy.
+__device__ __forceinline__ void decode_word_smem(uint32_t w, const uint4 v, int& col,
+                                                 const uint16_t* xs, float& acc0,
+                                                 float& acc1) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t P = (lo + hi) * 0x01010101u;
+  const uint32_t Q = P - hi;
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c0 = col + (int)__byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
+    const int c1 = col + (int)__byte_perm(P, 0u, 0x4440u + (uint32_t)j);
+    acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), xs[x_skew(c0)]);
+    acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), xs[x_skew(c1)]);
   }
   col += (int)(P >> 24);
 }
@@ -946,72 +973,88 @@ __global__ void __launch_bounds__(kDeltaThreads, SPMV_DELTA_MIN_BLOCKS)
 }
 
 // ------------------------------------- DELTA4, producer / consumer variant
-// One producer warp issues the TMA copies; the kDeltaWarps consumer warps
-// decode. A stage is handed back by each consumer warp arriving on the
-// stage's "empty" mbarrier once it has read it, so consumer warps never wait
-// for one another per unit (no CTA barrier in the loop): a warp that is done
-// with a unit moves on to the next staged one. A row's total is formed when
-// its last unit ends: each warp parks its shuffle-reduced sum in a slot, and
-// the warp whose shared-memory atomicAdd completes the slot's count adds the
-// kDeltaWarps sums in warp order (deterministic) and publishes the row.
+// One producer lane per group issues the TMA copies; each group's
+// kDeltaWarps consumer warps decode its units. A stage is handed back by
+// each consumer warp arriving on the stage's "empty" mbarrier once it has
+// read it, so consumer warps never wait for one another per unit (no CTA
+// barrier in the loop): a warp that is done with a unit moves on to the next
+// staged one. A row's total is formed when its last unit ends: each warp
+// parks its shuffle-reduced sum in a slot, and the warp whose shared-memory
+// atomicAdd completes the slot's count adds the kDeltaWarps sums in warp
+// order (deterministic) and publishes the row.
+// A CTA holds G groups, each with its own block of units (a "virtual CTA"
+// of the plan: v = blockIdx.x * G + g), stage ring and slots; with x in
+// shared memory the groups share one copy of it.
 #ifndef SPMV_DELTA_PC_STAGES
 #define SPMV_DELTA_PC_STAGES 3
 #endif
-#ifndef SPMV_DELTA_PC_MIN_BLOCKS
-#define SPMV_DELTA_PC_MIN_BLOCKS 5
+#ifndef SPMV_DELTA_PC_XS_STAGES
+#define SPMV_DELTA_PC_XS_STAGES 2
 #endif
-constexpr int kPcStages = SPMV_DELTA_PC_STAGES;
-// row sums in flight: warps are less than kPcStages units apart
-constexpr int kPcSlots = kPcStages + 2;
-constexpr int kPcThreads = kDeltaThreads + 32;
+#ifndef SPMV_DELTA_PC_XS_GROUPS
+#define SPMV_DELTA_PC_XS_GROUPS 3
+#endif
+template <bool XS>
+struct PcCfg {
+  static constexpr int kGroups = XS ? SPMV_DELTA_PC_XS_GROUPS : 1;
+  static constexpr int kStages = XS ? SPMV_DELTA_PC_XS_STAGES : SPMV_DELTA_PC_STAGES;
+  // row sums in flight: a group's warps are less than kStages units apart
+  static constexpr int kSlots = kStages + 2;
+  static constexpr int kThreads = kGroups * kDeltaThreads + 32;
+  static constexpr int kMinBlocks = XS ? 2 : 5;
+};
 
-__global__ void __launch_bounds__(kPcThreads, SPMV_DELTA_PC_MIN_BLOCKS)
+template <bool XS>
+__global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
     delta4_pc_kernel(const DeltaArgs a) {
+  using C = PcCfg<XS>;
+  constexpr int G = C::kGroups, S = C::kStages;
   extern __shared__ __align__(128) unsigned char dyn_smem[];
-  __shared__ __align__(8) uint64_t s_full[kPcStages];
-  __shared__ __align__(8) uint64_t s_empty[kPcStages];
-  __shared__ int4 s_desc[kPcStages];
-  __shared__ float s_part[kPcSlots][kDeltaWarps];
-  __shared__ int s_cnt[kPcSlots];
-  unsigned char* stages = dyn_smem;
+  __shared__ __align__(8) uint64_t s_full[G][S];
+  __shared__ __align__(8) uint64_t s_empty[G][S];
+  __shared__ int4 s_desc[G][S];
+  __shared__ float s_part[G][C::kSlots][kDeltaWarps];
+  __shared__ int s_cnt[G][C::kSlots];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int u_begin = __ldg(a.cta_first + blockIdx.x);
-  const int n_units = __ldg(a.cta_first + blockIdx.x + 1) - u_begin;
   if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < kPcStages; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], kDeltaWarps);
+    for (int g = 0; g < G; ++g) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(&s_full[g][s], 1);
+        mbar_init(&s_empty[g][s], kDeltaWarps);
+      }
+      for (int k = 0; k < C::kSlots; ++k) s_cnt[g][k] = 0;
     }
-#pragma unroll
-    for (int k = 0; k < kPcSlots; ++k) s_cnt[k] = 0;
     fence_mbar_init();
   }
   __syncthreads();  // the only CTA-wide barrier
 
-  if (warp == kDeltaWarps) {  // producer
-    if (lane == 0) {
+  if (warp == G * kDeltaWarps) {  // producer warp: lane g feeds group g
+    if (lane < G) {
+      const int g = lane;
+      const int v = blockIdx.x * G + g;
+      const int u_begin = __ldg(a.cta_first + v);
+      const int n_units = __ldg(a.cta_first + v + 1) - u_begin;
+      unsigned char* stages = dyn_smem + (size_t)g * S * DeltaStage::kBytes;
       const uint64_t pol = policy_evict_first();
       int issued = 0;
       bool ok = true;
       for (int i = 0; i < n_units; ++i) {
-        const int s = i % kPcStages;
-        if (i >= kPcStages &&
-            !mbar_wait_bounded(&s_empty[s], (uint32_t)(i / kPcStages - 1) & 1u)) {
+        const int s = i % S;
+        if (i >= S && !mbar_wait_bounded(&s_empty[g][s], (uint32_t)(i / S - 1) & 1u)) {
           ok = false;
           break;
         }
-        issue_unit(a, stages + s * DeltaStage::kBytes, &s_full[s], &s_desc[s], u_begin + i,
-                   __ldg(a.units + u_begin + i), pol);
+        issue_unit(a, stages + s * DeltaStage::kBytes, &s_full[g][s], &s_desc[g][s],
+                   u_begin + i, __ldg(a.units + u_begin + i), pol);
         issued = i + 1;
-        if (issued == kPcStages) pdl_launch_dependents();
+        if (issued == S) pdl_launch_dependents();
       }
-      if (issued < kPcStages) pdl_launch_dependents();
+      if (issued < S) pdl_launch_dependents();
       if (!ok) {
         atomicExch(a.status, 1);
         // let copies still in flight land before the CTA's shared memory goes
-        for (int j = (issued > kPcStages ? issued - kPcStages : 0); j < issued; ++j)
-          mbar_wait_bounded(&s_full[j % kPcStages], (uint32_t)(j / kPcStages) & 1u);
+        for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+          mbar_wait_bounded(&s_full[g][j % S], (uint32_t)(j / S) & 1u);
       }
     }
     return;
@@ -1019,17 +1062,30 @@ __global__ void __launch_bounds__(kPcThreads, SPMV_DELTA_PC_MIN_BLOCKS)
 
   // consumers; plan-owned data only above, x and y below
   pdl_wait();
+  const int g = warp / kDeltaWarps, lw = warp % kDeltaWarps;
+  const int gt = tid - g * kDeltaThreads;  // thread index within the group
+  const uint16_t* xs =
+      reinterpret_cast<const uint16_t*>(dyn_smem + (size_t)G * S * DeltaStage::kBytes);
+  if (XS) {
+    stage_x_skewed(reinterpret_cast<__half*>(dyn_smem + (size_t)G * S * DeltaStage::kBytes),
+                   a.x, a.n_cols, false, G * kDeltaThreads);
+    asm volatile("bar.sync 1, %0;" ::"n"(G * kDeltaThreads) : "memory");  // consumers only
+  }
+  const int v = blockIdx.x * G + g;
+  const int u_begin = __ldg(a.cta_first + v);
+  const int n_units = __ldg(a.cta_first + v + 1) - u_begin;
+  const unsigned char* stages = dyn_smem + (size_t)g * S * DeltaStage::kBytes;
   float acc0 = 0.f, acc1 = 0.f;  // this thread's share of the current row piece
   int piece_wb0 = -1;
   bool piece_first = false;
   int slot = 0;
   for (int i = 0; i < n_units; ++i) {
-    const int s = i % kPcStages;
-    if (!mbar_wait_bounded(&s_full[s], (uint32_t)(i / kPcStages) & 1u)) {
+    const int s = i % S;
+    if (!mbar_wait_bounded(&s_full[g][s], (uint32_t)(i / S) & 1u)) {
       if (lane == 0) atomicExch(a.status, 1);
       break;
     }
-    const int4 d = s_desc[s];
+    const int4 d = s_desc[g][s];
     const unsigned char* stage = stages + s * DeltaStage::kBytes;
     const uint32_t rw = (uint32_t)d.x;
     const int row = (int)(rw & kUnitRowMask);
@@ -1044,7 +1100,7 @@ __global__ void __launch_bounds__(kPcThreads, SPMV_DELTA_PC_MIN_BLOCKS)
     const uint4* s_vals =
         reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
     const int lg = (int)((rw >> kUnitLgShift) & 3u);  // log2(words per lane)
-    const int j0 = tid << lg;  // this lane's first word in the unit
+    const int j0 = gt << lg;  // this lane's first word in the unit
     uint32_t wd[kDeltaMaxLaneWords];
     uint4 vd[kDeltaMaxLaneWords];
     int ls = 0;
@@ -1055,9 +1111,9 @@ __global__ void __launch_bounds__(kPcThreads, SPMV_DELTA_PC_MIN_BLOCKS)
       vd[q] = in ? s_vals[j0 + q] : make_uint4(0, 0, 0, 0);
       ls += nibble_sum(wd[q]);
     }
-    const int base = s_base[warp];
+    const int base = s_base[lw];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s_empty[s]);  // this warp is done with the stage
+    if (lane == 0) mbar_arrive(&s_empty[g][s]);  // this warp is done with the stage
     int incl = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1068,25 +1124,30 @@ __global__ void __launch_bounds__(kPcThreads, SPMV_DELTA_PC_MIN_BLOCKS)
       int col = base + incl - ls;  // column before this lane's first entry
 #pragma unroll
       for (int q = 0; q < kDeltaMaxLaneWords; ++q)
-        if (q < (1 << lg) && j0 + q < n_w) decode_word_l1(wd[q], vd[q], col, a.x, acc0, acc1);
+        if (q < (1 << lg) && j0 + q < n_w) {
+          if (XS)
+            decode_word_smem(wd[q], vd[q], col, xs, acc0, acc1);
+          else
+            decode_word_l1(wd[q], vd[q], col, a.x, acc0, acc1);
+        }
     }
     const bool last = (rw & kUnitLast) != 0;
-    if (last || i == n_units - 1) {  // row ends, or this CTA's share does
-      const float v = warp_sum(acc0 + acc1);
+    if (last || i == n_units - 1) {  // row ends, or this group's share does
+      const float vsum = warp_sum(acc0 + acc1);
       if (lane == 0) {
-        s_part[slot][warp] = v;
+        s_part[g][slot][lw] = vsum;
         __threadfence_block();
-        if (atomicAdd(&s_cnt[slot], 1) == kDeltaWarps - 1) {
+        if (atomicAdd(&s_cnt[g][slot], 1) == kDeltaWarps - 1) {
           __threadfence_block();
-          const volatile float* sp = s_part[slot];
+          const volatile float* sp = s_part[g][slot];
           float t = 0.f;
 #pragma unroll
           for (int w2 = 0; w2 < kDeltaWarps; ++w2) t += sp[w2];
-          s_cnt[slot] = 0;
+          s_cnt[g][slot] = 0;
           delta_publish(a, row, piece_first && last, piece_wb0, wb, t);
         }
       }
-      slot = slot + 1 == kPcSlots ? 0 : slot + 1;
+      slot = slot + 1 == C::kSlots ? 0 : slot + 1;
       acc0 = acc1 = 0.f;
       piece_wb0 = -1;
     }
@@ -1106,6 +1167,11 @@ constexpr size_t stage_bytes() {
 const void* csr_entry(spmv_dtype dt, bool xs) {
   if (dt == SPMV_F32) return xs ? csr_fn<float, float, true>() : csr_fn<float, float, false>();
   return xs ? csr_fn<__half, __half, true>() : csr_fn<__half, __half, false>();
+}
+
+const void* delta_pc_entry(bool xs) {
+  return xs ? reinterpret_cast<const void*>(&delta4_pc_kernel<true>)
+            : reinterpret_cast<const void*>(&delta4_pc_kernel<false>);
 }
 
 const void* delta_entry(bool xs) {
@@ -1157,13 +1223,24 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t 
 
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget) {
   if (delta_use_pc(x_smem))
-    return occupancy_within(reinterpret_cast<const void*>(&delta4_pc_kernel), kPcThreads,
-                            dyn_smem, budget);
+    return occupancy_within(delta_pc_entry(x_smem), delta_block(x_smem), dyn_smem, budget);
   return occupancy_within(delta_entry(x_smem), kDeltaThreads, dyn_smem, budget);
 }
 
 size_t delta_stages_bytes(bool x_smem) {
-  return (size_t)(delta_use_pc(x_smem) ? kPcStages : kDeltaStages) * DeltaStage::kBytes;
+  if (!delta_use_pc(x_smem)) return (size_t)kDeltaStages * DeltaStage::kBytes;
+  return x_smem ? (size_t)PcCfg<true>::kGroups * PcCfg<true>::kStages * DeltaStage::kBytes
+                : (size_t)PcCfg<false>::kGroups * PcCfg<false>::kStages * DeltaStage::kBytes;
+}
+
+int delta_groups(bool x_smem) {
+  if (!delta_use_pc(x_smem)) return 1;
+  return x_smem ? PcCfg<true>::kGroups : PcCfg<false>::kGroups;
+}
+
+int delta_block(bool x_smem) {
+  if (!delta_use_pc(x_smem)) return kDeltaThreads;
+  return x_smem ? PcCfg<true>::kThreads : PcCfg<false>::kThreads;
 }
 
 size_t delta_stage_bytes() { return (size_t)DeltaStage::kBytes; }
@@ -1187,8 +1264,9 @@ int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn) {
   if (delta_dyn > 0 &&
       (cudaFuncSetAttribute(delta_entry(true), cudaFuncAttributeMaxDynamicSharedMemorySize,
                             (int)delta_dyn) != cudaSuccess ||
-       cudaFuncSetAttribute(reinterpret_cast<const void*>(&delta4_pc_kernel),
-                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+       cudaFuncSetAttribute(delta_pc_entry(true), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            (int)delta_dyn) != cudaSuccess ||
+       cudaFuncSetAttribute(delta_pc_entry(false), cudaFuncAttributeMaxDynamicSharedMemorySize,
                             (int)delta_dyn) != cudaSuccess))
     return -1;
   return 0;
@@ -1233,8 +1311,8 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.n_cols = p.n_cols;
   void* args[] = {&a};
   if (delta_use_pc(p.x_smem))
-    return launch_pdl(reinterpret_cast<const void*>(&delta4_pc_kernel), p.grid, kPcThreads,
-                      p.dyn_smem, stream, args);
+    return launch_pdl(delta_pc_entry(p.x_smem), p.grid, delta_block(p.x_smem), p.dyn_smem,
+                      stream, args);
   return launch_pdl(delta_entry(p.x_smem), p.grid, kDeltaThreads, p.dyn_smem, stream, args);
 }
 
