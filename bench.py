@@ -68,13 +68,18 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha() -> str:
-    p = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc", "spmv_kernels.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_sha(fmt: str) -> str:
+    """sha256[:16] of the device sources of a format's kernel (the shared
+    device header followed by the kernel's file)."""
+    csrc = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("spmv_device.cuh", "spmv_delta.cu" if fmt == "delta4" else "spmv_csr.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, fmt: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken
     on the current kernel source; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -83,7 +88,7 @@ def recorded_traffic(workload: str):
             rec = json.load(f).get(workload)
     except Exception:
         return None
-    if not rec or rec.get("kernel_sha") != kernel_source_sha():
+    if not rec or rec.get("kernel_sha") != kernel_source_sha(fmt):
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -361,7 +366,7 @@ def bench_one(args, name, world, rank, local, pg):
 
     line = None
     if rank == 0:
-        traffic = recorded_traffic(name)
+        traffic = recorded_traffic(name, fmt)
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,

@@ -1,0 +1,406 @@
+// DELTA4 kernel of y = A x for sm_103a ("MACKO-SpMV" 2.2): 4-bit column
+// deltas, 8 per 32-bit word, fp16 values, fp32 accumulation.
+//
+// A work unit is a slice of one row (at most 512 packed words = 4096
+// entries) whose starting column, and each warp's starting column in it, the
+// planner stored, so units and warps are independent. Lane l of warp w
+// decodes LW consecutive words (LW = 1 or 2): a per-lane sum of their nibbles
+// and a 5-step __shfl_up_sync inclusive scan give the column before its
+// first entry; each word's eight columns come from byte-wise prefix sums of
+// its nibbles, and each entry is accumulated with one mixed-precision fma.
+// Producer / consumer scheduling: no CTA barrier per unit (see below).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "spmv_device.cuh"
+#include "spmv_internal.h"
+
+namespace spmv {
+namespace {
+
+struct DeltaArgs {
+  const uint32_t* __restrict__ words;   // 8 nibbles per word
+  const __half* __restrict__ vals;      // 8 fp16 values per word, 16 bytes
+  const __half* __restrict__ x;
+  float* __restrict__ y;
+  const int4* __restrict__ units;       // {row | FIRST | LAST, wb, we, column base}
+  const int32_t* __restrict__ warp_base;  // kDeltaWarps starting columns per unit
+  const int32_t* __restrict__ cta_first;
+  const int32_t* __restrict__ row_split;
+  const SplitInfo* __restrict__ splits;  // {first_slot, n_units, row word, words/unit}
+  float* partials;
+  int32_t* counters;
+  int32_t* status;
+  int n_cols;
+};
+
+// Shared-memory stage of one DELTA4 unit: the warps' starting columns, the
+// unit's words (aligned out to 4 words) and its values (16 bytes per word).
+struct DeltaStage {
+  static constexpr int kBaseBytes = kDeltaWarps * 4;
+  static constexpr int kWordBytes = (kDeltaUnitWords + 8) * 4;
+  static constexpr int kValBytes = kDeltaUnitWords * 16;
+  static constexpr int kBytes = kBaseBytes + kWordBytes + kValBytes;
+};
+static_assert(DeltaStage::kBaseBytes % 16 == 0, "stage regions must stay 16-byte aligned");
+
+// Copy x (n halves) into shared memory with `nthreads` threads, 16 bytes at a
+// time when x is 16-byte aligned (no barrier: the caller synchronises).
+__device__ __forceinline__ void copy_x_half(uint16_t* xs, const __half* x, int n, int nthreads) {
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(x);
+  int done = 0;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+    const int nv = n >> 3;
+    for (int v = threadIdx.x; v < nv; v += nthreads)
+      reinterpret_cast<uint4*>(xs)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+    done = nv << 3;
+  }
+  for (int i = done + threadIdx.x; i < n; i += nthreads) xs[i] = __ldg(src + i);
+}
+
+// Sum of the eight 4-bit fields of w (<= 120).
+__device__ __forceinline__ int nibble_sum(uint32_t w) {
+  const uint32_t b = (w & 0x0F0F0F0Fu) + ((w >> 4) & 0x0F0F0F0Fu);
+  return (int)((b * 0x01010101u) >> 24);
+}
+
+// fp32 acc + a * x for fp16 a and x: the product is exact in fp32, so one
+// fp32 rounding (mixed-precision fma).
+__device__ __forceinline__ float fma_f16(float acc, uint16_t a, uint16_t x) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(x));
+  return acc;
+}
+
+// Decode one word (8 entries) whose first entry follows column `col`, with x
+// read through L1. The eight columns come from byte-wise prefix sums of the
+// nibbles: with lo / hi the even / odd nibbles spread into bytes, byte j of
+// P = (lo + hi) * 0x01010101 is the sum of nibbles 0..2j+1 (at most 120, so
+// no carries), and byte j of P - hi the sum of nibbles 0..2j; each column is
+// one byte extract and one address, and each entry one mixed fma.
+__device__ __forceinline__ void decode_word_l1(uint32_t w, const uint4 v, int& col,
+                                               const __half* xg, float& acc0, float& acc1) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t P = (lo + hi) * 0x01010101u;
+  const uint32_t Q = P - hi;
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(xg) + col;
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t c0 = __byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
+    const uint32_t c1 = __byte_perm(P, 0u, 0x4440u + (uint32_t)j);
+    const uint16_t x0 = __ldg(xb + c0);
+    const uint16_t x1 = __ldg(xb + c1);
+    acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), x0);
+    acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), x1);
+  }
+  col += (int)(P >> 24);
+}
+
+// decode_word_l1 with x from the shared-memory copy.
+__device__ __forceinline__ void decode_word_smem(uint32_t w, const uint4 v, int& col,
+                                                 const uint16_t* xs, float& acc0,
+                                                 float& acc1) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t P = (lo + hi) * 0x01010101u;
+  const uint32_t Q = P - hi;
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c0 = col + (int)__byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
+    const int c1 = col + (int)__byte_perm(P, 0u, 0x4440u + (uint32_t)j);
+    acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), xs[c0]);
+    acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), xs[c1]);
+  }
+  col += (int)(P >> 24);
+}
+
+// Thread 0: start the TMA copies of DELTA4 unit u (descriptor d) into a stage.
+__device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* stage,
+                                           uint64_t* bar, int4* desc, int u, const int4 d,
+                                           uint64_t pol) {
+  if (u < 0) {
+    *desc = make_int4(-1, 0, 0, 0);
+    mbar_arrive(bar);
+    return;
+  }
+  *desc = d;
+  const int wb = d.y, we = d.z;
+  const int wa = wb & ~3;
+  const uint32_t nwb = (uint32_t)(((we + 3) & ~3) - wa) * 4u;
+  const uint32_t nvb = (uint32_t)(we - wb) * 16u;
+  if (nvb == 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  mbar_arrive_expect_tx(bar, DeltaStage::kBaseBytes + nwb + nvb);
+  bulk_g2s(stage, a.warp_base + (size_t)u * kDeltaWarps, DeltaStage::kBaseBytes, bar, pol);
+  bulk_g2s(stage + DeltaStage::kBaseBytes, a.words + wa, nwb, bar, pol);
+  bulk_g2s(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes, a.vals + (size_t)wb * 8,
+           nvb, bar, pol);
+}
+
+// Thread 0, at the end of this CTA's piece of a row split into units: as
+// split_publish for CSR, with units in place of chunks.
+__device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool whole,
+                                              int wb0, int wb, float part) {
+  if (whole) {
+    a.y[row] = part;
+    return;
+  }
+  const int sid = __ldg(a.row_split + row);
+  const SplitInfo si = a.splits[sid];
+  const int k0 = (wb0 - si.row_begin) / si.reserved;
+  const int k = (wb - si.row_begin) / si.reserved;
+  a.partials[si.first_slot + k0] = part;
+  __threadfence();
+  const int add = k - k0 + 1;
+  const int before = atomicAdd(a.counters + sid, add);
+  if (before + add == si.n_chunks) {
+    __threadfence();
+    float sum = 0.f;
+    for (int j = 0; j < si.n_chunks; ++j) {
+      sum += __ldcg(a.partials + si.first_slot + j);
+      a.partials[si.first_slot + j] = 0.f;
+    }
+    a.y[row] = sum;
+    a.counters[sid] = 0;
+  }
+}
+
+// One producer lane per group issues the TMA copies; each group's
+// kDeltaWarps consumer warps decode its units. A stage is handed back by
+// each consumer warp arriving on the stage's "empty" mbarrier once it has
+// read it, so consumer warps never wait for one another per unit (no CTA
+// barrier in the loop): a warp that is done with a unit moves on to the next
+// staged one. A row's total is formed when its last unit ends: each warp
+// parks its shuffle-reduced sum in a slot, and the warp whose shared-memory
+// atomicAdd completes the slot's count adds the kDeltaWarps sums in warp
+// order (deterministic) and publishes the row.
+// A CTA holds G groups, each with its own block of units (a "virtual CTA"
+// of the plan: v = blockIdx.x * G + g), stage ring and slots; with x in
+// shared memory the groups share one copy of it.
+#ifndef SPMV_DELTA_PC_STAGES
+#define SPMV_DELTA_PC_STAGES 3
+#endif
+#ifndef SPMV_DELTA_PC_XS_STAGES
+#define SPMV_DELTA_PC_XS_STAGES 2
+#endif
+#ifndef SPMV_DELTA_PC_XS_GROUPS
+#define SPMV_DELTA_PC_XS_GROUPS 3
+#endif
+template <bool XS>
+struct PcCfg {
+  static constexpr int kGroups = XS ? SPMV_DELTA_PC_XS_GROUPS : 1;
+  static constexpr int kStages = XS ? SPMV_DELTA_PC_XS_STAGES : SPMV_DELTA_PC_STAGES;
+  // row sums in flight: a group's warps are less than kStages units apart
+  static constexpr int kSlots = kStages + 2;
+  static constexpr int kThreads = kGroups * kDeltaThreads + 32;
+  static constexpr int kMinBlocks = XS ? 2 : 5;
+};
+
+template <bool XS>
+__global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
+    delta4_pc_kernel(const DeltaArgs a) {
+  using C = PcCfg<XS>;
+  constexpr int G = C::kGroups, S = C::kStages;
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  __shared__ __align__(8) uint64_t s_full[G][S];
+  __shared__ __align__(8) uint64_t s_empty[G][S];
+  __shared__ int4 s_desc[G][S];
+  __shared__ float s_part[G][C::kSlots][kDeltaWarps];
+  __shared__ int s_cnt[G][C::kSlots];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int g = 0; g < G; ++g) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(&s_full[g][s], 1);
+        mbar_init(&s_empty[g][s], kDeltaWarps);
+      }
+      for (int k = 0; k < C::kSlots; ++k) s_cnt[g][k] = 0;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();  // the only CTA-wide barrier
+
+  if (warp == G * kDeltaWarps) {  // producer warp: lane g feeds group g
+    if (lane < G) {
+      const int g = lane;
+      const int v = blockIdx.x * G + g;
+      const int u_begin = __ldg(a.cta_first + v);
+      const int n_units = __ldg(a.cta_first + v + 1) - u_begin;
+      unsigned char* stages = dyn_smem + (size_t)g * S * DeltaStage::kBytes;
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n_units; ++i) {
+        const int s = i % S;
+        if (i >= S && !mbar_wait_bounded(&s_empty[g][s], (uint32_t)(i / S - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        issue_unit(a, stages + s * DeltaStage::kBytes, &s_full[g][s], &s_desc[g][s],
+                   u_begin + i, __ldg(a.units + u_begin + i), pol);
+        issued = i + 1;
+        if (issued == S) pdl_launch_dependents();
+      }
+      if (issued < S) pdl_launch_dependents();
+      if (!ok) {
+        atomicExch(a.status, 1);
+        // let copies still in flight land before the CTA's shared memory goes
+        for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+          mbar_wait_bounded(&s_full[g][j % S], (uint32_t)(j / S) & 1u);
+      }
+    }
+    return;
+  }
+
+  // consumers; plan-owned data only above, x and y below
+  pdl_wait();
+  const int g = warp / kDeltaWarps, lw = warp % kDeltaWarps;
+  const int gt = tid - g * kDeltaThreads;  // thread index within the group
+  const uint16_t* xs =
+      reinterpret_cast<const uint16_t*>(dyn_smem + (size_t)G * S * DeltaStage::kBytes);
+  if (XS) {
+    copy_x_half(const_cast<uint16_t*>(xs), a.x, a.n_cols, G * kDeltaThreads);
+    asm volatile("bar.sync 1, %0;" ::"n"(G * kDeltaThreads) : "memory");  // consumers only
+  }
+  const int v = blockIdx.x * G + g;
+  const int u_begin = __ldg(a.cta_first + v);
+  const int n_units = __ldg(a.cta_first + v + 1) - u_begin;
+  const unsigned char* stages = dyn_smem + (size_t)g * S * DeltaStage::kBytes;
+  float acc0 = 0.f, acc1 = 0.f;  // this thread's share of the current row piece
+  int piece_wb0 = -1;
+  bool piece_first = false;
+  int slot = 0;
+  for (int i = 0; i < n_units; ++i) {
+    const int s = i % S;
+    if (!mbar_wait_bounded(&s_full[g][s], (uint32_t)(i / S) & 1u)) {
+      if (lane == 0) atomicExch(a.status, 1);
+      break;
+    }
+    const int4 d = s_desc[g][s];
+    const unsigned char* stage = stages + s * DeltaStage::kBytes;
+    const uint32_t rw = (uint32_t)d.x;
+    const int row = (int)(rw & kUnitRowMask);
+    const int wb = d.y, n_w = d.z - d.y;
+    if (piece_wb0 < 0) {
+      piece_wb0 = wb;
+      piece_first = (rw & kUnitFirst) != 0;
+    }
+    const int* s_base = reinterpret_cast<const int*>(stage);
+    const uint32_t* s_words =
+        reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
+    const uint4* s_vals =
+        reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
+    const int lg = (int)((rw >> kUnitLgShift) & 3u);  // log2(words per lane)
+    const int j0 = gt << lg;  // this lane's first word in the unit
+    uint32_t wd[kDeltaMaxLaneWords];
+    uint4 vd[kDeltaMaxLaneWords];
+    int ls = 0;
+#pragma unroll
+    for (int q = 0; q < kDeltaMaxLaneWords; ++q) {
+      const bool in = q < (1 << lg) && j0 + q < n_w;
+      wd[q] = in ? s_words[j0 + q] : 0u;
+      vd[q] = in ? s_vals[j0 + q] : make_uint4(0, 0, 0, 0);
+      ls += nibble_sum(wd[q]);
+    }
+    const int base = s_base[lw];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[g][s]);  // this warp is done with the stage
+    int incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    if (j0 < n_w) {
+      int col = base + incl - ls;  // column before this lane's first entry
+#pragma unroll
+      for (int q = 0; q < kDeltaMaxLaneWords; ++q)
+        if (q < (1 << lg) && j0 + q < n_w) {
+          if (XS)
+            decode_word_smem(wd[q], vd[q], col, xs, acc0, acc1);
+          else
+            decode_word_l1(wd[q], vd[q], col, a.x, acc0, acc1);
+        }
+    }
+    const bool last = (rw & kUnitLast) != 0;
+    if (last || i == n_units - 1) {  // row ends, or this group's share does
+      const float vsum = warp_sum(acc0 + acc1);
+      if (lane == 0) {
+        s_part[g][slot][lw] = vsum;
+        __threadfence_block();
+        if (atomicAdd(&s_cnt[g][slot], 1) == kDeltaWarps - 1) {
+          __threadfence_block();
+          const volatile float* sp = s_part[g][slot];
+          float t = 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < kDeltaWarps; ++w2) t += sp[w2];
+          s_cnt[g][slot] = 0;
+          delta_publish(a, row, piece_first && last, piece_wb0, wb, t);
+        }
+      }
+      slot = slot + 1 == C::kSlots ? 0 : slot + 1;
+      acc0 = acc1 = 0.f;
+      piece_wb0 = -1;
+    }
+  }
+}
+
+const void* delta_entry(bool xs) {
+  return xs ? reinterpret_cast<const void*>(&delta4_pc_kernel<true>)
+            : reinterpret_cast<const void*>(&delta4_pc_kernel<false>);
+}
+
+}  // namespace
+
+int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget) {
+  return occupancy_within(delta_entry(x_smem), delta_block(x_smem), dyn_smem, budget);
+}
+
+size_t delta_stages_bytes(bool x_smem) {
+  return x_smem ? (size_t)PcCfg<true>::kGroups * PcCfg<true>::kStages * DeltaStage::kBytes
+                : (size_t)PcCfg<false>::kGroups * PcCfg<false>::kStages * DeltaStage::kBytes;
+}
+
+int delta_groups(bool x_smem) { return x_smem ? PcCfg<true>::kGroups : PcCfg<false>::kGroups; }
+
+int delta_block(bool x_smem) { return x_smem ? PcCfg<true>::kThreads : PcCfg<false>::kThreads; }
+
+size_t delta_x_smem_bytes(int n_cols) { return ((size_t)n_cols + 8) / 8 * 16; }
+
+int delta_set_smem_limit(size_t dyn) {
+  if (dyn == 0) return 0;
+  for (bool xs : {false, true})
+    if (cudaFuncSetAttribute(delta_entry(xs), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dyn) != cudaSuccess)
+      return -1;
+  return 0;
+}
+
+int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
+  if (p.n_tiles == 0) return 0;
+  DeltaArgs a;
+  a.words = p.words;
+  a.vals = static_cast<const __half*>(p.values);
+  a.x = static_cast<const __half*>(x);
+  a.y = y;
+  a.units = reinterpret_cast<const int4*>(p.tiles);
+  a.warp_base = p.warp_base;
+  a.cta_first = p.cta_first;
+  a.row_split = p.row_split;
+  a.splits = p.splits;
+  a.partials = p.partials;
+  a.counters = p.counters;
+  a.status = p.status;
+  a.n_cols = p.n_cols;
+  void* args[] = {&a};
+  return launch_pdl(delta_entry(p.x_smem), p.grid, delta_block(p.x_smem), p.dyn_smem, stream,
+                    args);
+}
+
+}  // namespace spmv

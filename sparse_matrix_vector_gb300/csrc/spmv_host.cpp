@@ -520,7 +520,7 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
   p->dyn_smem = (p->x_smem ? (xbytes + 15) / 16 * 16 : 0) +
                 kStages * csr_stage_bytes(m->value_dtype);
   p->split_chunk = o.split_chunk;
-  if (set_kernel_smem_limits(p->dyn_smem, 0) != 0) return SPMV_ERR_CUDA;
+  if (csr_set_smem_limit(p->dyn_smem) != 0) return SPMV_ERR_CUDA;
   // persistent grid: every CTA that fits on the device at once within the
   // shared-memory budget (so that L1 keeps at least 60 KB for the x gathers)
   const int occ = csr_kernel_occupancy(m->value_dtype, p->x_smem, p->dyn_smem, kSmemBudget);
@@ -595,7 +595,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
             : o.x_smem == -1 ? xbytes <= kXsAutoBytesDelta : false;
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
                 delta_stages_bytes(p->x_smem);
-  if (set_kernel_smem_limits(0, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
+  if (delta_set_smem_limit(p->dyn_smem) != 0) return SPMV_ERR_CUDA;
   // as for CSR: within the shared-memory budget that leaves L1 its share
   const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem, kSmemBudget);
   if (occ <= 0) return SPMV_ERR_CUDA;

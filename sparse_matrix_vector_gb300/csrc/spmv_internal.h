@@ -1,5 +1,5 @@
 // Internal declarations shared by the host planner (spmv_host.cpp) and the
-// device kernels (spmv_kernels.cu). Not part of the public ABI.
+// device kernels (spmv_csr.cu, spmv_delta.cu). Not part of the public ABI.
 #pragma once
 
 #include <cstddef>
@@ -54,10 +54,6 @@ constexpr int kDeltaUnitWords = SPMV_DELTA_UNIT_WORDS;
 constexpr int kDeltaMaxLaneWords = kDeltaUnitWords / kDeltaThreads;
 static_assert(kDeltaMaxLaneWords == 1 || kDeltaMaxLaneWords == 2 || kDeltaMaxLaneWords == 4,
               "words per lane must be 1, 2 or 4");
-#ifndef SPMV_DELTA_STAGES
-#define SPMV_DELTA_STAGES 2
-#endif
-constexpr int kDeltaStages = SPMV_DELTA_STAGES;
 // DELTA4 unit descriptor: {row | FIRST | LAST | log2(LW) << kUnitLgShift,
 // word_begin, word_end, column before the unit's first entry}; FIRST / LAST:
 // first / last unit of the row.
@@ -177,22 +173,16 @@ struct Plan {
   spmv_plan_info info{};
 };
 
-// Kernel-side entry points (spmv_kernels.cu).
+// Kernel-side entry points (spmv_csr.cu, spmv_delta.cu).
 int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t budget);
-int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget);
-// DELTA4 runs the producer / consumer kernel (the CTA-barrier kernel stays
-// for comparison builds).
-#ifndef SPMV_DELTA_PC
-#define SPMV_DELTA_PC 1
-#endif
-inline bool delta_use_pc(bool) { return SPMV_DELTA_PC != 0; }
-size_t delta_stages_bytes(bool x_smem);
-int delta_groups(bool x_smem);  // unit blocks ("virtual CTAs") per CTA
-int delta_block(bool x_smem);   // threads per CTA
-int set_kernel_smem_limits(size_t csr_dyn, size_t delta_dyn);
 size_t csr_stage_bytes(spmv_dtype dtype);
-size_t delta_stage_bytes();
+int csr_set_smem_limit(size_t dyn);
+int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget);
+size_t delta_stages_bytes(bool x_smem);  // every stage of every group
+int delta_groups(bool x_smem);           // unit blocks ("virtual CTAs") per CTA
+int delta_block(bool x_smem);            // threads per CTA
 size_t delta_x_smem_bytes(int n_cols);
+int delta_set_smem_limit(size_t dyn);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 
