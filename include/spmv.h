@@ -122,7 +122,11 @@ typedef struct spmv_plan_options {
                             2 walk mode (per-thread segmented sums)        */
   int32_t lanes;         /* lanes per row in forced lanes mode: 1..256
                             (rounded down to a power of two)               */
-  int32_t reserved[8];
+  int32_t interleave;    /* CSR order in which threads take a unit's
+                            nonzeros for the x gathers: 0 auto, 1 chunks of
+                            8 consecutive per thread, 2 element-interleaved
+                            (a warp's lanes take consecutive nonzeros)     */
+  int32_t reserved[7];
 } spmv_plan_options;
 
 /* What the planner decided; filled by spmv_plan_inspect / spmv_plan_get_info.
@@ -154,7 +158,8 @@ typedef struct spmv_plan_info {
   int64_t aux_bytes;         /* planner tables and scratch on the device   */
   int64_t algorithmic_bytes; /* matrix_bytes + x read once + y written     */
   int64_t walk_tiles;        /* short-row tiles reduced in walk mode       */
-  int64_t reserved[7];
+  int64_t interleaved;       /* 1 if products are taken element-interleaved */
+  int64_t reserved[6];
 } spmv_plan_info;
 
 typedef struct spmv_plan spmv_plan;

@@ -43,7 +43,7 @@ class spmv_plan_options(ctypes.Structure):
     _fields_ = [("tile_nnz", c_i32), ("tile_rows", c_i32),
                 ("cta_row_min", c_i32), ("split_row_min", c_i32),
                 ("split_chunk", c_i32), ("x_smem", c_i32), ("reduce", c_i32),
-                ("lanes", c_i32), ("reserved", c_i32 * 8)]
+                ("lanes", c_i32), ("interleave", c_i32), ("reserved", c_i32 * 7)]
 
 
 class spmv_plan_info(ctypes.Structure):
@@ -55,7 +55,7 @@ class spmv_plan_info(ctypes.Structure):
                 ("grid", c_i32), ("block", c_i32),
                 ("launches_per_run", c_i32), ("matrix_bytes", c_i64),
                 ("aux_bytes", c_i64), ("algorithmic_bytes", c_i64),
-                ("walk_tiles", c_i64), ("reserved", c_i64 * 7)]
+                ("walk_tiles", c_i64), ("interleaved", c_i64), ("reserved", c_i64 * 6)]
 
 
 # name -> (restype, argtypes); every function declared in include/spmv.h

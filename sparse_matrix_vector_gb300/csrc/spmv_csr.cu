@@ -160,12 +160,44 @@ __device__ __forceinline__ void chunk_products(const int* s_col, const VT* s_val
   }
 }
 
+// Value of staged element el, widened to fp32.
+__device__ __forceinline__ float staged_val(const float* v, int el) { return v[el]; }
+__device__ __forceinline__ float staged_val(const __half* v, int el) {
+  return __half2float(v[el]);
+}
+
+// Staged element el of thread t, step k < 8, element-interleaved over the
+// CTA: a warp-wide step spans 32 consecutive nonzeros, so its x gathers fall
+// in few sectors.
+__device__ __forceinline__ int strided_el(int base, int k) {
+  return base + (int)threadIdx.x + kThreads * k;
+}
+
+// Products of the staged elements strided_el(base, k), k < 8 (0 outside
+// [lo_rel, hi_rel)). All eight gathers are issued before any product is used.
+template <typename VT, typename XT, bool XS>
+__device__ __forceinline__ void strided_products(const int* s_col, const VT* s_val, int base,
+                                                 int lo_rel, int hi_rel, const XT* xg,
+                                                 const XT* xs, float (&p)[8]) {
+  float xv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int el = strided_el(base, k);
+    xv[k] = (el >= lo_rel && el < hi_rel) ? gather<XS>(xg, xs, s_col[el]) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int el = strided_el(base, k);
+    p[k] = (el >= lo_rel && el < hi_rel) ? staged_val(s_val, el) * xv[k] : 0.f;
+  }
+}
+
 // Short-row tile from a stage, lanes mode (rows of similar length): every
 // thread multiplies its 8 staged nonzeros by the gathered x and parks the
 // products in place of the staged columns; then each row is summed by
 // g = 2^lg lanes and a shuffle reduction (g = 64..256: by g / 32 warps, whose
 // sums meet in shared memory).
-template <typename VT, typename XT, bool XS>
+template <typename VT, typename XT, bool XS, bool IL>
 __device__ __forceinline__ void stream_tile_lanes(const CsrArgs& a, const int4 d,
                                                   unsigned char* stage, const XT* xs,
                                                   float* s_red) {
@@ -183,11 +215,23 @@ __device__ __forceinline__ void stream_tile_lanes(const CsrArgs& a, const int4 d
       (r0 - (r0 & ~3));
   float* s_prod = reinterpret_cast<float*>(s_col);  // products replace the columns
   const XT* xg = static_cast<const XT*>(a.x);
-  for (int c = tid; c < n8; c += kThreads) {
+  if (IL) {
+    // the tile spans at most kThreads * 8 elements; each thread replaces
+    // exactly the columns it read with their products
     float p[8];
-    chunk_products<VT, XT, XS>(s_col, s_val, c, s_rel, e_rel, xg, xs, p);
-    reinterpret_cast<float4*>(s_prod)[2 * c] = make_float4(p[0], p[1], p[2], p[3]);
-    reinterpret_cast<float4*>(s_prod)[2 * c + 1] = make_float4(p[4], p[5], p[6], p[7]);
+    strided_products<VT, XT, XS>(s_col, s_val, 0, s_rel, e_rel, xg, xs, p);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int el = strided_el(0, k);
+      if (el < e_rel) s_prod[el] = p[k];
+    }
+  } else {
+    for (int c = tid; c < n8; c += kThreads) {
+      float p[8];
+      chunk_products<VT, XT, XS>(s_col, s_val, c, s_rel, e_rel, xg, xs, p);
+      reinterpret_cast<float4*>(s_prod)[2 * c] = make_float4(p[0], p[1], p[2], p[3]);
+      reinterpret_cast<float4*>(s_prod)[2 * c + 1] = make_float4(p[4], p[5], p[6], p[7]);
+    }
   }
   __syncthreads();
   const int g = 1 << lg;
@@ -338,7 +382,7 @@ __device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
 }
 
 // Per-thread partial sum of a staged slice [b, e) of one row.
-template <typename VT, typename XT, bool XS>
+template <typename VT, typename XT, bool XS, bool IL>
 __device__ __forceinline__ float chunk_sum(const CsrArgs& a, const int4 d,
                                            unsigned char* stage, const XT* xs) {
   const int a0 = d.y & ~7;
@@ -348,11 +392,20 @@ __device__ __forceinline__ float chunk_sum(const CsrArgs& a, const int4 d,
   const VT* s_val = reinterpret_cast<const VT*>(stage + Stage<VT>::kColBytes);
   const XT* xg = static_cast<const XT*>(a.x);
   float acc = 0.f;
-  for (int c = threadIdx.x; c < n8; c += kThreads) {
-    float p[8];
-    chunk_products<VT, XT, XS>(s_col, s_val, c, lo_rel, hi_rel, xg, xs, p);
+  if (IL) {
+    for (int base = 0; base < hi_rel; base += 8 * kThreads) {
+      float p[8];
+      strided_products<VT, XT, XS>(s_col, s_val, base, lo_rel, hi_rel, xg, xs, p);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc += p[q];
+      for (int q = 0; q < 8; ++q) acc += p[q];
+    }
+  } else {
+    for (int c = threadIdx.x; c < n8; c += kThreads) {
+      float p[8];
+      chunk_products<VT, XT, XS>(s_col, s_val, c, lo_rel, hi_rel, xg, xs, p);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc += p[q];
+    }
   }
   return acc;
 }
@@ -394,7 +447,7 @@ __device__ __forceinline__ void split_publish(const CsrArgs& a, int row, int sid
 // memory stages) while the CTA computes the oldest one.
 // Register budget: as many CTAs per SM as the planner's shared-memory budget
 // lets in (5 with fp32 stages, 6 with fp16 ones).
-template <typename VT, typename XT, bool XS>
+template <typename VT, typename XT, bool XS, bool IL>
 __global__ void __launch_bounds__(kThreads, kCsrCtasPerSm<VT>) csr_kernel(const CsrArgs a) {
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_bar[kStages];
@@ -459,16 +512,16 @@ __global__ void __launch_bounds__(kThreads, kCsrCtasPerSm<VT>) csr_kernel(const 
       if (w & kStreamWalk)
         stream_tile_walk<VT, XT, XS>(a, d, stage, xs, s_carry);
       else
-        stream_tile_lanes<VT, XT, XS>(a, d, stage, xs, s_red);
+        stream_tile_lanes<VT, XT, XS, IL>(a, d, stage, xs, s_red);
     } else if (kind == kKindRow) {
-      const float part = cta_sum(chunk_sum<VT, XT, XS>(a, d, stage, xs), s_red);
+      const float part = cta_sum(chunk_sum<VT, XT, XS, IL>(a, d, stage, xs), s_red);
       if (tid == 0) a.y[d.x] = part;
     } else {
       if (piece_b0 < 0) {
         piece_b0 = d.y;
         piece_first = (w & kSplitFirst) != 0;
       }
-      row_acc += chunk_sum<VT, XT, XS>(a, d, stage, xs);
+      row_acc += chunk_sum<VT, XT, XS, IL>(a, d, stage, xs);
       const bool last = (w & kSplitLast) != 0;
       if (last || u_begin + i == u_end - 1) {  // row ends, or this CTA's share does
         const float part = cta_sum(row_acc, s_red);
@@ -500,8 +553,9 @@ __global__ void __launch_bounds__(kThreads, kCsrCtasPerSm<VT>) csr_kernel(const 
 }
 
 template <typename VT, typename XT, bool XS>
-const void* csr_fn() {
-  return reinterpret_cast<const void*>(&csr_kernel<VT, XT, XS>);
+const void* csr_fn(bool il) {
+  return il ? reinterpret_cast<const void*>(&csr_kernel<VT, XT, XS, true>)
+            : reinterpret_cast<const void*>(&csr_kernel<VT, XT, XS, false>);
 }
 
 template <typename VT>
@@ -509,15 +563,17 @@ constexpr size_t stage_bytes() {
   return (size_t)Stage<VT>::kBytes;
 }
 
-const void* csr_entry(spmv_dtype dt, bool xs) {
-  if (dt == SPMV_F32) return xs ? csr_fn<float, float, true>() : csr_fn<float, float, false>();
-  return xs ? csr_fn<__half, __half, true>() : csr_fn<__half, __half, false>();
+const void* csr_entry(spmv_dtype dt, bool xs, bool il) {
+  if (dt == SPMV_F32)
+    return xs ? csr_fn<float, float, true>(il) : csr_fn<float, float, false>(il);
+  return xs ? csr_fn<__half, __half, true>(il) : csr_fn<__half, __half, false>(il);
 }
 
 }  // namespace
 
-int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t budget) {
-  return occupancy_within(csr_entry(dtype, x_smem), kThreads, dyn_smem, budget);
+int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, bool il, size_t dyn_smem,
+                         size_t budget) {
+  return occupancy_within(csr_entry(dtype, x_smem, il), kThreads, dyn_smem, budget);
 }
 
 size_t csr_stage_bytes(spmv_dtype dtype) {
@@ -525,13 +581,13 @@ size_t csr_stage_bytes(spmv_dtype dtype) {
 }
 
 int csr_set_smem_limit(size_t dyn) {
-  const void* fns[] = {csr_entry(SPMV_F32, true), csr_entry(SPMV_F16, true),
-                       csr_entry(SPMV_F32, false), csr_entry(SPMV_F16, false)};
-  if (dyn > 0)
-    for (const void* f : fns)
-      if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) !=
-          cudaSuccess)
-        return -1;
+  if (dyn == 0) return 0;
+  for (spmv_dtype dt : {SPMV_F32, SPMV_F16})
+    for (bool xs : {false, true})
+      for (bool il : {false, true})
+        if (cudaFuncSetAttribute(csr_entry(dt, xs, il), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dyn) != cudaSuccess)
+          return -1;
   return 0;
 }
 
@@ -553,7 +609,8 @@ int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
   a.split_chunk = p.split_chunk;
   a.status = p.status;
   void* args[] = {&a};
-  return launch_pdl(csr_entry(p.dtype, p.x_smem), p.grid, kThreads, p.dyn_smem, stream, args);
+  return launch_pdl(csr_entry(p.dtype, p.x_smem, p.interleaved), p.grid, kThreads, p.dyn_smem,
+                    stream, args);
 }
 
 }  // namespace spmv

@@ -105,6 +105,7 @@ struct Options {
   int x_smem;  // -1 auto, 0 off, 1 on
   int reduce;  // short-row tiles: -1 per-tile choice, 0 lanes mode, 1 walk mode
   int lanes_log2;  // lanes mode when forced
+  int interleave;  // CSR products: 0 auto, 1 chunks of 8, 2 element-interleaved
 };
 
 Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype);
@@ -146,6 +147,7 @@ struct Plan {
   int n_rows = 0, n_cols = 0;
   int64_t nnz = 0, n_entries = 0;
   bool x_smem = false;
+  bool interleaved = false;  // CSR: products element-interleaved over the CTA
   bool x_aligned16 = false;
   int grid = 0;
   size_t dyn_smem = 0;
@@ -174,7 +176,8 @@ struct Plan {
 };
 
 // Kernel-side entry points (spmv_csr.cu, spmv_delta.cu).
-int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem, size_t budget);
+int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, bool il, size_t dyn_smem,
+                         size_t budget);
 size_t csr_stage_bytes(spmv_dtype dtype);
 int csr_set_smem_limit(size_t dyn);
 int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget);

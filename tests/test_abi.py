@@ -252,6 +252,28 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     assert info["matrix_bytes"] == 2 * enc.n_entries + enc.n_entries // 2 + 4 * (llm.n_rows + 1)
 
 
+def test_gather_order_choice(spmv_lib):
+    """Element-interleaved products where rows are long and 8 nonzeros of a
+    row span over 40 bytes of x; chunks of 8 otherwise; options force."""
+    lap = workloads.laplacian(60, 50)
+    info = S.spmv_plan_inspect(lap.row_ptr, lap.col_idx, lap.values, lap.n_cols)
+    assert info["interleaved"] == 0                      # rows of 5
+    sparse = workloads.llm(0.9, n=2048)
+    info = S.spmv_plan_inspect(sparse.row_ptr, sparse.col_idx, sparse.values, sparse.n_cols)
+    assert info["interleaved"] == 1                      # ~80 fp16 columns per 8
+    dense = workloads.llm(0.3, n=2048)
+    info = S.spmv_plan_inspect(dense.row_ptr, dense.col_idx, dense.values, dense.n_cols)
+    assert info["interleaved"] == 0                      # ~11 columns per 8
+    for force, want in ((1, 0), (2, 1)):
+        info = S.spmv_plan_inspect(sparse.row_ptr, sparse.col_idx, sparse.values,
+                                   sparse.n_cols,
+                                   options=S.spmv_plan_options(interleave=force))
+        assert info["interleaved"] == want
+        info = S.spmv_plan_inspect(lap.row_ptr, lap.col_idx, lap.values, lap.n_cols,
+                                   options=S.spmv_plan_options(interleave=force))
+        assert info["interleaved"] == want
+
+
 def test_empty_and_degenerate_inspect(spmv_lib):
     info = S.spmv_plan_inspect(np.zeros(1, np.int32), np.zeros(0, np.int32),
                                np.zeros(0, np.float32), 0)

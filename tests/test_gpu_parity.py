@@ -133,6 +133,9 @@ def test_full_size_delta4(name):
     {"reduce": 1, "lanes": 1}, {"reduce": 1, "lanes": 4}, {"reduce": 1, "lanes": 32},
     {"reduce": 1, "lanes": 64}, {"reduce": 1, "lanes": 256},
     {"reduce": 1, "lanes": 128, "tile_rows": 3},
+    {"interleave": 2}, {"interleave": 2, "reduce": 1, "lanes": 4},
+    {"interleave": 2, "cta_row_min": 100, "split_row_min": 200, "split_chunk": 64},
+    {"interleave": 1},
     {"reduce": 2}, {"reduce": 2, "tile_nnz": 97},
 ])
 def test_forced_planner_paths(kw):
@@ -145,7 +148,8 @@ def test_forced_planner_paths(kw):
 @pytest.mark.parametrize("kw", [{"x_smem": 0}, {"x_smem": 1},
                                 {"cta_row_min": 100, "split_row_min": 150,
                                  "split_chunk": 64},
-                                {"cta_row_min": 2000, "reduce": 1, "lanes": 128}])
+                                {"cta_row_min": 2000, "reduce": 1, "lanes": 128},
+                                {"interleave": 2}, {"interleave": 1}])
 def test_forced_paths_fp16_csr(kw):
     m = workloads.llm(0.8, n=1000, seed=3)
     y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
