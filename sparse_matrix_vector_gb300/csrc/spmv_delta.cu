@@ -192,6 +192,8 @@ __device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool 
 #ifndef SPMV_DELTA_PC_XS_GROUPS
 #define SPMV_DELTA_PC_XS_GROUPS 3
 #endif
+static_assert(kDeltaMaxLaneWords == 2, "the decode packs two words per lane");
+
 template <bool XS>
 struct PcCfg {
   static constexpr int kGroups = XS ? SPMV_DELTA_PC_XS_GROUPS : 1;
@@ -296,37 +298,45 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
         reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
     const uint4* s_vals =
         reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
-    const int lg = (int)((rw >> kUnitLgShift) & 3u);  // log2(words per lane)
-    const int j0 = gt << lg;  // this lane's first word in the unit
-    uint32_t wd[kDeltaMaxLaneWords];
-    uint4 vd[kDeltaMaxLaneWords];
-    int ls = 0;
-#pragma unroll
-    for (int q = 0; q < kDeltaMaxLaneWords; ++q) {
-      const bool in = q < (1 << lg) && j0 + q < n_w;
-      wd[q] = in ? s_words[j0 + q] : 0u;
-      vd[q] = in ? s_vals[j0 + q] : make_uint4(0, 0, 0, 0);
-      ls += nibble_sum(wd[q]);
-    }
+    // Lane l of warp w takes words 32 LW w + 32 q + l, q < LW: consecutive
+    // lanes read consecutive words and values (conflict-free shared-memory
+    // loads). The column before word q of a lane is the warp's starting column
+    // plus the nibbles of every earlier word of the warp's segment: one 5-step
+    // scan of both words' nibble sums packed in 16-bit halves (each at most
+    // 32 * 120) gives both.
+    const int lg = (int)((rw >> kUnitLgShift) & 1u);  // log2(words per lane): 0 or 1
+    const int wseg = lw << (5 + lg);                  // first word of the warp's segment
+    const int j0 = wseg + lane, j1 = j0 + 32;
+    const bool in0 = j0 < n_w, in1 = lg && j1 < n_w;
+    const uint32_t w0 = in0 ? s_words[j0] : 0u;
+    const uint32_t w1 = in1 ? s_words[j1] : 0u;
+    const uint4 v0 = in0 ? s_vals[j0] : make_uint4(0, 0, 0, 0);
+    const uint4 v1 = in1 ? s_vals[j1] : make_uint4(0, 0, 0, 0);
+    const int ns0 = nibble_sum(w0), ns1 = nibble_sum(w1);
     const int base = s_base[lw];
     __syncwarp();
     if (lane == 0) mbar_arrive(&s_empty[g][s]);  // this warp is done with the stage
-    int incl = ls;
+    int incl = ns0 | (ns1 << 16);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int up = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += up;
     }
-    if (j0 < n_w) {
-      int col = base + incl - ls;  // column before this lane's first entry
-#pragma unroll
-      for (int q = 0; q < kDeltaMaxLaneWords; ++q)
-        if (q < (1 << lg) && j0 + q < n_w) {
-          if (XS)
-            decode_word_smem(wd[q], vd[q], col, xs, acc0, acc1);
-          else
-            decode_word_l1(wd[q], vd[q], col, a.x, acc0, acc1);
-        }
+    const int incl0 = incl & 0xFFFF, incl1 = incl >> 16;
+    const int total0 = __shfl_sync(0xffffffffu, incl0, 31);
+    if (in0) {
+      int col = base + incl0 - ns0;  // column before word j0's first entry
+      if (XS)
+        decode_word_smem(w0, v0, col, xs, acc0, acc1);
+      else
+        decode_word_l1(w0, v0, col, a.x, acc0, acc1);
+    }
+    if (in1) {
+      int col = base + total0 + incl1 - ns1;  // column before word j1's first entry
+      if (XS)
+        decode_word_smem(w1, v1, col, xs, acc0, acc1);
+      else
+        decode_word_l1(w1, v1, col, a.x, acc0, acc1);
     }
     const bool last = (rw & kUnitLast) != 0;
     if (last || i == n_units - 1) {  // row ends, or this group's share does
