@@ -65,6 +65,13 @@ def _bind(path: str):
     lib.oracle_delta_fill.restype = ctypes.c_int
     lib.oracle_delta_decode.argtypes = [i64, p, p, p, p, p, p]
     lib.oracle_delta_decode.restype = i64
+    ci = ctypes.c_int
+    lib.oracle_delta_count_bits.argtypes = [i64, p, p, ci, p, p, p]
+    lib.oracle_delta_count_bits.restype = ctypes.c_int
+    lib.oracle_delta_fill_bits.argtypes = [i64, p, p, p, ci, p, p, p]
+    lib.oracle_delta_fill_bits.restype = ctypes.c_int
+    lib.oracle_delta_decode_bits.argtypes = [i64, p, p, p, ci, p, p, p]
+    lib.oracle_delta_decode_bits.restype = i64
     return lib
 
 
@@ -141,31 +148,35 @@ def csr_spmv(row_ptr, col_idx, values, x, with_abs: bool = True):
 
 
 class DeltaMatrix:
-    """The 4-bit column-delta format as plain numpy arrays."""
+    """The column-delta format as plain numpy arrays (fields of `bits` bits,
+    32 / bits to a word; 4 bits unless asked otherwise)."""
 
     def __init__(self, n_rows, n_cols, row_ptr, values, words, gap_pads,
-                 align_pads):
+                 align_pads, bits=4):
         self.n_rows = n_rows
         self.n_cols = n_cols
         self.row_ptr = row_ptr      # int64[n_rows+1], entry offsets
         self.values = values        # uint16[n_entries], fp16 bit patterns
-        self.words = words          # uint32[n_entries/8], packed nibbles
+        self.words = words          # uint32[n_entries*bits/32], packed fields
         self.gap_pads = gap_pads
         self.align_pads = align_pads
+        self.bits = bits
 
     @property
     def n_entries(self) -> int:
         return int(self.row_ptr[-1])
 
     def deltas(self) -> np.ndarray:
-        """Unpacked 4-bit codes, one per entry (little-nibble-first)."""
-        shifts = (4 * np.arange(8, dtype=np.uint32))
-        d = (self.words[:, None] >> shifts[None, :]) & np.uint32(0xF)
+        """Unpacked codes, one per entry (lowest field first)."""
+        per = 32 // self.bits
+        shifts = (self.bits * np.arange(per, dtype=np.uint32))
+        d = (self.words[:, None] >> shifts[None, :]) & np.uint32((1 << self.bits) - 1)
         return d.reshape(-1).astype(np.uint8)
 
 
-def delta_encode(n_cols, row_ptr, col_idx, values_f16) -> DeltaMatrix:
-    """Encode a CSR matrix with fp16 values into the 4-bit delta format."""
+def delta_encode(n_cols, row_ptr, col_idx, values_f16, bits: int = 4) -> DeltaMatrix:
+    """Encode a CSR matrix with fp16 values into the column-delta format with
+    deltas of `bits` bits (2, 4 or 8)."""
     rp, ci = _i64(row_ptr), _i64(col_idx)
     vb = np.ascontiguousarray(np.asarray(values_f16, dtype=np.float16)
                               .view(np.uint16))
@@ -174,18 +185,20 @@ def delta_encode(n_cols, row_ptr, col_idx, values_f16) -> DeltaMatrix:
     out_rp = np.empty(n_rows + 1, dtype=np.int64)
     gaps = np.zeros(1, dtype=np.int64)
     aligns = np.zeros(1, dtype=np.int64)
-    rc = lib.oracle_delta_count(n_rows, _ptr(rp), _ptr(ci), _ptr(out_rp),
-                                _ptr(gaps), _ptr(aligns))
+    rc = lib.oracle_delta_count_bits(n_rows, _ptr(rp), _ptr(ci), int(bits), _ptr(out_rp),
+                                     _ptr(gaps), _ptr(aligns))
+    if rc == -2:
+        raise ValueError("delta width must be 2, 4 or 8 bits")
     if rc != 0:
         raise ValueError("delta format needs strictly increasing, "
                          "non-negative columns in every row")
     n_entries = int(out_rp[-1])
     out_vals = np.zeros(n_entries, dtype=np.uint16)
-    out_words = np.zeros(n_entries // 8, dtype=np.uint32)
-    lib.oracle_delta_fill(n_rows, _ptr(rp), _ptr(ci), _ptr(vb), _ptr(out_rp),
-                          _ptr(out_vals), _ptr(out_words))
+    out_words = np.zeros(n_entries * bits // 32, dtype=np.uint32)
+    lib.oracle_delta_fill_bits(n_rows, _ptr(rp), _ptr(ci), _ptr(vb), int(bits), _ptr(out_rp),
+                               _ptr(out_vals), _ptr(out_words))
     return DeltaMatrix(n_rows, int(n_cols), out_rp, out_vals, out_words,
-                       int(gaps[0]), int(aligns[0]))
+                       int(gaps[0]), int(aligns[0]), bits=int(bits))
 
 
 def delta_decode(m: DeltaMatrix):
@@ -197,9 +210,9 @@ def delta_decode(m: DeltaMatrix):
     out_rp = np.empty(m.n_rows + 1, dtype=np.int64)
     out_col = np.empty(max(n, 1), dtype=np.int64)
     out_vals = np.empty(max(n, 1), dtype=np.uint16)
-    kept = _load().oracle_delta_decode(m.n_rows, _ptr(rp), _ptr(vals),
-                                       _ptr(words), _ptr(out_rp),
-                                       _ptr(out_col), _ptr(out_vals))
+    kept = _load().oracle_delta_decode_bits(m.n_rows, _ptr(rp), _ptr(vals), _ptr(words),
+                                            int(m.bits), _ptr(out_rp), _ptr(out_col),
+                                            _ptr(out_vals))
     return out_rp, out_col[:kept].copy(), out_vals[:kept].view(np.float16).copy()
 
 

@@ -14,6 +14,7 @@ import oracle
 import workloads
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "delta_examples.json")
+GOLDEN_WIDTHS = os.path.join(os.path.dirname(__file__), "golden", "delta_widths.json")
 
 
 # ---------------------------------------------------------------- helpers
@@ -165,9 +166,27 @@ def pin_delta_golden():
         assert np.array_equal(m.values[m.values != 0], vals.view(np.uint16))
 
 
-def expected_pad_counts(rp, ci):
-    """Closed form of the reading: a gap d (first gap = first column) needs
-    max(0, floor((d - 1) / 15)) padding entries; rows round up to 8."""
+def pin_delta_widths_golden():
+    with open(GOLDEN_WIDTHS) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        bits = c["bits"]
+        cols = np.array(c["cols"], dtype=np.int64)
+        n = cols.size
+        vals = (np.arange(1, n + 1) * 0.125).astype(np.float16)
+        rp = np.array([0, n], dtype=np.int64)
+        m = oracle.delta_encode(512, rp, cols, vals, bits=bits)
+        assert list(m.deltas()) == c["deltas"], c
+        assert list((m.values == 0).astype(int)) == c["pad"], c
+        assert list(m.words) == c["words"], c
+        assert m.n_entries % (32 // bits) == 0
+        assert np.array_equal(m.values[m.values != 0], vals.view(np.uint16))
+
+
+def expected_pad_counts(rp, ci, bits=4):
+    """Closed form of the reading: with b-bit fields a gap d (first gap =
+    first column) needs max(0, floor((d - 1) / (2^b - 1))) padding entries
+    (floor((d - 1) / 15) for 4 bits); rows round up to 32 / b entries."""
     rp = np.asarray(rp, np.int64)
     ci = np.asarray(ci, np.int64)
     n_rows = rp.size - 1
@@ -177,11 +196,13 @@ def expected_pad_counts(rp, ci):
     first[rp[:-1][lengths > 0]] = True
     prev[~first] = ci[np.nonzero(~first)[0] - 1]
     gaps = ci - prev
-    pads_per = np.maximum(0, (gaps - 1) // 15)
+    dmax = (1 << bits) - 1
+    per = 32 // bits
+    pads_per = np.maximum(0, (gaps - 1) // dmax)
     row_of = np.repeat(np.arange(n_rows), lengths)
     row_pads = np.bincount(row_of, weights=pads_per, minlength=n_rows).astype(np.int64)
     unaligned = lengths + row_pads
-    aligned = (unaligned + 7) // 8 * 8
+    aligned = (unaligned + per - 1) // per * per
     return int(pads_per.sum()), int((aligned - unaligned).sum()), aligned
 
 
@@ -189,16 +210,16 @@ def pin_delta_roundtrip_and_counts():
     mats = [workloads.llm(0.3, n=200), workloads.llm(0.9, n=333),
             workloads.from_lengths("mixed", np.r_[0, 1, 7, 8, 9, 0, 64, 3],
                                    400, seed=5, dtype=np.float16)]
-    for m in mats:
+    for m, bits in [(mm, b) for mm in mats for b in (4, 2, 8)]:
         vals = m.values.astype(np.float16)
         vals[vals == 0] = np.float16(0.5)   # the round trip needs no +-0.0
-        enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, vals)
-        gaps, aligns, aligned = expected_pad_counts(m.row_ptr, m.col_idx)
+        enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, vals, bits=bits)
+        gaps, aligns, aligned = expected_pad_counts(m.row_ptr, m.col_idx, bits)
         assert enc.gap_pads == gaps and enc.align_pads == aligns
         assert np.array_equal(np.diff(enc.row_ptr), aligned)
         assert enc.n_entries == m.nnz + gaps + aligns
         d = enc.deltas()
-        assert d.max(initial=0) <= 15
+        assert d.max(initial=0) <= (1 << bits) - 1
         rp, col, v = oracle.delta_decode(enc)
         assert np.array_equal(rp, m.row_ptr.astype(np.int64))
         assert np.array_equal(col, m.col_idx.astype(np.int64))
@@ -213,7 +234,7 @@ def pin_delta_roundtrip_and_counts():
 
 ALL_PINS = [pin_dense_bruteforce, pin_identity_and_permutation,
             pin_laplacian_constant, pin_row_of_ones, pin_scipy,
-            pin_delta_golden, pin_delta_roundtrip_and_counts]
+            pin_delta_golden, pin_delta_widths_golden, pin_delta_roundtrip_and_counts]
 
 
 # ---------------------------------------------------------------- tests
@@ -250,11 +271,12 @@ MUTANTS = [
     ("wrong_value_index", "values[k] * x[col_idx[k]]",
      "values[row_ptr[i]] * x[col_idx[k]]"),
     ("abs_sum_signed", "(prod < 0.0 ? -prod : prod)", "prod"),
-    ("pad_threshold", "#define DELTA_MAX 15", "#define DELTA_MAX 14"),
+    ("pad_threshold", "const int64_t dmax = ((int64_t)1 << bits) - 1; /* largest",
+     "const int64_t dmax = ((int64_t)1 << bits) - 2; /* largest"),
     ("prev_not_reset", "int64_t prev = 0;", "int64_t prev = 1;"),
-    ("nibble_order", "DELTA_BITS * (e % ROW_ALIGN)",
-     "DELTA_BITS * (7 - e % ROW_ALIGN)"),
-    ("no_row_alignment", "count % ROW_ALIGN != 0", "count % 1 != 0"),
+    ("nibble_order", "uint32_t shift = (uint32_t)(bits * (e % per_word));\n  out_words",
+     "uint32_t shift = (uint32_t)(bits * (per_word - 1 - e % per_word));\n  out_words"),
+    ("no_row_alignment", "count % per_word != 0", "count % 1 != 0"),
 ]
 
 
