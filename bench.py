@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Benchmark of y = A x on GB300 through the C ABI (include/spmv.h).
 
-One step = one spmv_run (the whole path: tile kernel or DELTA4 decode kernel)
+One step = one spmv_run (the whole path: tile kernel or DELTA decode kernel)
 over one resident copy of the workload. Copies rotate so that the footprint
 of the timed loop is several times the L2 size: every step streams its matrix
 from HBM. Steps are captured into CUDA graphs and replayed; the timed region
@@ -49,8 +49,9 @@ WORKLOADS = {
 for _s in (30, 50, 70, 90):
     WORKLOADS[f"llm{_s}_csr"] = (f"llm{_s}", "csr",
                                  f"llm_12288x12288_sparsity{_s}_f16_csr")
-    WORKLOADS[f"llm{_s}_delta4"] = (f"llm{_s}", "delta4",
-                                    f"llm_12288x12288_sparsity{_s}_f16_delta4")
+    for _b in (2, 4, 8):
+        WORKLOADS[f"llm{_s}_delta{_b}"] = (f"llm{_s}", f"delta{_b}",
+                                           f"llm_12288x12288_sparsity{_s}_f16_delta{_b}")
 DEFAULT_WORKLOAD = "laplacian"
 
 
@@ -73,7 +74,8 @@ def kernel_source_sha(fmt: str) -> str:
     device header followed by the kernel's file)."""
     csrc = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("spmv_device.cuh", "spmv_delta.cu" if fmt == "delta4" else "spmv_csr.cu"):
+    for name in ("spmv_device.cuh",
+                 "spmv_delta.cu" if fmt.startswith("delta") else "spmv_csr.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -185,9 +187,10 @@ def oracle_call(m, fmt, frac):
     rows = max(1, min(m.n_rows, int(math.ceil(m.n_rows * frac))))
     rp = m.row_ptr[:rows + 1]
     ci, vals = m.col_idx[:rp[-1]], m.values[:rp[-1]]
-    if fmt == "delta4":
-        enc = oracle.delta_encode(m.n_cols, rp, ci, vals)
-        nbytes = (enc.n_entries * 2 + enc.n_entries // 2 + (rows + 1) * 4
+    if fmt.startswith("delta"):
+        bits = int(fmt[5:])
+        enc = oracle.delta_encode(m.n_cols, rp, ci, vals, bits=bits)
+        nbytes = (enc.n_entries * 2 + enc.n_entries * bits // 8 + (rows + 1) * 4
                   + m.n_cols * 2 + rows * 4)
         return rows, nbytes, int(rp[-1]), (lambda: oracle.delta_spmv(enc, m.x))
     nbytes = (int(rp[-1]) * (vals.dtype.itemsize + 4) + (rows + 1) * 4

@@ -6,7 +6,8 @@
  *   - CSR (row_ptr / col_idx / values), values fp32 or fp16; or
  *   - DELTA4: fp16 values with 4-bit column deltas packed eight to a 32-bit
  *     word, zero-valued padding entries where a gap does not fit in 4 bits,
- *     and CSR-like row pointers over the stored entries.
+ *     and CSR-like row pointers over the stored entries (DELTA2 / DELTA8:
+ *     the same with 2- or 8-bit deltas, 16 or 4 to a word).
  * x is fp32 for fp32 CSR and fp16 otherwise; y is always fp32 and every
  * product is accumulated in fp32.
  *
@@ -42,14 +43,14 @@
 extern "C" {
 #endif
 
-#define SPMV_ABI_VERSION 1
+#define SPMV_ABI_VERSION 2
 
 typedef enum spmv_status {
   SPMV_OK = 0,
   SPMV_ERR_INVALID_ARG = 1,      /* null pointer, negative size, bad enum   */
   SPMV_ERR_BAD_ROW_PTR = 2,      /* row_ptr[0] != 0, decreasing, or last != nnz */
   SPMV_ERR_COL_OUT_OF_RANGE = 3, /* a column (or decoded column) >= n_cols  */
-  SPMV_ERR_UNSORTED_OR_DUPLICATE_COLS = 4, /* DELTA4 needs increasing cols */
+  SPMV_ERR_UNSORTED_OR_DUPLICATE_COLS = 4, /* DELTA needs increasing cols  */
   SPMV_ERR_UNSUPPORTED = 5,      /* format / dtype combination not provided */
   SPMV_ERR_OUT_OF_MEMORY = 6,    /* host or device allocation failed        */
   SPMV_ERR_CUDA = 7,             /* a CUDA runtime call failed (no device…) */
@@ -62,8 +63,10 @@ typedef enum spmv_status {
 typedef enum spmv_dtype { SPMV_F32 = 0, SPMV_F16 = 1 } spmv_dtype;
 
 typedef enum spmv_format {
-  SPMV_FORMAT_CSR = 0,    /* [CSR] section 2.1                                */
-  SPMV_FORMAT_DELTA4 = 1  /* [MACKO] section 2.1, 4-bit deltas                */
+  SPMV_FORMAT_CSR = 0,     /* [CSR] section 2.1                               */
+  SPMV_FORMAT_DELTA4 = 1,  /* [MACKO] section 2.1, 4-bit deltas               */
+  SPMV_FORMAT_DELTA2 = 2,  /* the same format with 2-bit deltas ([MACKO] 3.3) */
+  SPMV_FORMAT_DELTA8 = 3   /* the same format with 8-bit deltas ([MACKO] 3.3) */
 } spmv_format;
 
 /* A CSR matrix in HOST memory ([CSR] section 2.1).
@@ -82,28 +85,33 @@ typedef struct spmv_csr {
   spmv_dtype value_dtype;
 } spmv_csr;
 
-/* A DELTA4 matrix in HOST memory ([MACKO] section 2.1), as produced by
- * spmv_convert. Encoding of each row, with the running column c starting at
- * 0 at the start of the row:
+/* A column-delta matrix in HOST memory ([MACKO] section 2.1), as produced by
+ * spmv_convert (4-bit deltas) or spmv_convert_bits (b = 2, 4 or 8 bits;
+ * [MACKO] section 3.3 lists the widths). With D = 2^b - 1 and P = 32 / b
+ * deltas per 32-bit word, each row is encoded, with the running column c
+ * starting at 0 at the start of the row:
  *   for each nonzero (in increasing column order) at column j:
- *     d = j - c; while d > 15 emit (+0.0, 15), c += 15, d -= 15;
+ *     d = j - c; while d > D emit (+0.0, D), c += D, d -= D;
  *     emit (value, d); c = j;
- *   then emit (+0.0, 0) until the row holds a multiple of 8 entries.
- * Entry e stores its value in values[e] and its 4-bit delta in bits
- * 4*(e%8)..4*(e%8)+3 of words[e/8]. row_ptr[r] is the index of the first
- * entry of row r (always a multiple of 8). A stored +0.0 (bits 0x0000) is
- * indistinguishable from padding; decoding drops every such entry. */
+ *   then emit (+0.0, 0) until the row holds a multiple of P entries.
+ * Entry e stores its value in values[e] and its delta in bits
+ * b*(e%P)..b*(e%P)+b-1 of words[e/P] (for b = 4: nibble e%8 of word e/8).
+ * row_ptr[r] is the index of the first entry of row r (always a multiple of
+ * P). A stored +0.0 (bits 0x0000) is indistinguishable from padding;
+ * decoding drops every such entry. */
 typedef struct spmv_delta {
   int32_t n_rows;
   int32_t n_cols;
   int64_t nnz;              /* nonzeros encoded (entries that are not padding) */
   int64_t n_entries;        /* stored entries, padding included              */
-  int64_t n_gap_pads;       /* padding entries inserted for gaps > 15        */
-  int64_t n_align_pads;     /* padding entries that round rows up to 8       */
+  int64_t n_gap_pads;       /* padding entries inserted for gaps > D         */
+  int64_t n_align_pads;     /* padding entries that round rows up to P       */
   int64_t n_explicit_zeros; /* input values equal to +0.0 (stored as such)   */
   uint16_t* values;         /* n_entries fp16 bit patterns                   */
-  uint32_t* words;          /* n_entries / 8 words of packed deltas          */
+  uint32_t* words;          /* n_entries / P words of packed deltas          */
   int64_t* row_ptr;         /* n_rows + 1 entry offsets                      */
+  int32_t delta_bits;       /* b: 2, 4 or 8 (0 is read as 4)                 */
+  int32_t reserved;
 } spmv_delta;
 
 /* Planner knobs ([SPGEMM] section 2.1.1 grouping; [MACKO] section 3.3
@@ -184,6 +192,10 @@ void spmv_plan_options_init(spmv_plan_options* opts);
  * UNSORTED_OR_DUPLICATE_COLS, UNSUPPORTED (fp32 values), OUT_OF_MEMORY. */
 spmv_status spmv_convert(const spmv_csr* csr, spmv_delta* out);
 
+/* As spmv_convert, with deltas of `bits` bits (2, 4 or 8; anything else:
+ * INVALID_ARG). */
+spmv_status spmv_convert_bits(const spmv_csr* csr, int32_t bits, spmv_delta* out);
+
 /* Free the arrays of a spmv_delta filled by spmv_convert and zero it. */
 void spmv_delta_free(spmv_delta* d);
 
@@ -207,9 +219,10 @@ spmv_status spmv_plan_create_ex(const spmv_csr* csr, spmv_format format,
                                 const spmv_plan_options* opts,
                                 spmv_plan** out);
 
-/* Build a DELTA4 plan directly from an already converted matrix (for
- * weights converted once ahead of time). Every stored entry's decoded column
- * must be < n_cols and row_ptr entries must be multiples of 8. */
+/* Build a column-delta plan directly from an already converted matrix (for
+ * weights converted once ahead of time), at its delta_bits. Every stored
+ * entry's decoded column must be < n_cols and row_ptr entries must be
+ * multiples of 32 / delta_bits. */
 spmv_status spmv_plan_create_delta(const spmv_delta* delta,
                                    const spmv_plan_options* opts,
                                    spmv_plan** out);

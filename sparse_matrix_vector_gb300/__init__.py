@@ -1,5 +1,6 @@
 """GB300-native sparse matrix-vector multiply y = A x (fp32 CSR, fp16 CSR and
-the 4-bit column-delta format) behind a C ABI, ``include/spmv.h``.
+the column-delta format with 2-, 4- or 8-bit deltas) behind a C ABI,
+``include/spmv.h``.
 
 The compiled library is ``libspmv_gb300.so`` next to this file (built by
 ``sparse_matrix_vector_gb300.build``). This package only marshals arguments.
@@ -12,5 +13,6 @@ from .api import (  # noqa: F401
     spmv_run_host, spmv_status_string,
 )
 from ._lib import (  # noqa: F401
-    SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4,
+    SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA4,
+    SPMV_FORMAT_DELTA8,
 )

@@ -15,7 +15,7 @@ c_i64 = ctypes.c_int64
 c_p = ctypes.c_void_p
 
 SPMV_F32, SPMV_F16 = 0, 1
-SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4 = 0, 1
+SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA8 = 0, 1, 2, 3
 
 STATUS_NAMES = {
     0: "SPMV_OK", 1: "SPMV_ERR_INVALID_ARG", 2: "SPMV_ERR_BAD_ROW_PTR",
@@ -36,7 +36,8 @@ class spmv_delta(ctypes.Structure):
     _fields_ = [("n_rows", c_i32), ("n_cols", c_i32), ("nnz", c_i64),
                 ("n_entries", c_i64), ("n_gap_pads", c_i64),
                 ("n_align_pads", c_i64), ("n_explicit_zeros", c_i64),
-                ("values", c_p), ("words", c_p), ("row_ptr", c_p)]
+                ("values", c_p), ("words", c_p), ("row_ptr", c_p),
+                ("delta_bits", c_i32), ("reserved", c_i32)]
 
 
 class spmv_plan_options(ctypes.Structure):
@@ -65,6 +66,8 @@ SIGNATURES = {
     "spmv_plan_options_init": (None, [ctypes.POINTER(spmv_plan_options)]),
     "spmv_convert": (ctypes.c_int, [ctypes.POINTER(spmv_csr),
                                     ctypes.POINTER(spmv_delta)]),
+    "spmv_convert_bits": (ctypes.c_int, [ctypes.POINTER(spmv_csr), c_i32,
+                                         ctypes.POINTER(spmv_delta)]),
     "spmv_delta_free": (None, [ctypes.POINTER(spmv_delta)]),
     "spmv_plan_inspect": (ctypes.c_int, [ctypes.POINTER(spmv_csr), ctypes.c_int,
                                          ctypes.POINTER(spmv_plan_options),

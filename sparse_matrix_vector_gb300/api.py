@@ -13,9 +13,11 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import _lib
-from ._lib import SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4
+from ._lib import (SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2,
+                   SPMV_FORMAT_DELTA4, SPMV_FORMAT_DELTA8)
 
-FORMATS = {"csr": SPMV_FORMAT_CSR, "delta4": SPMV_FORMAT_DELTA4}
+FORMATS = {"csr": SPMV_FORMAT_CSR, "delta4": SPMV_FORMAT_DELTA4,
+           "delta2": SPMV_FORMAT_DELTA2, "delta8": SPMV_FORMAT_DELTA8}
 
 
 class SpmvError(RuntimeError):
@@ -100,44 +102,49 @@ def spmv_abi_version() -> int:
 
 @dataclass
 class DeltaMatrix:
-    """A DELTA4 matrix copied out of the library (numpy arrays)."""
+    """A DELTA matrix (deltas of `bits` bits) copied out of the library
+    (numpy arrays)."""
     n_rows: int
     n_cols: int
     nnz: int
     row_ptr: np.ndarray   # int64[n_rows + 1]
     values: np.ndarray    # uint16[n_entries] (fp16 bit patterns)
-    words: np.ndarray     # uint32[n_entries / 8]
+    words: np.ndarray     # uint32[n_entries * bits / 32]
     n_gap_pads: int
     n_align_pads: int
     n_explicit_zeros: int
+    bits: int = 4
 
     @property
     def n_entries(self) -> int:
         return int(self.row_ptr[-1]) if self.row_ptr.size else 0
 
 
-def spmv_convert(row_ptr, col_idx, values, n_cols: int) -> DeltaMatrix:
-    """CSR (fp16 values) -> DELTA4 on the host, by the library's converter."""
+def spmv_convert(row_ptr, col_idx, values, n_cols: int, bits: int = 4) -> DeltaMatrix:
+    """CSR (fp16 values) -> DELTA with `bits`-bit deltas (2, 4 or 8) on the
+    host, by the library's converter (spmv_convert_bits)."""
     h = _host_csr(row_ptr, col_idx, values, n_cols)
     d = _lib.spmv_delta()
     lib = _lib.load()
-    _check(lib.spmv_convert(ctypes.byref(h.struct), ctypes.byref(d)),
-           "spmv_convert")
+    _check(lib.spmv_convert_bits(ctypes.byref(h.struct), int(bits), ctypes.byref(d)),
+           "spmv_convert_bits")
     try:
         n = int(d.n_entries)
+        b = int(d.delta_bits)
         rp = np.ctypeslib.as_array(ctypes.cast(d.row_ptr, ctypes.POINTER(ctypes.c_int64)),
                                    shape=(d.n_rows + 1,)).copy()
         if n:
             vals = np.ctypeslib.as_array(
                 ctypes.cast(d.values, ctypes.POINTER(ctypes.c_uint16)), shape=(n,)).copy()
             words = np.ctypeslib.as_array(
-                ctypes.cast(d.words, ctypes.POINTER(ctypes.c_uint32)), shape=(n // 8,)).copy()
+                ctypes.cast(d.words, ctypes.POINTER(ctypes.c_uint32)),
+                shape=(n * b // 32,)).copy()
         else:
             vals = np.zeros(0, np.uint16)
             words = np.zeros(0, np.uint32)
         return DeltaMatrix(int(d.n_rows), int(d.n_cols), int(d.nnz), rp, vals,
                            words, int(d.n_gap_pads), int(d.n_align_pads),
-                           int(d.n_explicit_zeros))
+                           int(d.n_explicit_zeros), b)
     finally:
         lib.spmv_delta_free(ctypes.byref(d))
 
@@ -218,7 +225,7 @@ def spmv_plan_create(row_ptr, col_idx, values, n_cols: int, format="csr",
 
 
 def spmv_plan_create_delta(delta: DeltaMatrix, options=None) -> Plan:
-    """Plan from an already converted DELTA4 matrix."""
+    """Plan from an already converted DELTA matrix."""
     rp = np.ascontiguousarray(delta.row_ptr, dtype=np.int64)
     vals = np.ascontiguousarray(delta.values, dtype=np.uint16)
     words = np.ascontiguousarray(delta.words, dtype=np.uint32)
@@ -229,7 +236,7 @@ def spmv_plan_create_delta(delta: DeltaMatrix, options=None) -> Plan:
                         n_explicit_zeros=delta.n_explicit_zeros,
                         values=vals.ctypes.data if vals.size else None,
                         words=words.ctypes.data if words.size else None,
-                        row_ptr=rp.ctypes.data)
+                        row_ptr=rp.ctypes.data, delta_bits=int(delta.bits))
     out = ctypes.c_void_p()
     opts = ctypes.byref(options) if options is not None else None
     _check(_lib.load().spmv_plan_create_delta(ctypes.byref(d), opts,

@@ -1,6 +1,6 @@
 """In-tree build of the C-ABI library ``libspmv_gb300.so`` for sm_103a.
 
-The translation units (host planner and converter, CSR kernel, DELTA4
+The translation units (host planner and converter, CSR kernel, DELTA
 kernel, allocation-free entry point) are compiled in parallel with nvcc and
 linked into one shared object next to this file.
 Usage: ``python -m sparse_matrix_vector_gb300.build`` or ``build_library()``.

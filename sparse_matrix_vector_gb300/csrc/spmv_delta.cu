@@ -21,8 +21,8 @@ namespace spmv {
 namespace {
 
 struct DeltaArgs {
-  const uint32_t* __restrict__ words;   // 8 nibbles per word
-  const __half* __restrict__ vals;      // 8 fp16 values per word, 16 bytes
+  const uint32_t* __restrict__ words;   // 32 / B deltas of B bits per word
+  const __half* __restrict__ vals;      // 32 / B fp16 values per word
   const __half* __restrict__ x;
   float* __restrict__ y;
   const int4* __restrict__ units;       // {row | FIRST | LAST, wb, we, column base}
@@ -36,15 +36,27 @@ struct DeltaArgs {
   int n_cols;
 };
 
-// Shared-memory stage of one DELTA4 unit: the warps' starting columns, the
-// unit's words (aligned out to 4 words) and its values (16 bytes per word).
+// Shared-memory stage of one unit of deltas of B bits: the warps' starting
+// columns, the unit's words (aligned out to 4 words) and its values (32 / B
+// halves per word, aligned out to 16 bytes: 2 words when B = 8).
+template <int B>
 struct DeltaStage {
+  static constexpr int kPerWord = 32 / B;
+  static constexpr int kUnitWords = delta_unit_words(B);
+  static constexpr int kValAlign = kPerWord * 2 >= 16 ? 1 : 16 / (kPerWord * 2);  // words
   static constexpr int kBaseBytes = kDeltaWarps * 4;
-  static constexpr int kWordBytes = (kDeltaUnitWords + 8) * 4;
-  static constexpr int kValBytes = kDeltaUnitWords * 16;
+  static constexpr int kWordBytes = (kUnitWords + 8) * 4;
+  static constexpr int kValBytes = (kUnitWords + kValAlign) * kPerWord * 2;
   static constexpr int kBytes = kBaseBytes + kWordBytes + kValBytes;
+  static_assert(kBaseBytes % 16 == 0 && kWordBytes % 16 == 0 && kValBytes % 16 == 0,
+                "stage regions must stay 16-byte aligned");
 };
-static_assert(DeltaStage::kBaseBytes % 16 == 0, "stage regions must stay 16-byte aligned");
+
+// A word's values: 32 / B halves.
+template <int B> struct WordVals;
+template <> struct WordVals<4> { uint4 v; };
+template <> struct WordVals<8> { uint2 v; };
+template <> struct WordVals<2> { uint4 v0, v1; };
 
 // Copy x (n halves) into shared memory with `nthreads` threads, 16 bytes at a
 // time when x is 16-byte aligned (no barrier: the caller synchronises).
@@ -60,10 +72,20 @@ __device__ __forceinline__ void copy_x_half(uint16_t* xs, const __half* x, int n
   for (int i = done + threadIdx.x; i < n; i += nthreads) xs[i] = __ldg(src + i);
 }
 
-// Sum of the eight 4-bit fields of w (<= 120).
-__device__ __forceinline__ int nibble_sum(uint32_t w) {
-  const uint32_t b = (w & 0x0F0F0F0Fu) + ((w >> 4) & 0x0F0F0F0Fu);
-  return (int)((b * 0x01010101u) >> 24);
+// Sum of the 32 / B fields of w (at most 48, 120 or 1020).
+template <int B>
+__device__ __forceinline__ int field_sum(uint32_t w) {
+  if (B == 4) {
+    const uint32_t b = (w & 0x0F0F0F0Fu) + ((w >> 4) & 0x0F0F0F0Fu);
+    return (int)((b * 0x01010101u) >> 24);
+  } else if (B == 8) {
+    const uint32_t h = (w & 0x00FF00FFu) + ((w >> 8) & 0x00FF00FFu);
+    return (int)((h & 0xFFFFu) + (h >> 16));
+  } else {
+    const uint32_t g = (w & 0x33333333u) + ((w >> 2) & 0x33333333u);
+    const uint32_t b = (g & 0x0F0F0F0Fu) + ((g >> 4) & 0x0F0F0F0Fu);
+    return (int)((b * 0x01010101u) >> 24);
+  }
 }
 
 // fp32 acc + a * x for fp16 a and x: the product is exact in fp32, so one
@@ -73,55 +95,86 @@ __device__ __forceinline__ float fma_f16(float acc, uint16_t a, uint16_t x) {
   return acc;
 }
 
-// Decode one word (8 entries) whose first entry follows column `col`, with x
-// read through L1. The eight columns come from byte-wise prefix sums of the
-// nibbles: with lo / hi the even / odd nibbles spread into bytes, byte j of
-// P = (lo + hi) * 0x01010101 is the sum of nibbles 0..2j+1 (at most 120, so
-// no carries), and byte j of P - hi the sum of nibbles 0..2j; each column is
-// one byte extract and one address, and each entry one mixed fma.
-__device__ __forceinline__ void decode_word_l1(uint32_t w, const uint4 v, int& col,
-                                               const __half* xg, float& acc0, float& acc1) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
-  const uint32_t P = (lo + hi) * 0x01010101u;
-  const uint32_t Q = P - hi;
-  const uint16_t* xb = reinterpret_cast<const uint16_t*>(xg) + col;
-  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t c0 = __byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
-    const uint32_t c1 = __byte_perm(P, 0u, 0x4440u + (uint32_t)j);
-    const uint16_t x0 = __ldg(xb + c0);
-    const uint16_t x1 = __ldg(xb + c1);
-    acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), x0);
-    acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), x1);
-  }
-  col += (int)(P >> 24);
+// x at column col + off, from shared memory (XS) or through L1 (xb = x + col).
+template <bool XS>
+__device__ __forceinline__ uint16_t gx(const uint16_t* xs, const uint16_t* xb, int col,
+                                       uint32_t off) {
+  return XS ? xs[col + (int)off] : __ldg(xb + off);
 }
 
-// decode_word_l1 with x from the shared-memory copy.
-__device__ __forceinline__ void decode_word_smem(uint32_t w, const uint4 v, int& col,
-                                                 const uint16_t* xs, float& acc0,
-                                                 float& acc1) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
-  const uint32_t P = (lo + hi) * 0x01010101u;
-  const uint32_t Q = P - hi;
-  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+// Decode one word whose first entry follows column `col`: the columns come
+// from prefix sums of the fields computed several fields at a time inside
+// the register (SWAR), and each entry is one gather and one mixed fma.
+//  B = 4: with lo / hi the even / odd nibbles spread into bytes, byte j of
+//         P = (lo + hi) * 0x01010101 is the sum of nibbles 0..2j+1 (at most
+//         120, no carries) and byte j of P - hi the sum of nibbles 0..2j.
+//  B = 8: the same with bytes spread into 16-bit halves (at most 1020).
+//  B = 2: adjacent fields are first added into nibbles (g); the nibble
+//         prefix as for B = 4 gives the sums through fields 4i+1 and 4i+3,
+//         and fields 4i and 4i+2 take their upper neighbour back off.
+template <int B, bool XS>
+__device__ __forceinline__ void decode_word(uint32_t w, const WordVals<B>& v, int& col,
+                                            const uint16_t* xs, const __half* x,
+                                            float& acc0, float& acc1) {
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x) + (XS ? 0 : col);
+  if constexpr (B == 4) {
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t P = (lo + hi) * 0x01010101u;
+    const uint32_t Q = P - hi;
+    const uint32_t vw[4] = {v.v.x, v.v.y, v.v.z, v.v.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int c0 = col + (int)__byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
-    const int c1 = col + (int)__byte_perm(P, 0u, 0x4440u + (uint32_t)j);
-    acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), xs[c0]);
-    acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), xs[c1]);
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t o0 = __byte_perm(Q, 0u, 0x4440u + (uint32_t)j);
+      const uint32_t o1 = __byte_perm(P, 0u, 0x4440u + (uint32_t)j);
+      acc0 = fma_f16(acc0, (uint16_t)(vw[j] & 0xFFFFu), gx<XS>(xs, xb, col, o0));
+      acc1 = fma_f16(acc1, (uint16_t)(vw[j] >> 16), gx<XS>(xs, xb, col, o1));
+    }
+    col += (int)(P >> 24);
+  } else if constexpr (B == 8) {
+    const uint32_t lo = w & 0x00FF00FFu;
+    const uint32_t hi = (w >> 8) & 0x00FF00FFu;
+    const uint32_t P = (lo + hi) * 0x00010001u;
+    const uint32_t Q = P - hi;
+    acc0 = fma_f16(acc0, (uint16_t)(v.v.x & 0xFFFFu), gx<XS>(xs, xb, col, Q & 0xFFFFu));
+    acc1 = fma_f16(acc1, (uint16_t)(v.v.x >> 16), gx<XS>(xs, xb, col, P & 0xFFFFu));
+    acc0 = fma_f16(acc0, (uint16_t)(v.v.y & 0xFFFFu), gx<XS>(xs, xb, col, Q >> 16));
+    acc1 = fma_f16(acc1, (uint16_t)(v.v.y >> 16), gx<XS>(xs, xb, col, P >> 16));
+    col += (int)(P >> 16);
+  } else {
+    const uint32_t g = (w & 0x33333333u) + ((w >> 2) & 0x33333333u);
+    const uint32_t lo = g & 0x0F0F0F0Fu;
+    const uint32_t hi = (g >> 4) & 0x0F0F0F0Fu;
+    const uint32_t P = (lo + hi) * 0x01010101u;  // byte i: fields 0..4i+3
+    const uint32_t Q = P - hi;                   // byte i: fields 0..4i+1
+    const uint32_t vw[8] = {v.v0.x, v.v0.y, v.v0.z, v.v0.w, v.v1.x, v.v1.y, v.v1.z, v.v1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t o1 = __byte_perm(Q, 0u, 0x4440u + (uint32_t)i);
+      const uint32_t o3 = __byte_perm(P, 0u, 0x4440u + (uint32_t)i);
+      const uint32_t o0 = o1 - ((w >> (8 * i + 2)) & 3u);
+      const uint32_t o2 = o3 - ((w >> (8 * i + 6)) & 3u);
+      acc0 = fma_f16(acc0, (uint16_t)(vw[2 * i] & 0xFFFFu), gx<XS>(xs, xb, col, o0));
+      acc1 = fma_f16(acc1, (uint16_t)(vw[2 * i] >> 16), gx<XS>(xs, xb, col, o1));
+      acc0 = fma_f16(acc0, (uint16_t)(vw[2 * i + 1] & 0xFFFFu), gx<XS>(xs, xb, col, o2));
+      acc1 = fma_f16(acc1, (uint16_t)(vw[2 * i + 1] >> 16), gx<XS>(xs, xb, col, o3));
+    }
+    col += (int)(P >> 24);
   }
-  col += (int)(P >> 24);
 }
 
-// Thread 0: start the TMA copies of DELTA4 unit u (descriptor d) into a stage.
+// Values of word j of a stage.
+template <int B>
+__device__ __forceinline__ WordVals<B> load_vals(const unsigned char* s_vals, int j) {
+  return reinterpret_cast<const WordVals<B>*>(s_vals)[j];
+}
+
+// Thread 0: start the TMA copies of unit u (descriptor d) into a stage.
+template <int B>
 __device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* stage,
                                            uint64_t* bar, int4* desc, int u, const int4 d,
                                            uint64_t pol) {
+  using St = DeltaStage<B>;
   if (u < 0) {
     *desc = make_int4(-1, 0, 0, 0);
     mbar_arrive(bar);
@@ -129,18 +182,23 @@ __device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* st
   }
   *desc = d;
   const int wb = d.y, we = d.z;
-  const int wa = wb & ~3;
-  const uint32_t nwb = (uint32_t)(((we + 3) & ~3) - wa) * 4u;
-  const uint32_t nvb = (uint32_t)(we - wb) * 16u;
-  if (nvb == 0) {
+  if (we == wb) {
     mbar_arrive(bar);
     return;
   }
-  mbar_arrive_expect_tx(bar, DeltaStage::kBaseBytes + nwb + nvb);
-  bulk_g2s(stage, a.warp_base + (size_t)u * kDeltaWarps, DeltaStage::kBaseBytes, bar, pol);
-  bulk_g2s(stage + DeltaStage::kBaseBytes, a.words + wa, nwb, bar, pol);
-  bulk_g2s(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes, a.vals + (size_t)wb * 8,
-           nvb, bar, pol);
+  // bulk copies start on 16-byte boundaries and move multiples of 16 bytes:
+  // words from a multiple of 4, values from a multiple of kValAlign words
+  // (the device arrays carry a zero tail for the rounding up)
+  constexpr int VA = St::kValAlign;
+  const int wa = wb & ~3;
+  const uint32_t nwb = (uint32_t)(((we + 3) & ~3) - wa) * 4u;
+  const int va = wb & ~(VA - 1);
+  const uint32_t nvb = (uint32_t)(((we + VA - 1) & ~(VA - 1)) - va) * (uint32_t)(St::kPerWord * 2);
+  mbar_arrive_expect_tx(bar, St::kBaseBytes + nwb + nvb);
+  bulk_g2s(stage, a.warp_base + (size_t)u * kDeltaWarps, St::kBaseBytes, bar, pol);
+  bulk_g2s(stage + St::kBaseBytes, a.words + wa, nwb, bar, pol);
+  bulk_g2s(stage + St::kBaseBytes + St::kWordBytes, a.vals + (size_t)va * St::kPerWord, nvb,
+           bar, pol);
 }
 
 // Thread 0, at the end of this CTA's piece of a row split into units: as
@@ -192,7 +250,7 @@ __device__ __forceinline__ void delta_publish(const DeltaArgs& a, int row, bool 
 #ifndef SPMV_DELTA_PC_XS_GROUPS
 #define SPMV_DELTA_PC_XS_GROUPS 3
 #endif
-static_assert(kDeltaMaxLaneWords == 2, "the decode packs two words per lane");
+static_assert(kDeltaMaxLaneWords == 2, "the decode packs at most two words per lane");
 
 template <bool XS>
 struct PcCfg {
@@ -204,10 +262,11 @@ struct PcCfg {
   static constexpr int kMinBlocks = XS ? 2 : 5;
 };
 
-template <bool XS>
+template <int B, bool XS>
 __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
-    delta4_pc_kernel(const DeltaArgs a) {
+    delta_pc_kernel(const DeltaArgs a) {
   using C = PcCfg<XS>;
+  using St = DeltaStage<B>;
   constexpr int G = C::kGroups, S = C::kStages;
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_full[G][S];
@@ -234,7 +293,7 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
       const int v = blockIdx.x * G + g;
       const int u_begin = __ldg(a.cta_first + v);
       const int n_units = __ldg(a.cta_first + v + 1) - u_begin;
-      unsigned char* stages = dyn_smem + (size_t)g * S * DeltaStage::kBytes;
+      unsigned char* stages = dyn_smem + (size_t)g * S * St::kBytes;
       const uint64_t pol = policy_evict_first();
       int issued = 0;
       bool ok = true;
@@ -244,8 +303,8 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
           ok = false;
           break;
         }
-        issue_unit(a, stages + s * DeltaStage::kBytes, &s_full[g][s], &s_desc[g][s],
-                   u_begin + i, __ldg(a.units + u_begin + i), pol);
+        issue_unit<B>(a, stages + s * St::kBytes, &s_full[g][s], &s_desc[g][s], u_begin + i,
+                      __ldg(a.units + u_begin + i), pol);
         issued = i + 1;
         if (issued == S) pdl_launch_dependents();
       }
@@ -263,9 +322,8 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
   // consumers; plan-owned data only above, x and y below
   pdl_wait();
   const int g = warp / kDeltaWarps, lw = warp % kDeltaWarps;
-  const int gt = tid - g * kDeltaThreads;  // thread index within the group
   const uint16_t* xs =
-      reinterpret_cast<const uint16_t*>(dyn_smem + (size_t)G * S * DeltaStage::kBytes);
+      reinterpret_cast<const uint16_t*>(dyn_smem + (size_t)G * S * St::kBytes);
   if (XS) {
     copy_x_half(const_cast<uint16_t*>(xs), a.x, a.n_cols, G * kDeltaThreads);
     asm volatile("bar.sync 1, %0;" ::"n"(G * kDeltaThreads) : "memory");  // consumers only
@@ -273,7 +331,7 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
   const int v = blockIdx.x * G + g;
   const int u_begin = __ldg(a.cta_first + v);
   const int n_units = __ldg(a.cta_first + v + 1) - u_begin;
-  const unsigned char* stages = dyn_smem + (size_t)g * S * DeltaStage::kBytes;
+  const unsigned char* stages = dyn_smem + (size_t)g * S * St::kBytes;
   float acc0 = 0.f, acc1 = 0.f;  // this thread's share of the current row piece
   int piece_wb0 = -1;
   bool piece_first = false;
@@ -285,7 +343,7 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
       break;
     }
     const int4 d = s_desc[g][s];
-    const unsigned char* stage = stages + s * DeltaStage::kBytes;
+    const unsigned char* stage = stages + s * St::kBytes;
     const uint32_t rw = (uint32_t)d.x;
     const int row = (int)(rw & kUnitRowMask);
     const int wb = d.y, n_w = d.z - d.y;
@@ -295,24 +353,24 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
     }
     const int* s_base = reinterpret_cast<const int*>(stage);
     const uint32_t* s_words =
-        reinterpret_cast<const uint32_t*>(stage + DeltaStage::kBaseBytes) + (wb & 3);
-    const uint4* s_vals =
-        reinterpret_cast<const uint4*>(stage + DeltaStage::kBaseBytes + DeltaStage::kWordBytes);
+        reinterpret_cast<const uint32_t*>(stage + St::kBaseBytes) + (wb & 3);
+    const unsigned char* s_vals = stage + St::kBaseBytes + St::kWordBytes +
+                                  (wb & (St::kValAlign - 1)) * St::kPerWord * 2;
     // Lane l of warp w takes words 32 LW w + 32 q + l, q < LW: consecutive
     // lanes read consecutive words and values (conflict-free shared-memory
     // loads). The column before word q of a lane is the warp's starting column
-    // plus the nibbles of every earlier word of the warp's segment: one 5-step
-    // scan of both words' nibble sums packed in 16-bit halves (each at most
-    // 32 * 120) gives both.
-    const int lg = (int)((rw >> kUnitLgShift) & 1u);  // log2(words per lane): 0 or 1
+    // plus the fields of every earlier word of the warp's segment: one 5-step
+    // scan of both words' field sums packed in 16-bit halves (each at most
+    // 32 * 1020) gives both. A unit of 2-bit deltas has one word per lane.
+    const int lg = St::kUnitWords > kDeltaThreads ? (int)((rw >> kUnitLgShift) & 1u) : 0;
     const int wseg = lw << (5 + lg);                  // first word of the warp's segment
     const int j0 = wseg + lane, j1 = j0 + 32;
     const bool in0 = j0 < n_w, in1 = lg && j1 < n_w;
     const uint32_t w0 = in0 ? s_words[j0] : 0u;
     const uint32_t w1 = in1 ? s_words[j1] : 0u;
-    const uint4 v0 = in0 ? s_vals[j0] : make_uint4(0, 0, 0, 0);
-    const uint4 v1 = in1 ? s_vals[j1] : make_uint4(0, 0, 0, 0);
-    const int ns0 = nibble_sum(w0), ns1 = nibble_sum(w1);
+    const WordVals<B> v0 = in0 ? load_vals<B>(s_vals, j0) : WordVals<B>{};
+    const WordVals<B> v1 = in1 ? load_vals<B>(s_vals, j1) : WordVals<B>{};
+    const int ns0 = field_sum<B>(w0), ns1 = field_sum<B>(w1);
     const int base = s_base[lw];
     __syncwarp();
     if (lane == 0) mbar_arrive(&s_empty[g][s]);  // this warp is done with the stage
@@ -326,17 +384,11 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
     const int total0 = __shfl_sync(0xffffffffu, incl0, 31);
     if (in0) {
       int col = base + incl0 - ns0;  // column before word j0's first entry
-      if (XS)
-        decode_word_smem(w0, v0, col, xs, acc0, acc1);
-      else
-        decode_word_l1(w0, v0, col, a.x, acc0, acc1);
+      decode_word<B, XS>(w0, v0, col, xs, a.x, acc0, acc1);
     }
     if (in1) {
       int col = base + total0 + incl1 - ns1;  // column before word j1's first entry
-      if (XS)
-        decode_word_smem(w1, v1, col, xs, acc0, acc1);
-      else
-        decode_word_l1(w1, v1, col, a.x, acc0, acc1);
+      decode_word<B, XS>(w1, v1, col, xs, a.x, acc0, acc1);
     }
     const bool last = (rw & kUnitLast) != 0;
     if (last || i == n_units - 1) {  // row ends, or this group's share does
@@ -361,20 +413,31 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
   }
 }
 
-const void* delta_entry(bool xs) {
-  return xs ? reinterpret_cast<const void*>(&delta4_pc_kernel<true>)
-            : reinterpret_cast<const void*>(&delta4_pc_kernel<false>);
+template <int B>
+const void* delta_entry_b(bool xs) {
+  return xs ? reinterpret_cast<const void*>(&delta_pc_kernel<B, true>)
+            : reinterpret_cast<const void*>(&delta_pc_kernel<B, false>);
+}
+
+const void* delta_entry(int bits, bool xs) {
+  return bits == 2 ? delta_entry_b<2>(xs) : bits == 8 ? delta_entry_b<8>(xs) : delta_entry_b<4>(xs);
+}
+
+template <int B>
+size_t stages_bytes_b(bool x_smem) {
+  return x_smem ? (size_t)PcCfg<true>::kGroups * PcCfg<true>::kStages * DeltaStage<B>::kBytes
+                : (size_t)PcCfg<false>::kGroups * PcCfg<false>::kStages * DeltaStage<B>::kBytes;
 }
 
 }  // namespace
 
-int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget) {
-  return occupancy_within(delta_entry(x_smem), delta_block(x_smem), dyn_smem, budget);
+int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem, size_t budget) {
+  return occupancy_within(delta_entry(bits, x_smem), delta_block(x_smem), dyn_smem, budget);
 }
 
-size_t delta_stages_bytes(bool x_smem) {
-  return x_smem ? (size_t)PcCfg<true>::kGroups * PcCfg<true>::kStages * DeltaStage::kBytes
-                : (size_t)PcCfg<false>::kGroups * PcCfg<false>::kStages * DeltaStage::kBytes;
+size_t delta_stages_bytes(int bits, bool x_smem) {
+  return bits == 2 ? stages_bytes_b<2>(x_smem)
+                   : bits == 8 ? stages_bytes_b<8>(x_smem) : stages_bytes_b<4>(x_smem);
 }
 
 int delta_groups(bool x_smem) { return x_smem ? PcCfg<true>::kGroups : PcCfg<false>::kGroups; }
@@ -383,10 +446,10 @@ int delta_block(bool x_smem) { return x_smem ? PcCfg<true>::kThreads : PcCfg<fal
 
 size_t delta_x_smem_bytes(int n_cols) { return ((size_t)n_cols + 8) / 8 * 16; }
 
-int delta_set_smem_limit(size_t dyn) {
+int delta_set_smem_limit(int bits, size_t dyn) {
   if (dyn == 0) return 0;
   for (bool xs : {false, true})
-    if (cudaFuncSetAttribute(delta_entry(xs), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(delta_entry(bits, xs), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn) != cudaSuccess)
       return -1;
   return 0;
@@ -409,8 +472,8 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.status = p.status;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
-  return launch_pdl(delta_entry(p.x_smem), p.grid, delta_block(p.x_smem), p.dyn_smem, stream,
-                    args);
+  return launch_pdl(delta_entry(p.delta_bits, p.x_smem), p.grid, delta_block(p.x_smem),
+                    p.dyn_smem, stream, args);
 }
 
 }  // namespace spmv

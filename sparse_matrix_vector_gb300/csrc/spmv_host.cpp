@@ -1,12 +1,13 @@
-// Host half of the library: argument validation, the DELTA4 converter, the
+// Host half of the library: argument validation, the DELTA converter, the
 // row-binning planner, plan lifetime and the run entry points.
 //
 // Sources (web pages, by title and section):
 //   "CUDA CSR SpMV optimisation" (codechina.net), 2.1: CSR arrays and the
 //     row sum that defines y; 2.2: upload once, then launch by format.
 //   "MACKO-SpMV" (maplevalley.com.cn), 2.1: delta coding, zero padding for
-//     gaps that do not fit 4 bits, 8 nibbles per 32-bit word, row alignment;
-//     3.3: splitting long rows ("dynamic scheduling").
+//     gaps that do not fit the delta field, the fields packed into 32-bit
+//     words, row alignment; the 2-, 4- and 8-bit field widths; 3.3:
+//     splitting long rows ("dynamic scheduling").
 //   "Hash-based multi-phase SpGEMM" (mlqm.cn), 2.1.1 and 2.2: rows grouped by
 //     work into bins handled by partial-warp, warp and block-per-row
 //     kernels; 5.2: batching of tiny rows.
@@ -35,7 +36,7 @@ constexpr int64_t kMaxIndex = (int64_t)INT32_MAX - 4096;
 // costs a copy per CTA and, for the LLM shapes, a third of the CTAs per SM,
 // and was measured slower on GB300 than L1-resident gathers.
 constexpr size_t kXsAutoBytes = 0;
-// DELTA4: the producer / consumer kernel shares one shared-memory copy of x
+// DELTA: the producer / consumer kernel shares one shared-memory copy of x
 // among three groups of warps; up to 32 KB of x (16,384 columns) two such
 // CTAs still fit an SM, and gathers from shared memory beat L1 there
 // (12288-column LLM matrices, 30/50/70/90%: 0.47/0.44/0.40/0.27 of HBM peak
@@ -49,7 +50,16 @@ size_t dtype_size(spmv_dtype t) { return t == SPMV_F16 ? 2 : 4; }
 
 bool valid_dtype(int t) { return t == SPMV_F32 || t == SPMV_F16; }
 bool valid_format(int f) {
-  return f == SPMV_FORMAT_CSR || f == SPMV_FORMAT_DELTA4;
+  return f == SPMV_FORMAT_CSR || f == SPMV_FORMAT_DELTA4 || f == SPMV_FORMAT_DELTA2 ||
+         f == SPMV_FORMAT_DELTA8;
+}
+
+int32_t format_delta_bits(int f) {
+  return f == SPMV_FORMAT_DELTA2 ? 2 : f == SPMV_FORMAT_DELTA8 ? 8 : 4;
+}
+
+spmv_format delta_format(int32_t bits) {
+  return bits == 2 ? SPMV_FORMAT_DELTA2 : bits == 8 ? SPMV_FORMAT_DELTA8 : SPMV_FORMAT_DELTA4;
 }
 
 // Structure checks shared by every entry point that takes a CSR matrix.
@@ -78,17 +88,21 @@ spmv_status validate_csr(const spmv_csr* m, bool need_sorted) {
   return SPMV_OK;
 }
 
-// ------------------------------------------------------------ DELTA4 codec
-constexpr int kDeltaCap = 15;   // largest 4-bit code
-constexpr int kRowAlign = 8;    // entries per packed word
+// ------------------------------------------------------------ DELTA codec
+// Deltas of b bits (2, 4 or 8): codes 0..2^b-1, 32/b to a word.
+inline bool valid_delta_bits(int32_t b) { return b == 2 || b == 4 || b == 8; }
+inline int64_t delta_cap(int32_t b) { return ((int64_t)1 << b) - 1; }
+inline int64_t delta_per_word(int32_t b) { return 32 / b; }
+inline int32_t delta_bits_of(const spmv_delta* d) { return d->delta_bits ? d->delta_bits : 4; }
 
-// Stored entries of one row under the encoding of the header comment.
-int64_t delta_row_entries(const int32_t* cols, int32_t len, int64_t* gaps) {
+// Stored entries of one row (before row alignment) under the encoding of
+// the header comment.
+int64_t delta_row_entries(const int32_t* cols, int32_t len, int64_t cap, int64_t* gaps) {
   int64_t n = 0, c = 0;
   for (int32_t k = 0; k < len; ++k) {
     int64_t gap = (int64_t)cols[k] - c;
-    if (gap > kDeltaCap) {
-      int64_t pads = (gap - 1) / kDeltaCap;
+    if (gap > cap) {
+      int64_t pads = (gap - 1) / cap;
       n += pads;
       *gaps += pads;
     }
@@ -98,10 +112,24 @@ int64_t delta_row_entries(const int32_t* cols, int32_t len, int64_t* gaps) {
   return n;
 }
 
-inline void emit(uint16_t* vals, uint32_t* words, int64_t e, uint16_t bits,
+inline void emit(uint16_t* vals, uint32_t* words, int64_t e, int32_t b, uint16_t bits,
                  uint32_t code) {
+  const int64_t per = delta_per_word(b);
   vals[e] = bits;
-  words[e >> 3] |= code << (4 * (uint32_t)(e & 7));
+  words[e / per] |= code << ((uint32_t)b * (uint32_t)(e % per));
+}
+
+// Bytes the format stores: values, packed deltas, row pointers (int32 on
+// the device).
+inline int64_t delta_matrix_bytes(const spmv_delta& d) {
+  const int32_t b = delta_bits_of(&d);
+  return d.n_entries * 2 + d.n_entries * b / 8 + ((int64_t)d.n_rows + 1) * 4;
+}
+
+// Delta of stored entry e.
+inline uint32_t delta_at(const uint32_t* words, int64_t e, int32_t b) {
+  const int64_t per = delta_per_word(b);
+  return (words[e / per] >> ((uint32_t)b * (uint32_t)(e % per))) & (uint32_t)delta_cap(b);
 }
 
 }  // namespace
@@ -345,6 +373,11 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
   out->splits.clear();
   out->n_chunks = 0;
   const int64_t* rp = d->row_ptr;
+  const int32_t bits = delta_bits_of(d);
+  const int64_t per_word = 32 / bits;  // entries per word
+  const uint32_t cap = (1u << bits) - 1u;
+  const int64_t unit_words = delta_unit_words(bits);
+  const int max_lw = (int)(unit_words / kDeltaThreads);  // words per lane at most
   // weight of a unit: its entries, plus 8 for the row it starts
   const int64_t total_w = d->n_entries + 8 * (int64_t)d->n_rows;
   constexpr int64_t kMinShare = 4096;
@@ -357,12 +390,12 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
     out->row_split.assign((size_t)d->n_rows, -1);
     out->cta_first.push_back(0);
     for (int32_t r = 0; r < d->n_rows; ++r) {
-      const int64_t w0 = rp[r] >> 3, w1 = rp[r + 1] >> 3, nw = w1 - w0;
+      const int64_t w0 = rp[r] / per_word, w1 = rp[r + 1] / per_word, nw = w1 - w0;
       // words per lane: the least that fits the row in one unit, else the most
       uint32_t lg = 0;
-      while ((1 << lg) < kDeltaMaxLaneWords && nw > (int64_t)kDeltaThreads << lg) ++lg;
+      while ((1 << lg) < max_lw && nw > (int64_t)kDeltaThreads << lg) ++lg;
       const int64_t warp_words = (int64_t)32 << lg;
-      const int64_t n_u = std::max<int64_t>(1, (nw + kDeltaUnitWords - 1) / kDeltaUnitWords);
+      const int64_t n_u = std::max<int64_t>(1, (nw + unit_words - 1) / unit_words);
       const int64_t per = n_u > 1 ? (nw + n_u - 1) / n_u : std::max<int64_t>(nw, 1);
       if (n_u > 1) {
         if (out->n_chunks + n_u > kMaxIndex) return SPMV_ERR_TOO_LARGE;
@@ -371,7 +404,7 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
         out->n_chunks += n_u;
         info->rows_per_bin[3] += 1;
       } else {
-        info->rows_per_bin[nw * 8 > 256 ? 2 : (nw * 8 > 8 ? 1 : 0)] += 1;
+        info->rows_per_bin[nw * per_word > 256 ? 2 : (nw * per_word > 8 ? 1 : 0)] += 1;
       }
       int64_t col = 0;  // running column of the row, before word w
       int64_t w = w0;
@@ -387,7 +420,7 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
           const int64_t seg = std::min(ub + (int64_t)wi * warp_words, ue);
           for (; w < seg; ++w) {
             const uint32_t word = d->words[w];
-            for (int q = 0; q < 8; ++q) col += (word >> (4 * q)) & 0xFu;
+            for (int q = 0; q < per_word; ++q) col += (word >> (bits * q)) & cap;
           }
           if (col > INT32_MAX) return SPMV_ERR_TOO_LARGE;
           out->warp_base.push_back((int32_t)col);
@@ -396,7 +429,7 @@ spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out
                                (lg << kUnitLgShift);
         out->units.push_back({(int32_t)((uint32_t)r | flags), (int32_t)ub, (int32_t)ue,
                               out->warp_base[out->warp_base.size() - kDeltaWarps]});
-        cum += (ue - ub) * 8 + (k == 0 ? 8 : 0);
+        cum += (ue - ub) * per_word + (k == 0 ? 8 : 0);
       }
     }
     while ((int)out->cta_first.size() <= G) out->cta_first.push_back((int32_t)out->units.size());
@@ -605,17 +638,20 @@ spmv_status validate_delta(const spmv_delta* d, int64_t* nnz_out) {
   if (d->n_rows < 0 || d->n_cols < 0 || d->n_entries < 0 || !d->row_ptr)
     return SPMV_ERR_INVALID_ARG;
   if (d->n_entries > 0 && (!d->values || !d->words)) return SPMV_ERR_INVALID_ARG;
-  if (d->n_entries > kMaxIndex || (d->n_entries & 7)) {
+  const int32_t b = delta_bits_of(d);
+  if (!valid_delta_bits(b)) return SPMV_ERR_INVALID_ARG;
+  const int64_t per = delta_per_word(b);
+  if (d->n_entries > kMaxIndex || (d->n_entries % per)) {
     return d->n_entries > kMaxIndex ? SPMV_ERR_TOO_LARGE : SPMV_ERR_BAD_ROW_PTR;
   }
   const int64_t* rp = d->row_ptr;
   if (rp[0] != 0 || rp[d->n_rows] != d->n_entries) return SPMV_ERR_BAD_ROW_PTR;
   int64_t nnz = 0;
   for (int32_t r = 0; r < d->n_rows; ++r) {
-    if (rp[r + 1] < rp[r] || (rp[r] & 7)) return SPMV_ERR_BAD_ROW_PTR;
+    if (rp[r + 1] < rp[r] || (rp[r] % per)) return SPMV_ERR_BAD_ROW_PTR;
     int64_t c = 0;
     for (int64_t e = rp[r]; e < rp[r + 1]; ++e) {
-      c += (d->words[e >> 3] >> (4 * (e & 7))) & 0xFu;
+      c += delta_at(d->words, e, b);
       if (d->values[e] != 0) ++nnz;
     }
     if (rp[r + 1] > rp[r] && c >= d->n_cols) return SPMV_ERR_COL_OUT_OF_RANGE;
@@ -628,15 +664,19 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   spmv_status s;
   spmv_plan_info& info = p->info;
   if (d->n_rows > (int32_t)kUnitRowMask) return SPMV_ERR_TOO_LARGE;
+  // the kernel is chosen by the width the matrix was encoded with; the
+  // plan's format code must name the same width
+  p->delta_bits = delta_bits_of(d);
+  if (p->format != delta_format(p->delta_bits)) return SPMV_ERR_INVALID_ARG;
   if ((s = bind_device(p)) != SPMV_OK) return s;
   const size_t xbytes = (size_t)d->n_cols * 2;
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
             : o.x_smem == -1 ? xbytes <= kXsAutoBytesDelta : false;
   p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
-                delta_stages_bytes(p->x_smem);
-  if (delta_set_smem_limit(p->dyn_smem) != 0) return SPMV_ERR_CUDA;
+                delta_stages_bytes(p->delta_bits, p->x_smem);
+  if (delta_set_smem_limit(p->delta_bits, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
   // as for CSR: within the shared-memory budget that leaves L1 its share
-  const int occ = delta_kernel_occupancy(p->x_smem, p->dyn_smem, kSmemBudget);
+  const int occ = delta_kernel_occupancy(p->delta_bits, p->x_smem, p->dyn_smem, kSmemBudget);
   if (occ <= 0) return SPMV_ERR_CUDA;
   // a CTA may run several blocks of units (groups); the plan deals units to
   // groups, the grid has one CTA per `groups` of them
@@ -651,8 +691,9 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   const size_t e_alloc = (size_t)d->n_entries + 8 * kPadElems;
   if ((s = dev_upload(&p->values, d->values, (size_t)d->n_entries * 2,
                       e_alloc * 2)) != SPMV_OK) return s;
-  if ((s = dev_upload(&p->words, d->words, (size_t)d->n_entries / 2,
-                      e_alloc / 2)) != SPMV_OK) return s;
+  const size_t per_word = (size_t)delta_per_word(p->delta_bits);
+  if ((s = dev_upload(&p->words, d->words, (size_t)d->n_entries / per_word * 4,
+                      e_alloc / per_word * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->tiles, t.units.data(), t.units.size() * sizeof(Tile),
                       t.units.size() * sizeof(Tile))) != SPMV_OK) return s;
   if ((s = dev_upload(&p->warp_base, t.warp_base.data(), t.warp_base.size() * 4,
@@ -669,8 +710,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   info.x_in_smem = p->x_smem ? 1 : 0;
   info.block = delta_block(p->x_smem);
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
-  info.matrix_bytes = d->n_entries * 2 + d->n_entries / 2 +
-                      ((int64_t)d->n_rows + 1) * 4;
+  info.matrix_bytes = delta_matrix_bytes(*d);
   info.aux_bytes = (int64_t)(t.units.size() * sizeof(Tile) + t.warp_base.size() * 4 +
                              t.cta_first.size() * 4 + t.row_split.size() * 4 +
                              t.splits.size() * (sizeof(SplitInfo) + 4) +
@@ -714,12 +754,14 @@ void spmv_plan_options_init(spmv_plan_options* o) {
   o->x_smem = -1;
 }
 
-spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
+spmv_status spmv_convert_bits(const spmv_csr* m, int32_t b, spmv_delta* out) {
   if (!out) return SPMV_ERR_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));
+  if (!valid_delta_bits(b)) return SPMV_ERR_INVALID_ARG;
   spmv_status s = validate_csr(m, true);
   if (s != SPMV_OK) return s;
   if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+  const int64_t cap = delta_cap(b), per = delta_per_word(b);
   const int32_t* rp = m->row_ptr;
   const uint16_t* v = static_cast<const uint16_t*>(m->values);
   int64_t* erp = static_cast<int64_t*>(std::malloc(((size_t)m->n_rows + 1) * 8));
@@ -727,15 +769,14 @@ spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
   int64_t total = 0, gaps = 0, aligns = 0;
   erp[0] = 0;
   for (int32_t r = 0; r < m->n_rows; ++r) {
-    int64_t n = delta_row_entries(m->col_idx + rp[r], rp[r + 1] - rp[r], &gaps);
-    int64_t padded = (n + kRowAlign - 1) / kRowAlign * kRowAlign;
+    int64_t n = delta_row_entries(m->col_idx + rp[r], rp[r + 1] - rp[r], cap, &gaps);
+    int64_t padded = (n + per - 1) / per * per;
     aligns += padded - n;
     total += padded;
     erp[r + 1] = total;
   }
   uint16_t* vals = static_cast<uint16_t*>(std::malloc((size_t)total * 2 + 16));
-  uint32_t* words =
-      static_cast<uint32_t*>(std::calloc((size_t)total / kRowAlign + 1, 4));
+  uint32_t* words = static_cast<uint32_t*>(std::calloc((size_t)(total / per) + 1, 4));
   if (!vals || !words) {
     std::free(erp);
     std::free(vals);
@@ -748,12 +789,12 @@ spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
     for (int32_t k = rp[r]; k < rp[r + 1]; ++k) {
       const int64_t col = m->col_idx[k];
       int64_t gap = col - c;
-      for (; gap > kDeltaCap; gap -= kDeltaCap) emit(vals, words, e++, 0, kDeltaCap);
-      emit(vals, words, e++, v[k], (uint32_t)gap);
+      for (; gap > cap; gap -= cap) emit(vals, words, e++, b, 0, (uint32_t)cap);
+      emit(vals, words, e++, b, v[k], (uint32_t)gap);
       zeros += v[k] == 0;
       c = col;
     }
-    while (e < erp[r + 1]) emit(vals, words, e++, 0, 0);
+    while (e < erp[r + 1]) emit(vals, words, e++, b, 0, 0);
   }
   out->n_rows = m->n_rows;
   out->n_cols = m->n_cols;
@@ -765,7 +806,12 @@ spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
   out->values = vals;
   out->words = words;
   out->row_ptr = erp;
+  out->delta_bits = b;
   return SPMV_OK;
+}
+
+spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
+  return spmv_convert_bits(m, 4, out);
 }
 
 void spmv_delta_free(spmv_delta* d) {
@@ -781,7 +827,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
                               spmv_plan_info* info) {
   if (!info || !valid_format(format)) return SPMV_ERR_INVALID_ARG;
   std::memset(info, 0, sizeof(*info));
-  const bool delta = format == SPMV_FORMAT_DELTA4;
+  const bool delta = format != SPMV_FORMAT_CSR;
   spmv_status s = validate_csr(m, delta);
   if (s != SPMV_OK) return s;
   Options o = resolve_options(opts, m->value_dtype);
@@ -794,7 +840,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   if (delta) {
     if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
     spmv_delta d;
-    if ((s = spmv_convert(m, &d)) != SPMV_OK) return s;
+    if ((s = spmv_convert_bits(m, format_delta_bits(format), &d)) != SPMV_OK) return s;
     if (d.n_entries > kMaxIndex) {
       spmv_delta_free(&d);
       return SPMV_ERR_TOO_LARGE;
@@ -809,7 +855,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
     info->n_entries = d.n_entries;
     info->x_in_smem = xs ? 1 : 0;
     info->launches_per_run = m->n_rows > 0;
-    info->matrix_bytes = d.n_entries * 2 + d.n_entries / 2 + ((int64_t)m->n_rows + 1) * 4;
+    info->matrix_bytes = delta_matrix_bytes(d);
     fill_bytes(info, 2);
     spmv_delta_free(&d);
     return s;
@@ -838,7 +884,7 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
   if (!out) return SPMV_ERR_INVALID_ARG;
   *out = nullptr;
   if (!valid_format(format)) return SPMV_ERR_INVALID_ARG;
-  const bool delta = format == SPMV_FORMAT_DELTA4;
+  const bool delta = format != SPMV_FORMAT_CSR;
   spmv_status s = validate_csr(m, delta);
   if (s != SPMV_OK) return s;
   if (delta && m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
@@ -858,7 +904,7 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
   p->info.value_dtype = m->value_dtype;
   if (delta) {
     spmv_delta d;
-    s = spmv_convert(m, &d);
+    s = spmv_convert_bits(m, format_delta_bits(format), &d);
     if (s == SPMV_OK) {
       if (d.n_entries > kMaxIndex) {
         s = SPMV_ERR_TOO_LARGE;
@@ -899,7 +945,7 @@ spmv_status spmv_plan_create_delta(const spmv_delta* d,
   spmv_plan* plan = new (std::nothrow) spmv_plan();
   if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
   Plan* p = &plan->impl;
-  p->format = SPMV_FORMAT_DELTA4;
+  p->format = delta_format(delta_bits_of(d));
   p->dtype = SPMV_F16;
   p->n_rows = d->n_rows;
   p->n_cols = d->n_cols;
@@ -908,7 +954,7 @@ spmv_status spmv_plan_create_delta(const spmv_delta* d,
   p->info.n_rows = d->n_rows;
   p->info.n_cols = d->n_cols;
   p->info.nnz = nnz;
-  p->info.format = SPMV_FORMAT_DELTA4;
+  p->info.format = p->format;
   p->info.value_dtype = SPMV_F16;
   p->info.n_entries = d->n_entries;
   s = create_delta_plan(d, o, p);

@@ -37,23 +37,16 @@ constexpr int tile_cap(spmv_dtype t) { return t == SPMV_F16 ? kTileCapF16 : kTil
 constexpr int kStreamTileCap = (kTileCap < kThreads * 8 ? kTileCap : kThreads * 8) - 16;
 constexpr int kTileRowsCap = 512;        // rows of a short-row tile
 constexpr int kStages = SPMV_STAGES;
-// DELTA4 kernel: a work unit is a slice of one row of at most
-// kDeltaUnitWords packed words (8 entries each), decoded by a CTA of
-// kDeltaThreads threads, LW = 1, 2, ... kDeltaMaxLaneWords consecutive words
-// per thread (the least LW that fits the row in one unit, else the most), so
-// warp w decodes the unit's words [32 LW w, 32 LW (w + 1)).
-#ifndef SPMV_DELTA_THREADS
-#define SPMV_DELTA_THREADS 256
-#endif
-constexpr int kDeltaThreads = SPMV_DELTA_THREADS;
+// DELTA kernel: a work unit is a slice of one row of at most
+// delta_unit_words(b) packed words (32 / b entries each for deltas of b
+// bits), decoded by kDeltaThreads threads, LW = 1 or 2 words per thread (the
+// fewest that fit the row in one unit), so warp w decodes the unit's words
+// [32 LW w, 32 LW (w + 1)). Units hold at most 4096 entries (2048 at b = 8).
+constexpr int kDeltaThreads = 256;
 constexpr int kDeltaWarps = kDeltaThreads / 32;
-#ifndef SPMV_DELTA_UNIT_WORDS
-#define SPMV_DELTA_UNIT_WORDS 512
-#endif
-constexpr int kDeltaUnitWords = SPMV_DELTA_UNIT_WORDS;
+constexpr int kDeltaUnitWords = 512;  // the most, over the widths
+constexpr int delta_unit_words(int bits) { return bits == 2 ? 256 : 512; }
 constexpr int kDeltaMaxLaneWords = kDeltaUnitWords / kDeltaThreads;
-static_assert(kDeltaMaxLaneWords == 1 || kDeltaMaxLaneWords == 2 || kDeltaMaxLaneWords == 4,
-              "words per lane must be 1, 2 or 4");
 // DELTA4 unit descriptor: {row | FIRST | LAST | log2(LW) << kUnitLgShift,
 // word_begin, word_end, column before the unit's first entry}; FIRST / LAST:
 // first / last unit of the row.
@@ -147,6 +140,7 @@ struct Plan {
   int n_rows = 0, n_cols = 0;
   int64_t nnz = 0, n_entries = 0;
   bool x_smem = false;
+  int delta_bits = 4;          // DELTA: bits per column delta (2, 4 or 8)
   bool interleaved = false;  // CSR: products element-interleaved over the CTA
   bool x_aligned16 = false;
   int grid = 0;
@@ -155,16 +149,16 @@ struct Plan {
   int split_chunk = 0;
 
   // matrix (device)
-  int32_t* row_ptr = nullptr;   // CSR offsets or DELTA4 entry offsets
+  int32_t* row_ptr = nullptr;   // CSR offsets or DELTA entry offsets
   int32_t* col_idx = nullptr;   // CSR only
-  void* values = nullptr;       // fp32 / fp16 (CSR) or fp16 (DELTA4)
-  uint32_t* words = nullptr;    // DELTA4 packed deltas
+  void* values = nullptr;       // fp32 / fp16 (CSR) or fp16 (DELTA)
+  uint32_t* words = nullptr;    // DELTA packed deltas
   // planner tables and scratch (device)
   Tile* tiles = nullptr;
   SplitInfo* splits = nullptr;
   int32_t* cta_first = nullptr;
-  int32_t* row_split = nullptr;  // DELTA4: split id per row or -1
-  int32_t* warp_base = nullptr;  // DELTA4: kWarps starting columns per unit
+  int32_t* row_split = nullptr;  // DELTA: split id per row or -1
+  int32_t* warp_base = nullptr;  // DELTA: kWarps starting columns per unit
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
   int32_t* status = nullptr;    // device status word
@@ -180,12 +174,12 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, bool il, size_t dyn_smem
                          size_t budget);
 size_t csr_stage_bytes(spmv_dtype dtype);
 int csr_set_smem_limit(size_t dyn);
-int delta_kernel_occupancy(bool x_smem, size_t dyn_smem, size_t budget);
-size_t delta_stages_bytes(bool x_smem);  // every stage of every group
+int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem, size_t budget);
+size_t delta_stages_bytes(int bits, bool x_smem);  // every stage of every group
 int delta_groups(bool x_smem);           // unit blocks ("virtual CTAs") per CTA
 int delta_block(bool x_smem);            // threads per CTA
 size_t delta_x_smem_bytes(int n_cols);
-int delta_set_smem_limit(size_t dyn);
+int delta_set_smem_limit(int bits, size_t dyn);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 

@@ -1,6 +1,6 @@
 """CPU tests of the C ABI: the library loads, exports every function that
 include/spmv.h declares, its structs match the C layout, host-side
-validation and the DELTA4 converter behave, and the planner's bins are
+validation and the DELTA converter (2-, 4- and 8-bit deltas) behave, and the planner's bins are
 consistent. Nothing here launches a kernel."""
 import ctypes
 import os
@@ -35,7 +35,7 @@ def test_every_declared_function_is_exported(spmv_lib):
 
 
 def test_abi_version_and_status_strings(spmv_lib):
-    assert S.spmv_abi_version() == 1
+    assert S.spmv_abi_version() == 2
     for code in range(11):
         s = S.spmv_status_string(code)
         assert s and s != "unknown status"
@@ -130,12 +130,25 @@ def test_null_and_bad_args(spmv_lib):
     d = _lib.spmv_delta()
     spmv_lib.spmv_delta_free(ctypes.byref(d))
     assert spmv_lib.spmv_convert(None, ctypes.byref(d)) == 1
+    h = _csr([0, 1], [0], np.ones(1, np.float16), 4)
+    for bad in (0, 1, 3, 16, -4):
+        assert spmv_lib.spmv_convert_bits(ctypes.byref(h.struct), bad, ctypes.byref(d)) == 1
+    # a DELTA matrix whose width is not 2, 4 or 8 is refused before any
+    # device call
+    d = _lib.spmv_delta(n_rows=0, n_cols=4, row_ptr=ctypes.addressof(c_zero), delta_bits=3)
+    out = ctypes.c_void_p()
+    assert spmv_lib.spmv_plan_create_delta(ctypes.byref(d), None, ctypes.byref(out)) == 1
+    assert not out.value
 
 
-def _converter_matches_oracle(m, n_cols=None):
+c_zero = ctypes.c_int64(0)
+
+
+def _converter_matches_oracle(m, n_cols=None, bits=4):
     n_cols = m.n_cols if n_cols is None else n_cols
-    got = S.spmv_convert(m.row_ptr, m.col_idx, m.values, n_cols)
-    ref = oracle.delta_encode(n_cols, m.row_ptr, m.col_idx, m.values)
+    got = S.spmv_convert(m.row_ptr, m.col_idx, m.values, n_cols, bits=bits)
+    ref = oracle.delta_encode(n_cols, m.row_ptr, m.col_idx, m.values, bits=bits)
+    assert got.bits == bits
     assert np.array_equal(got.row_ptr, ref.row_ptr)
     assert np.array_equal(got.values, ref.values)
     assert np.array_equal(got.words, ref.words)
@@ -144,25 +157,28 @@ def _converter_matches_oracle(m, n_cols=None):
     return got
 
 
+@pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("sparsity", [0.3, 0.5, 0.7, 0.9, 0.99])
-def test_converter_bit_exact_llm_small(spmv_lib, sparsity):
-    _converter_matches_oracle(workloads.llm(sparsity, n=700))
+def test_converter_bit_exact_llm_small(spmv_lib, sparsity, bits):
+    _converter_matches_oracle(workloads.llm(sparsity, n=700), bits=bits)
 
 
-def test_converter_bit_exact_edge_rows(spmv_lib):
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_converter_bit_exact_edge_rows(spmv_lib, bits):
     lengths = np.array([0, 1, 8, 7, 9, 0, 0, 16, 33, 1, 2000])
     m = workloads.from_lengths("edges", lengths, 5000, seed=9, dtype=np.float16)
-    _converter_matches_oracle(m)
-    # first column 0, exact multiples of 15, a gap spanning the whole row
-    rp = np.array([0, 4, 6, 7], np.int32)
-    ci = np.array([0, 15, 30, 31, 0, 4999, 2999], np.int32)
-    vals = np.arange(1, 8).astype(np.float16)
+    _converter_matches_oracle(m, bits=bits)
+    # first column 0, exact multiples of 3, 15 and 255, a gap spanning the
+    # whole row
+    rp = np.array([0, 6, 8, 9], np.int32)
+    ci = np.array([0, 3, 15, 30, 255, 510, 0, 4999, 2999], np.int32)
+    vals = np.arange(1, 10).astype(np.float16)
     m = workloads.CSRInput("hand", 3, 5000, rp, ci, vals, np.zeros(5000, np.float16))
-    _converter_matches_oracle(m)
+    _converter_matches_oracle(m, bits=bits)
     # explicit +0.0 values are stored as such and counted
     vals0 = vals.copy()
     vals0[2] = 0
-    got = S.spmv_convert(rp, ci, vals0, 5000)
+    got = S.spmv_convert(rp, ci, vals0, 5000, bits=bits)
     assert got.n_explicit_zeros == 1
 
 
@@ -250,6 +266,15 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     enc = oracle.delta_encode(llm.n_cols, llm.row_ptr, llm.col_idx, llm.values)
     assert info["n_entries"] == enc.n_entries
     assert info["matrix_bytes"] == 2 * enc.n_entries + enc.n_entries // 2 + 4 * (llm.n_rows + 1)
+    for bits in (2, 8):
+        info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
+                                   format=f"delta{bits}")
+        enc = oracle.delta_encode(llm.n_cols, llm.row_ptr, llm.col_idx, llm.values,
+                                  bits=bits)
+        assert info["format"] == {2: 2, 8: 3}[bits]
+        assert info["n_entries"] == enc.n_entries
+        assert info["matrix_bytes"] == (2 * enc.n_entries + enc.n_entries * bits // 8
+                                        + 4 * (llm.n_rows + 1))
 
 
 def test_gather_order_choice(spmv_lib):

@@ -3,7 +3,7 @@ oracle, element by element, on the seeded workloads and on edge cases.
 
 Tolerances (per row i, s_i = sum_j |a_ij x_j| from the oracle):
   fp32 CSR:                   |y - y_ref| <= 1e-5 * s_i + 1e-30
-  fp16 values (CSR, DELTA4):  |y - y_ref| <= 2e-3 * s_i
+  fp16 values (CSR, DELTA):   |y - y_ref| <= 2e-3 * s_i
 """
 import functools
 
@@ -20,6 +20,8 @@ pytestmark = pytest.mark.gpu
 
 TOL32 = 1e-5
 TOL16 = 2e-3
+DELTAS = ["delta2", "delta4", "delta8"]
+FORMAT_CODE = {"csr": 0, "delta4": 1, "delta2": 2, "delta8": 3}
 
 
 @functools.lru_cache(maxsize=None)
@@ -98,11 +100,12 @@ def test_small_csr(name):
     assert_parity(m, y, tol_for(m))
 
 
+@pytest.mark.parametrize("fmt", DELTAS)
 @pytest.mark.parametrize("name", ["llm30_small", "llm90_small"])
-def test_small_delta4(name):
+def test_small_delta(name, fmt):
     m = small(name)
-    y, info = run_gpu(m, "delta4")
-    assert info["format"] == 1
+    y, info = run_gpu(m, fmt)
+    assert info["format"] == FORMAT_CODE[fmt]
     assert_parity(m, y, TOL16)
 
 
@@ -114,10 +117,11 @@ def test_full_size_csr(name):
     assert_parity(m, y, tol_for(m))
 
 
+@pytest.mark.parametrize("fmt", DELTAS)
 @pytest.mark.parametrize("name", ["llm30", "llm50", "llm70", "llm90"])
-def test_full_size_delta4(name):
+def test_full_size_delta(name, fmt):
     m = full(name)
-    y, info = run_gpu(m, "delta4")
+    y, info = run_gpu(m, fmt)
     assert info["n_entries"] >= m.nnz
     assert_parity(m, y, TOL16)
 
@@ -156,18 +160,20 @@ def test_forced_paths_fp16_csr(kw):
     assert_parity(m, y, TOL16)
 
 
+@pytest.mark.parametrize("fmt", DELTAS)
 @pytest.mark.parametrize("x_smem", [0, 1])
-def test_delta4_x_paths(x_smem):
+def test_delta_x_paths(x_smem, fmt):
     m = workloads.llm(0.6, n=3000, seed=8)
-    y, info = run_gpu(m, "delta4", options=S.spmv_plan_options(x_smem=x_smem))
+    y, info = run_gpu(m, fmt, options=S.spmv_plan_options(x_smem=x_smem))
     assert info["x_in_smem"] == x_smem
     assert_parity(m, y, TOL16)
 
 
-def test_delta4_mixed_rows_deterministic():
+@pytest.mark.parametrize("fmt", DELTAS)
+def test_delta_mixed_rows_deterministic(fmt):
     lengths = np.tile([0, 1, 0, 3, 9, 0, 257, 0, 5000, 2, 20000, 0, 700, 64, 65], 30)
     m = workloads.from_lengths("mixed16", lengths, 30000, seed=17, dtype=np.float16)
-    ys, info = run_gpu(m, "delta4", repeat=3)
+    ys, info = run_gpu(m, fmt, repeat=3)
     assert info["n_split_rows"] > 0
     for y in ys[1:]:
         assert np.array_equal(y, ys[0])
@@ -214,7 +220,7 @@ def test_one_by_one_and_single_row():
     assert_parity(m, y, TOL32)
 
 
-@pytest.mark.parametrize("fmt", ["csr", "delta4"])
+@pytest.mark.parametrize("fmt", ["csr"] + DELTAS)
 def test_interleaved_empty_and_long_rows(fmt):
     lengths = np.tile([0, 1, 0, 3, 9, 0, 257, 0, 5000, 2, 20000, 0], 40)
     dt = np.float32 if fmt == "csr" else np.float16
@@ -275,11 +281,14 @@ def test_x_unaligned_pointer_staging():
     assert_parity(m, y.cpu().numpy(), TOL32)
 
 
-def test_delta4_gap_patterns():
-    # first column 0, gaps of exactly 15/16/30/31, a gap across the row
+@pytest.mark.parametrize("fmt", DELTAS)
+def test_delta_gap_patterns(fmt):
+    # first column 0; gaps of exactly D, D + 1, 2D and 2D + 1 for each field
+    # width (D = 3, 15, 255); a gap across the row
     rows = [[0, 15, 30, 31, 47], [16], [31, 32, 33, 34, 35, 36, 37, 38],
+            [0, 3, 7, 13, 20], [3], [4], [0, 255, 511, 1021, 1533], [256], [255],
             [0], [4095], list(range(0, 4096, 17)), list(range(2000, 2050)),
-            list(range(0, 4096, 2))]
+            list(range(0, 4096, 2)), list(range(0, 4096, 4)), list(range(1, 4096, 3))]
     rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])])
     ci = np.concatenate([np.array(r) for r in rows])
     rng = np.random.default_rng(5)
@@ -287,19 +296,21 @@ def test_delta4_gap_patterns():
     vals[vals == 0] = np.float16(0.25)
     m = make("gaps", rp, ci, vals, 4096, rng.normal(0, 1, 4096).astype(np.float16))
     for kw in ({}, {"x_smem": 0}):
-        y, _ = run_gpu(m, "delta4", options=S.spmv_plan_options(**kw))
+        y, _ = run_gpu(m, fmt, options=S.spmv_plan_options(**kw))
         assert_parity(m, y, TOL16)
 
 
-def test_plan_from_converted_delta():
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_plan_from_converted_delta(bits):
     m = workloads.llm(0.75, n=900, seed=4)
-    d = S.spmv_convert(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    d = S.spmv_convert(m.row_ptr, m.col_idx, m.values, m.n_cols, bits=bits)
     plan = S.spmv_plan_create_delta(d)
+    assert plan.info["format"] == FORMAT_CODE[f"delta{bits}"]
     dev = torch.device("cuda", 0)
     y = torch.empty(m.n_rows, dtype=torch.float32, device=dev)
     S.spmv_run(plan, torch.from_numpy(m.x).to(dev), y)
     torch.cuda.synchronize()
-    y2, _ = run_gpu(m, "delta4")
+    y2, _ = run_gpu(m, f"delta{bits}")
     assert np.array_equal(y.cpu().numpy(), y2)
     assert_parity(m, y2, TOL16)
 
@@ -349,7 +360,8 @@ def test_side_stream_and_graph_capture():
     S.spmv_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("fmt,name", [("csr", "laplacian_small"), ("delta4", "llm90_small")])
+@pytest.mark.parametrize("fmt,name", [("csr", "laplacian_small"), ("delta4", "llm90_small"),
+                                      ("delta2", "llm30_small"), ("delta8", "llm90_small")])
 def test_run_host_end_to_end(fmt, name):
     m = small(name)
     plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
