@@ -66,8 +66,23 @@ typedef enum spmv_format {
   SPMV_FORMAT_CSR = 0,     /* [CSR] section 2.1                               */
   SPMV_FORMAT_DELTA4 = 1,  /* [MACKO] section 2.1, 4-bit deltas               */
   SPMV_FORMAT_DELTA2 = 2,  /* the same format with 2-bit deltas ([MACKO] 3.3) */
-  SPMV_FORMAT_DELTA8 = 3   /* the same format with 8-bit deltas ([MACKO] 3.3) */
+  SPMV_FORMAT_DELTA8 = 3,  /* the same format with 8-bit deltas ([MACKO] 3.3) */
+  SPMV_FORMAT_DELTA_AUTO = 4 /* the width spmv_delta_select_bits picks under
+                                SPMV_DELTA_FEWEST_BYTES; plans and their info
+                                report the chosen width's format code       */
 } spmv_format;
+
+/* How spmv_delta_select_bits picks a delta width ([MACKO] section 3.3). */
+typedef enum spmv_delta_policy {
+  /* the width whose encoding stores the fewest bytes (values, deltas and
+   * row pointers; padding included); ties go to the wider field */
+  SPMV_DELTA_FEWEST_BYTES = 0,
+  /* the sparsity table of [MACKO] 3.3 as printed, with s = 1 - nnz /
+   * (n_rows * n_cols): s < 0.3 -> 8 bits, 0.3 <= s <= 0.7 -> 4 (the default
+   * where the 2- and 4-bit ranges overlap), s > 0.7 -> 2 (the 1-bit width the
+   * table gives above 0.9 is not provided; 2 is the nearest) */
+  SPMV_DELTA_SPARSITY_TABLE = 1
+} spmv_delta_policy;
 
 /* A CSR matrix in HOST memory ([CSR] section 2.1).
  * row_ptr: n_rows+1 offsets, row_ptr[0] == 0, non-decreasing, last == nnz.
@@ -195,6 +210,14 @@ spmv_status spmv_convert(const spmv_csr* csr, spmv_delta* out);
 /* As spmv_convert, with deltas of `bits` bits (2, 4 or 8; anything else:
  * INVALID_ARG). */
 spmv_status spmv_convert_bits(const spmv_csr* csr, int32_t bits, spmv_delta* out);
+
+/* Pick a delta width (2, 4 or 8) for a CSR matrix with fp16 values under
+ * `policy`. entries, if not NULL, receives the number of entries the
+ * encoding would store at 2, 4 and 8 bits (padding included), counted
+ * exactly without building it. Errors: as spmv_convert, and INVALID_ARG for
+ * a NULL bits or an unknown policy. */
+spmv_status spmv_delta_select_bits(const spmv_csr* csr, spmv_delta_policy policy,
+                                   int32_t* bits, int64_t entries[3]);
 
 /* Free the arrays of a spmv_delta filled by spmv_convert and zero it. */
 void spmv_delta_free(spmv_delta* d);

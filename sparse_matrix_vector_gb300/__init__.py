@@ -6,7 +6,7 @@ The compiled library is ``libspmv_gb300.so`` next to this file (built by
 ``sparse_matrix_vector_gb300.build``). This package only marshals arguments.
 """
 from .api import (  # noqa: F401
-    DeltaMatrix, Plan, SpmvError, spmv_abi_version, spmv_convert,
+    DeltaMatrix, Plan, SpmvError, spmv_abi_version, spmv_convert, spmv_delta_select_bits,
     spmv_csr_run_noalloc,
     spmv_plan_check, spmv_plan_create, spmv_plan_create_delta,
     spmv_plan_destroy, spmv_plan_inspect, spmv_plan_options, spmv_run,
@@ -14,5 +14,5 @@ from .api import (  # noqa: F401
 )
 from ._lib import (  # noqa: F401
     SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA4,
-    SPMV_FORMAT_DELTA8,
+    SPMV_FORMAT_DELTA8, SPMV_FORMAT_DELTA_AUTO,
 )

@@ -16,6 +16,8 @@ c_p = ctypes.c_void_p
 
 SPMV_F32, SPMV_F16 = 0, 1
 SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA8 = 0, 1, 2, 3
+SPMV_FORMAT_DELTA_AUTO = 4
+SPMV_DELTA_FEWEST_BYTES, SPMV_DELTA_SPARSITY_TABLE = 0, 1
 
 STATUS_NAMES = {
     0: "SPMV_OK", 1: "SPMV_ERR_INVALID_ARG", 2: "SPMV_ERR_BAD_ROW_PTR",
@@ -68,6 +70,8 @@ SIGNATURES = {
                                     ctypes.POINTER(spmv_delta)]),
     "spmv_convert_bits": (ctypes.c_int, [ctypes.POINTER(spmv_csr), c_i32,
                                          ctypes.POINTER(spmv_delta)]),
+    "spmv_delta_select_bits": (ctypes.c_int, [ctypes.POINTER(spmv_csr), ctypes.c_int,
+                                              ctypes.POINTER(c_i32), ctypes.POINTER(c_i64)]),
     "spmv_delta_free": (None, [ctypes.POINTER(spmv_delta)]),
     "spmv_plan_inspect": (ctypes.c_int, [ctypes.POINTER(spmv_csr), ctypes.c_int,
                                          ctypes.POINTER(spmv_plan_options),

@@ -13,11 +13,15 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import _lib
-from ._lib import (SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2,
-                   SPMV_FORMAT_DELTA4, SPMV_FORMAT_DELTA8)
+from ._lib import (SPMV_DELTA_FEWEST_BYTES, SPMV_DELTA_SPARSITY_TABLE, SPMV_F16, SPMV_F32,
+                   SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA4,
+                   SPMV_FORMAT_DELTA8, SPMV_FORMAT_DELTA_AUTO)
 
 FORMATS = {"csr": SPMV_FORMAT_CSR, "delta4": SPMV_FORMAT_DELTA4,
-           "delta2": SPMV_FORMAT_DELTA2, "delta8": SPMV_FORMAT_DELTA8}
+           "delta2": SPMV_FORMAT_DELTA2, "delta8": SPMV_FORMAT_DELTA8,
+           "delta": SPMV_FORMAT_DELTA_AUTO}
+DELTA_POLICIES = {"fewest_bytes": SPMV_DELTA_FEWEST_BYTES,
+                  "sparsity_table": SPMV_DELTA_SPARSITY_TABLE}
 
 
 class SpmvError(RuntimeError):
@@ -147,6 +151,21 @@ def spmv_convert(row_ptr, col_idx, values, n_cols: int, bits: int = 4) -> DeltaM
                            int(d.n_explicit_zeros), b)
     finally:
         lib.spmv_delta_free(ctypes.byref(d))
+
+
+def spmv_delta_select_bits(row_ptr, col_idx, values, n_cols: int,
+                           policy="fewest_bytes"):
+    """Delta width (2, 4 or 8) for a CSR matrix with fp16 values under
+    `policy` ("fewest_bytes" or "sparsity_table"), and the entries each width
+    would store: returns (bits, {2: n, 4: n, 8: n})."""
+    h = _host_csr(row_ptr, col_idx, values, n_cols)
+    code = DELTA_POLICIES[policy] if isinstance(policy, str) else int(policy)
+    bits = ctypes.c_int32()
+    entries = (ctypes.c_int64 * 3)()
+    _check(_lib.load().spmv_delta_select_bits(ctypes.byref(h.struct), code,
+                                              ctypes.byref(bits), entries),
+           "spmv_delta_select_bits")
+    return int(bits.value), {2: int(entries[0]), 4: int(entries[1]), 8: int(entries[2])}
 
 
 def spmv_plan_inspect(row_ptr, col_idx, values, n_cols: int, format="csr",

@@ -51,7 +51,7 @@ size_t dtype_size(spmv_dtype t) { return t == SPMV_F16 ? 2 : 4; }
 bool valid_dtype(int t) { return t == SPMV_F32 || t == SPMV_F16; }
 bool valid_format(int f) {
   return f == SPMV_FORMAT_CSR || f == SPMV_FORMAT_DELTA4 || f == SPMV_FORMAT_DELTA2 ||
-         f == SPMV_FORMAT_DELTA8;
+         f == SPMV_FORMAT_DELTA8 || f == SPMV_FORMAT_DELTA_AUTO;
 }
 
 int32_t format_delta_bits(int f) {
@@ -814,6 +814,43 @@ spmv_status spmv_convert(const spmv_csr* m, spmv_delta* out) {
   return spmv_convert_bits(m, 4, out);
 }
 
+spmv_status spmv_delta_select_bits(const spmv_csr* m, spmv_delta_policy policy, int32_t* bits,
+                                   int64_t entries[3]) {
+  if (!bits || (policy != SPMV_DELTA_FEWEST_BYTES && policy != SPMV_DELTA_SPARSITY_TABLE))
+    return SPMV_ERR_INVALID_ARG;
+  spmv_status s = validate_csr(m, true);
+  if (s != SPMV_OK) return s;
+  if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+  static const int32_t kWidths[3] = {2, 4, 8};
+  int64_t n[3] = {0, 0, 0};
+  for (int i = 0; i < 3; ++i) {
+    const int32_t b = kWidths[i];
+    const int64_t per = delta_per_word(b);
+    for (int32_t r = 0; r < m->n_rows; ++r) {
+      int64_t gaps = 0;
+      const int64_t len = delta_row_entries(m->col_idx + m->row_ptr[r],
+                                            m->row_ptr[r + 1] - m->row_ptr[r], delta_cap(b),
+                                            &gaps);
+      n[i] += (len + per - 1) / per * per;
+    }
+  }
+  if (entries)
+    for (int i = 0; i < 3; ++i) entries[i] = n[i];
+  if (policy == SPMV_DELTA_SPARSITY_TABLE) {
+    const double cells = (double)m->n_rows * (double)m->n_cols;
+    const double sp = cells > 0 ? 1.0 - (double)m->nnz / cells : 0.0;
+    *bits = sp < 0.3 ? 8 : (sp <= 0.7 ? 4 : 2);
+    return SPMV_OK;
+  }
+  // stored bytes: 2 per entry for the values, b/8 per entry for the deltas
+  // (row pointers are the same for every width); ties go to the wider field
+  int best = 2;
+  for (int i = 1; i >= 0; --i)
+    if (n[i] * (16 + kWidths[i]) < n[best] * (16 + kWidths[best])) best = i;
+  *bits = kWidths[best];
+  return SPMV_OK;
+}
+
 void spmv_delta_free(spmv_delta* d) {
   if (!d) return;
   std::free(d->values);
@@ -830,6 +867,12 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   const bool delta = format != SPMV_FORMAT_CSR;
   spmv_status s = validate_csr(m, delta);
   if (s != SPMV_OK) return s;
+  if (format == SPMV_FORMAT_DELTA_AUTO) {
+    int32_t b = 4;
+    if ((s = spmv_delta_select_bits(m, SPMV_DELTA_FEWEST_BYTES, &b, nullptr)) != SPMV_OK)
+      return s;
+    format = delta_format(b);
+  }
   Options o = resolve_options(opts, m->value_dtype);
   info->n_rows = m->n_rows;
   info->n_cols = m->n_cols;
@@ -888,6 +931,12 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
   spmv_status s = validate_csr(m, delta);
   if (s != SPMV_OK) return s;
   if (delta && m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+  if (format == SPMV_FORMAT_DELTA_AUTO) {
+    int32_t b = 4;
+    if ((s = spmv_delta_select_bits(m, SPMV_DELTA_FEWEST_BYTES, &b, nullptr)) != SPMV_OK)
+      return s;
+    format = delta_format(b);
+  }
   Options o = resolve_options(opts, m->value_dtype);
   spmv_plan* plan = new (std::nothrow) spmv_plan();
   if (!plan) return SPMV_ERR_OUT_OF_MEMORY;

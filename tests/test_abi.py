@@ -306,3 +306,41 @@ def test_empty_and_degenerate_inspect(spmv_lib):
     info = S.spmv_plan_inspect(np.zeros(5001, np.int32), np.zeros(0, np.int32),
                                np.zeros(0, np.float32), 3)
     assert sum(info["rows_per_bin"]) == 5000 and info["n_tiles"] >= 5
+
+
+@pytest.mark.parametrize("sparsity", [0.1, 0.3, 0.5, 0.7, 0.9, 0.97])
+def test_delta_width_selection(spmv_lib, sparsity):
+    """The entry counts behind the choice equal the oracle encoder's at each
+    width; the fewest-bytes choice is the width that stores the fewest bytes
+    (ties to the wider field); the sparsity table follows the printed rows."""
+    m = workloads.llm(sparsity, n=600, seed=12)
+    bits, entries = S.spmv_delta_select_bits(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    stored = {}
+    for b in (2, 4, 8):
+        enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, bits=b)
+        assert entries[b] == enc.n_entries
+        stored[b] = enc.n_entries * 2 + enc.n_entries * b // 8
+    best = min(stored.values())
+    assert bits == max(b for b in stored if stored[b] == best)
+    table, _ = S.spmv_delta_select_bits(m.row_ptr, m.col_idx, m.values, m.n_cols,
+                                        policy="sparsity_table")
+    s = 1.0 - m.nnz / (m.n_rows * m.n_cols)
+    assert table == (8 if s < 0.3 else 4 if s <= 0.7 else 2)
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="delta")
+    assert info["format"] == {4: 1, 2: 2, 8: 3}[bits]
+    assert info["n_entries"] == entries[bits]
+
+
+def test_delta_width_selection_errors(spmv_lib):
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_delta_select_bits([0, 2], [1, 2], np.ones(2, np.float32), 4)
+    assert e.value.status == 5
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_delta_select_bits([0, 2], [2, 1], np.ones(2, np.float16), 4)
+    assert e.value.status == 4
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_delta_select_bits([0, 2], [1, 2], np.ones(2, np.float16), 4, policy=7)
+    assert e.value.status == 1
+    # an empty matrix: every width stores nothing; ties go to 8 bits
+    bits, entries = S.spmv_delta_select_bits([0, 0], [], np.zeros(0, np.float16), 4)
+    assert bits == 8 and entries == {2: 0, 4: 0, 8: 0}

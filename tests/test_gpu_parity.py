@@ -433,3 +433,14 @@ def test_chained_delta4_after_torch_kernels():
     y_ref2, s2 = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, x2.cpu().numpy())
     assert_parity(m, y2.cpu().numpy(), TOL16, y_ref2, s2)
     S.spmv_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("name", ["llm30_small", "llm90_small"])
+def test_delta_auto_width(name):
+    """format="delta": the width with the fewest stored bytes, reported by
+    the plan's format code."""
+    m = small(name)
+    bits, _ = S.spmv_delta_select_bits(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    y, info = run_gpu(m, "delta")
+    assert info["format"] == FORMAT_CODE[f"delta{bits}"]
+    assert_parity(m, y, TOL16)
