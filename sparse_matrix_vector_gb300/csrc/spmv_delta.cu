@@ -1,13 +1,16 @@
-// DELTA4 kernel of y = A x for sm_103a ("MACKO-SpMV" 2.2): 4-bit column
-// deltas, 8 per 32-bit word, fp16 values, fp32 accumulation.
+// Column-delta kernel of y = A x for sm_103a ("MACKO-SpMV" 2.2): deltas of
+// B = 2, 4 or 8 bits, 32 / B to a 32-bit word, fp16 values, fp32
+// accumulation.
 //
-// A work unit is a slice of one row (at most 512 packed words = 4096
-// entries) whose starting column, and each warp's starting column in it, the
-// planner stored, so units and warps are independent. Lane l of warp w
-// decodes LW consecutive words (LW = 1 or 2): a per-lane sum of their nibbles
-// and a 5-step __shfl_up_sync inclusive scan give the column before its
-// first entry; each word's eight columns come from byte-wise prefix sums of
-// its nibbles, and each entry is accumulated with one mixed-precision fma.
+// A work unit is a slice of one row (at most 512 packed words; 256 when
+// B = 2) whose starting column, and each warp's starting column in it, the
+// planner stored, so units and warps are independent. The plan keeps each
+// unit's starting columns, words and values together in one device block,
+// which one bulk copy stages. Lane l of warp w decodes LW words (LW = 1 or
+// 2): a per-lane sum of their fields and a 5-step __shfl_up_sync inclusive
+// scan give the column before its first entry; a word's columns come from
+// prefix sums of its fields computed inside the register, and each entry is
+// accumulated with one mixed-precision fma.
 // Producer / consumer scheduling: no CTA barrier per unit (see below).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -21,12 +24,13 @@ namespace spmv {
 namespace {
 
 struct DeltaArgs {
-  const uint32_t* __restrict__ words;   // 32 / B deltas of B bits per word
-  const __half* __restrict__ vals;      // 32 / B fp16 values per word
+  // one block per unit: kDeltaWarps starting columns, the unit's words
+  // (32 / B deltas of B bits each; padded to 4 words) and their values
+  // (32 / B fp16 per word; padded to 16 bytes)
+  const unsigned char* __restrict__ blocks;
   const __half* __restrict__ x;
   float* __restrict__ y;
-  const int4* __restrict__ units;       // {row | FIRST | LAST, wb, we, column base}
-  const int32_t* __restrict__ warp_base;  // kDeltaWarps starting columns per unit
+  const int4* __restrict__ units;       // {row | FIRST | LAST, wb, we, block offset / 16}
   const int32_t* __restrict__ cta_first;
   const int32_t* __restrict__ row_split;
   const SplitInfo* __restrict__ splits;  // {first_slot, n_units, row word, words/unit}
@@ -36,19 +40,15 @@ struct DeltaArgs {
   int n_cols;
 };
 
-// Shared-memory stage of one unit of deltas of B bits: the warps' starting
-// columns, the unit's words (aligned out to 4 words) and its values (32 / B
-// halves per word, aligned out to 16 bytes: 2 words when B = 8).
+// Shared-memory stage of one unit of deltas of B bits: a copy of the unit's
+// device block (the warps' starting columns, the words padded to 4, the
+// values; 32 / B halves per word).
 template <int B>
 struct DeltaStage {
-  static constexpr int kPerWord = 32 / B;
   static constexpr int kUnitWords = delta_unit_words(B);
-  static constexpr int kValAlign = kPerWord * 2 >= 16 ? 1 : 16 / (kPerWord * 2);  // words
   static constexpr int kBaseBytes = kDeltaWarps * 4;
-  static constexpr int kWordBytes = (kUnitWords + 8) * 4;
-  static constexpr int kValBytes = (kUnitWords + kValAlign) * kPerWord * 2;
-  static constexpr int kBytes = kBaseBytes + kWordBytes + kValBytes;
-  static_assert(kBaseBytes % 16 == 0 && kWordBytes % 16 == 0 && kValBytes % 16 == 0,
+  static constexpr int kBytes = (int)delta_block_bytes(B, kUnitWords);
+  static_assert(kBaseBytes % 16 == 0 && kBytes % 16 == 0 && kUnitWords % 4 == 0,
                 "stage regions must stay 16-byte aligned");
 };
 
@@ -169,36 +169,17 @@ __device__ __forceinline__ WordVals<B> load_vals(const unsigned char* s_vals, in
   return reinterpret_cast<const WordVals<B>*>(s_vals)[j];
 }
 
-// Thread 0: start the TMA copies of unit u (descriptor d) into a stage.
+// Producer lane: stage unit d (its whole device block, one bulk copy; copies
+// issued by one thread complete roughly one after another, so a unit costs one
+// of them).
 template <int B>
 __device__ __forceinline__ void issue_unit(const DeltaArgs& a, unsigned char* stage,
-                                           uint64_t* bar, int4* desc, int u, const int4 d,
+                                           uint64_t* bar, int4* desc, const int4 d,
                                            uint64_t pol) {
-  using St = DeltaStage<B>;
-  if (u < 0) {
-    *desc = make_int4(-1, 0, 0, 0);
-    mbar_arrive(bar);
-    return;
-  }
   *desc = d;
-  const int wb = d.y, we = d.z;
-  if (we == wb) {
-    mbar_arrive(bar);
-    return;
-  }
-  // bulk copies start on 16-byte boundaries and move multiples of 16 bytes:
-  // words from a multiple of 4, values from a multiple of kValAlign words
-  // (the device arrays carry a zero tail for the rounding up)
-  constexpr int VA = St::kValAlign;
-  const int wa = wb & ~3;
-  const uint32_t nwb = (uint32_t)(((we + 3) & ~3) - wa) * 4u;
-  const int va = wb & ~(VA - 1);
-  const uint32_t nvb = (uint32_t)(((we + VA - 1) & ~(VA - 1)) - va) * (uint32_t)(St::kPerWord * 2);
-  mbar_arrive_expect_tx(bar, St::kBaseBytes + nwb + nvb);
-  bulk_g2s(stage, a.warp_base + (size_t)u * kDeltaWarps, St::kBaseBytes, bar, pol);
-  bulk_g2s(stage + St::kBaseBytes, a.words + wa, nwb, bar, pol);
-  bulk_g2s(stage + St::kBaseBytes + St::kWordBytes, a.vals + (size_t)va * St::kPerWord, nvb,
-           bar, pol);
+  const uint32_t bytes = (uint32_t)delta_block_bytes(B, d.z - d.y);
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_g2s(stage, a.blocks + (size_t)d.w * 16, bytes, bar, pol);
 }
 
 // Thread 0, at the end of this CTA's piece of a row split into units: as
@@ -303,7 +284,7 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
           ok = false;
           break;
         }
-        issue_unit<B>(a, stages + s * St::kBytes, &s_full[g][s], &s_desc[g][s], u_begin + i,
+        issue_unit<B>(a, stages + s * St::kBytes, &s_full[g][s], &s_desc[g][s],
                       __ldg(a.units + u_begin + i), pol);
         issued = i + 1;
         if (issued == S) pdl_launch_dependents();
@@ -352,10 +333,8 @@ __global__ void __launch_bounds__(PcCfg<XS>::kThreads, PcCfg<XS>::kMinBlocks)
       piece_first = (rw & kUnitFirst) != 0;
     }
     const int* s_base = reinterpret_cast<const int*>(stage);
-    const uint32_t* s_words =
-        reinterpret_cast<const uint32_t*>(stage + St::kBaseBytes) + (wb & 3);
-    const unsigned char* s_vals = stage + St::kBaseBytes + St::kWordBytes +
-                                  (wb & (St::kValAlign - 1)) * St::kPerWord * 2;
+    const uint32_t* s_words = reinterpret_cast<const uint32_t*>(stage + St::kBaseBytes);
+    const unsigned char* s_vals = stage + St::kBaseBytes + ((n_w + 3) & ~3) * 4;
     // Lane l of warp w takes words 32 LW w + 32 q + l, q < LW: consecutive
     // lanes read consecutive words and values (conflict-free shared-memory
     // loads). The column before word q of a lane is the warp's starting column
@@ -458,12 +437,10 @@ int delta_set_smem_limit(int bits, size_t dyn) {
 int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   if (p.n_tiles == 0) return 0;
   DeltaArgs a;
-  a.words = p.words;
-  a.vals = static_cast<const __half*>(p.values);
+  a.blocks = p.blocks;
   a.x = static_cast<const __half*>(x);
   a.y = y;
   a.units = reinterpret_cast<const int4*>(p.tiles);
-  a.warp_base = p.warp_base;
   a.cta_first = p.cta_first;
   a.row_split = p.row_split;
   a.splits = p.splits;

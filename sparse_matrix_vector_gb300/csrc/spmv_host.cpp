@@ -493,10 +493,10 @@ void free_plan(spmv_plan* plan) {
   Plan* p = &plan->impl;
   {
     DeviceGuard g(p->device);
-    void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->words,
+    void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
-                    p->row_split, p->warp_base};
+                    p->row_split};
     for (void* b : bufs)
       if (b) cudaFree(b);
   }
@@ -660,6 +660,40 @@ spmv_status validate_delta(const spmv_delta* d, int64_t* nnz_out) {
   return SPMV_OK;
 }
 
+// Device layout of a DELTA plan: one block per work unit, each block the
+// unit's kDeltaWarps starting columns (32 bytes), its words (padded to a
+// multiple of 4) and its values (padded to a multiple of 16 bytes), so that
+// one bulk copy stages a whole unit. Unit descriptors' last field becomes the
+// block's offset in 16-byte steps.
+spmv_status build_delta_blocks(const spmv_delta* d, DeltaTables* t, std::vector<uint4>* out) {
+  const int32_t bits = delta_bits_of(d);
+  const int64_t per = delta_per_word(bits);
+  int64_t total = 0;  // in 16-byte steps
+  for (const Tile& u : t->units) total += delta_block_bytes(bits, (int64_t)u.c - u.b) / 16;
+  if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+  try {
+    out->assign((size_t)total, make_uint4(0, 0, 0, 0));
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  unsigned char* base = reinterpret_cast<unsigned char*>(out->data());
+  int64_t at = 0;
+  for (size_t k = 0; k < t->units.size(); ++k) {
+    Tile& u = t->units[k];
+    const int64_t wb = u.b, nw = (int64_t)u.c - u.b;
+    unsigned char* b = base + at * 16;
+    std::memcpy(b, t->warp_base.data() + k * kDeltaWarps, kDeltaWarps * 4);
+    if (nw > 0) {
+      std::memcpy(b + kDeltaWarps * 4, d->words + wb, (size_t)nw * 4);
+      std::memcpy(b + kDeltaWarps * 4 + ((nw + 3) & ~3) * 4, d->values + wb * per,
+                  (size_t)(nw * per) * 2);
+    }
+    u.d = (int32_t)at;
+    at += delta_block_bytes(bits, nw) / 16;
+  }
+  return SPMV_OK;
+}
+
 spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   spmv_status s;
   spmv_plan_info& info = p->info;
@@ -688,16 +722,12 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
     t.cta_first.push_back((int32_t)t.units.size());
   info.grid = p->grid;
   p->n_tiles = (int64_t)t.units.size();
-  const size_t e_alloc = (size_t)d->n_entries + 8 * kPadElems;
-  if ((s = dev_upload(&p->values, d->values, (size_t)d->n_entries * 2,
-                      e_alloc * 2)) != SPMV_OK) return s;
-  const size_t per_word = (size_t)delta_per_word(p->delta_bits);
-  if ((s = dev_upload(&p->words, d->words, (size_t)d->n_entries / per_word * 4,
-                      e_alloc / per_word * 4)) != SPMV_OK) return s;
+  std::vector<uint4> blocks;
+  if ((s = build_delta_blocks(d, &t, &blocks)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->blocks, blocks.data(), blocks.size() * 16,
+                      blocks.size() * 16)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->tiles, t.units.data(), t.units.size() * sizeof(Tile),
                       t.units.size() * sizeof(Tile))) != SPMV_OK) return s;
-  if ((s = dev_upload(&p->warp_base, t.warp_base.data(), t.warp_base.size() * 4,
-                      t.warp_base.size() * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->cta_first, t.cta_first.data(), t.cta_first.size() * 4,
                       t.cta_first.size() * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->row_split, t.row_split.data(), t.row_split.size() * 4,
@@ -711,9 +741,12 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   info.block = delta_block(p->x_smem);
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = delta_matrix_bytes(*d);
-  info.aux_bytes = (int64_t)(t.units.size() * sizeof(Tile) + t.warp_base.size() * 4 +
-                             t.cta_first.size() * 4 + t.row_split.size() * 4 +
-                             t.splits.size() * (sizeof(SplitInfo) + 4) +
+  // the unit blocks hold the matrix's values and deltas, the warps' starting
+  // columns and the 16-byte alignment padding; the rest of them is auxiliary
+  info.aux_bytes = (int64_t)(blocks.size() * 16) -
+                   (info.matrix_bytes - ((int64_t)d->n_rows + 1) * 4) +
+                   (int64_t)(t.units.size() * sizeof(Tile) + t.cta_first.size() * 4 +
+                             t.row_split.size() * 4 + t.splits.size() * (sizeof(SplitInfo) + 4) +
                              (size_t)t.n_chunks * 4);
   fill_bytes(&info, 2);
   return SPMV_OK;

@@ -47,9 +47,17 @@ constexpr int kDeltaWarps = kDeltaThreads / 32;
 constexpr int kDeltaUnitWords = 512;  // the most, over the widths
 constexpr int delta_unit_words(int bits) { return bits == 2 ? 256 : 512; }
 constexpr int kDeltaMaxLaneWords = kDeltaUnitWords / kDeltaThreads;
-// DELTA4 unit descriptor: {row | FIRST | LAST | log2(LW) << kUnitLgShift,
-// word_begin, word_end, column before the unit's first entry}; FIRST / LAST:
-// first / last unit of the row.
+// Bytes of a unit's device block (n_w words of b-bit deltas): the warps'
+// starting columns, the words padded to a multiple of 4 and the values padded
+// to a multiple of 16 bytes.
+constexpr int64_t delta_block_bytes(int bits, int64_t n_w) {
+  return kDeltaWarps * 4 + ((n_w + 3) & ~(int64_t)3) * 4 +
+         ((n_w * (32 / bits) * 2 + 15) & ~(int64_t)15);
+}
+// DELTA unit descriptor: {row | FIRST | LAST | log2(LW) << kUnitLgShift,
+// word_begin, word_end, offset of the unit's device block in 16-byte steps
+// (the planner leaves the column before the unit's first entry there, and
+// the block builder replaces it)}; FIRST / LAST: first / last unit of the row.
 constexpr uint32_t kUnitFirst = 1u << 31;
 constexpr uint32_t kUnitLast = 1u << 30;
 constexpr uint32_t kUnitLgShift = 28;
@@ -152,13 +160,12 @@ struct Plan {
   int32_t* row_ptr = nullptr;   // CSR offsets or DELTA entry offsets
   int32_t* col_idx = nullptr;   // CSR only
   void* values = nullptr;       // fp32 / fp16 (CSR) or fp16 (DELTA)
-  uint32_t* words = nullptr;    // DELTA packed deltas
+  unsigned char* blocks = nullptr;  // DELTA: one block per work unit
   // planner tables and scratch (device)
   Tile* tiles = nullptr;
   SplitInfo* splits = nullptr;
   int32_t* cta_first = nullptr;
   int32_t* row_split = nullptr;  // DELTA: split id per row or -1
-  int32_t* warp_base = nullptr;  // DELTA: kWarps starting columns per unit
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
   int32_t* status = nullptr;    // device status word
