@@ -1,4 +1,5 @@
-"""Oracle for y = A x and the 4-bit column-delta format (fp64, CPU, plain C).
+"""Oracle for y = A x, the column-delta format (fp64, CPU, plain C) and the
+sliced ELL layout (numpy).
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
 baseline leg may import this package; the library under test never does, and
@@ -15,6 +16,10 @@ What it computes, and the passages it follows:
   (delta coding, zero padding when a gap does not fit in 4 bits, eight nibbles
   per 32-bit word, row alignment). The readings taken where the page is
   silent or garbled are listed at the top of ``spmv_oracle.c``.
+
+* ``oracle.sell`` -- the sliced ELL layout and the choice of format by the
+  coefficient of variation of the row lengths ("CUDA CSR SpMV optimisation",
+  sections 2.1 and 2.2), in numpy; its readings are listed in its docstring.
 
 Parity pins (tests/test_oracle.py): dense brute force on tiny matrices,
 identity and permutation matrices, 5-point Laplacian rows on constant vectors,

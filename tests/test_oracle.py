@@ -5,6 +5,7 @@ in copies of the oracle's C source and checks that some pin fails for each.
 """
 import json
 import os
+import sys
 
 import numpy as np
 import pytest
@@ -232,9 +233,81 @@ def pin_delta_roundtrip_and_counts():
             assert np.array_equal(c[kept], m.col_idx[m.row_ptr[r]:m.row_ptr[r + 1]])
 
 
+GOLDEN_SELL = os.path.join(os.path.dirname(__file__), "golden", "sell_examples.json")
+
+
+def pin_sell_golden():
+    """Hand-worked sliced-ELL layouts (row order, length-sorted windows,
+    plain ELL as one slice) and the CV bands, boundaries included."""
+    from oracle import sell
+    g = json.load(open(GOLDEN_SELL))
+    mt = g["matrix"]
+    rp = np.array(mt["row_ptr"], np.int64)
+    ci = np.array(mt["col_idx"], np.int32)
+    vals = np.array(mt["values"], np.float32)
+    for lay in g["layouts"]:
+        m = sell.sell_encode(mt["n_cols"], rp, ci, vals, C=lay["C"], sigma=lay["sigma"])
+        assert m.slice_ptr.tolist() == lay["slice_ptr"], lay
+        assert m.perm.tolist() == lay["perm"], lay
+        assert m.cols.tolist() == lay["cols"], lay
+        assert m.vals.tolist() == lay["vals"], lay
+    for case in g["cv_cases"]:
+        rp2 = np.concatenate([[0], np.cumsum(case["lengths"])])
+        assert abs(sell.row_length_cv(rp2) - case["cv"]) <= 1e-12 * max(1.0, case["cv"])
+        assert list(sell.select_format(rp2)) == case["choice"], case
+
+
+def pin_sell_invariants():
+    """On random matrices (empty rows, ties, a ragged last slice): every row's
+    slots hold its entries in order and then value-0 padding at in-range
+    columns; slice widths are the slices' longest rows; perm is a permutation
+    whose windows are sorted by decreasing length, ties in row order; and
+    the product read from the layout equals the CSR product exactly."""
+    from oracle import sell
+    rng = np.random.default_rng(31)
+    for n, n_cols, C, sigma in ((101, 50, 32, 1), (101, 50, 32, 16), (77, 9, 7, 1000),
+                                (64, 200, 32, 64), (5, 3, 32, 1), (0, 4, 32, 1)):
+        lengths = rng.integers(0, min(n_cols, 12) + 1, n)
+        lengths[::9] = 0
+        rp = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+        ci = np.concatenate([np.sort(rng.choice(n_cols, L, replace=False)) for L in lengths]
+                            ).astype(np.int32) if n else np.zeros(0, np.int32)
+        vals = rng.uniform(0.5, 1.5, rp[-1]).astype(np.float32)
+        m = sell.sell_encode(n_cols, rp, ci, vals, C=C, sigma=sigma)
+        perm = m.perm[:n]
+        assert sorted(perm.tolist()) == list(range(n)) and np.all(m.perm[n:] == -1)
+        for w0 in range(0, n, max(sigma, 1)):
+            win = perm[w0:w0 + max(sigma, 1)]
+            L = lengths[win]
+            assert np.all(L[:-1] >= L[1:])
+            for a, b in zip(win[:-1], win[1:]):
+                if lengths[a] == lengths[b]:
+                    assert a < b
+        for sl in range(m.n_slices):
+            w = (m.slice_ptr[sl + 1] - m.slice_ptr[sl]) // C
+            rows = [r for r in m.perm[sl * C:(sl + 1) * C] if r >= 0]
+            assert w == max([lengths[r] for r in rows], default=0)
+            for lane in range(C):
+                r = m.perm[sl * C + lane]
+                at = m.slice_ptr[sl] + np.arange(w) * C + lane
+                if r < 0:
+                    assert np.all(m.vals[at] == 0) and np.all(m.cols[at] == 0)
+                    continue
+                L = lengths[r]
+                assert np.array_equal(m.cols[at[:L]], ci[rp[r]:rp[r + 1]])
+                assert np.array_equal(m.vals[at[:L]], vals[rp[r]:rp[r + 1]])
+                assert np.all(m.vals[at[L:]] == 0)
+                assert np.all(m.cols[at[L:]] == (ci[rp[r + 1] - 1] if L else 0))
+        x = rng.uniform(-1, 1, n_cols)
+        y1, s1 = sell.sell_spmv(m, x)
+        y2, s2 = oracle.csr_spmv(rp, ci, vals, x)
+        assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
+
+
 ALL_PINS = [pin_dense_bruteforce, pin_identity_and_permutation,
             pin_laplacian_constant, pin_row_of_ones, pin_scipy,
-            pin_delta_golden, pin_delta_widths_golden, pin_delta_roundtrip_and_counts]
+            pin_delta_golden, pin_delta_widths_golden, pin_delta_roundtrip_and_counts,
+            pin_sell_golden, pin_sell_invariants]
 
 
 # ---------------------------------------------------------------- tests
@@ -346,3 +419,42 @@ def test_llm_values():
     assert not np.any(m.values == 0)
     assert abs(m.nnz / 512 ** 2 - 0.5) < 0.01
     assert workloads.llm_seed(0.3) == 43 and workloads.llm_seed(0.9) == 49
+
+
+SELL_MUTANTS = {
+    "transposed_slots": ("at = slice_ptr[s] + k * C + lane", "at = slice_ptr[s] + lane * widths[s] + k"),
+    "ascending_sort": ('np.argsort(-lengths[w0:w1], kind="stable")',
+                       'np.argsort(lengths[w0:w1], kind="stable")'),
+    "padding_at_column_0": ("cols[at[~real]] = ci[rp[i + 1] - 1]", "pass"),
+    "sample_std": ("np.sqrt(np.mean((lengths - mean) ** 2))",
+                   "np.sqrt(np.sum((lengths - mean) ** 2) / max(lengths.size - 1, 1))"),
+    "strict_upper_band": ("if cv <= CV_CSR:", "if cv < CV_CSR:"),
+}
+
+
+@pytest.mark.parametrize("name", list(SELL_MUTANTS))
+def test_sell_planted_mistake_is_caught(name):
+    """A plausible mistake planted in the sliced-ELL oracle (on the CPU)
+    fails one of its pins."""
+    import types
+    import oracle.sell as real
+    old, new = SELL_MUTANTS[name]
+    src = open(real.__file__).read()
+    assert src.count(old) == 1
+    mutant = types.ModuleType("oracle.sell")
+    mutant.__package__ = "oracle"
+    exec(compile(src.replace(old, new), real.__file__ + ":" + name, "exec"), mutant.__dict__)
+    saved = sys.modules["oracle.sell"]
+    sys.modules["oracle.sell"] = mutant
+    oracle.sell = mutant
+    try:
+        failed = False
+        for pin in (pin_sell_golden, pin_sell_invariants):
+            try:
+                pin()
+            except AssertionError:
+                failed = True
+        assert failed, f"planted mistake {name} passed every pin"
+    finally:
+        sys.modules["oracle.sell"] = saved
+        oracle.sell = saved
