@@ -45,10 +45,13 @@ WORKLOADS = {
     "laplacian": ("laplacian", "csr", "laplacian_5pt_1000x999_f32_csr"),
     "powerlaw": ("powerlaw", "csr", "powerlaw_zipf2_916428_5105039nnz_f32_csr"),
     "fem": ("fem", "csr", "fem_hex_120x60x30_3dof_f32_csr"),
+    "laplacian_sell": ("laplacian", "sell", "laplacian_5pt_1000x999_f32_sell32"),
+    "fem_sell": ("fem", "sell", "fem_hex_120x60x30_3dof_f32_sell32"),
 }
 for _s in (30, 50, 70, 90):
     WORKLOADS[f"llm{_s}_csr"] = (f"llm{_s}", "csr",
                                  f"llm_12288x12288_sparsity{_s}_f16_csr")
+    WORKLOADS[f"llm{_s}_sell"] = (f"llm{_s}", "sell", f"llm_12288x12288_sparsity{_s}_f16_sell32")
     for _b in (2, 4, 8):
         WORKLOADS[f"llm{_s}_delta{_b}"] = (f"llm{_s}", f"delta{_b}",
                                            f"llm_12288x12288_sparsity{_s}_f16_delta{_b}")
@@ -74,8 +77,9 @@ def kernel_source_sha(fmt: str) -> str:
     device header followed by the kernel's file)."""
     csrc = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("spmv_device.cuh",
-                 "spmv_delta.cu" if fmt.startswith("delta") else "spmv_csr.cu"):
+    kernel_file = ("spmv_delta.cu" if fmt.startswith("delta")
+                   else "spmv_sell.cu" if fmt == "sell" else "spmv_csr.cu")
+    for name in ("spmv_device.cuh", kernel_file):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -193,6 +197,14 @@ def oracle_call(m, fmt, frac):
         nbytes = (enc.n_entries * 2 + enc.n_entries * bits // 8 + (rows + 1) * 4
                   + m.n_cols * 2 + rows * 4)
         return rows, nbytes, int(rp[-1]), (lambda: oracle.delta_spmv(enc, m.x))
+    if fmt == "sell":
+        # y = A x is the CSR definition; the bytes are those the sliced
+        # layout of these rows stores (rows in order)
+        from oracle import sell
+        slots, slices = sell.sell_slot_count(rp, 32, 1)
+        nbytes = (slots * (vals.dtype.itemsize + 4) + (slices + 1) * 4
+                  + m.n_cols * m.x.dtype.itemsize + rows * 4)
+        return rows, nbytes, int(rp[-1]), (lambda: oracle.csr_spmv(rp, ci, vals, m.x))
     nbytes = (int(rp[-1]) * (vals.dtype.itemsize + 4) + (rows + 1) * 4
               + m.n_cols * m.x.dtype.itemsize + rows * 4)
     return rows, nbytes, int(rp[-1]), (lambda: oracle.csr_spmv(rp, ci, vals, m.x))

@@ -7,8 +7,11 @@
  *   - DELTA4: fp16 values with 4-bit column deltas packed eight to a 32-bit
  *     word, zero-valued padding entries where a gap does not fit in 4 bits,
  *     and CSR-like row pointers over the stored entries (DELTA2 / DELTA8:
- *     the same with 2- or 8-bit deltas, 16 or 4 to a word).
- * x is fp32 for fp32 CSR and fp16 otherwise; y is always fp32 and every
+ *     the same with 2- or 8-bit deltas, 16 or 4 to a word); or
+ *   - SELL: sliced ELLPACK, fp32 or fp16 values: rows cut into slices of
+ *     SPMV_SELL_C rows, each slice padded with zeros to its longest row and
+ *     stored column-major (optionally rows sorted by length first).
+ * x is fp32 for fp32 values and fp16 otherwise; y is always fp32 and every
  * product is accumulated in fp32.
  *
  * Sources (web pages, by title and section):
@@ -21,6 +24,9 @@
  *           struct {values with zero placeholders, 4-bit deltas, row
  *           pointers} and its four encoding steps; section 2.2: the warp
  *           decode (prefix sum of deltas) and half2 multiply.
+ *           Section 2.1 also compares COO / CSR / ELL / HYB, and section
+ *           2.2 chooses among them by the coefficient of variation (CV) of
+ *           the row lengths.
  *   [SPGEMM] "Hash-based multi-phase SpGEMM" (mlqm.cn), section 2.1.1: rows
  *           grouped by work into bins served by partial-warp, warp and
  *           block-per-row kernels; section 5.2: batching of tiny rows.
@@ -43,7 +49,10 @@
 extern "C" {
 #endif
 
-#define SPMV_ABI_VERSION 2
+#define SPMV_ABI_VERSION 3
+
+/* Rows per slice of the SELL format (one warp of the kernel per slice). */
+#define SPMV_SELL_C 32
 
 typedef enum spmv_status {
   SPMV_OK = 0,
@@ -67,9 +76,17 @@ typedef enum spmv_format {
   SPMV_FORMAT_DELTA4 = 1,  /* [MACKO] section 2.1, 4-bit deltas               */
   SPMV_FORMAT_DELTA2 = 2,  /* the same format with 2-bit deltas ([MACKO] 3.3) */
   SPMV_FORMAT_DELTA8 = 3,  /* the same format with 8-bit deltas ([MACKO] 3.3) */
-  SPMV_FORMAT_DELTA_AUTO = 4 /* the width spmv_delta_select_bits picks under
-                                SPMV_DELTA_FEWEST_BYTES; plans and their info
-                                report the chosen width's format code       */
+  SPMV_FORMAT_DELTA_AUTO = 4, /* the width spmv_delta_select_bits picks under
+                                 SPMV_DELTA_FEWEST_BYTES; plans and their info
+                                 report the chosen width's format code      */
+  SPMV_FORMAT_SELL = 5,   /* sliced ELL ([CSR] 2.1 ELL, in slices of
+                             SPMV_SELL_C rows); sigma from the options      */
+  SPMV_FORMAT_AUTO = 6    /* CSR or SELL by the CV of the row lengths
+                             (spmv_select_format), except that matrices
+                             whose rows hold more than 128 nonzeros on
+                             average take CSR (a lane per row serialises
+                             long rows); plans and their info report the
+                             chosen format                                  */
 } spmv_format;
 
 /* How spmv_delta_select_bits picks a delta width ([MACKO] section 3.3). */
@@ -129,6 +146,33 @@ typedef struct spmv_delta {
   int32_t reserved;
 } spmv_delta;
 
+/* A sliced-ELL matrix in HOST memory ([CSR] section 2.1, ELL in slices), as
+ * produced by spmv_convert_sell. Rows are first put in sorted order: inside
+ * each window of `sigma` consecutive rows, by decreasing length, rows of
+ * equal length in their original order (sigma = 1: the original order). The
+ * sorted rows are cut into slices of C = SPMV_SELL_C; slice s is as wide as
+ * its longest row, w_s = (slice_ptr[s+1] - slice_ptr[s]) / C, and slot
+ * (k, lane) of slice s, at slice_ptr[s] + k * C + lane, holds the k-th
+ * stored entry (in CSR order) of the slice's lane-th row. Slots past a row's
+ * length hold value 0 at the row's last column (column 0 for an empty row
+ * and for lanes of the last slice that hold no row).
+ * perm[s * C + lane] is the original row index of that lane's row, or -1. */
+typedef struct spmv_sell {
+  int32_t n_rows;
+  int32_t n_cols;
+  int64_t nnz;
+  int32_t C;                /* SPMV_SELL_C                                   */
+  int32_t sigma;            /* sorting window (1: rows in order)             */
+  int64_t n_slices;         /* ceil(n_rows / C)                              */
+  int64_t n_slots;          /* stored slots, padding included                */
+  int64_t* slice_ptr;       /* n_slices + 1 slot offsets                     */
+  int32_t* perm;            /* n_slices * C original rows (-1: none)         */
+  int32_t* cols;            /* n_slots column indices                        */
+  void* values;             /* n_slots elements of value_dtype               */
+  spmv_dtype value_dtype;
+  int32_t reserved;
+} spmv_sell;
+
 /* Planner knobs ([SPGEMM] section 2.1.1 grouping; [MACKO] section 3.3
  * dynamic scheduling). Zero / negative fields mean "library default". */
 typedef struct spmv_plan_options {
@@ -149,7 +193,11 @@ typedef struct spmv_plan_options {
                             nonzeros for the x gathers: 0 auto, 1 chunks of
                             8 consecutive per thread, 2 element-interleaved
                             (a warp's lanes take consecutive nonzeros)     */
-  int32_t reserved[7];
+  int32_t sell_sigma;    /* SELL: rows are sorted by decreasing length inside
+                            windows of this many rows before slicing; 1 keeps
+                            the row order; 0 chooses by the CV of the row
+                            lengths as spmv_select_format does             */
+  int32_t reserved[6];
 } spmv_plan_options;
 
 /* What the planner decided; filled by spmv_plan_inspect / spmv_plan_get_info.
@@ -219,6 +267,26 @@ spmv_status spmv_convert_bits(const spmv_csr* csr, int32_t bits, spmv_delta* out
 spmv_status spmv_delta_select_bits(const spmv_csr* csr, spmv_delta_policy policy,
                                    int32_t* bits, int64_t entries[3]);
 
+/* [CSR] section 2.1, ELL in slices: lay a CSR matrix (fp32 or fp16 values;
+ * any column order, repeats allowed) out as spmv_sell with sorting window
+ * sigma >= 1. The library allocates the arrays with malloc; release them
+ * with spmv_sell_free. On error *out is left zeroed. Errors: INVALID_ARG
+ * (sigma < 1), BAD_ROW_PTR, COL_OUT_OF_RANGE, TOO_LARGE (more than 2^31 - 1
+ * slots), OUT_OF_MEMORY. */
+spmv_status spmv_convert_sell(const spmv_csr* csr, int32_t sigma, spmv_sell* out);
+
+/* Free the arrays of a spmv_sell filled by spmv_convert_sell and zero it. */
+void spmv_sell_free(spmv_sell* s);
+
+/* [CSR] section 2.2: choose a format by the coefficient of variation of the
+ * row lengths, CV = (population standard deviation) / mean (0 when the mean
+ * is 0): CV < 0.3 -> SELL with sigma 1 (ELL); 0.3 <= CV <= 0.7 -> SELL with
+ * sigma 1024 (rows sorted by length in windows: the page's hybrid ELL + COO
+ * band, served by sorted slices); CV > 0.7 -> CSR (sigma 0). Any output
+ * pointer may be NULL. Errors: INVALID_ARG, BAD_ROW_PTR. */
+spmv_status spmv_select_format(const spmv_csr* csr, spmv_format* format, int32_t* sigma,
+                               double* cv);
+
 /* Free the arrays of a spmv_delta filled by spmv_convert and zero it. */
 void spmv_delta_free(spmv_delta* d);
 
@@ -254,7 +322,7 @@ spmv_status spmv_plan_create_delta(const spmv_delta* delta,
 spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info);
 
 /* y = A x, asynchronously on `stream` (a cudaStream_t; NULL = legacy
- * default stream). x_dev: n_cols elements (fp32 for fp32 CSR plans, fp16
+ * default stream). x_dev: n_cols elements (fp32 for fp32-value plans, fp16
  * otherwise), aligned to its element size; y_dev: n_rows fp32, aligned to 4
  * bytes, fully overwritten (rows without nonzeros get 0). x and y must not
  * overlap. DELTA4 plans multiply padding entries as 0 * x[c], so x must be

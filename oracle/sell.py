@@ -152,3 +152,14 @@ def sell_spmv(m: SellMatrix, x, with_abs: bool = True):
     c = np.concatenate(cols) if cols else np.zeros(0, np.int32)
     v = np.concatenate(vals) if vals else np.zeros(0, m.vals.dtype)
     return csr_spmv(row_ptr, c, v, x, with_abs=with_abs)
+
+
+def sell_slot_count(row_ptr, C: int = 32, sigma: int = 1) -> tuple:
+    """(slots, slices) of the sliced layout, from the row lengths alone."""
+    lengths = np.diff(np.asarray(row_ptr, dtype=np.int64))
+    n = lengths.size
+    n_slices = (n + C - 1) // C
+    padded = np.zeros(n_slices * C, dtype=np.int64)
+    padded[:n] = lengths[sell_order(lengths, sigma)]
+    widths = padded.reshape(n_slices, C).max(axis=1) if n_slices else padded[:0]
+    return int(widths.sum()) * C, n_slices

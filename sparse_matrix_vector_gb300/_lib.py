@@ -16,7 +16,8 @@ c_p = ctypes.c_void_p
 
 SPMV_F32, SPMV_F16 = 0, 1
 SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA8 = 0, 1, 2, 3
-SPMV_FORMAT_DELTA_AUTO = 4
+SPMV_FORMAT_DELTA_AUTO, SPMV_FORMAT_SELL, SPMV_FORMAT_AUTO = 4, 5, 6
+SPMV_SELL_C = 32
 SPMV_DELTA_FEWEST_BYTES, SPMV_DELTA_SPARSITY_TABLE = 0, 1
 
 STATUS_NAMES = {
@@ -42,11 +43,20 @@ class spmv_delta(ctypes.Structure):
                 ("delta_bits", c_i32), ("reserved", c_i32)]
 
 
+class spmv_sell(ctypes.Structure):
+    _fields_ = [("n_rows", c_i32), ("n_cols", c_i32), ("nnz", c_i64),
+                ("C", c_i32), ("sigma", c_i32), ("n_slices", c_i64),
+                ("n_slots", c_i64), ("slice_ptr", c_p), ("perm", c_p),
+                ("cols", c_p), ("values", c_p), ("value_dtype", ctypes.c_int),
+                ("reserved", c_i32)]
+
+
 class spmv_plan_options(ctypes.Structure):
     _fields_ = [("tile_nnz", c_i32), ("tile_rows", c_i32),
                 ("cta_row_min", c_i32), ("split_row_min", c_i32),
                 ("split_chunk", c_i32), ("x_smem", c_i32), ("reduce", c_i32),
-                ("lanes", c_i32), ("interleave", c_i32), ("reserved", c_i32 * 7)]
+                ("lanes", c_i32), ("interleave", c_i32), ("sell_sigma", c_i32),
+                ("reserved", c_i32 * 6)]
 
 
 class spmv_plan_info(ctypes.Structure):
@@ -73,6 +83,11 @@ SIGNATURES = {
     "spmv_delta_select_bits": (ctypes.c_int, [ctypes.POINTER(spmv_csr), ctypes.c_int,
                                               ctypes.POINTER(c_i32), ctypes.POINTER(c_i64)]),
     "spmv_delta_free": (None, [ctypes.POINTER(spmv_delta)]),
+    "spmv_convert_sell": (ctypes.c_int, [ctypes.POINTER(spmv_csr), c_i32,
+                                         ctypes.POINTER(spmv_sell)]),
+    "spmv_sell_free": (None, [ctypes.POINTER(spmv_sell)]),
+    "spmv_select_format": (ctypes.c_int, [ctypes.POINTER(spmv_csr), ctypes.POINTER(ctypes.c_int),
+                                          ctypes.POINTER(c_i32), ctypes.POINTER(ctypes.c_double)]),
     "spmv_plan_inspect": (ctypes.c_int, [ctypes.POINTER(spmv_csr), ctypes.c_int,
                                          ctypes.POINTER(spmv_plan_options),
                                          ctypes.POINTER(spmv_plan_info)]),

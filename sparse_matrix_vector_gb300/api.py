@@ -15,11 +15,14 @@ import numpy as np
 from . import _lib
 from ._lib import (SPMV_DELTA_FEWEST_BYTES, SPMV_DELTA_SPARSITY_TABLE, SPMV_F16, SPMV_F32,
                    SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA4,
-                   SPMV_FORMAT_DELTA8, SPMV_FORMAT_DELTA_AUTO)
+                   SPMV_FORMAT_DELTA8, SPMV_FORMAT_DELTA_AUTO, SPMV_FORMAT_AUTO,
+                   SPMV_FORMAT_SELL)
 
 FORMATS = {"csr": SPMV_FORMAT_CSR, "delta4": SPMV_FORMAT_DELTA4,
            "delta2": SPMV_FORMAT_DELTA2, "delta8": SPMV_FORMAT_DELTA8,
-           "delta": SPMV_FORMAT_DELTA_AUTO}
+           "delta": SPMV_FORMAT_DELTA_AUTO, "sell": SPMV_FORMAT_SELL,
+           "auto": SPMV_FORMAT_AUTO}
+FORMAT_NAMES = {v: k for k, v in FORMATS.items()}
 DELTA_POLICIES = {"fewest_bytes": SPMV_DELTA_FEWEST_BYTES,
                   "sparsity_table": SPMV_DELTA_SPARSITY_TABLE}
 
@@ -168,6 +171,59 @@ def spmv_delta_select_bits(row_ptr, col_idx, values, n_cols: int,
     return int(bits.value), {2: int(entries[0]), 4: int(entries[1]), 8: int(entries[2])}
 
 
+@dataclass
+class SellMatrix:
+    """A sliced-ELL matrix copied out of the library (numpy arrays)."""
+    n_rows: int
+    n_cols: int
+    nnz: int
+    C: int
+    sigma: int
+    slice_ptr: np.ndarray   # int64[n_slices + 1]
+    perm: np.ndarray        # int32[n_slices * C], -1 past the last row
+    cols: np.ndarray        # int32[n_slots]
+    values: np.ndarray      # float32 or float16 [n_slots]
+
+
+def spmv_convert_sell(row_ptr, col_idx, values, n_cols: int, sigma: int = 1) -> SellMatrix:
+    """CSR (fp32 or fp16 values) -> sliced ELL on the host, by the library's
+    converter (spmv_convert_sell)."""
+    h = _host_csr(row_ptr, col_idx, values, n_cols)
+    sl = _lib.spmv_sell()
+    lib = _lib.load()
+    _check(lib.spmv_convert_sell(ctypes.byref(h.struct), int(sigma), ctypes.byref(sl)),
+           "spmv_convert_sell")
+    try:
+        ns, slots = int(sl.n_slices), int(sl.n_slots)
+
+        def arr(ptr, ctype, n, dtype):
+            if n == 0:
+                return np.zeros(0, dtype)
+            return np.ctypeslib.as_array(ctypes.cast(ptr, ctypes.POINTER(ctype)),
+                                         shape=(n,)).copy().view(dtype)
+        vdt = np.float32 if sl.value_dtype == SPMV_F32 else np.float16
+        vct = ctypes.c_uint32 if sl.value_dtype == SPMV_F32 else ctypes.c_uint16
+        return SellMatrix(int(sl.n_rows), int(sl.n_cols), int(sl.nnz), int(sl.C),
+                          int(sl.sigma),
+                          arr(sl.slice_ptr, ctypes.c_int64, ns + 1, np.int64),
+                          arr(sl.perm, ctypes.c_int32, ns * int(sl.C), np.int32),
+                          arr(sl.cols, ctypes.c_int32, slots, np.int32),
+                          arr(sl.values, vct, slots, vdt))
+    finally:
+        lib.spmv_sell_free(ctypes.byref(sl))
+
+
+def spmv_select_format(row_ptr, col_idx, values, n_cols: int):
+    """Format by the CV of the row lengths: returns (format name, sigma, cv)
+    with format "sell" or "csr"."""
+    h = _host_csr(row_ptr, col_idx, values, n_cols)
+    fmt, sigma, cv = ctypes.c_int(), ctypes.c_int32(), ctypes.c_double()
+    _check(_lib.load().spmv_select_format(ctypes.byref(h.struct), ctypes.byref(fmt),
+                                          ctypes.byref(sigma), ctypes.byref(cv)),
+           "spmv_select_format")
+    return FORMAT_NAMES[int(fmt.value)], int(sigma.value), float(cv.value)
+
+
 def spmv_plan_inspect(row_ptr, col_idx, values, n_cols: int, format="csr",
                       options=None) -> dict:
     """Host-only planner dry run (no device needed)."""
@@ -192,9 +248,7 @@ class Plan:
         _check(_lib.load().spmv_plan_get_info(self._handle, ctypes.byref(info)),
                "spmv_plan_get_info")
         self.info = _info_dict(info)
-        self.x_dtype_code = (SPMV_F32 if (self.info["format"] == SPMV_FORMAT_CSR
-                                          and self.info["value_dtype"] == SPMV_F32)
-                             else SPMV_F16)
+        self.x_dtype_code = SPMV_F32 if self.info["value_dtype"] == SPMV_F32 else SPMV_F16
 
     @property
     def handle(self):

@@ -146,9 +146,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // Launch with programmatic stream serialization: the kernel may begin while
 // the previous kernel on the stream drains; it orders itself with
-// griddepcontrol.wait before touching anything that kernel may write. Every
-// CTA of these grids is resident at once (persistent grids), so CTAs that
-// wait can never keep the kernel they wait on from running.
+// griddepcontrol.wait before touching anything that kernel may write. The
+// dependent grid is launched only once every CTA of the earlier one has
+// executed griddepcontrol.launch_dependents or exited, so by then all of the
+// earlier kernel's CTAs have started, and CTAs that wait can never keep it
+// from running.
 int launch_pdl(const void* fn, int grid, int block, size_t smem, void* stream, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -49,9 +50,13 @@ constexpr int kAssumedSms = 152;             // for host-only inspection
 size_t dtype_size(spmv_dtype t) { return t == SPMV_F16 ? 2 : 4; }
 
 bool valid_dtype(int t) { return t == SPMV_F32 || t == SPMV_F16; }
+bool is_delta_format(int f) {
+  return f == SPMV_FORMAT_DELTA4 || f == SPMV_FORMAT_DELTA2 || f == SPMV_FORMAT_DELTA8 ||
+         f == SPMV_FORMAT_DELTA_AUTO;
+}
 bool valid_format(int f) {
-  return f == SPMV_FORMAT_CSR || f == SPMV_FORMAT_DELTA4 || f == SPMV_FORMAT_DELTA2 ||
-         f == SPMV_FORMAT_DELTA8 || f == SPMV_FORMAT_DELTA_AUTO;
+  return f == SPMV_FORMAT_CSR || is_delta_format(f) || f == SPMV_FORMAT_SELL ||
+         f == SPMV_FORMAT_AUTO;
 }
 
 int32_t format_delta_bits(int f) {
@@ -148,8 +153,10 @@ Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype) {
   r.reduce = -1;
   r.lanes_log2 = 0;
   r.interleave = 0;
+  r.sell_sigma = 0;
   if (o) {
     if (o->interleave == 1 || o->interleave == 2) r.interleave = o->interleave;
+    if (o->sell_sigma > 0) r.sell_sigma = o->sell_sigma;
     if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, cap - 16);
     if (o->tile_rows > 0) r.tile_rows = std::min(o->tile_rows, kTileRowsCap);
     if (o->cta_row_min > 0) r.cta_row_min = o->cta_row_min;
@@ -496,7 +503,7 @@ void free_plan(spmv_plan* plan) {
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
-                    p->row_split};
+                    p->row_split, p->perm};
     for (void* b : bufs)
       if (b) cudaFree(b);
   }
@@ -517,7 +524,7 @@ spmv_status bind_device(Plan* p) {
 }
 
 spmv_status common_buffers(Plan* p) {
-  const size_t xs = p->dtype == SPMV_F32 && p->format == SPMV_FORMAT_CSR ? 4 : 2;
+  const size_t xs = p->dtype == SPMV_F32 ? 4 : 2;
   spmv_status s;
   if ((s = dev_upload(&p->status, nullptr, 0, 16)) != SPMV_OK) return s;
   if ((s = dev_alloc(&p->x_stage, (size_t)p->n_cols * xs + 16)) != SPMV_OK)
@@ -657,6 +664,189 @@ spmv_status validate_delta(const spmv_delta* d, int64_t* nnz_out) {
     if (rp[r + 1] > rp[r] && c >= d->n_cols) return SPMV_ERR_COL_OUT_OF_RANGE;
   }
   *nnz_out = nnz;
+  return SPMV_OK;
+}
+
+// ------------------------------------------------------------ SELL
+// "CUDA CSR SpMV optimisation" 2.1 (ELL) and 2.2 (choice by the CV of the
+// row lengths); the layout is described with spmv_sell in the header.
+
+constexpr int32_t kSellSigmaSorted = 1024;  // window of the middle CV band
+constexpr int32_t kSellMaxMeanRow = 128;    // AUTO: longer rows on average go to CSR
+
+double row_length_cv(const spmv_csr* m) {
+  if (m->n_rows == 0) return 0.0;
+  const double mean = (double)m->nnz / (double)m->n_rows;
+  if (mean == 0.0) return 0.0;
+  double ss = 0.0;
+  for (int32_t r = 0; r < m->n_rows; ++r) {
+    const double d = (double)(m->row_ptr[r + 1] - m->row_ptr[r]) - mean;
+    ss += d * d;
+  }
+  return std::sqrt(ss / (double)m->n_rows) / mean;
+}
+
+void choose_by_cv(double cv, spmv_format* f, int32_t* sigma) {
+  if (cv < 0.3) {
+    *f = SPMV_FORMAT_SELL;
+    *sigma = 1;
+  } else if (cv <= 0.7) {
+    *f = SPMV_FORMAT_SELL;
+    *sigma = kSellSigmaSorted;
+  } else {
+    *f = SPMV_FORMAT_CSR;
+    *sigma = 0;
+  }
+}
+
+// The sliced layout of a validated CSR matrix (arrays malloc'ed into *out).
+spmv_status sell_layout(const spmv_csr* m, int32_t sigma, spmv_sell* out) {
+  constexpr int C = SPMV_SELL_C;
+  const int32_t n = m->n_rows;
+  const int32_t* rp = m->row_ptr;
+  std::vector<int32_t> order;
+  try {
+    order.resize((size_t)n);
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  for (int32_t i = 0; i < n; ++i) order[i] = i;
+  if (sigma > 1)
+    for (int64_t w0 = 0; w0 < n; w0 += sigma) {
+      const int64_t w1 = std::min<int64_t>(n, w0 + sigma);
+      std::stable_sort(order.begin() + w0, order.begin() + w1, [&](int32_t a, int32_t b) {
+        return rp[a + 1] - rp[a] > rp[b + 1] - rp[b];
+      });
+    }
+  const int64_t n_slices = ((int64_t)n + C - 1) / C;
+  out->slice_ptr = static_cast<int64_t*>(std::malloc((size_t)(n_slices + 1) * 8));
+  out->perm = static_cast<int32_t*>(std::malloc((size_t)std::max<int64_t>(n_slices * C, 1) * 4));
+  if (!out->slice_ptr || !out->perm) return SPMV_ERR_OUT_OF_MEMORY;
+  out->slice_ptr[0] = 0;
+  for (int64_t sl = 0; sl < n_slices; ++sl) {
+    int64_t w = 0;
+    for (int64_t q = sl * C; q < std::min<int64_t>((sl + 1) * C, n); ++q)
+      w = std::max<int64_t>(w, rp[order[q] + 1] - rp[order[q]]);
+    out->slice_ptr[sl + 1] = out->slice_ptr[sl] + w * C;
+  }
+  const int64_t slots = out->slice_ptr[n_slices];
+  if (slots > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+  const size_t vs = dtype_size(m->value_dtype);
+  out->cols = static_cast<int32_t*>(std::calloc((size_t)std::max<int64_t>(slots, 1), 4));
+  out->values = std::calloc((size_t)std::max<int64_t>(slots, 1), vs);
+  if (!out->cols || !out->values) return SPMV_ERR_OUT_OF_MEMORY;
+  const unsigned char* src = static_cast<const unsigned char*>(m->values);
+  unsigned char* dst = static_cast<unsigned char*>(out->values);
+  for (int64_t q = 0; q < n_slices * C; ++q) {
+    out->perm[q] = q < n ? order[q] : -1;
+    if (q >= n) continue;
+    const int32_t i = order[q];
+    const int64_t sl = q / C, lane = q % C;
+    const int64_t w = (out->slice_ptr[sl + 1] - out->slice_ptr[sl]) / C;
+    const int64_t len = rp[i + 1] - rp[i];
+    for (int64_t k = 0; k < w; ++k) {
+      const int64_t at = out->slice_ptr[sl] + k * C + lane;
+      if (k < len) {
+        out->cols[at] = m->col_idx[rp[i] + k];
+        std::memcpy(dst + at * vs, src + (rp[i] + k) * vs, vs);
+      } else if (len > 0) {
+        out->cols[at] = m->col_idx[rp[i + 1] - 1];  // value stays 0
+      }
+    }
+  }
+  out->n_rows = n;
+  out->n_cols = m->n_cols;
+  out->nnz = m->nnz;
+  out->C = C;
+  out->sigma = sigma;
+  out->n_slices = n_slices;
+  out->n_slots = slots;
+  out->value_dtype = m->value_dtype;
+  return SPMV_OK;
+}
+
+// Bytes the sliced layout stores: every slot's column and value, the slice
+// offsets (int32 on the device) and, for sorted rows, the row of each lane.
+int64_t sell_matrix_bytes(const spmv_sell& sl) {
+  return sl.n_slots * (4 + (int64_t)dtype_size(sl.value_dtype)) + (sl.n_slices + 1) * 4 +
+         (sl.sigma > 1 ? sl.n_slices * sl.C * 4 : 0);
+}
+
+void sell_info(const spmv_sell& sl, spmv_plan_info* info) {
+  info->n_entries = sl.n_slots;
+  info->n_tiles = sl.n_slices;
+  info->tiles_per_bin[0] = sl.n_slices;
+  info->rows_per_bin[1] = sl.n_rows;
+  info->grid = (int32_t)((sl.n_slices + kSellSlicesPerCta - 1) / kSellSlicesPerCta);
+  info->block = kSellSlicesPerCta * 32;
+  info->launches_per_run = sl.n_rows > 0 ? 1 : 0;
+  info->matrix_bytes = sell_matrix_bytes(sl);
+  fill_bytes(info, dtype_size(sl.value_dtype));
+}
+
+spmv_status create_sell_plan(const spmv_sell* sl, Plan* p) {
+  spmv_status s;
+  if ((s = bind_device(p)) != SPMV_OK) return s;
+  const size_t vs = dtype_size(sl->value_dtype);
+  std::vector<int32_t> sp;
+  try {
+    sp.resize((size_t)sl->n_slices + 1);
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  for (int64_t i = 0; i <= sl->n_slices; ++i) sp[i] = (int32_t)sl->slice_ptr[i];
+  if ((s = dev_upload(&p->row_ptr, sp.data(), sp.size() * 4, sp.size() * 4)) != SPMV_OK)
+    return s;
+  if (sl->sigma > 1 &&
+      (s = dev_upload(&p->perm, sl->perm, (size_t)sl->n_slices * sl->C * 4,
+                      (size_t)sl->n_slices * sl->C * 4)) != SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->col_idx, sl->cols, (size_t)sl->n_slots * 4,
+                      (size_t)sl->n_slots * 4 + 16)) != SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->values, sl->values, (size_t)sl->n_slots * vs,
+                      (size_t)sl->n_slots * vs + 16)) != SPMV_OK)
+    return s;
+  if ((s = common_buffers(p)) != SPMV_OK) return s;
+  p->n_tiles = sl->n_slices;
+  p->n_entries = sl->n_slots;
+  sell_info(*sl, &p->info);
+  p->grid = p->info.grid;
+  p->info.aux_bytes = 16;
+  return SPMV_OK;
+}
+
+// Validate a CSR input for `format` and settle the automatic choices: the
+// delta width (DELTA_AUTO), CSR or SELL by the CV of the row lengths (AUTO),
+// and SELL's sorting window (options, else by the CV band; a SELL forced on
+// a matrix whose CV points to CSR gets the sorted window).
+spmv_status resolve_format(const spmv_csr* m, const Options& o, spmv_format* format,
+                           int32_t* sigma) {
+  const bool delta = is_delta_format(*format);
+  spmv_status s = validate_csr(m, delta);
+  if (s != SPMV_OK) return s;
+  if (delta && m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
+  *sigma = 0;
+  if (*format == SPMV_FORMAT_DELTA_AUTO) {
+    int32_t b = 4;
+    if ((s = spmv_delta_select_bits(m, SPMV_DELTA_FEWEST_BYTES, &b, nullptr)) != SPMV_OK)
+      return s;
+    *format = delta_format(b);
+  }
+  if (*format == SPMV_FORMAT_AUTO || *format == SPMV_FORMAT_SELL) {
+    spmv_format f;
+    int32_t sg;
+    choose_by_cv(row_length_cv(m), &f, &sg);
+    // a lane per row serialises a long row's gathers: the CV band is taken
+    // only for rows of at most kSellMaxMeanRow stored entries on average
+    if (*format == SPMV_FORMAT_AUTO)
+      *format = (f == SPMV_FORMAT_SELL &&
+                 (double)m->nnz > (double)kSellMaxMeanRow * (double)m->n_rows)
+                    ? SPMV_FORMAT_CSR
+                    : f;
+    if (*format == SPMV_FORMAT_SELL)
+      *sigma = o.sell_sigma > 0 ? o.sell_sigma : (f == SPMV_FORMAT_SELL ? sg : kSellSigmaSorted);
+  }
   return SPMV_OK;
 }
 
@@ -884,6 +1074,40 @@ spmv_status spmv_delta_select_bits(const spmv_csr* m, spmv_delta_policy policy, 
   return SPMV_OK;
 }
 
+spmv_status spmv_convert_sell(const spmv_csr* m, int32_t sigma, spmv_sell* out) {
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (sigma < 1) return SPMV_ERR_INVALID_ARG;
+  spmv_status s = validate_csr(m, false);
+  if (s != SPMV_OK) return s;
+  s = sell_layout(m, sigma, out);
+  if (s != SPMV_OK) spmv_sell_free(out);
+  return s;
+}
+
+void spmv_sell_free(spmv_sell* sl) {
+  if (!sl) return;
+  std::free(sl->slice_ptr);
+  std::free(sl->perm);
+  std::free(sl->cols);
+  std::free(sl->values);
+  std::memset(sl, 0, sizeof(*sl));
+}
+
+spmv_status spmv_select_format(const spmv_csr* m, spmv_format* format, int32_t* sigma,
+                               double* cv) {
+  spmv_status s = validate_csr(m, false);
+  if (s != SPMV_OK) return s;
+  const double c = row_length_cv(m);
+  spmv_format f;
+  int32_t sg;
+  choose_by_cv(c, &f, &sg);
+  if (format) *format = f;
+  if (sigma) *sigma = sg;
+  if (cv) *cv = c;
+  return SPMV_OK;
+}
+
 void spmv_delta_free(spmv_delta* d) {
   if (!d) return;
   std::free(d->values);
@@ -897,24 +1121,27 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
                               spmv_plan_info* info) {
   if (!info || !valid_format(format)) return SPMV_ERR_INVALID_ARG;
   std::memset(info, 0, sizeof(*info));
-  const bool delta = format != SPMV_FORMAT_CSR;
-  spmv_status s = validate_csr(m, delta);
-  if (s != SPMV_OK) return s;
-  if (format == SPMV_FORMAT_DELTA_AUTO) {
-    int32_t b = 4;
-    if ((s = spmv_delta_select_bits(m, SPMV_DELTA_FEWEST_BYTES, &b, nullptr)) != SPMV_OK)
-      return s;
-    format = delta_format(b);
-  }
+  if (!m) return SPMV_ERR_INVALID_ARG;
   Options o = resolve_options(opts, m->value_dtype);
+  int32_t sigma = 0;
+  spmv_status s = resolve_format(m, o, &format, &sigma);
+  if (s != SPMV_OK) return s;
+  const bool delta = is_delta_format(format);
   info->n_rows = m->n_rows;
   info->n_cols = m->n_cols;
   info->nnz = m->nnz;
   info->format = format;
   info->value_dtype = m->value_dtype;
   info->block = delta ? kDeltaThreads : kThreads;
+  if (format == SPMV_FORMAT_SELL) {
+    spmv_sell sl;
+    if ((s = spmv_convert_sell(m, sigma, &sl)) != SPMV_OK) return s;
+    sell_info(sl, info);
+    info->aux_bytes = 16;
+    spmv_sell_free(&sl);
+    return SPMV_OK;
+  }
   if (delta) {
-    if (m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
     spmv_delta d;
     if ((s = spmv_convert_bits(m, format_delta_bits(format), &d)) != SPMV_OK) return s;
     if (d.n_entries > kMaxIndex) {
@@ -959,18 +1186,12 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
                                 spmv_plan** out) {
   if (!out) return SPMV_ERR_INVALID_ARG;
   *out = nullptr;
-  if (!valid_format(format)) return SPMV_ERR_INVALID_ARG;
-  const bool delta = format != SPMV_FORMAT_CSR;
-  spmv_status s = validate_csr(m, delta);
-  if (s != SPMV_OK) return s;
-  if (delta && m->value_dtype != SPMV_F16) return SPMV_ERR_UNSUPPORTED;
-  if (format == SPMV_FORMAT_DELTA_AUTO) {
-    int32_t b = 4;
-    if ((s = spmv_delta_select_bits(m, SPMV_DELTA_FEWEST_BYTES, &b, nullptr)) != SPMV_OK)
-      return s;
-    format = delta_format(b);
-  }
+  if (!valid_format(format) || !m) return SPMV_ERR_INVALID_ARG;
   Options o = resolve_options(opts, m->value_dtype);
+  int32_t sigma = 0;
+  spmv_status s = resolve_format(m, o, &format, &sigma);
+  if (s != SPMV_OK) return s;
+  const bool delta = is_delta_format(format);
   spmv_plan* plan = new (std::nothrow) spmv_plan();
   if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
   Plan* p = &plan->impl;
@@ -984,7 +1205,14 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
   p->info.nnz = m->nnz;
   p->info.format = format;
   p->info.value_dtype = m->value_dtype;
-  if (delta) {
+  if (format == SPMV_FORMAT_SELL) {
+    spmv_sell sl;
+    s = spmv_convert_sell(m, sigma, &sl);
+    if (s == SPMV_OK) {
+      s = create_sell_plan(&sl, p);
+      spmv_sell_free(&sl);
+    }
+  } else if (delta) {
     spmv_delta d;
     s = spmv_convert_bits(m, format_delta_bits(format), &d);
     if (s == SPMV_OK) {
@@ -1057,7 +1285,7 @@ spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info) {
 static spmv_status check_run_args(const Plan& p, const void* x, const float* y,
                                   size_t* x_elem) {
   const size_t xs =
-      (p.format == SPMV_FORMAT_CSR && p.dtype == SPMV_F32) ? 4 : 2;
+      p.dtype == SPMV_F32 ? 4 : 2;
   *x_elem = xs;
   if ((p.n_cols > 0 && !x) || (p.n_rows > 0 && !y)) return SPMV_ERR_INVALID_ARG;
   if (((uintptr_t)x % xs) || ((uintptr_t)y % 4)) return SPMV_ERR_INVALID_ARG;
@@ -1078,8 +1306,9 @@ spmv_status spmv_run(spmv_plan* plan, const void* x, float* y, void* stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
   if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
   if (p.n_rows == 0) return SPMV_OK;
-  int rc = p.format == SPMV_FORMAT_CSR ? launch_csr(p, x, y, stream)
-                                       : launch_delta(p, x, y, stream);
+  int rc = p.format == SPMV_FORMAT_CSR    ? launch_csr(p, x, y, stream)
+           : p.format == SPMV_FORMAT_SELL ? launch_sell(p, x, y, stream)
+                                          : launch_delta(p, x, y, stream);
   return rc == 0 ? SPMV_OK : SPMV_ERR_CUDA;
 }
 
@@ -1094,7 +1323,7 @@ spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
   if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t xs =
-      (p.format == SPMV_FORMAT_CSR && p.dtype == SPMV_F32) ? 4 : 2;
+      p.dtype == SPMV_F32 ? 4 : 2;
   if (p.n_cols > 0 &&
       cudaMemcpyAsync(p.x_stage, x_host, (size_t)p.n_cols * xs,
                       cudaMemcpyHostToDevice, st) != cudaSuccess)

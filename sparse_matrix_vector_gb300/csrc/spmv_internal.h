@@ -42,6 +42,7 @@ constexpr int kStages = SPMV_STAGES;
 // bits), decoded by kDeltaThreads threads, LW = 1 or 2 words per thread (the
 // fewest that fit the row in one unit), so warp w decodes the unit's words
 // [32 LW w, 32 LW (w + 1)). Units hold at most 4096 entries (2048 at b = 8).
+constexpr int kSellSlicesPerCta = 8;  // SELL: one warp per slice
 constexpr int kDeltaThreads = 256;
 constexpr int kDeltaWarps = kDeltaThreads / 32;
 constexpr int kDeltaUnitWords = 512;  // the most, over the widths
@@ -107,6 +108,7 @@ struct Options {
   int reduce;  // short-row tiles: -1 per-tile choice, 0 lanes mode, 1 walk mode
   int lanes_log2;  // lanes mode when forced
   int interleave;  // CSR products: 0 auto, 1 chunks of 8, 2 element-interleaved
+  int sell_sigma;  // SELL sorting window, 0: by the CV of the row lengths
 };
 
 Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype);
@@ -157,15 +159,16 @@ struct Plan {
   int split_chunk = 0;
 
   // matrix (device)
-  int32_t* row_ptr = nullptr;   // CSR offsets or DELTA entry offsets
-  int32_t* col_idx = nullptr;   // CSR only
-  void* values = nullptr;       // fp32 / fp16 (CSR) or fp16 (DELTA)
+  int32_t* row_ptr = nullptr;   // CSR offsets, DELTA entry offsets, SELL slot offsets
+  int32_t* col_idx = nullptr;   // CSR and SELL columns
+  void* values = nullptr;       // fp32 / fp16 (CSR, SELL)
   unsigned char* blocks = nullptr;  // DELTA: one block per work unit
   // planner tables and scratch (device)
   Tile* tiles = nullptr;
   SplitInfo* splits = nullptr;
   int32_t* cta_first = nullptr;
   int32_t* row_split = nullptr;  // DELTA: split id per row or -1
+  int32_t* perm = nullptr;       // SELL: original row per slice lane (null: in order)
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
   int32_t* status = nullptr;    // device status word
@@ -189,5 +192,6 @@ size_t delta_x_smem_bytes(int n_cols);
 int delta_set_smem_limit(int bits, size_t dyn);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
+int launch_sell(const Plan& p, const void* x, float* y, void* stream);
 
 }  // namespace spmv

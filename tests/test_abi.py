@@ -35,7 +35,7 @@ def test_every_declared_function_is_exported(spmv_lib):
 
 
 def test_abi_version_and_status_strings(spmv_lib):
-    assert S.spmv_abi_version() == 2
+    assert S.spmv_abi_version() == 3
     for code in range(11):
         s = S.spmv_status_string(code)
         assert s and s != "unknown status"
@@ -344,3 +344,93 @@ def test_delta_width_selection_errors(spmv_lib):
     # an empty matrix: every width stores nothing; ties go to 8 bits
     bits, entries = S.spmv_delta_select_bits([0, 0], [], np.zeros(0, np.float16), 4)
     assert bits == 8 and entries == {2: 0, 4: 0, 8: 0}
+
+
+def _sell_matches_oracle(m, sigma):
+    from oracle import sell
+    got = S.spmv_convert_sell(m.row_ptr, m.col_idx, m.values, m.n_cols, sigma=sigma)
+    ref = sell.sell_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, C=32, sigma=sigma)
+    assert got.C == 32 and got.sigma == sigma and got.nnz == m.nnz
+    assert np.array_equal(got.slice_ptr, ref.slice_ptr)
+    assert np.array_equal(got.perm.astype(np.int64), ref.perm)
+    assert np.array_equal(got.cols, ref.cols)
+    assert got.values.dtype == ref.vals.dtype
+    assert np.array_equal(got.values.view(np.uint8), ref.vals.view(np.uint8))
+    return got
+
+
+@pytest.mark.parametrize("sigma", [1, 7, 1024])
+@pytest.mark.parametrize("name", ["tiny", "laplacian", "powerlaw", "fem", "llm", "edges"])
+def test_sell_converter_bit_exact(spmv_lib, name, sigma):
+    if name == "tiny":
+        m = workloads.tiny()
+    elif name == "laplacian":
+        m = workloads.laplacian(70, 41)
+    elif name == "powerlaw":
+        m = workloads.powerlaw(n=3000, nnz=16700, max_len=400, seed=4)
+    elif name == "fem":
+        m = workloads.fem(5, 4, 3)
+    elif name == "llm":
+        m = workloads.llm(0.8, n=300, seed=2)
+    else:
+        lengths = np.array([0, 1, 8, 7, 9, 0, 0, 16, 33, 1, 200, 0, 3])
+        m = workloads.from_lengths("edges", lengths, 500, seed=9)
+    _sell_matches_oracle(m, sigma)
+
+
+def test_sell_converter_unsorted_and_errors(spmv_lib):
+    # CSR order is kept inside a row, repeats included
+    rp = np.array([0, 3, 3, 5], np.int32)
+    ci = np.array([5, 1, 5, 0, 2], np.int32)
+    vals = np.arange(1, 6).astype(np.float32)
+    m = workloads.CSRInput("unsorted", 3, 6, rp, ci, vals, np.zeros(6, np.float32), {})
+    got = _sell_matches_oracle(m, 1)
+    assert got.cols[:3 * 32:32].tolist() == [5, 1, 5]
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_convert_sell(rp, ci, vals, 6, sigma=0)
+    assert e.value.status == 1
+    with pytest.raises(S.SpmvError) as e:
+        S.spmv_convert_sell(rp, ci, vals, 5, sigma=1)
+    assert e.value.status == 3
+    empty = S.spmv_convert_sell(np.zeros(1, np.int32), np.zeros(0, np.int32),
+                                np.zeros(0, np.float32), 4)
+    assert empty.slice_ptr.tolist() == [0] and empty.cols.size == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "laplacian", "powerlaw", "fem", "llm", "ragged"])
+def test_format_choice_matches_oracle(spmv_lib, name):
+    from oracle import sell
+    m = {"tiny": lambda: workloads.tiny(),
+         "laplacian": lambda: workloads.laplacian(70, 41),
+         "powerlaw": lambda: workloads.powerlaw(n=3000, nnz=16700, max_len=400, seed=4),
+         "fem": lambda: workloads.fem(5, 4, 3),
+         "llm": lambda: workloads.llm(0.8, n=300, seed=2),
+         "ragged": lambda: workloads.from_lengths("ragged", np.tile([3, 6, 9, 12], 50), 40,
+                                                  seed=3)}[name]()
+    fmt, sigma, cv = S.spmv_select_format(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    assert abs(cv - sell.row_length_cv(m.row_ptr)) <= 1e-12 * max(cv, 1.0)
+    assert (fmt, sigma) == sell.select_format(m.row_ptr)
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="auto")
+    long_rows = m.nnz > 128 * m.n_rows
+    assert info["format"] == S.api.FORMATS["csr" if long_rows else fmt]
+    if fmt == "sell":
+        ref = sell.sell_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, C=32, sigma=sigma)
+        assert info["n_entries"] == ref.n_slots and info["n_tiles"] == ref.n_slices
+        vs = m.values.dtype.itemsize
+        assert info["matrix_bytes"] == (ref.n_slots * (4 + vs) + (ref.n_slices + 1) * 4
+                                        + (ref.n_slices * 32 * 4 if sigma > 1 else 0))
+    # a SELL forced with explicit sigma keeps it
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="sell",
+                               options=S.spmv_plan_options(sell_sigma=64))
+    ref = sell.sell_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, C=32, sigma=64)
+    assert info["format"] == 5 and info["n_entries"] == ref.n_slots
+
+
+def test_auto_format_sends_long_rows_to_csr(spmv_lib):
+    """The CV band alone would give these uniform rows of ~1000 nonzeros to
+    SELL; AUTO keeps rows longer than 128 on average in CSR."""
+    m = workloads.llm(0.5, n=2048)
+    fmt, _, cv = S.spmv_select_format(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    assert fmt == "sell" and cv < 0.3
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="auto")
+    assert info["format"] == 0

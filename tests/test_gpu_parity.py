@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 TOL32 = 1e-5
 TOL16 = 2e-3
 DELTAS = ["delta2", "delta4", "delta8"]
-FORMAT_CODE = {"csr": 0, "delta4": 1, "delta2": 2, "delta8": 3}
+FORMAT_CODE = {"csr": 0, "delta4": 1, "delta2": 2, "delta8": 3, "sell": 5}
 
 
 @functools.lru_cache(maxsize=None)
@@ -444,3 +444,106 @@ def test_delta_auto_width(name):
     y, info = run_gpu(m, "delta")
     assert info["format"] == FORMAT_CODE[f"delta{bits}"]
     assert_parity(m, y, TOL16)
+
+
+# ------------------------------------------------------------ sliced ELL
+
+@pytest.mark.parametrize("sigma", [1, 1024])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_sell(name, sigma):
+    m = small(name)
+    y, info = run_gpu(m, "sell", options=S.spmv_plan_options(sell_sigma=sigma))
+    assert info["format"] == FORMAT_CODE["sell"]
+    assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("name", ["tiny", "laplacian", "fem", "powerlaw", "llm50", "llm90"])
+def test_full_size_sell(name):
+    m = full(name)
+    y, info = run_gpu(m, "sell")
+    assert info["n_entries"] >= m.nnz
+    assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("name,want", [("laplacian_small", "sell"), ("fem_small", "sell"),
+                                       ("powerlaw_small", "csr")])
+def test_auto_format(name, want):
+    m = small(name)
+    fmt, _, _ = S.spmv_select_format(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    assert fmt == want
+    y, info = run_gpu(m, "auto")
+    assert info["format"] == FORMAT_CODE[want]
+    assert_parity(m, y, tol_for(m))
+
+
+def test_sell_edge_cases():
+    # rows without nonzeros, a ragged last slice, one long row among empties
+    lengths = np.tile([0, 1, 0, 3, 40, 0, 2], 11)          # 77 rows
+    m = workloads.from_lengths("ragged_sell", lengths, 300, seed=3)
+    for sigma in (1, 5, 1024):
+        y, _ = run_gpu(m, "sell", options=S.spmv_plan_options(sell_sigma=sigma))
+        assert_parity(m, y, TOL32)
+    n = 5000
+    z = make("zero_nnz", np.zeros(n + 1), [], np.zeros(0, np.float32), 7, np.ones(7, np.float32))
+    y, _ = run_gpu(z, "sell")
+    assert np.all(y == 0)
+    one = make("1x1", [0, 1], [0], np.array([3.0], np.float32), 1, np.array([2.0], np.float32))
+    y, _ = run_gpu(one, "sell")
+    assert y[0] == 6.0
+    rng = np.random.default_rng(4)
+    n = 100_000
+    row = make("one_long_row", [0, n], np.arange(n), rng.uniform(-1, 1, n).astype(np.float32),
+               n, rng.uniform(-1, 1, n).astype(np.float32))
+    y, _ = run_gpu(row, "sell")
+    assert_parity(row, y, TOL32)
+    empty = make("empty", [0], [], np.zeros(0, np.float32), 5, np.ones(5, np.float32))
+    plan = S.spmv_plan_create(empty.row_ptr, empty.col_idx, empty.values, 5, format="sell")
+    S.spmv_run(plan, torch.ones(5, device="cuda"), torch.empty(0, device="cuda"))
+    torch.cuda.synchronize()
+    assert plan.info["launches_per_run"] == 0
+
+
+def test_sell_unsorted_duplicates_and_rectangular():
+    rng = np.random.default_rng(6)
+    n_rows, n_cols = 3000, 500
+    lengths = rng.integers(0, 40, n_rows)
+    rp = np.concatenate([[0], np.cumsum(lengths)])
+    ci = rng.integers(0, n_cols, rp[-1])
+    vals = rng.uniform(-1, 1, rp[-1]).astype(np.float32)
+    m = make("unsorted", rp, ci, vals, n_cols, rng.uniform(-1, 1, n_cols).astype(np.float32))
+    y, _ = run_gpu(m, "sell")
+    assert_parity(m, y, TOL32)
+    wide = workloads.from_lengths("wide", np.full(40, 3000), 100_000, seed=1)
+    y, _ = run_gpu(wide, "sell")
+    assert_parity(wide, y, TOL32)
+
+
+@pytest.mark.parametrize("sigma", [1, 1024])
+def test_sell_chained_runs_and_graph(sigma):
+    """y1 = A x, y2 = A y1, y3 = A y2 back to back on one stream (the kernel
+    may start before its predecessor ends), then the same under a CUDA
+    graph; every link matches the oracle on the GPU's own input."""
+    m = small("laplacian_small")
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format="sell",
+                              options=S.spmv_plan_options(sell_sigma=sigma))
+    x0 = torch.from_numpy(m.x).to(dev)
+    ys = [torch.full((m.n_rows,), float("nan"), dtype=torch.float32, device=dev)
+          for _ in range(3)]
+    S.spmv_run(plan, x0, ys[0])
+    S.spmv_run(plan, ys[0], ys[1])
+    S.spmv_run(plan, ys[1], ys[2])
+    torch.cuda.synchronize()
+    inputs = [m.x] + [y.cpu().numpy() for y in ys[:2]]
+    for xin, y in zip(inputs, ys):
+        y_ref, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, xin)
+        assert_parity(m, y.cpu().numpy(), TOL32, y_ref, s)
+    g = torch.cuda.CUDAGraph()
+    y = torch.zeros(m.n_rows, dtype=torch.float32, device=dev)
+    with torch.cuda.graph(g):
+        S.spmv_run(plan, x0, y)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), ys[0].cpu().numpy())
+    S.spmv_plan_destroy(plan)

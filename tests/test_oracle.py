@@ -298,6 +298,7 @@ def pin_sell_invariants():
                 assert np.array_equal(m.vals[at[:L]], vals[rp[r]:rp[r + 1]])
                 assert np.all(m.vals[at[L:]] == 0)
                 assert np.all(m.cols[at[L:]] == (ci[rp[r + 1] - 1] if L else 0))
+        assert sell.sell_slot_count(rp, C, sigma) == (m.n_slots, m.n_slices)
         x = rng.uniform(-1, 1, n_cols)
         y1, s1 = sell.sell_spmv(m, x)
         y2, s2 = oracle.csr_spmv(rp, ci, vals, x)
