@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of y = A x on GB300 through the C ABI (include/spmv.h).
 
-One step = one spmv_run (the whole path: tile kernel or DELTA decode kernel)
-over one resident copy of the workload. Copies rotate so that the footprint
+One step = one spmv_run (the whole path: the CSR tile kernel, the sliced-ELL
+kernel or the DELTA decode kernel) over one resident copy of the workload.
+Copies rotate so that the footprint
 of the timed loop is several times the L2 size: every step streams its matrix
 from HBM. Steps are captured into CUDA graphs and replayed; the timed region
 is bracketed by a barrier and torch.cuda.synchronize() and measured with CUDA
@@ -386,7 +387,7 @@ def bench_one(args, name, world, rank, local, pg):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if fmt == "csr" and m.values.dtype == np.float32 else "f16",
+            "dtype": "f32" if m.values.dtype == np.float32 else "f16",
             "data": "synthetic",
             "config": {"workload": desc, "format": fmt, "n_rows": m.n_rows,
                        "n_cols": m.n_cols, "nnz": m.nnz,
