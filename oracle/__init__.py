@@ -1,5 +1,5 @@
-"""Oracle for y = A x, the column-delta format (fp64, CPU, plain C) and the
-sliced ELL layout (numpy).
+"""Oracle for y = A x, the column-delta format (fp64, CPU, plain C), the
+sliced ELL layout and the matrix-free stiffness operator (numpy).
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
 baseline leg may import this package; the library under test never does, and
@@ -20,6 +20,11 @@ What it computes, and the passages it follows:
 * ``oracle.sell`` -- the sliced ELL layout and the choice of format by the
   coefficient of variation of the row lengths ("CUDA CSR SpMV optimisation",
   sections 2.1 and 2.2), in numpy; its readings are listed in its docstring.
+
+* ``oracle.fem`` -- the matrix-free stiffness operator of the "Fused FEM
+  matvec" page (gather, element product, scatter-add; one element matrix
+  scaled by a density per element), in numpy fp64, and the assembled matrix
+  it equals.
 
 Parity pins (tests/test_oracle.py): dense brute force on tiny matrices,
 identity and permutation matrices, 5-point Laplacian rows on constant vectors,

@@ -305,10 +305,70 @@ def pin_sell_invariants():
         assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
 
 
+def pin_fem_single_element():
+    """One element: the hand-derived dof table (corners in the order
+    (0,0,0) (1,0,0) (1,1,0) (0,1,0) then the top face; node = i + 2 j + 4 k),
+    and a K0 with one nonzero entry K0[a, b] = 1 moves rho * x[dof b] to
+    dof a and nothing else (a transposed K0 or a wrong dof fails)."""
+    from oracle import fem
+    edof = fem.element_dofs(1, 1, 1)
+    assert edof.tolist() == [[0, 1, 2, 3, 4, 5, 9, 10, 11, 6, 7, 8, 12, 13, 14,
+                              15, 16, 17, 21, 22, 23, 18, 19, 20]]
+    x = np.arange(1, 25, dtype=np.float64) * 0.5
+    for a, b in ((0, 0), (2, 17), (23, 5), (7, 20)):
+        k0 = np.zeros((24, 24))
+        k0[a, b] = 1.0
+        y, s = fem.fem_matvec(1, 1, 1, [2.0], k0, x)
+        want = np.zeros(24)
+        want[edof[0, a]] = 2.0 * x[edof[0, b]]
+        assert np.array_equal(y, want) and np.array_equal(s, np.abs(want))
+
+
+def pin_fem_identity_closed_form():
+    """K0 = I, rho = 1: y at a dof is x times the number of elements around
+    its node, the product over the axes of 1 (mesh boundary) or 2 (inside)."""
+    from oracle import fem
+    nex, ney, nez = 4, 3, 2
+    # eighths: every partial sum of up to 8 copies is exact
+    x = np.random.default_rng(3).integers(-64, 65, 3 * 5 * 4 * 3) / 8.0
+    y, _ = fem.fem_matvec(nex, ney, nez, np.ones(nex * ney * nez), np.eye(24), x)
+    mult = np.zeros(5 * 4 * 3)
+    for k in range(3):
+        for j in range(4):
+            for i in range(5):
+                m = ((1 if i in (0, nex) else 2) * (1 if j in (0, ney) else 2)
+                     * (1 if k in (0, nez) else 2))
+                mult[i + 5 * (j + 4 * k)] = m
+    assert np.array_equal(y, np.repeat(mult, 3) * x)
+
+
+def pin_fem_assembled_routes():
+    """The element loop equals the assembled matrix's product; the assembled
+    pattern is the one the fem workload generator builds independently, its
+    size is the closed form, and K is symmetric positive definite."""
+    from oracle import fem
+    m = workloads.fem_simp(5, 4, 3, seed=9)
+    y, s = fem.fem_matvec(m.nex, m.ney, m.nez, m.rho, m.K0, m.x)
+    y2, s2 = fem.fem_matvec_assembled(m.nex, m.ney, m.nez, m.rho, m.K0, m.x)
+    assert np.all(np.abs(y - y2) <= 1e-13 * s)
+    assert np.all(s2 <= s * (1 + 1e-12))
+    rp, ci, v = fem.fem_assemble(m.nex, m.ney, m.nez, m.rho, m.K0)
+    ref = workloads.fem(5, 4, 3)
+    assert np.array_equal(rp, ref.row_ptr) and np.array_equal(ci, ref.col_idx)
+    assert rp[-1] == workloads.fem_nnz(5, 4, 3)
+    A = sp.csr_matrix((v, ci, rp), shape=(m.n_dofs, m.n_dofs))
+    assert abs(A - A.T).max() == 0
+    rng = np.random.default_rng(1)
+    for _ in range(3):
+        z = rng.standard_normal(m.n_dofs)
+        assert z @ (A @ z) > 0
+
+
 ALL_PINS = [pin_dense_bruteforce, pin_identity_and_permutation,
             pin_laplacian_constant, pin_row_of_ones, pin_scipy,
             pin_delta_golden, pin_delta_widths_golden, pin_delta_roundtrip_and_counts,
-            pin_sell_golden, pin_sell_invariants]
+            pin_sell_golden, pin_sell_invariants,
+            pin_fem_single_element, pin_fem_identity_closed_form, pin_fem_assembled_routes]
 
 
 # ---------------------------------------------------------------- tests
@@ -459,3 +519,42 @@ def test_sell_planted_mistake_is_caught(name):
     finally:
         sys.modules["oracle.sell"] = saved
         oracle.sell = saved
+
+
+FEM_MUTANTS = {
+    "corner_order": ("(1, 1, 0), (0, 1, 0),\n                    (0, 0, 1)",
+                     "(0, 1, 0), (1, 1, 0),\n                    (0, 0, 1)"),
+    "transposed_K0": ("f = r[:, None] * (u @ k0.T)", "f = r[:, None] * (u @ k0)"),
+    "node_stride": ("node = i + (nex + 1) * (j + (ney + 1) * k)",
+                    "node = i + nex * (j + ney * k)"),
+    "dropped_density": ("f = r[:, None] * (u @ k0.T)", "f = (u @ k0.T)"),
+}
+
+
+@pytest.mark.parametrize("name", list(FEM_MUTANTS))
+def test_fem_planted_mistake_is_caught(name):
+    """A plausible mistake planted in the matrix-free oracle (on the CPU)
+    fails one of its pins."""
+    import types
+    import oracle.fem as real
+    old, new = FEM_MUTANTS[name]
+    src = open(real.__file__).read()
+    assert src.count(old) == 1, name
+    mutant = types.ModuleType("oracle.fem")
+    mutant.__package__ = "oracle"
+    exec(compile(src.replace(old, new), real.__file__ + ":" + name, "exec"), mutant.__dict__)
+    saved = sys.modules["oracle.fem"]
+    sys.modules["oracle.fem"] = mutant
+    oracle.fem = mutant
+    try:
+        failed = False
+        for pin in (pin_fem_single_element, pin_fem_identity_closed_form,
+                    pin_fem_assembled_routes):
+            try:
+                pin()
+            except (AssertionError, IndexError, ValueError):
+                failed = True
+        assert failed, f"planted mistake {name} passed every pin"
+    finally:
+        sys.modules["oracle.fem"] = saved
+        oracle.fem = saved

@@ -27,6 +27,10 @@ Workloads (sizes and value distributions as the pages describe them):
 * ``fem``        -- assembled stiffness pattern of a structured hexahedral mesh
   (8-node elements, 3 dofs per node) from random SPD 24 x 24 element matrices
   scaled by a density rho ~ U(0.001, 1), as in the topology-optimisation page.
+* ``fem_simp``   -- inputs of the matrix-free operator on the same mesh: one
+  SPD 24 x 24 element matrix K0 scaled per element by rho ~ U(0.001, 1) (the
+  page's SIMP setting, in which all elements share one stiffness matrix up to
+  the density factor), and x from U(-1, 1); returned as :class:`FemMesh`.
 """
 from __future__ import annotations
 
@@ -287,6 +291,50 @@ def fem_nnz(nex: int, ney: int, nez: int) -> int:
     """Closed-form stored-entry count of the assembled hex pattern: 9 times
     the product over axes of (3 m - 2), m = nodes along the axis."""
     return 9 * (3 * (nex + 1) - 2) * (3 * (ney + 1) - 2) * (3 * (nez + 1) - 2)
+
+
+@dataclass
+class FemMesh:
+    """Inputs of the matrix-free stiffness operator on a structured hex mesh:
+    element e = ex + nex*(ey + ney*ez) has matrix rho[e] * K0; nodes, dofs
+    and the local node order are those of ``fem`` (HEX_NODES)."""
+    name: str
+    nex: int
+    ney: int
+    nez: int
+    rho: np.ndarray      # float32[n_elem]
+    K0: np.ndarray       # float32[24, 24], symmetric positive definite
+    x: np.ndarray        # float32[n_dofs]
+    params: dict = field(default_factory=dict)
+
+    @property
+    def n_elem(self) -> int:
+        return self.nex * self.ney * self.nez
+
+    @property
+    def n_nodes(self) -> int:
+        return (self.nex + 1) * (self.ney + 1) * (self.nez + 1)
+
+    @property
+    def n_dofs(self) -> int:
+        return 3 * self.n_nodes
+
+
+def fem_simp(nex: int = 120, ney: int = 60, nez: int = 30, seed: int = 6) -> FemMesh:
+    """Densities rho_e ~ U(0.001, 1) scaling one element matrix
+    K0 = sym(G G^T) / 24 + I (G iid N(0, 1), computed in fp64 and rounded to
+    fp32 once, so K0 stays exactly symmetric), and x ~ U(-1, 1). Draw order:
+    rho, G, x."""
+    rng = _rng(seed)
+    n_elem = nex * ney * nez
+    rho = rng.uniform(0.001, 1.0, size=n_elem).astype(np.float32)
+    g = rng.standard_normal((24, 24))
+    m = g @ g.T
+    k0 = ((m + m.T) * 0.5 / 24.0 + np.eye(24)).astype(np.float32)
+    n_dofs = 3 * (nex + 1) * (ney + 1) * (nez + 1)
+    x = rng.uniform(-1.0, 1.0, size=n_dofs).astype(np.float32)
+    return FemMesh(f"fem_simp_{nex}x{ney}x{nez}", nex, ney, nez, rho, k0, x,
+                   {"seed": seed})
 
 
 WORKLOADS = {
