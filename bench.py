@@ -48,7 +48,14 @@ WORKLOADS = {
     "fem": ("fem", "csr", "fem_hex_120x60x30_3dof_f32_csr"),
     "laplacian_sell": ("laplacian", "sell", "laplacian_5pt_1000x999_f32_sell32"),
     "fem_sell": ("fem", "sell", "fem_hex_120x60x30_3dof_f32_sell32"),
+    "fem_matfree": ("fem_simp", "fem", "fem_hex_120x60x30_3dof_f32_matrix_free"),
 }
+# fp32 fma peak for the matrix-free operator's ALU roofline: 152 SMs x 128
+# fp32 lanes x 2 flops at the 2070 MHz maximum SM clock
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+# flops of the matrix-free operator per element: K0 (24 x 24) times 24
+# values, then 24 products with the density
+FEM_FLOPS_PER_ELEMENT = 2 * 24 * 24 + 24
 for _s in (30, 50, 70, 90):
     WORKLOADS[f"llm{_s}_csr"] = (f"llm{_s}", "csr",
                                  f"llm_12288x12288_sparsity{_s}_f16_csr")
@@ -79,7 +86,8 @@ def kernel_source_sha(fmt: str) -> str:
     csrc = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc")
     h = hashlib.sha256()
     kernel_file = ("spmv_delta.cu" if fmt.startswith("delta")
-                   else "spmv_sell.cu" if fmt == "sell" else "spmv_csr.cu")
+                   else "spmv_sell.cu" if fmt == "sell"
+                   else "spmv_fem.cu" if fmt == "fem" else "spmv_csr.cu")
     for name in ("spmv_device.cuh", kernel_file):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
@@ -185,10 +193,30 @@ def dist_setup():
     return world, rank, local
 
 
+def load_workload(key, fmt):
+    import workloads
+    if fmt == "fem":
+        m = workloads.fem_simp()
+        # the attributes the benchmark reads from a matrix workload
+        m.n_rows = m.n_cols = m.n_dofs
+        m.nnz = workloads.fem_nnz(m.nex, m.ney, m.nez)
+        m.values = m.rho
+        return m
+    return workloads.make(key)
+
+
+def fem_bytes(m):
+    return m.n_elem * 4 + 24 * 24 * 4 + 2 * m.n_dofs * 4
+
+
 def oracle_call(m, fmt, frac):
     """The oracle as it stands on the first ceil(frac * n_rows) rows of the
     workload: returns (rows, algorithmic bytes, nonzeros, zero-arg call)."""
     import oracle
+    if fmt == "fem":   # one call on the whole mesh (well under a second)
+        from oracle import fem
+        return m.n_rows, fem_bytes(m), m.nnz, (lambda: fem.fem_matvec(
+            m.nex, m.ney, m.nez, m.rho, m.K0, m.x, with_abs=False))
     rows = max(1, min(m.n_rows, int(math.ceil(m.n_rows * frac))))
     rp = m.row_ptr[:rows + 1]
     ci, vals = m.col_idx[:rp[-1]], m.values[:rp[-1]]
@@ -247,10 +275,8 @@ def run_reference(args, world, rank):
     block of rows), so that the run ends within a few minutes."""
     if rank != 0:
         return 0
-    import oracle
-    import workloads
     key, fmt, desc = WORKLOADS[args.workload]
-    m = workloads.make(key)
+    m = load_workload(key, fmt)
     steps, warmup = args.steps or 5, max(0, args.warmup)
 
     rows, nbytes, nnz, call = oracle_call(m, fmt, 1.0)
@@ -276,7 +302,7 @@ def run_reference(args, world, rank):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": desc, "n_rows": m.n_rows, "nnz": m.nnz,
                        "format": fmt},
-            "gflops": 2 * nnz / dt / 1e9,
+            "gflops": (m.n_elem * FEM_FLOPS_PER_ELEMENT if fmt == "fem" else 2 * nnz) / dt / 1e9,
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -287,27 +313,30 @@ def run_reference(args, world, rank):
 
 def bench_one(args, name, world, rank, local, pg):
     import torch
-    import workloads
     import sparse_matrix_vector_gb300 as S
 
     key, fmt, desc = WORKLOADS[name]
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     t0 = time.perf_counter()
-    m = workloads.make(key)
+    m = load_workload(key, fmt)
     log(f"[{name}] generated in {time.perf_counter() - t0:.1f}s "
         f"rows={m.n_rows} nnz={m.nnz}")
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
 
-    first = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
+    def make_plan():
+        if fmt == "fem":
+            return S.spmv_plan_create_fem(m.nex, m.ney, m.nez, m.rho, m.K0)
+        return S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
+
+    first = make_plan()
     info = first.info
     nbytes = int(info["algorithmic_bytes"])
     # rotate copies until the loop's footprint is >= 3x L2 (at most 64 copies:
     # below ~6 MB per copy the workload is latency-bound and stays L2-resident)
     copies = min(64, max(1, math.ceil(3 * l2 / nbytes)))
-    plans = [first] + [S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols,
-                                          format=fmt) for _ in range(copies - 1)]
+    plans = [first] + [make_plan() for _ in range(copies - 1)]
     xdt = torch.float32 if m.x.dtype == np.float32 else torch.float16
     xs = [torch.from_numpy(m.x).to(dev) for _ in range(copies)]
     ys = [torch.empty(m.n_rows, dtype=torch.float32, device=dev) for _ in range(copies)]
@@ -361,7 +390,8 @@ def bench_one(args, name, world, rank, local, pg):
     ms = max_over_ranks(ev0.elapsed_time(ev1), dev, pg)
     torch.cuda.synchronize(dev)
     sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
-    gflops = world * 2 * m.nnz / sec_per_step / 1e9
+    flops = m.n_elem * FEM_FLOPS_PER_ELEMENT if fmt == "fem" else 2 * m.nnz
+    gflops = world * flops / sec_per_step / 1e9
 
     # end to end through the C ABI with pinned host buffers
     x_host = torch.from_numpy(m.x).pin_memory().numpy()
@@ -405,9 +435,16 @@ def bench_one(args, name, world, rank, local, pg):
                                  "events on the launching stream",
                        "parallelism": f"replicas{world}"},
             "gflops": gflops,
-            "roofline": {"bound": "hbm", "achieved": per_launch, "peak": peak,
-                         "unit": "GB/s", "frac": per_launch / peak,
-                         "peak_source": peak_src, "traffic": traffic},
+            "roofline": ({"bound": "hbm", "achieved": per_launch, "peak": peak,
+                          "unit": "GB/s", "frac": per_launch / peak,
+                          "peak_source": peak_src, "traffic": traffic}
+                         if fmt != "fem" else
+                         {"bound": "alu", "achieved": gflops / world / 1e3,
+                          "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                          "frac": gflops / world / 1e3 / FP32_PEAK_TFLOPS,
+                          "peak_source": "152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                          "traffic": traffic,
+                          "hbm_achieved_GBs": per_launch}),
             "e2e": {"value": world * nbytes / e2e_sec / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": int(m.n_cols * m.x.dtype.itemsize),
                     "d2h_bytes_per_step": int(m.n_rows * 4),

@@ -10,7 +10,10 @@
  *     the same with 2- or 8-bit deltas, 16 or 4 to a word); or
  *   - SELL: sliced ELLPACK, fp32 or fp16 values: rows cut into slices of
  *     SPMV_SELL_C rows, each slice padded with zeros to its longest row and
- *     stored column-major (optionally rows sorted by length first).
+ *     stored column-major (optionally rows sorted by length first); or
+ *   - FEM: the stiffness matrix of a structured hexahedral mesh, never
+ *     assembled: y = sum over elements of rho_e K0 applied to the element's
+ *     24 dofs (spmv_plan_create_fem).
  * x is fp32 for fp32 values and fp16 otherwise; y is always fp32 and every
  * product is accumulated in fp32.
  *
@@ -27,6 +30,10 @@
  *           Section 2.1 also compares COO / CSR / ELL / HYB, and section
  *           2.2 chooses among them by the coefficient of variation (CV) of
  *           the row lengths.
+ *   [FEM]   "Fused FEM matvec" (bbs.csdn.net), section 2.1: y = K x as gather,
+ *           element product and scatter-add; section 2.2: the three fused in
+ *           one kernel; section 5.2: one element matrix shared by all
+ *           elements (here scaled per element by a density, as in SIMP).
  *   [SPGEMM] "Hash-based multi-phase SpGEMM" (mlqm.cn), section 2.1.1: rows
  *           grouped by work into bins served by partial-warp, warp and
  *           block-per-row kernels; section 5.2: batching of tiny rows.
@@ -49,7 +56,7 @@
 extern "C" {
 #endif
 
-#define SPMV_ABI_VERSION 3
+#define SPMV_ABI_VERSION 4
 
 /* Rows per slice of the SELL format (one warp of the kernel per slice). */
 #define SPMV_SELL_C 32
@@ -81,6 +88,8 @@ typedef enum spmv_format {
                                  report the chosen width's format code      */
   SPMV_FORMAT_SELL = 5,   /* sliced ELL ([CSR] 2.1 ELL, in slices of
                              SPMV_SELL_C rows); sigma from the options      */
+  SPMV_FORMAT_FEM = 7,    /* matrix-free hex-mesh stiffness operator; made
+                             by spmv_plan_create_fem only                  */
   SPMV_FORMAT_AUTO = 6    /* CSR or SELL by the CV of the row lengths
                              (spmv_select_format), except that matrices
                              whose rows hold more than 128 nonzeros on
@@ -317,6 +326,55 @@ spmv_status spmv_plan_create_ex(const spmv_csr* csr, spmv_format format,
 spmv_status spmv_plan_create_delta(const spmv_delta* delta,
                                    const spmv_plan_options* opts,
                                    spmv_plan** out);
+
+/* A structured hexahedral mesh for the matrix-free operator ([FEM] 2.1,
+ * 5.2), in HOST memory. nex x ney x nez elements; element
+ * e = ex + nex*(ey + ney*ez); node (i, j, k) = i + (nex+1)*(j + (ney+1)*k);
+ * dof = 3*node + c (n = 3 * (nex+1)(ney+1)(nez+1) dofs). Element e's local
+ * node b is at (ex, ey, ez) + corner b, corners in the order (0,0,0),
+ * (1,0,0), (1,1,0), (0,1,0), (0,0,1), (1,0,1), (1,1,1), (0,1,1); local dof
+ * 3*b + c. The element's matrix is rho[e] * K0. */
+typedef struct spmv_fem_mesh {
+  int32_t nex;
+  int32_t ney;
+  int32_t nez;
+  int32_t reserved;
+  const float* rho;  /* nex*ney*nez element densities (finite)             */
+  const float* K0;   /* 24*24 element matrix, row-major (finite)           */
+} spmv_fem_mesh;
+
+/* Plan y = K x for K = sum_e P_e^T (rho_e K0) P_e without assembling K:
+ * the plan copies rho to the device and K0 into itself. x and y are fp32,
+ * n elements each; runs are deterministic (no atomics). info.nnz reports the
+ * stored entries K would have if assembled. Errors: INVALID_ARG (a size < 1,
+ * NULL arrays, non-finite values), TOO_LARGE (n > 2^31 - 4097), CUDA,
+ * OUT_OF_MEMORY. */
+spmv_status spmv_plan_create_fem(const spmv_fem_mesh* mesh, spmv_plan** out);
+
+/* Outcome of spmv_pcg_solve. */
+typedef struct spmv_pcg_result {
+  int32_t iterations;    /* iterations taken                                */
+  int32_t status;        /* 1 converged, 2 iteration limit reached,
+                            3 breakdown (p . A p <= 0: A not SPD)           */
+  double rel_residual;   /* ||r|| / ||b|| of the recurrence's residual      */
+} spmv_pcg_result;
+
+/* Jacobi-preconditioned conjugate gradients for A x = b ([FEM] 6.1), A the
+ * square fp32 plan's operator (CSR, SELL or FEM; symmetric positive
+ * definite), preconditioner the diagonal of A (diag_dev, n fp32 on the
+ * device, or NULL for the plan's own diagonal; a zero entry leaves its row
+ * unscaled). x_dev holds the initial guess and receives the solution; b_dev
+ * is not written. Stops when ||r|| <= rel_tol ||b|| or after max_iter
+ * iterations; the host checks the device-side state every check_every
+ * iterations (<= 0: 16), and kernels after convergence inside a batch do
+ * nothing. Each iteration is one spmv_run and three vector kernels on
+ * `stream`; the call synchronizes the stream. Vectors are fp32 and the
+ * recurrence's scalars fp64; the result is the same bits on every run.
+ * Errors: INVALID_ARG (NULL pointers, non-square or non-fp32 plan, no
+ * diagonal), OUT_OF_MEMORY, CUDA. */
+spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag_dev, const float* b_dev,
+                           float* x_dev, double rel_tol, int32_t max_iter, int32_t check_every,
+                           void* stream, spmv_pcg_result* result);
 
 /* Copy the plan's planner report into *info. */
 spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info);

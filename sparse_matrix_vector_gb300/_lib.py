@@ -16,7 +16,7 @@ c_p = ctypes.c_void_p
 
 SPMV_F32, SPMV_F16 = 0, 1
 SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA4, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA8 = 0, 1, 2, 3
-SPMV_FORMAT_DELTA_AUTO, SPMV_FORMAT_SELL, SPMV_FORMAT_AUTO = 4, 5, 6
+SPMV_FORMAT_DELTA_AUTO, SPMV_FORMAT_SELL, SPMV_FORMAT_AUTO, SPMV_FORMAT_FEM = 4, 5, 6, 7
 SPMV_SELL_C = 32
 SPMV_DELTA_FEWEST_BYTES, SPMV_DELTA_SPARSITY_TABLE = 0, 1
 
@@ -49,6 +49,15 @@ class spmv_sell(ctypes.Structure):
                 ("n_slots", c_i64), ("slice_ptr", c_p), ("perm", c_p),
                 ("cols", c_p), ("values", c_p), ("value_dtype", ctypes.c_int),
                 ("reserved", c_i32)]
+
+
+class spmv_fem_mesh(ctypes.Structure):
+    _fields_ = [("nex", c_i32), ("ney", c_i32), ("nez", c_i32), ("reserved", c_i32),
+                ("rho", c_p), ("K0", c_p)]
+
+
+class spmv_pcg_result(ctypes.Structure):
+    _fields_ = [("iterations", c_i32), ("status", c_i32), ("rel_residual", ctypes.c_double)]
 
 
 class spmv_plan_options(ctypes.Structure):
@@ -100,6 +109,10 @@ SIGNATURES = {
     "spmv_plan_create_delta": (ctypes.c_int, [ctypes.POINTER(spmv_delta),
                                               ctypes.POINTER(spmv_plan_options),
                                               ctypes.POINTER(c_p)]),
+    "spmv_plan_create_fem": (ctypes.c_int, [ctypes.POINTER(spmv_fem_mesh),
+                                            ctypes.POINTER(c_p)]),
+    "spmv_pcg_solve": (ctypes.c_int, [c_p, c_p, c_p, c_p, ctypes.c_double, c_i32, c_i32, c_p,
+                                      ctypes.POINTER(spmv_pcg_result)]),
     "spmv_plan_get_info": (ctypes.c_int, [c_p, ctypes.POINTER(spmv_plan_info)]),
     "spmv_run": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
     "spmv_run_host": (ctypes.c_int, [c_p, c_p, c_p, c_p]),

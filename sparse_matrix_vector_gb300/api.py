@@ -297,6 +297,22 @@ def spmv_plan_create(row_ptr, col_idx, values, n_cols: int, format="csr",
     return Plan(out.value, _current_device())
 
 
+def spmv_plan_create_fem(nex: int, ney: int, nez: int, rho, K0) -> Plan:
+    """Plan the matrix-free stiffness operator of an nex x ney x nez hex mesh
+    (element matrices rho[e] * K0) on the current CUDA device; x and y are
+    fp32 with 3 (nex+1)(ney+1)(nez+1) entries."""
+    r = np.ascontiguousarray(rho, dtype=np.float32)
+    k = np.ascontiguousarray(K0, dtype=np.float32).reshape(-1)
+    if k.size != 24 * 24:
+        raise ValueError("K0 must hold 24 x 24 values")
+    mesh = _lib.spmv_fem_mesh(nex=int(nex), ney=int(ney), nez=int(nez),
+                              rho=r.ctypes.data if r.size else None, K0=k.ctypes.data)
+    out = ctypes.c_void_p()
+    _check(_lib.load().spmv_plan_create_fem(ctypes.byref(mesh), ctypes.byref(out)),
+           "spmv_plan_create_fem")
+    return Plan(out.value, _current_device())
+
+
 def spmv_plan_create_delta(delta: DeltaMatrix, options=None) -> Plan:
     """Plan from an already converted DELTA matrix."""
     rp = np.ascontiguousarray(delta.row_ptr, dtype=np.int64)
@@ -349,6 +365,28 @@ def spmv_run(plan: Plan, x, y, stream=None) -> None:
     yp = _dev_ptr(y, plan.n_rows, SPMV_F32, "y")
     _check(_lib.load().spmv_run(plan.handle, xp, yp, _stream_handle(stream)),
            "spmv_run")
+
+
+PCG_STATUS = {1: "converged", 2: "iteration limit", 3: "breakdown"}
+
+
+def spmv_pcg_solve(plan: Plan, b, x, rel_tol: float = 1e-6, max_iter: int = 1000,
+                   check_every: int = 16, diag=None, stream=None) -> dict:
+    """Jacobi-preconditioned CG for A x = b on the plan's device: b and x
+    are fp32 CUDA tensors of n (x: initial guess in, solution out); diag is
+    the preconditioner's diagonal (default: the plan's own). Synchronizes
+    the stream; returns iterations, status and ||r|| / ||b||."""
+    n = plan.n_rows
+    bp = _dev_ptr(b, n, SPMV_F32, "b")
+    xp = _dev_ptr(x, n, SPMV_F32, "x")
+    dp = None if diag is None else _dev_ptr(diag, n, SPMV_F32, "diag")
+    res = _lib.spmv_pcg_result()
+    _check(_lib.load().spmv_pcg_solve(plan.handle, dp, bp, xp, float(rel_tol), int(max_iter),
+                                      int(check_every), _stream_handle(stream),
+                                      ctypes.byref(res)),
+           "spmv_pcg_solve")
+    return {"iterations": int(res.iterations), "status": PCG_STATUS.get(int(res.status), "?"),
+            "rel_residual": float(res.rel_residual)}
 
 
 def spmv_run_host(plan: Plan, x_host: np.ndarray, y_host: np.ndarray,

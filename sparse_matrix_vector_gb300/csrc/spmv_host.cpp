@@ -503,7 +503,7 @@ void free_plan(spmv_plan* plan) {
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
-                    p->row_split, p->perm};
+                    p->row_split, p->perm, p->diag, p->pcg_work};
     for (void* b : bufs)
       if (b) cudaFree(b);
   }
@@ -665,6 +665,23 @@ spmv_status validate_delta(const spmv_delta* d, int64_t* nnz_out) {
   }
   *nnz_out = nnz;
   return SPMV_OK;
+}
+
+// The diagonal of a square fp32 matrix (entries with column == row, repeats
+// summed in stored order; 0 where a row has none), kept on the device for
+// the Jacobi preconditioner of spmv_pcg_solve.
+spmv_status upload_csr_diagonal(const spmv_csr* m, Plan* p) {
+  std::vector<float> d;
+  try {
+    d.assign((size_t)m->n_rows, 0.f);
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  const float* v = static_cast<const float*>(m->values);
+  for (int32_t r = 0; r < m->n_rows; ++r)
+    for (int32_t k = m->row_ptr[r]; k < m->row_ptr[r + 1]; ++k)
+      if (m->col_idx[k] == r) d[r] += v[k];
+  return dev_upload(&p->diag, d.data(), d.size() * 4, d.size() * 4 + 16);
 }
 
 // ------------------------------------------------------------ SELL
@@ -1230,6 +1247,8 @@ spmv_status spmv_plan_create_ex(const spmv_csr* m, spmv_format format,
     p->info.n_entries = m->nnz;
     s = create_csr_plan(m, o, p);
   }
+  if (s == SPMV_OK && !delta && m->value_dtype == SPMV_F32 && m->n_rows == m->n_cols)
+    s = upload_csr_diagonal(m, p);
   if (s != SPMV_OK) {
     free_plan(plan);
     return s;
@@ -1276,6 +1295,134 @@ spmv_status spmv_plan_create_delta(const spmv_delta* d,
   return SPMV_OK;
 }
 
+spmv_status spmv_plan_create_fem(const spmv_fem_mesh* mesh, spmv_plan** out) {
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!mesh || !mesh->rho || !mesh->K0 || mesh->nex < 1 || mesh->ney < 1 || mesh->nez < 1)
+    return SPMV_ERR_INVALID_ARG;
+  const int64_t nnx = (int64_t)mesh->nex + 1, nny = (int64_t)mesh->ney + 1,
+                nnz = (int64_t)mesh->nez + 1;
+  const int64_t n_nodes = nnx * nny * nnz;
+  if (3 * n_nodes > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+  const int64_t n_elem = (int64_t)mesh->nex * mesh->ney * mesh->nez;
+  for (int q = 0; q < 24 * 24; ++q)
+    if (!std::isfinite(mesh->K0[q])) return SPMV_ERR_INVALID_ARG;
+  for (int64_t e = 0; e < n_elem; ++e)
+    if (!std::isfinite(mesh->rho[e])) return SPMV_ERR_INVALID_ARG;
+  spmv_plan* plan = new (std::nothrow) spmv_plan();
+  if (!plan) return SPMV_ERR_OUT_OF_MEMORY;
+  Plan* p = &plan->impl;
+  p->format = SPMV_FORMAT_FEM;
+  p->dtype = SPMV_F32;
+  p->n_rows = p->n_cols = (int)(3 * n_nodes);
+  // the stored entries the assembled matrix would have: node pairs that share
+  // an element, 9 per pair, 3 m - 2 neighbours summed along an axis of m nodes
+  p->nnz = 9 * (3 * nnx - 2) * (3 * nny - 2) * (3 * nnz - 2);
+  p->n_tiles = n_nodes;
+  p->fem_dims[0] = mesh->nex;
+  p->fem_dims[1] = mesh->ney;
+  p->fem_dims[2] = mesh->nez;
+  std::memcpy(p->fem_k0, mesh->K0, sizeof(p->fem_k0));
+  spmv_plan_info& info = p->info;
+  info.n_rows = info.n_cols = p->n_rows;
+  info.nnz = p->nnz;
+  info.format = SPMV_FORMAT_FEM;
+  info.value_dtype = SPMV_F32;
+  info.n_tiles = n_nodes;
+  info.block = kFemThreads;
+  info.launches_per_run = 1;
+  info.matrix_bytes = n_elem * 4 + 24 * 24 * 4;
+  fill_bytes(&info, 4);
+  spmv_status s = bind_device(p);
+  if (s == SPMV_OK) s = dev_upload(&p->values, mesh->rho, (size_t)n_elem * 4, (size_t)n_elem * 4);
+  if (s == SPMV_OK) s = common_buffers(p);
+  if (s == SPMV_OK) {
+    // the diagonal, for the Jacobi preconditioner: every element adds
+    // rho_e K0[d][d] at each of its local dofs d (element order, fp64, one
+    // rounding to fp32)
+    std::vector<double> dd;
+    std::vector<float> d;
+    try {
+      dd.assign((size_t)(3 * n_nodes), 0.0);
+      d.resize(dd.size());
+    } catch (const std::bad_alloc&) {
+      s = SPMV_ERR_OUT_OF_MEMORY;
+    }
+    static const int kCx[8] = {0, 1, 1, 0, 0, 1, 1, 0}, kCy[8] = {0, 0, 1, 1, 0, 0, 1, 1};
+    for (int64_t e = 0; s == SPMV_OK && e < n_elem; ++e) {
+      const int64_t ex = e % mesh->nex, ey = (e / mesh->nex) % mesh->ney,
+                    ez = e / ((int64_t)mesh->nex * mesh->ney);
+      for (int b = 0; b < 8; ++b) {
+        const int64_t nd = (ex + kCx[b]) + nnx * ((ey + kCy[b]) + nny * (ez + (b >= 4)));
+        for (int c = 0; c < 3; ++c)
+          dd[3 * nd + c] += (double)mesh->rho[e] * (double)mesh->K0[(3 * b + c) * 25];
+      }
+    }
+    for (size_t q = 0; s == SPMV_OK && q < d.size(); ++q) d[q] = (float)dd[q];
+    if (s == SPMV_OK) s = dev_upload(&p->diag, d.data(), d.size() * 4, d.size() * 4 + 16);
+  }
+  if (s != SPMV_OK) {
+    free_plan(plan);
+    return s;
+  }
+  p->grid = (int)((n_nodes + kFemThreads - 1) / kFemThreads);
+  info.grid = p->grid;
+  info.aux_bytes = 16;
+  *out = plan;
+  return SPMV_OK;
+}
+
+spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, float* x,
+                           double rel_tol, int32_t max_iter, int32_t check_every, void* stream,
+                           spmv_pcg_result* result) {
+  if (!plan || !result) return SPMV_ERR_INVALID_ARG;
+  std::memset(result, 0, sizeof(*result));
+  Plan& p = plan->impl;
+  if (p.dtype != SPMV_F32 || p.n_rows != p.n_cols || is_delta_format(p.format))
+    return SPMV_ERR_INVALID_ARG;
+  const float* d = diag ? diag : p.diag;
+  if (p.n_rows > 0 && (!b || !x || !d)) return SPMV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
+  if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
+  if (p.n_rows == 0) {
+    result->status = kPcgConverged;
+    return SPMV_OK;
+  }
+  spmv_status s;
+  if (!p.pcg_work && (s = dev_alloc(&p.pcg_work, pcg_work_bytes(p.n_rows))) != SPMV_OK) return s;
+  const size_t vec = ((size_t)p.n_rows * 4 + 255) / 256 * 256;
+  float* pv = reinterpret_cast<float*>(p.pcg_work + 2 * vec);
+  float* qv = reinterpret_cast<float*>(p.pcg_work + 3 * vec);
+  PcgScalars* sc_dev =
+      reinterpret_cast<PcgScalars*>(p.pcg_work + 4 * vec + 3 * kPcgBlocks * sizeof(double));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PcgScalars sc{};
+  sc.tol2 = rel_tol * rel_tol;
+  sc.max_iter = max_iter;
+  if (cudaMemcpyAsync(sc_dev, &sc, sizeof(sc), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return SPMV_ERR_CUDA;
+  if ((s = spmv_run(plan, x, qv, stream)) != SPMV_OK) return s;  // q = A x0
+  if (launch_pcg(0, p, b, x, d, stream) != 0) return SPMV_ERR_CUDA;
+  const int batch = check_every > 0 ? check_every : 16;
+  for (int64_t it = 0;;) {
+    if (cudaMemcpyAsync(&sc, sc_dev, sizeof(sc), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return SPMV_ERR_CUDA;
+    if (sc.done || it >= max_iter) break;
+    for (int k = 0; k < batch; ++k) {
+      if ((s = spmv_run(plan, pv, qv, stream)) != SPMV_OK) return s;  // q = A p
+      for (int stage = 1; stage <= 3; ++stage)
+        if (launch_pcg(stage, p, b, x, d, stream) != 0) return SPMV_ERR_CUDA;
+    }
+    it += batch;
+  }
+  result->iterations = sc.iter;
+  result->status = sc.done ? sc.done : kPcgMaxIter;
+  result->rel_residual = sc.bb > 0 ? std::sqrt(sc.rr / sc.bb) : std::sqrt(sc.rr);
+  return SPMV_OK;
+}
+
 spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info) {
   if (!plan || !info) return SPMV_ERR_INVALID_ARG;
   *info = plan->impl.info;
@@ -1308,6 +1455,7 @@ spmv_status spmv_run(spmv_plan* plan, const void* x, float* y, void* stream) {
   if (p.n_rows == 0) return SPMV_OK;
   int rc = p.format == SPMV_FORMAT_CSR    ? launch_csr(p, x, y, stream)
            : p.format == SPMV_FORMAT_SELL ? launch_sell(p, x, y, stream)
+           : p.format == SPMV_FORMAT_FEM  ? launch_fem(p, x, y, stream)
                                           : launch_delta(p, x, y, stream);
   return rc == 0 ? SPMV_OK : SPMV_ERR_CUDA;
 }

@@ -43,6 +43,16 @@ constexpr int kStages = SPMV_STAGES;
 // fewest that fit the row in one unit), so warp w decodes the unit's words
 // [32 LW w, 32 LW (w + 1)). Units hold at most 4096 entries (2048 at b = 8).
 constexpr int kSellSlicesPerCta = 8;  // SELL: one warp per slice
+constexpr int kFemThreads = 128;      // matrix-free FEM: one thread per node
+constexpr int kPcgThreads = 256;      // conjugate gradients: vector kernels
+constexpr int kPcgBlocks = 608;       // at most 4 blocks per SM of 152 (grid-stride)
+constexpr int kPcgConverged = 1, kPcgMaxIter = 2, kPcgBreakdown = 3;
+
+// Device-side scalars of a conjugate-gradient solve.
+struct PcgScalars {
+  double rz, rr, bb, alpha, beta, tol2;
+  int iter, max_iter, done, arrived;
+};
 constexpr int kDeltaThreads = 256;
 constexpr int kDeltaWarps = kDeltaThreads / 32;
 constexpr int kDeltaUnitWords = 512;  // the most, over the widths
@@ -169,6 +179,14 @@ struct Plan {
   int32_t* cta_first = nullptr;
   int32_t* row_split = nullptr;  // DELTA: split id per row or -1
   int32_t* perm = nullptr;       // SELL: original row per slice lane (null: in order)
+  // matrix-free FEM: elements per axis and the element matrix (the device
+  // holds the densities in `values`)
+  int fem_dims[3] = {0, 0, 0};
+  // square fp32 plans: the matrix diagonal (Jacobi preconditioner) and the
+  // conjugate-gradient workspace, allocated by the first solve
+  float* diag = nullptr;
+  unsigned char* pcg_work = nullptr;
+  float fem_k0[24 * 24] = {};
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
   int32_t* status = nullptr;    // device status word
@@ -193,5 +211,11 @@ int delta_set_smem_limit(int bits, size_t dyn);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 int launch_sell(const Plan& p, const void* x, float* y, void* stream);
+int launch_fem(const Plan& p, const void* x, float* y, void* stream);
+// Conjugate gradients (spmv_pcg.cu): workspace bytes for n unknowns, and one
+// of its kernels (stage 0 init, 1 step length, 2 updates, 3 direction).
+size_t pcg_work_bytes(int n);
+int launch_pcg(int stage, const Plan& p, const float* b, float* x, const float* diag,
+               void* stream);
 
 }  // namespace spmv

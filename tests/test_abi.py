@@ -35,7 +35,7 @@ def test_every_declared_function_is_exported(spmv_lib):
 
 
 def test_abi_version_and_status_strings(spmv_lib):
-    assert S.spmv_abi_version() == 3
+    assert S.spmv_abi_version() == 4
     for code in range(11):
         s = S.spmv_status_string(code)
         assert s and s != "unknown status"
@@ -44,6 +44,8 @@ def test_abi_version_and_status_strings(spmv_lib):
 
 STRUCTS = {
     "spmv_csr": _lib.spmv_csr, "spmv_delta": _lib.spmv_delta,
+    "spmv_sell": _lib.spmv_sell, "spmv_fem_mesh": _lib.spmv_fem_mesh,
+    "spmv_pcg_result": _lib.spmv_pcg_result,
     "spmv_plan_options": _lib.spmv_plan_options,
     "spmv_plan_info": _lib.spmv_plan_info,
 }
@@ -434,3 +436,36 @@ def test_auto_format_sends_long_rows_to_csr(spmv_lib):
     assert fmt == "sell" and cv < 0.3
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="auto")
     assert info["format"] == 0
+
+
+def test_fem_plan_argument_errors(spmv_lib):
+    """Bad meshes are refused on the host, before any device call."""
+    k0 = np.eye(24, dtype=np.float32)
+    out = ctypes.c_void_p()
+    for dims in ((0, 1, 1), (1, -1, 1), (2, 2, 0)):
+        rho = np.ones(max(1, dims[0] * dims[1] * dims[2]), np.float32)
+        mesh = _lib.spmv_fem_mesh(nex=dims[0], ney=dims[1], nez=dims[2],
+                                  rho=rho.ctypes.data, K0=k0.ctypes.data)
+        assert spmv_lib.spmv_plan_create_fem(ctypes.byref(mesh), ctypes.byref(out)) == 1
+    rho = np.ones(8, np.float32)
+    bad_k = k0.copy()
+    bad_k[3, 4] = np.inf
+    bad_r = rho.copy()
+    bad_r[5] = np.nan
+    for r, k in ((bad_r, k0), (rho, bad_k)):
+        mesh = _lib.spmv_fem_mesh(nex=2, ney=2, nez=2, rho=r.ctypes.data, K0=k.ctypes.data)
+        assert spmv_lib.spmv_plan_create_fem(ctypes.byref(mesh), ctypes.byref(out)) == 1
+    mesh = _lib.spmv_fem_mesh(nex=2, ney=2, nez=2, rho=None, K0=k0.ctypes.data)
+    assert spmv_lib.spmv_plan_create_fem(ctypes.byref(mesh), ctypes.byref(out)) == 1
+    mesh = _lib.spmv_fem_mesh(nex=2000, ney=2000, nez=2000, rho=rho.ctypes.data,
+                              K0=k0.ctypes.data)
+    assert spmv_lib.spmv_plan_create_fem(ctypes.byref(mesh), ctypes.byref(out)) == 8
+    assert not out.value
+
+
+def test_pcg_argument_errors(spmv_lib):
+    """A NULL plan or result pointer is refused without touching a device."""
+    res = _lib.spmv_pcg_result()
+    assert spmv_lib.spmv_pcg_solve(None, None, None, None, 1e-6, 10, 0, None,
+                                   ctypes.byref(res)) == 1
+    assert spmv_lib.spmv_pcg_solve(None, None, None, None, 1e-6, 10, 0, None, None) == 1

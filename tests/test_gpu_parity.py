@@ -8,6 +8,7 @@ Tolerances (per row i, s_i = sum_j |a_ij x_j| from the oracle):
 import functools
 
 import numpy as np
+import scipy.sparse as sp
 import pytest
 
 import oracle
@@ -546,4 +547,201 @@ def test_sell_chained_runs_and_graph(sigma):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(y.cpu().numpy(), ys[0].cpu().numpy())
+    S.spmv_plan_destroy(plan)
+
+
+# ------------------------------------------------------------ matrix-free FEM
+
+def run_fem(m, x=None, repeat=1):
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create_fem(m.nex, m.ney, m.nez, m.rho, m.K0)
+    xt = torch.from_numpy(np.ascontiguousarray(m.x if x is None else x)).to(dev)
+    outs = []
+    for _ in range(repeat):
+        y = torch.full((m.n_dofs,), float("nan"), dtype=torch.float32, device=dev)
+        S.spmv_run(plan, xt, y)
+        outs.append(y)
+    torch.cuda.synchronize()
+    S.spmv_plan_check(plan)
+    info = plan.info
+    S.spmv_plan_destroy(plan)
+    ys = [o.cpu().numpy() for o in outs]
+    return (ys if repeat > 1 else ys[0]), info
+
+
+def assert_fem_parity(m, y, x=None):
+    from oracle import fem
+    y_ref, s = fem.fem_matvec(m.nex, m.ney, m.nez, m.rho, m.K0, m.x if x is None else x)
+    y = y.astype(np.float64)
+    assert np.all(np.isfinite(y))
+    err = np.abs(y - y_ref)
+    bad = np.nonzero(err > TOL32 * s + 1e-30)[0]
+    assert bad.size == 0, (f"{m.name}: {bad.size} dofs out of tolerance, first {bad[:5]}, "
+                           f"max |dy|/s = {np.max(err / np.maximum(s, 1e-300)):.3e}")
+
+
+@pytest.mark.parametrize("dims", [(1, 1, 1), (2, 1, 1), (1, 1, 3), (4, 3, 2), (13, 7, 5),
+                                  (33, 2, 9)])
+def test_fem_small(dims):
+    m = workloads.fem_simp(*dims, seed=sum(dims))
+    y, info = run_fem(m)
+    assert info["format"] == 7 and info["n_rows"] == m.n_dofs
+    assert info["nnz"] == workloads.fem_nnz(*dims)
+    assert_fem_parity(m, y)
+
+
+def test_fem_full_size_deterministic():
+    m = workloads.fem_simp()
+    ys, info = run_fem(m, repeat=3)
+    for y in ys[1:]:
+        assert np.array_equal(y, ys[0])
+    assert_fem_parity(m, ys[0])
+
+
+def test_fem_general_K0_and_single_entries():
+    """A non-symmetric K0 (the operator applies K0 as given, rows by
+    columns), and K0 with one nonzero entry against the hand rule."""
+    m = workloads.fem_simp(3, 2, 2, seed=4)
+    k0 = np.random.default_rng(8).normal(size=(24, 24)).astype(np.float32)
+    m2 = workloads.FemMesh("fem_nonsym", 3, 2, 2, m.rho, k0, m.x)
+    y, _ = run_fem(m2)
+    assert_fem_parity(m2, y)
+    from oracle import fem
+    edof = fem.element_dofs(1, 1, 1)[0]
+    x = (np.arange(24, dtype=np.float32) + 1) * 0.25
+    for a, b in ((0, 0), (2, 17), (23, 5)):
+        k1 = np.zeros((24, 24), np.float32)
+        k1[a, b] = 1.0
+        one = workloads.FemMesh("one_entry", 1, 1, 1, np.array([2.0], np.float32), k1, x)
+        y, _ = run_fem(one)
+        want = np.zeros(24, np.float32)
+        want[edof[a]] = 2.0 * x[edof[b]]
+        assert np.array_equal(y, want)
+
+
+def test_fem_matches_assembled_csr_on_gpu():
+    """The same K x through the matrix-free operator and through the
+    assembled matrix (fp32 CSR from the oracle's assembly) agree within both
+    kernels' tolerances."""
+    from oracle import fem
+    m = workloads.fem_simp(20, 10, 6, seed=2)
+    rp, ci, v = fem.fem_assemble(m.nex, m.ney, m.nez, m.rho, m.K0)
+    csr = workloads.CSRInput("fem_assembled", m.n_dofs, m.n_dofs, rp.astype(np.int32),
+                             ci.astype(np.int32), v.astype(np.float32), m.x, {})
+    y_mf, _ = run_fem(m)
+    y_csr, _ = run_gpu(csr, "csr")
+    y_ref, s = fem.fem_matvec(m.nex, m.ney, m.nez, m.rho, m.K0, m.x)
+    assert np.all(np.abs(y_mf.astype(np.float64) - y_csr) <= 3e-5 * s + 1e-30)
+
+
+def test_fem_chained_runs_and_graph():
+    m = workloads.fem_simp(10, 8, 6, seed=3)
+    dev = torch.device("cuda", 0)
+    plan = S.spmv_plan_create_fem(m.nex, m.ney, m.nez, m.rho, m.K0)
+    x0 = torch.from_numpy(m.x).to(dev)
+    ys = [torch.full((m.n_dofs,), float("nan"), dtype=torch.float32, device=dev)
+          for _ in range(3)]
+    S.spmv_run(plan, x0, ys[0])
+    S.spmv_run(plan, ys[0], ys[1])
+    S.spmv_run(plan, ys[1], ys[2])
+    torch.cuda.synchronize()
+    inputs = [m.x] + [y.cpu().numpy() for y in ys[:2]]
+    for xin, y in zip(inputs, ys):
+        assert_fem_parity(m, y.cpu().numpy(), x=xin)
+    g = torch.cuda.CUDAGraph()
+    y = torch.zeros(m.n_dofs, dtype=torch.float32, device=dev)
+    with torch.cuda.graph(g):
+        S.spmv_run(plan, x0, y)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), ys[0].cpu().numpy())
+    xh = torch.from_numpy(m.x).pin_memory().numpy()
+    yh = torch.empty(m.n_dofs, dtype=torch.float32).pin_memory().numpy()
+    S.spmv_run_host(plan, xh, yh)
+    assert np.array_equal(yh, ys[0].cpu().numpy())
+    S.spmv_plan_destroy(plan)
+
+
+# ------------------------------------------------------------ Jacobi-PCG
+
+def _pcg_gpu(plan, b, tol, max_iter, diag=None, check_every=16):
+    dev = torch.device("cuda", 0)
+    bt = torch.from_numpy(np.ascontiguousarray(b, dtype=np.float32)).to(dev)
+    xt = torch.zeros(b.size, dtype=torch.float32, device=dev)
+    dt = None if diag is None else torch.from_numpy(np.ascontiguousarray(diag, np.float32)).to(dev)
+    res = S.spmv_pcg_solve(plan, bt, xt, rel_tol=tol, max_iter=max_iter,
+                           check_every=check_every, diag=dt)
+    return xt.cpu().numpy(), res
+
+
+def _check_pcg(matvec, diag, b, x_gpu, res, tol, max_iter):
+    from oracle import pcg
+    x_ref, it_ref, st_ref, hist = pcg.jacobi_pcg(matvec, diag, b, np.zeros(b.size), tol, max_iter)
+    assert st_ref == 1 and res["status"] == "converged"
+    # fp32 vectors against the fp64 recurrence: the step count may differ a
+    # little near the threshold
+    assert abs(res["iterations"] - it_ref) <= max(3, it_ref // 20), (res, it_ref)
+    bn = np.linalg.norm(b)
+    true_res = np.linalg.norm(b - matvec(x_gpu.astype(np.float64))) / bn
+    assert true_res <= 5 * tol, true_res
+    assert np.linalg.norm(x_gpu - x_ref) <= 1e-3 * np.linalg.norm(x_ref)
+
+
+@pytest.mark.parametrize("fmt", ["csr", "sell"])
+def test_pcg_laplacian(fmt):
+    m = workloads.laplacian(120, 90)
+    A = sp.csr_matrix((m.values.astype(np.float64), m.col_idx, m.row_ptr),
+                      shape=(m.n_rows, m.n_cols))
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
+    b = m.x.astype(np.float64)
+    x, res = _pcg_gpu(plan, b, 1e-5, 2000)
+    _check_pcg(lambda v: A @ v, A.diagonal(), b, x, res, 1e-5, 2000)
+    # same bits on a second solve, and with the diagonal passed explicitly
+    x2, res2 = _pcg_gpu(plan, b, 1e-5, 2000, diag=A.diagonal(), check_every=7)
+    assert np.array_equal(x, x2) and res == res2
+    S.spmv_plan_destroy(plan)
+
+
+def test_pcg_fem_matrix_free_and_assembled():
+    from oracle import fem
+    m = workloads.fem_simp(12, 8, 6, seed=7)
+    plan = S.spmv_plan_create_fem(m.nex, m.ney, m.nez, m.rho, m.K0)
+    rp, ci, v = fem.fem_assemble(m.nex, m.ney, m.nez, m.rho, m.K0)
+    A = sp.csr_matrix((v, ci, rp), shape=(m.n_dofs, m.n_dofs))
+    b = m.x.astype(np.float64)
+    x, res = _pcg_gpu(plan, b, 1e-6, 3000)
+    _check_pcg(lambda u: fem.fem_matvec(m.nex, m.ney, m.nez, m.rho, m.K0, u, with_abs=False),
+               A.diagonal(), b, x, res, 1e-6, 3000)
+    x2, res2 = _pcg_gpu(plan, b, 1e-6, 3000, diag=A.diagonal())
+    assert np.array_equal(x, x2)
+    S.spmv_plan_destroy(plan)
+    # the same system through the assembled fp32 matrix
+    csr = S.spmv_plan_create(rp.astype(np.int32), ci.astype(np.int32), v.astype(np.float32),
+                             m.n_dofs, format="sell")
+    x3, res3 = _pcg_gpu(csr, b, 1e-6, 3000)
+    _check_pcg(lambda u: A @ u, A.diagonal(), b, x3, res3, 1e-6, 3000)
+    S.spmv_plan_destroy(csr)
+
+
+def test_pcg_limits_and_breakdown():
+    m = workloads.laplacian(60, 40)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    x, res = _pcg_gpu(plan, m.x.astype(np.float64), 1e-12, 5)
+    assert res["status"] == "iteration limit" and res["iterations"] == 5
+    S.spmv_plan_destroy(plan)
+    # indefinite: diag(1, -1, 1, -1, ...) gives p . A p = 0 on the first step
+    n = 64
+    rp = np.arange(n + 1, dtype=np.int32)
+    ci = np.arange(n, dtype=np.int32)
+    vals = np.where(np.arange(n) % 2 == 0, 1.0, -1.0).astype(np.float32)
+    plan = S.spmv_plan_create(rp, ci, vals, n)
+    x, res = _pcg_gpu(plan, np.ones(n), 1e-6, 10)
+    assert res["status"] == "breakdown"
+    S.spmv_plan_destroy(plan)
+    # fp16 plans are refused
+    llm = workloads.llm(0.9, n=256)
+    plan = S.spmv_plan_create(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols)
+    with pytest.raises(S.SpmvError):
+        _pcg_gpu(plan, np.ones(256), 1e-6, 10)
     S.spmv_plan_destroy(plan)

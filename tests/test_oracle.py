@@ -364,11 +364,41 @@ def pin_fem_assembled_routes():
         assert z @ (A @ z) > 0
 
 
+def pin_pcg_closed_forms():
+    """Jacobi-PCG: on a diagonal matrix the preconditioner is the inverse,
+    so one step lands on b / d exactly; on 2 x 2 [[4, 1], [1, 3]] x = [1, 2]
+    two steps give the exact [1/11, 7/11] (CG ends in n steps); on a random
+    SPD 40 x 40 system it reaches the direct solution within n + 2 steps;
+    an indefinite matrix breaks down (p . A p = 0) and a step limit stops."""
+    from oracle import pcg
+    d = np.array([2.0, 4.0, 0.5, 8.0])
+    b = np.array([1.0, -2.0, 3.0, 0.25])
+    x, it, st, _ = pcg.jacobi_pcg(lambda v: d * v, d, b, np.zeros(4), 1e-12, 50)
+    assert it == 1 and st == 1 and np.array_equal(x, b / d)
+    A = np.array([[4.0, 1.0], [1.0, 3.0]])
+    x, it, st, _ = pcg.jacobi_pcg(lambda v: A @ v, np.diag(A), np.array([1.0, 2.0]),
+                                  np.zeros(2), 1e-14, 2)
+    assert it <= 2 and np.allclose(x, [1 / 11, 7 / 11], rtol=0, atol=1e-15)
+    rng = np.random.default_rng(5)
+    G = rng.standard_normal((40, 40))
+    A = G @ G.T + 40 * np.eye(40)
+    b = rng.standard_normal(40)
+    x, it, st, hist = pcg.jacobi_pcg(lambda v: A @ v, np.diag(A), b, np.zeros(40), 1e-12, 42)
+    assert st == 1 and it <= 42
+    assert np.allclose(x, np.linalg.solve(A, b), rtol=0, atol=1e-9)
+    D = np.diag([1.0, -1.0])
+    x, it, st, _ = pcg.jacobi_pcg(lambda v: D @ v, np.diag(D), np.ones(2), np.zeros(2), 1e-12, 5)
+    assert st == 3
+    x, it, st, _ = pcg.jacobi_pcg(lambda v: A @ v, np.diag(A), b, np.zeros(40), 1e-14, 3)
+    assert st == 2 and it == 3
+
+
 ALL_PINS = [pin_dense_bruteforce, pin_identity_and_permutation,
             pin_laplacian_constant, pin_row_of_ones, pin_scipy,
             pin_delta_golden, pin_delta_widths_golden, pin_delta_roundtrip_and_counts,
             pin_sell_golden, pin_sell_invariants,
-            pin_fem_single_element, pin_fem_identity_closed_form, pin_fem_assembled_routes]
+            pin_fem_single_element, pin_fem_identity_closed_form, pin_fem_assembled_routes,
+            pin_pcg_closed_forms]
 
 
 # ---------------------------------------------------------------- tests
@@ -558,3 +588,34 @@ def test_fem_planted_mistake_is_caught(name):
     finally:
         sys.modules["oracle.fem"] = saved
         oracle.fem = saved
+
+
+PCG_MUTANTS = {
+    "no_preconditioner": ("z = dinv * r\n        rz_new", "z = r\n        rz_new"),
+    "residual_sign": ("r -= alpha * q", "r += alpha * q"),
+    "beta_inverted": ("beta = rz_new / rz", "beta = rz / rz_new"),
+    "direction_without_z": ("p = z + beta * p", "p = r + beta * p"),
+}
+
+
+@pytest.mark.parametrize("name", list(PCG_MUTANTS))
+def test_pcg_planted_mistake_is_caught(name):
+    """A plausible mistake planted in the CG oracle (on the CPU) fails its
+    pins."""
+    import types
+    import oracle.pcg as real
+    old, new = PCG_MUTANTS[name]
+    src = open(real.__file__).read()
+    assert src.count(old) == 1, name
+    mutant = types.ModuleType("oracle.pcg")
+    mutant.__package__ = "oracle"
+    exec(compile(src.replace(old, new), real.__file__ + ":" + name, "exec"), mutant.__dict__)
+    saved = sys.modules["oracle.pcg"]
+    sys.modules["oracle.pcg"] = mutant
+    oracle.pcg = mutant
+    try:
+        with pytest.raises(AssertionError):
+            pin_pcg_closed_forms()
+    finally:
+        sys.modules["oracle.pcg"] = saved
+        oracle.pcg = saved
