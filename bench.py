@@ -49,7 +49,15 @@ WORKLOADS = {
     "laplacian_sell": ("laplacian", "sell", "laplacian_5pt_1000x999_f32_sell32"),
     "fem_sell": ("fem", "sell", "fem_hex_120x60x30_3dof_f32_sell32"),
     "fem_matfree": ("fem_simp", "fem", "fem_hex_120x60x30_3dof_f32_matrix_free"),
+    "fem_pcg_sell": ("fem", "pcg_sell", "fem_hex_120x60x30_3dof_f32_jacobi_pcg_sell32"),
+    "fem_pcg_matfree": ("fem_simp", "pcg_fem", "fem_hex_120x60x30_3dof_f32_jacobi_pcg_matrix_free"),
 }
+# bytes of vector traffic per conjugate-gradient iteration and unknown, next
+# to the matrix product's: step length reads p, q (8); the update reads x,
+# p, r, q, diag and writes x, r, z (32); the direction reads z, p and writes
+# p (12)
+PCG_VECTOR_BYTES = 52
+PCG_TOL = 1e-6
 # fp32 fma peak for the matrix-free operator's ALU roofline: 152 SMs x 128
 # fp32 lanes x 2 flops at the 2070 MHz maximum SM clock
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
@@ -213,6 +221,26 @@ def oracle_call(m, fmt, frac):
     """The oracle as it stands on the first ceil(frac * n_rows) rows of the
     workload: returns (rows, algorithmic bytes, nonzeros, zero-arg call)."""
     import oracle
+    if fmt.startswith("pcg"):   # a few Jacobi-PCG iterations on the whole system
+        from oracle import pcg, fem
+        k = 3
+        if fmt == "pcg_fem":
+            matvec = (lambda u: fem.fem_matvec(m.nex, m.ney, m.nez, m.rho, m.K0, u,
+                                               with_abs=False))
+            diag = fem.fem_diagonal(m.nex, m.ney, m.nez, m.rho, m.K0)
+            per_iter = fem_bytes(m)
+        else:
+            rows = np.repeat(np.arange(m.n_rows), np.diff(m.row_ptr))
+            diag = np.zeros(m.n_rows)
+            on = m.col_idx == rows
+            np.add.at(diag, rows[on], m.values[on].astype(np.float64))
+            matvec = (lambda u: oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, u,
+                                                with_abs=False))
+            per_iter = algorithmic_bytes_csr(m)
+        nbytes = k * (per_iter + PCG_VECTOR_BYTES * m.n_rows)
+        b = m.x.astype(np.float64)
+        return m.n_rows, nbytes, m.nnz, (lambda: pcg.jacobi_pcg(
+            matvec, diag, b, np.zeros(m.n_rows), 0.0, k))
     if fmt == "fem":   # one call on the whole mesh (well under a second)
         from oracle import fem
         return m.n_rows, fem_bytes(m), m.nnz, (lambda: fem.fem_matvec(
@@ -276,7 +304,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     key, fmt, desc = WORKLOADS[args.workload]
-    m = load_workload(key, fmt)
+    m = load_workload(key, "fem" if fmt == "pcg_fem" else fmt)
     steps, warmup = args.steps or 5, max(0, args.warmup)
 
     rows, nbytes, nnz, call = oracle_call(m, fmt, 1.0)
@@ -311,11 +339,118 @@ def run_reference(args, world, rank):
     return 0
 
 
+def bench_pcg(args, name, world, rank, local, pg):
+    """A step is one Jacobi-PCG iteration (one y = A x and three vector
+    kernels), timed over whole solves to ||r|| <= 1e-6 ||b|| from x = 0
+    (every solve takes the same iterations: checked); the time includes the
+    host's convergence checks and the up to 15 no-op iterations of the last
+    batch. Bytes per step are the product's algorithmic bytes plus
+    PCG_VECTOR_BYTES per unknown."""
+    import torch
+    import sparse_matrix_vector_gb300 as S
+
+    key, fmt, desc = WORKLOADS[name]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    m = load_workload(key, "fem" if fmt == "pcg_fem" else "csr")
+    if fmt == "pcg_fem":
+        plan = S.spmv_plan_create_fem(m.nex, m.ney, m.nez, m.rho, m.K0)
+    else:
+        plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format="sell")
+    n = m.n_rows
+    nbytes = int(plan.info["algorithmic_bytes"]) + PCG_VECTOR_BYTES * n
+    b = torch.from_numpy(m.x).to(dev)
+    x = torch.zeros(n, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    warmup = max(3, args.warmup)
+    first = {}
+
+    def solve():
+        x.zero_()
+        res = S.spmv_pcg_solve(plan, b, x, rel_tol=PCG_TOL, max_iter=20000, stream=stream)
+        if res["status"] != "converged" or res["iterations"] != first.setdefault(
+                "it", res["iterations"]):
+            raise RuntimeError(f"solve did not repeat: {res}, first {first}")
+        return res
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            sol = solve()
+    iters = first["it"]
+    solves = max(3, (args.steps or 2000) // max(iters, 1))
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    if pg is not None:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(solves):
+            solve()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    steps = solves * iters
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev, pg)
+    sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
+    t_sol = ms / solves / 1e3
+    # end to end: b copied in from pinned host memory, x copied back
+    bh = torch.from_numpy(m.x).pin_memory()
+    xh = torch.empty(n, dtype=torch.float32).pin_memory()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        b.copy_(bh, non_blocking=True)
+        x.zero_()
+        res = S.spmv_pcg_solve(plan, b, x, rel_tol=PCG_TOL, max_iter=20000, stream=stream)
+        xh.copy_(x, non_blocking=True)
+    stream.synchronize()
+    e2e_sec = time.perf_counter() - t0
+    S.spmv_plan_destroy(plan)
+    if rank != 0:
+        return None
+    traffic = recorded_traffic(name, "fem" if fmt == "pcg_fem" else "sell")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup * iters, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "format": fmt, "n_rows": n, "nnz": m.nnz,
+                   "algorithmic_bytes": nbytes,
+                   "step": "one Jacobi-PCG iteration (y = A p + 3 vector kernels)",
+                   "iterations_per_solve": iters, "rel_tol": PCG_TOL,
+                   "l2": "matrix >= 3x L2" if nbytes > 3 * 129e6 else
+                         "working set fits L2 (matrix-free operator)",
+                   "timing": "CUDA events around whole solves",
+                   "parallelism": f"replicas{world}"},
+        "solve": {"iterations": sol["iterations"], "status": sol["status"],
+                  "ms": t_sol * 1e3, "rel_residual": sol["rel_residual"]},
+        "roofline": {"bound": "hbm", "achieved": per_launch, "peak": load_peak()[0],
+                     "unit": "GB/s", "frac": per_launch / load_peak()[0],
+                     "peak_source": load_peak()[1], "traffic": traffic},
+        "e2e": {"value": world * nbytes * res["iterations"] / e2e_sec / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,
+                "note": "one whole solve to 1e-6 per step, b in and x out",
+                "ms_per_solve": e2e_sec * 1e3},
+        "gpu_launches": 4 * steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cpu_gbs, sample = oracle_baseline(m, fmt, args.cpu_budget)
+        line["cpu_baseline"] = {"value": cpu_gbs, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": sample}
+    return line
+
+
 def bench_one(args, name, world, rank, local, pg):
     import torch
     import sparse_matrix_vector_gb300 as S
 
     key, fmt, desc = WORKLOADS[name]
+    if fmt.startswith("pcg"):
+        return bench_pcg(args, name, world, rank, local, pg)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     t0 = time.perf_counter()

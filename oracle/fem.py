@@ -87,3 +87,15 @@ def fem_matvec_assembled(nex, ney, nez, rho, K0, x):
     """y = K x through the assembled matrix (csr_spmv)."""
     rp, ci, v = fem_assemble(nex, ney, nez, rho, K0)
     return csr_spmv(rp, ci, v, x)
+
+
+def fem_diagonal(nex, ney, nez, rho, K0):
+    """The diagonal of the assembled K: every element adds rho_e K0[d, d] at
+    each of its local dofs d."""
+    edof = element_dofs(nex, ney, nez)
+    n_dofs = 3 * (nex + 1) * (ney + 1) * (nez + 1)
+    r = np.asarray(rho, dtype=np.float64)
+    kd = np.diag(np.asarray(K0, dtype=np.float64))
+    d = np.zeros(n_dofs)
+    np.add.at(d, edof.reshape(-1), (r[:, None] * kd[None, :]).reshape(-1))
+    return d

@@ -186,6 +186,11 @@ struct Plan {
   // conjugate-gradient workspace, allocated by the first solve
   float* diag = nullptr;
   unsigned char* pcg_work = nullptr;
+  // a captured batch of CG iterations (cudaGraphExec_t) and what it was
+  // captured for: b, x, diag and the batch length
+  void* pcg_exec = nullptr;
+  const void* pcg_key[3] = {nullptr, nullptr, nullptr};
+  int pcg_batch = 0;
   float fem_k0[24 * 24] = {};
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs

@@ -6,8 +6,9 @@
 // (step length, updates, new direction). Vectors are fp32; the scalars of
 // the recurrence live in device memory in fp64, so the host never waits
 // inside an iteration. Dot products are reduced in two fixed-order levels
-// (per block, then the block partials in block order by whichever block
-// finishes last), so a solve gives the same bits every time. Once the
+// (per block; then the block partials by whichever block finishes last, each
+// of its threads a fixed stride of them before a fixed-order block sum), so a
+// solve gives the same bits every time. Once the
 // residual test passes (or the iteration limit or a breakdown is hit) a
 // device flag turns the remaining kernels of a batch into no-ops, and the
 // host only reads the scalars between batches.
@@ -35,7 +36,7 @@ struct PcgVectors {
 };
 
 // Fixed-order sums of up to three per-thread values over the block; thread 0
-// gets the totals.
+// gets the totals. Called by every thread.
 template <int K>
 __device__ __forceinline__ void block_sums(double (&v)[K]) {
   __shared__ double s_w[K][kPcgThreads / 32];
@@ -57,23 +58,36 @@ __device__ __forceinline__ void block_sums(double (&v)[K]) {
   }
 }
 
-// Thread 0 of each block: park the block's sums; returns true in the block
-// that finishes last, with the grid totals (block order) in tot.
+// Every thread: thread 0 parks the block's sums (from block_sums); the block
+// that arrives last then adds all the blocks' sums, each thread a fixed
+// stride of them and then block_sums in fixed order, and returns true with
+// the grid totals in thread 0's tot. Every other block returns false.
 template <int K>
 __device__ __forceinline__ bool grid_sums(const PcgVectors& a, const double (&v)[K],
                                           double (&tot)[K]) {
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
 #pragma unroll
-  for (int k = 0; k < K; ++k) a.partials[k * kPcgBlocks + blockIdx.x] = v[k];
+    for (int k = 0; k < K; ++k) a.partials[k * kPcgBlocks + blockIdx.x] = v[k];
+    __threadfence();
+    s_last = atomicAdd(&a.sc->arrived, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return false;
   __threadfence();
-  if (atomicAdd(&a.sc->arrived, 1) != (int)gridDim.x - 1) return false;
-  __threadfence();
+  double w[K];
 #pragma unroll
   for (int k = 0; k < K; ++k) {
-    double t = 0.0;
-    for (int i = 0; i < (int)gridDim.x; ++i) t += __ldcg(a.partials + k * kPcgBlocks + i);
-    tot[k] = t;
+    w[k] = 0.0;
+    for (int i = threadIdx.x; i < (int)gridDim.x; i += kPcgThreads)
+      w[k] += __ldcg(a.partials + k * kPcgBlocks + i);
   }
-  a.sc->arrived = 0;
+  block_sums<K>(w);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) tot[k] = w[k];
+    a.sc->arrived = 0;
+  }
   return true;
 }
 
@@ -98,7 +112,7 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_init(const PcgVectors a) {
   }
   block_sums<3>(v);
   double t[3];
-  if (threadIdx.x == 0 && grid_sums<3>(a, v, t)) {
+  if (grid_sums<3>(a, v, t) && threadIdx.x == 0) {
     PcgScalars* sc = a.sc;
     sc->rz = t[0];
     sc->rr = t[1];
@@ -116,7 +130,7 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_alpha(const PcgVectors a) {
     v[0] += (double)a.p[i] * a.q[i];
   block_sums<1>(v);
   double t[1];
-  if (threadIdx.x == 0 && grid_sums<1>(a, v, t)) {
+  if (grid_sums<1>(a, v, t) && threadIdx.x == 0) {
     PcgScalars* sc = a.sc;
     if (!(t[0] > 0.0)) {
       sc->done = kPcgBreakdown;  // p . A p <= 0: A is not positive definite
@@ -142,7 +156,7 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
   }
   block_sums<2>(v);
   double t[2];
-  if (threadIdx.x == 0 && grid_sums<2>(a, v, t)) {
+  if (grid_sums<2>(a, v, t) && threadIdx.x == 0) {
     PcgScalars* sc = a.sc;
     sc->beta = t[0] / sc->rz;
     sc->rz = t[0];

@@ -358,6 +358,8 @@ def pin_fem_assembled_routes():
     assert rp[-1] == workloads.fem_nnz(5, 4, 3)
     A = sp.csr_matrix((v, ci, rp), shape=(m.n_dofs, m.n_dofs))
     assert abs(A - A.T).max() == 0
+    assert np.allclose(fem.fem_diagonal(m.nex, m.ney, m.nez, m.rho, m.K0), A.diagonal(),
+                       rtol=1e-15, atol=0)
     rng = np.random.default_rng(1)
     for _ in range(3):
         z = rng.standard_normal(m.n_dofs)
