@@ -6,14 +6,20 @@
 // with one thread per element and atomic adds into y. Here the same sum is
 // taken from the output side: one thread per node adds, for each of the (up
 // to) 8 elements around it, rho_e times the node's 3 rows of K0 times the
-// element's 24 values, gathered through L1 element by element (48 registers:
-// on GB300 the 120x60x30 mesh takes 11.1 us, against 14.4 us when the 81
-// values of the 27 neighbouring nodes are held in registers at once, 85
-// registers). Every y entry is written once (no atomics, results
-// reproducible run to run), and the only per-element data read is rho_e. K0 travels in the kernel's parameter space: in the
-// fully unrolled loops every K0 index is a compile-time constant that is
-// the same for all threads, so it is read as a constant-bank operand of the
-// fma. The kernel is bound by fp32 fma issue, not by memory.
+// element's 24 values, gathered through L1 element by element. Neighbour
+// coordinates are clamped into the mesh once (only elements outside it,
+// weighted by rho = 0, ever reach a clamped node), so each gather is a base
+// offset plus a constant. Every y entry is written once (no atomics, results
+// reproducible run to run), and the only per-element data read is rho_e.
+// K0 travels in the kernel's parameter space: in the fully unrolled loops
+// every K0 index is a compile-time constant that is the same for all
+// threads. The row products use the paired fp32 fma (two independent
+// round-to-nearest fmas per instruction, even and odd columns summed
+// separately). The kernel is bound by fp32 issue, not by memory. On GB300,
+// 120x60x30 mesh: 10.1 us; 10.4 us with scalar fmas, 10.8 us loading each of
+// the 27 neighbours once and accumulating per element, 11.1 us without the
+// clamped bases, 14.4 us holding all 81 neighbour values in registers,
+// 22.9 us staging them in shared memory.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -52,6 +58,16 @@ __global__ void __launch_bounds__(kFemThreads) fem_kernel(const __grid_constant_
   const int i = node % nnx, j = (node / nnx) % nny, k = node / (nnx * nny);
   // x and y belong to the stream's earlier work
   pdl_wait();
+  // neighbour coordinates clamped into the mesh: only elements outside the
+  // mesh (weighted by rho = 0 below) ever reach a clamped node
+  const int xo[3] = {3 * (i > 0 ? i - 1 : 0), 3 * i, 3 * (i + 1 < nnx ? i + 1 : i)};
+  const int yc[3] = {j > 0 ? j - 1 : 0, j, j + 1 < nny ? j + 1 : j};
+  const int zc[3] = {k > 0 ? k - 1 : 0, k, k + 1 <= a.nez ? k + 1 : k};
+  int line[9];  // offset of node (0, j + dy, k + dz) in x, (dz + 1) * 3 + (dy + 1)
+#pragma unroll
+  for (int dz = 0; dz < 3; ++dz)
+#pragma unroll
+    for (int dy = 0; dy < 3; ++dy) line[dz * 3 + dy] = 3 * nnx * (yc[dy] + nny * zc[dz]);
   float f[3] = {0.f, 0.f, 0.f};
 #pragma unroll
   for (int oz = 0; oz < 2; ++oz)
@@ -61,27 +77,25 @@ __global__ void __launch_bounds__(kFemThreads) fem_kernel(const __grid_constant_
       for (int ox = 0; ox < 2; ++ox) {
         const int ex = i - 1 + ox, ey = j - 1 + oy, ez = k - 1 + oz;
         const bool in = ex >= 0 && ex < a.nex && ey >= 0 && ey < a.ney && ez >= 0 && ez < a.nez;
-        const int e = in ? ex + a.nex * (ey + a.ney * ez) : 0;
-        const float rv = __ldg(a.rho + e);
+        const float rv = __ldg(a.rho + (in ? ex + a.nex * (ey + a.ney * ez) : 0));
         const float r = in ? rv : 0.f;
-        // the element's 24 values (an element outside the mesh reads
-        // element 0's, in bounds, and is weighted by 0)
-        const int exx = in ? ex : 0, eyy = in ? ey : 0, ezz = in ? ez : 0;
         float u[24];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const float* p = a.x + 3 * ((exx + hx(b)) + nnx * ((eyy + hy(b)) + nny * (ezz + hz(b))));
+        for (int bb = 0; bb < 8; ++bb) {
+          const float* p = a.x + (line[(oz + hz(bb)) * 3 + (oy + hy(bb))] + xo[ox + hx(bb)]);
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc) u[3 * b + cc] = __ldg(p + cc);
+          for (int cc = 0; cc < 3; ++cc) u[3 * bb + cc] = __ldg(p + cc);
         }
         const int an = corner_of(1 - ox, 1 - oy, 1 - oz);
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
           const float* krow = a.K0 + (3 * an + c) * 24;
-          float t = 0.f;
+          float2 t2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < 24; ++q) t = fmaf(krow[q], u[q], t);
-          f[c] = fmaf(r, t, f[c]);
+          for (int q = 0; q < 12; ++q)
+            t2 = __ffma2_rn(make_float2(krow[2 * q], krow[2 * q + 1]),
+                            make_float2(u[2 * q], u[2 * q + 1]), t2);
+          f[c] = fmaf(r, t2.x + t2.y, f[c]);
         }
       }
 #pragma unroll
