@@ -500,7 +500,8 @@ void free_plan(spmv_plan* plan) {
   Plan* p = &plan->impl;
   {
     DeviceGuard g(p->device);
-    if (p->pcg_exec) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->pcg_exec));
+    for (void* g : p->pcg_exec)
+      if (g) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(g));
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
@@ -1405,9 +1406,12 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
     return SPMV_ERR_CUDA;
   if ((s = spmv_run(plan, x, qv, stream)) != SPMV_OK) return s;  // q = A x0
   if (launch_pcg(0, p, b, x, d, stream) != 0) return SPMV_ERR_CUDA;
-  const int batch = check_every > 0 ? check_every : 16;
-  auto enqueue_batch = [&]() -> spmv_status {
-    for (int k = 0; k < batch; ++k) {
+  // Batches of 4, then 8, then check_every (default 16) iterations: short
+  // solves stop within a few iterations of convergence, long ones pay one
+  // host check per check_every iterations.
+  const int full = check_every > 0 ? check_every : 16;
+  auto enqueue_batch = [&](int n_it) -> spmv_status {
+    for (int k = 0; k < n_it; ++k) {
       spmv_status e = spmv_run(plan, pv, qv, stream);  // q = A p
       if (e != SPMV_OK) return e;
       for (int stage = 1; stage <= 3; ++stage)
@@ -1416,46 +1420,63 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
     return SPMV_OK;
   };
   // A batch is 4 launches per iteration; replaying it as one CUDA graph
-  // takes the host's launch cost out of the loop. The graph bakes in b, x and
-  // the diagonal, so it is kept for the next solve with the same ones. The
-  // legacy default stream cannot be captured, nor can a stream the caller is
-  // already capturing: those take the direct launches.
+  // takes the host's launch cost out of the loop. The graphs bake in b, x
+  // and the diagonal, so they are kept for the next solve with the same
+  // ones. The legacy default stream cannot be captured, nor can a stream the
+  // caller is already capturing: those take the direct launches.
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   const bool graphable = st != nullptr && cudaStreamIsCapturing(st, &cap) == cudaSuccess &&
                          cap == cudaStreamCaptureStatusNone;
   cudaGetLastError();
   const void* key[3] = {b, x, d};
-  if (graphable && !(p.pcg_exec && p.pcg_batch == batch && p.pcg_key[0] == key[0] &&
-                     p.pcg_key[1] == key[1] && p.pcg_key[2] == key[2])) {
-    if (p.pcg_exec) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p.pcg_exec));
-    p.pcg_exec = nullptr;
-    cudaGraph_t g = nullptr;
+  if (p.pcg_key[0] != key[0] || p.pcg_key[1] != key[1] || p.pcg_key[2] != key[2]) {
+    for (int g = 0; g < Plan::kPcgGraphs; ++g) {
+      if (p.pcg_exec[g]) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p.pcg_exec[g]));
+      p.pcg_exec[g] = nullptr;
+      p.pcg_batch[g] = 0;
+    }
+    for (int q = 0; q < 3; ++q) p.pcg_key[q] = key[q];
+  }
+  // the graph of a batch length, captured on first use (null: launch directly)
+  auto graph_for = [&](int n_it) -> cudaGraphExec_t {
+    if (!graphable) return nullptr;
+    int slot = -1;
+    for (int g = 0; g < Plan::kPcgGraphs; ++g)
+      if (p.pcg_batch[g] == n_it && p.pcg_exec[g])
+        return static_cast<cudaGraphExec_t>(p.pcg_exec[g]);
+      else if (slot < 0 && !p.pcg_exec[g])
+        slot = g;
+    if (slot < 0) return nullptr;
+    cudaGraph_t gr = nullptr;
+    cudaGraphExec_t exec = nullptr;
     if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
-      const spmv_status e = enqueue_batch();
-      const cudaError_t ce = cudaStreamEndCapture(st, &g);
-      cudaGraphExec_t exec = nullptr;
-      if (e == SPMV_OK && ce == cudaSuccess && g &&
-          cudaGraphInstantiate(&exec, g, 0) == cudaSuccess) {
-        p.pcg_exec = exec;
-        p.pcg_batch = batch;
-        for (int q = 0; q < 3; ++q) p.pcg_key[q] = key[q];
-      }
-      if (g) cudaGraphDestroy(g);
+      const spmv_status e = enqueue_batch(n_it);
+      const cudaError_t ce = cudaStreamEndCapture(st, &gr);
+      if (e != SPMV_OK || ce != cudaSuccess || !gr ||
+          cudaGraphInstantiate(&exec, gr, 0) != cudaSuccess)
+        exec = nullptr;
+      if (gr) cudaGraphDestroy(gr);
     }
     cudaGetLastError();  // a failed capture leaves the direct launches
-  }
+    if (exec) {
+      p.pcg_exec[slot] = exec;
+      p.pcg_batch[slot] = n_it;
+    }
+    return exec;
+  };
   for (int64_t it = 0;;) {
     if (cudaMemcpyAsync(&sc, sc_dev, sizeof(sc), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
       return SPMV_ERR_CUDA;
     if (sc.done || it >= max_iter) break;
-    if (graphable && p.pcg_exec) {
-      if (cudaGraphLaunch(static_cast<cudaGraphExec_t>(p.pcg_exec), st) != cudaSuccess)
-        return SPMV_ERR_CUDA;
-    } else if ((s = enqueue_batch()) != SPMV_OK) {
+    const int n_it = it == 0 ? std::min(4, full) : (it == std::min(4, full) ? std::min(8, full) : full);
+    cudaGraphExec_t exec = graph_for(n_it);
+    if (exec) {
+      if (cudaGraphLaunch(exec, st) != cudaSuccess) return SPMV_ERR_CUDA;
+    } else if ((s = enqueue_batch(n_it)) != SPMV_OK) {
       return s;
     }
-    it += batch;
+    it += n_it;
   }
   result->iterations = sc.iter;
   result->status = sc.done ? sc.done : kPcgMaxIter;

@@ -186,11 +186,12 @@ struct Plan {
   // conjugate-gradient workspace, allocated by the first solve
   float* diag = nullptr;
   unsigned char* pcg_work = nullptr;
-  // a captured batch of CG iterations (cudaGraphExec_t) and what it was
-  // captured for: b, x, diag and the batch length
-  void* pcg_exec = nullptr;
+  // captured batches of CG iterations (cudaGraphExec_t), one per batch
+  // length, and the b, x and diag they were captured for
+  static constexpr int kPcgGraphs = 3;
+  void* pcg_exec[kPcgGraphs] = {nullptr, nullptr, nullptr};
+  int pcg_batch[kPcgGraphs] = {0, 0, 0};
   const void* pcg_key[3] = {nullptr, nullptr, nullptr};
-  int pcg_batch = 0;
   float fem_k0[24 * 24] = {};
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
