@@ -113,8 +113,8 @@ typedef enum spmv_delta_policy {
 /* A CSR matrix in HOST memory ([CSR] section 2.1).
  * row_ptr: n_rows+1 offsets, row_ptr[0] == 0, non-decreasing, last == nnz.
  * col_idx: nnz column indices in [0, n_cols). Any order and repeats are
- *          accepted for SPMV_FORMAT_CSR (repeats add up); DELTA4 needs
- *          strictly increasing columns inside every row.
+ *          accepted for SPMV_FORMAT_CSR and SELL (repeats add up); the
+ *          DELTA formats need strictly increasing columns inside every row.
  * values:  nnz elements of value_dtype (fp16 given as its 16-bit pattern). */
 typedef struct spmv_csr {
   int32_t n_rows;
@@ -308,7 +308,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* csr, spmv_format format,
                               spmv_plan_info* info);
 
 /* Build a plan on the current CUDA device ([CSR] section 2.2): validate,
- * convert (DELTA4), bin the rows, then copy the matrix and the planner's
+ * convert (DELTA, SELL), bin the rows, then copy the matrix and the planner's
  * tables into device memory owned by the plan. The caller may free its host
  * arrays as soon as this returns. Synchronous. On error *out is NULL. */
 spmv_status spmv_plan_create(const spmv_csr* csr, spmv_format format,
@@ -386,8 +386,8 @@ spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info);
  * default stream). x_dev: n_cols elements (fp32 for fp32-value plans, fp16
  * otherwise), aligned to its element size; y_dev: n_rows fp32, aligned to 4
  * bytes, fully overwritten (rows without nonzeros get 0). x and y must not
- * overlap. DELTA4 plans multiply padding entries as 0 * x[c], so x must be
- * finite there. Does not synchronize. Errors: INVALID_ARG, WRONG_DEVICE,
+ * overlap. DELTA, SELL and FEM plans multiply padding (or out-of-mesh)
+ * entries as 0 * x[c], so x must be finite there. Does not synchronize. Errors: INVALID_ARG, WRONG_DEVICE,
  * CUDA (launch failure). */
 spmv_status spmv_run(spmv_plan* plan, const void* x_dev, float* y_dev,
                      void* stream);
