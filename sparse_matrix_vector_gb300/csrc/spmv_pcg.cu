@@ -91,24 +91,50 @@ __device__ __forceinline__ bool grid_sums(const PcgVectors& a, const double (&v)
   return true;
 }
 
-__device__ __forceinline__ float jacobi(const float* diag, int i, float r) {
-  const float d = diag[i];
+__device__ __forceinline__ float jacobi(float d, float r) {
   return d != 0.f ? r / d : r;  // a row without a diagonal is left unscaled
 }
 
+// Each thread takes elements i, i + S, i + 2S, i + 3S (S = the grid's
+// threads) per pass, all four loads issued before any is used, so a thread
+// waits on one memory round trip per pass instead of one per element. A
+// thread's share of a dot product is summed in fp32 over a pass (at most 4
+// terms) and then added into an fp64 total (fp64 arithmetic is scarce on
+// this part).
+constexpr int kPcgUnroll = 4;
+
 // r = b - q (q = A x0), z = D^-1 r, p = z; rz, rr, bb.
 __global__ void __launch_bounds__(kPcgThreads) pcg_init(const PcgVectors a) {
+  const int S = gridDim.x * kPcgThreads;
   double v[3] = {0.0, 0.0, 0.0};
-  for (int i = blockIdx.x * kPcgThreads + threadIdx.x; i < a.n; i += gridDim.x * kPcgThreads) {
-    const float bi = a.b[i];
-    const float ri = bi - a.q[i];
-    const float zi = jacobi(a.diag, i, ri);
-    a.r[i] = ri;
-    a.z[i] = zi;
-    a.p[i] = zi;
-    v[0] += (double)ri * zi;
-    v[1] += (double)ri * ri;
-    v[2] += (double)bi * bi;
+  for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
+    float bv[kPcgUnroll], qv[kPcgUnroll], dv[kPcgUnroll];
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      if (i < a.n) {
+        bv[u] = a.b[i];
+        qv[u] = a.q[i];
+        dv[u] = a.diag[i];
+      }
+    }
+    float c[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      if (i < a.n) {
+        const float ri = bv[u] - qv[u];
+        const float zi = jacobi(dv[u], ri);
+        a.r[i] = ri;
+        a.z[i] = zi;
+        a.p[i] = zi;
+        c[0] = fmaf(ri, zi, c[0]);
+        c[1] = fmaf(ri, ri, c[1]);
+        c[2] = fmaf(bv[u], bv[u], c[2]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) v[q] += c[q];
   }
   block_sums<3>(v);
   double t[3];
@@ -125,9 +151,21 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_init(const PcgVectors a) {
 // alpha = rz / (p . q).
 __global__ void __launch_bounds__(kPcgThreads) pcg_alpha(const PcgVectors a) {
   if (a.sc->done) return;
+  const int S = gridDim.x * kPcgThreads;
   double v[1] = {0.0};
-  for (int i = blockIdx.x * kPcgThreads + threadIdx.x; i < a.n; i += gridDim.x * kPcgThreads)
-    v[0] += (double)a.p[i] * a.q[i];
+  for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
+    float pv[kPcgUnroll], qv[kPcgUnroll];
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      pv[u] = i < a.n ? a.p[i] : 0.f;
+      qv[u] = i < a.n ? a.q[i] : 0.f;
+    }
+    float c = 0.f;
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) c = fmaf(pv[u], qv[u], c);
+    v[0] += c;
+  }
   block_sums<1>(v);
   double t[1];
   if (grid_sums<1>(a, v, t) && threadIdx.x == 0) {
@@ -144,15 +182,37 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_alpha(const PcgVectors a) {
 __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
   if (a.sc->done) return;
   const float alpha = (float)a.sc->alpha;
+  const int S = gridDim.x * kPcgThreads;
   double v[2] = {0.0, 0.0};
-  for (int i = blockIdx.x * kPcgThreads + threadIdx.x; i < a.n; i += gridDim.x * kPcgThreads) {
-    a.x[i] = fmaf(alpha, a.p[i], a.x[i]);
-    const float ri = fmaf(-alpha, a.q[i], a.r[i]);
-    const float zi = jacobi(a.diag, i, ri);
-    a.r[i] = ri;
-    a.z[i] = zi;
-    v[0] += (double)ri * zi;
-    v[1] += (double)ri * ri;
+  for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
+    float xv[kPcgUnroll], pv[kPcgUnroll], rv[kPcgUnroll], qv[kPcgUnroll], dv[kPcgUnroll];
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      if (i < a.n) {
+        xv[u] = a.x[i];
+        pv[u] = a.p[i];
+        rv[u] = a.r[i];
+        qv[u] = a.q[i];
+        dv[u] = a.diag[i];
+      }
+    }
+    float c[2] = {0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      if (i < a.n) {
+        a.x[i] = fmaf(alpha, pv[u], xv[u]);
+        const float ri = fmaf(-alpha, qv[u], rv[u]);
+        const float zi = jacobi(dv[u], ri);
+        a.r[i] = ri;
+        a.z[i] = zi;
+        c[0] = fmaf(ri, zi, c[0]);
+        c[1] = fmaf(ri, ri, c[1]);
+      }
+    }
+    v[0] += c[0];
+    v[1] += c[1];
   }
   block_sums<2>(v);
   double t[2];
@@ -173,8 +233,23 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
 __global__ void __launch_bounds__(kPcgThreads) pcg_direction(const PcgVectors a) {
   if (a.sc->done) return;
   const float beta = (float)a.sc->beta;
-  for (int i = blockIdx.x * kPcgThreads + threadIdx.x; i < a.n; i += gridDim.x * kPcgThreads)
-    a.p[i] = fmaf(beta, a.p[i], a.z[i]);
+  const int S = gridDim.x * kPcgThreads;
+  for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
+    float zv[kPcgUnroll], pv[kPcgUnroll];
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      if (i < a.n) {
+        zv[u] = a.z[i];
+        pv[u] = a.p[i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPcgUnroll; ++u) {
+      const int i = i0 + u * S;
+      if (i < a.n) a.p[i] = fmaf(beta, pv[u], zv[u]);
+    }
+  }
 }
 
 }  // namespace
