@@ -469,3 +469,20 @@ def test_pcg_argument_errors(spmv_lib):
     assert spmv_lib.spmv_pcg_solve(None, None, None, None, 1e-6, 10, 0, None,
                                    ctypes.byref(res)) == 1
     assert spmv_lib.spmv_pcg_solve(None, None, None, None, 1e-6, 10, 0, None, None) == 1
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_delta_planner_unit_counts(spmv_lib, bits):
+    """Every row becomes ceil(words / unit words) units (one for an empty
+    row); unit words are 256 at 2 bits and 512 otherwise; rows of more than
+    one unit are the split rows."""
+    lengths = np.array([0, 1, 7, 300, 2000, 5000, 12000, 0, 4096, 4097, 8193])
+    m = workloads.from_lengths("units", lengths, 20000, seed=5, dtype=np.float16)
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format=f"delta{bits}")
+    enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, bits=bits)
+    words = np.diff(enc.row_ptr) * bits // 32
+    unit_words = 256 if bits == 2 else 512
+    units = np.maximum(1, -(-words // unit_words))
+    assert info["n_tiles"] == units.sum()
+    assert info["n_split_rows"] == (units > 1).sum()
+    assert info["n_entries"] == enc.n_entries
