@@ -140,7 +140,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100",
+                 "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception as e:  # nvidia-smi missing: report no clocks
             log("clock sampling unavailable:", e)
@@ -194,6 +194,61 @@ def job_throughput(nbytes: int, world: int, ms: float, steps: int):
     `nbytes` in `ms`) and one launch's GB/s."""
     sec_per_step = ms / 1e3 / steps
     return sec_per_step, world * nbytes / sec_per_step / 1e9, nbytes / sec_per_step / 1e9
+
+
+# A timed region is K back-to-back steps. Regions repeat until about
+# REGION_SECONDS of device time has been timed (at least MIN_REGIONS), and the
+# line reports their median (min and max beside it).
+REGION_SECONDS = 0.6
+MIN_REGIONS = 5
+MAX_REGIONS = 5000
+# clock cycles of torch's bounded spin kernel queued ahead of every region:
+# the host submits the region's graph replays while it runs, so the region's
+# first event is followed at once by the first SpMV kernel rather than by the
+# replay's submission
+LEAD_CYCLES = 300_000
+
+
+def timed_regions(run_region, stream, dev, pg, local, steps, est_step_s):
+    """Time `steps` steps (one call of run_region, which enqueues them on
+    `stream`) several times over. Each
+    region is bracketed by a barrier and torch.cuda.synchronize() on both
+    sides and timed with CUDA events on the launching stream. Returns the
+    per-region statistics in ms (max over ranks of each) and the clock record
+    sampled across all regions."""
+    import torch
+    n = int(min(MAX_REGIONS, max(MIN_REGIONS, math.ceil(
+        REGION_SECONDS / max(steps * est_step_s, 1e-7)))))
+    clocks = ClockSampler(local)
+    clocks.start()
+    times = []
+    for _ in range(n):
+        if pg is not None:
+            torch.distributed.barrier(group=pg)
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(LEAD_CYCLES)
+            ev0.record(stream)
+            run_region()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(ev0.elapsed_time(ev1))
+    clk = clocks.stop()
+    stats = [statistics.median(times), min(times), max(times), times[0]]
+    stats = [max_over_ranks(t, dev, pg) for t in stats]
+    return {"regions": n, "median_ms": stats[0], "min_ms": stats[1],
+            "max_ms": stats[2], "first_ms": stats[3]}, clk
+
+
+def region_report(regions, steps):
+    """config.timing's statistics, per step."""
+    return {"regions": regions["regions"], "steps_per_region": steps,
+            "median_ms_per_step": regions["median_ms"] / steps,
+            "min_ms_per_step": regions["min_ms"] / steps,
+            "max_ms_per_step": regions["max_ms"] / steps,
+            "first_region_ms_per_step": regions["first_ms"] / steps}
 
 
 def dist_setup():
@@ -292,6 +347,48 @@ def oracle_baseline(m, fmt, budget_s: float):
     return nbytes / dt / 1e9, f"whole matrix, {reps} calls"
 
 
+def parallel_baseline(m, fmt, budget_s: float):
+    """The all-core CPU baseline: the oracle's loop with its rows shared out
+    over OpenMP threads (oracle/parallel.py), on the whole matrix, repeated
+    for about budget_s. Same byte model as the GPU line. None for the
+    matrix-free operator and the solver, or when it could not be built."""
+    if fmt == "fem" or fmt.startswith("pcg"):
+        return None
+    try:
+        import oracle
+        from oracle import parallel
+        n_threads = parallel.threads()
+    except Exception as e:  # noqa: BLE001
+        return {"unavailable": f"OpenMP baseline not built: {e}"}
+    if fmt.startswith("delta"):
+        bits = int(fmt[5:])
+        enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, bits=bits)
+        call = parallel.DeltaOperands(enc, m.x)
+        nbytes = (enc.n_entries * 2 + enc.n_entries * bits // 8 + (m.n_rows + 1) * 4
+                  + m.n_cols * 2 + m.n_rows * 4)
+    else:
+        call = parallel.CsrOperands(m.row_ptr, m.col_idx, m.values, m.x)
+        if fmt == "sell":
+            from oracle import sell
+            slots, slices = sell.sell_slot_count(m.row_ptr, 32, 1)
+            nbytes = (slots * (m.values.dtype.itemsize + 4) + (slices + 1) * 4
+                      + m.n_cols * m.x.dtype.itemsize + m.n_rows * 4)
+        else:
+            nbytes = algorithmic_bytes_csr(m)
+    call()
+    t0 = time.perf_counter()
+    call()
+    t1 = time.perf_counter() - t0
+    reps = max(3, int(budget_s / max(t1, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        call()
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": n_threads,
+            "nproc": os.cpu_count(), "kind": "oracle loop, rows over OpenMP threads",
+            "sample": f"whole matrix, {reps} calls"}
+
+
 def algorithmic_bytes_csr(m):
     vs = m.values.dtype.itemsize
     return (m.nnz * (vs + 4) + (m.n_rows + 1) * 4 + m.n_cols * m.x.dtype.itemsize
@@ -378,25 +475,24 @@ def bench_pcg(args, name, world, rank, local, pg):
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             sol = solve()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        solve()
+    torch.cuda.synchronize(dev)
+    sol_ms = (time.perf_counter() - t0) * 1e3
     iters = first["it"]
     solves = max(3, (args.steps or 2000) // max(iters, 1))
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local)
-    if pg is not None:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
+    steps = solves * iters
+
+    def solves_region():
         for _ in range(solves):
             solve()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    steps = solves * iters
-    ms = max_over_ranks(ev0.elapsed_time(ev1), dev, pg)
+
+    regions, clk = timed_regions(solves_region, stream, dev, pg, local, steps,
+                                 sol_ms / 1e3 / iters)
+    ms = regions["median_ms"]
     sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
     t_sol = ms / solves / 1e3
     # end to end: b copied in from pinned host memory, x copied back
@@ -425,7 +521,9 @@ def bench_pcg(args, name, world, rank, local, pg):
                    "iterations_per_solve": iters, "rel_tol": PCG_TOL,
                    "l2": "matrix >= 3x L2" if nbytes > 3 * 129e6 else
                          "working set fits L2 (matrix-free operator)",
-                   "timing": "CUDA events around whole solves",
+                   "timing": ("CUDA events around each region of whole solves; "
+                              "value and ms_per_step from the median region"),
+                   "regions": region_report(regions, steps),
                    "parallelism": f"replicas{world}"},
         "solve": {"iterations": sol["iterations"], "status": sol["status"],
                   "ms": t_sol * 1e3, "rel_residual": sol["rel_residual"]},
@@ -482,9 +580,9 @@ def bench_one(args, name, world, rank, local, pg):
     peak, peak_src = load_peak()
 
     steps = args.steps
-    if not steps:   # ~1.5 s of timed work at 70% of peak (>= 3 us a step)
+    if not steps:   # ~0.1 s of work per region at 70% of peak (>= 3 us a step)
         est = max(nbytes / (0.7 * peak * 1e9), 3e-6)
-        steps = min(200_000, max(200, int(1.5 / est)))
+        steps = min(20_000, max(200, int(0.1 / est)))
         steps = int(math.ceil(steps / copies) * copies)
     warmup = max(3, args.warmup)
 
@@ -510,22 +608,13 @@ def bench_one(args, name, world, rank, local, pg):
             g.replay()
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local)
-    if pg is not None:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
+    def replay():
         for g in graphs:
             g.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), dev, pg)
-    torch.cuda.synchronize(dev)
+
+    regions, clk = timed_regions(replay, stream, dev, pg, local, steps,
+                                 max(nbytes / (0.7 * peak * 1e9), 1e-6))
+    ms = regions["median_ms"]
     sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
     flops = m.n_elem * FEM_FLOPS_PER_ELEMENT if fmt == "fem" else 2 * m.nnz
     gflops = world * flops / sec_per_step / 1e9
@@ -568,8 +657,11 @@ def bench_one(args, name, world, rank, local, pg):
                               + (">= 3x" if copies * nbytes >= 3 * l2 else
                                  "< L2: latency-bound, L2-resident,")
                               + f" L2 ({l2 / 2**20:.0f} MiB)"),
-                       "timing": "CUDA graphs of back-to-back spmv_run, CUDA "
-                                 "events on the launching stream",
+                       "timing": ("CUDA graphs of back-to-back spmv_run, CUDA "
+                                  "events on the launching stream around each "
+                                  "region of `steps` steps; value and "
+                                  "ms_per_step from the median region"),
+                       "regions": region_report(regions, steps),
                        "parallelism": f"replicas{world}"},
             "gflops": gflops,
             "roofline": ({"bound": "hbm", "achieved": per_launch, "peak": peak,
@@ -593,6 +685,9 @@ def bench_one(args, name, world, rank, local, pg):
             cpu_gbs, sample = oracle_baseline(m, fmt, args.cpu_budget)
             line["cpu_baseline"] = {"value": cpu_gbs, "unit": "GB/s", "cores": 1,
                                     "kind": "oracle", "sample": sample}
+            par = parallel_baseline(m, fmt, args.cpu_budget / 2)
+            if par is not None:
+                line["cpu_baseline_all_cores"] = par
     for p in plans:
         S.spmv_plan_destroy(p)
     del xs, ys, graphs

@@ -20,16 +20,16 @@
  * Sources (web pages, by title and section):
  *   [CSR]   "CUDA CSR SpMV optimisation" (codechina.net), section 2.1: the CSR
  *           arrays and the definition y[row] = sum over k in
- *           [row_ptr[row], row_ptr[row+1]) of values[k] * x[col_idx[k]];
- *           section 2.2: one-time upload of the arrays with cudaMalloc and
- *           an asynchronous copy, then kernel launches chosen by the format.
+ *           [row_ptr[row], row_ptr[row+1]) of values[k] * x[col_idx[k]],
+ *           and a table comparing COO / CSR / ELL / HYB; section 2.2:
+ *           one-time upload of the arrays with cudaMalloc and an
+ *           asynchronous copy, kernel launches on a stream chosen by the
+ *           format, and the choice among ELL / HYB / CSR by the coefficient
+ *           of variation (CV) of the row lengths.
  *   [MACKO] "MACKO-SpMV" (maplevalley.com.cn), section 2.1: the format
  *           struct {values with zero placeholders, 4-bit deltas, row
  *           pointers} and its four encoding steps; section 2.2: the warp
  *           decode (prefix sum of deltas) and half2 multiply.
- *           Section 2.1 also compares COO / CSR / ELL / HYB, and section
- *           2.2 chooses among them by the coefficient of variation (CV) of
- *           the row lengths.
  *   [FEM]   "Fused FEM matvec" (bbs.csdn.net), section 2.1: y = K x as gather,
  *           element product and scatter-add; section 2.2: the three fused in
  *           one kernel; section 5.2: one element matrix shared by all
@@ -92,10 +92,12 @@ typedef enum spmv_format {
                              by spmv_plan_create_fem only                  */
   SPMV_FORMAT_AUTO = 6    /* CSR or SELL by the CV of the row lengths
                              (spmv_select_format), except that matrices
-                             whose rows hold more than 128 nonzeros on
-                             average take CSR (a lane per row serialises
-                             long rows); plans and their info report the
-                             chosen format                                  */
+                             whose rows hold more than 128 or fewer than
+                             16 nonzeros on average take CSR (a lane per
+                             row serialises long rows; a SELL warp over
+                             very short rows has too little to read);
+                             plans and their info report the chosen
+                             format                                         */
 } spmv_format;
 
 /* How spmv_delta_select_bits picks a delta width ([MACKO] section 3.3). */
@@ -244,7 +246,9 @@ typedef struct spmv_plan_info {
 
 typedef struct spmv_plan spmv_plan;
 
-/* Short English text for a status code (static storage). */
+/* Short English text for a status code (static storage). The pages have no
+ * counterpart: status codes replace the exceptions and aborts of their
+ * snippets. */
 const char* spmv_status_string(spmv_status status);
 
 /* Returns SPMV_ABI_VERSION of the built library. */
@@ -383,7 +387,8 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag_dev, const float* 
 spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info);
 
 /* y = A x, asynchronously on `stream` (a cudaStream_t; NULL = legacy
- * default stream). x_dev: n_cols elements (fp32 for fp32-value plans, fp16
+ * default stream): the launch step of [CSR] 2.2 (the matrix is already
+ * resident, so only kernels chosen by the plan's format run). x_dev: n_cols elements (fp32 for fp32-value plans, fp16
  * otherwise), aligned to its element size; y_dev: n_rows fp32, aligned to 4
  * bytes, fully overwritten (rows without nonzeros get 0). x and y must not
  * overlap. DELTA, SELL and FEM plans multiply padding (or out-of-mesh)
@@ -394,8 +399,10 @@ spmv_status spmv_run(spmv_plan* plan, const void* x_dev, float* y_dev,
 
 /* End-to-end variant with HOST buffers: copies x_host (n_cols elements of
  * the plan's x type) into a plan-owned device buffer, runs y = A x, copies
- * y back into y_host (n_rows fp32) and synchronizes `stream`. Pinned host
- * memory gives the fastest copies. */
+ * y back into y_host (n_rows fp32) and synchronizes `stream`: the copy-in,
+ * launch and copy-out of [CSR] 2.2 for the vectors. Pinned host memory gives
+ * the fastest copies. Errors: INVALID_ARG (null buffer), WRONG_DEVICE,
+ * CUDA. */
 spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
                           void* stream);
 
@@ -409,8 +416,10 @@ spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
  * row_ptr (n_rows+1), col_idx (nnz), values (nnz, value_dtype) and x (n_cols,
  * fp32 for SPMV_F32 values, fp16 for SPMV_F16) are caller-owned DEVICE
  * arrays on the current device and must form a valid CSR matrix (row_ptr
- * non-decreasing from 0 to nnz, columns in [0, n_cols)); they are not
- * validated. Alignment: col_idx 16 bytes, values 16 (fp32) or 8 (fp16)
+ * non-decreasing from 0 to nnz, columns in [0, n_cols)); their contents
+ * are not validated, but each pointer is checked (cudaPointerGetAttributes,
+ * which allocates nothing) to be device or managed memory of the current
+ * device. Alignment: col_idx 16 bytes, values 16 (fp32) or 8 (fp16)
  * bytes, row_ptr and y 4 bytes. y (n_rows fp32) is overwritten. Runs two
  * kernels on `stream`; calls no allocating routine.
  * Scratch: a file-scope device array of 768 KiB per device, shared by all
@@ -418,8 +427,9 @@ spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
  * race on it, so order them (one stream). The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress); make that first call
  * before any stream capture.
- * Errors: INVALID_ARG (negative sizes, null or misaligned pointers),
- * TOO_LARGE (nnz > 134,217,728, the scratch limit), CUDA. */
+ * Errors: INVALID_ARG (negative sizes, null or misaligned pointers, an
+ * array that is not on the current device), TOO_LARGE (nnz > 134,217,728,
+ * the scratch limit), CUDA. */
 spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols, int64_t nnz,
                                  const int32_t* row_ptr,
                                  const int32_t* col_idx, const void* values,
@@ -431,8 +441,9 @@ spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols, int64_t nnz,
  * word is cleared by this call). */
 spmv_status spmv_plan_check(spmv_plan* plan);
 
-/* Release the plan and its device memory (synchronizes the device first).
- * NULL is accepted. */
+/* Release the plan and its device memory (synchronizes the device first):
+ * the cudaFree counterpart of [CSR] 2.2's one-time upload. NULL is
+ * accepted. */
 void spmv_plan_destroy(spmv_plan* plan);
 
 #ifdef __cplusplus

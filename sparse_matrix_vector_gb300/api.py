@@ -408,14 +408,16 @@ def spmv_run_host(plan: Plan, x_host: np.ndarray, y_host: np.ndarray,
 def spmv_csr_run_noalloc(n_rows: int, n_cols: int, row_ptr, col_idx, values,
                          x, y, stream=None) -> None:
     """Allocation-free y = A x on a CSR matrix held in caller-owned CUDA
-    tensors (row_ptr/col_idx int32, values and x fp32 or fp16, y fp32).
-    For callers that may not allocate device memory; see include/spmv.h."""
+    tensors (row_ptr/col_idx int32, values and x fp32 or fp16, y fp32), all
+    contiguous and on the current CUDA device. For callers that may not
+    allocate device memory; see include/spmv.h."""
     import torch
     for name, t in (("row_ptr", row_ptr), ("col_idx", col_idx)):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
-    if values.dtype not in (torch.float32, torch.float16):
-        raise TypeError("values must be float32 or float16")
+    if (values.dtype not in (torch.float32, torch.float16) or not values.is_cuda
+            or not values.is_contiguous()):
+        raise TypeError("values must be a contiguous float32 or float16 CUDA tensor")
     code = SPMV_F32 if values.dtype == torch.float32 else SPMV_F16
     if row_ptr.numel() != n_rows + 1:
         raise ValueError("row_ptr must have n_rows + 1 elements")
@@ -424,6 +426,11 @@ def spmv_csr_run_noalloc(n_rows: int, n_cols: int, row_ptr, col_idx, values,
         raise ValueError("values and col_idx differ in length")
     xp = _dev_ptr(x, n_cols, code, "x")
     yp = _dev_ptr(y, n_rows, SPMV_F32, "y")
+    here = torch.cuda.current_device()
+    for name, t in (("row_ptr", row_ptr), ("col_idx", col_idx), ("values", values),
+                    ("x", x), ("y", y)):
+        if isinstance(t, torch.Tensor) and t.device.index != here:
+            raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{here}")
     _check(_lib.load().spmv_csr_run_noalloc(
         n_rows, n_cols, nnz, row_ptr.data_ptr(), col_idx.data_ptr(),
         values.data_ptr(), code, xp, yp, _stream_handle(stream)),

@@ -692,6 +692,12 @@ spmv_status upload_csr_diagonal(const spmv_csr* m, Plan* p) {
 
 constexpr int32_t kSellSigmaSorted = 1024;  // window of the middle CV band
 constexpr int32_t kSellMaxMeanRow = 128;    // AUTO: longer rows on average go to CSR
+// AUTO: rows shorter than this on average go to CSR too. A warp of SELL then
+// reads only a few slots and exits after two latency rounds, while CSR's
+// short-row tiles already read such rows with coalesced copies: on the
+// 1000 x 999 5-point Laplacian (5 per row) CSR runs 10.8 us and SELL 11.5 us;
+// on the hex-mesh stiffness matrix (78 per row) SELL runs 71 us and CSR 83 us.
+constexpr int32_t kSellMinMeanRow = 16;
 
 double row_length_cv(const spmv_csr* m) {
   if (m->n_rows == 0) return 0.0;
@@ -856,11 +862,13 @@ spmv_status resolve_format(const spmv_csr* m, const Options& o, spmv_format* for
     spmv_format f;
     int32_t sg;
     choose_by_cv(row_length_cv(m), &f, &sg);
-    // a lane per row serialises a long row's gathers: the CV band is taken
-    // only for rows of at most kSellMaxMeanRow stored entries on average
+    // a lane per row serialises a long row's gathers, and very short rows
+    // leave a SELL warp with too little to read: the CV band is taken only
+    // for rows of kSellMinMeanRow to kSellMaxMeanRow stored entries on average
+    const double nnz = (double)m->nnz, rows = (double)m->n_rows;
     if (*format == SPMV_FORMAT_AUTO)
-      *format = (f == SPMV_FORMAT_SELL &&
-                 (double)m->nnz > (double)kSellMaxMeanRow * (double)m->n_rows)
+      *format = (f == SPMV_FORMAT_SELL && (nnz > (double)kSellMaxMeanRow * rows ||
+                                           nnz < (double)kSellMinMeanRow * rows))
                     ? SPMV_FORMAT_CSR
                     : f;
     if (*format == SPMV_FORMAT_SELL)

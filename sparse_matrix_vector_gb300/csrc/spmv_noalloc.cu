@@ -175,6 +175,11 @@ noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ 
 
 // One thread per slice with a tail: y[row] = tail + heads of the slices the
 // row covers, in slice order.
+// Every head read here was written by this call: a row r whose tail sits in
+// slice k ends in slice last = (row_ptr[r+1] - 1) / kChunk > k, and for each
+// slice j in (k, last] the row is still open at its first nonzero lo_j (row r
+// started before lo_j and ends after it), so lower_bound gives that slice
+// rb > r, row_ptr[rb] > lo_j and h_end > 0: noalloc_slices stores head[j].
 __global__ void __launch_bounds__(kThreads)
 noalloc_fixup(const int32_t* __restrict__ row_ptr, float* __restrict__ y,
               int n_slices, Scratch s) {
@@ -217,6 +222,18 @@ spmv_status scratch_on_current_device(Scratch* out) {
   return SPMV_OK;
 }
 
+// True when p points to memory of device `dev` (device or managed memory).
+// cudaPointerGetAttributes allocates nothing.
+bool on_device(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) &&
+         a.device == dev;
+}
+
 }  // namespace
 
 extern "C" spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols,
@@ -235,6 +252,11 @@ extern "C" spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols,
   const uintptr_t vs = value_dtype == SPMV_F32 ? 4 : 2;
   if (((uintptr_t)row_ptr & 3u) || ((uintptr_t)y & 3u) || ((uintptr_t)col_idx & 15u) ||
       ((uintptr_t)values & (4 * vs - 1)) || ((uintptr_t)x & (vs - 1)))
+    return SPMV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
+  if (!on_device(row_ptr, dev) || !on_device(y, dev) ||
+      (nnz > 0 && (!on_device(col_idx, dev) || !on_device(values, dev) || !on_device(x, dev))))
     return SPMV_ERR_INVALID_ARG;
   Scratch s;
   spmv_status st = scratch_on_current_device(&s);

@@ -413,9 +413,9 @@ def test_format_choice_matches_oracle(spmv_lib, name):
     assert abs(cv - sell.row_length_cv(m.row_ptr)) <= 1e-12 * max(cv, 1.0)
     assert (fmt, sigma) == sell.select_format(m.row_ptr)
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="auto")
-    long_rows = m.nnz > 128 * m.n_rows
-    assert info["format"] == S.api.FORMATS["csr" if long_rows else fmt]
-    if fmt == "sell":
+    off_band = m.nnz > 128 * m.n_rows or m.nnz < 16 * m.n_rows
+    assert info["format"] == S.api.FORMATS["csr" if off_band else fmt]
+    if fmt == "sell" and not off_band:
         ref = sell.sell_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, C=32, sigma=sigma)
         assert info["n_entries"] == ref.n_slots and info["n_tiles"] == ref.n_slices
         vs = m.values.dtype.itemsize
@@ -436,6 +436,20 @@ def test_auto_format_sends_long_rows_to_csr(spmv_lib):
     assert fmt == "sell" and cv < 0.3
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="auto")
     assert info["format"] == 0
+
+
+def test_auto_format_sends_short_rows_to_csr(spmv_lib):
+    """The 5-point Laplacian's rows have CV < 0.3, the ELL band, but average
+    5 nonzeros: AUTO keeps rows shorter than 16 on average in CSR, and still
+    gives the stiffness matrix's ~78-long rows to SELL."""
+    m = workloads.laplacian(70, 41)
+    fmt, _, cv = S.spmv_select_format(m.row_ptr, m.col_idx, m.values, m.n_cols)
+    assert fmt == "sell" and cv < 0.3
+    info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format="auto")
+    assert info["format"] == 0
+    f = workloads.fem(5, 4, 3)
+    info = S.spmv_plan_inspect(f.row_ptr, f.col_idx, f.values, f.n_cols, format="auto")
+    assert info["format"] == 5
 
 
 def test_fem_plan_argument_errors(spmv_lib):

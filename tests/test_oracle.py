@@ -427,6 +427,22 @@ def test_delta_spmv_equals_csr_spmv():
     assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
 
 
+def test_all_core_baseline_equals_oracle():
+    """The OpenMP baseline shares the rows out over threads but sums each row
+    in the oracle's order, so its y is the oracle's bit for bit (CSR and the
+    three delta widths)."""
+    from oracle import parallel
+    m = workloads.powerlaw(n=20000, nnz=111000, max_len=3000)
+    y0 = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x, with_abs=False)
+    assert np.array_equal(y0, parallel.CsrOperands(m.row_ptr, m.col_idx, m.values, m.x)())
+    w = workloads.llm(0.7, n=600)
+    for bits in (2, 4, 8):
+        enc = oracle.delta_encode(w.n_cols, w.row_ptr, w.col_idx, w.values, bits=bits)
+        y1 = oracle.delta_spmv(enc, w.x, with_abs=False)
+        assert np.array_equal(y1, parallel.DeltaOperands(enc, w.x)())
+    assert parallel.threads() >= 1
+
+
 # mutations of the oracle source: (name, old text, new text)
 MUTANTS = [
     ("dropped_term", "k < row_ptr[i + 1]; ++k) {\n      double prod",

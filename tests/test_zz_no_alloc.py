@@ -1,5 +1,7 @@
 """The allocation-free entry point spmv_csr_run_noalloc, called through the C
-ABI, against the plan-based entry point (spmv_plan_create + spmv_run).
+ABI, against the fp64 oracle's y and against the plan-based entry point
+(spmv_plan_create + spmv_run); two of the cases also go through the public
+Python wrapper.
 
 spmv_csr_run_noalloc exists for callers that may not allocate device memory
 (for example a latency-critical loop after its set-up phase, a component
@@ -24,6 +26,8 @@ S = pytest.importorskip("sparse_matrix_vector_gb300")
 pytestmark = pytest.mark.gpu
 
 TOL = {np.dtype(np.float32): 1e-5, np.dtype(np.float16): 2e-3}
+# cases that also run through sparse_matrix_vector_gb300.spmv_csr_run_noalloc
+WRAPPER_CASES = ("llm70", "fem")
 
 
 def cases():
@@ -65,7 +69,7 @@ def test_noalloc_matches_plan_entry_point(spmv_lib, m):
     y_plan = y_plan.cpu().numpy().astype(np.float64)
     S.spmv_plan_destroy(plan)
 
-    _, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x)
+    y_ref, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x)
     bound = TOL[m.values.dtype] * s + 1e-30
     outs = []
     for _ in range(2):                      # two calls in a row
@@ -73,11 +77,20 @@ def test_noalloc_matches_plan_entry_point(spmv_lib, m):
         call_noalloc(spmv_lib, m, d_rp, d_ci, d_v, d_x, y, stream)
         torch.cuda.synchronize()
         outs.append(y.cpu().numpy().astype(np.float64))
+    if m.name in WRAPPER_CASES:             # the public wrapper, twice more
+        for _ in range(2):
+            y = torch.full((m.n_rows,), float("nan"), dtype=torch.float32, device=dev)
+            S.spmv_csr_run_noalloc(m.n_rows, m.n_cols, d_rp, d_ci, d_v, d_x, y)
+            torch.cuda.synchronize()
+            outs.append(y.cpu().numpy().astype(np.float64))
     for y in outs:
         assert np.all(np.isfinite(y))
+        assert np.all(np.abs(y - y_ref) <= bound), \
+            f"max |dy|/s = {np.max(np.abs(y - y_ref) / np.maximum(s, 1e-300)):.3e} (oracle)"
         assert np.all(np.abs(y - y_plan) <= bound), \
-            f"max |dy|/s = {np.max(np.abs(y - y_plan) / np.maximum(s, 1e-300)):.3e}"
-    assert np.array_equal(outs[0], outs[1])
+            f"max |dy|/s = {np.max(np.abs(y - y_plan) / np.maximum(s, 1e-300)):.3e} (plan)"
+    for y in outs[1:]:
+        assert np.array_equal(outs[0], y)
 
 
 def test_noalloc_rejects_bad_arguments(spmv_lib):
@@ -95,4 +108,9 @@ def test_noalloc_rejects_bad_arguments(spmv_lib):
     assert st == 1                           # misaligned col_idx
     st = spmv_lib.spmv_csr_run_noalloc(-1, 4, 0, None, None, None, S.SPMV_F32,
                                        None, None, None)
+    assert st == 1
+    # y in host memory: refused on the host, before any launch
+    y_host = np.zeros(4, np.float32)
+    st = spmv_lib.spmv_csr_run_noalloc(4, 4, 0, rp.data_ptr(), None, None, S.SPMV_F32,
+                                       None, y_host.ctypes.data, None)
     assert st == 1
