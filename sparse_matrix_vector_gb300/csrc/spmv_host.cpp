@@ -46,6 +46,7 @@ constexpr size_t kXsAutoBytesDelta = 32 * 1024;
 constexpr size_t kXsMaxBytes = 160 * 1024;   // hard limit when forced
 constexpr int kPadElems = 16;                // zero tail after device arrays
 constexpr int kAssumedSms = 152;             // for host-only inspection
+constexpr size_t kAssumedSmemOptin = 232448; // shared memory a CTA may opt in to (227 KB)
 
 size_t dtype_size(spmv_dtype t) { return t == SPMV_F16 ? 2 : 4; }
 
@@ -371,84 +372,97 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
   return SPMV_OK;
 }
 
-spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out,
-                             spmv_plan_info* info) {
-  out->units.clear();
-  out->warp_base.clear();
-  out->cta_first.clear();
-  out->row_split.clear();
-  out->splits.clear();
-  out->n_chunks = 0;
+spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
+                                DeltaTables* out, spmv_plan_info* info) {
+  *out = DeltaTables();
   const int64_t* rp = d->row_ptr;
   const int32_t bits = delta_bits_of(d);
   const int64_t per_word = 32 / bits;  // entries per word
   const uint32_t cap = (1u << bits) - 1u;
-  const int64_t unit_words = delta_unit_words(bits);
-  const int max_lw = (int)(unit_words / kDeltaThreads);  // words per lane at most
-  // weight of a unit: its entries, plus 8 for the row it starts
-  const int64_t total_w = d->n_entries + 8 * (int64_t)d->n_rows;
-  constexpr int64_t kMinShare = 4096;
-  const int G = (int)std::max<int64_t>(
-      1, std::min<int64_t>(max_ctas, (total_w + kMinShare - 1) / kMinShare));
-  auto boundary = [&](int b) { return (int64_t)((__int128)b * total_w / G); };
-  int64_t cum = 0;
-  int next_b = 1;
+  const int64_t seg_words = delta_seg_words(bits);
+  // weight of a segment: its words plus a fixed cost (header, scans, copy)
+  constexpr int64_t kSegCost = 16;
+  constexpr int64_t kMinShare = 256;  // words a warp should get at least
   try {
-    out->row_split.assign((size_t)d->n_rows, -1);
-    out->cta_first.push_back(0);
+    // 1. cut every row into the fewest segments of at most seg_words words,
+    //    of nearly equal size; record each segment's starting column
+    int64_t total_w = 0;
     for (int32_t r = 0; r < d->n_rows; ++r) {
       const int64_t w0 = rp[r] / per_word, w1 = rp[r + 1] / per_word, nw = w1 - w0;
-      // words per lane: the least that fits the row in one unit, else the most
-      uint32_t lg = 0;
-      while ((1 << lg) < max_lw && nw > (int64_t)kDeltaThreads << lg) ++lg;
-      const int64_t warp_words = (int64_t)32 << lg;
-      const int64_t n_u = std::max<int64_t>(1, (nw + unit_words - 1) / unit_words);
-      const int64_t per = n_u > 1 ? (nw + n_u - 1) / n_u : std::max<int64_t>(nw, 1);
-      if (n_u > 1) {
-        if (out->n_chunks + n_u > kMaxIndex) return SPMV_ERR_TOO_LARGE;
-        out->row_split[r] = (int32_t)out->splits.size();
-        out->splits.push_back({(int32_t)out->n_chunks, (int32_t)n_u, (int32_t)w0, (int32_t)per});
-        out->n_chunks += n_u;
-        info->rows_per_bin[3] += 1;
-      } else {
-        info->rows_per_bin[nw * per_word > 256 ? 2 : (nw * per_word > 8 ? 1 : 0)] += 1;
+      if (nw == 0) {
+        out->empty_rows.push_back(r);
+        info->rows_per_bin[0] += 1;
+        continue;
       }
+      const int64_t n_s = (nw + seg_words - 1) / seg_words;
+      const int64_t per = (nw + n_s - 1) / n_s;
+      const int64_t entries = nw * per_word;
+      info->rows_per_bin[n_s > 1 ? 3 : entries > 256 ? 2 : entries > 8 ? 1 : 0] += 1;
       int64_t col = 0;  // running column of the row, before word w
       int64_t w = w0;
-      for (int64_t k = 0; k < n_u; ++k) {
-        const int64_t ub = std::min(w0 + k * per, w1), ue = std::min(ub + per, w1);
-        while (next_b < G && cum >= boundary(next_b)) {
-          out->cta_first.push_back((int32_t)out->units.size());
-          ++next_b;
+      for (int64_t k = 0; k < n_s; ++k) {
+        const int64_t sb = w0 + k * per, se = std::min(sb + per, w1);
+        for (; w < sb; ++w) {
+          const uint32_t word = d->words[w];
+          for (int q = 0; q < per_word; ++q) col += (word >> (bits * q)) & cap;
         }
-        // starting column of each warp's words of the unit (warp 0's is the
-        // unit's own starting column)
-        for (int wi = 0; wi < kDeltaWarps; ++wi) {
-          const int64_t seg = std::min(ub + (int64_t)wi * warp_words, ue);
-          for (; w < seg; ++w) {
-            const uint32_t word = d->words[w];
-            for (int q = 0; q < per_word; ++q) col += (word >> (bits * q)) & cap;
-          }
-          if (col > INT32_MAX) return SPMV_ERR_TOO_LARGE;
-          out->warp_base.push_back((int32_t)col);
-        }
-        const uint32_t flags = (k == 0 ? kUnitFirst : 0u) | (k == n_u - 1 ? kUnitLast : 0u) |
-                               (lg << kUnitLgShift);
-        out->units.push_back({(int32_t)((uint32_t)r | flags), (int32_t)ub, (int32_t)ue,
-                              out->warp_base[out->warp_base.size() - kDeltaWarps]});
-        cum += (ue - ub) * per_word + (k == 0 ? 8 : 0);
+        if (col > INT32_MAX || se > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+        const uint32_t flags = (k == 0 ? kSegFirst : 0u) | (k == n_s - 1 ? kSegLast : 0u);
+        out->segs.push_back({r, (int32_t)sb, (int32_t)se, (int32_t)col, flags});
+        total_w += (se - sb) + kSegCost;
       }
+      (n_s > 1 ? info->tiles_per_bin[3] : info->tiles_per_bin[2]) += n_s;
     }
-    while ((int)out->cta_first.size() <= G) out->cta_first.push_back((int32_t)out->units.size());
+    const int64_t n_segs = (int64_t)out->segs.size();
+    if (n_segs > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+    // 2. deal the segments to warps as contiguous shares of equal weight
+    const int64_t want = std::max<int64_t>(1, (total_w + kMinShare - 1) / kMinShare);
+    const int G = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)max_warps, want,
+                                                                std::max<int64_t>(n_segs, 1)}));
+    const int grid = (G + warps_per_cta - 1) / warps_per_cta;
+    const int n_warps = grid * warps_per_cta;
+    out->warp_first.assign((size_t)n_warps + 1, (int32_t)n_segs);
+    out->warp_first[0] = 0;
+    {
+      int64_t cum = 0;
+      int g = 1;
+      for (int64_t t = 0; t < n_segs; ++t) {
+        while (g < G && cum >= (int64_t)((__int128)g * total_w / G)) out->warp_first[g++] = (int32_t)t;
+        const DeltaSeg& sg = out->segs[(size_t)t];
+        cum += (int64_t)(sg.word_end - sg.word_begin) + kSegCost;
+      }
+      while (g < G) out->warp_first[g++] = (int32_t)n_segs;
+    }
+    // 3. rows whose segments fall in more than one warp's share: one partial
+    //    per such warp (its piece), combined by the last to arrive
+    out->seg_split.assign((size_t)n_segs, -1);
+    std::vector<int32_t> seg_warp((size_t)n_segs);
+    for (int g = 0; g < n_warps; ++g)
+      for (int32_t t = out->warp_first[g]; t < out->warp_first[g + 1]; ++t) seg_warp[t] = g;
+    out->seg_piece.assign((size_t)n_segs, 0);
+    for (int64_t t = 0; t < n_segs;) {
+      int64_t e = t + 1;
+      while (e < n_segs && out->segs[(size_t)e].row == out->segs[(size_t)t].row) ++e;
+      if (seg_warp[t] != seg_warp[e - 1]) {
+        int32_t pieces = 0;
+        for (int64_t u = t; u < e; ++u) {
+          if (u > t && seg_warp[u] != seg_warp[u - 1]) ++pieces;
+          out->seg_piece[(size_t)u] = pieces;
+          out->seg_split[(size_t)u] = (int32_t)out->splits.size();
+        }
+        ++pieces;
+        if (out->n_chunks + pieces > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+        out->splits.push_back({(int32_t)out->n_chunks, pieces, 0, 0});
+        out->n_chunks += pieces;
+      }
+      t = e;
+    }
+    info->n_tiles = n_segs;
+    info->n_split_rows = (int64_t)out->splits.size();
+    info->grid = grid;
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
   }
-  if ((int64_t)out->units.size() > kMaxIndex) return SPMV_ERR_TOO_LARGE;
-  info->n_tiles = (int64_t)out->units.size();
-  info->n_split_rows = (int64_t)out->splits.size();
-  info->tiles_per_bin[2] = info->n_tiles - out->n_chunks;
-  info->tiles_per_bin[3] = out->n_chunks;
-  info->grid = G;
   return SPMV_OK;
 }
 
@@ -505,7 +519,8 @@ void free_plan(spmv_plan* plan) {
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
-                    p->row_split, p->perm, p->diag, p->pcg_work};
+                    p->row_split, p->perm, p->diag, p->pcg_work,
+                    p->seg_off, p->empty_rows};
     for (void* b : bufs)
       if (b) cudaFree(b);
   }
@@ -877,93 +892,127 @@ spmv_status resolve_format(const spmv_csr* m, const Options& o, spmv_format* for
   return SPMV_OK;
 }
 
-// Device layout of a DELTA plan: one block per work unit, each block the
-// unit's kDeltaWarps starting columns (32 bytes), its words (padded to a
-// multiple of 4) and its values (padded to a multiple of 16 bytes), so that
-// one bulk copy stages a whole unit. Unit descriptors' last field becomes the
-// block's offset in 16-byte steps.
-spmv_status build_delta_blocks(const spmv_delta* d, DeltaTables* t, std::vector<uint4>* out) {
+// Device layout of a DELTA plan: one block per segment, back to back in
+// segment order (so each warp's share is contiguous), each block a 32-byte
+// header (DeltaSegHeader), the segment's words (padded to 16 bytes) and their
+// values (padded to 16 bytes; at 2 bits each word's 32 bytes of values are
+// split into two planes of 16-byte halves). One bulk copy stages a block.
+// seg_off receives every block's offset in 16-byte steps (n_segs + 1).
+spmv_status build_delta_blocks(const spmv_delta* d, const DeltaTables& t, int stages,
+                               std::vector<uint4>* out, std::vector<int32_t>* seg_off) {
   const int32_t bits = delta_bits_of(d);
   const int64_t per = delta_per_word(bits);
-  int64_t total = 0;  // in 16-byte steps
-  for (const Tile& u : t->units) total += delta_block_bytes(bits, (int64_t)u.c - u.b) / 16;
-  if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+  const size_t n_segs = t.segs.size();
   try {
+    seg_off->assign(n_segs + 1, 0);
+    int64_t total = 0;  // in 16-byte steps
+    for (size_t k = 0; k < n_segs; ++k) {
+      (*seg_off)[k] = (int32_t)total;
+      total += delta_seg_bytes(bits, (int64_t)t.segs[k].word_end - t.segs[k].word_begin) / 16;
+      if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+    }
+    (*seg_off)[n_segs] = (int32_t)total;
     out->assign((size_t)total, make_uint4(0, 0, 0, 0));
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
   }
+  std::vector<int32_t> next((size_t)n_segs, -1);  // segment staged `stages` later by the same warp
+  for (size_t g = 0; g + 1 < t.warp_first.size(); ++g)
+    for (int32_t k = t.warp_first[g]; k + stages < t.warp_first[g + 1]; ++k) next[k] = k + stages;
   unsigned char* base = reinterpret_cast<unsigned char*>(out->data());
-  int64_t at = 0;
-  for (size_t k = 0; k < t->units.size(); ++k) {
-    Tile& u = t->units[k];
-    const int64_t wb = u.b, nw = (int64_t)u.c - u.b;
-    unsigned char* b = base + at * 16;
-    std::memcpy(b, t->warp_base.data() + k * kDeltaWarps, kDeltaWarps * 4);
-    if (nw > 0) {
-      std::memcpy(b + kDeltaWarps * 4, d->words + wb, (size_t)nw * 4);
-      std::memcpy(b + kDeltaWarps * 4 + ((nw + 3) & ~3) * 4, d->values + wb * per,
-                  (size_t)(nw * per) * 2);
+  for (size_t k = 0; k < n_segs; ++k) {
+    const DeltaSeg& sg = t.segs[k];
+    const int64_t wb = sg.word_begin, nw = (int64_t)sg.word_end - sg.word_begin;
+    unsigned char* b = base + (size_t)(*seg_off)[k] * 16;
+    DeltaSegHeader h{};
+    h.base = sg.base;
+    h.row_flags = (uint32_t)sg.row | sg.flags;
+    h.n_words = (int32_t)nw;
+    h.split = t.seg_split[k];
+    h.piece = t.seg_piece[k];
+    if (next[k] >= 0) {
+      h.next_off = (*seg_off)[next[k]];
+      h.next_bytes = ((*seg_off)[next[k] + 1] - (*seg_off)[next[k]]) * 16;
     }
-    u.d = (int32_t)at;
-    at += delta_block_bytes(bits, nw) / 16;
+    std::memcpy(b, &h, sizeof(h));
+    unsigned char* words = b + kDeltaHeaderBytes;
+    unsigned char* vals = words + delta_pad16(nw * 4);
+    std::memcpy(words, d->words + wb, (size_t)nw * 4);
+    const uint16_t* src = d->values + wb * per;
+    if (bits == 2) {  // two planes: halves 0..7 of each word, then 8..15
+      for (int64_t j = 0; j < nw; ++j) {
+        std::memcpy(vals + 16 * j, src + 16 * j, 16);
+        std::memcpy(vals + 16 * (nw + j), src + 16 * j + 8, 16);
+      }
+    } else {
+      std::memcpy(vals, src, (size_t)(nw * per) * 2);
+    }
   }
   return SPMV_OK;
+}
+
+// x in shared memory: by default when it is at most kXsAutoBytesDelta, and
+// when forced as long as the warps' rings and x fit the CTA's shared memory.
+bool delta_x_fits(int bits, int n_cols, int forced, size_t smem_optin) {
+  const size_t xb = delta_x_smem_bytes(n_cols);
+  const size_t reserve = 4096;  // static shared memory and the runtime's share
+  const bool fits = delta_rings_bytes(bits) + xb + reserve <= smem_optin;
+  return forced == 1 ? fits : forced == -1 ? (fits && xb <= kXsAutoBytesDelta) : false;
 }
 
 spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   spmv_status s;
   spmv_plan_info& info = p->info;
-  if (d->n_rows > (int32_t)kUnitRowMask) return SPMV_ERR_TOO_LARGE;
+  if ((uint32_t)d->n_rows > kSegRowMask) return SPMV_ERR_TOO_LARGE;
   // the kernel is chosen by the width the matrix was encoded with; the
   // plan's format code must name the same width
   p->delta_bits = delta_bits_of(d);
   if (p->format != delta_format(p->delta_bits)) return SPMV_ERR_INVALID_ARG;
   if ((s = bind_device(p)) != SPMV_OK) return s;
-  const size_t xbytes = (size_t)d->n_cols * 2;
-  p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
-            : o.x_smem == -1 ? xbytes <= kXsAutoBytesDelta : false;
-  p->dyn_smem = (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0) +
-                delta_stages_bytes(p->delta_bits, p->x_smem);
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) !=
+      cudaSuccess)
+    return SPMV_ERR_CUDA;
+  p->x_smem = delta_x_fits(p->delta_bits, d->n_cols, o.x_smem, (size_t)optin);
+  p->dyn_smem = delta_rings_bytes(p->delta_bits) +
+                (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0);
   if (delta_set_smem_limit(p->delta_bits, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  // as for CSR: within the shared-memory budget that leaves L1 its share
-  const int occ = delta_kernel_occupancy(p->delta_bits, p->x_smem, p->dyn_smem, kSmemBudget);
+  const int occ = delta_kernel_occupancy(p->delta_bits, p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
-  // a CTA may run several blocks of units (groups); the plan deals units to
-  // groups, the grid has one CTA per `groups` of them
-  const int groups = delta_groups(p->x_smem);
+  const int wpc = delta_warps_per_cta(p->delta_bits);
   DeltaTables t;
-  if ((s = plan_delta_units(d, occ * p->sm_count * groups, &t, &info)) != SPMV_OK) return s;
-  p->grid = (info.grid + groups - 1) / groups;
-  while ((int64_t)t.cta_first.size() < (int64_t)p->grid * groups + 1)
-    t.cta_first.push_back((int32_t)t.units.size());
-  info.grid = p->grid;
-  p->n_tiles = (int64_t)t.units.size();
+  if ((s = plan_delta_segments(d, occ * p->sm_count * wpc, wpc, &t, &info)) != SPMV_OK)
+    return s;
+  p->grid = info.grid;
+  p->n_tiles = (int64_t)t.segs.size();
   std::vector<uint4> blocks;
-  if ((s = build_delta_blocks(d, &t, &blocks)) != SPMV_OK) return s;
+  std::vector<int32_t> seg_off;
+  if ((s = build_delta_blocks(d, t, delta_stages(p->delta_bits), &blocks, &seg_off)) != SPMV_OK)
+    return s;
   if ((s = dev_upload(&p->blocks, blocks.data(), blocks.size() * 16,
                       blocks.size() * 16)) != SPMV_OK) return s;
-  if ((s = dev_upload(&p->tiles, t.units.data(), t.units.size() * sizeof(Tile),
-                      t.units.size() * sizeof(Tile))) != SPMV_OK) return s;
-  if ((s = dev_upload(&p->cta_first, t.cta_first.data(), t.cta_first.size() * 4,
-                      t.cta_first.size() * 4)) != SPMV_OK) return s;
-  if ((s = dev_upload(&p->row_split, t.row_split.data(), t.row_split.size() * 4,
-                      t.row_split.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->seg_off, seg_off.data(), seg_off.size() * 4,
+                      seg_off.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->cta_first, t.warp_first.data(), t.warp_first.size() * 4,
+                      t.warp_first.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->empty_rows, t.empty_rows.data(), t.empty_rows.size() * 4,
+                      t.empty_rows.size() * 4)) != SPMV_OK) return s;
+  p->n_empty_rows = (int32_t)t.empty_rows.size();
   if ((s = dev_upload(&p->splits, t.splits.data(), t.splits.size() * sizeof(SplitInfo),
                       t.splits.size() * sizeof(SplitInfo))) != SPMV_OK) return s;
   if ((s = dev_upload(&p->partials, nullptr, 0, (size_t)t.n_chunks * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
-  info.block = delta_block(p->x_smem);
+  info.block = wpc * 32;
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = delta_matrix_bytes(*d);
-  // the unit blocks hold the matrix's values and deltas, the warps' starting
-  // columns and the 16-byte alignment padding; the rest of them is auxiliary
+  // the blocks hold the matrix's values and deltas, the segment headers and
+  // the 16-byte alignment padding; the rest of them is auxiliary
   info.aux_bytes = (int64_t)(blocks.size() * 16) -
                    (info.matrix_bytes - ((int64_t)d->n_rows + 1) * 4) +
-                   (int64_t)(t.units.size() * sizeof(Tile) + t.cta_first.size() * 4 +
-                             t.row_split.size() * 4 + t.splits.size() * (sizeof(SplitInfo) + 4) +
+                   (int64_t)(seg_off.size() * 4 + t.warp_first.size() * 4 +
+                             t.empty_rows.size() * 4 + t.splits.size() * (sizeof(SplitInfo) + 4) +
                              (size_t)t.n_chunks * 4);
   fill_bytes(&info, 2);
   return SPMV_OK;
@@ -1159,7 +1208,7 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
   info->nnz = m->nnz;
   info->format = format;
   info->value_dtype = m->value_dtype;
-  info->block = delta ? kDeltaThreads : kThreads;
+  info->block = kThreads;
   if (format == SPMV_FORMAT_SELL) {
     spmv_sell sl;
     if ((s = spmv_convert_sell(m, sigma, &sl)) != SPMV_OK) return s;
@@ -1175,13 +1224,12 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
       spmv_delta_free(&d);
       return SPMV_ERR_TOO_LARGE;
     }
-    const bool xs = o.x_smem != 0 && (size_t)m->n_cols * 2 <=
-                    (o.x_smem == 1 ? kXsMaxBytes : kXsAutoBytesDelta);
-    const int groups = delta_groups(xs);
+    const bool xs = delta_x_fits(format_delta_bits(format), m->n_cols, o.x_smem,
+                                 kAssumedSmemOptin);
+    const int wpc = delta_warps_per_cta(format_delta_bits(format));
     DeltaTables t;
-    s = plan_delta_units(&d, (xs ? 2 : 5) * kAssumedSms * groups, &t, info);
-    info->grid = (info->grid + groups - 1) / groups;
-    info->block = delta_block(xs);
+    s = plan_delta_segments(&d, kAssumedSms * wpc, wpc, &t, info);
+    info->block = wpc * 32;
     info->n_entries = d.n_entries;
     info->x_in_smem = xs ? 1 : 0;
     info->launches_per_run = m->n_rows > 0;

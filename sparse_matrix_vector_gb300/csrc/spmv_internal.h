@@ -37,11 +37,6 @@ constexpr int tile_cap(spmv_dtype t) { return t == SPMV_F16 ? kTileCapF16 : kTil
 constexpr int kStreamTileCap = (kTileCap < kThreads * 8 ? kTileCap : kThreads * 8) - 16;
 constexpr int kTileRowsCap = 512;        // rows of a short-row tile
 constexpr int kStages = SPMV_STAGES;
-// DELTA kernel: a work unit is a slice of one row of at most
-// delta_unit_words(b) packed words (32 / b entries each for deltas of b
-// bits), decoded by kDeltaThreads threads, LW = 1 or 2 words per thread (the
-// fewest that fit the row in one unit), so warp w decodes the unit's words
-// [32 LW w, 32 LW (w + 1)). Units hold at most 4096 entries (2048 at b = 8).
 constexpr int kSellSlicesPerCta = 8;  // SELL: one warp per slice
 constexpr int kFemThreads = 128;      // matrix-free FEM: one thread per node
 constexpr int kPcgThreads = 256;      // conjugate gradients: vector kernels
@@ -53,26 +48,45 @@ struct PcgScalars {
   double rz, rr, bb, alpha, beta, tol2;
   int iter, max_iter, done, arrived;
 };
-constexpr int kDeltaThreads = 256;
-constexpr int kDeltaWarps = kDeltaThreads / 32;
-constexpr int kDeltaUnitWords = 512;  // the most, over the widths
-constexpr int delta_unit_words(int bits) { return bits == 2 ? 256 : 512; }
-constexpr int kDeltaMaxLaneWords = kDeltaUnitWords / kDeltaThreads;
-// Bytes of a unit's device block (n_w words of b-bit deltas): the warps'
-// starting columns, the words padded to a multiple of 4 and the values padded
-// to a multiple of 16 bytes.
-constexpr int64_t delta_block_bytes(int bits, int64_t n_w) {
-  return kDeltaWarps * 4 + ((n_w + 3) & ~(int64_t)3) * 4 +
-         ((n_w * (32 / bits) * 2 + 15) & ~(int64_t)15);
+// DELTA kernel ("MACKO-SpMV" 2.2): rows are cut into segments of at most
+// delta_seg_words(b) packed words; every warp of the grid owns a contiguous
+// share of the segments and stages them through its own ring of shared-memory
+// buffers, one bulk copy per segment. Lane l decodes words l, l + 32, ... of a
+// segment (delta_lane_words(b) of them at most).
+constexpr int delta_lane_words(int bits) { return bits == 2 ? 2 : 4; }
+constexpr int delta_seg_words(int bits) { return 32 * delta_lane_words(bits); }
+constexpr int kDeltaHeaderBytes = 32;
+constexpr int64_t delta_pad16(int64_t b) { return (b + 15) & ~(int64_t)15; }
+// Bytes of the device block of a segment of n_w words of b-bit deltas: the
+// header, the words (padded to 16 bytes) and their values (32 / b halves a
+// word, padded to 16 bytes).
+constexpr int64_t delta_seg_bytes(int bits, int64_t n_w) {
+  return kDeltaHeaderBytes + delta_pad16(n_w * 4) + delta_pad16(n_w * (64 / bits));
 }
-// DELTA unit descriptor: {row | FIRST | LAST | log2(LW) << kUnitLgShift,
-// word_begin, word_end, offset of the unit's device block in 16-byte steps
-// (the planner leaves the column before the unit's first entry there, and
-// the block builder replaces it)}; FIRST / LAST: first / last unit of the row.
-constexpr uint32_t kUnitFirst = 1u << 31;
-constexpr uint32_t kUnitLast = 1u << 30;
-constexpr uint32_t kUnitLgShift = 28;
-constexpr uint32_t kUnitRowMask = (1u << 28) - 1u;
+// Segment header, the first 32 bytes of its block:
+//   base       column before the segment's first entry
+//   row_flags  row | kSegFirst (first segment of the row) | kSegLast (last)
+//   n_words    packed words in the segment
+//   split      index into the split table when the row's segments are shared
+//              by several warps, else -1
+//   next_off   the block that this warp stages S segments later: offset in
+//   next_bytes 16-byte steps and size in bytes (0 when there is none)
+//   piece      for a split row: which of the row's partial sums this warp's
+//              share produces
+struct DeltaSegHeader {
+  int32_t base;
+  uint32_t row_flags;
+  int32_t n_words;
+  int32_t split;
+  int32_t next_off;
+  int32_t next_bytes;
+  int32_t piece;
+  int32_t reserved;
+};
+static_assert(sizeof(DeltaSegHeader) == kDeltaHeaderBytes, "segment header is 32 bytes");
+constexpr uint32_t kSegFirst = 1u << 31;
+constexpr uint32_t kSegLast = 1u << 30;
+constexpr uint32_t kSegRowMask = (1u << 30) - 1u;
 
 // Tile descriptor (one int4 per work unit of the CSR kernel).
 //   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | WALK? | lg << 16 | rows}
@@ -98,8 +112,8 @@ struct Tile {
 // A row whose sum is assembled from partial sums.
 //   CSR:    {first slot, chunks, row_ptr[row] (chunk k starts at row_begin +
 //            k * per_chunk), nonzeros per chunk}
-//   DELTA4: {first slot, units, the row's first word (unit k starts at
-//            row_begin + k * per_unit), words per unit}
+//   DELTA:  {first slot, pieces (warps whose shares hold part of the row),
+//            0, 0}; a segment's header names its warp's piece
 struct SplitInfo {
   int32_t first_slot;  // index of the first partial sum in the scratch array
   int32_t n_chunks;    // partial sums to wait for
@@ -137,19 +151,29 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* row_ptr,
                            const Options& opt, int max_ctas, CsrTables* out,
                            spmv_plan_info* info);
 
-// Host-side result of planning a DELTA4 matrix.
-struct DeltaTables {
-  std::vector<Tile> units;
-  std::vector<int32_t> warp_base;  // per unit, kWarps columns: the column before
-                                   // the first entry of each warp's words
-  std::vector<int32_t> cta_first;  // CTA b runs units [cta_first[b], cta_first[b+1])
-  std::vector<int32_t> row_split;  // per row: index into splits, or -1
-  std::vector<SplitInfo> splits;   // {first_slot, n_units, row's first word, words per unit}
-  int64_t n_chunks = 0;
+// One segment of a DELTA plan, as the planner cuts it.
+struct DeltaSeg {
+  int32_t row;
+  int32_t word_begin, word_end;  // into the format's words
+  int32_t base;                  // column before the first entry
+  uint32_t flags;                // kSegFirst / kSegLast
 };
 
-spmv_status plan_delta_units(const spmv_delta* d, int max_ctas, DeltaTables* out,
-                             spmv_plan_info* info);
+// Host-side result of planning a DELTA matrix.
+struct DeltaTables {
+  std::vector<DeltaSeg> segs;
+  std::vector<int32_t> warp_first;  // warp g runs segments [warp_first[g], warp_first[g+1])
+  std::vector<int32_t> seg_split;   // per segment: index into splits, or -1
+  std::vector<int32_t> seg_piece;   // per segment of a split row: its warp's piece
+  std::vector<SplitInfo> splits;    // {first_slot, pieces, 0, 0}
+  std::vector<int32_t> empty_rows;  // rows without stored entries (y = 0)
+  int64_t n_chunks = 0;             // partial-sum slots over all split rows
+};
+
+// Cut the rows into segments and deal them to at most `max_warps` warps as
+// contiguous shares of equal weight (words + a per-segment cost).
+spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
+                                DeltaTables* out, spmv_plan_info* info);
 
 // Device resources of a plan.
 struct Plan {
@@ -172,12 +196,15 @@ struct Plan {
   int32_t* row_ptr = nullptr;   // CSR offsets, DELTA entry offsets, SELL slot offsets
   int32_t* col_idx = nullptr;   // CSR and SELL columns
   void* values = nullptr;       // fp32 / fp16 (CSR, SELL)
-  unsigned char* blocks = nullptr;  // DELTA: one block per work unit
+  unsigned char* blocks = nullptr;  // DELTA: one block per segment
+  int32_t* seg_off = nullptr;       // DELTA: block offsets (16-byte steps), n_segs + 1
+  int32_t* empty_rows = nullptr;    // DELTA: rows without stored entries
+  int32_t n_empty_rows = 0;
   // planner tables and scratch (device)
   Tile* tiles = nullptr;
   SplitInfo* splits = nullptr;
-  int32_t* cta_first = nullptr;
-  int32_t* row_split = nullptr;  // DELTA: split id per row or -1
+  int32_t* cta_first = nullptr;   // CSR: first tile per CTA; DELTA: first segment per warp
+  int32_t* row_split = nullptr;
   int32_t* perm = nullptr;       // SELL: original row per slice lane (null: in order)
   // matrix-free FEM: elements per axis and the element matrix (the device
   // holds the densities in `values`)
@@ -208,12 +235,12 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, bool il, size_t dyn_smem
                          size_t budget);
 size_t csr_stage_bytes(spmv_dtype dtype);
 int csr_set_smem_limit(size_t dyn);
-int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem, size_t budget);
-size_t delta_stages_bytes(int bits, bool x_smem);  // every stage of every group
-int delta_groups(bool x_smem);           // unit blocks ("virtual CTAs") per CTA
-int delta_block(bool x_smem);            // threads per CTA
+int delta_warps_per_cta(int bits);      // warps of a DELTA CTA (each with its own ring)
+int delta_stages(int bits);              // ring depth per warp
+size_t delta_rings_bytes(int bits);      // every stage of every warp of a CTA
 size_t delta_x_smem_bytes(int n_cols);
 int delta_set_smem_limit(int bits, size_t dyn);
+int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 int launch_sell(const Plan& p, const void* x, float* y, void* stream);

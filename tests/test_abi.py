@@ -487,16 +487,20 @@ def test_pcg_argument_errors(spmv_lib):
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_delta_planner_unit_counts(spmv_lib, bits):
-    """Every row becomes ceil(words / unit words) units (one for an empty
-    row); unit words are 256 at 2 bits and 512 otherwise; rows of more than
-    one unit are the split rows."""
+    """Every row becomes ceil(words / segment words) segments (none for an
+    empty row); segments hold at most 64 words at 2 bits and 128 otherwise;
+    only rows of more than one segment can be shared by several warps."""
     lengths = np.array([0, 1, 7, 300, 2000, 5000, 12000, 0, 4096, 4097, 8193])
     m = workloads.from_lengths("units", lengths, 20000, seed=5, dtype=np.float16)
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols, format=f"delta{bits}")
     enc = oracle.delta_encode(m.n_cols, m.row_ptr, m.col_idx, m.values, bits=bits)
     words = np.diff(enc.row_ptr) * bits // 32
-    unit_words = 256 if bits == 2 else 512
-    units = np.maximum(1, -(-words // unit_words))
-    assert info["n_tiles"] == units.sum()
-    assert info["n_split_rows"] == (units > 1).sum()
+    seg_words = 64 if bits == 2 else 128
+    segs = -(-words // seg_words)
+    assert info["n_tiles"] == segs.sum()
+    assert info["tiles_per_bin"][2] == (segs == 1).sum()
+    assert info["tiles_per_bin"][3] == segs[segs > 1].sum()
+    assert info["rows_per_bin"][3] == (segs > 1).sum()
+    assert 0 <= info["n_split_rows"] <= (segs > 1).sum()
+    assert info["block"] % 32 == 0
     assert info["n_entries"] == enc.n_entries
