@@ -36,13 +36,23 @@ namespace spmv {
 namespace {
 
 #ifndef SPMV_DELTA_WARPS
-#define SPMV_DELTA_WARPS 24
+#define SPMV_DELTA_WARPS 28
 #endif
 #ifndef SPMV_DELTA_STAGES
-#define SPMV_DELTA_STAGES 3
+#define SPMV_DELTA_STAGES 2
+#endif
+#ifndef SPMV_DELTA_GRID_PER_SM
+#define SPMV_DELTA_GRID_PER_SM 1
+#endif
+#ifndef SPMV_DELTA_MIN_BLOCKS
+#define SPMV_DELTA_MIN_BLOCKS 1
 #endif
 // Warps per CTA; each has a ring of kStages segment buffers. One CTA per SM:
-// the rings and x fill its shared memory.
+// the rings and x fill its shared memory. Measured on the 12288^2 LLM
+// matrices (fraction of HBM peak at 30 / 50 / 70 / 90% sparsity): 28 warps x
+// 2 stages 0.70 / 0.65 / 0.57 / 0.41; 24 x 3 0.68 / 0.62 / 0.53 / 0.38;
+// 16 x 4 0.67 / 0.62 / 0.54 / 0.39; two CTAs of 14 x 2 per SM, or one CTA of
+// 14 x 2 leaving room for the next launch's CTA, no better.
 constexpr int kDW = SPMV_DELTA_WARPS;
 constexpr int kDS = SPMV_DELTA_STAGES;
 
@@ -195,6 +205,17 @@ __device__ __forceinline__ WordVals<B> load_vals(const unsigned char* vals, int 
   return r;
 }
 
+// The two entries held in one 32-bit word of values (halves lo, hi), with
+// their gathered x (bits): acc_lo += lo * x_lo, acc_hi += hi * x_hi, each one
+// mixed-precision fma (exact product, one fp32 rounding). Measured against
+// converting both operands and an fp32 fma, and against a half2 product
+// widened and added: the same time, 19% more instructions for either.
+__device__ __forceinline__ void fma_pair(float& acc_lo, float& acc_hi, uint32_t v, uint16_t x_lo,
+                                         uint16_t x_hi) {
+  acc_lo = fma_half<0>(acc_lo, v, x_lo);
+  acc_hi = fma_half<1>(acc_hi, v, x_hi);
+}
+
 // Accumulate one word whose first entry follows column `col` (p: x at col).
 // Four accumulators, entry e of the word into acc[e % 4].
 template <int B, bool XS>
@@ -207,14 +228,12 @@ __device__ __forceinline__ void decode_word(uint32_t w, const WordPrefix<B>& pf,
     for (int j = 0; j < 4; ++j) {
       const uint32_t o0 = __byte_perm(pf.Q2, 0u, 0x4440u + (uint32_t)j);
       const uint32_t o1 = __byte_perm(pf.P2, 0u, 0x4440u + (uint32_t)j);
-      acc[(2 * j) & 3] = fma_half<0>(acc[(2 * j) & 3], vw[j], gather<XS>(p, o0));
-      acc[(2 * j + 1) & 3] = fma_half<1>(acc[(2 * j + 1) & 3], vw[j], gather<XS>(p, o1));
+      fma_pair(acc[(2 * j) & 3], acc[(2 * j + 1) & 3], vw[j], gather<XS>(p, o0),
+               gather<XS>(p, o1));
     }
   } else if constexpr (B == 8) {
-    acc[0] = fma_half<0>(acc[0], v.v.x, gather<XS>(p, pf.Q2 & 0xFFFFu));
-    acc[1] = fma_half<1>(acc[1], v.v.x, gather<XS>(p, pf.P2 & 0xFFFFu));
-    acc[2] = fma_half<0>(acc[2], v.v.y, gather<XS>(p, pf.Q2 >> 16));
-    acc[3] = fma_half<1>(acc[3], v.v.y, gather<XS>(p, pf.P2 >> 16));
+    fma_pair(acc[0], acc[1], v.v.x, gather<XS>(p, pf.Q2 & 0xFFFFu), gather<XS>(p, pf.P2 & 0xFFFFu));
+    fma_pair(acc[2], acc[3], v.v.y, gather<XS>(p, pf.Q2 >> 16), gather<XS>(p, pf.P2 >> 16));
   } else {
     const uint32_t vw[8] = {v.v0.x, v.v0.y, v.v0.z, v.v0.w, v.v1.x, v.v1.y, v.v1.z, v.v1.w};
 #pragma unroll
@@ -223,10 +242,8 @@ __device__ __forceinline__ void decode_word(uint32_t w, const WordPrefix<B>& pf,
       const uint32_t o3 = __byte_perm(pf.P2, 0u, 0x4440u + (uint32_t)i);
       const uint32_t o0 = o1 - ((w >> (8 * i + 1)) & 6u);   // 2 x field 4i+1
       const uint32_t o2 = o3 - ((w >> (8 * i + 5)) & 6u);   // 2 x field 4i+3
-      acc[0] = fma_half<0>(acc[0], vw[2 * i], gather<XS>(p, o0));
-      acc[1] = fma_half<1>(acc[1], vw[2 * i], gather<XS>(p, o1));
-      acc[2] = fma_half<0>(acc[2], vw[2 * i + 1], gather<XS>(p, o2));
-      acc[3] = fma_half<1>(acc[3], vw[2 * i + 1], gather<XS>(p, o3));
+      fma_pair(acc[0], acc[1], vw[2 * i], gather<XS>(p, o0), gather<XS>(p, o1));
+      fma_pair(acc[2], acc[3], vw[2 * i + 1], gather<XS>(p, o2), gather<XS>(p, o3));
     }
   }
 }
@@ -239,27 +256,84 @@ __device__ __forceinline__ void issue_block(unsigned char* buf, uint64_t* bar,
   bulk_g2s(buf, src, bytes, bar, pol);
 }
 
-// Lane 0, at the end of this warp's piece of a row shared by several warps:
-// park the piece's sum; the warp that completes the row's count adds the
-// pieces in warp order, writes y and re-arms the count.
-__device__ __forceinline__ void publish_piece(const DeltaArgs& a, int row, int sid, int piece,
-                                              float part) {
-  const SplitInfo si = a.splits[sid];
-  a.partials[si.first_slot + piece] = part;
+// Lane 0, after its share: the pieces this warp parked for rows shared with
+// other warps are made visible (one fence for all), then each is counted;
+// the warp that completes a row's count adds its pieces in warp order, writes
+// y and re-arms the count.
+__device__ __forceinline__ void finish_pieces(const DeltaArgs& a, const int2 (&pend)[2],
+                                              int n_pend) {
   __threadfence();
-  if (atomicAdd(a.counters + sid, 1) == si.n_chunks - 1) {
-    __threadfence();
-    float sum = 0.f;
-    for (int j = 0; j < si.n_chunks; ++j) sum += __ldcg(a.partials + si.first_slot + j);
-    a.y[row] = sum;
-    a.counters[sid] = 0;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (p >= n_pend) break;
+    const int row = pend[p].x, sid = pend[p].y;
+    const SplitInfo si = a.splits[sid];
+    if (atomicAdd(a.counters + sid, 1) == si.n_chunks - 1) {
+      __threadfence();
+      float sum = 0.f;
+      for (int j = 0; j < si.n_chunks; ++j) sum += __ldcg(a.partials + si.first_slot + j);
+      a.y[row] = sum;
+      a.counters[sid] = 0;
+    }
+  }
+}
+
+// Lane l takes words l, l + 32, ... of the segment (LW of them). The column before word 32 k + l is the segment's base plus
+// the field sums of rows 0..k-1 and the exclusive prefix of row k; the field
+// sums of two rows share one 5-step scan.
+template <int B, bool XS>
+__device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, int n_w, int base,
+                                                     int lane, uint32_t xs_addr,
+                                                     const __half* x, float (&acc)[4]) {
+  constexpr int LW = Seg<B>::kLaneWords;
+  const uint32_t* s_words = reinterpret_cast<const uint32_t*>(st + kDeltaHeaderBytes);
+  const unsigned char* s_vals = st + kDeltaHeaderBytes + ((n_w * 4 + 15) & ~15);
+  const bool full = n_w == Seg<B>::kWords;  // the common case: no lane idles
+  uint32_t w[LW];
+  WordPrefix<B> pf[LW];
+#pragma unroll
+  for (int k = 0; k < LW; ++k) {
+    const int j = 32 * k + lane;
+    w[k] = (full || j < n_w) ? s_words[j] : 0u;
+    pf[k] = word_prefix<B>(w[k]);
+  }
+  int incl[LW / 2];
+#pragma unroll
+  for (int q = 0; q < LW / 2; ++q) incl[q] = pf[2 * q].S | (pf[2 * q + 1].S << 16);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int q = 0; q < LW / 2; ++q) {
+      const int up = __shfl_up_sync(0xffffffffu, incl[q], o);
+      if (lane >= o) incl[q] += up;
+    }
+  }
+  XPtr<XS> xp[LW];
+  int col = base;
+#pragma unroll
+  for (int q = 0; q < LW / 2; ++q) {
+    const int tot = __shfl_sync(0xffffffffu, incl[q], 31);
+    xp[2 * q] = xptr<XS>(xs_addr, x, col + (incl[q] & 0xFFFF) - pf[2 * q].S);
+    col += tot & 0xFFFF;
+    xp[2 * q + 1] = xptr<XS>(xs_addr, x, col + (incl[q] >> 16) - pf[2 * q + 1].S);
+    col += tot >> 16;
+  }
+  if (full) {  // one straight-line block: the gathers of all words can overlap
+#pragma unroll
+    for (int k = 0; k < LW; ++k)
+      decode_word<B, XS>(w[k], pf[k], load_vals<B>(s_vals, 32 * k + lane, n_w), xp[k], acc);
+  } else {
+#pragma unroll
+    for (int k = 0; k < LW; ++k)
+      if (32 * k + lane < n_w)
+        decode_word<B, XS>(w[k], pf[k], load_vals<B>(s_vals, 32 * k + lane, n_w), xp[k], acc);
   }
 }
 
 template <int B, bool XS>
-__global__ void __launch_bounds__(kDW * 32, 1) delta_seg_kernel(const DeltaArgs a) {
+__global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
+    delta_seg_kernel(const DeltaArgs a) {
   using Sg = Seg<B>;
-  constexpr int LW = Sg::kLaneWords;
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_full[kDW][kDS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -270,17 +344,19 @@ __global__ void __launch_bounds__(kDW * 32, 1) delta_seg_kernel(const DeltaArgs 
   const int n = __ldg(a.warp_first + gw + 1) - t0;
   const uint64_t pol = policy_evict_first();
 
-  // plan-owned data only until pdl_wait: the first kDS blocks of the share
+  // plan-owned data only until pdl_wait: the first kDS blocks of the share.
+  // Lane s issues every copy into buffer s (copies issued by one thread
+  // complete roughly one after another).
   if (lane == 0) {
     for (int s = 0; s < kDS; ++s) mbar_init(&s_full[warp][s], 1);
     fence_mbar_init();
-    for (int i = 0; i < kDS && i < n; ++i) {
-      const int o0 = __ldg(a.seg_off + t0 + i), o1 = __ldg(a.seg_off + t0 + i + 1);
-      issue_block(ring + i * Sg::kBytes, &s_full[warp][i], a.blocks + (size_t)o0 * 16,
-                  (uint32_t)(o1 - o0) * 16u, pol);
-    }
   }
   __syncwarp();
+  if (lane < kDS && lane < n) {
+    const int o0 = __ldg(a.seg_off + t0 + lane), o1 = __ldg(a.seg_off + t0 + lane + 1);
+    issue_block(ring + lane * Sg::kBytes, &s_full[warp][lane], a.blocks + (size_t)o0 * 16,
+                (uint32_t)(o1 - o0) * 16u, pol);
+  }
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();
   if (XS) copy_x_half(xs, a.x, a.n_cols);
@@ -290,6 +366,10 @@ __global__ void __launch_bounds__(kDW * 32, 1) delta_seg_kernel(const DeltaArgs 
   const uint32_t xs_addr = smem_u32(xs);
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // pieces of rows shared with other warps (lane 0): {row, split id}; a share
+  // holds at most two, its first row's and its last row's
+  int2 pend[2];
+  int n_pend = 0;
   int s = 0;
   uint32_t phase = 0;
   int i = 0;
@@ -301,51 +381,12 @@ __global__ void __launch_bounds__(kDW * 32, 1) delta_seg_kernel(const DeltaArgs 
     }
     const unsigned char* st = ring + s * Sg::kBytes;
     const int4 h0 = *reinterpret_cast<const int4*>(st);       // base, row | flags, words, split
-    const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; piece
+    const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; slot
     const int n_w = h0.z;
-    const uint32_t* s_words = reinterpret_cast<const uint32_t*>(st + kDeltaHeaderBytes);
-    const unsigned char* s_vals = st + kDeltaHeaderBytes + ((n_w * 4 + 15) & ~15);
-
-    uint32_t w[LW];
-    WordPrefix<B> pf[LW];
-#pragma unroll
-    for (int k = 0; k < LW; ++k) {
-      const int j = 32 * k + lane;
-      w[k] = j < n_w ? s_words[j] : 0u;
-      pf[k] = word_prefix<B>(w[k]);
-    }
-    // inclusive warp scans of the field sums, two words' rows to a scan
-    int incl[LW / 2];
-#pragma unroll
-    for (int q = 0; q < LW / 2; ++q) incl[q] = pf[2 * q].S | (pf[2 * q + 1].S << 16);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-      for (int q = 0; q < LW / 2; ++q) {
-        const int up = __shfl_up_sync(0xffffffffu, incl[q], o);
-        if (lane >= o) incl[q] += up;
-      }
-    }
-    // column before word 32 k + lane: the base, the totals of rows 0..k-1 and
-    // the exclusive prefix of row k
-    int col = h0.x;
-#pragma unroll
-    for (int q = 0; q < LW / 2; ++q) {
-      const int tot = __shfl_sync(0xffffffffu, incl[q], 31);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int k = 2 * q + h;
-        const int ex = (h == 0 ? (incl[q] & 0xFFFF) : (incl[q] >> 16)) - pf[k].S;
-        if (32 * k + lane < n_w) {
-          const WordVals<B> v = load_vals<B>(s_vals, 32 * k + lane, n_w);
-          decode_word<B, XS>(w[k], pf[k], v, xptr<XS>(xs_addr, a.x, col + ex), acc);
-        }
-        col += h == 0 ? (tot & 0xFFFF) : (tot >> 16);
-      }
-    }
+    decode_segment_lanes<B, XS>(st, n_w, h0.x, lane, xs_addr, a.x, acc);
     // every lane has used the buffer's contents: refill it
     __syncwarp();
-    if (lane == 0 && h1.y > 0)
+    if (lane == s && h1.y > 0)
       issue_block(ring + s * Sg::kBytes, &s_full[warp][s], a.blocks + (size_t)h1.x * 16,
                   (uint32_t)h1.y, pol);
     const uint32_t rf = (uint32_t)h0.y;
@@ -354,10 +395,18 @@ __global__ void __launch_bounds__(kDW * 32, 1) delta_seg_kernel(const DeltaArgs 
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
       if (lane == 0) {
         const int row = (int)(rf & kSegRowMask);
-        if (h0.w < 0)
+        if (h0.w < 0) {
           a.y[row] = v;
-        else
-          publish_piece(a, row, h0.w, h1.z, v);
+        } else if (n_pend < 2) {  // a piece of a shared row: park it, combine after the loop
+          a.partials[h1.z] = v;
+          if (n_pend == 0)
+            pend[0] = make_int2(row, h0.w);
+          else
+            pend[1] = make_int2(row, h0.w);
+          ++n_pend;
+        } else {
+          atomicExch(a.status, 2);  // the plan broke its own rule: report, never write
+        }
       }
     }
     if (++s == kDS) {
@@ -365,6 +414,7 @@ __global__ void __launch_bounds__(kDW * 32, 1) delta_seg_kernel(const DeltaArgs 
       phase ^= 1u;
     }
   }
+  if (i == n && lane == 0 && n_pend > 0) finish_pieces(a, pend, n_pend);
   if (i < n && lane == 0) {
     // a wait gave up: let this warp's copies still in flight land before the
     // CTA's shared memory goes (bounded again)
@@ -391,6 +441,8 @@ const void* delta_entry(int bits, bool xs) {
 }  // namespace
 
 int delta_warps_per_cta(int) { return kDW; }
+
+int delta_grid_per_sm(int) { return SPMV_DELTA_GRID_PER_SM; }
 
 int delta_stages(int) { return kDS; }
 

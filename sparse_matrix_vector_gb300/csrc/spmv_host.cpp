@@ -384,8 +384,9 @@ spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_pe
   constexpr int64_t kSegCost = 16;
   constexpr int64_t kMinShare = 256;  // words a warp should get at least
   try {
-    // 1. cut every row into the fewest segments of at most seg_words words,
-    //    of nearly equal size; record each segment's starting column
+    // 1. cut every row into full segments of seg_words words and one shorter
+    //    last segment (full segments take the kernel's unpredicated path);
+    //    record each segment's starting column
     int64_t total_w = 0;
     for (int32_t r = 0; r < d->n_rows; ++r) {
       const int64_t w0 = rp[r] / per_word, w1 = rp[r + 1] / per_word, nw = w1 - w0;
@@ -395,7 +396,7 @@ spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_pe
         continue;
       }
       const int64_t n_s = (nw + seg_words - 1) / seg_words;
-      const int64_t per = (nw + n_s - 1) / n_s;
+      const int64_t per = seg_words;
       const int64_t entries = nw * per_word;
       info->rows_per_bin[n_s > 1 ? 3 : entries > 256 ? 2 : entries > 8 ? 1 : 0] += 1;
       int64_t col = 0;  // running column of the row, before word w
@@ -929,7 +930,7 @@ spmv_status build_delta_blocks(const spmv_delta* d, const DeltaTables& t, int st
     h.row_flags = (uint32_t)sg.row | sg.flags;
     h.n_words = (int32_t)nw;
     h.split = t.seg_split[k];
-    h.piece = t.seg_piece[k];
+    h.slot = h.split >= 0 ? t.splits[(size_t)h.split].first_slot + t.seg_piece[k] : -1;
     if (next[k] >= 0) {
       h.next_off = (*seg_off)[next[k]];
       h.next_bytes = ((*seg_off)[next[k] + 1] - (*seg_off)[next[k]]) * 16;
@@ -981,7 +982,8 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if (occ <= 0) return SPMV_ERR_CUDA;
   const int wpc = delta_warps_per_cta(p->delta_bits);
   DeltaTables t;
-  if ((s = plan_delta_segments(d, occ * p->sm_count * wpc, wpc, &t, &info)) != SPMV_OK)
+  const int per_sm = std::min(occ, delta_grid_per_sm(p->delta_bits));
+  if ((s = plan_delta_segments(d, per_sm * p->sm_count * wpc, wpc, &t, &info)) != SPMV_OK)
     return s;
   p->grid = info.grid;
   p->n_tiles = (int64_t)t.segs.size();

@@ -71,8 +71,7 @@ constexpr int64_t delta_seg_bytes(int bits, int64_t n_w) {
 //              by several warps, else -1
 //   next_off   the block that this warp stages S segments later: offset in
 //   next_bytes 16-byte steps and size in bytes (0 when there is none)
-//   piece      for a split row: which of the row's partial sums this warp's
-//              share produces
+//   slot       for a split row: the partial-sum slot of this warp's piece
 struct DeltaSegHeader {
   int32_t base;
   uint32_t row_flags;
@@ -80,7 +79,7 @@ struct DeltaSegHeader {
   int32_t split;
   int32_t next_off;
   int32_t next_bytes;
-  int32_t piece;
+  int32_t slot;
   int32_t reserved;
 };
 static_assert(sizeof(DeltaSegHeader) == kDeltaHeaderBytes, "segment header is 32 bytes");
@@ -237,6 +236,7 @@ size_t csr_stage_bytes(spmv_dtype dtype);
 int csr_set_smem_limit(size_t dyn);
 int delta_warps_per_cta(int bits);      // warps of a DELTA CTA (each with its own ring)
 int delta_stages(int bits);              // ring depth per warp
+int delta_grid_per_sm(int bits);         // CTAs per SM the grid uses (at most)
 size_t delta_rings_bytes(int bits);      // every stage of every warp of a CTA
 size_t delta_x_smem_bytes(int n_cols);
 int delta_set_smem_limit(int bits, size_t dyn);
