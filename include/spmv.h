@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define SPMV_ABI_VERSION 4
+#define SPMV_ABI_VERSION 5
 
 /* Rows per slice of the SELL format (one warp of the kernel per slice). */
 #define SPMV_SELL_C 32
@@ -208,7 +208,12 @@ typedef struct spmv_plan_options {
                             windows of this many rows before slicing; 1 keeps
                             the row order; 0 chooses by the CV of the row
                             lengths as spmv_select_format does             */
-  int32_t reserved[6];
+  int32_t csr_kernel;    /* CSR: 0 auto (warp segments when rows average at
+                            least 256 nonzeros, else CTA tiles), 1 CTA tiles
+                            (the bins above), 2 warp segments (rows cut into
+                            slices of at most 512 nonzeros, each warp a
+                            contiguous share; [CSR] 4.1 warp per row)      */
+  int32_t reserved[5];
 } spmv_plan_options;
 
 /* What the planner decided; filled by spmv_plan_inspect / spmv_plan_get_info.
@@ -241,7 +246,10 @@ typedef struct spmv_plan_info {
   int64_t algorithmic_bytes; /* matrix_bytes + x read once + y written     */
   int64_t walk_tiles;        /* short-row tiles reduced in walk mode       */
   int64_t interleaved;       /* 1 if products are taken element-interleaved */
-  int64_t reserved[6];
+  int64_t segments;          /* 1 if the plan runs warp-owned row segments
+                                (DELTA, CSR with long rows); n_tiles then
+                                counts segments                            */
+  int64_t reserved[5];
 } spmv_plan_info;
 
 typedef struct spmv_plan spmv_plan;

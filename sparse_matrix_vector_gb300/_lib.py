@@ -65,7 +65,7 @@ class spmv_plan_options(ctypes.Structure):
                 ("cta_row_min", c_i32), ("split_row_min", c_i32),
                 ("split_chunk", c_i32), ("x_smem", c_i32), ("reduce", c_i32),
                 ("lanes", c_i32), ("interleave", c_i32), ("sell_sigma", c_i32),
-                ("reserved", c_i32 * 6)]
+                ("csr_kernel", c_i32), ("reserved", c_i32 * 5)]
 
 
 class spmv_plan_info(ctypes.Structure):
@@ -77,7 +77,8 @@ class spmv_plan_info(ctypes.Structure):
                 ("grid", c_i32), ("block", c_i32),
                 ("launches_per_run", c_i32), ("matrix_bytes", c_i64),
                 ("aux_bytes", c_i64), ("algorithmic_bytes", c_i64),
-                ("walk_tiles", c_i64), ("interleaved", c_i64), ("reserved", c_i64 * 6)]
+                ("walk_tiles", c_i64), ("interleaved", c_i64), ("segments", c_i64),
+                ("reserved", c_i64 * 5)]
 
 
 # name -> (restype, argtypes); every function declared in include/spmv.h

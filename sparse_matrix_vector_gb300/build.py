@@ -1,8 +1,8 @@
 """In-tree build of the C-ABI library ``libspmv_gb300.so`` for sm_103a.
 
-The translation units (host planner and converters, CSR kernel, DELTA
-kernel, sliced-ELL kernel, matrix-free FEM kernel, conjugate-gradient
-kernels, allocation-free entry point) are compiled in parallel with nvcc
+The translation units (host planner and converters, CSR tile kernel, CSR
+segment kernel, DELTA kernel, sliced-ELL kernel, matrix-free FEM kernel,
+conjugate-gradient kernels, allocation-free entry point) are compiled in parallel with nvcc
 and linked into one shared object next to this file.
 Usage: ``python -m sparse_matrix_vector_gb300.build`` or ``build_library()``.
 """
@@ -21,8 +21,8 @@ LIB_NAME = "libspmv_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["spmv_host.cpp", "spmv_csr.cu", "spmv_delta.cu", "spmv_sell.cu", "spmv_fem.cu",
-           "spmv_pcg.cu", "spmv_noalloc.cu"]
+SOURCES = ["spmv_host.cpp", "spmv_csr.cu", "spmv_csr_seg.cu", "spmv_delta.cu", "spmv_sell.cu",
+           "spmv_fem.cu", "spmv_pcg.cu", "spmv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]

@@ -1,0 +1,293 @@
+// CSR kernel for matrices with long rows (fp32 or fp16 values, int32
+// columns): y[row] = sum over the row's nonzeros of values[k] * x[col[k]]
+// ("CUDA CSR SpMV optimisation" 2.1), with the work laid out as for the
+// column-delta kernel.
+//
+// The planner cuts every row into segments of at most kCsrSegNnz nonzeros
+// (full ones first) and gives each warp of the grid a contiguous share of the
+// segments, of equal weight. A segment's block (a 32-byte header, its
+// columns, its values) is staged by one bulk copy into the warp's own ring of
+// shared-memory buffers; lane s of the warp issues the copies into buffer s,
+// so warps never wait for one another and no CTA barrier sits in the loop
+// (the CTA-wide tiles of spmv_csr.cu pay one per work unit, which dominates
+// when a row of ~1,000 nonzeros leaves a 256-thread CTA five per thread).
+// Lane l takes nonzeros l, l + 32, ... of a segment: a warp-wide step reads
+// 32 consecutive columns and values (conflict-free) and gathers x at 32
+// neighbouring columns of the row ("CUDA CSR SpMV optimisation" 4.1: a warp
+// per row, shuffle reduction). fp16 values multiply fp16 x exactly in fp32
+// (mixed-precision fma); fp32 values use fp32 fma.
+// Rows: lanes keep fp32 partials; at a row's last segment, or the end of the
+// warp's share, the warp reduces them. A row inside one share is written at
+// once; a row shared by several warps leaves one partial per warp, and the
+// warp whose atomicAdd completes the row's count adds them in warp order.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "spmv_device.cuh"
+#include "spmv_internal.h"
+
+namespace spmv {
+namespace {
+
+#ifndef SPMV_CSR_SEG_STAGES
+#define SPMV_CSR_SEG_STAGES 2
+#endif
+constexpr int kCS = SPMV_CSR_SEG_STAGES;
+// Warps per CTA (one CTA per SM): the rings fill its shared memory.
+template <typename VT>
+constexpr int kCW = sizeof(VT) == 2 ? 28 : 24;
+constexpr int kSegK = kCsrSegNnz / 32;  // nonzeros per lane in a full segment
+
+template <typename VT>
+struct CSeg {
+  static constexpr int kBytes = (int)csr_seg_bytes(kCsrSegNnz, (int)sizeof(VT));
+  static_assert(kBytes % 16 == 0, "segment buffers stay 16-byte aligned");
+};
+
+struct CsrSegArgs {
+  const unsigned char* __restrict__ blocks;  // one block per segment
+  const int32_t* __restrict__ seg_off;       // block offsets (16-byte steps), n_segs + 1
+  const int32_t* __restrict__ warp_first;    // first segment per warp, n_warps + 1
+  const int32_t* __restrict__ empty_rows;
+  const SplitInfo* __restrict__ splits;      // {first slot, pieces, 0, 0}
+  const void* __restrict__ x;
+  float* __restrict__ y;
+  float* partials;
+  int32_t* counters;
+  int32_t* status;
+  int n_empty;
+  int n_cols;
+};
+
+// acc + a * x: fp32 fma, or for fp16 the mixed-precision fma (exact product).
+__device__ __forceinline__ float fma_v(float acc, float a, float x) { return fmaf(a, x, acc); }
+__device__ __forceinline__ float fma_v(float acc, uint16_t a, uint16_t x) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(x));
+  return acc;
+}
+
+template <typename VT> struct Bits;
+template <> struct Bits<float> { using T = float; };
+template <> struct Bits<__half> { using T = uint16_t; };
+
+// x at column c: shared memory (XS) or the read-only path.
+template <typename VT, bool XS>
+__device__ __forceinline__ typename Bits<VT>::T load_x(const typename Bits<VT>::T* xs,
+                                                       const void* x, int c) {
+  using T = typename Bits<VT>::T;
+  return XS ? xs[c] : __ldg(static_cast<const T*>(x) + c);
+}
+
+// Copy x (n elements) into shared memory with every thread of the CTA.
+template <typename VT>
+__device__ __forceinline__ void copy_x(typename Bits<VT>::T* xs, const void* x, int n) {
+  using T = typename Bits<VT>::T;
+  const T* src = static_cast<const T*>(x);
+  const int nt = kCW<VT> * 32;
+  constexpr int per = 16 / (int)sizeof(T);
+  int done = 0;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+    const int nv = n / per;
+    for (int v = threadIdx.x; v < nv; v += nt)
+      reinterpret_cast<uint4*>(xs)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+    done = nv * per;
+  }
+  for (int i = done + threadIdx.x; i < n; i += nt) xs[i] = __ldg(src + i);
+}
+
+// Lane 0, after its share: make the parked pieces of rows shared with other
+// warps visible (one fence), count each; the warp that completes a row's
+// count adds its pieces in warp order, writes y and re-arms the count.
+__device__ __forceinline__ void finish_pieces(const CsrSegArgs& a, const int2 (&pend)[2],
+                                              int n_pend) {
+  __threadfence();
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (p >= n_pend) break;
+    const int row = pend[p].x, sid = pend[p].y;
+    const SplitInfo si = a.splits[sid];
+    if (atomicAdd(a.counters + sid, 1) == si.n_chunks - 1) {
+      __threadfence();
+      float sum = 0.f;
+      for (int j = 0; j < si.n_chunks; ++j) sum += __ldcg(a.partials + si.first_slot + j);
+      a.y[row] = sum;
+      a.counters[sid] = 0;
+    }
+  }
+}
+
+template <typename VT, bool XS>
+__global__ void __launch_bounds__(kCW<VT> * 32, 1) csr_seg_kernel(const CsrSegArgs a) {
+  using T = typename Bits<VT>::T;
+  constexpr int W = kCW<VT>;
+  constexpr int kBytes = CSeg<VT>::kBytes;
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  __shared__ __align__(8) uint64_t s_full[W][kCS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * W + warp;
+  unsigned char* ring = dyn_smem + (size_t)warp * kCS * kBytes;
+  T* xs = reinterpret_cast<T*>(dyn_smem + (size_t)W * kCS * kBytes);
+  const int t0 = __ldg(a.warp_first + gw);
+  const int n = __ldg(a.warp_first + gw + 1) - t0;
+  const uint64_t pol = policy_evict_first();
+
+  // plan-owned data only until pdl_wait: the first kCS blocks of the share;
+  // lane s issues every copy into buffer s
+  if (lane == 0) {
+    for (int s = 0; s < kCS; ++s) mbar_init(&s_full[warp][s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane < kCS && lane < n) {
+    const int o0 = __ldg(a.seg_off + t0 + lane), o1 = __ldg(a.seg_off + t0 + lane + 1);
+    mbar_arrive_expect_tx(&s_full[warp][lane], (uint32_t)(o1 - o0) * 16u);
+    bulk_g2s(ring + lane * kBytes, a.blocks + (size_t)o0 * 16, (uint32_t)(o1 - o0) * 16u,
+             &s_full[warp][lane], pol);
+  }
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();
+  if (XS) copy_x<VT>(xs, a.x, a.n_cols);
+  for (int i = blockIdx.x * W * 32 + threadIdx.x; i < a.n_empty; i += gridDim.x * W * 32)
+    a.y[__ldg(a.empty_rows + i)] = 0.f;
+  if (XS) __syncthreads();
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // pieces of rows shared with other warps (lane 0): {row, split id}; a share
+  // holds at most two, its first row's and its last row's
+  int2 pend[2];
+  int n_pend = 0;
+  int s = 0;
+  uint32_t phase = 0;
+  int i = 0;
+  for (; i < n; ++i) {
+    // the warp decides together (its shuffles below need every lane)
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[warp][s], phase))) {
+      if (lane == 0) atomicExch(a.status, 1);
+      break;
+    }
+    const unsigned char* st = ring + s * kBytes;
+    const int4 h0 = *reinterpret_cast<const int4*>(st);       // -, row | flags, nonzeros, split
+    const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; slot
+    const int nz = h0.z;
+    const int* s_col = reinterpret_cast<const int*>(st + kSegHeaderBytes);
+    const T* s_val = reinterpret_cast<const T*>(st + kSegHeaderBytes + ((nz * 4 + 15) & ~15));
+    if (nz == kCsrSegNnz) {  // one straight-line block: all gathers can overlap
+#pragma unroll
+      for (int k = 0; k < kSegK; ++k) {
+        const int j = 32 * k + lane;
+        acc[k & 3] = fma_v(acc[k & 3], s_val[j], load_x<VT, XS>(xs, a.x, s_col[j]));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kSegK; ++k) {
+        const int j = 32 * k + lane;
+        if (j < nz) acc[k & 3] = fma_v(acc[k & 3], s_val[j], load_x<VT, XS>(xs, a.x, s_col[j]));
+      }
+    }
+    // every lane has used the buffer's contents: refill it
+    __syncwarp();
+    if (lane == s && h1.y > 0) {
+      mbar_arrive_expect_tx(&s_full[warp][s], (uint32_t)h1.y);
+      bulk_g2s(ring + s * kBytes, a.blocks + (size_t)h1.x * 16, (uint32_t)h1.y, &s_full[warp][s],
+               pol);
+    }
+    const uint32_t rf = (uint32_t)h0.y;
+    if ((rf & kSegLast) || i == n - 1) {  // the row ends, or this warp's share does
+      const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      if (lane == 0) {
+        const int row = (int)(rf & kSegRowMask);
+        if (h0.w < 0) {
+          a.y[row] = v;
+        } else if (n_pend < 2) {  // a piece of a shared row: park it, combine after the loop
+          a.partials[h1.z] = v;
+          if (n_pend == 0)
+            pend[0] = make_int2(row, h0.w);
+          else
+            pend[1] = make_int2(row, h0.w);
+          ++n_pend;
+        } else {
+          atomicExch(a.status, 2);  // the plan broke its own rule: report, never write
+        }
+      }
+    }
+    if (++s == kCS) {
+      s = 0;
+      phase ^= 1u;
+    }
+  }
+  if (i == n && lane == 0 && n_pend > 0) finish_pieces(a, pend, n_pend);
+  if (i < n && lane == 0) {
+    // a wait gave up: let this warp's copies still in flight land before the
+    // CTA's shared memory goes (bounded again)
+    for (int j = i; j < n && j < i + kCS; ++j) {
+      mbar_wait_bounded(&s_full[warp][s], phase);
+      if (++s == kCS) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
+const void* csr_seg_entry(spmv_dtype dt, bool xs) {
+  if (dt == SPMV_F32)
+    return xs ? reinterpret_cast<const void*>(&csr_seg_kernel<float, true>)
+              : reinterpret_cast<const void*>(&csr_seg_kernel<float, false>);
+  return xs ? reinterpret_cast<const void*>(&csr_seg_kernel<__half, true>)
+            : reinterpret_cast<const void*>(&csr_seg_kernel<__half, false>);
+}
+
+}  // namespace
+
+int csr_seg_warps_per_cta(spmv_dtype dt) { return dt == SPMV_F32 ? kCW<float> : kCW<__half>; }
+
+int csr_seg_stages(spmv_dtype) { return kCS; }
+
+size_t csr_seg_rings_bytes(spmv_dtype dt) {
+  return dt == SPMV_F32 ? (size_t)kCW<float> * kCS * CSeg<float>::kBytes
+                        : (size_t)kCW<__half> * kCS * CSeg<__half>::kBytes;
+}
+
+int csr_seg_set_smem_limit(size_t dyn) {
+  if (dyn == 0) return 0;
+  for (spmv_dtype dt : {SPMV_F32, SPMV_F16})
+    for (bool xs : {false, true})
+      if (cudaFuncSetAttribute(csr_seg_entry(dt, xs), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dyn) != cudaSuccess)
+        return -1;
+  return 0;
+}
+
+int csr_seg_occupancy(spmv_dtype dt, bool x_smem, size_t dyn_smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, csr_seg_entry(dt, x_smem),
+                                                    csr_seg_warps_per_cta(dt) * 32,
+                                                    dyn_smem) != cudaSuccess)
+    return -1;
+  return n;
+}
+
+int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream) {
+  if (p.grid == 0) return 0;
+  CsrSegArgs a;
+  a.blocks = p.blocks;
+  a.seg_off = p.seg_off;
+  a.warp_first = p.cta_first;
+  a.empty_rows = p.empty_rows;
+  a.splits = p.splits;
+  a.x = x;
+  a.y = y;
+  a.partials = p.partials;
+  a.counters = p.counters;
+  a.status = p.status;
+  a.n_empty = p.n_empty_rows;
+  a.n_cols = p.n_cols;
+  void* args[] = {&a};
+  return launch_pdl(csr_seg_entry(p.dtype, p.x_smem), p.grid, csr_seg_warps_per_cta(p.dtype) * 32,
+                    p.dyn_smem, stream, args);
+}
+
+}  // namespace spmv

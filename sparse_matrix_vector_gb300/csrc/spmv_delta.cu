@@ -286,8 +286,8 @@ __device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, in
                                                      int lane, uint32_t xs_addr,
                                                      const __half* x, float (&acc)[4]) {
   constexpr int LW = Seg<B>::kLaneWords;
-  const uint32_t* s_words = reinterpret_cast<const uint32_t*>(st + kDeltaHeaderBytes);
-  const unsigned char* s_vals = st + kDeltaHeaderBytes + ((n_w * 4 + 15) & ~15);
+  const uint32_t* s_words = reinterpret_cast<const uint32_t*>(st + kSegHeaderBytes);
+  const unsigned char* s_vals = st + kSegHeaderBytes + ((n_w * 4 + 15) & ~15);
   const bool full = n_w == Seg<B>::kWords;  // the common case: no lane idles
   uint32_t w[LW];
   WordPrefix<B> pf[LW];

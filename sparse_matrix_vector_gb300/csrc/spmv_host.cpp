@@ -155,7 +155,9 @@ Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype) {
   r.lanes_log2 = 0;
   r.interleave = 0;
   r.sell_sigma = 0;
+  r.csr_kernel = 0;
   if (o) {
+    if (o->csr_kernel == 1 || o->csr_kernel == 2) r.csr_kernel = o->csr_kernel;
     if (o->interleave == 1 || o->interleave == 2) r.interleave = o->interleave;
     if (o->sell_sigma > 0) r.sell_sigma = o->sell_sigma;
     if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, cap - 16);
@@ -372,45 +374,32 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
   return SPMV_OK;
 }
 
-spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
-                                DeltaTables* out, spmv_plan_info* info) {
-  *out = DeltaTables();
-  const int64_t* rp = d->row_ptr;
-  const int32_t bits = delta_bits_of(d);
-  const int64_t per_word = 32 / bits;  // entries per word
-  const uint32_t cap = (1u << bits) - 1u;
-  const int64_t seg_words = delta_seg_words(bits);
-  // weight of a segment: its words plus a fixed cost (header, scans, copy)
-  constexpr int64_t kSegCost = 16;
-  constexpr int64_t kMinShare = 256;  // words a warp should get at least
+spmv_status plan_segments(int32_t n_rows, const std::function<int64_t(int32_t)>& row_begin,
+                          int64_t cap, int64_t seg_cost, int64_t entries_per_item,
+                          int max_warps, int warps_per_cta, SegTables* out,
+                          spmv_plan_info* info) {
+  *out = SegTables();
+  constexpr int64_t kMinShare = 256;  // items a warp should get at least
   try {
-    // 1. cut every row into full segments of seg_words words and one shorter
-    //    last segment (full segments take the kernel's unpredicated path);
-    //    record each segment's starting column
+    // 1. cut every row into full segments of `cap` items and one shorter last
+    //    segment (full segments take the kernels' unpredicated path)
     int64_t total_w = 0;
-    for (int32_t r = 0; r < d->n_rows; ++r) {
-      const int64_t w0 = rp[r] / per_word, w1 = rp[r + 1] / per_word, nw = w1 - w0;
-      if (nw == 0) {
+    for (int32_t r = 0; r < n_rows; ++r) {
+      const int64_t i0 = row_begin(r), i1 = row_begin(r + 1), ni = i1 - i0;
+      if (ni == 0) {
         out->empty_rows.push_back(r);
         info->rows_per_bin[0] += 1;
         continue;
       }
-      const int64_t n_s = (nw + seg_words - 1) / seg_words;
-      const int64_t per = seg_words;
-      const int64_t entries = nw * per_word;
+      if (i1 > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+      const int64_t n_s = (ni + cap - 1) / cap;
+      const int64_t entries = ni * entries_per_item;
       info->rows_per_bin[n_s > 1 ? 3 : entries > 256 ? 2 : entries > 8 ? 1 : 0] += 1;
-      int64_t col = 0;  // running column of the row, before word w
-      int64_t w = w0;
       for (int64_t k = 0; k < n_s; ++k) {
-        const int64_t sb = w0 + k * per, se = std::min(sb + per, w1);
-        for (; w < sb; ++w) {
-          const uint32_t word = d->words[w];
-          for (int q = 0; q < per_word; ++q) col += (word >> (bits * q)) & cap;
-        }
-        if (col > INT32_MAX || se > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+        const int64_t sb = i0 + k * cap, se = std::min(sb + cap, i1);
         const uint32_t flags = (k == 0 ? kSegFirst : 0u) | (k == n_s - 1 ? kSegLast : 0u);
-        out->segs.push_back({r, (int32_t)sb, (int32_t)se, (int32_t)col, flags});
-        total_w += (se - sb) + kSegCost;
+        out->segs.push_back({r, (int32_t)sb, (int32_t)se, 0, flags});
+        total_w += (se - sb) + seg_cost;
       }
       (n_s > 1 ? info->tiles_per_bin[3] : info->tiles_per_bin[2]) += n_s;
     }
@@ -429,18 +418,18 @@ spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_pe
       int g = 1;
       for (int64_t t = 0; t < n_segs; ++t) {
         while (g < G && cum >= (int64_t)((__int128)g * total_w / G)) out->warp_first[g++] = (int32_t)t;
-        const DeltaSeg& sg = out->segs[(size_t)t];
-        cum += (int64_t)(sg.word_end - sg.word_begin) + kSegCost;
+        const SegDesc& sg = out->segs[(size_t)t];
+        cum += (int64_t)(sg.end - sg.begin) + seg_cost;
       }
       while (g < G) out->warp_first[g++] = (int32_t)n_segs;
     }
     // 3. rows whose segments fall in more than one warp's share: one partial
     //    per such warp (its piece), combined by the last to arrive
     out->seg_split.assign((size_t)n_segs, -1);
+    out->seg_slot.assign((size_t)n_segs, -1);
     std::vector<int32_t> seg_warp((size_t)n_segs);
     for (int g = 0; g < n_warps; ++g)
       for (int32_t t = out->warp_first[g]; t < out->warp_first[g + 1]; ++t) seg_warp[t] = g;
-    out->seg_piece.assign((size_t)n_segs, 0);
     for (int64_t t = 0; t < n_segs;) {
       int64_t e = t + 1;
       while (e < n_segs && out->segs[(size_t)e].row == out->segs[(size_t)t].row) ++e;
@@ -448,7 +437,7 @@ spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_pe
         int32_t pieces = 0;
         for (int64_t u = t; u < e; ++u) {
           if (u > t && seg_warp[u] != seg_warp[u - 1]) ++pieces;
-          out->seg_piece[(size_t)u] = pieces;
+          out->seg_slot[(size_t)u] = (int32_t)out->n_chunks + pieces;
           out->seg_split[(size_t)u] = (int32_t)out->splits.size();
         }
         ++pieces;
@@ -463,6 +452,36 @@ spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_pe
     info->grid = grid;
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  return SPMV_OK;
+}
+
+spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
+                                SegTables* out, spmv_plan_info* info) {
+  const int64_t* rp = d->row_ptr;
+  const int32_t bits = delta_bits_of(d);
+  const int64_t per_word = 32 / bits;  // entries per word
+  const uint32_t cap = (1u << bits) - 1u;
+  // a segment's weight: its words plus a fixed cost (header, scans, copy)
+  spmv_status s = plan_segments(
+      d->n_rows, [&](int32_t r) { return rp[r] / per_word; }, delta_seg_words(bits), 16,
+      per_word, max_warps, warps_per_cta, out, info);
+  if (s != SPMV_OK) return s;
+  // each segment's starting column: the running column of its row
+  int32_t row = -1;
+  int64_t col = 0, w = 0;
+  for (SegDesc& sg : out->segs) {
+    if (sg.row != row) {
+      row = sg.row;
+      col = 0;
+      w = sg.begin;
+    }
+    for (; w < sg.begin; ++w) {
+      const uint32_t word = d->words[w];
+      for (int q = 0; q < per_word; ++q) col += (word >> (bits * q)) & cap;
+    }
+    if (col > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+    sg.base = (int32_t)col;
   }
   return SPMV_OK;
 }
@@ -602,11 +621,132 @@ static bool csr_interleave_auto(const spmv_csr* m) {
   return mean_len >= 32.0 && span8_bytes >= 40.0;
 }
 
+// CSR with warp segments: the auto rule and the plan.
+constexpr int64_t kCsrSegMinMeanRow = 256;  // rows averaging this many nonzeros or more
+
+bool csr_use_segments(const spmv_csr* m, const Options& o) {
+  if (o.csr_kernel != 0) return o.csr_kernel == 2;
+  return m->n_rows > 0 && m->nnz >= kCsrSegMinMeanRow * (int64_t)m->n_rows;
+}
+
+// Device layout of a CSR segment plan: one block per segment, back to back in
+// segment order, each a 32-byte header (SegHeader), the segment's columns
+// (padded to 16 bytes) and values (padded to 16 bytes).
+spmv_status build_csr_seg_blocks(const spmv_csr* m, const SegTables& t, int stages,
+                                 std::vector<uint4>* out, std::vector<int32_t>* seg_off) {
+  const int vs = (int)dtype_size(m->value_dtype);
+  const size_t n_segs = t.segs.size();
+  try {
+    seg_off->assign(n_segs + 1, 0);
+    int64_t total = 0;  // in 16-byte steps
+    for (size_t k = 0; k < n_segs; ++k) {
+      (*seg_off)[k] = (int32_t)total;
+      total += csr_seg_bytes((int64_t)t.segs[k].end - t.segs[k].begin, vs) / 16;
+      if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+    }
+    (*seg_off)[n_segs] = (int32_t)total;
+    out->assign((size_t)total, make_uint4(0, 0, 0, 0));
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
+  unsigned char* base = reinterpret_cast<unsigned char*>(out->data());
+  const unsigned char* vals = static_cast<const unsigned char*>(m->values);
+  for (size_t k = 0; k < n_segs; ++k) {
+    const SegDesc& sg = t.segs[k];
+    const int64_t nz = (int64_t)sg.end - sg.begin;
+    unsigned char* b = base + (size_t)(*seg_off)[k] * 16;
+    SegHeader h{};
+    h.row_flags = (uint32_t)sg.row | sg.flags;
+    h.n_words = (int32_t)nz;
+    h.split = t.seg_split[k];
+    h.slot = t.seg_slot[k];
+    const size_t nk = k + (size_t)stages;  // staged S segments later by the same warp
+    const int32_t g_end = t.warp_first[(size_t)(std::upper_bound(t.warp_first.begin(),
+                                                                 t.warp_first.end(),
+                                                                 (int32_t)k) -
+                                                t.warp_first.begin())];
+    if ((int64_t)nk < g_end) {
+      h.next_off = (*seg_off)[nk];
+      h.next_bytes = ((*seg_off)[nk + 1] - (*seg_off)[nk]) * 16;
+    }
+    std::memcpy(b, &h, sizeof(h));
+    std::memcpy(b + kSegHeaderBytes, m->col_idx + sg.begin, (size_t)nz * 4);
+    std::memcpy(b + kSegHeaderBytes + delta_pad16(nz * 4), vals + (size_t)sg.begin * vs,
+                (size_t)nz * vs);
+  }
+  return SPMV_OK;
+}
+
+spmv_status create_csr_seg_plan(const spmv_csr* m, const Options& o, Plan* p) {
+  spmv_plan_info& info = p->info;
+  spmv_status s;
+  const size_t vs = dtype_size(m->value_dtype);
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) !=
+      cudaSuccess)
+    return SPMV_ERR_CUDA;
+  const size_t xbytes = ((size_t)m->n_cols * vs + 15) / 16 * 16;
+  const size_t rings = csr_seg_rings_bytes(m->value_dtype);
+  const bool fits = rings + xbytes + 4096 <= (size_t)optin;
+  p->x_smem = o.x_smem == 0 ? false : o.x_smem == 1 ? fits : (fits && xbytes <= kXsAutoBytesDelta);
+  p->dyn_smem = rings + (p->x_smem ? xbytes : 0);
+  if (csr_seg_set_smem_limit(p->dyn_smem) != 0) return SPMV_ERR_CUDA;
+  const int occ = csr_seg_occupancy(m->value_dtype, p->x_smem, p->dyn_smem);
+  if (occ <= 0) return SPMV_ERR_CUDA;
+  const int wpc = csr_seg_warps_per_cta(m->value_dtype);
+  SegTables t;
+  if ((s = plan_segments(
+           m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; }, kCsrSegNnz, 64, 1,
+           std::min(occ, 1) * p->sm_count * wpc, wpc, &t, &info)) != SPMV_OK)
+    return s;
+  p->csr_segments = true;
+  p->grid = info.grid;
+  p->n_tiles = (int64_t)t.segs.size();
+  std::vector<uint4> blocks;
+  std::vector<int32_t> seg_off;
+  if ((s = build_csr_seg_blocks(m, t, csr_seg_stages(m->value_dtype), &blocks, &seg_off)) !=
+      SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->blocks, blocks.data(), blocks.size() * 16, blocks.size() * 16)) !=
+      SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->seg_off, seg_off.data(), seg_off.size() * 4, seg_off.size() * 4)) !=
+      SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->cta_first, t.warp_first.data(), t.warp_first.size() * 4,
+                      t.warp_first.size() * 4)) != SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->empty_rows, t.empty_rows.data(), t.empty_rows.size() * 4,
+                      t.empty_rows.size() * 4)) != SPMV_OK)
+    return s;
+  p->n_empty_rows = (int32_t)t.empty_rows.size();
+  if ((s = dev_upload(&p->splits, t.splits.data(), t.splits.size() * sizeof(SplitInfo),
+                      t.splits.size() * sizeof(SplitInfo))) != SPMV_OK)
+    return s;
+  if ((s = dev_upload(&p->partials, nullptr, 0, (size_t)t.n_chunks * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
+  if ((s = common_buffers(p)) != SPMV_OK) return s;
+  info.x_in_smem = p->x_smem ? 1 : 0;
+  info.block = wpc * 32;
+  info.segments = 1;
+  info.launches_per_run = m->n_rows > 0 ? 1 : 0;
+  info.matrix_bytes = (int64_t)m->nnz * (int64_t)(vs + 4) + ((int64_t)m->n_rows + 1) * 4;
+  // the blocks hold the columns and values plus headers and padding; the
+  // row pointers are not kept on the device
+  info.aux_bytes = (int64_t)(blocks.size() * 16) - (int64_t)m->nnz * (int64_t)(vs + 4) +
+                   (int64_t)(seg_off.size() * 4 + t.warp_first.size() * 4 +
+                             t.empty_rows.size() * 4 + t.splits.size() * (sizeof(SplitInfo) + 4) +
+                             (size_t)t.n_chunks * 4);
+  fill_bytes(&info, vs);
+  return SPMV_OK;
+}
+
 spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
   CsrTables t;
   spmv_plan_info& info = p->info;
   spmv_status s;
   if ((s = bind_device(p)) != SPMV_OK) return s;
+  if (csr_use_segments(m, o)) return create_csr_seg_plan(m, o, p);
   const size_t vs = dtype_size(m->value_dtype);
   const size_t xbytes = (size_t)m->n_cols * vs;
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
@@ -895,11 +1035,11 @@ spmv_status resolve_format(const spmv_csr* m, const Options& o, spmv_format* for
 
 // Device layout of a DELTA plan: one block per segment, back to back in
 // segment order (so each warp's share is contiguous), each block a 32-byte
-// header (DeltaSegHeader), the segment's words (padded to 16 bytes) and their
+// header (SegHeader), the segment's words (padded to 16 bytes) and their
 // values (padded to 16 bytes; at 2 bits each word's 32 bytes of values are
 // split into two planes of 16-byte halves). One bulk copy stages a block.
 // seg_off receives every block's offset in 16-byte steps (n_segs + 1).
-spmv_status build_delta_blocks(const spmv_delta* d, const DeltaTables& t, int stages,
+spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stages,
                                std::vector<uint4>* out, std::vector<int32_t>* seg_off) {
   const int32_t bits = delta_bits_of(d);
   const int64_t per = delta_per_word(bits);
@@ -909,7 +1049,7 @@ spmv_status build_delta_blocks(const spmv_delta* d, const DeltaTables& t, int st
     int64_t total = 0;  // in 16-byte steps
     for (size_t k = 0; k < n_segs; ++k) {
       (*seg_off)[k] = (int32_t)total;
-      total += delta_seg_bytes(bits, (int64_t)t.segs[k].word_end - t.segs[k].word_begin) / 16;
+      total += delta_seg_bytes(bits, (int64_t)t.segs[k].end - t.segs[k].begin) / 16;
       if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
     }
     (*seg_off)[n_segs] = (int32_t)total;
@@ -922,21 +1062,21 @@ spmv_status build_delta_blocks(const spmv_delta* d, const DeltaTables& t, int st
     for (int32_t k = t.warp_first[g]; k + stages < t.warp_first[g + 1]; ++k) next[k] = k + stages;
   unsigned char* base = reinterpret_cast<unsigned char*>(out->data());
   for (size_t k = 0; k < n_segs; ++k) {
-    const DeltaSeg& sg = t.segs[k];
-    const int64_t wb = sg.word_begin, nw = (int64_t)sg.word_end - sg.word_begin;
+    const SegDesc& sg = t.segs[k];
+    const int64_t wb = sg.begin, nw = (int64_t)sg.end - sg.begin;
     unsigned char* b = base + (size_t)(*seg_off)[k] * 16;
-    DeltaSegHeader h{};
+    SegHeader h{};
     h.base = sg.base;
     h.row_flags = (uint32_t)sg.row | sg.flags;
     h.n_words = (int32_t)nw;
     h.split = t.seg_split[k];
-    h.slot = h.split >= 0 ? t.splits[(size_t)h.split].first_slot + t.seg_piece[k] : -1;
+    h.slot = t.seg_slot[k];
     if (next[k] >= 0) {
       h.next_off = (*seg_off)[next[k]];
       h.next_bytes = ((*seg_off)[next[k] + 1] - (*seg_off)[next[k]]) * 16;
     }
     std::memcpy(b, &h, sizeof(h));
-    unsigned char* words = b + kDeltaHeaderBytes;
+    unsigned char* words = b + kSegHeaderBytes;
     unsigned char* vals = words + delta_pad16(nw * 4);
     std::memcpy(words, d->words + wb, (size_t)nw * 4);
     const uint16_t* src = d->values + wb * per;
@@ -981,7 +1121,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   const int occ = delta_kernel_occupancy(p->delta_bits, p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
   const int wpc = delta_warps_per_cta(p->delta_bits);
-  DeltaTables t;
+  SegTables t;
   const int per_sm = std::min(occ, delta_grid_per_sm(p->delta_bits));
   if ((s = plan_delta_segments(d, per_sm * p->sm_count * wpc, wpc, &t, &info)) != SPMV_OK)
     return s;
@@ -1007,6 +1147,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
   info.block = wpc * 32;
+  info.segments = 1;
   info.launches_per_run = d->n_rows > 0 ? 1 : 0;
   info.matrix_bytes = delta_matrix_bytes(*d);
   // the blocks hold the matrix's values and deltas, the segment headers and
@@ -1229,9 +1370,10 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
     const bool xs = delta_x_fits(format_delta_bits(format), m->n_cols, o.x_smem,
                                  kAssumedSmemOptin);
     const int wpc = delta_warps_per_cta(format_delta_bits(format));
-    DeltaTables t;
+    SegTables t;
     s = plan_delta_segments(&d, kAssumedSms * wpc, wpc, &t, info);
     info->block = wpc * 32;
+    info->segments = 1;
     info->n_entries = d.n_entries;
     info->x_in_smem = xs ? 1 : 0;
     info->launches_per_run = m->n_rows > 0;
@@ -1239,6 +1381,25 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
     fill_bytes(info, 2);
     spmv_delta_free(&d);
     return s;
+  }
+  const size_t vsz = dtype_size(m->value_dtype);
+  if (csr_use_segments(m, o)) {
+    const int wpc = csr_seg_warps_per_cta(m->value_dtype);
+    SegTables t;
+    s = plan_segments(
+        m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; }, kCsrSegNnz, 64, 1,
+        kAssumedSms * wpc, wpc, &t, info);
+    if (s != SPMV_OK) return s;
+    info->block = wpc * 32;
+    info->segments = 1;
+    info->n_entries = m->nnz;
+    const size_t xbytes = ((size_t)m->n_cols * vsz + 15) / 16 * 16;
+    const bool fits = csr_seg_rings_bytes(m->value_dtype) + xbytes + 4096 <= kAssumedSmemOptin;
+    info->x_in_smem = o.x_smem == 0 ? 0 : o.x_smem == 1 ? fits : (fits && xbytes <= kXsAutoBytesDelta);
+    info->launches_per_run = m->n_rows > 0;
+    info->matrix_bytes = m->nnz * (int64_t)(vsz + 4) + ((int64_t)m->n_rows + 1) * 4;
+    fill_bytes(info, vsz);
+    return SPMV_OK;
   }
   CsrTables t;
   s = plan_csr_tiles(m->n_rows, m->row_ptr, o, 5 * kAssumedSms, &t, info);
@@ -1572,7 +1733,8 @@ spmv_status spmv_run(spmv_plan* plan, const void* x, float* y, void* stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
   if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
   if (p.n_rows == 0) return SPMV_OK;
-  int rc = p.format == SPMV_FORMAT_CSR    ? launch_csr(p, x, y, stream)
+  int rc = p.format == SPMV_FORMAT_CSR    ? (p.csr_segments ? launch_csr_seg(p, x, y, stream)
+                                                             : launch_csr(p, x, y, stream))
            : p.format == SPMV_FORMAT_SELL ? launch_sell(p, x, y, stream)
            : p.format == SPMV_FORMAT_FEM  ? launch_fem(p, x, y, stream)
                                           : launch_delta(p, x, y, stream);

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <vector>
 
 #include "../../include/spmv.h"
@@ -55,24 +56,25 @@ struct PcgScalars {
 // segment (delta_lane_words(b) of them at most).
 constexpr int delta_lane_words(int bits) { return bits == 2 ? 2 : 4; }
 constexpr int delta_seg_words(int bits) { return 32 * delta_lane_words(bits); }
-constexpr int kDeltaHeaderBytes = 32;
+constexpr int kSegHeaderBytes = 32;
 constexpr int64_t delta_pad16(int64_t b) { return (b + 15) & ~(int64_t)15; }
 // Bytes of the device block of a segment of n_w words of b-bit deltas: the
 // header, the words (padded to 16 bytes) and their values (32 / b halves a
 // word, padded to 16 bytes).
 constexpr int64_t delta_seg_bytes(int bits, int64_t n_w) {
-  return kDeltaHeaderBytes + delta_pad16(n_w * 4) + delta_pad16(n_w * (64 / bits));
+  return kSegHeaderBytes + delta_pad16(n_w * 4) + delta_pad16(n_w * (64 / bits));
 }
-// Segment header, the first 32 bytes of its block:
-//   base       column before the segment's first entry
+// Segment header (DELTA, and CSR with long rows), the first 32 bytes of its
+// block:
+//   base       DELTA: column before the segment's first entry (CSR: 0)
 //   row_flags  row | kSegFirst (first segment of the row) | kSegLast (last)
-//   n_words    packed words in the segment
+//   n_words    items in the segment (DELTA: packed words; CSR: nonzeros)
 //   split      index into the split table when the row's segments are shared
 //              by several warps, else -1
 //   next_off   the block that this warp stages S segments later: offset in
 //   next_bytes 16-byte steps and size in bytes (0 when there is none)
 //   slot       for a split row: the partial-sum slot of this warp's piece
-struct DeltaSegHeader {
+struct SegHeader {
   int32_t base;
   uint32_t row_flags;
   int32_t n_words;
@@ -82,7 +84,13 @@ struct DeltaSegHeader {
   int32_t slot;
   int32_t reserved;
 };
-static_assert(sizeof(DeltaSegHeader) == kDeltaHeaderBytes, "segment header is 32 bytes");
+static_assert(sizeof(SegHeader) == kSegHeaderBytes, "segment header is 32 bytes");
+// CSR segments: at most kCsrSegNnz nonzeros of one row; the block is the
+// header, the columns (padded to 16 bytes) and the values (padded to 16).
+constexpr int kCsrSegNnz = 512;
+constexpr int64_t csr_seg_bytes(int64_t nnz, int value_bytes) {
+  return kSegHeaderBytes + delta_pad16(nnz * 4) + delta_pad16(nnz * value_bytes);
+}
 constexpr uint32_t kSegFirst = 1u << 31;
 constexpr uint32_t kSegLast = 1u << 30;
 constexpr uint32_t kSegRowMask = (1u << 30) - 1u;
@@ -132,6 +140,7 @@ struct Options {
   int lanes_log2;  // lanes mode when forced
   int interleave;  // CSR products: 0 auto, 1 chunks of 8, 2 element-interleaved
   int sell_sigma;  // SELL sorting window, 0: by the CV of the row lengths
+  int csr_kernel;  // CSR: 0 auto, 1 CTA tiles, 2 warp segments
 };
 
 Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype);
@@ -150,29 +159,36 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* row_ptr,
                            const Options& opt, int max_ctas, CsrTables* out,
                            spmv_plan_info* info);
 
-// One segment of a DELTA plan, as the planner cuts it.
-struct DeltaSeg {
+// One segment of a warp-segment plan (DELTA, or CSR with long rows), as the
+// planner cuts it: a slice [begin, end) of one row's items (packed words for
+// DELTA, nonzeros for CSR).
+struct SegDesc {
   int32_t row;
-  int32_t word_begin, word_end;  // into the format's words
-  int32_t base;                  // column before the first entry
-  uint32_t flags;                // kSegFirst / kSegLast
+  int32_t begin, end;
+  int32_t base;    // DELTA: column before the first entry
+  uint32_t flags;  // kSegFirst / kSegLast
 };
 
-// Host-side result of planning a DELTA matrix.
-struct DeltaTables {
-  std::vector<DeltaSeg> segs;
+// Host-side result of cutting rows into segments and dealing them to warps.
+struct SegTables {
+  std::vector<SegDesc> segs;
   std::vector<int32_t> warp_first;  // warp g runs segments [warp_first[g], warp_first[g+1])
   std::vector<int32_t> seg_split;   // per segment: index into splits, or -1
-  std::vector<int32_t> seg_piece;   // per segment of a split row: its warp's piece
+  std::vector<int32_t> seg_slot;    // per segment of a split row: its warp's partial slot
   std::vector<SplitInfo> splits;    // {first_slot, pieces, 0, 0}
   std::vector<int32_t> empty_rows;  // rows without stored entries (y = 0)
   int64_t n_chunks = 0;             // partial-sum slots over all split rows
 };
 
-// Cut the rows into segments and deal them to at most `max_warps` warps as
-// contiguous shares of equal weight (words + a per-segment cost).
+// Cut every row's items [row_begin(r), row_begin(r + 1)) into segments of at
+// most `cap` (full ones first) and deal them to at most `max_warps` warps as
+// contiguous shares of equal weight (items + seg_cost per segment).
+spmv_status plan_segments(int32_t n_rows, const std::function<int64_t(int32_t)>& row_begin,
+                          int64_t cap, int64_t seg_cost, int64_t entries_per_item,
+                          int max_warps, int warps_per_cta, SegTables* out,
+                          spmv_plan_info* info);
 spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
-                                DeltaTables* out, spmv_plan_info* info);
+                                SegTables* out, spmv_plan_info* info);
 
 // Device resources of a plan.
 struct Plan {
@@ -185,6 +201,7 @@ struct Plan {
   bool x_smem = false;
   int delta_bits = 4;          // DELTA: bits per column delta (2, 4 or 8)
   bool interleaved = false;  // CSR: products element-interleaved over the CTA
+  bool csr_segments = false;  // CSR: warp-owned row segments (long rows)
   bool x_aligned16 = false;
   int grid = 0;
   size_t dyn_smem = 0;
@@ -242,6 +259,13 @@ size_t delta_x_smem_bytes(int n_cols);
 int delta_set_smem_limit(int bits, size_t dyn);
 int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
+// CSR with long rows (spmv_csr_seg.cu): warp-owned segments, as DELTA.
+int csr_seg_warps_per_cta(spmv_dtype dtype);
+int csr_seg_stages(spmv_dtype dtype);
+size_t csr_seg_rings_bytes(spmv_dtype dtype);
+int csr_seg_set_smem_limit(size_t dyn);
+int csr_seg_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem);
+int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 int launch_sell(const Plan& p, const void* x, float* y, void* stream);
 int launch_fem(const Plan& p, const void* x, float* y, void* stream);

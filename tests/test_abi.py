@@ -35,7 +35,7 @@ def test_every_declared_function_is_exported(spmv_lib):
 
 
 def test_abi_version_and_status_strings(spmv_lib):
-    assert S.spmv_abi_version() == 4
+    assert S.spmv_abi_version() == 5
     for code in range(11):
         s = S.spmv_status_string(code)
         assert s and s != "unknown status"
@@ -254,15 +254,25 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     info = S.spmv_plan_inspect(fem.row_ptr, fem.col_idx, fem.values, fem.n_cols)
     assert info["rows_per_bin"] == [0, fem.n_rows, 0, 0]   # warp
     llm = workloads.llm(0.3, n=2048)
-    info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols)
+    tiles = S.spmv_plan_options(csr_kernel=1)
+    info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols, options=tiles)
     assert info["rows_per_bin"] == [0, 0, llm.n_rows, 0]   # CTA
-    assert info["x_in_smem"] == 0                            # x via L1 by default
+    assert info["x_in_smem"] == 0 and info["segments"] == 0  # x via L1 by default
     forced = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
-                                 options=S.spmv_plan_options(x_smem=1))
+                                 options=S.spmv_plan_options(x_smem=1, csr_kernel=1))
     assert forced["x_in_smem"] == 1
     big = workloads.llm(0.3, n=6144)   # ~4300 nonzeros per row > one stage (2048)
-    info = S.spmv_plan_inspect(big.row_ptr, big.col_idx, big.values, big.n_cols)
+    info = S.spmv_plan_inspect(big.row_ptr, big.col_idx, big.values, big.n_cols, options=tiles)
     assert info["rows_per_bin"] == [0, 0, 0, big.n_rows]   # split
+    # rows averaging >= 256 nonzeros take warp segments of <= 512 by default
+    info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols)
+    lengths = llm.row_lengths()
+    segs = -(-lengths // 512)
+    assert info["segments"] == 1 and info["n_tiles"] == segs.sum()
+    assert info["rows_per_bin"][3] == (segs > 1).sum()
+    assert info["x_in_smem"] == 1                            # 4 KB of fp16 x
+    assert info["algorithmic_bytes"] == (6 * llm.nnz + 4 * (llm.n_rows + 1)
+                                         + 2 * llm.n_cols + 4 * llm.n_rows)
     info = S.spmv_plan_inspect(llm.row_ptr, llm.col_idx, llm.values, llm.n_cols,
                                format="delta4")
     enc = oracle.delta_encode(llm.n_cols, llm.row_ptr, llm.col_idx, llm.values)

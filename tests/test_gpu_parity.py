@@ -127,6 +127,44 @@ def test_full_size_delta(name, fmt):
     assert_parity(m, y, TOL16)
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_csr_both_kernels(name, kernel):
+    """Each CSR kernel forced on every small shape: CTA tiles (1) and warp
+    segments (2, rows cut into slices of at most 512 nonzeros)."""
+    m = small(name)
+    y, info = run_gpu(m, options=S.spmv_plan_options(csr_kernel=kernel))
+    assert info["segments"] == (1 if kernel == 2 else 0)
+    assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("name", ["llm30", "llm90", "fem", "powerlaw"])
+def test_full_size_csr_both_kernels(name, kernel):
+    m = full(name)
+    y, info = run_gpu(m, options=S.spmv_plan_options(csr_kernel=kernel))
+    assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("x_smem", [0, 1])
+def test_csr_segments_edge_rows(x_smem):
+    """Warp segments on rows of 0, 1, 511, 512, 513, 1024 and 30,001
+    nonzeros, runs of empty rows, rows shared by several warps; repeated runs
+    are bit-identical (split counters re-arm), fp32 and fp16."""
+    longest, n_cols = (30001, 40000) if x_smem == 0 else (7001, 8000)  # fp16 x fits smem
+    lengths = np.array([0, 1, 511, 512, 513, 0, 0, 1024, longest, 7, 0] * 9 + [2047, 0])
+    opts = S.spmv_plan_options(csr_kernel=2, x_smem=x_smem)
+    for dtype, tol in ((np.float32, TOL32), (np.float16, TOL16)):
+        m = workloads.from_lengths("seg_edges", lengths, n_cols, seed=9, dtype=dtype)
+        ys, info = run_gpu(m, options=opts, repeat=3)
+        assert info["segments"] == 1 and info["n_split_rows"] > 0
+        if dtype == np.float16:
+            assert info["x_in_smem"] == x_smem
+        for y in ys:
+            assert_parity(m, y, tol)
+        assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
+
+
 # ------------------------------------------------------------ forced paths
 
 @pytest.mark.parametrize("kw", [
