@@ -209,10 +209,15 @@ typedef struct spmv_plan_options {
                             the row order; 0 chooses by the CV of the row
                             lengths as spmv_select_format does             */
   int32_t csr_kernel;    /* CSR: 0 auto (warp segments when rows average at
-                            least 256 nonzeros, else CTA tiles), 1 CTA tiles
+                            least 256 nonzeros; else mixed warp segments
+                            when the CV of the row lengths exceeds 2; else
+                            CTA tiles), 1 CTA tiles
                             (the bins above), 2 warp segments (rows cut into
                             slices of at most 512 nonzeros, each warp a
-                            contiguous share; [CSR] 4.1 warp per row)      */
+                            contiguous share; [CSR] 4.1 warp per row),
+                            3 mixed warp segments (runs of rows of at most
+                            128 nonzeros packed 256 nonzeros to a segment,
+                            [SPGEMM] 5.2; longer rows in slices of 256)    */
   int32_t reserved[5];
 } spmv_plan_options;
 

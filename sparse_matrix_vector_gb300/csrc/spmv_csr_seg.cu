@@ -1,11 +1,14 @@
-// CSR kernel for matrices with long rows (fp32 or fp16 values, int32
-// columns): y[row] = sum over the row's nonzeros of values[k] * x[col[k]]
-// ("CUDA CSR SpMV optimisation" 2.1), with the work laid out as for the
-// column-delta kernel.
+// CSR kernel with warp-owned segments (fp32 or fp16 values, int32 columns):
+// y[row] = sum over the row's nonzeros of values[k] * x[col[k]] ("CUDA CSR
+// SpMV optimisation" 2.1), with the work laid out as for the column-delta
+// kernel.
 //
-// The planner cuts every row into segments of at most kCsrSegNnz nonzeros
-// (full ones first) and gives each warp of the grid a contiguous share of the
-// segments, of equal weight. A segment's block (a 32-byte header, its
+// The planner cuts the rows into segments and gives each warp of the grid a
+// contiguous share of them, of equal weight. Long-row plans: every segment is
+// a slice of at most 512 nonzeros of one row (full ones first). Mixed plans
+// (irregular matrices): a run of consecutive rows of at most 256 nonzeros in
+// all is packed into one segment ("Hash-based multi-phase SpGEMM" 5.2,
+// batching tiny rows), longer rows are cut into slices of 256. A segment's block (a 32-byte header, its
 // columns, its values) is staged by one bulk copy into the warp's own ring of
 // shared-memory buffers; lane s of the warp issues the copies into buffer s,
 // so warps never wait for one another and no CTA barrier sits in the loop
@@ -16,8 +19,9 @@
 // neighbouring columns of the row ("CUDA CSR SpMV optimisation" 4.1: a warp
 // per row, shuffle reduction). fp16 values multiply fp16 x exactly in fp32
 // (mixed-precision fma); fp32 values use fp32 fma.
-// Rows: lanes keep fp32 partials; at a row's last segment, or the end of the
-// warp's share, the warp reduces them. A row inside one share is written at
+// Packed rows: the products are parked in shared memory and lane l sums rows
+// l, l + 32, ... of the run. Slices: lanes keep fp32 partials; at a row's
+// last segment, or the end of the warp's share, the warp reduces them. A row inside one share is written at
 // once; a row shared by several warps leaves one partial per warp, and the
 // warp whose atomicAdd completes the row's count adds them in warp order.
 #include <cuda_fp16.h>
@@ -35,14 +39,23 @@ namespace {
 #define SPMV_CSR_SEG_STAGES 2
 #endif
 constexpr int kCS = SPMV_CSR_SEG_STAGES;
-// Warps per CTA (one CTA per SM): the rings fill its shared memory.
-template <typename VT>
-constexpr int kCW = sizeof(VT) == 2 ? 28 : 24;
-constexpr int kSegK = kCsrSegNnz / 32;  // nonzeros per lane in a full segment
+// Warps per CTA (one CTA per SM). Long-row plans: the rings fill the shared
+// memory. Mixed plans gather x mostly at random: their rings stay near
+// 125 KB so that L1 keeps about 100 KB, which random gathers through L1 need
+// (with 28 KB of L1 they ran at half the rate). On the power-law matrix
+// (916k rows, 5.1M nonzeros) 24 or 32 warps, and packing rows of at most 32,
+// 64, 128 or 256 nonzeros, all measured 28.9-30.4 us: the kernel is bound by
+// the rate of random x gathers that miss L1 (~0.5 L2 requests per clock per
+// SM beside the matrix stream), not by their latency.
+template <typename VT, bool MIXED>
+constexpr int kCW = MIXED ? 24 : (sizeof(VT) == 2 ? 28 : 24);
 
-template <typename VT>
+template <typename VT, bool MIXED>
 struct CSeg {
-  static constexpr int kBytes = (int)csr_seg_bytes(kCsrSegNnz, (int)sizeof(VT));
+  static constexpr int kCap = MIXED ? kCsrSegNnzMixed : kCsrSegNnzLong;
+  static constexpr int kK = kCap / 32;  // nonzeros per lane in a full segment
+  static constexpr int kBytes =
+      (int)csr_seg_bytes(kCap, MIXED ? kCsrSegNnzMixed : 0, (int)sizeof(VT));
   static_assert(kBytes % 16 == 0, "segment buffers stay 16-byte aligned");
 };
 
@@ -68,6 +81,12 @@ __device__ __forceinline__ float fma_v(float acc, uint16_t a, uint16_t x) {
   return acc;
 }
 
+// a * x as fp32 (exact for fp16 operands).
+__device__ __forceinline__ float mul_v(float a, float x) { return a * x; }
+__device__ __forceinline__ float mul_v(uint16_t a, uint16_t x) {
+  return __half2float(__ushort_as_half(a)) * __half2float(__ushort_as_half(x));
+}
+
 template <typename VT> struct Bits;
 template <> struct Bits<float> { using T = float; };
 template <> struct Bits<__half> { using T = uint16_t; };
@@ -82,10 +101,9 @@ __device__ __forceinline__ typename Bits<VT>::T load_x(const typename Bits<VT>::
 
 // Copy x (n elements) into shared memory with every thread of the CTA.
 template <typename VT>
-__device__ __forceinline__ void copy_x(typename Bits<VT>::T* xs, const void* x, int n) {
+__device__ __forceinline__ void copy_x(typename Bits<VT>::T* xs, const void* x, int n, int nt) {
   using T = typename Bits<VT>::T;
   const T* src = static_cast<const T*>(x);
-  const int nt = kCW<VT> * 32;
   constexpr int per = 16 / (int)sizeof(T);
   int done = 0;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
@@ -118,11 +136,61 @@ __device__ __forceinline__ void finish_pieces(const CsrSegArgs& a, const int2 (&
   }
 }
 
-template <typename VT, bool XS>
-__global__ void __launch_bounds__(kCW<VT> * 32, 1) csr_seg_kernel(const CsrSegArgs a) {
+// A packed run of R whole rows: every lane forms the products of nonzeros
+// lane, lane + 32, ... (a warp-wide step gathers x for 32 consecutive
+// nonzeros) and parks them in place of the columns. Then, 32 rows at a time,
+// lane l sums row l of the group from there in nonzero order if it holds at
+// most kLaneRowMax nonzeros; the longer rows of the group are summed by the
+// whole warp one after another (strided partials, shuffle tree). y is
+// written once per row; the order of every sum is fixed.
+constexpr int kLaneRowMax = 32;
+
+template <typename VT, bool XS, int K>
+__device__ __forceinline__ void packed_rows(const CsrSegArgs& a, unsigned char* st, int R,
+                                            int nz, int row0, int lane,
+                                            const typename Bits<VT>::T* xs) {
   using T = typename Bits<VT>::T;
-  constexpr int W = kCW<VT>;
-  constexpr int kBytes = CSeg<VT>::kBytes;
+  const int16_t* rs = reinterpret_cast<const int16_t*>(st + kSegHeaderBytes);
+  unsigned char* cols = st + kSegHeaderBytes + (((R + 1) * 2 + 15) & ~15);
+  const int* s_col = reinterpret_cast<const int*>(cols);
+  const T* s_val = reinterpret_cast<const T*>(cols + ((nz * 4 + 15) & ~15));
+  float* s_prod = reinterpret_cast<float*>(cols);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int j = 32 * k + lane;
+    if (j < nz) s_prod[j] = mul_v(s_val[j], load_x<VT, XS>(xs, a.x, s_col[j]));
+  }
+  __syncwarp();
+  for (int q0 = 0; q0 < R; q0 += 32) {
+    const int q = q0 + lane;
+    int b = 0, e = 0;
+    if (q < R) {
+      b = rs[q];
+      e = rs[q + 1];
+    }
+    const bool wide = e - b > kLaneRowMax;
+    if (q < R && !wide) {
+      float sum = 0.f;
+      for (int j = b; j < e; ++j) sum += s_prod[j];
+      a.y[row0 + q] = sum;
+    }
+    for (unsigned m = __ballot_sync(0xffffffffu, wide); m != 0u; m &= m - 1u) {
+      const int src = __ffs(m) - 1;
+      const int bb = __shfl_sync(0xffffffffu, b, src), ee = __shfl_sync(0xffffffffu, e, src);
+      float v = 0.f;
+      for (int j = bb + lane; j < ee; j += 32) v += s_prod[j];
+      v = warp_sum(v);
+      if (lane == 0) a.y[row0 + q0 + src] = v;
+    }
+  }
+}
+
+template <typename VT, bool XS, bool MIXED>
+__global__ void __launch_bounds__(kCW<VT, MIXED> * 32, 1) csr_seg_kernel(const CsrSegArgs a) {
+  using T = typename Bits<VT>::T;
+  using Sg = CSeg<VT, MIXED>;
+  constexpr int W = kCW<VT, MIXED>;
+  constexpr int kBytes = Sg::kBytes;
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_full[W][kCS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -148,7 +216,7 @@ __global__ void __launch_bounds__(kCW<VT> * 32, 1) csr_seg_kernel(const CsrSegAr
   }
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();
-  if (XS) copy_x<VT>(xs, a.x, a.n_cols);
+  if (XS) copy_x<VT>(xs, a.x, a.n_cols, W * 32);
   for (int i = blockIdx.x * W * 32 + threadIdx.x; i < a.n_empty; i += gridDim.x * W * 32)
     a.y[__ldg(a.empty_rows + i)] = 0.f;
   if (XS) __syncthreads();
@@ -167,21 +235,36 @@ __global__ void __launch_bounds__(kCW<VT> * 32, 1) csr_seg_kernel(const CsrSegAr
       if (lane == 0) atomicExch(a.status, 1);
       break;
     }
-    const unsigned char* st = ring + s * kBytes;
-    const int4 h0 = *reinterpret_cast<const int4*>(st);       // -, row | flags, nonzeros, split
+    unsigned char* st = ring + s * kBytes;
+    const int4 h0 = *reinterpret_cast<const int4*>(st);       // rows, row | flags, nonzeros, split
     const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; slot
     const int nz = h0.z;
+    const uint32_t rf = (uint32_t)h0.y;
+    if (MIXED && (rf & kSegPacked)) {
+      packed_rows<VT, XS, Sg::kK>(a, st, h0.x, nz, (int)(rf & kSegRowMask), lane, xs);
+      __syncwarp();
+      if (lane == s && h1.y > 0) {
+        mbar_arrive_expect_tx(&s_full[warp][s], (uint32_t)h1.y);
+        bulk_g2s(ring + s * kBytes, a.blocks + (size_t)h1.x * 16, (uint32_t)h1.y,
+                 &s_full[warp][s], pol);
+      }
+      if (++s == kCS) {
+        s = 0;
+        phase ^= 1u;
+      }
+      continue;
+    }
     const int* s_col = reinterpret_cast<const int*>(st + kSegHeaderBytes);
     const T* s_val = reinterpret_cast<const T*>(st + kSegHeaderBytes + ((nz * 4 + 15) & ~15));
-    if (nz == kCsrSegNnz) {  // one straight-line block: all gathers can overlap
+    if (nz == Sg::kCap) {  // one straight-line block: all gathers can overlap
 #pragma unroll
-      for (int k = 0; k < kSegK; ++k) {
+      for (int k = 0; k < Sg::kK; ++k) {
         const int j = 32 * k + lane;
         acc[k & 3] = fma_v(acc[k & 3], s_val[j], load_x<VT, XS>(xs, a.x, s_col[j]));
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < kSegK; ++k) {
+      for (int k = 0; k < Sg::kK; ++k) {
         const int j = 32 * k + lane;
         if (j < nz) acc[k & 3] = fma_v(acc[k & 3], s_val[j], load_x<VT, XS>(xs, a.x, s_col[j]));
       }
@@ -193,7 +276,6 @@ __global__ void __launch_bounds__(kCW<VT> * 32, 1) csr_seg_kernel(const CsrSegAr
       bulk_g2s(ring + s * kBytes, a.blocks + (size_t)h1.x * 16, (uint32_t)h1.y, &s_full[warp][s],
                pol);
     }
-    const uint32_t rf = (uint32_t)h0.y;
     if ((rf & kSegLast) || i == n - 1) {  // the row ends, or this warp's share does
       const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -232,39 +314,52 @@ __global__ void __launch_bounds__(kCW<VT> * 32, 1) csr_seg_kernel(const CsrSegAr
   }
 }
 
-const void* csr_seg_entry(spmv_dtype dt, bool xs) {
+template <bool MIXED>
+const void* csr_seg_entry_m(spmv_dtype dt, bool xs) {
   if (dt == SPMV_F32)
-    return xs ? reinterpret_cast<const void*>(&csr_seg_kernel<float, true>)
-              : reinterpret_cast<const void*>(&csr_seg_kernel<float, false>);
-  return xs ? reinterpret_cast<const void*>(&csr_seg_kernel<__half, true>)
-            : reinterpret_cast<const void*>(&csr_seg_kernel<__half, false>);
+    return xs ? reinterpret_cast<const void*>(&csr_seg_kernel<float, true, MIXED>)
+              : reinterpret_cast<const void*>(&csr_seg_kernel<float, false, MIXED>);
+  return xs ? reinterpret_cast<const void*>(&csr_seg_kernel<__half, true, MIXED>)
+            : reinterpret_cast<const void*>(&csr_seg_kernel<__half, false, MIXED>);
+}
+
+const void* csr_seg_entry(spmv_dtype dt, bool xs, bool mixed) {
+  return mixed ? csr_seg_entry_m<true>(dt, xs) : csr_seg_entry_m<false>(dt, xs);
 }
 
 }  // namespace
 
-int csr_seg_warps_per_cta(spmv_dtype dt) { return dt == SPMV_F32 ? kCW<float> : kCW<__half>; }
+int csr_seg_warps_per_cta(spmv_dtype dt, bool mixed) {
+  if (mixed) return dt == SPMV_F32 ? kCW<float, true> : kCW<__half, true>;
+  return dt == SPMV_F32 ? kCW<float, false> : kCW<__half, false>;
+}
 
 int csr_seg_stages(spmv_dtype) { return kCS; }
 
-size_t csr_seg_rings_bytes(spmv_dtype dt) {
-  return dt == SPMV_F32 ? (size_t)kCW<float> * kCS * CSeg<float>::kBytes
-                        : (size_t)kCW<__half> * kCS * CSeg<__half>::kBytes;
+size_t csr_seg_rings_bytes(spmv_dtype dt, bool mixed) {
+  if (mixed)
+    return dt == SPMV_F32 ? (size_t)kCW<float, true> * kCS * CSeg<float, true>::kBytes
+                          : (size_t)kCW<__half, true> * kCS * CSeg<__half, true>::kBytes;
+  return dt == SPMV_F32 ? (size_t)kCW<float, false> * kCS * CSeg<float, false>::kBytes
+                        : (size_t)kCW<__half, false> * kCS * CSeg<__half, false>::kBytes;
 }
 
 int csr_seg_set_smem_limit(size_t dyn) {
   if (dyn == 0) return 0;
   for (spmv_dtype dt : {SPMV_F32, SPMV_F16})
     for (bool xs : {false, true})
-      if (cudaFuncSetAttribute(csr_seg_entry(dt, xs), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)dyn) != cudaSuccess)
-        return -1;
+      for (bool mixed : {false, true})
+        if (cudaFuncSetAttribute(csr_seg_entry(dt, xs, mixed),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dyn) != cudaSuccess)
+          return -1;
   return 0;
 }
 
-int csr_seg_occupancy(spmv_dtype dt, bool x_smem, size_t dyn_smem) {
+int csr_seg_occupancy(spmv_dtype dt, bool x_smem, bool mixed, size_t dyn_smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, csr_seg_entry(dt, x_smem),
-                                                    csr_seg_warps_per_cta(dt) * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, csr_seg_entry(dt, x_smem, mixed),
+                                                    csr_seg_warps_per_cta(dt, mixed) * 32,
                                                     dyn_smem) != cudaSuccess)
     return -1;
   return n;
@@ -286,8 +381,8 @@ int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream) {
   a.n_empty = p.n_empty_rows;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
-  return launch_pdl(csr_seg_entry(p.dtype, p.x_smem), p.grid, csr_seg_warps_per_cta(p.dtype) * 32,
-                    p.dyn_smem, stream, args);
+  return launch_pdl(csr_seg_entry(p.dtype, p.x_smem, p.csr_mixed), p.grid,
+                    csr_seg_warps_per_cta(p.dtype, p.csr_mixed) * 32, p.dyn_smem, stream, args);
 }
 
 }  // namespace spmv

@@ -157,7 +157,7 @@ Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype) {
   r.sell_sigma = 0;
   r.csr_kernel = 0;
   if (o) {
-    if (o->csr_kernel == 1 || o->csr_kernel == 2) r.csr_kernel = o->csr_kernel;
+    if (o->csr_kernel >= 1 && o->csr_kernel <= 3) r.csr_kernel = o->csr_kernel;
     if (o->interleave == 1 || o->interleave == 2) r.interleave = o->interleave;
     if (o->sell_sigma > 0) r.sell_sigma = o->sell_sigma;
     if (o->tile_nnz > 0) r.tile_nnz = std::min(o->tile_nnz, cap - 16);
@@ -374,16 +374,72 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
   return SPMV_OK;
 }
 
+// Deal out->segs to at most max_warps warps as contiguous shares of equal
+// weight, and set up the rows whose segments fall in more than one share: one
+// partial per such warp (its piece), combined by the last to arrive. Packed
+// segments (whole short rows) are never shared.
+spmv_status deal_segments(const std::function<int64_t(const SegDesc&)>& weight, int max_warps,
+                          int warps_per_cta, SegTables* out, spmv_plan_info* info) {
+  constexpr int64_t kMinShare = 256;  // weight a warp should get at least
+  const int64_t n_segs = (int64_t)out->segs.size();
+  if (n_segs > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+  int64_t total_w = 0;
+  for (const SegDesc& sg : out->segs) total_w += weight(sg);
+  const int64_t want = std::max<int64_t>(1, (total_w + kMinShare - 1) / kMinShare);
+  const int G = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)max_warps, want,
+                                                              std::max<int64_t>(n_segs, 1)}));
+  const int grid = (G + warps_per_cta - 1) / warps_per_cta;
+  const int n_warps = grid * warps_per_cta;
+  out->warp_first.assign((size_t)n_warps + 1, (int32_t)n_segs);
+  out->warp_first[0] = 0;
+  {
+    int64_t cum = 0;
+    int g = 1;
+    for (int64_t t = 0; t < n_segs; ++t) {
+      while (g < G && cum >= (int64_t)((__int128)g * total_w / G)) out->warp_first[g++] = (int32_t)t;
+      cum += weight(out->segs[(size_t)t]);
+    }
+    while (g < G) out->warp_first[g++] = (int32_t)n_segs;
+  }
+  out->seg_split.assign((size_t)n_segs, -1);
+  out->seg_slot.assign((size_t)n_segs, -1);
+  std::vector<int32_t> seg_warp((size_t)n_segs);
+  for (int g = 0; g < n_warps; ++g)
+    for (int32_t t = out->warp_first[g]; t < out->warp_first[g + 1]; ++t) seg_warp[t] = g;
+  for (int64_t t = 0; t < n_segs;) {
+    int64_t e = t + 1;
+    if (!(out->segs[(size_t)t].flags & kSegPacked))
+      while (e < n_segs && !(out->segs[(size_t)e].flags & kSegPacked) &&
+             out->segs[(size_t)e].row == out->segs[(size_t)t].row)
+        ++e;
+    if (seg_warp[t] != seg_warp[e - 1]) {
+      int32_t pieces = 0;
+      for (int64_t u = t; u < e; ++u) {
+        if (u > t && seg_warp[u] != seg_warp[u - 1]) ++pieces;
+        out->seg_slot[(size_t)u] = (int32_t)out->n_chunks + pieces;
+        out->seg_split[(size_t)u] = (int32_t)out->splits.size();
+      }
+      ++pieces;
+      if (out->n_chunks + pieces > kMaxIndex) return SPMV_ERR_TOO_LARGE;
+      out->splits.push_back({(int32_t)out->n_chunks, pieces, 0, 0});
+      out->n_chunks += pieces;
+    }
+    t = e;
+  }
+  info->n_tiles = n_segs;
+  info->n_split_rows = (int64_t)out->splits.size();
+  info->grid = grid;
+  return SPMV_OK;
+}
+
 spmv_status plan_segments(int32_t n_rows, const std::function<int64_t(int32_t)>& row_begin,
                           int64_t cap, int64_t seg_cost, int64_t entries_per_item,
                           int max_warps, int warps_per_cta, SegTables* out,
                           spmv_plan_info* info) {
   *out = SegTables();
-  constexpr int64_t kMinShare = 256;  // items a warp should get at least
   try {
-    // 1. cut every row into full segments of `cap` items and one shorter last
-    //    segment (full segments take the kernels' unpredicated path)
-    int64_t total_w = 0;
+    // cut every row into full segments of `cap` items and one shorter last
+    // segment (full segments take the kernels' unpredicated path)
     for (int32_t r = 0; r < n_rows; ++r) {
       const int64_t i0 = row_begin(r), i1 = row_begin(r + 1), ni = i1 - i0;
       if (ni == 0) {
@@ -399,61 +455,63 @@ spmv_status plan_segments(int32_t n_rows, const std::function<int64_t(int32_t)>&
         const int64_t sb = i0 + k * cap, se = std::min(sb + cap, i1);
         const uint32_t flags = (k == 0 ? kSegFirst : 0u) | (k == n_s - 1 ? kSegLast : 0u);
         out->segs.push_back({r, (int32_t)sb, (int32_t)se, 0, flags});
-        total_w += (se - sb) + seg_cost;
       }
       (n_s > 1 ? info->tiles_per_bin[3] : info->tiles_per_bin[2]) += n_s;
     }
-    const int64_t n_segs = (int64_t)out->segs.size();
-    if (n_segs > kMaxIndex) return SPMV_ERR_TOO_LARGE;
-    // 2. deal the segments to warps as contiguous shares of equal weight
-    const int64_t want = std::max<int64_t>(1, (total_w + kMinShare - 1) / kMinShare);
-    const int G = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)max_warps, want,
-                                                                std::max<int64_t>(n_segs, 1)}));
-    const int grid = (G + warps_per_cta - 1) / warps_per_cta;
-    const int n_warps = grid * warps_per_cta;
-    out->warp_first.assign((size_t)n_warps + 1, (int32_t)n_segs);
-    out->warp_first[0] = 0;
-    {
-      int64_t cum = 0;
-      int g = 1;
-      for (int64_t t = 0; t < n_segs; ++t) {
-        while (g < G && cum >= (int64_t)((__int128)g * total_w / G)) out->warp_first[g++] = (int32_t)t;
-        const SegDesc& sg = out->segs[(size_t)t];
-        cum += (int64_t)(sg.end - sg.begin) + seg_cost;
-      }
-      while (g < G) out->warp_first[g++] = (int32_t)n_segs;
-    }
-    // 3. rows whose segments fall in more than one warp's share: one partial
-    //    per such warp (its piece), combined by the last to arrive
-    out->seg_split.assign((size_t)n_segs, -1);
-    out->seg_slot.assign((size_t)n_segs, -1);
-    std::vector<int32_t> seg_warp((size_t)n_segs);
-    for (int g = 0; g < n_warps; ++g)
-      for (int32_t t = out->warp_first[g]; t < out->warp_first[g + 1]; ++t) seg_warp[t] = g;
-    for (int64_t t = 0; t < n_segs;) {
-      int64_t e = t + 1;
-      while (e < n_segs && out->segs[(size_t)e].row == out->segs[(size_t)t].row) ++e;
-      if (seg_warp[t] != seg_warp[e - 1]) {
-        int32_t pieces = 0;
-        for (int64_t u = t; u < e; ++u) {
-          if (u > t && seg_warp[u] != seg_warp[u - 1]) ++pieces;
-          out->seg_slot[(size_t)u] = (int32_t)out->n_chunks + pieces;
-          out->seg_split[(size_t)u] = (int32_t)out->splits.size();
-        }
-        ++pieces;
-        if (out->n_chunks + pieces > kMaxIndex) return SPMV_ERR_TOO_LARGE;
-        out->splits.push_back({(int32_t)out->n_chunks, pieces, 0, 0});
-        out->n_chunks += pieces;
-      }
-      t = e;
-    }
-    info->n_tiles = n_segs;
-    info->n_split_rows = (int64_t)out->splits.size();
-    info->grid = grid;
+    return deal_segments([&](const SegDesc& sg) { return (int64_t)(sg.end - sg.begin) + seg_cost; },
+                         max_warps, warps_per_cta, out, info);
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
   }
-  return SPMV_OK;
+}
+
+// Mixed plans pack rows of at most this many nonzeros (longer rows are cut
+// into slices of kCsrSegNnzMixed).
+constexpr int64_t kCsrPackRowMax = 128;
+
+spmv_status plan_csr_mixed_segments(const spmv_csr* m, int max_warps, int warps_per_cta,
+                                    SegTables* out, spmv_plan_info* info) {
+  *out = SegTables();
+  const int32_t* rp = m->row_ptr;
+  const int64_t cap = kCsrSegNnzMixed;
+  const int64_t pack_max = std::min<int64_t>(kCsrPackRowMax, cap);
+  try {
+    for (int32_t r = 0; r < m->n_rows;) {
+      const int64_t len = (int64_t)rp[r + 1] - rp[r];
+      if (len > pack_max) {  // a long row: slices of at most cap nonzeros
+        const int64_t n_s = (len + cap - 1) / cap;
+        info->rows_per_bin[n_s > 1 ? 3 : len > 256 ? 2 : 1] += 1;
+        for (int64_t k = 0; k < n_s; ++k) {
+          const int64_t sb = rp[r] + k * cap, se = std::min(sb + cap, (int64_t)rp[r + 1]);
+          const uint32_t flags = (k == 0 ? kSegFirst : 0u) | (k == n_s - 1 ? kSegLast : 0u);
+          out->segs.push_back({r, (int32_t)sb, (int32_t)se, 0, flags});
+        }
+        (n_s > 1 ? info->tiles_per_bin[3] : info->tiles_per_bin[2]) += n_s;
+        ++r;
+        continue;
+      }
+      // a run of whole rows (empty ones included), packed into one segment
+      const int32_t r0 = r;
+      int64_t nz = 0;
+      while (r < m->n_rows && r - r0 < cap) {
+        const int64_t l = (int64_t)rp[r + 1] - rp[r];
+        if (l > pack_max || nz + l > cap) break;
+        nz += l;
+        info->rows_per_bin[l > 8 ? 1 : 0] += 1;
+        ++r;
+      }
+      out->segs.push_back({r0, rp[r0], (int32_t)(rp[r0] + nz), r - r0, kSegPacked});
+      info->tiles_per_bin[0] += 1;
+    }
+    // a packed segment's weight counts its rows too (the row sums)
+    return deal_segments(
+        [](const SegDesc& sg) {
+          return (int64_t)(sg.end - sg.begin) + 32 + (sg.flags & kSegPacked ? 2 * sg.base : 0);
+        },
+        max_warps, warps_per_cta, out, info);
+  } catch (const std::bad_alloc&) {
+    return SPMV_ERR_OUT_OF_MEMORY;
+  }
 }
 
 spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
@@ -624,24 +682,38 @@ static bool csr_interleave_auto(const spmv_csr* m) {
 // CSR with warp segments: the auto rule and the plan.
 constexpr int64_t kCsrSegMinMeanRow = 256;  // rows averaging this many nonzeros or more
 
-bool csr_use_segments(const spmv_csr* m, const Options& o) {
-  if (o.csr_kernel != 0) return o.csr_kernel == 2;
-  return m->n_rows > 0 && m->nnz >= kCsrSegMinMeanRow * (int64_t)m->n_rows;
+// Irregular row lengths (CV of the row lengths above this) take mixed
+// segments: on the power-law matrix (CV 11.9) 28.9 us against 38.3 us for CTA
+// tiles; regular short rows keep the tiles (5-point Laplacian 10.9 us against
+// 15.2 us, hex-mesh stiffness 84 us against 164 us).
+constexpr double kCsrMixedMinCv = 2.0;
+double row_length_cv(const spmv_csr* m);
+
+// 1: CTA tiles, 2: warp segments (long rows), 3: mixed segments
+int csr_kernel_choice(const spmv_csr* m, const Options& o) {
+  if (o.csr_kernel != 0) return o.csr_kernel;
+  if (m->n_rows > 0 && m->nnz >= kCsrSegMinMeanRow * (int64_t)m->n_rows) return 2;
+  return row_length_cv(m) > kCsrMixedMinCv ? 3 : 1;
 }
 
 // Device layout of a CSR segment plan: one block per segment, back to back in
-// segment order, each a 32-byte header (SegHeader), the segment's columns
-// (padded to 16 bytes) and values (padded to 16 bytes).
+// segment order, each a 32-byte header (SegHeader), for a packed run of short
+// rows the rows' starts relative to the segment (int16), the segment's
+// columns (padded to 16 bytes) and values (padded to 16 bytes).
 spmv_status build_csr_seg_blocks(const spmv_csr* m, const SegTables& t, int stages,
                                  std::vector<uint4>* out, std::vector<int32_t>* seg_off) {
   const int vs = (int)dtype_size(m->value_dtype);
   const size_t n_segs = t.segs.size();
+  auto packed_rows = [&](const SegDesc& sg) -> int64_t {
+    return (sg.flags & kSegPacked) ? sg.base : 0;
+  };
   try {
     seg_off->assign(n_segs + 1, 0);
     int64_t total = 0;  // in 16-byte steps
     for (size_t k = 0; k < n_segs; ++k) {
       (*seg_off)[k] = (int32_t)total;
-      total += csr_seg_bytes((int64_t)t.segs[k].end - t.segs[k].begin, vs) / 16;
+      total += csr_seg_bytes((int64_t)t.segs[k].end - t.segs[k].begin, packed_rows(t.segs[k]),
+                             vs) / 16;
       if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
     }
     (*seg_off)[n_segs] = (int32_t)total;
@@ -649,35 +721,39 @@ spmv_status build_csr_seg_blocks(const spmv_csr* m, const SegTables& t, int stag
   } catch (const std::bad_alloc&) {
     return SPMV_ERR_OUT_OF_MEMORY;
   }
+  std::vector<int32_t> next(n_segs, -1);  // segment staged `stages` later by the same warp
+  for (size_t g = 0; g + 1 < t.warp_first.size(); ++g)
+    for (int32_t k = t.warp_first[g]; k + stages < t.warp_first[g + 1]; ++k) next[k] = k + stages;
   unsigned char* base = reinterpret_cast<unsigned char*>(out->data());
   const unsigned char* vals = static_cast<const unsigned char*>(m->values);
   for (size_t k = 0; k < n_segs; ++k) {
     const SegDesc& sg = t.segs[k];
-    const int64_t nz = (int64_t)sg.end - sg.begin;
+    const int64_t nz = (int64_t)sg.end - sg.begin, R = packed_rows(sg);
     unsigned char* b = base + (size_t)(*seg_off)[k] * 16;
     SegHeader h{};
+    h.base = (int32_t)R;
     h.row_flags = (uint32_t)sg.row | sg.flags;
     h.n_words = (int32_t)nz;
     h.split = t.seg_split[k];
     h.slot = t.seg_slot[k];
-    const size_t nk = k + (size_t)stages;  // staged S segments later by the same warp
-    const int32_t g_end = t.warp_first[(size_t)(std::upper_bound(t.warp_first.begin(),
-                                                                 t.warp_first.end(),
-                                                                 (int32_t)k) -
-                                                t.warp_first.begin())];
-    if ((int64_t)nk < g_end) {
-      h.next_off = (*seg_off)[nk];
-      h.next_bytes = ((*seg_off)[nk + 1] - (*seg_off)[nk]) * 16;
+    if (next[k] >= 0) {
+      h.next_off = (*seg_off)[next[k]];
+      h.next_bytes = ((*seg_off)[next[k] + 1] - (*seg_off)[next[k]]) * 16;
     }
     std::memcpy(b, &h, sizeof(h));
-    std::memcpy(b + kSegHeaderBytes, m->col_idx + sg.begin, (size_t)nz * 4);
-    std::memcpy(b + kSegHeaderBytes + delta_pad16(nz * 4), vals + (size_t)sg.begin * vs,
-                (size_t)nz * vs);
+    unsigned char* p = b + kSegHeaderBytes;
+    if (R > 0) {
+      int16_t* rs = reinterpret_cast<int16_t*>(p);
+      for (int64_t q = 0; q <= R; ++q) rs[q] = (int16_t)(m->row_ptr[sg.row + q] - sg.begin);
+      p += delta_pad16((R + 1) * 2);
+    }
+    std::memcpy(p, m->col_idx + sg.begin, (size_t)nz * 4);
+    std::memcpy(p + delta_pad16(nz * 4), vals + (size_t)sg.begin * vs, (size_t)nz * vs);
   }
   return SPMV_OK;
 }
 
-spmv_status create_csr_seg_plan(const spmv_csr* m, const Options& o, Plan* p) {
+spmv_status create_csr_seg_plan(const spmv_csr* m, const Options& o, bool mixed, Plan* p) {
   spmv_plan_info& info = p->info;
   spmv_status s;
   const size_t vs = dtype_size(m->value_dtype);
@@ -686,19 +762,21 @@ spmv_status create_csr_seg_plan(const spmv_csr* m, const Options& o, Plan* p) {
       cudaSuccess)
     return SPMV_ERR_CUDA;
   const size_t xbytes = ((size_t)m->n_cols * vs + 15) / 16 * 16;
-  const size_t rings = csr_seg_rings_bytes(m->value_dtype);
+  const size_t rings = csr_seg_rings_bytes(m->value_dtype, mixed);
   const bool fits = rings + xbytes + 4096 <= (size_t)optin;
   p->x_smem = o.x_smem == 0 ? false : o.x_smem == 1 ? fits : (fits && xbytes <= kXsAutoBytesDelta);
   p->dyn_smem = rings + (p->x_smem ? xbytes : 0);
   if (csr_seg_set_smem_limit(p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  const int occ = csr_seg_occupancy(m->value_dtype, p->x_smem, p->dyn_smem);
+  const int occ = csr_seg_occupancy(m->value_dtype, p->x_smem, mixed, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
-  const int wpc = csr_seg_warps_per_cta(m->value_dtype);
+  const int wpc = csr_seg_warps_per_cta(m->value_dtype, mixed);
   SegTables t;
-  if ((s = plan_segments(
-           m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; }, kCsrSegNnz, 64, 1,
-           std::min(occ, 1) * p->sm_count * wpc, wpc, &t, &info)) != SPMV_OK)
-    return s;
+  s = mixed ? plan_csr_mixed_segments(m, p->sm_count * wpc, wpc, &t, &info)
+            : plan_segments(
+                  m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; }, kCsrSegNnzLong,
+                  64, 1, p->sm_count * wpc, wpc, &t, &info);
+  if (s != SPMV_OK) return s;
+  p->csr_mixed = mixed;
   p->csr_segments = true;
   p->grid = info.grid;
   p->n_tiles = (int64_t)t.segs.size();
@@ -746,7 +824,8 @@ spmv_status create_csr_plan(const spmv_csr* m, const Options& o, Plan* p) {
   spmv_plan_info& info = p->info;
   spmv_status s;
   if ((s = bind_device(p)) != SPMV_OK) return s;
-  if (csr_use_segments(m, o)) return create_csr_seg_plan(m, o, p);
+  const int kernel = csr_kernel_choice(m, o);
+  if (kernel >= 2) return create_csr_seg_plan(m, o, kernel == 3, p);
   const size_t vs = dtype_size(m->value_dtype);
   const size_t xbytes = (size_t)m->n_cols * vs;
   p->x_smem = o.x_smem == 1 ? xbytes <= kXsMaxBytes
@@ -1383,18 +1462,22 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
     return s;
   }
   const size_t vsz = dtype_size(m->value_dtype);
-  if (csr_use_segments(m, o)) {
-    const int wpc = csr_seg_warps_per_cta(m->value_dtype);
+  const int kernel = csr_kernel_choice(m, o);
+  if (kernel >= 2) {
+    const bool mixed = kernel == 3;
+    const int wpc = csr_seg_warps_per_cta(m->value_dtype, mixed);
     SegTables t;
-    s = plan_segments(
-        m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; }, kCsrSegNnz, 64, 1,
-        kAssumedSms * wpc, wpc, &t, info);
+    s = mixed ? plan_csr_mixed_segments(m, kAssumedSms * wpc, wpc, &t, info)
+              : plan_segments(
+                    m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; },
+                    kCsrSegNnzLong, 64, 1, kAssumedSms * wpc, wpc, &t, info);
     if (s != SPMV_OK) return s;
     info->block = wpc * 32;
     info->segments = 1;
     info->n_entries = m->nnz;
     const size_t xbytes = ((size_t)m->n_cols * vsz + 15) / 16 * 16;
-    const bool fits = csr_seg_rings_bytes(m->value_dtype) + xbytes + 4096 <= kAssumedSmemOptin;
+    const bool fits =
+        csr_seg_rings_bytes(m->value_dtype, mixed) + xbytes + 4096 <= kAssumedSmemOptin;
     info->x_in_smem = o.x_smem == 0 ? 0 : o.x_smem == 1 ? fits : (fits && xbytes <= kXsAutoBytesDelta);
     info->launches_per_run = m->n_rows > 0;
     info->matrix_bytes = m->nnz * (int64_t)(vsz + 4) + ((int64_t)m->n_rows + 1) * 4;

@@ -66,7 +66,8 @@ constexpr int64_t delta_seg_bytes(int bits, int64_t n_w) {
 }
 // Segment header (DELTA, and CSR with long rows), the first 32 bytes of its
 // block:
-//   base       DELTA: column before the segment's first entry (CSR: 0)
+//   base       DELTA: column before the segment's first entry; CSR: rows of
+//              a packed run (0 for a slice)
 //   row_flags  row | kSegFirst (first segment of the row) | kSegLast (last)
 //   n_words    items in the segment (DELTA: packed words; CSR: nonzeros)
 //   split      index into the split table when the row's segments are shared
@@ -85,15 +86,26 @@ struct SegHeader {
   int32_t reserved;
 };
 static_assert(sizeof(SegHeader) == kSegHeaderBytes, "segment header is 32 bytes");
-// CSR segments: at most kCsrSegNnz nonzeros of one row; the block is the
-// header, the columns (padded to 16 bytes) and the values (padded to 16).
-constexpr int kCsrSegNnz = 512;
-constexpr int64_t csr_seg_bytes(int64_t nnz, int value_bytes) {
-  return kSegHeaderBytes + delta_pad16(nnz * 4) + delta_pad16(nnz * value_bytes);
-}
 constexpr uint32_t kSegFirst = 1u << 31;
 constexpr uint32_t kSegLast = 1u << 30;
-constexpr uint32_t kSegRowMask = (1u << 30) - 1u;
+constexpr uint32_t kSegPacked = 1u << 29;  // CSR: a run of whole short rows (see below)
+constexpr uint32_t kSegRowMask = (1u << 29) - 1u;
+// CSR segments, two plans:
+//  long rows  -- every segment a slice of at most kCsrSegNnzLong nonzeros of
+//                one row;
+//  mixed rows -- runs of consecutive rows (at most kCsrSegNnzMixed nonzeros
+//                and as many rows in all) packed into one segment
+//                (kSegPacked; base = rows), and slices of at most
+//                kCsrSegNnzMixed of the rows longer than that.
+// A block is the header, for a packed segment its rows' starts relative to
+// the segment (int16, rows + 1, padded to 16 bytes), the columns (padded to
+// 16 bytes) and the values (padded to 16 bytes).
+constexpr int kCsrSegNnzLong = 512;
+constexpr int kCsrSegNnzMixed = 256;
+constexpr int64_t csr_seg_bytes(int64_t nnz, int64_t packed_rows, int value_bytes) {
+  return kSegHeaderBytes + (packed_rows ? delta_pad16((packed_rows + 1) * 2) : 0) +
+         delta_pad16(nnz * 4) + delta_pad16(nnz * value_bytes);
+}
 
 // Tile descriptor (one int4 per work unit of the CSR kernel).
 //   short-row tile: {row_begin, nnz_begin, nnz_end, KIND_STREAM | WALK? | lg << 16 | rows}
@@ -140,7 +152,7 @@ struct Options {
   int lanes_log2;  // lanes mode when forced
   int interleave;  // CSR products: 0 auto, 1 chunks of 8, 2 element-interleaved
   int sell_sigma;  // SELL sorting window, 0: by the CV of the row lengths
-  int csr_kernel;  // CSR: 0 auto, 1 CTA tiles, 2 warp segments
+  int csr_kernel;  // CSR: 0 auto, 1 CTA tiles, 2 warp segments (long rows), 3 mixed
 };
 
 Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype);
@@ -189,6 +201,8 @@ spmv_status plan_segments(int32_t n_rows, const std::function<int64_t(int32_t)>&
                           spmv_plan_info* info);
 spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_per_cta,
                                 SegTables* out, spmv_plan_info* info);
+spmv_status plan_csr_mixed_segments(const spmv_csr* m, int max_warps, int warps_per_cta,
+                                    SegTables* out, spmv_plan_info* info);
 
 // Device resources of a plan.
 struct Plan {
@@ -201,7 +215,8 @@ struct Plan {
   bool x_smem = false;
   int delta_bits = 4;          // DELTA: bits per column delta (2, 4 or 8)
   bool interleaved = false;  // CSR: products element-interleaved over the CTA
-  bool csr_segments = false;  // CSR: warp-owned row segments (long rows)
+  bool csr_segments = false;  // CSR: warp-owned row segments
+  bool csr_mixed = false;     // CSR segments: packed short rows + slices of long ones
   bool x_aligned16 = false;
   int grid = 0;
   size_t dyn_smem = 0;
@@ -259,12 +274,12 @@ size_t delta_x_smem_bytes(int n_cols);
 int delta_set_smem_limit(int bits, size_t dyn);
 int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem);
 int launch_csr(const Plan& p, const void* x, float* y, void* stream);
-// CSR with long rows (spmv_csr_seg.cu): warp-owned segments, as DELTA.
-int csr_seg_warps_per_cta(spmv_dtype dtype);
+// CSR with warp-owned segments (spmv_csr_seg.cu), long-row or mixed plans.
+int csr_seg_warps_per_cta(spmv_dtype dtype, bool mixed);
 int csr_seg_stages(spmv_dtype dtype);
-size_t csr_seg_rings_bytes(spmv_dtype dtype);
+size_t csr_seg_rings_bytes(spmv_dtype dtype, bool mixed);
 int csr_seg_set_smem_limit(size_t dyn);
-int csr_seg_occupancy(spmv_dtype dtype, bool x_smem, size_t dyn_smem);
+int csr_seg_occupancy(spmv_dtype dtype, bool x_smem, bool mixed, size_t dyn_smem);
 int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
 int launch_sell(const Plan& p, const void* x, float* y, void* stream);

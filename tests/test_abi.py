@@ -219,7 +219,7 @@ def expected_bins(lengths, opts):
                                 {"tile_nnz": 300, "tile_rows": 64}])
 def test_planner_bins(spmv_lib, kw):
     m = workloads.powerlaw(n=40000, nnz=223000, max_len=2500)
-    opts = S.spmv_plan_options(**kw)
+    opts = S.spmv_plan_options(csr_kernel=1, **kw)
     info = S.spmv_plan_inspect(m.row_ptr, m.col_idx, m.values, m.n_cols,
                                options=opts)
     L = m.row_lengths()
@@ -244,12 +244,23 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
     assert info["rows_per_bin"] == [lap.n_rows, 0, 0, 0]   # sub-warp
     assert info["walk_tiles"] == 0                           # regular rows: lanes mode
     pl = workloads.powerlaw(n=300000, nnz=1_670_000, max_len=2500)
-    info = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols)
+    info = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols,
+                               options=S.spmv_plan_options(csr_kernel=1))
     assert info["walk_tiles"] > 0                            # irregular rows: walk mode
     for reduce, walk in ((1, 0), (2, info["tiles_per_bin"][0])):
         forced = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols,
-                                     options=S.spmv_plan_options(reduce=reduce, lanes=4))
+                                     options=S.spmv_plan_options(reduce=reduce, lanes=4,
+                                                                 csr_kernel=1))
         assert forced["walk_tiles"] == walk
+    # by default the irregular rows (CV > 2) take mixed warp segments: runs of
+    # rows of at most 128 nonzeros packed 256 to a segment, longer rows sliced
+    info = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols)
+    assert info["segments"] == 1
+    L = pl.row_lengths()
+    long_rows = L[L > 128]
+    assert info["tiles_per_bin"][2] + info["tiles_per_bin"][3] == (-(-long_rows // 256)).sum()
+    assert info["rows_per_bin"][1] + info["rows_per_bin"][2] + info["rows_per_bin"][3] >= \
+        long_rows.size
     fem = workloads.fem(6, 5, 4)
     info = S.spmv_plan_inspect(fem.row_ptr, fem.col_idx, fem.values, fem.n_cols)
     assert info["rows_per_bin"] == [0, fem.n_rows, 0, 0]   # warp

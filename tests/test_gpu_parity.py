@@ -127,23 +127,43 @@ def test_full_size_delta(name, fmt):
     assert_parity(m, y, TOL16)
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_small_csr_both_kernels(name, kernel):
-    """Each CSR kernel forced on every small shape: CTA tiles (1) and warp
-    segments (2, rows cut into slices of at most 512 nonzeros)."""
+def test_small_csr_every_kernel(name, kernel):
+    """Each CSR kernel forced on every small shape: CTA tiles (1), warp
+    segments (2, rows cut into slices of at most 512 nonzeros) and mixed warp
+    segments (3, runs of short rows packed, longer rows in slices of 256)."""
     m = small(name)
     y, info = run_gpu(m, options=S.spmv_plan_options(csr_kernel=kernel))
-    assert info["segments"] == (1 if kernel == 2 else 0)
+    assert info["segments"] == (1 if kernel >= 2 else 0)
     assert_parity(m, y, tol_for(m))
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
-@pytest.mark.parametrize("name", ["llm30", "llm90", "fem", "powerlaw"])
-def test_full_size_csr_both_kernels(name, kernel):
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("name", ["laplacian", "llm30", "llm90", "fem", "powerlaw"])
+def test_full_size_csr_every_kernel(name, kernel):
     m = full(name)
     y, info = run_gpu(m, options=S.spmv_plan_options(csr_kernel=kernel))
     assert_parity(m, y, tol_for(m))
+
+
+@pytest.mark.parametrize("x_smem", [0, 1])
+def test_csr_mixed_segments_edge_rows(x_smem):
+    """Packed runs: 300 empty rows in a row (more than one run), rows of 16
+    (summed by one lane) and 17 to 256 (summed by the warp) nonzeros, a run
+    ending exactly at 256 nonzeros, rows of 257+ (sliced) between runs, an
+    empty last row; fp32 and fp16, repeated runs bit-identical."""
+    lengths = np.concatenate([[0] * 300, [32] * 8, [16, 17], [1] * 7, [31, 1], [256, 600, 0, 5],
+                              np.tile([1, 2, 0, 16, 32, 257, 3, 100, 200], 20), [1000, 4], [0]])
+    opts = S.spmv_plan_options(csr_kernel=3, x_smem=x_smem)
+    for dtype, tol in ((np.float32, TOL32), (np.float16, TOL16)):
+        m = workloads.from_lengths("packed_edges", lengths, 3000, seed=4, dtype=dtype)
+        ys, info = run_gpu(m, options=opts, repeat=3)
+        assert info["segments"] == 1
+        assert info["x_in_smem"] == x_smem
+        for y in ys:
+            assert_parity(m, y, tol)
+        assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
 
 
 @pytest.mark.parametrize("x_smem", [0, 1])
@@ -183,7 +203,7 @@ def test_csr_segments_edge_rows(x_smem):
 ])
 def test_forced_planner_paths(kw):
     m = workloads.powerlaw(n=30000, nnz=167000, max_len=3000, seed=11)
-    opts = S.spmv_plan_options(**kw)
+    opts = S.spmv_plan_options(csr_kernel=1, **kw)   # the CTA-tile planner's knobs
     y, info = run_gpu(m, options=opts)
     assert_parity(m, y, TOL32)
 
@@ -195,7 +215,7 @@ def test_forced_planner_paths(kw):
                                 {"interleave": 2}, {"interleave": 1}])
 def test_forced_paths_fp16_csr(kw):
     m = workloads.llm(0.8, n=1000, seed=3)
-    y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
+    y, _ = run_gpu(m, options=S.spmv_plan_options(csr_kernel=1, **kw))
     assert_parity(m, y, TOL16)
 
 
@@ -299,7 +319,7 @@ def test_unaligned_row_starts_every_length():
     lengths = np.tile(np.arange(41), 30)
     m = workloads.from_lengths("ragged", lengths, 4096, seed=21)
     for kw in ({}, {"tile_nnz": 40}, {"tile_rows": 3}, {"cta_row_min": 8},
-               {"reduce": 2}, {"reduce": 1, "lanes": 2}):
+               {"reduce": 2}, {"reduce": 1, "lanes": 2}, {"csr_kernel": 2}, {"csr_kernel": 3}):
         y, _ = run_gpu(m, options=S.spmv_plan_options(**kw))
         assert_parity(m, y, TOL32)
 
@@ -368,7 +388,7 @@ def test_delta_plan_rejects_bad_columns():
 def test_repeated_runs_identical_and_split_counters_rearm():
     m = workloads.powerlaw(n=20000, nnz=111000, max_len=3000, seed=2)
     ys, info = run_gpu(m, options=S.spmv_plan_options(cta_row_min=200, split_row_min=300,
-                                                      split_chunk=100),
+                                                      split_chunk=100, csr_kernel=1),
                        repeat=4)
     assert info["rows_per_bin"][3] > 0
     for y in ys[1:]:
