@@ -59,6 +59,7 @@ struct CsrArgs {
   int32_t* counters;
   int split_chunk;
   int32_t* status;
+  const int* skip;  // when set and nonzero at launch: do nothing (a finished solve)
 };
 
 // Shared-memory stage of one work unit: the columns and values of its
@@ -489,6 +490,11 @@ __global__ void __launch_bounds__(kThreads, kCsrCtasPerSm<VT>) csr_kernel(const 
   // no kernel writes); x, y and the split scratch are touched only after the
   // kernels this launch depends on have completed.
   pdl_wait();
+  if (a.skip && *a.skip) {  // let the copies issued above land, then leave
+    if (tid == 0)
+      for (int s = 0; s < kStages; ++s) mbar_wait_bounded(&s_bar[s], 0u);
+    return;
+  }
   if (XS) stage_x<XT>(xs, static_cast<const XT*>(a.x), a.n_cols);
   bool aborted = false;
   float row_acc = 0.f;  // this thread's share of the current split-row piece
@@ -591,9 +597,10 @@ int csr_set_smem_limit(size_t dyn) {
   return 0;
 }
 
-int launch_csr(const Plan& p, const void* x, float* y, void* stream) {
+int launch_csr(const Plan& p, const void* x, float* y, void* stream, const int* skip) {
   if (p.n_tiles == 0) return 0;
   CsrArgs a;
+  a.skip = skip;
   a.row_ptr = p.row_ptr;
   a.col = p.col_idx;
   a.val = p.values;

@@ -70,6 +70,7 @@ struct CsrSegArgs {
   float* partials;
   int32_t* counters;
   int32_t* status;
+  const int* skip;  // when set and nonzero at launch: do nothing (a finished solve)
   int n_empty;
   int n_cols;
 };
@@ -216,6 +217,10 @@ __global__ void __launch_bounds__(kCW<VT, MIXED> * 32, 1) csr_seg_kernel(const C
   }
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();
+  if (a.skip && *a.skip) {  // let the copies issued above land, then leave
+    if (lane < kCS && lane < n) mbar_wait_bounded(&s_full[warp][lane], 0u);
+    return;
+  }
   if (XS) copy_x<VT>(xs, a.x, a.n_cols, W * 32);
   for (int i = blockIdx.x * W * 32 + threadIdx.x; i < a.n_empty; i += gridDim.x * W * 32)
     a.y[__ldg(a.empty_rows + i)] = 0.f;
@@ -365,9 +370,10 @@ int csr_seg_occupancy(spmv_dtype dt, bool x_smem, bool mixed, size_t dyn_smem) {
   return n;
 }
 
-int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream) {
+int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream, const int* skip) {
   if (p.grid == 0) return 0;
   CsrSegArgs a;
+  a.skip = skip;
   a.blocks = p.blocks;
   a.seg_off = p.seg_off;
   a.warp_first = p.cta_first;

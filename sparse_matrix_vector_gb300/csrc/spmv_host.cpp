@@ -594,6 +594,7 @@ void free_plan(spmv_plan* plan) {
     DeviceGuard g(p->device);
     for (void* g : p->pcg_exec)
       if (g) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(g));
+    if (p->pcg_loop) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->pcg_loop));
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
@@ -1240,6 +1241,17 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   return SPMV_OK;
 }
 
+// The plan's y = A x launch (skip: see launch_csr; dot: see launch_sell,
+// SELL and FEM plans only).
+int launch_product(const Plan& p, const void* x, float* y, void* stream, const int* skip,
+                   float* dot = nullptr) {
+  return p.format == SPMV_FORMAT_CSR    ? (p.csr_segments ? launch_csr_seg(p, x, y, stream, skip)
+                                                         : launch_csr(p, x, y, stream, skip))
+         : p.format == SPMV_FORMAT_SELL ? launch_sell(p, x, y, stream, skip, dot)
+         : p.format == SPMV_FORMAT_FEM  ? launch_fem(p, x, y, stream, skip, dot)
+                                        : launch_delta(p, x, y, stream);
+}
+
 }  // namespace
 }  // namespace spmv
 
@@ -1694,12 +1706,19 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
     return SPMV_OK;
   }
   spmv_status s;
-  if (!p.pcg_work && (s = dev_alloc(&p.pcg_work, pcg_work_bytes(p.n_rows))) != SPMV_OK) return s;
+  if (!p.pcg_work &&
+      (s = dev_alloc(&p.pcg_work, pcg_work_bytes(p.n_rows, p.grid))) != SPMV_OK)
+    return s;
   const size_t vec = ((size_t)p.n_rows * 4 + 255) / 256 * 256;
   float* pv = reinterpret_cast<float*>(p.pcg_work + 2 * vec);
   float* qv = reinterpret_cast<float*>(p.pcg_work + 3 * vec);
   PcgScalars* sc_dev =
-      reinterpret_cast<PcgScalars*>(p.pcg_work + 4 * vec + 3 * kPcgBlocks * sizeof(double));
+      reinterpret_cast<PcgScalars*>(p.pcg_work + 4 * vec + 3 * kPcgBlocks * sizeof(float));
+  // SELL and FEM products also hand over p . q per CTA: no step-length kernel
+  const bool fused = pcg_fused_dot(p);
+  float* pq_dev = fused ? reinterpret_cast<float*>(p.pcg_work + 4 * vec +
+                                                   3 * kPcgBlocks * sizeof(float) + 256)
+                        : nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   PcgScalars sc{};
   sc.tol2 = rel_tol * rel_tol;
@@ -1712,11 +1731,12 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
   // solves stop within a few iterations of convergence, long ones pay one
   // host check per check_every iterations.
   const int full = check_every > 0 ? check_every : 16;
+  // the products skip themselves once the solve is done (the device flag)
+  const int* done_flag = &sc_dev->done;
   auto enqueue_batch = [&](int n_it) -> spmv_status {
     for (int k = 0; k < n_it; ++k) {
-      spmv_status e = spmv_run(plan, pv, qv, stream);  // q = A p
-      if (e != SPMV_OK) return e;
-      for (int stage = 1; stage <= 3; ++stage)
+      if (launch_product(p, pv, qv, stream, done_flag, pq_dev) != 0) return SPMV_ERR_CUDA;
+      for (int stage = fused ? 2 : 1; stage <= 3; ++stage)
         if (launch_pcg(stage, p, b, x, d, stream) != 0) return SPMV_ERR_CUDA;
     }
     return SPMV_OK;
@@ -1737,7 +1757,64 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
       p.pcg_exec[g] = nullptr;
       p.pcg_batch[g] = 0;
     }
+    if (p.pcg_loop) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p.pcg_loop));
+    p.pcg_loop = nullptr;
+    p.pcg_loop_failed = false;
     for (int q = 0; q < 3; ++q) p.pcg_key[q] = key[q];
+  }
+  // The whole loop on the device: a graph whose while node runs one
+  // iteration (product and three vector kernels) as long as the direction
+  // kernel says so (it stops the loop on convergence, the iteration limit or
+  // a breakdown), so the host waits once per solve and no iteration runs
+  // past the end. Built once per b, x and diag; a device or driver that
+  // refuses it leaves the batches below.
+  if (graphable && !p.pcg_loop && !p.pcg_loop_failed) {
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaGraphConditionalHandle h = 0;
+    bool ok = cudaGraphCreate(&g, 0) == cudaSuccess &&
+              cudaGraphConditionalHandleCreate(&h, g, 1, cudaGraphCondAssignDefault) ==
+                  cudaSuccess;
+    cudaGraphNodeParams np{};
+    cudaGraphNode_t node = nullptr;
+    if (ok) {
+      np.type = cudaGraphNodeTypeConditional;
+      np.conditional.handle = h;
+      np.conditional.type = cudaGraphCondTypeWhile;
+      np.conditional.size = 1;
+      ok = cudaGraphAddNode(&node, g, nullptr, nullptr, 0, &np) == cudaSuccess;
+    }
+    if (ok) {
+      cudaGraph_t body = np.conditional.phGraph_out[0];
+      ok = cudaStreamBeginCaptureToGraph(st, body, nullptr, nullptr, 0,
+                                         cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+      if (ok) {
+        const bool launched = launch_product(p, pv, qv, stream, done_flag, pq_dev) == 0 &&
+                              (fused || launch_pcg(1, p, b, x, d, stream) == 0) &&
+                              launch_pcg(2, p, b, x, d, stream) == 0 &&
+                              launch_pcg(3, p, b, x, d, stream, (unsigned long long)h) == 0;
+        ok = cudaStreamEndCapture(st, &body) == cudaSuccess && launched;
+      }
+    }
+    if (ok) ok = cudaGraphInstantiate(&exec, g, 0) == cudaSuccess;
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    if (ok && exec) {
+      p.pcg_loop = exec;
+    } else {
+      if (exec) cudaGraphExecDestroy(exec);
+      p.pcg_loop_failed = true;
+    }
+  }
+  if (p.pcg_loop && max_iter > 0) {
+    if (cudaGraphLaunch(static_cast<cudaGraphExec_t>(p.pcg_loop), st) != cudaSuccess ||
+        cudaMemcpyAsync(&sc, sc_dev, sizeof(sc), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return SPMV_ERR_CUDA;
+    result->iterations = sc.iter;
+    result->status = sc.done ? sc.done : kPcgMaxIter;
+    result->rel_residual = sc.bb > 0 ? std::sqrt(sc.rr / sc.bb) : std::sqrt(sc.rr);
+    return SPMV_OK;
   }
   // the graph of a batch length, captured on first use (null: launch directly)
   auto graph_for = [&](int n_it) -> cudaGraphExec_t {
@@ -1767,10 +1844,14 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
     return exec;
   };
   for (int64_t it = 0;;) {
-    if (cudaMemcpyAsync(&sc, sc_dev, sizeof(sc), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-      return SPMV_ERR_CUDA;
-    if (sc.done || it >= max_iter) break;
+    // the first batch goes out unchecked: if x0 already solves the system,
+    // the device flag makes it a run of no-ops
+    if (it > 0 || max_iter <= 0) {
+      if (cudaMemcpyAsync(&sc, sc_dev, sizeof(sc), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess)
+        return SPMV_ERR_CUDA;
+      if (sc.done || it >= max_iter) break;
+    }
     const int n_it = it == 0 ? std::min(4, full) : (it == std::min(4, full) ? std::min(8, full) : full);
     cudaGraphExec_t exec = graph_for(n_it);
     if (exec) {
@@ -1816,11 +1897,7 @@ spmv_status spmv_run(spmv_plan* plan, const void* x, float* y, void* stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
   if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
   if (p.n_rows == 0) return SPMV_OK;
-  int rc = p.format == SPMV_FORMAT_CSR    ? (p.csr_segments ? launch_csr_seg(p, x, y, stream)
-                                                             : launch_csr(p, x, y, stream))
-           : p.format == SPMV_FORMAT_SELL ? launch_sell(p, x, y, stream)
-           : p.format == SPMV_FORMAT_FEM  ? launch_fem(p, x, y, stream)
-                                          : launch_delta(p, x, y, stream);
+  int rc = launch_product(p, x, y, stream, nullptr);
   return rc == 0 ? SPMV_OK : SPMV_ERR_CUDA;
 }
 

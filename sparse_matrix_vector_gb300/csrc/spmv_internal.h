@@ -47,6 +47,7 @@ constexpr int kPcgConverged = 1, kPcgMaxIter = 2, kPcgBreakdown = 3;
 // Device-side scalars of a conjugate-gradient solve.
 struct PcgScalars {
   double rz, rr, bb, alpha, beta, tol2;
+  double rz_prev;  // rz at the start of the current iteration
   int iter, max_iter, done, arrived;
 };
 // DELTA kernel ("MACKO-SpMV" 2.2): rows are cut into segments of at most
@@ -250,6 +251,10 @@ struct Plan {
   void* pcg_exec[kPcgGraphs] = {nullptr, nullptr, nullptr};
   int pcg_batch[kPcgGraphs] = {0, 0, 0};
   const void* pcg_key[3] = {nullptr, nullptr, nullptr};
+  // the whole iteration loop as one graph with a device-side while node
+  // (cudaGraphExec_t), for the same b, x and diag as pcg_key
+  void* pcg_loop = nullptr;
+  bool pcg_loop_failed = false;
   float fem_k0[24 * 24] = {};
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
@@ -273,21 +278,35 @@ size_t delta_rings_bytes(int bits);      // every stage of every warp of a CTA
 size_t delta_x_smem_bytes(int n_cols);
 int delta_set_smem_limit(int bits, size_t dyn);
 int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem);
-int launch_csr(const Plan& p, const void* x, float* y, void* stream);
+// `skip`: a device flag read at launch (after the kernels the launch depends
+// on); when it is set the product is skipped (conjugate gradients, after
+// convergence). nullptr for ordinary runs.
+int launch_csr(const Plan& p, const void* x, float* y, void* stream, const int* skip = nullptr);
 // CSR with warp-owned segments (spmv_csr_seg.cu), long-row or mixed plans.
 int csr_seg_warps_per_cta(spmv_dtype dtype, bool mixed);
 int csr_seg_stages(spmv_dtype dtype);
 size_t csr_seg_rings_bytes(spmv_dtype dtype, bool mixed);
 int csr_seg_set_smem_limit(size_t dyn);
 int csr_seg_occupancy(spmv_dtype dtype, bool x_smem, bool mixed, size_t dyn_smem);
-int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream);
+int launch_csr_seg(const Plan& p, const void* x, float* y, void* stream,
+                   const int* skip = nullptr);
 int launch_delta(const Plan& p, const void* x, float* y, void* stream);
-int launch_sell(const Plan& p, const void* x, float* y, void* stream);
-int launch_fem(const Plan& p, const void* x, float* y, void* stream);
+// `dot` (SELL and FEM plans, square): when set, every CTA also writes its
+// rows' x . y to dot[blockIdx] (the step length of conjugate gradients).
+int launch_sell(const Plan& p, const void* x, float* y, void* stream, const int* skip = nullptr,
+                float* dot = nullptr);
+int launch_fem(const Plan& p, const void* x, float* y, void* stream, const int* skip = nullptr,
+               float* dot = nullptr);
 // Conjugate gradients (spmv_pcg.cu): workspace bytes for n unknowns, and one
 // of its kernels (stage 0 init, 1 step length, 2 updates, 3 direction).
-size_t pcg_work_bytes(int n);
+size_t pcg_work_bytes(int n, int product_grid);
+// Whether the plan's product kernel can hand over p . q itself (SELL, FEM).
+inline bool pcg_fused_dot(const Plan& p) {
+  return p.format == SPMV_FORMAT_SELL || p.format == SPMV_FORMAT_FEM;
+}
+// `cond`: a conditional-node handle that the direction kernel sets to 0 once
+// the solve is done and to 1 otherwise (0: no conditional node).
 int launch_pcg(int stage, const Plan& p, const float* b, float* x, const float* diag,
-               void* stream);
+               void* stream, unsigned long long cond = 0);
 
 }  // namespace spmv

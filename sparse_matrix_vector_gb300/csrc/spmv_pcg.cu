@@ -5,13 +5,14 @@
 // One iteration is the plan's y = A x launch followed by three small kernels
 // (step length, updates, new direction). Vectors are fp32; the scalars of
 // the recurrence live in device memory in fp64, so the host never waits
-// inside an iteration. Dot products are reduced in two fixed-order levels
-// (per block; then the block partials by whichever block finishes last, each
-// of its threads a fixed stride of them before a fixed-order block sum), so a
-// solve gives the same bits every time. Once the
+// inside an iteration. Dot products are reduced in two fixed-order levels:
+// per block, parked in a partials array, then summed by every block of the
+// next kernel in the same fixed order (each thread a fixed stride, then a
+// fixed-order block sum), so a solve gives the same bits every time and no
+// kernel ends with one block reducing while the rest of the GPU idles. Once the
 // residual test passes (or the iteration limit or a breakdown is hit) a
-// device flag turns the remaining kernels of a batch into no-ops, and the
-// host only reads the scalars between batches.
+// device flag turns the remaining kernels of a batch, the products included,
+// into no-ops, and the host only reads the scalars between batches.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,28 +31,41 @@ struct PcgVectors {
   float* __restrict__ p;
   float* __restrict__ q;
   const float* __restrict__ diag;
-  double* partials;  // 3 * kPcgBlocks
+  float* partials;  // 3 * kPcgBlocks
+  const float* pq_parts;  // per-block p . q: partials, or the product kernel's
+  int pq_count;           // how many
   PcgScalars* sc;
+  unsigned long long cond;  // while-node handle set by pcg_direction (0: none)
   int n;
 };
 
-// Fixed-order sums of up to three per-thread values over the block; thread 0
-// gets the totals. Called by every thread.
+// Continue (1) or stop (0) the device-side iteration loop, if there is one:
+// called once per iteration by one thread of pcg_direction.
+__device__ __forceinline__ void set_continue(const PcgVectors& a, bool go) {
+  if (a.cond) cudaGraphSetConditional((cudaGraphConditionalHandle)a.cond, go ? 1u : 0u);
+}
+
+// Fixed-order sums of up to three per-thread values over the block (a
+// shuffle tree per warp, then the warps' sums in order); thread 0 gets the
+// totals. Called by every thread. fp32: fp64 arithmetic runs at about 1/64
+// of the fp32 rate on this part, and a fixed-order tree over the ~7e5 terms
+// of a dot product keeps a relative error near 1e-6, far below what the
+// recurrence needs; the order is fixed, so the bits repeat.
 template <int K>
-__device__ __forceinline__ void block_sums(double (&v)[K]) {
-  __shared__ double s_w[K][kPcgThreads / 32];
+__device__ __forceinline__ void block_sums(float (&v)[K]) {
+  __shared__ float s_w[K][kPcgThreads / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int k = 0; k < K; ++k) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_down_sync(0xffffffffu, v[k], o);
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
     if (lane == 0) s_w[k][w] = v[k];
   }
   __syncthreads();
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      double t = 0.0;
+      float t = 0.f;
       for (int i = 0; i < kPcgThreads / 32; ++i) t += s_w[k][i];
       v[k] = t;
     }
@@ -63,7 +77,7 @@ __device__ __forceinline__ void block_sums(double (&v)[K]) {
 // stride of them and then block_sums in fixed order, and returns true with
 // the grid totals in thread 0's tot. Every other block returns false.
 template <int K>
-__device__ __forceinline__ bool grid_sums(const PcgVectors& a, const double (&v)[K],
+__device__ __forceinline__ bool grid_sums(const PcgVectors& a, const float (&v)[K],
                                           double (&tot)[K]) {
   __shared__ int s_last;
   if (threadIdx.x == 0) {
@@ -75,10 +89,10 @@ __device__ __forceinline__ bool grid_sums(const PcgVectors& a, const double (&v)
   __syncthreads();
   if (!s_last) return false;
   __threadfence();
-  double w[K];
+  float w[K];
 #pragma unroll
   for (int k = 0; k < K; ++k) {
-    w[k] = 0.0;
+    w[k] = 0.f;
     for (int i = threadIdx.x; i < (int)gridDim.x; i += kPcgThreads)
       w[k] += __ldcg(a.partials + k * kPcgBlocks + i);
   }
@@ -95,18 +109,18 @@ __device__ __forceinline__ float jacobi(float d, float r) {
   return d != 0.f ? r / d : r;  // a row without a diagonal is left unscaled
 }
 
-// Each thread takes elements i, i + S, i + 2S, i + 3S (S = the grid's
-// threads) per pass, all four loads issued before any is used, so a thread
-// waits on one memory round trip per pass instead of one per element. A
-// thread's share of a dot product is summed in fp32 over a pass (at most 4
-// terms) and then added into an fp64 total (fp64 arithmetic is scarce on
-// this part).
-constexpr int kPcgUnroll = 4;
+// Each thread takes elements i, i + S, ..., i + 5S (S = the grid's threads)
+// per pass, all loads issued before any is used, so a thread waits on one
+// memory round trip per pass instead of one per element; one pass covers up
+// to 608 x 256 x 6 = 933,888 unknowns (the 686k of the hex-mesh system: with
+// four per pass, 41% of the threads took a second round trip). A thread's
+// share of a dot product is summed in fp32.
+constexpr int kPcgUnroll = 6;
 
 // r = b - q (q = A x0), z = D^-1 r, p = z; rz, rr, bb.
 __global__ void __launch_bounds__(kPcgThreads) pcg_init(const PcgVectors a) {
   const int S = gridDim.x * kPcgThreads;
-  double v[3] = {0.0, 0.0, 0.0};
+  float v[3] = {0.f, 0.f, 0.f};
   for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
     float bv[kPcgUnroll], qv[kPcgUnroll], dv[kPcgUnroll];
 #pragma unroll
@@ -148,11 +162,49 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_init(const PcgVectors a) {
   }
 }
 
-// alpha = rz / (p . q).
+// The three per-iteration kernels are launched with programmatic dependent
+// launch: each waits for the kernel before it (whose results it reads) and
+// then lets the next one be scheduled, so launch latency overlaps the tail.
+__device__ __forceinline__ void pcg_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
+// Every block: the grid total of K rows of per-block values parked at
+// `partials` by the previous kernel (rows kPcgBlocks apart, `blocks` values
+// each), summed in one fixed order: each thread a fixed stride, then
+// block_sums. Every block gets the same bits; no block waits for another
+// (the previous kernel's completion, via pdl_wait, makes them visible).
+// Returned in every thread.
+template <int K>
+__device__ __forceinline__ void grid_totals(const float* partials, int blocks, float (&tot)[K]) {
+  __shared__ float s_tot[K];
+  float w[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    w[k] = 0.f;
+    for (int i = threadIdx.x; i < blocks; i += kPcgThreads) w[k] += partials[k * kPcgBlocks + i];
+  }
+  block_sums<K>(w);
+  if (threadIdx.x == 0)
+#pragma unroll
+    for (int k = 0; k < K; ++k) s_tot[k] = w[k];
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < K; ++k) tot[k] = s_tot[k];
+}
+
+// Scalars each kernel reads were written by earlier kernels only: the step
+// length kernel parks p . q; the update kernel reads rz (and records it as
+// rz_prev for the direction kernel); the direction kernel reads rz_prev and
+// writes the new rz, rr, iter and the done flag.
+
+// p . q, per block.
 __global__ void __launch_bounds__(kPcgThreads) pcg_alpha(const PcgVectors a) {
+  pcg_enter();
   if (a.sc->done) return;
   const int S = gridDim.x * kPcgThreads;
-  double v[1] = {0.0};
+  float v[1] = {0.f};
   for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
     float pv[kPcgUnroll], qv[kPcgUnroll];
 #pragma unroll
@@ -167,44 +219,61 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_alpha(const PcgVectors a) {
     v[0] += c;
   }
   block_sums<1>(v);
-  double t[1];
-  if (grid_sums<1>(a, v, t) && threadIdx.x == 0) {
-    PcgScalars* sc = a.sc;
-    if (!(t[0] > 0.0)) {
-      sc->done = kPcgBreakdown;  // p . A p <= 0: A is not positive definite
-    } else {
-      sc->alpha = sc->rz / t[0];
+  if (threadIdx.x == 0) a.partials[blockIdx.x] = v[0];
+}
+
+// alpha = rz / (p . q); x += alpha p, r -= alpha q, z = D^-1 r; r . z and
+// r . r per block. A thread's loads of its first pass are issued before the
+// step length is summed, so the two latencies overlap.
+struct UpdateLoads {
+  float x[kPcgUnroll], p[kPcgUnroll], r[kPcgUnroll], q[kPcgUnroll], d[kPcgUnroll];
+};
+
+__device__ __forceinline__ void update_load(const PcgVectors& a, int i0, int S, UpdateLoads& L) {
+#pragma unroll
+  for (int u = 0; u < kPcgUnroll; ++u) {
+    const int i = i0 + u * S;
+    if (i < a.n) {
+      L.x[u] = a.x[i];
+      L.p[u] = a.p[i];
+      L.r[u] = a.r[i];
+      L.q[u] = a.q[i];
+      L.d[u] = a.diag[i];
     }
   }
 }
 
-// x += alpha p, r -= alpha q, z = D^-1 r; beta = (r . z) / rz, convergence.
 __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
-  if (a.sc->done) return;
-  const float alpha = (float)a.sc->alpha;
+  pcg_enter();
+  PcgScalars* sc = a.sc;
+  if (sc->done) return;
   const int S = gridDim.x * kPcgThreads;
-  double v[2] = {0.0, 0.0};
-  for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
-    float xv[kPcgUnroll], pv[kPcgUnroll], rv[kPcgUnroll], qv[kPcgUnroll], dv[kPcgUnroll];
-#pragma unroll
-    for (int u = 0; u < kPcgUnroll; ++u) {
-      const int i = i0 + u * S;
-      if (i < a.n) {
-        xv[u] = a.x[i];
-        pv[u] = a.p[i];
-        rv[u] = a.r[i];
-        qv[u] = a.q[i];
-        dv[u] = a.diag[i];
-      }
-    }
+  int i0 = blockIdx.x * kPcgThreads + threadIdx.x;
+  UpdateLoads L;
+  update_load(a, i0, S, L);
+  float pq[1];
+  grid_totals<1>(a.pq_parts, a.pq_count, pq);
+  const double rz = sc->rz;
+  if (!(pq[0] > 0.0f)) {  // p . A p <= 0: A is not positive definite (every block agrees)
+    if (blockIdx.x == 0 && threadIdx.x == 0) sc->done = kPcgBreakdown;
+    return;
+  }
+  const double alpha_d = rz / (double)pq[0];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    sc->alpha = alpha_d;
+    sc->rz_prev = rz;
+  }
+  const float alpha = (float)alpha_d;
+  float v[2] = {0.f, 0.f};
+  for (; i0 < a.n; i0 += kPcgUnroll * S) {
     float c[2] = {0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < kPcgUnroll; ++u) {
       const int i = i0 + u * S;
       if (i < a.n) {
-        a.x[i] = fmaf(alpha, pv[u], xv[u]);
-        const float ri = fmaf(-alpha, qv[u], rv[u]);
-        const float zi = jacobi(dv[u], ri);
+        a.x[i] = fmaf(alpha, L.p[u], L.x[u]);
+        const float ri = fmaf(-alpha, L.q[u], L.r[u]);
+        const float zi = jacobi(L.d[u], ri);
         a.r[i] = ri;
         a.z[i] = zi;
         c[0] = fmaf(ri, zi, c[0]);
@@ -213,50 +282,81 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
     }
     v[0] += c[0];
     v[1] += c[1];
+    if (i0 + kPcgUnroll * S < a.n) update_load(a, i0 + kPcgUnroll * S, S, L);
   }
   block_sums<2>(v);
-  double t[2];
-  if (grid_sums<2>(a, v, t) && threadIdx.x == 0) {
-    PcgScalars* sc = a.sc;
-    sc->beta = t[0] / sc->rz;
-    sc->rz = t[0];
-    sc->rr = t[1];
-    sc->iter += 1;
-    if (t[1] <= sc->tol2 * sc->bb)
-      sc->done = kPcgConverged;
-    else if (sc->iter >= sc->max_iter)
-      sc->done = kPcgMaxIter;
+  if (threadIdx.x == 0) {
+    a.partials[kPcgBlocks + blockIdx.x] = v[0];
+    a.partials[2 * kPcgBlocks + blockIdx.x] = v[1];
   }
 }
 
-// p = z + beta p.
+// beta = (r . z) / rz_prev; p = z + beta p; block 0 records the new rz and
+// r . r and decides convergence.
 __global__ void __launch_bounds__(kPcgThreads) pcg_direction(const PcgVectors a) {
-  if (a.sc->done) return;
-  const float beta = (float)a.sc->beta;
+  pcg_enter();
+  PcgScalars* sc = a.sc;
+  if (sc->done) {  // solved, stopped or broken down before this iteration
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_continue(a, false);
+    return;
+  }
   const int S = gridDim.x * kPcgThreads;
-  for (int i0 = blockIdx.x * kPcgThreads + threadIdx.x; i0 < a.n; i0 += kPcgUnroll * S) {
-    float zv[kPcgUnroll], pv[kPcgUnroll];
+  int i0 = blockIdx.x * kPcgThreads + threadIdx.x;
+  // this thread's first loads go out before the new rz is summed
+  float zv[kPcgUnroll], pv[kPcgUnroll];
 #pragma unroll
-    for (int u = 0; u < kPcgUnroll; ++u) {
-      const int i = i0 + u * S;
-      if (i < a.n) {
-        zv[u] = a.z[i];
-        pv[u] = a.p[i];
-      }
+  for (int u = 0; u < kPcgUnroll; ++u) {
+    const int i = i0 + u * S;
+    if (i < a.n) {
+      zv[u] = a.z[i];
+      pv[u] = a.p[i];
     }
+  }
+  float t[1];
+  grid_totals<1>(a.partials + kPcgBlocks, gridDim.x, t);
+  const double beta_d = (double)t[0] / sc->rz_prev;
+  if (blockIdx.x == 0) {
+    float rr[1];
+    grid_totals<1>(a.partials + 2 * kPcgBlocks, gridDim.x, rr);
+    if (threadIdx.x == 0) {
+      sc->beta = beta_d;
+      sc->rz = t[0];
+      sc->rr = rr[0];
+      sc->iter += 1;
+      int done = 0;
+      if ((double)rr[0] <= sc->tol2 * sc->bb)
+        done = kPcgConverged;
+      else if (sc->iter >= sc->max_iter)
+        done = kPcgMaxIter;
+      sc->done = done;
+      set_continue(a, done == 0);
+    }
+  }
+  const float beta = (float)beta_d;
+  for (; i0 < a.n; i0 += kPcgUnroll * S) {
 #pragma unroll
     for (int u = 0; u < kPcgUnroll; ++u) {
       const int i = i0 + u * S;
       if (i < a.n) a.p[i] = fmaf(beta, pv[u], zv[u]);
+    }
+    if (i0 + kPcgUnroll * S < a.n) {
+#pragma unroll
+      for (int u = 0; u < kPcgUnroll; ++u) {
+        const int i = i0 + kPcgUnroll * S + u * S;
+        if (i < a.n) {
+          zv[u] = a.z[i];
+          pv[u] = a.p[i];
+        }
+      }
     }
   }
 }
 
 }  // namespace
 
-size_t pcg_work_bytes(int n) {
+size_t pcg_work_bytes(int n, int product_grid) {
   const size_t vec = ((size_t)n * 4 + 255) / 256 * 256;
-  return 4 * vec + 3 * kPcgBlocks * sizeof(double) + 256;
+  return 4 * vec + 3 * kPcgBlocks * sizeof(float) + 256 + (size_t)product_grid * sizeof(float);
 }
 
 int pcg_grid(int n) {
@@ -265,7 +365,7 @@ int pcg_grid(int n) {
 }
 
 int launch_pcg(int stage, const Plan& p, const float* b, float* x, const float* diag,
-               void* stream) {
+               void* stream, unsigned long long cond) {
   const int n = p.n_rows;
   const size_t vec = ((size_t)n * 4 + 255) / 256 * 256;
   unsigned char* w = p.pcg_work;
@@ -276,19 +376,27 @@ int launch_pcg(int stage, const Plan& p, const float* b, float* x, const float* 
   a.z = reinterpret_cast<float*>(w + vec);
   a.p = reinterpret_cast<float*>(w + 2 * vec);
   a.q = reinterpret_cast<float*>(w + 3 * vec);
-  a.partials = reinterpret_cast<double*>(w + 4 * vec);
-  a.sc = reinterpret_cast<PcgScalars*>(w + 4 * vec + 3 * kPcgBlocks * sizeof(double));
+  a.partials = reinterpret_cast<float*>(w + 4 * vec);
+  a.sc = reinterpret_cast<PcgScalars*>(w + 4 * vec + 3 * kPcgBlocks * sizeof(float));
+  // SELL and FEM products hand over p . q per CTA, after the scalars
+  const bool fused = pcg_fused_dot(p);
+  a.pq_parts = fused ? reinterpret_cast<float*>(w + 4 * vec + 3 * kPcgBlocks * sizeof(float) + 256)
+                     : a.partials;
+  a.pq_count = fused ? p.grid : pcg_grid(n);
   a.diag = diag;
+  a.cond = cond;
   a.n = n;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = pcg_grid(n);
-  switch (stage) {
-    case 0: pcg_init<<<grid, kPcgThreads, 0, st>>>(a); break;
-    case 1: pcg_alpha<<<grid, kPcgThreads, 0, st>>>(a); break;
-    case 2: pcg_update<<<grid, kPcgThreads, 0, st>>>(a); break;
-    default: pcg_direction<<<grid, kPcgThreads, 0, st>>>(a); break;
+  if (stage == 0) {
+    pcg_init<<<grid, kPcgThreads, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
   }
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  const void* fn = stage == 1   ? reinterpret_cast<const void*>(&pcg_alpha)
+                   : stage == 2 ? reinterpret_cast<const void*>(&pcg_update)
+                                : reinterpret_cast<const void*>(&pcg_direction);
+  void* args[] = {&a};
+  return launch_pdl(fn, grid, kPcgThreads, 0, stream, args);
 }
 
 }  // namespace spmv

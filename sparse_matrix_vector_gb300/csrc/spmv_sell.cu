@@ -29,6 +29,8 @@ struct SellArgs {
   const void* __restrict__ vals;
   const void* __restrict__ x;
   float* __restrict__ y;
+  const int* skip;  // when set and nonzero at launch: do nothing (a finished solve)
+  float* dot;       // when set: per-block x . y of a square matrix (conjugate gradients)
   int n_rows;
   int n_slices;
 };
@@ -74,16 +76,18 @@ __global__ void __launch_bounds__(kSellSlicesPerCta * 32, SPMV_SELL_MIN_BLOCKS)
   const int slice = blockIdx.x * kSellSlicesPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   pdl_launch_dependents();
-  if (slice >= a.n_slices) return;
-  const int s0 = __ldg(a.slice_ptr + slice);
-  const int width = (__ldg(a.slice_ptr + slice + 1) - s0) >> 5;
+  const bool live = slice < a.n_slices;
+  if (!live && !a.dot) return;
+  const int s0 = live ? __ldg(a.slice_ptr + slice) : 0;
+  const int width = live ? (__ldg(a.slice_ptr + slice + 1) - s0) >> 5 : 0;
   const int32_t* cols = a.cols + s0 + lane;
   const VT* vals = static_cast<const VT*>(a.vals) + s0 + lane;
   const int pos = slice * 32 + lane;
-  const int row = a.perm ? __ldg(a.perm + pos) : (pos < a.n_rows ? pos : -1);
+  const int row = !live ? -1 : a.perm ? __ldg(a.perm + pos) : (pos < a.n_rows ? pos : -1);
   // x and y belong to the stream's earlier work: read and write them only
   // after the kernels this launch depends on have completed
   pdl_wait();
+  if (a.skip && *a.skip) return;
   const VT* x = static_cast<const VT*>(a.x);
   float acc[2] = {0.f, 0.f};
   // steps in groups of U, the last group predicated: a slice of width <= U
@@ -102,14 +106,24 @@ __global__ void __launch_bounds__(kSellSlicesPerCta * 32, SPMV_SELL_MIN_BLOCKS)
     for (int j = 0; j < U; ++j)
       if (k + j < width) acc[j & 1] = sell_fma(acc[j & 1], v[j], gather(x, c[j]));
   }
-  if (row >= 0) a.y[row] = acc[0] + acc[1];
+  const float yv = acc[0] + acc[1];
+  if (row >= 0) a.y[row] = yv;
+  if (a.dot) {  // the block's x . y (square matrix: x[row] pairs with y[row]), fixed order
+    __shared__ float s_red[kSellSlicesPerCta];
+    const float xy = row >= 0 ? static_cast<float>(gather(x, row)) * yv : 0.f;
+    const float t = block_sum<kSellSlicesPerCta>(xy, s_red);
+    if (threadIdx.x == 0) a.dot[blockIdx.x] = t;
+  }
 }
 
 }  // namespace
 
-int launch_sell(const Plan& p, const void* x, float* y, void* stream) {
+int launch_sell(const Plan& p, const void* x, float* y, void* stream, const int* skip,
+                float* dot) {
   if (p.n_tiles == 0) return 0;
   SellArgs a;
+  a.skip = skip;
+  a.dot = dot;
   a.slice_ptr = p.row_ptr;
   a.perm = p.perm;
   a.cols = p.col_idx;
