@@ -435,7 +435,8 @@ spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
  * device. Alignment: col_idx 16 bytes, values 16 (fp32) or 8 (fp16)
  * bytes, row_ptr and y 4 bytes. y (n_rows fp32) is overwritten. Runs two
  * kernels on `stream`; calls no allocating routine.
- * Scratch: a file-scope device array of 768 KiB per device, shared by all
+ * Scratch: a file-scope device array of 768 KiB (and a status word) per
+ * device, shared by all
  * calls and held until the process exits; calls that overlap on the GPU
  * race on it, so order them (one stream). The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress); make that first call
@@ -451,8 +452,24 @@ spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols, int64_t nnz,
 
 /* Synchronize the plan's device and read its device status word: OK, or
  * DEVICE_STATUS if a kernel reported an error since the last check (the
- * word is cleared by this call). */
+ * word is cleared by this call). In a checked build (below) a column index
+ * or row offset found out of range also sets it. */
 spmv_status spmv_plan_check(spmv_plan* plan);
+
+/* 1 if this library was built with SPMV_CHECKED=1, else 0. A checked build
+ * (a separate build of the same sources, for debugging; the pages have no
+ * counterpart: it stands in for a memory checker) makes the CSR kernels and
+ * spmv_csr_run_noalloc test every column index against n_cols and every row
+ * offset against its slice before using it; an index out of range is
+ * replaced by a safe one and reported through the status word (no trap, no
+ * access outside any buffer; the results are then not meaningful). */
+int32_t spmv_checked_build(void);
+
+/* Checked builds: synchronize the current device and read the status word
+ * of spmv_csr_run_noalloc (kept in its scratch array): OK, or DEVICE_STATUS
+ * if a call found an index out of range since the last check (the word is
+ * cleared). Ordinary builds return OK at once. Allocates nothing. */
+spmv_status spmv_noalloc_check(void);
 
 /* Release the plan and its device memory (synchronizes the device first):
  * the cudaFree counterpart of [CSR] 2.2's one-time upload. NULL is

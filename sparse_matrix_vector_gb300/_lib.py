@@ -120,6 +120,8 @@ SIGNATURES = {
     "spmv_csr_run_noalloc": (ctypes.c_int, [c_i32, c_i32, c_i64, c_p, c_p, c_p,
                                             ctypes.c_int, c_p, c_p, c_p]),
     "spmv_plan_check": (ctypes.c_int, [c_p]),
+    "spmv_checked_build": (c_i32, []),
+    "spmv_noalloc_check": (ctypes.c_int, []),
     "spmv_plan_destroy": (None, [c_p]),
 }
 
@@ -149,3 +151,24 @@ def load():
                 fn.argtypes = args
             _lib = lib
     return _lib
+
+
+_checked = None
+
+
+def load_checked():
+    """The checked build of the library (built in-tree on first use): the
+    same C ABI, with every column index and row offset tested on the device
+    before use (include/spmv.h, spmv_checked_build). For tests and
+    debugging; the package's functions use load()."""
+    global _checked
+    with _lock:
+        if _checked is None:
+            path = _build.build_library(checked=True)
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _checked = lib
+    return _checked

@@ -48,17 +48,28 @@ def up_to_date() -> bool:
             and os.path.getmtime(LIB_PATH) >= _newest_input())
 
 
+# The checked build (SPMV_CHECKED=1: kernels test indices before use; see
+# include/spmv.h, spmv_checked_build), a separate library for debugging.
+CHECKED_LIB_PATH = os.path.join(HERE, "libspmv_gb300_checked.so")
+CHECKED_BUILD_DIR = os.path.join(HERE, "_build_checked")
+
+
 def build_library(force: bool = False, verbose: bool = False,
-                  extra_flags: list[str] | None = None) -> str:
-    """Compile and link the library if any input is newer. Returns its path."""
-    if not force and not extra_flags and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+                  extra_flags: list[str] | None = None, checked: bool = False) -> str:
+    """Compile and link the library (or its checked build) if any input is
+    newer. Returns its path."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    build_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    if (not force and not extra_flags and os.path.exists(lib_path)
+            and os.path.getmtime(lib_path) >= _newest_input()):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = nvcc_path()
-    flags = NVCC_FLAGS + ARCH + ["-I", INCLUDE] + list(extra_flags or [])
+    flags = (NVCC_FLAGS + ARCH + ["-I", INCLUDE] + (["-DSPMV_CHECKED=1"] if checked else [])
+             + list(extra_flags or []))
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -71,13 +82,13 @@ def build_library(force: bool = False, verbose: bool = False,
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
         objs = list(pool.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

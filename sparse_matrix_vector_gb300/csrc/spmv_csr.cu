@@ -382,6 +382,31 @@ __device__ __forceinline__ void stream_tile_walk(const CsrArgs& a, const int4 d,
   if (closes) y[close_row] = before + close_val;
 }
 
+// Checked builds: before a staged unit is used, every column is tested
+// against n_cols and every staged row offset of a short-row tile is clamped
+// into the tile's nonzeros (the first and last exactly to its ends), so a
+// corrupt index can neither gather outside x nor walk outside the stage.
+template <typename VT>
+__device__ __noinline__ void check_stage(const CsrArgs& a, const int4 d, unsigned char* stage) {
+  bool bad = false;
+  const int a0 = d.y & ~7;
+  int* s_col = reinterpret_cast<int*>(stage);
+  for (int el = d.y - a0 + (int)threadIdx.x; el < d.z - a0; el += kThreads)
+    s_col[el] = checked_col(s_col[el], a.n_cols, &bad);
+  if (((uint32_t)d.w >> kKindShift) == kKindStream) {
+    const int R = (int)((uint32_t)d.w & kRowsMask);
+    int* s_rp = reinterpret_cast<int*>(stage + Stage<VT>::kColBytes + Stage<VT>::kValBytes) +
+                (d.x - (d.x & ~3));
+    for (int r = threadIdx.x; r <= R; r += kThreads) {
+      const int v = checked_offset(s_rp[r], d.y, d.z, &bad);
+      s_rp[r] = r == 0 ? d.y : r == R ? d.z : v;
+      if ((r == 0 && v != d.y) || (r == R && v != d.z)) bad = true;
+    }
+  }
+  if (bad) atomicExch(a.status, kStatusBadIndex);
+  __syncthreads();
+}
+
 // Per-thread partial sum of a staged slice [b, e) of one row.
 template <typename VT, typename XT, bool XS, bool IL>
 __device__ __forceinline__ float chunk_sum(const CsrArgs& a, const int4 d,
@@ -514,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, kCsrCtasPerSm<VT>) csr_kernel(const 
     unsigned char* stage = stages + s * Stage<VT>::kBytes;
     const uint32_t w = (uint32_t)d.w;
     const uint32_t kind = w >> kKindShift;
+    if (kChecked) check_stage<VT>(a, d, stage);
     if (kind == kKindStream) {
       if (w & kStreamWalk)
         stream_tile_walk<VT, XT, XS>(a, d, stage, xs, s_carry);

@@ -137,6 +137,29 @@ __device__ __forceinline__ void finish_pieces(const CsrSegArgs& a, const int2 (&
   }
 }
 
+// Checked builds: the staged columns of a segment are tested against n_cols
+// and a packed run's row starts clamped into [0, nonzeros] (first and last
+// exactly to its ends) before the segment is used (see spmv_internal.h).
+template <typename VT>
+__device__ __noinline__ void check_segment(const CsrSegArgs& a, unsigned char* st, int nz,
+                                           int R, int lane) {
+  bool bad = false;
+  unsigned char* cols = st + kSegHeaderBytes;
+  if (R > 0) {
+    int16_t* rs = reinterpret_cast<int16_t*>(cols);
+    for (int q = lane; q <= R; q += 32) {
+      const int v = checked_offset(rs[q], 0, nz, &bad);
+      rs[q] = (int16_t)(q == 0 ? 0 : q == R ? nz : v);
+      if ((q == 0 && v != 0) || (q == R && v != nz)) bad = true;
+    }
+    cols += ((R + 1) * 2 + 15) & ~15;
+  }
+  int* s_col = reinterpret_cast<int*>(cols);
+  for (int j = lane; j < nz; j += 32) s_col[j] = checked_col(s_col[j], a.n_cols, &bad);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(a.status, kStatusBadIndex);
+  __syncwarp();
+}
+
 // A packed run of R whole rows: every lane forms the products of nonzeros
 // lane, lane + 32, ... (a warp-wide step gathers x for 32 consecutive
 // nonzeros) and parks them in place of the columns. Then, 32 rows at a time,
@@ -245,6 +268,7 @@ __global__ void __launch_bounds__(kCW<VT, MIXED> * 32, 1) csr_seg_kernel(const C
     const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; slot
     const int nz = h0.z;
     const uint32_t rf = (uint32_t)h0.y;
+    if (kChecked) check_segment<VT>(a, st, nz, (MIXED && (rf & kSegPacked)) ? h0.x : 0, lane);
     if (MIXED && (rf & kSegPacked)) {
       packed_rows<VT, XS, Sg::kK>(a, st, h0.x, nz, (int)(rf & kSegRowMask), lane, xs);
       __syncwarp();

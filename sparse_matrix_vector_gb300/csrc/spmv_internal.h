@@ -11,6 +11,29 @@
 
 namespace spmv {
 
+// ---------------------------------------------------------------- checked builds
+// SPMV_CHECKED=1 (a separate build of the library, for debugging) makes the
+// CSR kernels and the allocation-free entry point test every column index
+// against the column count and every row offset against its slice before
+// using it. An index out of range is replaced by a safe one (column 0; the
+// nearest end of the slice) and the kernel records kStatusBadIndex in the
+// device status word: results are then wrong but no access leaves its
+// buffer, and nothing traps. Ordinary builds compile the checks away.
+#ifndef SPMV_CHECKED
+#define SPMV_CHECKED 0
+#endif
+constexpr bool kChecked = SPMV_CHECKED != 0;
+constexpr int32_t kStatusBadIndex = 3;
+// A column as a checked build uses it: c if 0 <= c < n, else 0 (bad set).
+__host__ __device__ constexpr int checked_col(int c, int n, bool* bad) {
+  return ((unsigned)c < (unsigned)n) ? c : (*bad = true, 0);
+}
+// An offset as a checked build uses it: clamped into [lo, hi] (bad set when
+// it was outside).
+__host__ __device__ constexpr int checked_offset(int v, int lo, int hi, bool* bad) {
+  return v < lo ? (*bad = true, lo) : v > hi ? (*bad = true, hi) : v;
+}
+
 // ---------------------------------------------------------------- geometry
 constexpr int kThreads = 256;            // CTA size of every kernel
 constexpr int kWarps = kThreads / 32;

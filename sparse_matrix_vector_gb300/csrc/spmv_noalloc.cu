@@ -29,6 +29,7 @@
 #include <mutex>
 
 #include "../../include/spmv.h"
+#include "spmv_internal.h"
 
 namespace {
 
@@ -38,7 +39,8 @@ constexpr int kMaxSlices = 65536; // => at most 134,217,728 nonzeros
 constexpr size_t kTailOffset = 0;
 constexpr size_t kHeadOffset = (size_t)kMaxSlices * 4;
 constexpr size_t kRowOffset = (size_t)kMaxSlices * 8;
-constexpr size_t kScratchBytes = (size_t)kMaxSlices * 12;  // 768 KiB
+constexpr size_t kStatusOffset = (size_t)kMaxSlices * 12;
+constexpr size_t kScratchBytes = (size_t)kMaxSlices * 12 + 256;  // 768 KiB + a status word
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -48,6 +50,7 @@ struct Scratch {
                       //         and continues past it
   float* head;        // [slice] partial of the row that started before it
   int32_t* tail_row;  // [slice] that row's index, or -1
+  int32_t* status;    // checked builds: set when an index was out of range
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -90,8 +93,9 @@ template <typename VT>
 __global__ void __launch_bounds__(kThreads)
 noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
                const VT* __restrict__ val, const VT* __restrict__ x,
-               float* __restrict__ y, int n_rows, int nnz, int n_slices,
+               float* __restrict__ y, int n_rows, int n_cols, int nnz, int n_slices,
                Scratch s) {
+  bool bad = false;  // checked builds: an index was out of range
   __shared__ __align__(16) float s_prod[kChunk];
   __shared__ int s_rows[2];
   __shared__ float s_red[kThreads / 32];
@@ -112,7 +116,13 @@ noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ 
     const int i0 = lo + 4 * j;
     float p[4] = {0.f, 0.f, 0.f, 0.f};
     if (i0 + 4 <= hi) {
-      const int4 c = __ldg(reinterpret_cast<const int4*>(col + i0));
+      int4 c = __ldg(reinterpret_cast<const int4*>(col + i0));
+      if (spmv::kChecked) {
+        c.x = spmv::checked_col(c.x, n_cols, &bad);
+        c.y = spmv::checked_col(c.y, n_cols, &bad);
+        c.z = spmv::checked_col(c.z, n_cols, &bad);
+        c.w = spmv::checked_col(c.w, n_cols, &bad);
+      }
       float v[4];
       load4(val + i0, v);
       p[0] = v[0] * as_float(__ldg(x + c.x));
@@ -120,8 +130,11 @@ noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ 
       p[2] = v[2] * as_float(__ldg(x + c.z));
       p[3] = v[3] * as_float(__ldg(x + c.w));
     } else {
-      for (int q = 0; q < 4 && i0 + q < hi; ++q)
-        p[q] = as_float(__ldg(val + i0 + q)) * as_float(__ldg(x + __ldg(col + i0 + q)));
+      for (int q = 0; q < 4 && i0 + q < hi; ++q) {
+        int c = __ldg(col + i0 + q);
+        if (spmv::kChecked) c = spmv::checked_col(c, n_cols, &bad);
+        p[q] = as_float(__ldg(val + i0 + q)) * as_float(__ldg(x + c));
+      }
     }
     *reinterpret_cast<float4*>(s_prod + 4 * j) = make_float4(p[0], p[1], p[2], p[3]);
   }
@@ -130,7 +143,8 @@ noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ 
 
   // head: nonzeros [lo, min(row_ptr[rb], hi)) belong to a row that started
   // before this slice
-  const int h_end = min(__ldg(row_ptr + rb), hi) - lo;
+  int h_end = min(__ldg(row_ptr + rb), hi) - lo;
+  if (spmv::kChecked) h_end = spmv::checked_offset(h_end, 0, hi - lo, &bad);
   if (h_end > 0) {
     float v = 0.f;
     for (int i = tid; i < h_end; i += kThreads) v += s_prod[i];
@@ -156,9 +170,13 @@ noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ 
     float acc = 0.f;
     int end = 0;
     if (r < re) {
-      const int b = __ldg(row_ptr + r) - lo;
+      int b = __ldg(row_ptr + r) - lo;
       end = __ldg(row_ptr + r + 1);
-      const int e = min(end, hi) - lo;
+      int e = min(end, hi) - lo;
+      if (spmv::kChecked) {
+        b = spmv::checked_offset(b, 0, hi - lo, &bad);
+        e = spmv::checked_offset(e, 0, hi - lo, &bad);
+      }
       for (int i = b + lig; i < e; i += g) acc += s_prod[i];
     }
     for (int o = g >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -171,6 +189,7 @@ noalloc_slices(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ 
       }
     }
   }
+  if (spmv::kChecked && bad) atomicExch(s.status, spmv::kStatusBadIndex);
 }
 
 // One thread per slice with a tail: y[row] = tail + heads of the slices the
@@ -187,7 +206,12 @@ noalloc_fixup(const int32_t* __restrict__ row_ptr, float* __restrict__ y,
   if (k >= n_slices) return;
   const int r = s.tail_row[k];
   if (r < 0) return;
-  const int last = (__ldg(row_ptr + r + 1) - 1) / kChunk;
+  int last = (__ldg(row_ptr + r + 1) - 1) / kChunk;
+  if (spmv::kChecked) {
+    bool bad = false;
+    last = spmv::checked_offset(last, k, n_slices - 1, &bad);
+    if (bad) atomicExch(s.status, spmv::kStatusBadIndex);
+  }
   float v = s.tail[k];
   for (int j = k + 1; j <= last; ++j) v += s.head[j];
   y[r] = v;
@@ -219,6 +243,7 @@ spmv_status scratch_on_current_device(Scratch* out) {
   out->tail = reinterpret_cast<float*>(b + kTailOffset);
   out->head = reinterpret_cast<float*>(b + kHeadOffset);
   out->tail_row = reinterpret_cast<int32_t*>(b + kRowOffset);
+  out->status = reinterpret_cast<int32_t*>(b + kStatusOffset);
   return SPMV_OK;
 }
 
@@ -269,8 +294,9 @@ extern "C" spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols,
   int n_rows_arg = n_rows;
   int nnz32 = (int)nnz;
   float* y_arg = y;
+  int n_cols_arg = n_cols;
   void* slice_args[] = {&row_ptr, &col_idx, &values, &x, &y_arg, &n_rows_arg,
-                        &nnz32, &n_slices, &s};
+                        &n_cols_arg, &nnz32, &n_slices, &s};
   const void* slice_fn = value_dtype == SPMV_F32
                              ? reinterpret_cast<const void*>(&noalloc_slices<float>)
                              : reinterpret_cast<const void*>(&noalloc_slices<__half>);
@@ -282,4 +308,20 @@ extern "C" spmv_status spmv_csr_run_noalloc(int32_t n_rows, int32_t n_cols,
                        dim3((unsigned)((n_slices + kThreads - 1) / kThreads)),
                        dim3(kThreads), fix_args, 0, cs);
   return e == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
+}
+
+extern "C" int32_t spmv_checked_build(void) { return spmv::kChecked ? 1 : 0; }
+
+extern "C" spmv_status spmv_noalloc_check(void) {
+  if (!spmv::kChecked) return SPMV_OK;
+  Scratch s;
+  spmv_status st = scratch_on_current_device(&s);
+  if (st != SPMV_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPMV_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, s.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return SPMV_ERR_CUDA;
+  if (word == 0) return SPMV_OK;
+  const int32_t zero = 0;
+  if (cudaMemcpy(s.status, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) return SPMV_ERR_CUDA;
+  return SPMV_ERR_DEVICE_STATUS;
 }
