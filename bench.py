@@ -90,21 +90,29 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha(fmt: str) -> str:
-    """sha256[:16] of the device sources of a format's kernel (the shared
-    device header followed by the kernel's file)."""
+def kernel_file(fmt: str, segments: bool = False) -> str:
+    """The source file of the kernel a format's plan runs."""
+    if fmt.startswith("delta"):
+        return "spmv_delta.cu"
+    if fmt == "sell":
+        return "spmv_sell.cu"
+    if fmt == "fem":
+        return "spmv_fem.cu"
+    return "spmv_csr_seg.cu" if segments else "spmv_csr.cu"
+
+
+def kernel_source_sha(fmt: str, segments: bool = False) -> str:
+    """sha256[:16] of the device sources of a plan's kernel (the shared
+    device header and internal header, then the kernel's file)."""
     csrc = os.path.join(ROOT, "sparse_matrix_vector_gb300", "csrc")
     h = hashlib.sha256()
-    kernel_file = ("spmv_delta.cu" if fmt.startswith("delta")
-                   else "spmv_sell.cu" if fmt == "sell"
-                   else "spmv_fem.cu" if fmt == "fem" else "spmv_csr.cu")
-    for name in ("spmv_device.cuh", kernel_file):
+    for name in ("spmv_device.cuh", "spmv_internal.h", kernel_file(fmt, segments)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, fmt: str):
+def recorded_traffic(workload: str, fmt: str, segments: bool = False):
     """DRAM bytes per launch from a committed ncu summary, if it was taken
     on the current kernel source; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -113,7 +121,7 @@ def recorded_traffic(workload: str, fmt: str):
             rec = json.load(f).get(workload)
     except Exception:
         return None
-    if not rec or rec.get("kernel_sha") != kernel_source_sha(fmt):
+    if not rec or rec.get("kernel_sha") != kernel_source_sha(fmt, segments):
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -209,7 +217,7 @@ MAX_REGIONS = 5000
 LEAD_CYCLES = 300_000
 
 
-def timed_regions(run_region, stream, dev, pg, local, steps, est_step_s):
+def timed_regions(run_region, stream, dev, pg, local, steps, est_step_s, regions=0):
     """Time `steps` steps (one call of run_region, which enqueues them on
     `stream`) several times over. Each
     region is bracketed by a barrier and torch.cuda.synchronize() on both
@@ -217,7 +225,7 @@ def timed_regions(run_region, stream, dev, pg, local, steps, est_step_s):
     per-region statistics in ms (max over ranks of each) and the clock record
     sampled across all regions."""
     import torch
-    n = int(min(MAX_REGIONS, max(MIN_REGIONS, math.ceil(
+    n = regions or int(min(MAX_REGIONS, max(MIN_REGIONS, math.ceil(
         REGION_SECONDS / max(steps * est_step_s, 1e-7)))))
     clocks = ClockSampler(local)
     clocks.start()
@@ -491,7 +499,7 @@ def bench_pcg(args, name, world, rank, local, pg):
             solve()
 
     regions, clk = timed_regions(solves_region, stream, dev, pg, local, steps,
-                                 sol_ms / 1e3 / iters)
+                                 sol_ms / 1e3 / iters, args.regions)
     ms = regions["median_ms"]
     sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
     t_sol = ms / solves / 1e3
@@ -613,7 +621,8 @@ def bench_one(args, name, world, rank, local, pg):
             g.replay()
 
     regions, clk = timed_regions(replay, stream, dev, pg, local, steps,
-                                 max(nbytes / (0.7 * peak * 1e9), 1e-6))
+                                 max(nbytes / (0.7 * peak * 1e9), 1e-6),
+                                 args.regions)
     ms = regions["median_ms"]
     sec_per_step, value, per_launch = job_throughput(nbytes, world, ms, steps)
     flops = m.n_elem * FEM_FLOPS_PER_ELEMENT if fmt == "fem" else 2 * m.nnz
@@ -638,7 +647,7 @@ def bench_one(args, name, world, rank, local, pg):
 
     line = None
     if rank == 0:
-        traffic = recorded_traffic(name, fmt)
+        traffic = recorded_traffic(name, fmt, bool(info.get("segments", 0)))
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
@@ -699,8 +708,11 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0,
-                    help="timed steps (default: ~1.5 s of work)")
+                    help="timed steps per timed region (default: ~0.1 s of work)")
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--regions", type=int, default=0,
+                    help="timed regions (default: enough for ~0.6 s of timed "
+                         "work, at least %d)" % MIN_REGIONS)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="one of %s, or 'all'" % ", ".join(WORKLOADS))
