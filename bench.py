@@ -57,6 +57,8 @@ WORKLOADS = {
 # p, r, q, diag and writes x, r, z (32); the direction reads z, p and writes
 # p (12)
 PCG_VECTOR_BYTES = 52
+# iterations per pass of the solve's device-side loop (the library's default)
+PCG_BODY = 2
 PCG_TOL = 1e-6
 # fp32 fma peak for the matrix-free operator's ALU roofline: 152 SMs x 128
 # fp32 lanes x 2 flops at the 2070 MHz maximum SM clock
@@ -525,7 +527,8 @@ def bench_pcg(args, name, world, rank, local, pg):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": desc, "format": fmt, "n_rows": n, "nnz": m.nnz,
                    "algorithmic_bytes": nbytes,
-                   "step": "one Jacobi-PCG iteration (y = A p + 3 vector kernels)",
+                   "step": ("one Jacobi-PCG iteration (y = A p with p . q fused in, "
+                            "then the update and direction kernels)"),
                    "iterations_per_solve": iters, "rel_tol": PCG_TOL,
                    "l2": "matrix >= 3x L2" if nbytes > 3 * 129e6 else
                          "working set fits L2 (matrix-free operator)",
@@ -542,7 +545,9 @@ def bench_pcg(args, name, world, rank, local, pg):
                 "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,
                 "note": "one whole solve to 1e-6 per step, b in and x out",
                 "ms_per_solve": e2e_sec * 1e3},
-        "gpu_launches": 4 * steps,
+        # per solve: q = A x0 and the initial residual, then passes of the
+        # device-side loop, PCG_BODY iterations of 3 kernels each
+        "gpu_launches": solves * (2 + 3 * PCG_BODY * -(-iters // PCG_BODY)),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -382,14 +382,17 @@ typedef struct spmv_pcg_result {
  * device, or NULL for the plan's own diagonal; a zero entry leaves its row
  * unscaled). x_dev holds the initial guess and receives the solution; b_dev
  * is not written. Stops when ||r|| <= rel_tol ||b|| or after max_iter
- * iterations; the host checks the device-side state after 4 iterations,
- * after 8 more, then every check_every iterations (<= 0: 16), and kernels
- * after convergence inside a batch do nothing. Each iteration is one
- * spmv_run and three vector kernels on `stream` (a batch is replayed as a
- * CUDA graph, kept in the plan for the same b, x and diag, unless `stream`
- * is the legacy default stream or is being captured); the call
- * synchronizes the stream. Vectors are fp32 and the
- * recurrence's scalars fp64; the result is the same bits on every run.
+ * iterations. Each iteration is the plan's product and two or three vector
+ * kernels on `stream`. The iterations run as one CUDA graph with a
+ * device-side loop (two iterations per pass; the direction kernel ends the
+ * loop on convergence, the limit or a breakdown), kept in the plan for the
+ * same b, x and diag, so the host waits once per solve. When `stream` is
+ * the legacy default stream or is being captured, or the graph cannot be
+ * built, the host runs batches of 4, then 8, then check_every (<= 0: 16)
+ * iterations instead and checks the device-side state between them;
+ * kernels after convergence inside a batch do nothing. The call
+ * synchronizes the stream. Vectors are fp32 and the recurrence's scalars
+ * fp64; the result is the same bits on every run.
  * Errors: INVALID_ARG (NULL pointers, non-square or non-fp32 plan, no
  * diagonal), OUT_OF_MEMORY, CUDA. */
 spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag_dev, const float* b_dev,

@@ -47,8 +47,11 @@ constexpr int kCS = SPMV_CSR_SEG_STAGES;
 // 64, 128 or 256 nonzeros, all measured 28.9-30.4 us: the kernel is bound by
 // the rate of random x gathers that miss L1 (~0.5 L2 requests per clock per
 // SM beside the matrix stream), not by their latency.
+#ifndef SPMV_CSR_MIXED_WARPS
+#define SPMV_CSR_MIXED_WARPS 24
+#endif
 template <typename VT, bool MIXED>
-constexpr int kCW = MIXED ? 24 : (sizeof(VT) == 2 ? 28 : 24);
+constexpr int kCW = MIXED ? SPMV_CSR_MIXED_WARPS : (sizeof(VT) == 2 ? 28 : 24);
 
 template <typename VT, bool MIXED>
 struct CSeg {
@@ -179,10 +182,20 @@ __device__ __forceinline__ void packed_rows(const CsrSegArgs& a, unsigned char* 
   const int* s_col = reinterpret_cast<const int*>(cols);
   const T* s_val = reinterpret_cast<const T*>(cols + ((nz * 4 + 15) & ~15));
   float* s_prod = reinterpret_cast<float*>(cols);
+  // every column, then every x gather, before the first product is parked
+  // over the columns: the K gathers of a lane are in flight together
+  // (a lane overwrites only its own columns)
+  int c[K];
+  T xv[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) c[k] = 32 * k + lane < nz ? s_col[32 * k + lane] : 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+    if (32 * k + lane < nz) xv[k] = load_x<VT, XS>(xs, a.x, c[k]);
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int j = 32 * k + lane;
-    if (j < nz) s_prod[j] = mul_v(s_val[j], load_x<VT, XS>(xs, a.x, s_col[j]));
+    if (j < nz) s_prod[j] = mul_v(s_val[j], xv[k]);
   }
   __syncwarp();
   for (int q0 = 0; q0 < R; q0 += 32) {

@@ -467,7 +467,10 @@ spmv_status plan_segments(int32_t n_rows, const std::function<int64_t(int32_t)>&
 
 // Mixed plans pack rows of at most this many nonzeros (longer rows are cut
 // into slices of kCsrSegNnzMixed).
-constexpr int64_t kCsrPackRowMax = 128;
+#ifndef SPMV_CSR_PACK_MAX
+#define SPMV_CSR_PACK_MAX 256
+#endif
+constexpr int64_t kCsrPackRowMax = SPMV_CSR_PACK_MAX;
 
 spmv_status plan_csr_mixed_segments(const spmv_csr* m, int max_warps, int warps_per_cta,
                                     SegTables* out, spmv_plan_info* info) {
@@ -1688,6 +1691,16 @@ spmv_status spmv_plan_create_fem(const spmv_fem_mesh* mesh, spmv_plan** out) {
   return SPMV_OK;
 }
 
+// Iterations in one pass of the device-side loop's body; the ones after
+// convergence skip themselves. On the hex-mesh system (686k unknowns,
+// matrix-free, 10 iterations) 1 and 2 measured 25.8 and 24.3 us per
+// iteration (each pass of the loop costs about 1.5 us); 4 was no faster
+// than 2.
+#ifndef SPMV_PCG_BODY
+#define SPMV_PCG_BODY 2
+#endif
+constexpr int kPcgBodyIterations = SPMV_PCG_BODY;
+
 spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, float* x,
                            double rel_tol, int32_t max_iter, int32_t check_every, void* stream,
                            spmv_pcg_result* result) {
@@ -1733,12 +1746,16 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
   const int full = check_every > 0 ? check_every : 16;
   // the products skip themselves once the solve is done (the device flag)
   const int* done_flag = &sc_dev->done;
+  // one iteration's vector kernels after the product; cond goes to the
+  // direction kernel, which decides whether the loop goes on
+  auto launch_vectors = [&](unsigned long long cond) -> bool {
+    if (!fused && launch_pcg(1, p, b, x, d, stream) != 0) return false;
+    return launch_pcg(2, p, b, x, d, stream) == 0 && launch_pcg(3, p, b, x, d, stream, cond) == 0;
+  };
   auto enqueue_batch = [&](int n_it) -> spmv_status {
-    for (int k = 0; k < n_it; ++k) {
-      if (launch_product(p, pv, qv, stream, done_flag, pq_dev) != 0) return SPMV_ERR_CUDA;
-      for (int stage = fused ? 2 : 1; stage <= 3; ++stage)
-        if (launch_pcg(stage, p, b, x, d, stream) != 0) return SPMV_ERR_CUDA;
-    }
+    for (int k = 0; k < n_it; ++k)
+      if (launch_product(p, pv, qv, stream, done_flag, pq_dev) != 0 || !launch_vectors(0))
+        return SPMV_ERR_CUDA;
     return SPMV_OK;
   };
   // A batch is 4 launches per iteration; replaying it as one CUDA graph
@@ -1789,10 +1806,10 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
       ok = cudaStreamBeginCaptureToGraph(st, body, nullptr, nullptr, 0,
                                          cudaStreamCaptureModeThreadLocal) == cudaSuccess;
       if (ok) {
-        const bool launched = launch_product(p, pv, qv, stream, done_flag, pq_dev) == 0 &&
-                              (fused || launch_pcg(1, p, b, x, d, stream) == 0) &&
-                              launch_pcg(2, p, b, x, d, stream) == 0 &&
-                              launch_pcg(3, p, b, x, d, stream, (unsigned long long)h) == 0;
+        bool launched = true;
+        for (int u = 0; u < kPcgBodyIterations && launched; ++u)
+          launched = launch_product(p, pv, qv, stream, done_flag, pq_dev) == 0 &&
+                     launch_vectors(u + 1 == kPcgBodyIterations ? (unsigned long long)h : 0ull);
         ok = cudaStreamEndCapture(st, &body) == cudaSuccess && launched;
       }
     }

@@ -2,17 +2,19 @@
 // matvec" 6.1: CG with the diagonal preconditioner, its iterations the
 // consumer of the matrix-vector products).
 //
-// One iteration is the plan's y = A x launch followed by three small kernels
-// (step length, updates, new direction). Vectors are fp32; the scalars of
-// the recurrence live in device memory in fp64, so the host never waits
-// inside an iteration. Dot products are reduced in two fixed-order levels:
-// per block, parked in a partials array, then summed by every block of the
-// next kernel in the same fixed order (each thread a fixed stride, then a
+// One iteration is the plan's y = A x launch followed by small kernels: the
+// step length (only for plans whose product does not hand over p . q
+// itself), the updates, the new direction. Vectors are fp32; the scalars of
+// the recurrence live in device memory in fp64, formed once per block (fp64
+// runs at about 1/64 of the fp32 rate here), so the host never waits inside
+// an iteration. Dot products are reduced in two fixed-order levels: per
+// block, parked in a partials array, then summed by every block of the next
+// kernel in the same fixed order (each thread a fixed stride, then a
 // fixed-order block sum), so a solve gives the same bits every time and no
-// kernel ends with one block reducing while the rest of the GPU idles. Once the
-// residual test passes (or the iteration limit or a breakdown is hit) a
-// device flag turns the remaining kernels of a batch, the products included,
-// into no-ops, and the host only reads the scalars between batches.
+// kernel ends with one block reducing while the rest of the GPU idles. The
+// direction kernel decides, on the device, whether the solve goes on: it
+// sets the condition of the solve's device-side loop, and a done flag turns
+// any kernels still queued into no-ops.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -72,6 +74,36 @@ __device__ __forceinline__ void block_sums(float (&v)[K]) {
   }
 }
 
+// This thread's fixed-stride share of K rows of parked per-block values
+// (rows kPcgBlocks apart; elements threadIdx.x, + kPcgThreads, ... below
+// `blocks`), added in that order. The loads of a group of kPcgLoadGroup go
+// out before the first add, so a share costs one memory round trip per group
+// rather than one per element. CG: read through L2 only (values written by
+// other blocks of the running grid).
+constexpr int kPcgLoadGroup = 8;
+
+template <int K, bool CG>
+__device__ __forceinline__ void thread_share(const float* partials, int blocks, float (&w)[K]) {
+#pragma unroll
+  for (int k = 0; k < K; ++k) w[k] = 0.f;
+  for (int i0 = threadIdx.x; i0 < blocks; i0 += kPcgLoadGroup * kPcgThreads) {
+    float t[K][kPcgLoadGroup];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+      for (int j = 0; j < kPcgLoadGroup; ++j) {
+        const int i = i0 + j * kPcgThreads;
+        const float* q = partials + k * kPcgBlocks + i;
+        t[k][j] = i < blocks ? (CG ? __ldcg(q) : *q) : 0.f;
+      }
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+      for (int j = 0; j < kPcgLoadGroup; ++j)
+        if (i0 + j * kPcgThreads < blocks) w[k] += t[k][j];
+  }
+}
+
 // Every thread: thread 0 parks the block's sums (from block_sums); the block
 // that arrives last then adds all the blocks' sums, each thread a fixed
 // stride of them and then block_sums in fixed order, and returns true with
@@ -90,12 +122,7 @@ __device__ __forceinline__ bool grid_sums(const PcgVectors& a, const float (&v)[
   if (!s_last) return false;
   __threadfence();
   float w[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    w[k] = 0.f;
-    for (int i = threadIdx.x; i < (int)gridDim.x; i += kPcgThreads)
-      w[k] += __ldcg(a.partials + k * kPcgBlocks + i);
-  }
+  thread_share<K, true>(a.partials, (int)gridDim.x, w);
   block_sums<K>(w);
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -103,6 +130,20 @@ __device__ __forceinline__ bool grid_sums(const PcgVectors& a, const float (&v)[
     a.sc->arrived = 0;
   }
   return true;
+}
+
+// num / den in fp64, formed by one thread of the block and handed to all
+// as fp32 (thread 0 also gets the fp64 value in *q64). fp64 runs at about
+// 1/64 of the fp32 rate on this part: the same division done by every thread
+// of the grid cost about 2.5 us per kernel. Called by every thread.
+__device__ __forceinline__ float block_ratio(double num, double den, double* q64) {
+  __shared__ float s_q;
+  if (threadIdx.x == 0) {
+    *q64 = num / den;
+    s_q = (float)*q64;
+  }
+  __syncthreads();
+  return s_q;
 }
 
 __device__ __forceinline__ float jacobi(float d, float r) {
@@ -180,11 +221,7 @@ template <int K>
 __device__ __forceinline__ void grid_totals(const float* partials, int blocks, float (&tot)[K]) {
   __shared__ float s_tot[K];
   float w[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    w[k] = 0.f;
-    for (int i = threadIdx.x; i < blocks; i += kPcgThreads) w[k] += partials[k * kPcgBlocks + i];
-  }
+  thread_share<K, false>(partials, blocks, w);
   block_sums<K>(w);
   if (threadIdx.x == 0)
 #pragma unroll
@@ -229,41 +266,60 @@ struct UpdateLoads {
   float x[kPcgUnroll], p[kPcgUnroll], r[kPcgUnroll], q[kPcgUnroll], d[kPcgUnroll];
 };
 
-__device__ __forceinline__ void update_load(const PcgVectors& a, int i0, int S, UpdateLoads& L) {
+// x, r and diag: not written by the product before this kernel nor by the
+// direction kernel before that (which may still be running under
+// programmatic dependent launch), so these loads may go out before the wait.
+__device__ __forceinline__ void update_load_xrd(const PcgVectors& a, int i0, int S,
+                                                UpdateLoads& L) {
 #pragma unroll
   for (int u = 0; u < kPcgUnroll; ++u) {
     const int i = i0 + u * S;
     if (i < a.n) {
-      L.x[u] = a.x[i];
-      L.p[u] = a.p[i];
-      L.r[u] = a.r[i];
-      L.q[u] = a.q[i];
+      L.x[u] = __ldcg(a.x + i);
+      L.r[u] = __ldcg(a.r + i);
       L.d[u] = a.diag[i];
     }
   }
 }
 
+// p and q: written by the two kernels before this one; after the wait only.
+__device__ __forceinline__ void update_load_pq(const PcgVectors& a, int i0, int S,
+                                               UpdateLoads& L) {
+#pragma unroll
+  for (int u = 0; u < kPcgUnroll; ++u) {
+    const int i = i0 + u * S;
+    if (i < a.n) {
+      L.p[u] = a.p[i];
+      L.q[u] = a.q[i];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
-  pcg_enter();
-  PcgScalars* sc = a.sc;
-  if (sc->done) return;
   const int S = gridDim.x * kPcgThreads;
   int i0 = blockIdx.x * kPcgThreads + threadIdx.x;
   UpdateLoads L;
-  update_load(a, i0, S, L);
+  update_load_xrd(a, i0, S, L);
+  pcg_enter();
+  update_load_pq(a, i0, S, L);
+  // the scalars' loads go out with the partials' (one round trip); a done
+  // solve (uniform over the grid) leaves after them
+  PcgScalars* sc = a.sc;
+  const int done = sc->done;
+  const double rz = sc->rz;
   float pq[1];
   grid_totals<1>(a.pq_parts, a.pq_count, pq);
-  const double rz = sc->rz;
+  if (done) return;
   if (!(pq[0] > 0.0f)) {  // p . A p <= 0: A is not positive definite (every block agrees)
     if (blockIdx.x == 0 && threadIdx.x == 0) sc->done = kPcgBreakdown;
     return;
   }
-  const double alpha_d = rz / (double)pq[0];
+  double alpha_d = 0.0;
+  const float alpha = block_ratio(rz, (double)pq[0], &alpha_d);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     sc->alpha = alpha_d;
     sc->rz_prev = rz;
   }
-  const float alpha = (float)alpha_d;
   float v[2] = {0.f, 0.f};
   for (; i0 < a.n; i0 += kPcgUnroll * S) {
     float c[2] = {0.f, 0.f};
@@ -282,7 +338,10 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
     }
     v[0] += c[0];
     v[1] += c[1];
-    if (i0 + kPcgUnroll * S < a.n) update_load(a, i0 + kPcgUnroll * S, S, L);
+    if (i0 + kPcgUnroll * S < a.n) {
+      update_load_xrd(a, i0 + kPcgUnroll * S, S, L);
+      update_load_pq(a, i0 + kPcgUnroll * S, S, L);
+    }
   }
   block_sums<2>(v);
   if (threadIdx.x == 0) {
@@ -294,45 +353,48 @@ __global__ void __launch_bounds__(kPcgThreads) pcg_update(const PcgVectors a) {
 // beta = (r . z) / rz_prev; p = z + beta p; block 0 records the new rz and
 // r . r and decides convergence.
 __global__ void __launch_bounds__(kPcgThreads) pcg_direction(const PcgVectors a) {
-  pcg_enter();
-  PcgScalars* sc = a.sc;
-  if (sc->done) {  // solved, stopped or broken down before this iteration
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_continue(a, false);
-    return;
-  }
   const int S = gridDim.x * kPcgThreads;
   int i0 = blockIdx.x * kPcgThreads + threadIdx.x;
-  // this thread's first loads go out before the new rz is summed
+  // p: last written by the direction kernel of the previous iteration, which
+  // has finished once the update kernel before this one passed its wait, so
+  // its loads go out before this kernel's wait; z after it
   float zv[kPcgUnroll], pv[kPcgUnroll];
 #pragma unroll
   for (int u = 0; u < kPcgUnroll; ++u) {
     const int i = i0 + u * S;
-    if (i < a.n) {
-      zv[u] = a.z[i];
-      pv[u] = a.p[i];
-    }
+    if (i < a.n) pv[u] = __ldcg(a.p + i);
   }
-  float t[1];
-  grid_totals<1>(a.partials + kPcgBlocks, gridDim.x, t);
-  const double beta_d = (double)t[0] / sc->rz_prev;
-  if (blockIdx.x == 0) {
-    float rr[1];
-    grid_totals<1>(a.partials + 2 * kPcgBlocks, gridDim.x, rr);
-    if (threadIdx.x == 0) {
-      sc->beta = beta_d;
-      sc->rz = t[0];
-      sc->rr = rr[0];
-      sc->iter += 1;
-      int done = 0;
-      if ((double)rr[0] <= sc->tol2 * sc->bb)
-        done = kPcgConverged;
-      else if (sc->iter >= sc->max_iter)
-        done = kPcgMaxIter;
-      sc->done = done;
-      set_continue(a, done == 0);
-    }
+  pcg_enter();
+#pragma unroll
+  for (int u = 0; u < kPcgUnroll; ++u) {
+    const int i = i0 + u * S;
+    if (i < a.n) zv[u] = a.z[i];
   }
-  const float beta = (float)beta_d;
+  PcgScalars* sc = a.sc;
+  const int done = sc->done;
+  const double rz_prev = sc->rz_prev;
+  // r . z and r . r (only block 0 uses the latter), in one round trip
+  float t[2];
+  grid_totals<2>(a.partials + kPcgBlocks, gridDim.x, t);
+  if (done) {  // solved, stopped or broken down before this iteration
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_continue(a, false);
+    return;
+  }
+  double beta_d = 0.0;
+  const float beta = block_ratio((double)t[0], rz_prev, &beta_d);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    sc->beta = beta_d;
+    sc->rz = t[0];
+    sc->rr = t[1];
+    sc->iter += 1;
+    int state = 0;
+    if ((double)t[1] <= sc->tol2 * sc->bb)
+      state = kPcgConverged;
+    else if (sc->iter >= sc->max_iter)
+      state = kPcgMaxIter;
+    sc->done = state;
+    set_continue(a, state == 0);
+  }
   for (; i0 < a.n; i0 += kPcgUnroll * S) {
 #pragma unroll
     for (int u = 0; u < kPcgUnroll; ++u) {
@@ -392,11 +454,12 @@ int launch_pcg(int stage, const Plan& p, const float* b, float* x, const float* 
     pcg_init<<<grid, kPcgThreads, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
   }
+  void* args[] = {&a};
   const void* fn = stage == 1   ? reinterpret_cast<const void*>(&pcg_alpha)
                    : stage == 2 ? reinterpret_cast<const void*>(&pcg_update)
                                 : reinterpret_cast<const void*>(&pcg_direction);
-  void* args[] = {&a};
   return launch_pdl(fn, grid, kPcgThreads, 0, stream, args);
 }
+
 
 }  // namespace spmv
