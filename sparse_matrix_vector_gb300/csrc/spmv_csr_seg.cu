@@ -6,14 +6,15 @@
 // The planner cuts the rows into segments and gives each warp of the grid a
 // contiguous share of them, of equal weight. Long-row plans: every segment is
 // a slice of at most 512 nonzeros of one row (full ones first). Mixed plans
-// (irregular matrices): a run of consecutive rows of at most 256 nonzeros in
-// all is packed into one segment ("Hash-based multi-phase SpGEMM" 5.2,
-// batching tiny rows), longer rows are cut into slices of 256. A segment's block (a 32-byte header, its
-// columns, its values) is staged by one bulk copy into the warp's own ring of
-// shared-memory buffers; lane s of the warp issues the copies into buffer s,
-// so warps never wait for one another and no CTA barrier sits in the loop
-// (the CTA-wide tiles of spmv_csr.cu pay one per work unit, which dominates
-// when a row of ~1,000 nonzeros leaves a 256-thread CTA five per thread).
+// (irregular matrices): a run of consecutive whole rows of at most 256
+// nonzeros in all is packed into one segment ("Hash-based multi-phase
+// SpGEMM" 5.2, batching tiny rows), longer rows are cut into slices of 256.
+// A segment's block (a 32-byte header, its columns, its values) is staged by
+// one bulk copy into the warp's own ring of shared-memory buffers; lane s of
+// the warp issues the copies into buffer s, so warps never wait for one
+// another and no CTA barrier sits in the loop (the CTA-wide tiles of
+// spmv_csr.cu pay one per work unit, which dominates when a row of ~1,000
+// nonzeros leaves a 256-thread CTA five per thread).
 // Lane l takes nonzeros l, l + 32, ... of a segment: a warp-wide step reads
 // 32 consecutive columns and values (conflict-free) and gathers x at 32
 // neighbouring columns of the row ("CUDA CSR SpMV optimisation" 4.1: a warp
@@ -21,9 +22,10 @@
 // (mixed-precision fma); fp32 values use fp32 fma.
 // Packed rows: the products are parked in shared memory and lane l sums rows
 // l, l + 32, ... of the run. Slices: lanes keep fp32 partials; at a row's
-// last segment, or the end of the warp's share, the warp reduces them. A row inside one share is written at
-// once; a row shared by several warps leaves one partial per warp, and the
-// warp whose atomicAdd completes the row's count adds them in warp order.
+// last segment, or the end of the warp's share, the warp reduces them. A row
+// inside one share is written at once; a row shared by several warps leaves
+// one partial per warp, and the warp whose atomicAdd completes the row's
+// count adds them in warp order.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -43,10 +45,8 @@ constexpr int kCS = SPMV_CSR_SEG_STAGES;
 // memory. Mixed plans gather x mostly at random: their rings stay near
 // 125 KB so that L1 keeps about 100 KB, which random gathers through L1 need
 // (with 28 KB of L1 they ran at half the rate). On the power-law matrix
-// (916k rows, 5.1M nonzeros) 24 or 32 warps, and packing rows of at most 32,
-// 64, 128 or 256 nonzeros, all measured 28.9-30.4 us: the kernel is bound by
-// the rate of random x gathers that miss L1 (~0.5 L2 requests per clock per
-// SM beside the matrix stream), not by their latency.
+// (916k rows, 5.1M nonzeros): 16, 24 or 32 warps 27.8, 26.6, 26.6 us;
+// packing rows of at most 64, 128 or 256 nonzeros 27.1, 26.6, 26.0 us.
 #ifndef SPMV_CSR_MIXED_WARPS
 #define SPMV_CSR_MIXED_WARPS 24
 #endif

@@ -253,11 +253,11 @@ def test_planner_bins_of_the_workload_shapes(spmv_lib):
                                                                  csr_kernel=1))
         assert forced["walk_tiles"] == walk
     # by default the irregular rows (CV > 2) take mixed warp segments: runs of
-    # rows of at most 128 nonzeros packed 256 to a segment, longer rows sliced
+    # whole rows packed 256 nonzeros to a segment, longer rows sliced by 256
     info = S.spmv_plan_inspect(pl.row_ptr, pl.col_idx, pl.values, pl.n_cols)
     assert info["segments"] == 1
     L = pl.row_lengths()
-    long_rows = L[L > 128]
+    long_rows = L[L > 256]
     assert info["tiles_per_bin"][2] + info["tiles_per_bin"][3] == (-(-long_rows // 256)).sum()
     assert info["rows_per_bin"][1] + info["rows_per_bin"][2] + info["rows_per_bin"][3] >= \
         long_rows.size
