@@ -404,12 +404,14 @@ spmv_status spmv_plan_get_info(const spmv_plan* plan, spmv_plan_info* info);
 
 /* y = A x, asynchronously on `stream` (a cudaStream_t; NULL = legacy
  * default stream): the launch step of [CSR] 2.2 (the matrix is already
- * resident, so only kernels chosen by the plan's format run). x_dev: n_cols elements (fp32 for fp32-value plans, fp16
- * otherwise), aligned to its element size; y_dev: n_rows fp32, aligned to 4
- * bytes, fully overwritten (rows without nonzeros get 0). x and y must not
- * overlap. DELTA, SELL and FEM plans multiply padding (or out-of-mesh)
- * entries as 0 * x[c], so x must be finite there. Does not synchronize. Errors: INVALID_ARG, WRONG_DEVICE,
- * CUDA (launch failure). */
+ * resident, so only kernels chosen by the plan's format run). x_dev: n_cols
+ * elements (fp32 for fp32-value plans, fp16 otherwise), aligned to its
+ * element size; y_dev: n_rows fp32, aligned to 4 bytes, fully overwritten
+ * (rows without nonzeros get 0). x and y must not overlap. DELTA, SELL and
+ * FEM plans multiply padding (or out-of-mesh) entries as 0 * x[c], so x
+ * must be finite there (DELTA plans whose entries are more than 18% +0.0
+ * skip those products altogether). Does not synchronize. Errors:
+ * INVALID_ARG, WRONG_DEVICE, CUDA (launch failure). */
 spmv_status spmv_run(spmv_plan* plan, const void* x_dev, float* y_dev,
                      void* stream);
 

@@ -129,6 +129,23 @@ __device__ __forceinline__ uint16_t gather(const XPtr<XS>& p, uint32_t off) {
   }
 }
 
+// SKZ: the entry's value (fp16 bits `vb`) may be +0.0 -- a padding entry, or
+// an explicit zero -- and then x is not read at all (the product is 0 either
+// way for finite x): a lane whose entry is padding takes no shared-memory
+// bank in that gather.
+template <bool XS, bool SKZ>
+__device__ __forceinline__ uint16_t gather_v(const XPtr<XS>& p, uint32_t off, uint32_t vb) {
+  if (!SKZ) return gather<XS>(p, off);
+  if (XS) {
+    uint16_t v = 0;
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.shared.u16 %0, [%1];\n\t}"
+        : "+h"(v) : "r"(p.s + off), "r"(vb));
+    return v;
+  } else {
+    return vb ? __ldg(reinterpret_cast<const unsigned short*>(p.g + off)) : (uint16_t)0;
+  }
+}
+
 template <bool XS>
 __device__ __forceinline__ XPtr<XS> xptr(uint32_t xs_addr, const __half* x, int col) {
   XPtr<XS> p;
@@ -218,7 +235,7 @@ __device__ __forceinline__ void fma_pair(float& acc_lo, float& acc_hi, uint32_t 
 
 // Accumulate one word whose first entry follows column `col` (p: x at col).
 // Four accumulators, entry e of the word into acc[e % 4].
-template <int B, bool XS>
+template <int B, bool XS, bool SKZ>
 __device__ __forceinline__ void decode_word(uint32_t w, const WordPrefix<B>& pf,
                                             const WordVals<B>& v, const XPtr<XS>& p,
                                             float (&acc)[4]) {
@@ -228,12 +245,14 @@ __device__ __forceinline__ void decode_word(uint32_t w, const WordPrefix<B>& pf,
     for (int j = 0; j < 4; ++j) {
       const uint32_t o0 = __byte_perm(pf.Q2, 0u, 0x4440u + (uint32_t)j);
       const uint32_t o1 = __byte_perm(pf.P2, 0u, 0x4440u + (uint32_t)j);
-      fma_pair(acc[(2 * j) & 3], acc[(2 * j + 1) & 3], vw[j], gather<XS>(p, o0),
-               gather<XS>(p, o1));
+      fma_pair(acc[(2 * j) & 3], acc[(2 * j + 1) & 3], vw[j],
+               gather_v<XS, SKZ>(p, o0, vw[j] & 0xFFFFu), gather_v<XS, SKZ>(p, o1, vw[j] >> 16));
     }
   } else if constexpr (B == 8) {
-    fma_pair(acc[0], acc[1], v.v.x, gather<XS>(p, pf.Q2 & 0xFFFFu), gather<XS>(p, pf.P2 & 0xFFFFu));
-    fma_pair(acc[2], acc[3], v.v.y, gather<XS>(p, pf.Q2 >> 16), gather<XS>(p, pf.P2 >> 16));
+    fma_pair(acc[0], acc[1], v.v.x, gather_v<XS, SKZ>(p, pf.Q2 & 0xFFFFu, v.v.x & 0xFFFFu),
+             gather_v<XS, SKZ>(p, pf.P2 & 0xFFFFu, v.v.x >> 16));
+    fma_pair(acc[2], acc[3], v.v.y, gather_v<XS, SKZ>(p, pf.Q2 >> 16, v.v.y & 0xFFFFu),
+             gather_v<XS, SKZ>(p, pf.P2 >> 16, v.v.y >> 16));
   } else {
     const uint32_t vw[8] = {v.v0.x, v.v0.y, v.v0.z, v.v0.w, v.v1.x, v.v1.y, v.v1.z, v.v1.w};
 #pragma unroll
@@ -242,8 +261,11 @@ __device__ __forceinline__ void decode_word(uint32_t w, const WordPrefix<B>& pf,
       const uint32_t o3 = __byte_perm(pf.P2, 0u, 0x4440u + (uint32_t)i);
       const uint32_t o0 = o1 - ((w >> (8 * i + 1)) & 6u);   // 2 x field 4i+1
       const uint32_t o2 = o3 - ((w >> (8 * i + 5)) & 6u);   // 2 x field 4i+3
-      fma_pair(acc[0], acc[1], vw[2 * i], gather<XS>(p, o0), gather<XS>(p, o1));
-      fma_pair(acc[2], acc[3], vw[2 * i + 1], gather<XS>(p, o2), gather<XS>(p, o3));
+      const uint32_t va = vw[2 * i], vb = vw[2 * i + 1];
+      fma_pair(acc[0], acc[1], va, gather_v<XS, SKZ>(p, o0, va & 0xFFFFu),
+               gather_v<XS, SKZ>(p, o1, va >> 16));
+      fma_pair(acc[2], acc[3], vb, gather_v<XS, SKZ>(p, o2, vb & 0xFFFFu),
+               gather_v<XS, SKZ>(p, o3, vb >> 16));
     }
   }
 }
@@ -281,7 +303,7 @@ __device__ __forceinline__ void finish_pieces(const DeltaArgs& a, const int2 (&p
 // Lane l takes words l, l + 32, ... of the segment (LW of them). The column before word 32 k + l is the segment's base plus
 // the field sums of rows 0..k-1 and the exclusive prefix of row k; the field
 // sums of two rows share one 5-step scan.
-template <int B, bool XS>
+template <int B, bool XS, bool SKZ>
 __device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, int n_w, int base,
                                                      int lane, uint32_t xs_addr,
                                                      const __half* x, float (&acc)[4]) {
@@ -321,16 +343,16 @@ __device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, in
   if (full) {  // one straight-line block: the gathers of all words can overlap
 #pragma unroll
     for (int k = 0; k < LW; ++k)
-      decode_word<B, XS>(w[k], pf[k], load_vals<B>(s_vals, 32 * k + lane, n_w), xp[k], acc);
+      decode_word<B, XS, SKZ>(w[k], pf[k], load_vals<B>(s_vals, 32 * k + lane, n_w), xp[k], acc);
   } else {
 #pragma unroll
     for (int k = 0; k < LW; ++k)
       if (32 * k + lane < n_w)
-        decode_word<B, XS>(w[k], pf[k], load_vals<B>(s_vals, 32 * k + lane, n_w), xp[k], acc);
+        decode_word<B, XS, SKZ>(w[k], pf[k], load_vals<B>(s_vals, 32 * k + lane, n_w), xp[k], acc);
   }
 }
 
-template <int B, bool XS>
+template <int B, bool XS, bool SKZ>
 __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
     delta_seg_kernel(const DeltaArgs a) {
   using Sg = Seg<B>;
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
     const int4 h0 = *reinterpret_cast<const int4*>(st);       // base, row | flags, words, split
     const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; slot
     const int n_w = h0.z;
-    decode_segment_lanes<B, XS>(st, n_w, h0.x, lane, xs_addr, a.x, acc);
+    decode_segment_lanes<B, XS, SKZ>(st, n_w, h0.x, lane, xs_addr, a.x, acc);
     // every lane has used the buffer's contents: refill it
     __syncwarp();
     if (lane == s && h1.y > 0)
@@ -428,14 +450,21 @@ __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
   }
 }
 
-template <int B>
-const void* delta_entry_b(bool xs) {
-  return xs ? reinterpret_cast<const void*>(&delta_seg_kernel<B, true>)
-            : reinterpret_cast<const void*>(&delta_seg_kernel<B, false>);
+template <int B, bool SKZ>
+const void* delta_entry_bz(bool xs) {
+  return xs ? reinterpret_cast<const void*>(&delta_seg_kernel<B, true, SKZ>)
+            : reinterpret_cast<const void*>(&delta_seg_kernel<B, false, SKZ>);
 }
 
-const void* delta_entry(int bits, bool xs) {
-  return bits == 2 ? delta_entry_b<2>(xs) : bits == 8 ? delta_entry_b<8>(xs) : delta_entry_b<4>(xs);
+template <int B>
+const void* delta_entry_b(bool xs, bool skz) {
+  return skz ? delta_entry_bz<B, true>(xs) : delta_entry_bz<B, false>(xs);
+}
+
+const void* delta_entry(int bits, bool xs, bool skz) {
+  return bits == 2   ? delta_entry_b<2>(xs, skz)
+         : bits == 8 ? delta_entry_b<8>(xs, skz)
+                     : delta_entry_b<4>(xs, skz);
 }
 
 }  // namespace
@@ -456,16 +485,17 @@ size_t delta_x_smem_bytes(int n_cols) { return ((size_t)n_cols * 2 + 15) / 16 * 
 int delta_set_smem_limit(int bits, size_t dyn) {
   if (dyn == 0) return 0;
   for (bool xs : {false, true})
-    if (cudaFuncSetAttribute(delta_entry(bits, xs), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dyn) != cudaSuccess)
-      return -1;
+    for (bool skz : {false, true})
+      if (cudaFuncSetAttribute(delta_entry(bits, xs, skz),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
+        return -1;
   return 0;
 }
 
 int delta_kernel_occupancy(int bits, bool x_smem, size_t dyn_smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(bits, x_smem), kDW * 32,
-                                                    dyn_smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(bits, x_smem, false),
+                                                    kDW * 32, dyn_smem) != cudaSuccess)
     return -1;
   return n;
 }
@@ -486,8 +516,8 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.n_empty = p.n_empty_rows;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
-  return launch_pdl(delta_entry(p.delta_bits, p.x_smem), p.grid, kDW * 32, p.dyn_smem, stream,
-                    args);
+  return launch_pdl(delta_entry(p.delta_bits, p.x_smem, p.delta_skip_zero), p.grid, kDW * 32,
+                    p.dyn_smem, stream, args);
 }
 
 }  // namespace spmv

@@ -238,6 +238,7 @@ struct Plan {
   int64_t nnz = 0, n_entries = 0;
   bool x_smem = false;
   int delta_bits = 4;          // DELTA: bits per column delta (2, 4 or 8)
+  bool delta_skip_zero = false;  // DELTA: +0.0 entries (padding) read no x
   bool interleaved = false;  // CSR: products element-interleaved over the CTA
   bool csr_segments = false;  // CSR: warp-owned row segments
   bool csr_mixed = false;     // CSR segments: packed short rows + slices of long ones
