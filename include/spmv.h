@@ -424,6 +424,20 @@ spmv_status spmv_run(spmv_plan* plan, const void* x_dev, float* y_dev,
 spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
                           void* stream);
 
+/* The end-to-end product of `count` independent vectors with HOST buffers:
+ * y_host[i*n_rows ..] = A x_host[i*n_cols ..] for i < count (x: the plan's x
+ * type, y: fp32, both contiguous, vector after vector). The copy-in of one
+ * vector, the product of the one before it and the copy-out of the one
+ * before that run at the same time (two plan-owned staging pairs, the
+ * products on `stream`, the copies on two streams of the plan's own, ordered
+ * by events); returns after the last y is in host memory. Pinned host
+ * memory gives the fastest copies and lets the copies overlap. The
+ * copy-in / launch / copy-out of [CSR] 2.2, pipelined over a batch. Errors:
+ * INVALID_ARG (count < 0, null buffer), WRONG_DEVICE, OUT_OF_MEMORY (the
+ * second staging pair, first call only), CUDA. */
+spmv_status spmv_run_host_batch(spmv_plan* plan, int32_t count, const void* x_host,
+                                float* y_host, void* stream);
+
 /* Allocation-free y = A x for a CSR matrix the caller already holds in
  * device memory (the pages have no counterpart: this entry point exists for
  * callers that may not allocate device memory -- a latency-critical loop

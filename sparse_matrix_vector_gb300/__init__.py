@@ -11,7 +11,7 @@ from .api import (  # noqa: F401
     spmv_csr_run_noalloc,
     spmv_plan_check, spmv_plan_create, spmv_plan_create_delta, spmv_plan_create_fem,
     spmv_pcg_solve, spmv_plan_destroy, spmv_plan_inspect, spmv_plan_options, spmv_run,
-    spmv_run_host, spmv_status_string,
+    spmv_run_host, spmv_run_host_batch, spmv_status_string,
 )
 from ._lib import (  # noqa: F401
     SPMV_F16, SPMV_F32, SPMV_FORMAT_CSR, SPMV_FORMAT_DELTA2, SPMV_FORMAT_DELTA4,

@@ -117,6 +117,7 @@ SIGNATURES = {
     "spmv_plan_get_info": (ctypes.c_int, [c_p, ctypes.POINTER(spmv_plan_info)]),
     "spmv_run": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
     "spmv_run_host": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
+    "spmv_run_host_batch": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_p]),
     "spmv_csr_run_noalloc": (ctypes.c_int, [c_i32, c_i32, c_i64, c_p, c_p, c_p,
                                             ctypes.c_int, c_p, c_p, c_p]),
     "spmv_plan_check": (ctypes.c_int, [c_p]),

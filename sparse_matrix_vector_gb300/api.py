@@ -406,6 +406,25 @@ def spmv_run_host(plan: Plan, x_host: np.ndarray, y_host: np.ndarray,
            "spmv_run_host")
 
 
+def spmv_run_host_batch(plan: Plan, x_host: np.ndarray, y_host: np.ndarray,
+                        stream=None) -> None:
+    """End-to-end y[i] = A x[i] for a batch of host vectors (x_host: count x
+    n_cols of the plan's x dtype, y_host: count x n_rows float32, both
+    C-contiguous); copies and products of neighbouring vectors overlap.
+    Returns after the last y is in host memory."""
+    want = np.float32 if plan.x_dtype_code == SPMV_F32 else np.float16
+    if (x_host.dtype != want or not x_host.flags.c_contiguous or x_host.ndim != 2
+            or x_host.shape[1] != plan.n_cols):
+        raise ValueError("x_host must be a C-contiguous (count, n_cols) array of the plan's x dtype")
+    count = x_host.shape[0]
+    if (y_host.dtype != np.float32 or not y_host.flags.c_contiguous or y_host.ndim != 2
+            or y_host.shape != (count, plan.n_rows) or not y_host.flags.writeable):
+        raise ValueError("y_host must be a writeable C-contiguous (count, n_rows) float32 array")
+    _check(_lib.load().spmv_run_host_batch(plan.handle, int(count), x_host.ctypes.data,
+                                           y_host.ctypes.data, _stream_handle(stream)),
+           "spmv_run_host_batch")
+
+
 def spmv_csr_run_noalloc(n_rows: int, n_cols: int, row_ptr, col_idx, values,
                          x, y, stream=None) -> None:
     """Allocation-free y = A x on a CSR matrix held in caller-owned CUDA

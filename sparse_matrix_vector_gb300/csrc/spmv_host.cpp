@@ -598,6 +598,12 @@ void free_plan(spmv_plan* plan) {
     for (void* g : p->pcg_exec)
       if (g) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(g));
     if (p->pcg_loop) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->pcg_loop));
+    for (void* e : p->batch_events)
+      if (e) cudaEventDestroy(static_cast<cudaEvent_t>(e));
+    for (void* q : p->batch_streams)
+      if (q) cudaStreamDestroy(static_cast<cudaStream_t>(q));
+    if (p->x_stage2) cudaFree(p->x_stage2);
+    if (p->y_stage2) cudaFree(p->y_stage2);
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
                     p->tiles,   p->splits,   p->partials, p->counters,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
@@ -1958,6 +1964,73 @@ spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
                       cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return SPMV_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
+}
+
+spmv_status spmv_run_host_batch(spmv_plan* plan, int32_t count, const void* x_host,
+                                float* y_host, void* stream) {
+  if (!plan || count < 0) return SPMV_ERR_INVALID_ARG;
+  Plan& p = plan->impl;
+  if (count == 0) return SPMV_OK;
+  if ((p.n_cols > 0 && !x_host) || (p.n_rows > 0 && !y_host)) return SPMV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPMV_ERR_CUDA;
+  if (dev != p.device) return SPMV_ERR_WRONG_DEVICE;
+  const size_t xs = p.dtype == SPMV_F32 ? 4 : 2;
+  const size_t xb = (size_t)p.n_cols * xs, yb = (size_t)p.n_rows * 4;
+  spmv_status s;
+  // the second staging pair, the two copy streams and the events, once per plan
+  if (!p.x_stage2) {
+    if ((s = dev_alloc(&p.x_stage2, xb + 16)) != SPMV_OK) return s;
+    if ((s = dev_alloc(&p.y_stage2, yb + 16)) != SPMV_OK) return s;
+  }
+  for (void*& q : p.batch_streams)
+    if (!q) {
+      cudaStream_t c = nullptr;
+      if (cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking) != cudaSuccess) return SPMV_ERR_CUDA;
+      q = c;
+    }
+  for (void*& e : p.batch_events)
+    if (!e) {
+      cudaEvent_t c = nullptr;
+      if (cudaEventCreateWithFlags(&c, cudaEventDisableTiming) != cudaSuccess) return SPMV_ERR_CUDA;
+      e = c;
+    }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t s_in = static_cast<cudaStream_t>(p.batch_streams[0]);
+  cudaStream_t s_out = static_cast<cudaStream_t>(p.batch_streams[1]);
+  auto ev = [&](int k) { return static_cast<cudaEvent_t>(p.batch_events[k]); };
+  // events 0-1: copy-in of slot 0 / 1 done; 2-3: product done; 4-5: copy-out
+  // done; 6: the caller's earlier work on `stream`
+  void* xst[2] = {p.x_stage, p.x_stage2};
+  float* yst[2] = {p.y_stage, p.y_stage2};
+  const unsigned char* xh = static_cast<const unsigned char*>(x_host);
+  bool ok = cudaEventRecord(ev(6), st) == cudaSuccess &&
+            cudaStreamWaitEvent(s_in, ev(6), 0) == cudaSuccess &&
+            cudaStreamWaitEvent(s_out, ev(6), 0) == cudaSuccess;
+  // vector i: copy in on s_in, product on `stream`, copy out on s_out; slot
+  // i % 2 is reused by vector i + 2 only after vector i's product has read
+  // it (copy-in) and its y has been copied out (product)
+  for (int32_t i = 0; ok && i < count; ++i) {
+    const int sl = i & 1;
+    if (i >= 2) ok = cudaStreamWaitEvent(s_in, ev(2 + sl), 0) == cudaSuccess;
+    ok = ok && (xb == 0 || cudaMemcpyAsync(xst[sl], xh + (size_t)i * xb, xb,
+                                           cudaMemcpyHostToDevice, s_in) == cudaSuccess) &&
+         cudaEventRecord(ev(sl), s_in) == cudaSuccess &&
+         cudaStreamWaitEvent(st, ev(sl), 0) == cudaSuccess &&
+         (i < 2 || cudaStreamWaitEvent(st, ev(4 + sl), 0) == cudaSuccess);
+    if (!ok) break;
+    if ((s = spmv_run(plan, xst[sl], yst[sl], stream)) != SPMV_OK) return s;
+    ok = cudaEventRecord(ev(2 + sl), st) == cudaSuccess &&
+         cudaStreamWaitEvent(s_out, ev(2 + sl), 0) == cudaSuccess &&
+         (yb == 0 || cudaMemcpyAsync(y_host + (size_t)i * p.n_rows, yst[sl], yb,
+                                     cudaMemcpyDeviceToHost, s_out) == cudaSuccess) &&
+         cudaEventRecord(ev(4 + sl), s_out) == cudaSuccess;
+  }
+  // every stream drained, also after a failed enqueue
+  const bool drained = cudaStreamSynchronize(s_in) == cudaSuccess &&
+                       cudaStreamSynchronize(st) == cudaSuccess &&
+                       cudaStreamSynchronize(s_out) == cudaSuccess;
+  return ok && drained ? SPMV_OK : SPMV_ERR_CUDA;
 }
 
 spmv_status spmv_plan_check(spmv_plan* plan) {

@@ -286,6 +286,13 @@ struct Plan {
   // staging for spmv_run_host
   void* x_stage = nullptr;
   float* y_stage = nullptr;
+  // spmv_run_host_batch: a second staging pair, the copy-in and copy-out
+  // streams and, per staging slot, the events that order them (copy-in done,
+  // product done, copy-out done); created on first use
+  void* x_stage2 = nullptr;
+  float* y_stage2 = nullptr;
+  void* batch_streams[2] = {nullptr, nullptr};
+  void* batch_events[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
 
   spmv_plan_info info{};
 };

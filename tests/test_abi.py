@@ -127,6 +127,7 @@ def test_null_and_bad_args(spmv_lib):
                                       ctypes.byref(info)) == 1
     assert spmv_lib.spmv_run(None, None, None, None) == 1
     assert spmv_lib.spmv_run_host(None, None, None, None) == 1
+    assert spmv_lib.spmv_run_host_batch(None, 1, None, None, None) == 1
     assert spmv_lib.spmv_plan_check(None) == 1
     spmv_lib.spmv_plan_destroy(None)
     d = _lib.spmv_delta()

@@ -431,6 +431,35 @@ def test_run_host_end_to_end(fmt, name):
     S.spmv_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("fmt,name,count", [("csr", "laplacian_small", 5),
+                                            ("csr", "powerlaw_small", 2),
+                                            ("delta4", "llm90_small", 3),
+                                            ("sell", "fem_small", 1), ("csr", "tiny", 0)])
+def test_run_host_batch_end_to_end(fmt, name, count):
+    """Vectors through the pipelined host-buffer entry point: each y equals
+    the oracle's and spmv_run's for its own x (slots reused, two calls in a
+    row), and a call over no vectors does nothing."""
+    m = small(name)
+    plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols, format=fmt)
+    rng = np.random.default_rng(31)
+    xs = [m.x] + [rng.uniform(-1, 1, m.n_cols).astype(m.x.dtype) for _ in range(max(count, 1) - 1)]
+    xh = torch.from_numpy(np.stack(xs[:count]) if count else
+                          np.zeros((0, m.n_cols), m.x.dtype)).pin_memory().numpy()
+    dev = torch.device("cuda", 0)
+    for _ in range(2):
+        yh = torch.full((count, m.n_rows), float("nan"), dtype=torch.float32).pin_memory().numpy()
+        S.spmv_run_host_batch(plan, xh, yh)
+        for i in range(count):
+            y_ref, sm = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, xh[i])
+            assert np.all(np.abs(yh[i] - y_ref) <= tol_for(m) * sm + 1e-30)
+            yd = torch.empty(m.n_rows, dtype=torch.float32, device=dev)
+            S.spmv_run(plan, torch.from_numpy(np.ascontiguousarray(xh[i])).to(dev), yd)
+            assert np.array_equal(yd.cpu().numpy(), yh[i])
+    with pytest.raises(ValueError):
+        S.spmv_run_host_batch(plan, xh.reshape(-1), yh)
+    S.spmv_plan_destroy(plan)
+
+
 def test_argument_errors():
     m = small("tiny")
     plan = S.spmv_plan_create(m.row_ptr, m.col_idx, m.values, m.n_cols)
