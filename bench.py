@@ -470,7 +470,11 @@ def bench_pcg(args, name, world, rank, local, pg):
     nbytes = int(plan.info["algorithmic_bytes"]) + PCG_VECTOR_BYTES * n
     b = torch.from_numpy(m.x).to(dev)
     x = torch.zeros(n, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
+    # "device": the solve's device-side loop (one graph launch a solve);
+    # "host": the legacy default stream, on which the library runs host-driven
+    # batches of direct launches (for per-kernel profiling; not the headline)
+    stream = (torch.cuda.Stream(device=dev) if args.pcg_loop == "device"
+              else torch.cuda.default_stream(dev))
     warmup = max(3, args.warmup)
     first = {}
 
@@ -530,6 +534,9 @@ def bench_pcg(args, name, world, rank, local, pg):
                    "step": ("one Jacobi-PCG iteration (y = A p with p . q fused in, "
                             "then the update and direction kernels)"),
                    "iterations_per_solve": iters, "rel_tol": PCG_TOL,
+                   "pcg_loop": ("device-side loop, one graph launch a solve"
+                                if args.pcg_loop == "device" else
+                                "host-driven batches on the legacy default stream"),
                    "l2": "matrix >= 3x L2" if nbytes > 3 * 129e6 else
                          "working set fits L2 (matrix-free operator)",
                    "timing": ("CUDA events around each region of whole solves; "
@@ -746,6 +753,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pcg-loop", choices=["device", "host"], default="device",
+                    help="CG lines: the solve's device-side loop (default), or host-driven "
+                         "batches of direct launches (for per-kernel profiling)")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.workload != "all" and args.workload not in WORKLOADS:

@@ -431,8 +431,9 @@ spmv_status spmv_run_host(spmv_plan* plan, const void* x_host, float* y_host,
  * before that run at the same time (two plan-owned staging pairs, the
  * products on `stream`, the copies on two streams of the plan's own, ordered
  * by events); returns after the last y is in host memory. Pinned host
- * memory gives the fastest copies and lets the copies overlap. The
- * copy-in / launch / copy-out of [CSR] 2.2, pipelined over a batch. Errors:
+ * memory gives the fastest copies and lets the copies overlap. The call
+ * synchronizes, so it cannot be captured into a CUDA graph. The copy-in /
+ * launch / copy-out of [CSR] 2.2, pipelined over a batch. Errors:
  * INVALID_ARG (count < 0, null buffer), WRONG_DEVICE, OUT_OF_MEMORY (the
  * second staging pair, first call only), CUDA. */
 spmv_status spmv_run_host_batch(spmv_plan* plan, int32_t count, const void* x_host,

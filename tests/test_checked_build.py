@@ -113,3 +113,42 @@ def test_checked_build_on_valid_inputs(m):
     assert lib.spmv_noalloc_check() == 0
     yv = y.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(yv - y_ref) <= bound)
+
+
+@pytest.mark.gpu
+def test_checked_build_reports_bad_columns_through_the_status_word():
+    """The checked build on a caller-owned CSR matrix with two column
+    indices out of range (one past n_cols, one negative): its own bounds
+    checks substitute column 0 before any access, so nothing faults; the
+    status word reports the error once (the check clears it); the rows
+    without a bad column are right. Only the checked build is given this
+    input: the ordinary build trusts the caller's device arrays."""
+    torch = pytest.importorskip("torch")
+    lib = _lib.load_checked()
+    assert lib.spmv_checked_build() == 1
+    m = workloads.powerlaw(n=5000, nnz=27800, max_len=400, seed=9)
+    ci = m.col_idx.copy()
+    bad_at = [int(m.row_ptr[10]), int(m.row_ptr[2000])]
+    ci[bad_at[0]] = m.n_cols + 7
+    ci[bad_at[1]] = -3
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    d_rp = torch.from_numpy(m.row_ptr).to(dev)
+    d_ci = torch.from_numpy(ci).to(dev)
+    d_v = torch.from_numpy(m.values).to(dev)
+    x = torch.from_numpy(m.x).to(dev)
+    y = torch.full((m.n_rows,), float("nan"), dtype=torch.float32, device=dev)
+    assert lib.spmv_noalloc_check() == 0                 # nothing pending
+    assert lib.spmv_csr_run_noalloc(m.n_rows, m.n_cols, m.nnz, d_rp.data_ptr(),
+                                    d_ci.data_ptr(), d_v.data_ptr(), S.SPMV_F32,
+                                    x.data_ptr(), y.data_ptr(),
+                                    ctypes.c_void_p(stream.cuda_stream)) == 0
+    assert lib.spmv_noalloc_check() == 10                # SPMV_ERR_DEVICE_STATUS
+    assert lib.spmv_noalloc_check() == 0                 # cleared by the check
+    yv = y.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(yv))
+    y_ref, s = oracle.csr_spmv(m.row_ptr, m.col_idx, m.values, m.x)
+    rows = np.searchsorted(m.row_ptr, bad_at, side="right") - 1
+    good = np.ones(m.n_rows, bool)
+    good[rows] = False
+    assert np.all(np.abs(yv - y_ref)[good] <= 1e-5 * s[good] + 1e-30)
