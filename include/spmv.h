@@ -215,9 +215,9 @@ typedef struct spmv_plan_options {
                             (the bins above), 2 warp segments (rows cut into
                             slices of at most 512 nonzeros, each warp a
                             contiguous share; [CSR] 4.1 warp per row),
-                            3 mixed warp segments (runs of rows of at most
-                            128 nonzeros packed 256 nonzeros to a segment,
-                            [SPGEMM] 5.2; longer rows in slices of 256)    */
+                            3 mixed warp segments (runs of whole rows packed
+                            256 nonzeros to a segment, [SPGEMM] 5.2;
+                            longer rows in slices of 256)                  */
   int32_t reserved[5];
 } spmv_plan_options;
 
@@ -252,8 +252,8 @@ typedef struct spmv_plan_info {
   int64_t walk_tiles;        /* short-row tiles reduced in walk mode       */
   int64_t interleaved;       /* 1 if products are taken element-interleaved */
   int64_t segments;          /* 1 if the plan runs warp-owned row segments
-                                (DELTA, CSR with long rows); n_tiles then
-                                counts segments                            */
+                                (DELTA; CSR with long or irregular rows);
+                                n_tiles then counts segments               */
   int64_t reserved[5];
 } spmv_plan_info;
 
