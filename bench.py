@@ -449,12 +449,13 @@ def run_reference(args, world, rank):
 
 
 def bench_pcg(args, name, world, rank, local, pg):
-    """A step is one Jacobi-PCG iteration (one y = A x and three vector
+    """A step is one Jacobi-PCG iteration (one y = A x and its vector
     kernels), timed over whole solves to ||r|| <= 1e-6 ||b|| from x = 0
-    (every solve takes the same iterations: checked); the time includes the
-    host's convergence checks and the up to 15 no-op iterations of the last
-    batch. Bytes per step are the product's algorithmic bytes plus
-    PCG_VECTOR_BYTES per unknown."""
+    (every solve takes the same iterations: checked); the time includes each
+    solve's set-up (q = A x0, the initial residual, the graph launch and the
+    host's final wait) and, when the iteration count is odd, the skipped
+    second half of the last pass of the device-side loop. Bytes per step are
+    the product's algorithmic bytes plus PCG_VECTOR_BYTES per unknown."""
     import torch
     import sparse_matrix_vector_gb300 as S
 

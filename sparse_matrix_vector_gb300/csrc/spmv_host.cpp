@@ -1802,12 +1802,13 @@ spmv_status spmv_pcg_solve(spmv_plan* plan, const float* diag, const float* b, f
     p.pcg_loop_failed = false;
     for (int q = 0; q < 3; ++q) p.pcg_key[q] = key[q];
   }
-  // The whole loop on the device: a graph whose while node runs one
-  // iteration (product and three vector kernels) as long as the direction
-  // kernel says so (it stops the loop on convergence, the iteration limit or
-  // a breakdown), so the host waits once per solve and no iteration runs
-  // past the end. Built once per b, x and diag; a device or driver that
-  // refuses it leaves the batches below.
+  // The whole loop on the device: a graph whose while node runs
+  // kPcgBodyIterations iterations (each the product and its vector kernels)
+  // as long as the last direction kernel says so (it stops the loop on
+  // convergence, the iteration limit or a breakdown; iterations after that
+  // inside the same pass skip themselves), so the host waits once per
+  // solve. Built once per b, x and diag; a device or driver that refuses it
+  // leaves the batches below.
   if (graphable && !p.pcg_loop && !p.pcg_loop_failed) {
     cudaGraph_t g = nullptr;
     cudaGraphExec_t exec = nullptr;
