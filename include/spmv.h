@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define SPMV_ABI_VERSION 5
+#define SPMV_ABI_VERSION 6
 
 /* Rows per slice of the SELL format (one warp of the kernel per slice). */
 #define SPMV_SELL_C 32
@@ -218,7 +218,12 @@ typedef struct spmv_plan_options {
                             3 mixed warp segments (runs of whole rows packed
                             256 nonzeros to a segment, [SPGEMM] 5.2;
                             longer rows in slices of 256)                  */
-  int32_t reserved[5];
+  int32_t delta_kernel;  /* DELTA decode ([MACKO] 2.2): 0 auto (four lanes
+                            per word for 4-bit deltas), 1 a lane per packed
+                            word, 2 four lanes per word (4-bit deltas only;
+                            each lane two entries, so a warp's gathers fall
+                            in a narrow window of x)                       */
+  int32_t reserved[4];
 } spmv_plan_options;
 
 /* What the planner decided; filled by spmv_plan_inspect / spmv_plan_get_info.

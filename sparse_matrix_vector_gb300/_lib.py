@@ -65,7 +65,7 @@ class spmv_plan_options(ctypes.Structure):
                 ("cta_row_min", c_i32), ("split_row_min", c_i32),
                 ("split_chunk", c_i32), ("x_smem", c_i32), ("reduce", c_i32),
                 ("lanes", c_i32), ("interleave", c_i32), ("sell_sigma", c_i32),
-                ("csr_kernel", c_i32), ("reserved", c_i32 * 5)]
+                ("csr_kernel", c_i32), ("delta_kernel", c_i32), ("reserved", c_i32 * 4)]
 
 
 class spmv_plan_info(ctypes.Structure):

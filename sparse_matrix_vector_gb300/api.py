@@ -80,7 +80,7 @@ def _host_csr(row_ptr, col_idx, values, n_cols: int) -> _HostCSR:
 def spmv_plan_options(**kw) -> _lib.spmv_plan_options:
     """Library defaults, overridden by keyword (tile_nnz, tile_rows,
     cta_row_min, split_row_min, split_chunk, x_smem, reduce, lanes,
-    interleave, sell_sigma, csr_kernel)."""
+    interleave, sell_sigma, csr_kernel, delta_kernel)."""
     o = _lib.spmv_plan_options()
     _lib.load().spmv_plan_options_init(ctypes.byref(o))
     for k, v in kw.items():

@@ -35,7 +35,7 @@ def test_every_declared_function_is_exported(spmv_lib):
 
 
 def test_abi_version_and_status_strings(spmv_lib):
-    assert S.spmv_abi_version() == 5
+    assert S.spmv_abi_version() == 6
     for code in range(11):
         s = S.spmv_status_string(code)
         assert s and s != "unknown status"

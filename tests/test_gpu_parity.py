@@ -359,6 +359,34 @@ def test_delta_gap_patterns(fmt):
         assert_parity(m, y, TOL16)
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_delta4_decodes(kernel):
+    """4-bit deltas through both decodes (a lane per word; four lanes per
+    word with the planner's per-word offsets): rows of every length class,
+    gaps that need padding, partial segments, rows shared by warps, x in
+    shared memory and through L1; repeat runs give the same bits."""
+    cases = [workloads.llm(0.3, n=1536, seed=6), workloads.llm(0.6, n=3000, seed=8),
+             workloads.llm(0.9, n=2000, seed=2)]
+    lengths = np.tile([0, 1, 0, 3, 9, 0, 257, 0, 5000, 2, 20000, 0, 700, 64, 65], 30)
+    cases.append(workloads.from_lengths("mixed16", lengths, 30000, seed=17, dtype=np.float16))
+    rows = [[0, 15, 30, 31, 47], [16], list(range(0, 4096, 17)), list(range(0, 4096, 2)),
+            list(range(1, 4096, 3)), [4095]]
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])])
+    ci = np.concatenate([np.array(r) for r in rows])
+    rng = np.random.default_rng(3)
+    vals = rng.normal(0, 0.5, ci.size).astype(np.float16)
+    vals[vals == 0] = np.float16(0.25)
+    cases.append(make("gaps", rp, ci, vals, 4096, rng.normal(0, 1, 4096).astype(np.float16)))
+    for m in cases:
+        for xs in (0, 1):
+            opts = S.spmv_plan_options(delta_kernel=kernel, x_smem=xs)
+            ys, info = run_gpu(m, "delta4", options=opts, repeat=2)
+            if m.n_cols * 2 <= 32768:   # a larger x does not fit beside the rings
+                assert info["x_in_smem"] == xs
+            assert np.array_equal(ys[0], ys[1])
+            assert_parity(m, ys[0], TOL16)
+
+
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_plan_from_converted_delta(bits):
     m = workloads.llm(0.75, n=900, seed=4)
