@@ -71,12 +71,12 @@ struct DeltaArgs {
   int n_cols;
 };
 
-template <int B, bool QUAD = false>
+template <int B, bool WIDE = false>
 struct Seg {
   static constexpr int kLaneWords = delta_lane_words(B);
   static constexpr int kWords = 32 * kLaneWords;
   static constexpr int kBytes =
-      (int)(QUAD ? delta_quad_seg_bytes(kWords) : delta_seg_bytes(B, kWords));
+      (int)(WIDE ? delta_wide_seg_bytes(B, kWords) : delta_seg_bytes(B, kWords));
   static_assert(kBytes % 16 == 0, "segment buffers stay 16-byte aligned");
 };
 
@@ -353,56 +353,71 @@ __device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, in
   }
 }
 
-// Four lanes per word (4-bit deltas): lane l takes entries 2q and 2q+1
-// (q = l % 4) of word 8s + l / 4 at step s, so one warp-wide gather covers
-// 32 consecutive entries of 8 consecutive words -- a narrow window of x whose
-// shared-memory reads spread over the banks (at 50% sparsity about 2.2
-// wavefronts per 32 gathers against 3.2 when the lanes hold 32 different
-// words). Each word's starting offset is stored beside it by the planner, so
-// no scan is needed; the lane's two columns are bytes q of the word's
-// doubled nibble prefixes (as in word_prefix<4>).
-template <bool XS, bool SKZ>
-__device__ __forceinline__ void quad_step(const uint2* s_wb, const uint32_t* s_v, int j, int q,
+// Several lanes per word (4 lanes for 4-bit deltas, 8 for 2-bit): lane l
+// takes entries 2q and 2q+1 (q = l % L) of word (32 / L) s + l / L at step
+// s, so one warp-wide gather covers 32 consecutive entries of a few
+// consecutive words -- a narrow window of x whose shared-memory reads spread
+// over the banks (4-bit deltas at 50% sparsity: about 2.2 wavefronts per 32
+// gathers, against 3.2 when the lanes hold 32 different words). Each word's
+// starting offset is stored beside it by the planner, so no scan is needed;
+// the lane's two columns come from the word's doubled prefix sums (as in
+// word_prefix).
+template <int B, bool XS, bool SKZ>
+__device__ __forceinline__ void wide_step(const uint2* s_wb, const uint32_t* s_v, int j, int q,
                                           const XPtr<XS>& p0, float& acc_lo, float& acc_hi) {
+  static_assert(B == 4 || B == 2, "several lanes per word: 2- and 4-bit deltas");
   const uint2 wb = s_wb[j];
-  const uint32_t v = s_v[4 * j + q];
-  const uint32_t lo = (wb.x << 1) & 0x1E1E1E1Eu;
-  const uint32_t hi = (wb.x >> 3) & 0x1E1E1E1Eu;
-  const uint32_t P2 = (lo + hi) * 0x01010101u;
-  const uint32_t Q2 = P2 - hi;
-  const uint32_t sel = 0x4440u + (uint32_t)q;
-  const uint32_t o0 = wb.y + __byte_perm(Q2, 0u, sel);
-  const uint32_t o1 = wb.y + __byte_perm(P2, 0u, sel);
-  fma_pair(acc_lo, acc_hi, v, gather_v<XS, SKZ>(p0, o0, v & 0xFFFFu),
-           gather_v<XS, SKZ>(p0, o1, v >> 16));
+  const uint32_t v = s_v[(16 / B) * j + q];
+  uint32_t o0, o1;
+  if constexpr (B == 4) {
+    const uint32_t lo = (wb.x << 1) & 0x1E1E1E1Eu;
+    const uint32_t hi = (wb.x >> 3) & 0x1E1E1E1Eu;
+    const uint32_t P2 = (lo + hi) * 0x01010101u;  // byte i: 2 x fields 0..2i+1
+    const uint32_t sel = 0x4440u + (uint32_t)q;
+    o0 = __byte_perm(P2 - hi, 0u, sel);            // 2 x fields 0..2q
+    o1 = __byte_perm(P2, 0u, sel);                 // 2 x fields 0..2q+1
+  } else {
+    const uint32_t g = (wb.x & 0x33333333u) + ((wb.x >> 2) & 0x33333333u);
+    const uint32_t lo = (g << 1) & 0x1E1E1E1Eu;
+    const uint32_t hi = (g >> 3) & 0x1E1E1E1Eu;
+    const uint32_t P2 = (lo + hi) * 0x01010101u;  // byte i: 2 x fields 0..4i+3
+    const uint32_t t = (q & 1) ? P2 : P2 - hi;     // byte i: 2 x fields 0..2q+1
+    o1 = __byte_perm(t, 0u, 0x4440u + (uint32_t)(q >> 1));
+    o0 = o1 - ((wb.x >> (4 * q + 1)) & 6u);        // less 2 x field 2q+1
+  }
+  fma_pair(acc_lo, acc_hi, v, gather_v<XS, SKZ>(p0, wb.y + o0, v & 0xFFFFu),
+           gather_v<XS, SKZ>(p0, wb.y + o1, v >> 16));
 }
 
-template <bool XS, bool SKZ>
-__device__ __forceinline__ void decode_segment_quad(const unsigned char* st, int n_w, int base,
+template <int B, bool XS, bool SKZ>
+__device__ __forceinline__ void decode_segment_wide(const unsigned char* st, int n_w, int base,
                                                     int lane, uint32_t xs_addr,
                                                     const __half* x, float (&acc)[4]) {
+  constexpr int L = B == 4 ? 4 : 8;  // lanes per word
+  constexpr int WPS = 32 / L;        // words per step
+  constexpr int kSteps = Seg<B, true>::kWords / WPS;
+  static_assert(kSteps % 8 == 0, "whole blocks of eight steps");
   const uint2* s_wb = reinterpret_cast<const uint2*>(st + kSegHeaderBytes);
   const uint32_t* s_v =
       reinterpret_cast<const uint32_t*>(st + kSegHeaderBytes + ((n_w * 8 + 15) & ~15));
-  const int g = lane >> 2, q = lane & 3;
+  const int g = lane / L, q = lane % L;
   const XPtr<XS> p0 = xptr<XS>(xs_addr, x, base);
-  if (n_w == Seg<4, true>::kWords) {  // the common case: straight-line steps
-    static_assert(Seg<4, true>::kWords % 64 == 0, "whole blocks of eight steps");
-    for (int h = 0; h < Seg<4, true>::kWords / 64; ++h) {
+  if (n_w == Seg<B, true>::kWords) {  // the common case: straight-line steps
+    for (int h = 0; h < kSteps / 8; ++h) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        quad_step<XS, SKZ>(s_wb, s_v, 64 * h + 8 * k + g, q, p0, acc[(2 * k) & 3],
-                           acc[(2 * k + 1) & 3]);
+        wide_step<B, XS, SKZ>(s_wb, s_v, WPS * (8 * h + k) + g, q, p0, acc[(2 * k) & 3],
+                              acc[(2 * k + 1) & 3]);
     }
   } else {
-    for (int j = g; j < n_w; j += 8) quad_step<XS, SKZ>(s_wb, s_v, j, q, p0, acc[0], acc[1]);
+    for (int j = g; j < n_w; j += WPS) wide_step<B, XS, SKZ>(s_wb, s_v, j, q, p0, acc[0], acc[1]);
   }
 }
 
-template <int B, bool XS, bool SKZ, bool QUAD>
+template <int B, bool XS, bool SKZ, bool WIDE>
 __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
     delta_seg_kernel(const DeltaArgs a) {
-  using Sg = Seg<B, QUAD>;
+  using Sg = Seg<B, WIDE>;
   extern __shared__ __align__(128) unsigned char dyn_smem[];
   __shared__ __align__(8) uint64_t s_full[kDW][kDS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -452,8 +467,8 @@ __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
     const int4 h0 = *reinterpret_cast<const int4*>(st);       // base, row | flags, words, split
     const int4 h1 = *reinterpret_cast<const int4*>(st + 16);  // next block's offset, bytes; slot
     const int n_w = h0.z;
-    if constexpr (QUAD)
-      decode_segment_quad<XS, SKZ>(st, n_w, h0.x, lane, xs_addr, a.x, acc);
+    if constexpr (WIDE)
+      decode_segment_wide<B, XS, SKZ>(st, n_w, h0.x, lane, xs_addr, a.x, acc);
     else
       decode_segment_lanes<B, XS, SKZ>(st, n_w, h0.x, lane, xs_addr, a.x, acc);
     // every lane has used the buffer's contents: refill it
@@ -500,23 +515,22 @@ __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
   }
 }
 
-template <int B, bool SKZ, bool QUAD>
-const void* delta_entry_bzq(bool xs) {
-  return xs ? reinterpret_cast<const void*>(&delta_seg_kernel<B, true, SKZ, QUAD>)
-            : reinterpret_cast<const void*>(&delta_seg_kernel<B, false, SKZ, QUAD>);
+template <int B, bool SKZ, bool WIDE>
+const void* delta_entry_bzw(bool xs) {
+  return xs ? reinterpret_cast<const void*>(&delta_seg_kernel<B, true, SKZ, WIDE>)
+            : reinterpret_cast<const void*>(&delta_seg_kernel<B, false, SKZ, WIDE>);
 }
 
-template <int B, bool QUAD>
-const void* delta_entry_bq(bool xs, bool skz) {
-  return skz ? delta_entry_bzq<B, true, QUAD>(xs) : delta_entry_bzq<B, false, QUAD>(xs);
+template <int B, bool WIDE>
+const void* delta_entry_bw(bool xs, bool skz) {
+  return skz ? delta_entry_bzw<B, true, WIDE>(xs) : delta_entry_bzw<B, false, WIDE>(xs);
 }
 
-// quad: the four-lanes-per-word kernel, built for 4-bit deltas only
-const void* delta_entry(int bits, bool quad, bool xs, bool skz) {
-  return bits == 2   ? delta_entry_bq<2, false>(xs, skz)
-         : bits == 8 ? delta_entry_bq<8, false>(xs, skz)
-         : quad      ? delta_entry_bq<4, true>(xs, skz)
-                     : delta_entry_bq<4, false>(xs, skz);
+// wide: several lanes per word, built for 2- and 4-bit deltas
+const void* delta_entry(int bits, bool wide, bool xs, bool skz) {
+  if (bits == 8) return delta_entry_bw<8, false>(xs, skz);
+  if (bits == 2) return wide ? delta_entry_bw<2, true>(xs, skz) : delta_entry_bw<2, false>(xs, skz);
+  return wide ? delta_entry_bw<4, true>(xs, skz) : delta_entry_bw<4, false>(xs, skz);
 }
 
 }  // namespace
@@ -527,29 +541,28 @@ int delta_grid_per_sm(int) { return SPMV_DELTA_GRID_PER_SM; }
 
 int delta_stages(int) { return kDS; }
 
-size_t delta_rings_bytes(int bits, bool quad) {
-  const int seg = bits == 2   ? Seg<2>::kBytes
-                  : bits == 8 ? Seg<8>::kBytes
-                  : quad      ? Seg<4, true>::kBytes
-                              : Seg<4>::kBytes;
+size_t delta_rings_bytes(int bits, bool wide) {
+  const int seg = bits == 8   ? Seg<8>::kBytes
+                  : bits == 2 ? (wide ? Seg<2, true>::kBytes : Seg<2>::kBytes)
+                              : (wide ? Seg<4, true>::kBytes : Seg<4>::kBytes);
   return (size_t)kDW * kDS * seg;
 }
 
 size_t delta_x_smem_bytes(int n_cols) { return ((size_t)n_cols * 2 + 15) / 16 * 16; }
 
-int delta_set_smem_limit(int bits, bool quad, size_t dyn) {
+int delta_set_smem_limit(int bits, bool wide, size_t dyn) {
   if (dyn == 0) return 0;
   for (bool xs : {false, true})
     for (bool skz : {false, true})
-      if (cudaFuncSetAttribute(delta_entry(bits, quad, xs, skz),
+      if (cudaFuncSetAttribute(delta_entry(bits, wide, xs, skz),
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
         return -1;
   return 0;
 }
 
-int delta_kernel_occupancy(int bits, bool quad, bool x_smem, size_t dyn_smem) {
+int delta_kernel_occupancy(int bits, bool wide, bool x_smem, size_t dyn_smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(bits, quad, x_smem, false),
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(bits, wide, x_smem, false),
                                                     kDW * 32, dyn_smem) != cudaSuccess)
     return -1;
   return n;
@@ -571,7 +584,7 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.n_empty = p.n_empty_rows;
   a.n_cols = p.n_cols;
   void* args[] = {&a};
-  return launch_pdl(delta_entry(p.delta_bits, p.delta_quad, p.x_smem, p.delta_skip_zero), p.grid,
+  return launch_pdl(delta_entry(p.delta_bits, p.delta_wide, p.x_smem, p.delta_skip_zero), p.grid,
                     kDW * 32, p.dyn_smem, stream, args);
 }
 

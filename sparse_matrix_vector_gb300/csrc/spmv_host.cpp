@@ -1130,7 +1130,7 @@ spmv_status resolve_format(const spmv_csr* m, const Options& o, spmv_format* for
 // values (padded to 16 bytes; at 2 bits each word's 32 bytes of values are
 // split into two planes of 16-byte halves). One bulk copy stages a block.
 // seg_off receives every block's offset in 16-byte steps (n_segs + 1).
-spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stages, bool quad,
+spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stages, bool wide,
                                std::vector<uint4>* out, std::vector<int32_t>* seg_off) {
   const int32_t bits = delta_bits_of(d);
   const int64_t per = delta_per_word(bits);
@@ -1141,7 +1141,7 @@ spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stag
     for (size_t k = 0; k < n_segs; ++k) {
       (*seg_off)[k] = (int32_t)total;
       const int64_t nw = (int64_t)t.segs[k].end - t.segs[k].begin;
-      total += (quad ? delta_quad_seg_bytes(nw) : delta_seg_bytes(bits, nw)) / 16;
+      total += (wide ? delta_wide_seg_bytes(bits, nw) : delta_seg_bytes(bits, nw)) / 16;
       if (total > INT32_MAX) return SPMV_ERR_TOO_LARGE;
     }
     (*seg_off)[n_segs] = (int32_t)total;
@@ -1169,20 +1169,21 @@ spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stag
     }
     std::memcpy(b, &h, sizeof(h));
     unsigned char* words = b + kSegHeaderBytes;
-    unsigned char* vals = words + delta_pad16(nw * (quad ? 8 : 4));
-    if (quad) {  // {word, doubled column offset of the entry before it}
+    unsigned char* vals = words + delta_pad16(nw * (wide ? 8 : 4));
+    if (wide) {  // {word, doubled column offset of the entry before it}
+      const uint32_t cap = (1u << bits) - 1u;
       uint32_t off2 = 0;
       for (int64_t j = 0; j < nw; ++j) {
         const uint32_t w = d->words[wb + j];
         std::memcpy(words + 8 * j, &w, 4);
         std::memcpy(words + 8 * j + 4, &off2, 4);
-        for (int q = 0; q < 8; ++q) off2 += 2u * ((w >> (4 * q)) & 15u);
+        for (int64_t q = 0; q < per; ++q) off2 += 2u * ((w >> (bits * q)) & cap);
       }
     } else {
       std::memcpy(words, d->words + wb, (size_t)nw * 4);
     }
     const uint16_t* src = d->values + wb * per;
-    if (bits == 2) {  // two planes: halves 0..7 of each word, then 8..15
+    if (bits == 2 && !wide) {  // two planes: halves 0..7 of each word, then 8..15
       for (int64_t j = 0; j < nw; ++j) {
         std::memcpy(vals + 16 * j, src + 16 * j, 16);
         std::memcpy(vals + 16 * (nw + j), src + 16 * j + 8, 16);
@@ -1196,18 +1197,25 @@ spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stag
 
 // x in shared memory: by default when it is at most kXsAutoBytesDelta, and
 // when forced as long as the warps' rings and x fit the CTA's shared memory.
-// The DELTA decode of 4-bit deltas: four lanes per word unless a lane per
-// word is asked for. LLM 12288^2 (us, a lane per word / four lanes per
-// word): 30% sparsity 55.5 / 52.4, 50% 42.9 / 38.6, 70% 29.6 / 27.4,
-// 90% 16.8 / 16.3.
-bool delta_quad_choice(const spmv_delta* d, const Options& o) {
-  return delta_bits_of(d) == 4 && o.delta_kernel != 1;
+// The DELTA decode of 2- and 4-bit deltas: several lanes per word, except
+// for 2-bit deltas that are mostly padding (a lane per word, with the
+// padding skip), or when a lane per word is asked for. LLM 12288^2 (us, a
+// lane per word / several lanes per word): 4-bit deltas at 30 / 50 / 70 /
+// 90% sparsity 55.5 / 52.4, 42.9 / 38.6, 29.6 / 27.4, 16.8 / 16.3; 2-bit
+// deltas 57.8 / 51.3, 44.7 / 42.4, and with 35% and 73% padding at 70% and
+// 90% 36.0 / 43.4, 28.3 / 36.4.
+bool delta_wide_choice(const spmv_delta* d, const Options& o, bool skip_zero) {
+  const int32_t b = delta_bits_of(d);
+  if ((b != 4 && b != 2) || o.delta_kernel == 1) return false;
+  return o.delta_kernel == 2 || b == 4 || !skip_zero;
 }
 
-bool delta_x_fits(int bits, bool quad, int n_cols, int forced, size_t smem_optin) {
+bool delta_skip_zero_choice(const spmv_delta* d);
+
+bool delta_x_fits(int bits, bool wide, int n_cols, int forced, size_t smem_optin) {
   const size_t xb = delta_x_smem_bytes(n_cols);
   const size_t reserve = 4096;  // static shared memory and the runtime's share
-  const bool fits = delta_rings_bytes(bits, quad) + xb + reserve <= smem_optin;
+  const bool fits = delta_rings_bytes(bits, wide) + xb + reserve <= smem_optin;
   return forced == 1 ? fits : forced == -1 ? (fits && xb <= kXsAutoBytesDelta) : false;
 }
 
@@ -1219,6 +1227,15 @@ bool delta_x_fits(int bits, bool quad, int n_cols, int forced, size_t smem_optin
 #define SPMV_DELTA_SKIPZ_PCT 18
 #endif
 constexpr int kDeltaSkipZeroPercent = SPMV_DELTA_SKIPZ_PCT;
+
+// Entries stored as +0.0 (gap padding, row alignment, explicit zeros): when
+// they are a noticeable share, the kernel variant that reads no x for them
+// is used.
+bool delta_skip_zero_choice(const spmv_delta* d) {
+  int64_t zeros = 0;
+  for (int64_t e = 0; e < d->n_entries; ++e) zeros += d->values[e] == 0;
+  return zeros * 100 > d->n_entries * (int64_t)kDeltaSkipZeroPercent;
+}
 
 spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   spmv_status s;
@@ -1233,20 +1250,13 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) !=
       cudaSuccess)
     return SPMV_ERR_CUDA;
-  p->delta_quad = delta_quad_choice(d, o);
-  p->x_smem = delta_x_fits(p->delta_bits, p->delta_quad, d->n_cols, o.x_smem, (size_t)optin);
-  {
-    // entries stored as +0.0 (gap padding, row alignment, explicit zeros):
-    // when they are a noticeable share, the kernel variant that reads no x
-    // for them is used
-    int64_t zeros = 0;
-    for (int64_t e = 0; e < d->n_entries; ++e) zeros += d->values[e] == 0;
-    p->delta_skip_zero = zeros * 100 > d->n_entries * (int64_t)kDeltaSkipZeroPercent;
-  }
-  p->dyn_smem = delta_rings_bytes(p->delta_bits, p->delta_quad) +
+  p->delta_skip_zero = delta_skip_zero_choice(d);
+  p->delta_wide = delta_wide_choice(d, o, p->delta_skip_zero);
+  p->x_smem = delta_x_fits(p->delta_bits, p->delta_wide, d->n_cols, o.x_smem, (size_t)optin);
+  p->dyn_smem = delta_rings_bytes(p->delta_bits, p->delta_wide) +
                 (p->x_smem ? delta_x_smem_bytes(d->n_cols) : 0);
-  if (delta_set_smem_limit(p->delta_bits, p->delta_quad, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
-  const int occ = delta_kernel_occupancy(p->delta_bits, p->delta_quad, p->x_smem, p->dyn_smem);
+  if (delta_set_smem_limit(p->delta_bits, p->delta_wide, p->dyn_smem) != 0) return SPMV_ERR_CUDA;
+  const int occ = delta_kernel_occupancy(p->delta_bits, p->delta_wide, p->x_smem, p->dyn_smem);
   if (occ <= 0) return SPMV_ERR_CUDA;
   const int wpc = delta_warps_per_cta(p->delta_bits);
   SegTables t;
@@ -1257,7 +1267,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
   p->n_tiles = (int64_t)t.segs.size();
   std::vector<uint4> blocks;
   std::vector<int32_t> seg_off;
-  if ((s = build_delta_blocks(d, t, delta_stages(p->delta_bits), p->delta_quad, &blocks,
+  if ((s = build_delta_blocks(d, t, delta_stages(p->delta_bits), p->delta_wide, &blocks,
                               &seg_off)) != SPMV_OK)
     return s;
   if ((s = dev_upload(&p->blocks, blocks.data(), blocks.size() * 16,
@@ -1507,7 +1517,8 @@ spmv_status spmv_plan_inspect(const spmv_csr* m, spmv_format format,
       spmv_delta_free(&d);
       return SPMV_ERR_TOO_LARGE;
     }
-    const bool xs = delta_x_fits(format_delta_bits(format), delta_quad_choice(&d, o), m->n_cols,
+    const bool xs = delta_x_fits(format_delta_bits(format),
+                                 delta_wide_choice(&d, o, delta_skip_zero_choice(&d)), m->n_cols,
                                  o.x_smem, kAssumedSmemOptin);
     const int wpc = delta_warps_per_cta(format_delta_bits(format));
     SegTables t;

@@ -88,11 +88,12 @@ constexpr int64_t delta_pad16(int64_t b) { return (b + 15) & ~(int64_t)15; }
 constexpr int64_t delta_seg_bytes(int bits, int64_t n_w) {
   return kSegHeaderBytes + delta_pad16(n_w * 4) + delta_pad16(n_w * (64 / bits));
 }
-// The four-lanes-per-word layout (4-bit deltas): each word is stored with
-// the doubled column offset, from the segment's starting column, of the
-// entry before it ({word, offset}, 8 bytes), then the values as above.
-constexpr int64_t delta_quad_seg_bytes(int64_t n_w) {
-  return kSegHeaderBytes + delta_pad16(n_w * 8) + delta_pad16(n_w * 16);
+// The several-lanes-per-word layout (2- and 4-bit deltas): each word is
+// stored with the doubled column offset, from the segment's starting
+// column, of the entry before it ({word, offset}, 8 bytes), then the values
+// in entry order (32 / b halves a word).
+constexpr int64_t delta_wide_seg_bytes(int bits, int64_t n_w) {
+  return kSegHeaderBytes + delta_pad16(n_w * 8) + delta_pad16(n_w * (64 / bits));
 }
 // Segment header (DELTA, and CSR with long rows), the first 32 bytes of its
 // block:
@@ -183,7 +184,7 @@ struct Options {
   int interleave;  // CSR products: 0 auto, 1 chunks of 8, 2 element-interleaved
   int sell_sigma;  // SELL sorting window, 0: by the CV of the row lengths
   int csr_kernel;  // CSR: 0 auto, 1 CTA tiles, 2 warp segments (long rows), 3 mixed
-  int delta_kernel;  // DELTA: 0 auto, 1 a lane per word, 2 four lanes per word (4-bit)
+  int delta_kernel;  // DELTA: 0 auto, 1 a lane per word, 2 several lanes per word (2/4-bit)
 };
 
 Options resolve_options(const spmv_plan_options* o, spmv_dtype dtype);
@@ -246,7 +247,7 @@ struct Plan {
   bool x_smem = false;
   int delta_bits = 4;          // DELTA: bits per column delta (2, 4 or 8)
   bool delta_skip_zero = false;  // DELTA: +0.0 entries (padding) read no x
-  bool delta_quad = false;       // DELTA: four lanes per word (4-bit deltas)
+  bool delta_wide = false;       // DELTA: several lanes per word (2- and 4-bit deltas)
   bool interleaved = false;  // CSR: products element-interleaved over the CTA
   bool csr_segments = false;  // CSR: warp-owned row segments
   bool csr_mixed = false;     // CSR segments: packed short rows + slices of long ones
@@ -311,13 +312,13 @@ int csr_kernel_occupancy(spmv_dtype dtype, bool x_smem, bool il, size_t dyn_smem
 size_t csr_stage_bytes(spmv_dtype dtype);
 int csr_set_smem_limit(size_t dyn);
 int delta_warps_per_cta(int bits);      // warps of a DELTA CTA (each with its own ring)
-// `quad`: the four-lanes-per-word kernel (4-bit deltas only)
+// `wide`: the several-lanes-per-word kernel (2- and 4-bit deltas)
 int delta_stages(int bits);              // ring depth per warp
 int delta_grid_per_sm(int bits);         // CTAs per SM the grid uses (at most)
-size_t delta_rings_bytes(int bits, bool quad);  // every stage of every warp of a CTA
+size_t delta_rings_bytes(int bits, bool wide);  // every stage of every warp of a CTA
 size_t delta_x_smem_bytes(int n_cols);
-int delta_set_smem_limit(int bits, bool quad, size_t dyn);
-int delta_kernel_occupancy(int bits, bool quad, bool x_smem, size_t dyn_smem);
+int delta_set_smem_limit(int bits, bool wide, size_t dyn);
+int delta_kernel_occupancy(int bits, bool wide, bool x_smem, size_t dyn_smem);
 // `skip`: a device flag read at launch (after the kernels the launch depends
 // on); when it is set the product is skipped (conjugate gradients, after
 // convergence). nullptr for ordinary runs.

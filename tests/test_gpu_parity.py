@@ -359,10 +359,12 @@ def test_delta_gap_patterns(fmt):
         assert_parity(m, y, TOL16)
 
 
+@pytest.mark.parametrize("fmt", ["delta4", "delta2"])
 @pytest.mark.parametrize("kernel", [1, 2])
-def test_delta4_decodes(kernel):
-    """4-bit deltas through both decodes (a lane per word; four lanes per
-    word with the planner's per-word offsets): rows of every length class,
+def test_delta_decodes(kernel, fmt):
+    """2- and 4-bit deltas through both decodes (a lane per word; several
+    lanes per word -- 4 for 4-bit, 8 for 2-bit deltas -- with the planner's
+    per-word offsets): rows of every length class,
     gaps that need padding, partial segments, rows shared by warps, x in
     shared memory and through L1; repeat runs give the same bits."""
     cases = [workloads.llm(0.3, n=1536, seed=6), workloads.llm(0.6, n=3000, seed=8),
@@ -380,7 +382,7 @@ def test_delta4_decodes(kernel):
     for m in cases:
         for xs in (0, 1):
             opts = S.spmv_plan_options(delta_kernel=kernel, x_smem=xs)
-            ys, info = run_gpu(m, "delta4", options=opts, repeat=2)
+            ys, info = run_gpu(m, fmt, options=opts, repeat=2)
             if m.n_cols * 2 <= 32768:   # a larger x does not fit beside the rings
                 assert info["x_in_smem"] == xs
             assert np.array_equal(ys[0], ys[1])
