@@ -284,8 +284,11 @@ __global__ void __launch_bounds__(kCW<VT, MIXED> * 32, 1) csr_seg_kernel(const C
     if (kChecked) check_segment<VT>(a, st, nz, (MIXED && (rf & kSegPacked)) ? h0.x : 0, lane);
     if (MIXED && (rf & kSegPacked)) {
       packed_rows<VT, XS, Sg::kK>(a, st, h0.x, nz, (int)(rf & kSegRowMask), lane, xs);
+      // the products written into the buffer are ordered before the bulk
+      // copy's writes into it
       __syncwarp();
       if (lane == s && h1.y > 0) {
+        fence_proxy_async_smem();
         mbar_arrive_expect_tx(&s_full[warp][s], (uint32_t)h1.y);
         bulk_g2s(ring + s * kBytes, a.blocks + (size_t)h1.x * 16, (uint32_t)h1.y,
                  &s_full[warp][s], pol);

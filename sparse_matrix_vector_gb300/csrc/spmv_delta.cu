@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "spmv_device.cuh"
 #include "spmv_internal.h"
@@ -359,14 +360,18 @@ __device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, in
 // consecutive words -- a narrow window of x whose shared-memory reads spread
 // over the banks (4-bit deltas at 50% sparsity: about 2.2 wavefronts per 32
 // gathers, against 3.2 when the lanes hold 32 different words). Each word's
-// starting offset is stored beside it by the planner, so no scan is needed;
-// the lane's two columns come from the word's doubled prefix sums (as in
-// word_prefix).
+// starting offset (doubled, from the segment's base) is stored by the
+// planner, so no scan is needed; the lane's two columns come from the word's
+// doubled prefix sums (as in word_prefix).
+template <int B>
+using WideOff = std::conditional_t<delta_wide_off_bytes(B) == 2, uint16_t, uint32_t>;
+
 template <int B, bool XS, bool SKZ>
-__device__ __forceinline__ void wide_step(const uint2* s_wb, const uint32_t* s_v, int j, int q,
-                                          const XPtr<XS>& p0, float& acc_lo, float& acc_hi) {
+__device__ __forceinline__ void wide_step(const uint32_t* s_w, const WideOff<B>* s_o,
+                                          const uint32_t* s_v, int j, int q, const XPtr<XS>& p0,
+                                          float& acc_lo, float& acc_hi) {
   static_assert(B == 4 || B == 2, "several lanes per word: 2- and 4-bit deltas");
-  const uint2 wb = s_wb[j];
+  const uint2 wb = make_uint2(s_w[j], s_o[j]);
   const uint32_t v = s_v[(16 / B) * j + q];
   uint32_t o0, o1;
   if constexpr (B == 4) {
@@ -397,20 +402,23 @@ __device__ __forceinline__ void decode_segment_wide(const unsigned char* st, int
   constexpr int WPS = 32 / L;        // words per step
   constexpr int kSteps = Seg<B, true>::kWords / WPS;
   static_assert(kSteps % 8 == 0, "whole blocks of eight steps");
-  const uint2* s_wb = reinterpret_cast<const uint2*>(st + kSegHeaderBytes);
+  const uint32_t* s_w = reinterpret_cast<const uint32_t*>(st + kSegHeaderBytes);
+  const unsigned char* offs = st + kSegHeaderBytes + ((n_w * 4 + 15) & ~15);
+  const WideOff<B>* s_o = reinterpret_cast<const WideOff<B>*>(offs);
   const uint32_t* s_v =
-      reinterpret_cast<const uint32_t*>(st + kSegHeaderBytes + ((n_w * 8 + 15) & ~15));
+      reinterpret_cast<const uint32_t*>(offs + ((n_w * delta_wide_off_bytes(B) + 15) & ~15));
   const int g = lane / L, q = lane % L;
   const XPtr<XS> p0 = xptr<XS>(xs_addr, x, base);
   if (n_w == Seg<B, true>::kWords) {  // the common case: straight-line steps
     for (int h = 0; h < kSteps / 8; ++h) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        wide_step<B, XS, SKZ>(s_wb, s_v, WPS * (8 * h + k) + g, q, p0, acc[(2 * k) & 3],
+        wide_step<B, XS, SKZ>(s_w, s_o, s_v, WPS * (8 * h + k) + g, q, p0, acc[(2 * k) & 3],
                               acc[(2 * k + 1) & 3]);
     }
   } else {
-    for (int j = g; j < n_w; j += WPS) wide_step<B, XS, SKZ>(s_wb, s_v, j, q, p0, acc[0], acc[1]);
+    for (int j = g; j < n_w; j += WPS)
+      wide_step<B, XS, SKZ>(s_w, s_o, s_v, j, q, p0, acc[0], acc[1]);
   }
 }
 

@@ -1169,18 +1169,22 @@ spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stag
     }
     std::memcpy(b, &h, sizeof(h));
     unsigned char* words = b + kSegHeaderBytes;
-    unsigned char* vals = words + delta_pad16(nw * (wide ? 8 : 4));
-    if (wide) {  // {word, doubled column offset of the entry before it}
+    unsigned char* offs = words + delta_pad16(nw * 4);
+    unsigned char* vals = wide ? offs + delta_pad16(nw * delta_wide_off_bytes(bits)) : offs;
+    std::memcpy(words, d->words + wb, (size_t)nw * 4);
+    if (wide) {  // each word's doubled column offset of the entry before it
       const uint32_t cap = (1u << bits) - 1u;
       uint32_t off2 = 0;
       for (int64_t j = 0; j < nw; ++j) {
         const uint32_t w = d->words[wb + j];
-        std::memcpy(words + 8 * j, &w, 4);
-        std::memcpy(words + 8 * j + 4, &off2, 4);
+        if (delta_wide_off_bytes(bits) == 2) {
+          const uint16_t o = (uint16_t)off2;
+          std::memcpy(offs + 2 * j, &o, 2);
+        } else {
+          std::memcpy(offs + 4 * j, &off2, 4);
+        }
         for (int64_t q = 0; q < per; ++q) off2 += 2u * ((w >> (bits * q)) & cap);
       }
-    } else {
-      std::memcpy(words, d->words + wb, (size_t)nw * 4);
     }
     const uint16_t* src = d->values + wb * per;
     if (bits == 2 && !wide) {  // two planes: halves 0..7 of each word, then 8..15
