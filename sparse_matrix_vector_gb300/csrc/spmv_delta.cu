@@ -77,7 +77,7 @@ struct Seg {
   static constexpr int kLaneWords = delta_lane_words(B);
   static constexpr int kWords = 32 * kLaneWords;
   static constexpr int kBytes =
-      (int)(WIDE ? delta_wide_seg_bytes(B, kWords) : delta_seg_bytes(B, kWords));
+      (int)(WIDE ? delta_wide_seg_bytes_max(B) : delta_seg_bytes(B, kWords));
   static_assert(kBytes % 16 == 0, "segment buffers stay 16-byte aligned");
 };
 
@@ -355,71 +355,109 @@ __device__ __forceinline__ void decode_segment_lanes(const unsigned char* st, in
 }
 
 // Several lanes per word (4 lanes for 4-bit deltas, 8 for 2-bit): lane l
-// takes entries 2q and 2q+1 (q = l % L) of word (32 / L) s + l / L at step
-// s, so one warp-wide gather covers 32 consecutive entries of a few
-// consecutive words -- a narrow window of x whose shared-memory reads spread
-// over the banks (4-bit deltas at 50% sparsity: about 2.2 wavefronts per 32
-// gathers, against 3.2 when the lanes hold 32 different words). Each word's
-// starting offset (doubled, from the segment's base) is stored by the
-// planner, so no scan is needed; the lane's two columns come from the word's
-// doubled prefix sums (as in word_prefix).
-template <int B>
-using WideOff = std::conditional_t<delta_wide_off_bytes(B) == 2, uint16_t, uint32_t>;
-
+// takes entries 2q and 2q+1 (q = l % L) of word W s + l / L at step s, so
+// one warp-wide gather covers 32 entries of a few consecutive words -- a
+// narrow window of x whose shared-memory reads spread over the banks (4-bit
+// deltas at 50% sparsity: about 2.2 wavefronts per 32 gathers, against 3.2
+// when the lanes hold 32 different words). Each word's starting offset
+// (doubled, from the segment's base) is stored by the planner, so no scan
+// is needed; the lane's two columns come from the word's doubled prefix
+// sums (as in word_prefix). Words, offsets and values are stored in blocks
+// of four steps, so that a lane loads a block's with three vector loads
+// (five shared-memory loads a step, two of them gathers, would otherwise
+// fill the load queue).
 template <int B, bool XS, bool SKZ>
-__device__ __forceinline__ void wide_step(const uint32_t* s_w, const WideOff<B>* s_o,
-                                          const uint32_t* s_v, int j, int q, const XPtr<XS>& p0,
-                                          float& acc_lo, float& acc_hi) {
+__device__ __forceinline__ void wide_pair(uint32_t w, uint32_t off, uint32_t v, int q,
+                                          const XPtr<XS>& p0, float& acc_lo, float& acc_hi) {
   static_assert(B == 4 || B == 2, "several lanes per word: 2- and 4-bit deltas");
-  const uint2 wb = make_uint2(s_w[j], s_o[j]);
-  const uint32_t v = s_v[(16 / B) * j + q];
   uint32_t o0, o1;
   if constexpr (B == 4) {
-    const uint32_t lo = (wb.x << 1) & 0x1E1E1E1Eu;
-    const uint32_t hi = (wb.x >> 3) & 0x1E1E1E1Eu;
+    const uint32_t lo = (w << 1) & 0x1E1E1E1Eu;
+    const uint32_t hi = (w >> 3) & 0x1E1E1E1Eu;
     const uint32_t P2 = (lo + hi) * 0x01010101u;  // byte i: 2 x fields 0..2i+1
     const uint32_t sel = 0x4440u + (uint32_t)q;
     o0 = __byte_perm(P2 - hi, 0u, sel);            // 2 x fields 0..2q
     o1 = __byte_perm(P2, 0u, sel);                 // 2 x fields 0..2q+1
   } else {
-    const uint32_t g = (wb.x & 0x33333333u) + ((wb.x >> 2) & 0x33333333u);
+    const uint32_t g = (w & 0x33333333u) + ((w >> 2) & 0x33333333u);
     const uint32_t lo = (g << 1) & 0x1E1E1E1Eu;
     const uint32_t hi = (g >> 3) & 0x1E1E1E1Eu;
     const uint32_t P2 = (lo + hi) * 0x01010101u;  // byte i: 2 x fields 0..4i+3
     const uint32_t t = (q & 1) ? P2 : P2 - hi;     // byte i: 2 x fields 0..2q+1
     o1 = __byte_perm(t, 0u, 0x4440u + (uint32_t)(q >> 1));
-    o0 = o1 - ((wb.x >> (4 * q + 1)) & 6u);        // less 2 x field 2q+1
+    o0 = o1 - ((w >> (4 * q + 1)) & 6u);           // less 2 x field 2q+1
   }
-  fma_pair(acc_lo, acc_hi, v, gather_v<XS, SKZ>(p0, wb.y + o0, v & 0xFFFFu),
-           gather_v<XS, SKZ>(p0, wb.y + o1, v >> 16));
+  fma_pair(acc_lo, acc_hi, v, gather_v<XS, SKZ>(p0, off + o0, v & 0xFFFFu),
+           gather_v<XS, SKZ>(p0, off + o1, v >> 16));
+}
+
+// The several-lanes layout's constants for B-bit deltas.
+template <int B>
+struct Wide {
+  static constexpr int kL = delta_wide_lanes(B);         // lanes per word
+  static constexpr int kW = delta_wide_step_words(B);    // words per step
+  static constexpr int kBW = delta_wide_block_words(B);  // words per block of four steps
+  static constexpr int kOB = delta_wide_off_bytes(B);    // bytes per word offset
+};
+template <int B>
+using WideOff = std::conditional_t<Wide<B>::kOB == 2, uint16_t, uint32_t>;
+
+// One block of four steps: the lane's four words, offsets and values.
+template <int B, bool XS, bool SKZ>
+__device__ __forceinline__ void wide_block(const unsigned char* bw, const unsigned char* bo,
+                                           const unsigned char* bv, int h, int g, int lane,
+                                           int q, const XPtr<XS>& p0, float (&acc)[4]) {
+  constexpr int W = Wide<B>::kW;
+  const uint4 w = reinterpret_cast<const uint4*>(bw)[h * W + g];
+  const uint4 v = reinterpret_cast<const uint4*>(bv)[h * 32 + lane];
+  uint32_t o[4];
+  if constexpr (Wide<B>::kOB == 2) {
+    const uint2 t = reinterpret_cast<const uint2*>(bo)[h * W + g];
+    o[0] = t.x & 0xFFFFu;
+    o[1] = t.x >> 16;
+    o[2] = t.y & 0xFFFFu;
+    o[3] = t.y >> 16;
+  } else {
+    const uint4 t = reinterpret_cast<const uint4*>(bo)[h * W + g];
+    o[0] = t.x;
+    o[1] = t.y;
+    o[2] = t.z;
+    o[3] = t.w;
+  }
+  wide_pair<B, XS, SKZ>(w.x, o[0], v.x, q, p0, acc[0], acc[1]);
+  wide_pair<B, XS, SKZ>(w.y, o[1], v.y, q, p0, acc[2], acc[3]);
+  wide_pair<B, XS, SKZ>(w.z, o[2], v.z, q, p0, acc[0], acc[1]);
+  wide_pair<B, XS, SKZ>(w.w, o[3], v.w, q, p0, acc[2], acc[3]);
 }
 
 template <int B, bool XS, bool SKZ>
 __device__ __forceinline__ void decode_segment_wide(const unsigned char* st, int n_w, int base,
                                                     int lane, uint32_t xs_addr,
                                                     const __half* x, float (&acc)[4]) {
-  constexpr int L = B == 4 ? 4 : 8;  // lanes per word
-  constexpr int WPS = 32 / L;        // words per step
-  constexpr int kSteps = Seg<B, true>::kWords / WPS;
-  static_assert(kSteps % 8 == 0, "whole blocks of eight steps");
-  const uint32_t* s_w = reinterpret_cast<const uint32_t*>(st + kSegHeaderBytes);
-  const unsigned char* offs = st + kSegHeaderBytes + ((n_w * 4 + 15) & ~15);
-  const WideOff<B>* s_o = reinterpret_cast<const WideOff<B>*>(offs);
-  const uint32_t* s_v =
-      reinterpret_cast<const uint32_t*>(offs + ((n_w * delta_wide_off_bytes(B) + 15) & ~15));
+  constexpr int L = Wide<B>::kL, W = Wide<B>::kW, BW = Wide<B>::kBW, OB = Wide<B>::kOB;
+  constexpr int kBlocks = Seg<B, true>::kWords / BW;
   const int g = lane / L, q = lane % L;
   const XPtr<XS> p0 = xptr<XS>(xs_addr, x, base);
-  if (n_w == Seg<B, true>::kWords) {  // the common case: straight-line steps
-    for (int h = 0; h < kSteps / 8; ++h) {
+  const unsigned char* bw = st + kSegHeaderBytes;
+  if (n_w == Seg<B, true>::kWords) {  // the common case: straight-line blocks
+    const unsigned char* bo = bw + kBlocks * W * 16;
+    const unsigned char* bv = bo + kBlocks * W * 4 * OB;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        wide_step<B, XS, SKZ>(s_w, s_o, s_v, WPS * (8 * h + k) + g, q, p0, acc[(2 * k) & 3],
-                              acc[(2 * k + 1) & 3]);
-    }
-  } else {
-    for (int j = g; j < n_w; j += WPS)
-      wide_step<B, XS, SKZ>(s_w, s_o, s_v, j, q, p0, acc[0], acc[1]);
+    for (int h = 0; h < kBlocks; ++h) wide_block<B, XS, SKZ>(bw, bo, bv, h, g, lane, q, p0, acc);
+    return;
   }
+  const int nb = n_w / BW, nt = n_w - nb * BW;
+  const unsigned char* bo = bw + nb * W * 16;
+  const unsigned char* bv = bo + nb * W * 4 * OB;
+  for (int h = 0; h < nb; ++h) wide_block<B, XS, SKZ>(bw, bo, bv, h, g, lane, q, p0, acc);
+  // the words after the last whole block, in plain order
+  const uint32_t* tw = reinterpret_cast<const uint32_t*>(bv + nb * 512);
+  const WideOff<B>* to = reinterpret_cast<const WideOff<B>*>(
+      reinterpret_cast<const unsigned char*>(tw) + ((nt * 4 + 15) & ~15));
+  const uint32_t* tv = reinterpret_cast<const uint32_t*>(
+      reinterpret_cast<const unsigned char*>(to) + ((nt * OB + 15) & ~15));
+  for (int t = g; t < nt; t += W)
+    wide_pair<B, XS, SKZ>(tw[t], to[t], tv[t * L + q], q, p0, acc[0], acc[1]);
 }
 
 template <int B, bool XS, bool SKZ, bool WIDE>

@@ -1124,11 +1124,67 @@ spmv_status resolve_format(const spmv_csr* m, const Options& o, spmv_format* for
   return SPMV_OK;
 }
 
+// The data of one segment in the several-lanes-per-word layout (the block
+// layout described with delta_wide_seg_bytes): nw words of b-bit fields and
+// their values (32 / b halves a word) into `out`.
+void write_delta_wide(int bits, const uint32_t* words, const uint16_t* values, int64_t nw,
+                      unsigned char* out) {
+  const int L = delta_wide_lanes(bits), W = delta_wide_step_words(bits);
+  const int BW = delta_wide_block_words(bits), ob = delta_wide_off_bytes(bits);
+  const int64_t per = 32 / bits, nb = nw / BW, nt = nw % BW;
+  const uint32_t cap = (1u << bits) - 1u;
+  std::vector<uint32_t> off2((size_t)nw);
+  uint32_t o = 0;
+  for (int64_t j = 0; j < nw; ++j) {
+    off2[j] = o;
+    for (int64_t q = 0; q < per; ++q) o += 2u * ((words[j] >> (bits * q)) & cap);
+  }
+  auto put_off = [ob](unsigned char* at, uint32_t v) {
+    if (ob == 2) {
+      const uint16_t h = (uint16_t)v;
+      std::memcpy(at, &h, 2);
+    } else {
+      std::memcpy(at, &v, 4);
+    }
+  };
+  // value word q (halves 2q, 2q + 1) of word j
+  auto val32 = [values, per](int64_t j, int q) {
+    uint32_t v;
+    std::memcpy(&v, values + j * per + 2 * q, 4);
+    return v;
+  };
+  unsigned char* bw = out;
+  unsigned char* bo = bw + nb * W * 16;
+  unsigned char* bv = bo + nb * W * 4 * ob;
+  for (int64_t h = 0; h < nb; ++h)
+    for (int g = 0; g < W; ++g)
+      for (int k = 0; k < 4; ++k) {
+        const int64_t j = (int64_t)BW * h + (int64_t)W * k + g;
+        std::memcpy(bw + ((h * W + g) * 4 + k) * 4, words + j, 4);
+        put_off(bo + ((h * W + g) * 4 + k) * ob, off2[j]);
+        for (int q = 0; q < L; ++q) {
+          const uint32_t v = val32(j, q);
+          std::memcpy(bv + ((h * 32 + (int64_t)g * L + q) * 4 + k) * 4, &v, 4);
+        }
+      }
+  unsigned char* tw = bv + nb * 512;
+  unsigned char* to = tw + delta_pad16(nt * 4);
+  unsigned char* tv = to + delta_pad16(nt * ob);
+  for (int64_t t = 0; t < nt; ++t) {
+    const int64_t j = nb * BW + t;
+    std::memcpy(tw + 4 * t, words + j, 4);
+    put_off(to + ob * t, off2[j]);
+  }
+  std::memcpy(tv, values + nb * BW * per, (size_t)(nt * per) * 2);
+}
+
 // Device layout of a DELTA plan: one block per segment, back to back in
 // segment order (so each warp's share is contiguous), each block a 32-byte
-// header (SegHeader), the segment's words (padded to 16 bytes) and their
-// values (padded to 16 bytes; at 2 bits each word's 32 bytes of values are
-// split into two planes of 16-byte halves). One bulk copy stages a block.
+// header (SegHeader) and the segment's data. A lane per word: the words
+// (padded to 16 bytes) and their values (padded to 16 bytes; at 2 bits each
+// word's 32 bytes of values are split into two planes of 16-byte halves).
+// Several lanes per word (wide): write_delta_wide. One bulk copy stages a
+// block.
 // seg_off receives every block's offset in 16-byte steps (n_segs + 1).
 spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stages, bool wide,
                                std::vector<uint4>* out, std::vector<int32_t>* seg_off) {
@@ -1169,25 +1225,14 @@ spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stag
     }
     std::memcpy(b, &h, sizeof(h));
     unsigned char* words = b + kSegHeaderBytes;
-    unsigned char* offs = words + delta_pad16(nw * 4);
-    unsigned char* vals = wide ? offs + delta_pad16(nw * delta_wide_off_bytes(bits)) : offs;
-    std::memcpy(words, d->words + wb, (size_t)nw * 4);
-    if (wide) {  // each word's doubled column offset of the entry before it
-      const uint32_t cap = (1u << bits) - 1u;
-      uint32_t off2 = 0;
-      for (int64_t j = 0; j < nw; ++j) {
-        const uint32_t w = d->words[wb + j];
-        if (delta_wide_off_bytes(bits) == 2) {
-          const uint16_t o = (uint16_t)off2;
-          std::memcpy(offs + 2 * j, &o, 2);
-        } else {
-          std::memcpy(offs + 4 * j, &off2, 4);
-        }
-        for (int64_t q = 0; q < per; ++q) off2 += 2u * ((w >> (bits * q)) & cap);
-      }
-    }
     const uint16_t* src = d->values + wb * per;
-    if (bits == 2 && !wide) {  // two planes: halves 0..7 of each word, then 8..15
+    if (wide) {
+      write_delta_wide(bits, d->words + wb, src, nw, words);
+      continue;
+    }
+    unsigned char* vals = words + delta_pad16(nw * 4);
+    std::memcpy(words, d->words + wb, (size_t)nw * 4);
+    if (bits == 2) {  // two planes: halves 0..7 of each word, then 8..15
       for (int64_t j = 0; j < nw; ++j) {
         std::memcpy(vals + 16 * j, src + 16 * j, 16);
         std::memcpy(vals + 16 * (nw + j), src + 16 * j + 8, 16);

@@ -88,20 +88,43 @@ constexpr int64_t delta_pad16(int64_t b) { return (b + 15) & ~(int64_t)15; }
 constexpr int64_t delta_seg_bytes(int bits, int64_t n_w) {
   return kSegHeaderBytes + delta_pad16(n_w * 4) + delta_pad16(n_w * (64 / bits));
 }
-// The several-lanes-per-word layout (2- and 4-bit deltas): the words, then
-// for each word the doubled column offset, from the segment's starting
-// column, of the entry before it, then the values in entry order (32 / b
-// halves a word), each part padded to 16 bytes. The offsets are uint16 for
-// 4-bit deltas (at most 2 x 127 words x 120 = 30,480): 2 bytes a word where
-// 4 would add a fifth to the block (LLM 12288^2 at 30% sparsity 51.3 ->
-// 48.6 us); for 2-bit deltas, whose words carry 36 bytes, uint32 measured
-// no slower (53.6 / 55.1 us at 30%).
+// The several-lanes-per-word layout (2- and 4-bit deltas). Each word has a
+// doubled column offset, from the segment's starting column, of the entry
+// before it: uint16 for 4-bit deltas (at most 2 x 127 words x 120 = 30,480;
+// 2 bytes a word where 4 would add a fifth to the block: LLM 12288^2 at 30%
+// sparsity 51.3 -> 48.6 us), uint32 for 2-bit deltas (their words carry 36
+// bytes; uint16 measured no faster). L lanes share a word (4 for 4-bit
+// deltas, 8 for 2-bit), a warp-wide step covers W = 32 / L words, and the
+// words are stored in blocks of four steps (4 W words) so that a lane loads
+// a block's words, offsets and values with three vector loads:
+//   block h, lane l = g L + q (g = l / L, q = l % L), step k < 4 covers word
+//   j = 4 W h + W k + g, whose 32-bit value word q the lane multiplies:
+//   words   uint32 [h][g][k]      (16 bytes per (h, g))
+//   offsets uint16/32 [h][g][k]
+//   values  uint32 [h][l][k]      (16 bytes per (h, l))
+// The n_w mod 4 W words after the last whole block follow in plain order:
+// their words, their offsets (each part padded to 16 bytes) and their
+// values (L uint32 a word).
 constexpr int delta_wide_off_bytes(int bits) { return bits == 4 ? 2 : 4; }
 static_assert(2 * (delta_seg_words(4) - 1) * 8 * 15 < 65536,
               "a 4-bit segment's doubled word offsets fit uint16");
+constexpr int delta_wide_lanes(int bits) { return bits == 4 ? 4 : 8; }
+constexpr int delta_wide_step_words(int bits) { return 32 / delta_wide_lanes(bits); }
+constexpr int delta_wide_block_words(int bits) { return 4 * delta_wide_step_words(bits); }
+constexpr int64_t delta_wide_block_bytes(int bits) {
+  return delta_wide_block_words(bits) * (4 + delta_wide_off_bytes(bits) + 64 / bits);
+}
 constexpr int64_t delta_wide_seg_bytes(int bits, int64_t n_w) {
-  return kSegHeaderBytes + delta_pad16(n_w * 4) +
-         delta_pad16(n_w * delta_wide_off_bytes(bits)) + delta_pad16(n_w * (64 / bits));
+  const int64_t nb = n_w / delta_wide_block_words(bits), nt = n_w % delta_wide_block_words(bits);
+  return kSegHeaderBytes + nb * delta_wide_block_bytes(bits) + delta_pad16(nt * 4) +
+         delta_pad16(nt * delta_wide_off_bytes(bits)) + nt * (64 / bits);
+}
+// The largest block of a segment (its ring buffer's size).
+constexpr int64_t delta_wide_seg_bytes_max(int bits) {
+  int64_t m = 0;
+  for (int64_t n = 0; n <= delta_seg_words(bits); ++n)
+    m = delta_wide_seg_bytes(bits, n) > m ? delta_wide_seg_bytes(bits, n) : m;
+  return m;
 }
 // Segment header (DELTA, and CSR with long rows), the first 32 bytes of its
 // block:
