@@ -37,7 +37,10 @@ namespace spmv {
 namespace {
 
 #ifndef SPMV_DELTA_WARPS
-#define SPMV_DELTA_WARPS 28
+#define SPMV_DELTA_WARPS 20
+#endif
+#ifndef SPMV_DELTA_WARPS_B8
+#define SPMV_DELTA_WARPS_B8 28
 #endif
 #ifndef SPMV_DELTA_STAGES
 #define SPMV_DELTA_STAGES 2
@@ -48,13 +51,21 @@ namespace {
 #ifndef SPMV_DELTA_MIN_BLOCKS
 #define SPMV_DELTA_MIN_BLOCKS 1
 #endif
-// Warps per CTA; each has a ring of kStages segment buffers. One CTA per SM:
-// the rings and x fill its shared memory. Measured on the 12288^2 LLM
-// matrices (fraction of HBM peak at 30 / 50 / 70 / 90% sparsity): 28 warps x
-// 2 stages 0.70 / 0.65 / 0.57 / 0.41; 24 x 3 0.68 / 0.62 / 0.53 / 0.38;
-// 16 x 4 0.67 / 0.62 / 0.54 / 0.39; two CTAs of 14 x 2 per SM, or one CTA of
-// 14 x 2 leaving room for the next launch's CTA, no better.
-constexpr int kDW = SPMV_DELTA_WARPS;
+
+// Warps per CTA for B-bit deltas; each has a ring of kDS segment buffers.
+// One CTA per SM. Fewer warps leave each thread more registers (the
+// several-lanes decode of 4-bit deltas uses 96 at 20 warps, 72 at 28),
+// which keeps more of a block's loads and gathers in flight. Measured on the
+// 12288^2 LLM matrices (fraction of HBM peak at 30 / 50 / 70 / 90%
+// sparsity), 4-bit deltas: 20 warps x 2 stages 0.84 / 0.79 / 0.66 / 0.45;
+// 16 x 2 0.83 / 0.79 / 0.66 / 0.45; 24 x 2 0.84 / 0.79 / 0.64 / 0.45; 28 x 2
+// 0.80 / 0.79 / 0.63 / 0.43; 16 x 3, 12 x 3, 12 x 4 and 8 x 4 slower; two
+// CTAs of 14 x 2 per SM no better, one CTA of 14 x 2 leaving room for the
+// next launch's CTA slower. 2-bit deltas at 30 / 70 / 90%: 20 warps 0.71 /
+// 0.66 / 0.67, 28 warps 0.71 / 0.63 / 0.65. 8-bit deltas at 50 / 90%: 20
+// warps 0.67 / 0.41, 28 warps 0.70 / 0.41.
+template <int B>
+constexpr int kDW = B == 8 ? SPMV_DELTA_WARPS_B8 : SPMV_DELTA_WARPS;
 constexpr int kDS = SPMV_DELTA_STAGES;
 
 struct DeltaArgs {
@@ -86,7 +97,7 @@ struct Seg {
 // synchronises).
 __device__ __forceinline__ void copy_x_half(uint16_t* xs, const __half* x, int n) {
   const uint16_t* src = reinterpret_cast<const uint16_t*>(x);
-  const int nt = kDW * 32;
+  const int nt = blockDim.x;
   int done = 0;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
     const int nv = n >> 3;
@@ -461,15 +472,15 @@ __device__ __forceinline__ void decode_segment_wide(const unsigned char* st, int
 }
 
 template <int B, bool XS, bool SKZ, bool WIDE>
-__global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
+__global__ void __launch_bounds__(kDW<B> * 32, SPMV_DELTA_MIN_BLOCKS)
     delta_seg_kernel(const DeltaArgs a) {
   using Sg = Seg<B, WIDE>;
   extern __shared__ __align__(128) unsigned char dyn_smem[];
-  __shared__ __align__(8) uint64_t s_full[kDW][kDS];
+  __shared__ __align__(8) uint64_t s_full[kDW<B>][kDS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kDW + warp;
+  const int gw = blockIdx.x * kDW<B> + warp;
   unsigned char* ring = dyn_smem + (size_t)warp * kDS * Sg::kBytes;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(dyn_smem + (size_t)kDW * kDS * Sg::kBytes);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(dyn_smem + (size_t)kDW<B> * kDS * Sg::kBytes);
   const int t0 = __ldg(a.warp_first + gw);
   const int n = __ldg(a.warp_first + gw + 1) - t0;
   const uint64_t pol = policy_evict_first();
@@ -490,7 +501,7 @@ __global__ void __launch_bounds__(kDW * 32, SPMV_DELTA_MIN_BLOCKS)
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();
   if (XS) copy_x_half(xs, a.x, a.n_cols);
-  for (int i = blockIdx.x * kDW * 32 + threadIdx.x; i < a.n_empty; i += gridDim.x * kDW * 32)
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_empty; i += gridDim.x * blockDim.x)
     a.y[__ldg(a.empty_rows + i)] = 0.f;
   if (XS) __syncthreads();
   const uint32_t xs_addr = smem_u32(xs);
@@ -581,7 +592,7 @@ const void* delta_entry(int bits, bool wide, bool xs, bool skz) {
 
 }  // namespace
 
-int delta_warps_per_cta(int) { return kDW; }
+int delta_warps_per_cta(int bits) { return bits == 8 ? kDW<8> : kDW<4>; }
 
 int delta_grid_per_sm(int) { return SPMV_DELTA_GRID_PER_SM; }
 
@@ -591,7 +602,7 @@ size_t delta_rings_bytes(int bits, bool wide) {
   const int seg = bits == 8   ? Seg<8>::kBytes
                   : bits == 2 ? (wide ? Seg<2, true>::kBytes : Seg<2>::kBytes)
                               : (wide ? Seg<4, true>::kBytes : Seg<4>::kBytes);
-  return (size_t)kDW * kDS * seg;
+  return (size_t)delta_warps_per_cta(bits) * kDS * seg;
 }
 
 size_t delta_x_smem_bytes(int n_cols) { return ((size_t)n_cols * 2 + 15) / 16 * 16; }
@@ -609,7 +620,8 @@ int delta_set_smem_limit(int bits, bool wide, size_t dyn) {
 int delta_kernel_occupancy(int bits, bool wide, bool x_smem, size_t dyn_smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, delta_entry(bits, wide, x_smem, false),
-                                                    kDW * 32, dyn_smem) != cudaSuccess)
+                                                    delta_warps_per_cta(bits) * 32,
+                                                    dyn_smem) != cudaSuccess)
     return -1;
   return n;
 }
@@ -631,7 +643,7 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.n_cols = p.n_cols;
   void* args[] = {&a};
   return launch_pdl(delta_entry(p.delta_bits, p.delta_wide, p.x_smem, p.delta_skip_zero), p.grid,
-                    kDW * 32, p.dyn_smem, stream, args);
+                    delta_warps_per_cta(p.delta_bits) * 32, p.dyn_smem, stream, args);
 }
 
 }  // namespace spmv
