@@ -41,17 +41,28 @@ namespace {
 #define SPMV_CSR_SEG_STAGES 2
 #endif
 constexpr int kCS = SPMV_CSR_SEG_STAGES;
-// Warps per CTA (one CTA per SM). Long-row plans: the rings fill the shared
-// memory. Mixed plans gather x mostly at random: their rings stay near
-// 125 KB so that L1 keeps about 100 KB, which random gathers through L1 need
-// (with 28 KB of L1 they ran at half the rate). On the power-law matrix
-// (916k rows, 5.1M nonzeros): 16, 24 or 32 warps 27.8, 26.6, 26.6 us;
-// packing rows of at most 64, 128 or 256 nonzeros 27.1, 26.6, 26.0 us.
+// Warps per CTA (one CTA per SM). Long-row plans: fewer warps give each
+// thread more registers and keep more gathers in flight; the LLM 12288^2
+// fp16 matrices at 30 / 70 / 90% sparsity (fraction of HBM peak): 20 warps
+// 0.99 / 0.94 / 0.74, 16 warps 1.00 / 0.94 / 0.74, 24 warps 1.00 / 0.93 /
+// 0.73, 28 warps 0.92 / 0.89 / 0.72. Mixed plans gather x mostly at
+// random: their rings stay near 125 KB so that L1 keeps about 100 KB, which
+// random gathers through L1 need (with 28 KB of L1 they ran at half the
+// rate). On the power-law matrix (916k rows, 5.1M nonzeros): 16, 24 or 32
+// warps 27.8, 26.6, 26.6 us; packing rows of at most 64, 128 or 256
+// nonzeros 27.1, 26.6, 26.0 us.
 #ifndef SPMV_CSR_MIXED_WARPS
 #define SPMV_CSR_MIXED_WARPS 24
 #endif
+#ifndef SPMV_CSR_LONG_WARPS_F16
+#define SPMV_CSR_LONG_WARPS_F16 20
+#endif
+#ifndef SPMV_CSR_LONG_WARPS_F32
+#define SPMV_CSR_LONG_WARPS_F32 24
+#endif
 template <typename VT, bool MIXED>
-constexpr int kCW = MIXED ? SPMV_CSR_MIXED_WARPS : (sizeof(VT) == 2 ? 28 : 24);
+constexpr int kCW = MIXED ? SPMV_CSR_MIXED_WARPS
+                          : (sizeof(VT) == 2 ? SPMV_CSR_LONG_WARPS_F16 : SPMV_CSR_LONG_WARPS_F32);
 
 template <typename VT, bool MIXED>
 struct CSeg {
