@@ -20,10 +20,13 @@
 // 2.2.3, would round it).
 //
 // Rows: each lane keeps fp32 partial sums of the current row piece; at the
-// row's last segment, or at the end of the warp's share, the warp reduces
-// them. A row inside one share is written at once; a row shared by several
-// warps leaves one partial per warp, and the warp whose atomicAdd completes
-// the row's count adds them in warp order (deterministic).
+// row's last segment, or at the end of the warp's piece of it, the warp
+// reduces them. A row inside one share is written at once; a row shared by
+// several warps leaves one partial per warp, and the warp whose atomicAdd
+// completes the row's count adds them in warp order (deterministic). The
+// planner puts the piece of the row a warp shares with the next warp at the
+// front of its share, so that the warp counts its pieces early, while it
+// still streams whole rows, instead of delaying its CTA's exit.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -78,6 +81,7 @@ struct DeltaArgs {
   float* __restrict__ y;
   float* partials;
   int32_t* counters;
+  unsigned long long* cells;  // one per split row, zero between runs
   int32_t* status;
   int n_empty;
   int n_cols;
@@ -511,6 +515,11 @@ __global__ void __launch_bounds__(kDW<B> * 32, SPMV_DELTA_MIN_BLOCKS)
   // holds at most two, its first row's and its last row's
   int2 pend[2];
   int n_pend = 0;
+  // lane 0: pieces of rows split in two, each handed over in one exchange
+  // whose result is read only after the share: {row, this piece's sum} and
+  // the cell's previous content (nonzero: the other piece, which was first)
+  Pair pair0, pair1;
+  int n_pair = 0;
   int s = 0;
   uint32_t phase = 0;
   int i = 0;
@@ -534,14 +543,21 @@ __global__ void __launch_bounds__(kDW<B> * 32, SPMV_DELTA_MIN_BLOCKS)
       issue_block(ring + s * Sg::kBytes, &s_full[warp][s], a.blocks + (size_t)h1.x * 16,
                   (uint32_t)h1.y, pol);
     const uint32_t rf = (uint32_t)h0.y;
-    if ((rf & kSegLast) || i == n - 1) {  // the row ends, or this warp's share does
+    // the row ends, this warp's piece of it does, or this warp's share does
+    if ((rf & kSegLast) || (h1.w & kSegCtlPieceEnd) || i == n - 1) {
       const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
       if (lane == 0) {
         const int row = (int)(rf & kSegRowMask);
         if (h0.w < 0) {
           a.y[row] = v;
-        } else if (n_pend < 2) {  // a piece of a shared row: park it, combine after the loop
+        } else if ((h1.w & kSegCtlPair) && n_pair < 2) {
+          if (n_pair == 0)
+            pair0 = hand_over(a.cells, h0.w, row, v);
+          else
+            pair1 = hand_over(a.cells, h0.w, row, v);
+          ++n_pair;
+        } else if (!(h1.w & kSegCtlPair) && n_pend < 2) {  // park it, count it later
           a.partials[h1.z] = v;
           if (n_pend == 0)
             pend[0] = make_int2(row, h0.w);
@@ -553,12 +569,22 @@ __global__ void __launch_bounds__(kDW<B> * 32, SPMV_DELTA_MIN_BLOCKS)
         }
       }
     }
+    // every piece of a shared row this warp holds is parked: count them now,
+    // while the warp still has rows to stream, not at the end of the launch
+    if ((h1.w & kSegCtlCombine) && lane == 0 && n_pend > 0) {
+      finish_pieces(a, pend, n_pend);
+      n_pend = 0;
+    }
     if (++s == kDS) {
       s = 0;
       phase ^= 1u;
     }
   }
   if (i == n && lane == 0 && n_pend > 0) finish_pieces(a, pend, n_pend);
+  if (i == n && lane == 0) {
+    if (n_pair > 0) settle(pair0, a.y, a.cells);
+    if (n_pair > 1) settle(pair1, a.y, a.cells);
+  }
   if (i < n && lane == 0) {
     // a wait gave up: let this warp's copies still in flight land before the
     // CTA's shared memory goes (bounded again)
@@ -638,6 +664,7 @@ int launch_delta(const Plan& p, const void* x, float* y, void* stream) {
   a.y = y;
   a.partials = p.partials;
   a.counters = p.counters;
+  a.cells = p.cells;
   a.status = p.status;
   a.n_empty = p.n_empty_rows;
   a.n_cols = p.n_cols;

@@ -144,6 +144,37 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// A warp's piece of a row split into exactly two pieces (segment kernels).
+// Each piece's warp swaps {1, its fp32 sum} into the row's 64-bit cell (zero
+// between runs) and goes on without waiting: the swap returns the cell's
+// previous content, which is read only after the warp's share. The piece
+// that finds the other's sum there came second; it writes y = its sum + the
+// other (fp32 addition is commutative, so the result does not depend on
+// which came first) and empties the cell. No fence is needed: the other
+// piece's sum travels in the exchange itself.
+struct Pair {
+  int row;
+  int cell;
+  float mine;
+  unsigned long long prev;
+};
+
+__device__ __forceinline__ Pair hand_over(unsigned long long* cells, int cell, int row, float v) {
+  Pair p;
+  p.row = row;
+  p.cell = cell;
+  p.mine = v;
+  p.prev = atomicExch(cells + cell, (1ull << 32) | __float_as_uint(v));
+  return p;
+}
+
+__device__ __forceinline__ void settle(const Pair& p, float* y, unsigned long long* cells) {
+  if (p.prev != 0) {
+    y[p.row] = p.mine + __uint_as_float((uint32_t)p.prev);
+    cells[p.cell] = 0;
+  }
+}
+
 // Launch with programmatic stream serialization: the kernel may begin while
 // the previous kernel on the stream drains; it orders itself with
 // griddepcontrol.wait before touching anything that kernel may write. The

@@ -380,6 +380,54 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* rp, const Options& o,
 // weight, and set up the rows whose segments fall in more than one share: one
 // partial per such warp (its piece), combined by the last to arrive. Packed
 // segments (whole short rows) are never shared.
+// Mark the segments of rows split into exactly two pieces (kSegCtlPair).
+// Within each warp's share, move the piece of the row that continues into
+// the next share to the front (kSegCtlPieceEnd on its last segment), so that
+// a warp hands over both its pieces of shared rows early: a two-piece row's
+// exchange then returns long before the warp needs its result at the end of
+// the share, and the rows of more pieces are counted (kSegCtlCombine) while
+// the warp still has whole rows to stream. The exchange and count used to
+// sit at the end of every share, about 2 us before each CTA could exit.
+void order_shares(SegTables* out, int n_warps) {
+  std::vector<SegDesc>& sg = out->segs;
+  for (size_t u = 0; u < sg.size(); ++u)
+    if (out->seg_split[u] >= 0 && out->splits[(size_t)out->seg_split[u]].n_chunks == 2)
+      sg[u].ctl |= kSegCtlPair;
+  auto slice = [&](int64_t u) { return !(sg[(size_t)u].flags & kSegPacked); };
+  auto split = [&](int64_t u) { return out->seg_split[(size_t)u] >= 0; };
+  for (int g = 0; g < n_warps; ++g) {
+    const int64_t a = out->warp_first[g], b = out->warp_first[g + 1];
+    if (b - a < 2) continue;
+    // the leading piece: a row begun by an earlier warp, segments [a, f]
+    int64_t f = -1;
+    if (split(a) && !(sg[(size_t)a].flags & kSegFirst)) {
+      f = a;
+      while (f + 1 < b && slice(f + 1) && sg[(size_t)(f + 1)].row == sg[(size_t)a].row) ++f;
+      if (f == b - 1) continue;  // the share is one piece of one row
+    }
+    // the trailing piece: a row that a later warp finishes, segments [c, b)
+    int64_t c = b;
+    if (split(b - 1) && !(sg[(size_t)(b - 1)].flags & kSegLast)) {
+      c = b - 1;
+      while (c - 1 > f && c - 1 >= a && slice(c - 1) &&
+             sg[(size_t)(c - 1)].row == sg[(size_t)(b - 1)].row)
+        --c;
+    }
+    if (c < b && c > a) {
+      std::rotate(sg.begin() + a, sg.begin() + c, sg.begin() + b);
+      std::rotate(out->seg_split.begin() + a, out->seg_split.begin() + c,
+                  out->seg_split.begin() + b);
+      std::rotate(out->seg_slot.begin() + a, out->seg_slot.begin() + c,
+                  out->seg_slot.begin() + b);
+      const int64_t moved_end = a + (b - c) - 1;
+      sg[(size_t)moved_end].ctl |= kSegCtlPieceEnd;
+      sg[(size_t)(f >= 0 ? f + (b - c) : moved_end)].ctl |= kSegCtlCombine;
+    } else if (c == b && f >= 0) {
+      sg[(size_t)f].ctl |= kSegCtlCombine;
+    }
+  }
+}
+
 spmv_status deal_segments(const std::function<int64_t(const SegDesc&)>& weight, int max_warps,
                           int warps_per_cta, SegTables* out, spmv_plan_info* info) {
   constexpr int64_t kMinShare = 256;  // weight a warp should get at least
@@ -546,6 +594,7 @@ spmv_status plan_delta_segments(const spmv_delta* d, int max_warps, int warps_pe
     if (col > INT32_MAX) return SPMV_ERR_TOO_LARGE;
     sg.base = (int32_t)col;
   }
+  order_shares(out, (int)out->warp_first.size() - 1);  // after the bases (row order)
   return SPMV_OK;
 }
 
@@ -607,7 +656,7 @@ void free_plan(spmv_plan* plan) {
     if (p->x_stage2) cudaFree(p->x_stage2);
     if (p->y_stage2) cudaFree(p->y_stage2);
     void* bufs[] = {p->row_ptr, p->col_idx,  p->values,   p->blocks,
-                    p->tiles,   p->splits,   p->partials, p->counters,
+                    p->tiles,   p->splits,   p->partials, p->counters, p->cells,
                     p->status,  p->x_stage,  p->y_stage,  p->cta_first,
                     p->row_split, p->perm, p->diag, p->pcg_work,
                     p->seg_off, p->empty_rows};
@@ -748,6 +797,7 @@ spmv_status build_csr_seg_blocks(const spmv_csr* m, const SegTables& t, int stag
     h.n_words = (int32_t)nz;
     h.split = t.seg_split[k];
     h.slot = t.seg_slot[k];
+    h.ctl = t.segs[k].ctl;
     if (next[k] >= 0) {
       h.next_off = (*seg_off)[next[k]];
       h.next_bytes = ((*seg_off)[next[k] + 1] - (*seg_off)[next[k]]) * 16;
@@ -788,6 +838,7 @@ spmv_status create_csr_seg_plan(const spmv_csr* m, const Options& o, bool mixed,
                   m->n_rows, [&](int32_t r) { return (int64_t)m->row_ptr[r]; }, kCsrSegNnzLong,
                   64, 1, p->sm_count * wpc, wpc, &t, &info);
   if (s != SPMV_OK) return s;
+  order_shares(&t, (int)t.warp_first.size() - 1);
   p->csr_mixed = mixed;
   p->csr_segments = true;
   p->grid = info.grid;
@@ -815,6 +866,7 @@ spmv_status create_csr_seg_plan(const spmv_csr* m, const Options& o, bool mixed,
     return s;
   if ((s = dev_upload(&p->partials, nullptr, 0, (size_t)t.n_chunks * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->cells, nullptr, 0, t.splits.size() * 8)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
   info.block = wpc * 32;
@@ -1219,6 +1271,7 @@ spmv_status build_delta_blocks(const spmv_delta* d, const SegTables& t, int stag
     h.n_words = (int32_t)nw;
     h.split = t.seg_split[k];
     h.slot = t.seg_slot[k];
+    h.ctl = t.segs[k].ctl;
     if (next[k] >= 0) {
       h.next_off = (*seg_off)[next[k]];
       h.next_bytes = ((*seg_off)[next[k] + 1] - (*seg_off)[next[k]]) * 16;
@@ -1332,6 +1385,7 @@ spmv_status create_delta_plan(const spmv_delta* d, const Options& o, Plan* p) {
                       t.splits.size() * sizeof(SplitInfo))) != SPMV_OK) return s;
   if ((s = dev_upload(&p->partials, nullptr, 0, (size_t)t.n_chunks * 4)) != SPMV_OK) return s;
   if ((s = dev_upload(&p->counters, nullptr, 0, t.splits.size() * 4)) != SPMV_OK) return s;
+  if ((s = dev_upload(&p->cells, nullptr, 0, t.splits.size() * 8)) != SPMV_OK) return s;
   if ((s = common_buffers(p)) != SPMV_OK) return s;
   info.x_in_smem = p->x_smem ? 1 : 0;
   info.block = wpc * 32;

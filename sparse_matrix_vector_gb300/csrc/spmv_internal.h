@@ -137,6 +137,13 @@ constexpr int64_t delta_wide_seg_bytes_max(int bits) {
 //   next_off   the block that this warp stages S segments later: offset in
 //   next_bytes 16-byte steps and size in bytes (0 when there is none)
 //   slot       for a split row: the partial-sum slot of this warp's piece
+//   ctl        kSegCtlPieceEnd: the last segment of this warp's piece of a
+//              split row that is not the row's last segment (the warp
+//              reduces and parks its piece here); kSegCtlCombine: every
+//              piece of this warp is parked after this segment (the warp
+//              counts them and combines the rows it completes here);
+//              kSegCtlPair: the row is split into exactly two pieces (they
+//              meet in one 64-bit exchange, see the kernels)
 struct SegHeader {
   int32_t base;
   uint32_t row_flags;
@@ -145,8 +152,11 @@ struct SegHeader {
   int32_t next_off;
   int32_t next_bytes;
   int32_t slot;
-  int32_t reserved;
+  int32_t ctl;
 };
+constexpr int32_t kSegCtlPieceEnd = 1;
+constexpr int32_t kSegCtlCombine = 2;
+constexpr int32_t kSegCtlPair = 4;
 static_assert(sizeof(SegHeader) == kSegHeaderBytes, "segment header is 32 bytes");
 constexpr uint32_t kSegFirst = 1u << 31;
 constexpr uint32_t kSegLast = 1u << 30;
@@ -240,8 +250,9 @@ spmv_status plan_csr_tiles(int n_rows, const int32_t* row_ptr,
 struct SegDesc {
   int32_t row;
   int32_t begin, end;
-  int32_t base;    // DELTA: column before the first entry
-  uint32_t flags;  // kSegFirst / kSegLast
+  int32_t base;      // DELTA: column before the first entry
+  uint32_t flags;    // kSegFirst / kSegLast
+  int32_t ctl = 0;   // kSegCtlPieceEnd / kSegCtlCombine
 };
 
 // Host-side result of cutting rows into segments and dealing them to warps.
@@ -322,6 +333,8 @@ struct Plan {
   float fem_k0[24 * 24] = {};
   float* partials = nullptr;    // one per split chunk
   int32_t* counters = nullptr;  // one per split row, zero between runs
+  // segment plans: one exchange cell per split row, zero between runs
+  unsigned long long* cells = nullptr;
   int32_t* status = nullptr;    // device status word
   // staging for spmv_run_host
   void* x_stage = nullptr;
