@@ -218,11 +218,15 @@ typedef struct spmv_plan_options {
                             3 mixed warp segments (runs of whole rows packed
                             256 nonzeros to a segment, [SPGEMM] 5.2;
                             longer rows in slices of 256)                  */
-  int32_t delta_kernel;  /* DELTA decode ([MACKO] 2.2): 0 auto (four lanes
-                            per word for 4-bit deltas), 1 a lane per packed
-                            word, 2 four lanes per word (4-bit deltas only;
+  int32_t delta_kernel;  /* DELTA decode ([MACKO] 2.2): 0 auto (several
+                            lanes per word for 4-bit deltas, and for 2-bit
+                            deltas unless more than 18% of the stored
+                            entries are +0.0 padding), 1 a lane per packed
+                            word, 2 several lanes per word (2- and 4-bit
+                            deltas: 4 lanes per word for 4-bit, 8 for 2-bit,
                             each lane two entries, so a warp's gathers fall
-                            in a narrow window of x)                       */
+                            in a narrow window of x; 8-bit deltas always
+                            take a lane per word)                          */
   int32_t reserved[4];
 } spmv_plan_options;
 

@@ -239,6 +239,23 @@ def test_delta_mixed_rows_deterministic(fmt):
     assert_parity(m, ys[0], TOL16)
 
 
+@pytest.mark.parametrize("dtype,kernel", [(np.float16, 2), (np.float32, 2), (np.float16, 3),
+                                          (np.float32, 3)])
+def test_segment_plans_split_rows_rearm(dtype, kernel):
+    """CSR warp segments (long-row and mixed plans) with rows shared by two
+    warps (one exchange per piece) and by many (counted): every run of the
+    same plan gives the same bits, so the exchange cells and the counts are
+    left empty for the next run."""
+    lengths = np.tile([0, 3, 300, 450, 700, 1500, 5000, 20000, 64, 65, 257], 20)
+    m = workloads.from_lengths("split16" if dtype == np.float16 else "split32", lengths, 30000,
+                               seed=23, dtype=dtype)
+    ys, info = run_gpu(m, options=S.spmv_plan_options(csr_kernel=kernel), repeat=4)
+    assert info["n_split_rows"] > 0
+    for y in ys[1:]:
+        assert np.array_equal(y, ys[0])
+    assert_parity(m, ys[0], TOL16 if dtype == np.float16 else TOL32)
+
+
 # ------------------------------------------------------------ edge cases
 
 def make(name, rp, ci, vals, n_cols, x):
