@@ -23,11 +23,13 @@
 // Packed rows: the products are parked in shared memory and lane l sums rows
 // l, l + 32, ... of the run. Slices: lanes keep fp32 partials; at a row's
 // last segment, or the end of the warp's piece of it, the warp reduces them.
-// A row inside one share is written at once; a row shared by several warps
-// leaves one partial per warp, and the warp whose atomicAdd completes the
-// row's count adds them in warp order. The planner puts the piece a warp
-// shares with the next warp at the front of its share, so that its pieces
-// are counted early rather than at the end of the launch.
+// A row inside one share is written at once. A row split into two pieces
+// (two warps) meets in one 64-bit exchange per piece (hand_over, settle:
+// nothing waits, and the sum is the same bits in either order); a row of
+// more pieces leaves one partial per warp, and the warp whose atomicAdd
+// completes the row's count adds them in warp order. The planner puts the
+// piece a warp shares with the next warp at the front of its share, so that
+// both of the warp's hand-overs go out early.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 

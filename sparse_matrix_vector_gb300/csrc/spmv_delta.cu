@@ -6,27 +6,34 @@
 // words (LW = 2 for B = 2, else 4) and gives each warp of the grid a
 // contiguous share of the segments, of equal weight. A segment's device block
 // (a 32-byte header, its words, its values) is staged by one bulk copy into
-// the warp's own ring of kStages shared-memory buffers; lane 0 of the warp
-// issues the copies, so warps never wait for one another.
+// the warp's own ring of kDS shared-memory buffers; lane s of the warp
+// issues the copies into buffer s, so warps never wait for one another.
 //
-// Decode: lane l takes words l, l + 32, ... of a segment. The column before a
-// word is the segment's starting column (stored by the planner) plus the
-// fields of every earlier word: the per-word field sums of two words' rows
-// are packed in 16-bit halves and prefix-summed over the warp by one 5-step
-// __shfl_up_sync scan ("MACKO-SpMV" 2.2.2). A word's own columns come from
-// prefix sums of its fields computed inside the register (SWAR), and each
-// entry is one shared-memory (or L1) gather of x and one mixed-precision fma
-// (the fp16 x fp16 product is exact in fp32; the page's half2 product,
-// 2.2.3, would round it).
+// Decode, several lanes per word (4-bit deltas, and 2-bit deltas with
+// little padding): L lanes share a word and each takes two of its entries,
+// so one warp-wide gather reads x for 32 entries of a few neighbouring words.
+// The planner stores each word's column offset, so no scan is needed (see
+// wide_pair).
+// Decode, a lane per word (8-bit deltas, and 2-bit deltas that are mostly
+// padding): lane l takes words l, l + 32, ... of a segment. The column
+// before a word is the segment's starting column (stored by the planner)
+// plus the fields of every earlier word: the per-word field sums of two
+// words' rows are packed in 16-bit halves and prefix-summed over the warp by
+// one 5-step __shfl_up_sync scan ("MACKO-SpMV" 2.2.2).
+// Either way a word's own columns come from prefix sums of its fields
+// computed inside the register (SWAR), and each entry is one shared-memory
+// (or L1) gather of x and one mixed-precision fma (the fp16 x fp16 product is
+// exact in fp32; the page's half2 product, 2.2.3, would round it).
 //
 // Rows: each lane keeps fp32 partial sums of the current row piece; at the
 // row's last segment, or at the end of the warp's piece of it, the warp
-// reduces them. A row inside one share is written at once; a row shared by
-// several warps leaves one partial per warp, and the warp whose atomicAdd
-// completes the row's count adds them in warp order (deterministic). The
-// planner puts the piece of the row a warp shares with the next warp at the
-// front of its share, so that the warp counts its pieces early, while it
-// still streams whole rows, instead of delaying its CTA's exit.
+// reduces them. A row inside one share is written at once. A row split into
+// two pieces (two warps) meets in one 64-bit exchange per piece (hand_over,
+// settle: nothing waits, and the sum is the same bits in either order); a
+// row of more pieces leaves one partial per warp, and the warp whose
+// atomicAdd completes the row's count adds them in warp order. The planner
+// puts the piece of the row a warp shares with the next warp at the front of
+// its share, so that both of the warp's hand-overs go out early.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
