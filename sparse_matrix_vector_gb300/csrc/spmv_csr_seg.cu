@@ -47,9 +47,11 @@ namespace {
 constexpr int kCS = SPMV_CSR_SEG_STAGES;
 // Warps per CTA (one CTA per SM). Long-row plans: fewer warps give each
 // thread more registers and keep more gathers in flight; the LLM 12288^2
-// fp16 matrices at 30 / 70 / 90% sparsity (fraction of HBM peak): 20 warps
-// 0.99 / 0.94 / 0.74, 16 warps 1.00 / 0.94 / 0.74, 24 warps 1.00 / 0.93 /
-// 0.73, 28 warps 0.92 / 0.89 / 0.72. Mixed plans gather x mostly at
+// fp16 matrices at 30 / 70 / 90% sparsity (fraction of HBM peak, before
+// rows of two pieces met in one exchange): 20 warps 0.99 / 0.94 / 0.74, 16
+// warps 1.00 / 0.94 / 0.74, 24 warps 1.00 / 0.93 / 0.73, 28 warps 0.92 /
+// 0.89 / 0.72; after it, 20 warps 1.01 / 1.01 / 0.86, 16 and 24 warps
+// within 2%. Mixed plans gather x mostly at
 // random: their rings stay near 125 KB so that L1 keeps about 100 KB, which
 // random gathers through L1 need (with 28 KB of L1 they ran at half the
 // rate). On the power-law matrix (916k rows, 5.1M nonzeros): 16, 24 or 32

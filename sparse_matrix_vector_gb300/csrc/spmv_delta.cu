@@ -67,7 +67,9 @@ namespace {
 // several-lanes decode of 4-bit deltas uses 96 at 20 warps, 72 at 28),
 // which keeps more of a block's loads and gathers in flight. Measured on the
 // 12288^2 LLM matrices (fraction of HBM peak at 30 / 50 / 70 / 90%
-// sparsity), 4-bit deltas: 20 warps x 2 stages 0.84 / 0.79 / 0.66 / 0.45;
+// sparsity, before rows of two pieces met in one exchange; after it, 20
+// warps x 2 stages 0.88 / 0.84 / 0.70 / 0.51 and 20 x 3 0.85 / 0.83 / 0.67
+// / 0.47), 4-bit deltas: 20 warps x 2 stages 0.84 / 0.79 / 0.66 / 0.45;
 // 16 x 2 0.83 / 0.79 / 0.66 / 0.45; 24 x 2 0.84 / 0.79 / 0.64 / 0.45; 28 x 2
 // 0.80 / 0.79 / 0.63 / 0.43; 16 x 3, 12 x 3, 12 x 4 and 8 x 4 slower; two
 // CTAs of 14 x 2 per SM no better, one CTA of 14 x 2 leaving room for the
