@@ -130,8 +130,19 @@ __device__ __forceinline__ void copy_x(typename Bits<VT>::T* xs, const void* x, 
   int done = 0;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
     const int nv = n / per;
-    for (int v = threadIdx.x; v < nv; v += nt)
-      reinterpret_cast<uint4*>(xs)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(xs);
+    // four loads a thread before their stores: one trip to memory for the x
+    // that fits shared memory
+    for (int v0 = 0; v0 < nv; v0 += 4 * nt) {
+      uint4 r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (v0 + k * nt + (int)threadIdx.x < nv) r[k] = __ldg(s4 + v0 + k * nt + threadIdx.x);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (v0 + k * nt + (int)threadIdx.x < nv) d4[v0 + k * nt + threadIdx.x] = r[k];
+    }
     done = nv * per;
   }
   for (int i = done + threadIdx.x; i < n; i += nt) xs[i] = __ldg(src + i);

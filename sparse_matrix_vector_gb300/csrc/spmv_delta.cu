@@ -114,8 +114,19 @@ __device__ __forceinline__ void copy_x_half(uint16_t* xs, const __half* x, int n
   int done = 0;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
     const int nv = n >> 3;
-    for (int v = threadIdx.x; v < nv; v += nt)
-      reinterpret_cast<uint4*>(xs)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(xs);
+    // four loads a thread before their stores: x of up to 32 KB takes one
+    // trip to memory
+    for (int v0 = 0; v0 < nv; v0 += 4 * nt) {
+      uint4 r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (v0 + k * nt + (int)threadIdx.x < nv) r[k] = __ldg(s4 + v0 + k * nt + threadIdx.x);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (v0 + k * nt + (int)threadIdx.x < nv) d4[v0 + k * nt + threadIdx.x] = r[k];
+    }
     done = nv << 3;
   }
   for (int i = done + threadIdx.x; i < n; i += nt) xs[i] = __ldg(src + i);
